@@ -1,0 +1,165 @@
+"""fp64 CPU oracle for GroupNorm-3D forward/backward -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline /
+reference leg import this package.  The CUDA library never does, and this
+package never imports the library: the two share no code.  The arithmetic
+lives in ``gn3d_oracle.c`` (plain C, fp64, compensated sums); this module only
+compiles it with gcc and marshals numpy arrays through ctypes.
+
+Functions (all cite the ScaFFold pages' GroupNorm definition; see the C file):
+  stats(x, dtype, N, C, S, G, eps)            -> mean, var, rstd   (fp64 [N*G])
+  forward(x, dtype, gamma, beta, N, C, S, G, eps) -> y64, mean, rstd
+  forward_at(..., mean, rstd, idx)             -> y64 at flat indices
+  backward(dy, x, dtype, mean, rstd, gamma, N, C, S, G) -> dx64, dgamma, dbeta
+  backward_at(..., idx)                        -> dx64 at indices, dgamma, dbeta
+  round_bf16(v64) -> uint16 bit patterns (RNE straight from fp64)
+  round_f32(v64)  -> float32 (RNE)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gn3d_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_SO = os.path.join(_BUILD, "libgn3d_oracle.so")
+
+F32, BF16 = 0, 1
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (OpenMP, no FMA contraction, IEEE math)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+        tmp = _SO + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+               "-fno-fast-math", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _SO)
+    return _SO
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i64, vp, dp, fp = ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
+            lib.gn3d_oracle_stats.argtypes = [vp, ctypes.c_int, i64, i64, i64, i64, ctypes.c_double, dp, dp, dp]
+            lib.gn3d_oracle_forward.argtypes = [vp, ctypes.c_int, fp, fp, i64, i64, i64, i64,
+                                                ctypes.c_double, dp, dp, dp]
+            lib.gn3d_oracle_forward_at.argtypes = [vp, ctypes.c_int, fp, fp, i64, i64, i64, i64, dp, dp,
+                                                   vp, i64, dp]
+            lib.gn3d_oracle_backward.argtypes = [vp, vp, ctypes.c_int, dp, dp, fp, i64, i64, i64, i64,
+                                                 dp, dp, dp]
+            lib.gn3d_oracle_backward_at.argtypes = [vp, vp, ctypes.c_int, dp, dp, fp, i64, i64, i64, i64,
+                                                    vp, i64, dp, dp, dp]
+            lib.gn3d_oracle_round_bf16.argtypes = [dp, i64, vp]
+            lib.gn3d_oracle_round_f32.argtypes = [dp, i64, fp]
+            for f in ("stats", "forward", "forward_at", "backward", "backward_at"):
+                getattr(lib, "gn3d_oracle_" + f).restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _raw(x: np.ndarray):
+    """Input bytes as the GPU sees them: float32 array, or uint16 bf16 bit patterns."""
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.float32:
+        return x, F32
+    if x.dtype == np.uint16:
+        return x, BF16
+    raise TypeError(f"oracle inputs are float32 or uint16 (bf16 bits), got {x.dtype}")
+
+
+def _params(p):
+    return None if p is None else np.ascontiguousarray(p, dtype=np.float32)
+
+
+def _check(rc):
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+
+
+def stats(x, N, C, S, G, eps):
+    xr, dt = _raw(x)
+    mean, var, rstd = (np.empty(N * G) for _ in range(3))
+    _check(_load().gn3d_oracle_stats(_ptr(xr), dt, N, C, S, G, eps, _ptr(mean), _ptr(var), _ptr(rstd)))
+    return mean, var, rstd
+
+
+def forward(x, gamma, beta, N, C, S, G, eps):
+    xr, dt = _raw(x)
+    g, b = _params(gamma), _params(beta)
+    y = np.empty(N * C * S)
+    mean, rstd = np.empty(N * G), np.empty(N * G)
+    _check(_load().gn3d_oracle_forward(_ptr(xr), dt, _ptr(g), _ptr(b), N, C, S, G, eps, _ptr(y),
+                                       _ptr(mean), _ptr(rstd)))
+    return y, mean, rstd
+
+
+def forward_at(x, gamma, beta, N, C, S, G, mean, rstd, idx):
+    xr, dt = _raw(x)
+    g, b = _params(gamma), _params(beta)
+    idx = np.ascontiguousarray(idx, dtype=np.int64)
+    mean = np.ascontiguousarray(mean, dtype=np.float64)
+    rstd = np.ascontiguousarray(rstd, dtype=np.float64)
+    y = np.empty(idx.size)
+    _check(_load().gn3d_oracle_forward_at(_ptr(xr), dt, _ptr(g), _ptr(b), N, C, S, G, _ptr(mean),
+                                          _ptr(rstd), _ptr(idx), idx.size, _ptr(y)))
+    return y
+
+
+def backward(dy, x, mean, rstd, gamma, N, C, S, G, want_dx=True):
+    xr, dt = _raw(x)
+    dyr, dt2 = _raw(dy)
+    if dt != dt2:
+        raise TypeError("dy and x must share a dtype")
+    g = _params(gamma)
+    mean = np.ascontiguousarray(mean, dtype=np.float64)
+    rstd = np.ascontiguousarray(rstd, dtype=np.float64)
+    dx = np.empty(N * C * S) if want_dx else None
+    dgamma, dbeta = np.empty(C), np.empty(C)
+    _check(_load().gn3d_oracle_backward(_ptr(dyr), _ptr(xr), dt, _ptr(mean), _ptr(rstd), _ptr(g),
+                                        N, C, S, G, _ptr(dx), _ptr(dgamma), _ptr(dbeta)))
+    return dx, dgamma, dbeta
+
+
+def backward_at(dy, x, mean, rstd, gamma, N, C, S, G, idx):
+    xr, dt = _raw(x)
+    dyr, _ = _raw(dy)
+    g = _params(gamma)
+    idx = np.ascontiguousarray(idx, dtype=np.int64)
+    mean = np.ascontiguousarray(mean, dtype=np.float64)
+    rstd = np.ascontiguousarray(rstd, dtype=np.float64)
+    dx = np.empty(idx.size)
+    dgamma, dbeta = np.empty(C), np.empty(C)
+    _check(_load().gn3d_oracle_backward_at(_ptr(dyr), _ptr(xr), dt, _ptr(mean), _ptr(rstd), _ptr(g),
+                                           N, C, S, G, _ptr(idx), idx.size, _ptr(dx), _ptr(dgamma),
+                                           _ptr(dbeta)))
+    return dx, dgamma, dbeta
+
+
+def round_bf16(v):
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    out = np.empty(v.shape, dtype=np.uint16)
+    _load().gn3d_oracle_round_bf16(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+def round_f32(v):
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    out = np.empty(v.shape, dtype=np.float32)
+    _load().gn3d_oracle_round_f32(_ptr(v), v.size, _ptr(out))
+    return out
