@@ -1,1 +1,149 @@
-"""libgn3d: GroupNorm-3D forward/backward for GB300 (sm_103a) behind a C ABI."""
+"""libgn3d: GroupNorm-3D forward/backward for GB300 (sm_103a) behind a C ABI.
+
+Python binding.  It only marshals arguments: every step of the GroupNorm runs
+in the library's CUDA kernels.  There is no CPU or PyTorch fallback -- if the
+library is missing or fails to load, every call raises.
+
+Two levels:
+  * ``gn3d_forward`` / ``gn3d_backward`` / ``gn3d_stream_status`` mirror the C
+    entry points one to one (integer pointers, sizes, dtype codes, stream
+    handle) and raise ``GN3DError`` on a non-zero status.
+  * ``forward`` / ``backward`` take torch CUDA tensors, allocate the outputs
+    with torch and pass torch's current stream.  torch is used for device
+    memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+F32, BF16 = 0, 1
+OK, ERR_INVALID_ARG, ERR_DEVICE, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_lock = threading.Lock()
+_lib = None
+
+
+class GN3DError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"gn3d status {status}: {msg}")
+        self.status = status
+
+
+def library_path() -> str:
+    from . import build as _b
+
+    return _b.LIB
+
+
+def lib():
+    """Load libgn3d (built in-tree by ``bwd_gn3d_stats_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(f"libgn3d is not built ({path} missing): run "
+                                   "python -m bwd_gn3d_stats_gb300.build")
+            L = ctypes.CDLL(path)
+            i64, vp, dbl, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_double, ctypes.c_int
+            L.gn3d_forward.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, dbl, ci, ci, vp, vp, vp, vp]
+            L.gn3d_forward.restype = ci
+            L.gn3d_backward.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, ci, vp, vp, vp, vp]
+            L.gn3d_backward.restype = ci
+            L.gn3d_stream_status.argtypes = [vp]
+            L.gn3d_stream_status.restype = ci
+            L.gn3d_error_string.argtypes = [ci]
+            L.gn3d_error_string.restype = ctypes.c_char_p
+            L.gn3d_launch_count.argtypes = []
+            L.gn3d_launch_count.restype = ctypes.c_uint64
+            L.gn3d_version.argtypes = []
+            L.gn3d_version.restype = ctypes.c_char_p
+            _lib = L
+    return _lib
+
+
+def _check(status: int):
+    if status != OK:
+        raise GN3DError(status, lib().gn3d_error_string(status).decode())
+
+
+# ------------------------------------------------------------ C-ABI mirrors
+
+def gn3d_forward(x, gamma, beta, N, C, D, H, W, G, eps, in_dtype, out_dtype, y, mean, rstd, stream):
+    _check(lib().gn3d_forward(x, gamma, beta, N, C, D, H, W, G, eps, in_dtype, out_dtype, y, mean, rstd,
+                              stream))
+
+
+def gn3d_backward(dy, x, mean, rstd, gamma, N, C, D, H, W, G, dtype, dx, dgamma, dbeta, stream):
+    _check(lib().gn3d_backward(dy, x, mean, rstd, gamma, N, C, D, H, W, G, dtype, dx, dgamma, dbeta, stream))
+
+
+def gn3d_stream_status(stream):
+    _check(lib().gn3d_stream_status(stream))
+
+
+def gn3d_launch_count() -> int:
+    return int(lib().gn3d_launch_count())
+
+
+def gn3d_version() -> str:
+    return lib().gn3d_version().decode()
+
+
+# ------------------------------------------------------------ torch level
+
+def _dtype_code(t):
+    import torch
+
+    if t == torch.bfloat16:
+        return BF16
+    if t == torch.float32:
+        return F32
+    raise TypeError(f"libgn3d supports bfloat16 and float32, got {t}")
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _shape5(x):
+    if x.dim() != 5:
+        raise ValueError("expected an NCDHW tensor")
+    if not x.is_contiguous():
+        raise ValueError("libgn3d takes contiguous NCDHW tensors")
+    return tuple(int(s) for s in x.shape)
+
+
+def forward(x, gamma, beta, G: int, eps: float = 1e-5, out_dtype=None):
+    """y, mean, rstd = GroupNorm(x) on x's device; y has out_dtype (default x.dtype)."""
+    import torch
+
+    N, C, D, H, W = _shape5(x)
+    out_dtype = x.dtype if out_dtype is None else out_dtype
+    y = torch.empty((N, C, D, H, W), dtype=out_dtype, device=x.device)
+    mean = torch.empty((N, G), dtype=torch.float32, device=x.device)
+    rstd = torch.empty((N, G), dtype=torch.float32, device=x.device)
+    gn3d_forward(x.data_ptr(), _ptr(gamma), _ptr(beta), N, C, D, H, W, G, float(eps), _dtype_code(x.dtype),
+                 _dtype_code(out_dtype), y.data_ptr(), mean.data_ptr(), rstd.data_ptr(),
+                 torch.cuda.current_stream(x.device).cuda_stream)
+    return y, mean, rstd
+
+
+def backward(dy, x, mean, rstd, gamma, G: int):
+    """dx, dgamma, dbeta of GroupNorm at the saved (mean, rstd)."""
+    import torch
+
+    N, C, D, H, W = _shape5(x)
+    if dy.shape != x.shape or dy.dtype != x.dtype:
+        raise ValueError("dy must match x in shape and dtype")
+    dy = dy.contiguous()
+    dx = torch.empty_like(x)
+    dgamma = torch.empty((C,), dtype=torch.float32, device=x.device)
+    dbeta = torch.empty((C,), dtype=torch.float32, device=x.device)
+    gn3d_backward(dy.data_ptr(), x.data_ptr(), mean.data_ptr(), rstd.data_ptr(), _ptr(gamma), N, C, D, H, W, G,
+                  _dtype_code(x.dtype), dx.data_ptr(), dgamma.data_ptr(), dbeta.data_ptr(),
+                  torch.cuda.current_stream(x.device).cuda_stream)
+    return dx, dgamma, dbeta

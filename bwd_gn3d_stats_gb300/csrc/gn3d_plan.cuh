@@ -1,0 +1,96 @@
+// gn3d_plan.cuh -- the launch plan: how a GroupNorm shape is cut into work units.
+//
+// The plan is a pure function of (N, C, D*H*W, G).  It never looks at the dtype,
+// the GPU's SM count or the grid a kernel happens to be launched with, so the
+// order of every floating-point reduction -- and therefore every output bit --
+// depends on the shape alone (ScaFFold PR #105: "_plan takes no dtype"; PR #93's
+// launch-folding commit: grid, split count, tiles and reduction order are pure
+// functions of the shape).
+//
+// Units.  Row (n, c) is the contiguous span of S = D*H*W elements at flat offset
+// (n*C + c)*S.  Each row is cut into R = ceil(S / kUnitElems) units.  Inside a
+// row, the "body" is the part between the first and last flat index that is a
+// multiple of 8 (kVec); body unit k covers body elements [k*kUnitElems,
+// (k+1)*kUnitElems), read as 8-element vectors (16 B of bf16, 32 B of fp32).
+// The up to 7 elements before the body (the head) belong to unit 0 and the up to
+// 7 after it (the tail) to unit R-1; a row too short to hold an aligned 8-block
+// is all head.  Groups are Cg = C/G consecutive rows, so group (n, g) owns the
+// Cg*R consecutive units starting at ((n*C + g*Cg) * R).
+#pragma once
+#include <stdint.h>
+
+namespace gn3d {
+
+constexpr int kVec = 8;             // elements per vector
+constexpr int kUnitElems = 8192;    // body elements per unit (multiple of kVec)
+constexpr int kThreads = 256;       // threads per CTA of the unit kernels
+constexpr int kWarps = kThreads / 32;
+constexpr int kVecPerThread = kUnitElems / kVec / kThreads;  // 4
+constexpr int kMaxScalars = 14;     // head + tail elements of one unit, at most
+
+struct Plan {
+  int64_t N, C, S, G;
+  int64_t Cg;     // channels per group
+  int64_t M;      // elements per group = Cg * S
+  int64_t NG;     // N * G groups
+  int64_t NC;     // N * C rows
+  int64_t R;      // units per row
+  int64_t upg;    // units per group = Cg * R
+  int64_t units;  // total units = NC * R
+};
+
+inline Plan make_plan(int64_t N, int64_t C, int64_t S, int64_t G) {
+  Plan p;
+  p.N = N; p.C = C; p.S = S; p.G = G;
+  p.Cg = C / G;
+  p.M = p.Cg * S;
+  p.NG = N * G;
+  p.NC = N * C;
+  p.R = S > 0 ? (S + kUnitElems - 1) / kUnitElems : 0;
+  p.upg = p.Cg * p.R;
+  p.units = p.NC * p.R;
+  return p;
+}
+
+// Element ranges of one unit (flat indices into the NCDHW tensor).
+struct URange {
+  int64_t row;
+  int64_t h0, h1;   // head scalars (or the whole row when it has no body)
+  int64_t b0, b1;   // body: multiple-of-8 aligned, possibly empty
+  int64_t t0, t1;   // tail scalars
+  int n;            // element count
+};
+
+__host__ __device__ inline URange unit_range(const Plan& p, int64_t u) {
+  URange q;
+  const int64_t row = u / p.R, k = u - row * p.R;
+  const int64_t r0 = row * p.S, r1 = r0 + p.S;
+  const int64_t bl = (r0 + kVec - 1) & ~(int64_t)(kVec - 1);
+  const int64_t bh = r1 & ~(int64_t)(kVec - 1);
+  q.row = row;
+  if (bh <= bl) {
+    q.h0 = r0; q.h1 = (k == 0) ? r1 : r0;
+    q.b0 = q.b1 = r0;
+    q.t0 = q.t1 = r1;
+  } else {
+    q.h0 = r0; q.h1 = (k == 0) ? bl : r0;
+    const int64_t lo = bl + k * (int64_t)kUnitElems, hi = lo + kUnitElems;
+    q.b0 = lo < bh ? lo : bh;
+    q.b1 = hi < bh ? hi : bh;
+    q.t0 = bh; q.t1 = (k == p.R - 1) ? r1 : bh;
+  }
+  q.n = (int)((q.h1 - q.h0) + (q.b1 - q.b0) + (q.t1 - q.t0));
+  return q;
+}
+
+// Flat index of scalar number s (0 <= s < head+tail) of a unit: head first, then tail.
+__host__ __device__ inline int64_t scalar_index(const URange& q, int s) {
+  const int64_t nh = q.h1 - q.h0;
+  return s < nh ? q.h0 + s : q.t0 + (s - nh);
+}
+
+__host__ __device__ inline int scalar_count(const URange& q) {
+  return (int)((q.h1 - q.h0) + (q.t1 - q.t0));
+}
+
+}  // namespace gn3d

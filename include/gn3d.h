@@ -1,0 +1,121 @@
+/*
+ * gn3d.h -- C ABI of libgn3d: GroupNorm forward and backward over contiguous
+ * NCDHW volumes on an NVIDIA GB300 (sm_103a).
+ *
+ * Operation (ScaFFold PR #93 "Optimize GroupNorm": a drop-in for torch's
+ * nn.GroupNorm, same weight and bias; PR #105 "Preserve GroupNorm dtype":
+ * statistics accumulated in fp32, the normalized value computed in fp32, only
+ * the store narrows):
+ *
+ *   x has shape [N, C, D, H, W], contiguous.  Group (n, g), 0 <= g < G, is the
+ *   channel block g*C/G .. (g+1)*C/G - 1 of sample n: M = (C/G)*D*H*W
+ *   elements, one contiguous span.
+ *     mean = sum(x)/M,  var = sum((x-mean)^2)/M  (biased),
+ *     rstd = 1/sqrt(var + eps)
+ *     y    = (x - mean) * rstd * gamma[c] + beta[c]
+ *   Backward at the saved (mean, rstd), with xhat = (x-mean)*rstd and
+ *   g = dy*gamma[c]:
+ *     dx       = rstd * (g - mean_group(g) - xhat * mean_group(g*xhat))
+ *     dgamma_c = sum over n and positions of dy*xhat,   dbeta_c = sum of dy
+ *
+ * Determinism: every reduction runs in a fixed order chosen from the shape
+ * alone (never from the dtype, the GPU's SM count or timing) and no float
+ * atomics are used, so repeated calls give bit-identical results, and fp32
+ * and bf16 inputs that hold the same values give bit-identical mean, rstd,
+ * dgamma and dbeta (PR #105: the launch plan takes no dtype).
+ *
+ * Conventions for every entry point:
+ *   - Tensors are dense, contiguous NCDHW, in device memory of the CURRENT
+ *     device (cudaSetDevice), 16-byte aligned.  A pointer on another device or
+ *     in unregistered host memory is rejected with GN3D_ERR_DEVICE (PR #93's
+ *     review found a kernel launched on the wrong device faulting; this library
+ *     checks instead of switching devices).
+ *   - gamma, beta, mean, rstd, dgamma, dbeta are fp32 arrays.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls are asynchronous with respect to the host and ordered on
+ *     `stream`; results are ready when the stream reaches the call.
+ *   - Ownership: the caller owns every buffer; the library keeps no pointer
+ *     after a call returns.  Per-call scratch is allocated and freed
+ *     stream-ordered on `stream` (cudaMallocAsync / cudaFreeAsync).
+ *   - Return value: GN3D_OK, or an error code below; on error nothing has been
+ *     enqueued.  gn3d_error_string() describes the code and, for
+ *     GN3D_ERR_CUDA, the CUDA error of the calling thread's last failure.
+ *   - Empty tensors (N, C or D*H*W zero) are a successful no-op, except that
+ *     dgamma/dbeta are zero-filled and, for M == 0 groups, mean = 0 and
+ *     rstd = 1/sqrt(eps) are written.
+ *   - Shapes with N*(C/G)*D*H*W == 1 are rejected (GN3D_ERR_INVALID_ARG), as
+ *     stock GroupNorm raises for them (PR #93 review: "(1,C,1,1,1) ... where
+ *     stock raises").
+ */
+#ifndef GN3D_H_
+#define GN3D_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { GN3D_F32 = 0, GN3D_BF16 = 1 } gn3d_dtype;
+
+enum {
+  GN3D_OK = 0,
+  GN3D_ERR_INVALID_ARG = 1, /* bad shape, dtype, NULL required pointer, misalignment */
+  GN3D_ERR_DEVICE = 2,      /* a pointer is not device memory of the current device */
+  GN3D_ERR_CUDA = 3,        /* a CUDA runtime call (allocation, launch) failed */
+  GN3D_ERR_TIMEOUT = 4      /* a bounded device-side wait gave up (see gn3d_stream_status) */
+};
+
+/*
+ * GroupNorm forward.
+ *   x      [N,C,D,H,W] in_dtype, read only.
+ *   gamma  [C] fp32 or NULL (gamma = 1);  beta [C] fp32 or NULL (beta = 0).
+ *   G      number of groups, G >= 1, C % G == 0.
+ *   eps    added to the variance inside the square root; used as its fp32
+ *          value (finite, >= 0).
+ *   in_dtype / out_dtype: GN3D_BF16 or GN3D_F32, any pair.  y is the fp32
+ *          result rounded once (round to nearest even) to out_dtype.
+ *   y      [N,C,D,H,W] out_dtype, written; must not overlap x.
+ *   mean, rstd  [N*G] fp32 (row-major (n, g)), written, or NULL (not saved).
+ */
+int gn3d_forward(const void* x, const float* gamma, const float* beta, int64_t N, int64_t C,
+                 int64_t D, int64_t H, int64_t W, int64_t G, double eps, gn3d_dtype in_dtype,
+                 gn3d_dtype out_dtype, void* y, float* mean, float* rstd, void* stream);
+
+/*
+ * GroupNorm backward at the forward's saved statistics.
+ *   dy, x  [N,C,D,H,W] dtype, read only.
+ *   mean, rstd  [N*G] fp32 as written by gn3d_forward for the same x, G, eps.
+ *   gamma  [C] fp32 or NULL (gamma = 1).
+ *   dx     [N,C,D,H,W] dtype, written (the fp32 result rounded once); must not
+ *          overlap dy or x.
+ *   dgamma, dbeta  [C] fp32, written (overwritten, not accumulated), or NULL.
+ */
+int gn3d_backward(const void* dy, const void* x, const float* mean, const float* rstd,
+                  const float* gamma, int64_t N, int64_t C, int64_t D, int64_t H, int64_t W,
+                  int64_t G, gn3d_dtype dtype, void* dx, float* dgamma, float* dbeta,
+                  void* stream);
+
+/*
+ * Synchronizes `stream`, then returns and clears the device-side error word
+ * that bounded waits inside the kernels set (GN3D_ERR_TIMEOUT), or
+ * GN3D_ERR_CUDA if the stream reports a CUDA error, else GN3D_OK.
+ */
+int gn3d_stream_status(void* stream);
+
+/* Static description of a status code (thread-local detail for GN3D_ERR_CUDA). */
+const char* gn3d_error_string(int status);
+
+/* Number of CUDA kernels libgn3d has launched in this process, all devices and
+ * threads together (diagnostics: lets a caller count the kernels of a timed
+ * region).  Memory-set and copy operations are not counted. */
+uint64_t gn3d_launch_count(void);
+
+/* Library version, e.g. "gn3d 0.1.0 sm_103a". */
+const char* gn3d_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GN3D_H_ */

@@ -1,0 +1,158 @@
+"""The C ABI: the library builds, loads and exports what include/gn3d.h declares;
+argument checks return the documented status codes."""
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import bwd_gn3d_stats_gb300 as gn
+from bwd_gn3d_stats_gb300 import build, synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gn3d.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return gn.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gn3d_\w+)\s*\(", src)))
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for n in ("gn3d_forward", "gn3d_backward", "gn3d_stream_status", "gn3d_error_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    out = subprocess.run(["nm", "-D", "--defined-only", build.LIB], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\bT (gn3d_\w+)", out))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, f"declared but not exported: {missing}"
+    for n in declared_functions():
+        assert hasattr(L, n)
+
+
+def test_header_compiles_as_c(tmp_path):
+    src = tmp_path / "t.c"
+    src.write_text('#include "gn3d.h"\nint (*f)(void*) = gn3d_stream_status;\n'
+                   'int main(void){ return f == 0; }\n')
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), "-c", str(src),
+                    "-o", str(tmp_path / "t.o")], check=True)
+
+
+def test_version(L):
+    assert gn.gn3d_version().startswith("gn3d ")
+
+
+# Argument checks that fail before any CUDA call (no GPU needed).
+BAD_SHAPES = [
+    dict(N=1, C=8, D=4, H=4, W=4, G=3),      # C % G != 0
+    dict(N=1, C=8, D=4, H=4, W=4, G=0),      # G < 1
+    dict(N=-1, C=8, D=4, H=4, W=4, G=2),     # negative dimension
+    dict(N=1, C=4, D=1, H=1, W=1, G=4),      # one value per group: stock GroupNorm raises
+]
+
+
+@pytest.mark.parametrize("shape", BAD_SHAPES)
+def test_invalid_shapes_rejected(L, shape):
+    s = shape
+    rc = L.gn3d_forward(None, None, None, s["N"], s["C"], s["D"], s["H"], s["W"], s["G"], 1e-5, gn.BF16, gn.BF16,
+                        None, None, None, None)
+    assert rc == gn.ERR_INVALID_ARG
+    assert L.gn3d_error_string(rc).decode().startswith("invalid argument")
+    rc = L.gn3d_backward(None, None, None, None, None, s["N"], s["C"], s["D"], s["H"], s["W"], s["G"], gn.BF16,
+                         None, None, None, None)
+    assert rc == gn.ERR_INVALID_ARG
+
+
+def test_invalid_dtype_and_eps_rejected(L):
+    assert L.gn3d_forward(None, None, None, 1, 4, 2, 2, 2, 2, 1e-5, 7, gn.BF16, None, None, None, None) == 1
+    assert L.gn3d_forward(None, None, None, 1, 4, 2, 2, 2, 2, -1.0, gn.BF16, gn.BF16, None, None, None, None) == 1
+    assert L.gn3d_forward(None, None, None, 1, 4, 2, 2, 2, 2, float("nan"), gn.BF16, gn.BF16, None, None, None,
+                          None) == 1
+    assert L.gn3d_backward(None, None, None, None, None, 1, 4, 2, 2, 2, 2, 9, None, None, None, None) == 1
+
+
+def test_python_raises_gn3derror(L):
+    with pytest.raises(gn.GN3DError) as e:
+        gn.gn3d_forward(None, None, None, 1, 6, 1, 1, 1, 4, 1e-5, gn.BF16, gn.BF16, None, None, None, None)
+    assert e.value.status == gn.ERR_INVALID_ARG
+
+
+# ----------------------------------------------------------- on the GPU
+
+@pytest.mark.gpu
+def test_gpu_pointer_checks(L):
+    import torch
+
+    x = torch.zeros(64 * 4, dtype=torch.bfloat16, device="cuda")
+    y = torch.empty_like(x)
+    st = torch.cuda.current_stream().cuda_stream
+    # misaligned x (2-byte offset)
+    rc = L.gn3d_forward(x.data_ptr() + 2, None, None, 1, 4, 1, 1, 63, 2, 1e-5, gn.BF16, gn.BF16, y.data_ptr(),
+                        None, None, st)
+    assert rc == gn.ERR_INVALID_ARG
+    # host memory for y
+    h = np.zeros(64 * 4, dtype=np.uint16)
+    rc = L.gn3d_forward(x.data_ptr(), None, None, 1, 4, 1, 1, 64, 2, 1e-5, gn.BF16, gn.BF16, h.ctypes.data, None,
+                        None, st)
+    assert rc == gn.ERR_DEVICE
+    # pinned host memory is not device memory either
+    hp = torch.zeros(64 * 4, dtype=torch.bfloat16).pin_memory()
+    rc = L.gn3d_forward(x.data_ptr(), None, None, 1, 4, 1, 1, 64, 2, 1e-5, gn.BF16, gn.BF16, hp.data_ptr(), None,
+                        None, st)
+    assert rc == gn.ERR_DEVICE
+    assert L.gn3d_stream_status(st) == gn.OK
+
+
+@pytest.mark.gpu
+def test_gpu_empty_tensors(L):
+    import torch
+
+    st = torch.cuda.current_stream().cuda_stream
+    mean = torch.full((2 * 4,), 7.0, device="cuda")
+    rstd = torch.full((2 * 4,), 7.0, device="cuda")
+    x = torch.empty(0, device="cuda")
+    rc = L.gn3d_forward(x.data_ptr(), None, None, 2, 8, 0, 5, 5, 4, 1e-5, gn.F32, gn.F32, x.data_ptr(),
+                        mean.data_ptr(), rstd.data_ptr(), st)
+    assert rc == gn.OK
+    assert torch.all(mean == 0) and torch.allclose(rstd, torch.full_like(rstd, 1e-5 ** -0.5))
+    dg = torch.full((8,), 3.0, device="cuda")
+    db = torch.full((8,), 3.0, device="cuda")
+    rc = L.gn3d_backward(x.data_ptr(), x.data_ptr(), mean.data_ptr(), rstd.data_ptr(), None, 2, 8, 0, 5, 5, 4,
+                         gn.F32, x.data_ptr(), dg.data_ptr(), db.data_ptr(), st)
+    assert rc == gn.OK
+    assert torch.all(dg == 0) and torch.all(db == 0)
+    # N = 0: nothing to do at all
+    rc = L.gn3d_forward(None, None, None, 0, 8, 4, 4, 4, 4, 1e-5, gn.BF16, gn.BF16, None, None, None, st)
+    assert rc == gn.OK
+    assert L.gn3d_stream_status(st) == gn.OK
+
+
+@pytest.mark.gpu
+def test_gpu_torch_level_wrappers():
+    import torch
+
+    site = synth.Site(1, 8, 6, 6, 6, 4, synth.BF16)
+    inp = synth.make_inputs(site, seed=0)
+    x = torch.from_numpy(inp["x"].view(np.int16)).cuda().view(torch.bfloat16).reshape(1, 8, 6, 6, 6)
+    g = torch.from_numpy(inp["gamma"]).cuda()
+    b = torch.from_numpy(inp["beta"]).cuda()
+    y, mean, rstd = gn.forward(x, g, b, 4)
+    assert y.dtype == torch.bfloat16 and mean.shape == (1, 4)
+    y32, _, _ = gn.forward(x, g, b, 4, out_dtype=torch.float32)
+    assert y32.dtype == torch.float32
+    assert torch.equal(y32.to(torch.bfloat16), y)
+    dx, dg, db = gn.backward(torch.ones_like(x), x, mean, rstd, g, 4)
+    assert dx.dtype == torch.bfloat16 and dg.shape == (8,)
