@@ -102,13 +102,13 @@ T* carve(char*& cur, int64_t count) {
 template <class TI, class TO>
 int launch_forward(const void* x, const float* gamma, const float* beta, const Plan& p, float eps,
                    void* y, float* mean, float* rstd, cudaStream_t st, const DevInfo& di) {
-  const int64_t bytes = 256 * 4 + p.units * (int64_t)sizeof(Part) + p.NG * (int64_t)(sizeof(float2) + sizeof(unsigned));
+  const int64_t bytes = 256 * 4 + p.units * (int64_t)sizeof(Part) + p.NG * (int64_t)(sizeof(float4) + sizeof(unsigned));
   void* ws = nullptr;
   GN3D_CUDA(cudaMallocAsync(&ws, (size_t)bytes, st), "cudaMallocAsync(workspace)");
   char* cur = static_cast<char*>(ws);
   FwdWs w;
   w.cnt = carve<unsigned>(cur, p.NG);
-  w.stats = carve<float2>(cur, p.NG);
+  w.stats = carve<float4>(cur, p.NG);
   w.parts = carve<Part>(cur, p.units);
   cudaError_t e = cudaMemsetAsync(w.cnt, 0, (size_t)p.NG * sizeof(unsigned), st);
   if (e == cudaSuccess) {

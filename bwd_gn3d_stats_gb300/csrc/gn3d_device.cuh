@@ -1,5 +1,6 @@
 // gn3d_device.cuh -- device building blocks shared by the GroupNorm kernels:
-// vector loads/stores, fixed-order block reductions, Chan's parallel merge.
+// vector loads/stores, fixed-order block reductions, the group merge of the
+// per-unit statistics.
 //
 // Every floating-point operation that feeds a statistic or an output is written
 // with an explicit round-to-nearest intrinsic (__fadd_rn, __fmul_rn, __fmaf_rn,
@@ -90,68 +91,69 @@ __device__ __forceinline__ float2 block_sum2(float a, float b, float2* sh) {
   return r;
 }
 
-// --------------------------------------------------------- Chan's merge
-// (count, mean, M2) of the union of two disjoint sets (Chan, Golub & LeVeque's
-// parallel variance update, the combine ScaFFold's GroupNorm stats use), in fp32
-// with a fixed operand order.  Empty sets are identities.
-struct Moments {
-  float mean, m2;
-  int64_t n;
-};
-
-__device__ __forceinline__ Moments chan_merge(Moments a, Moments b) {
-  if (b.n == 0) return a;
-  if (a.n == 0) return b;
-  Moments r;
-  r.n = a.n + b.n;
-  const float fb = __fdiv_rn((float)b.n, (float)r.n);
-  const float d = fsub(b.mean, a.mean);
-  r.mean = ffma(d, fb, a.mean);
-  r.m2 = ffma(fmul(d, d), fmul((float)a.n, fb), fadd(a.m2, b.m2));
-  return r;
-}
-
-__device__ __forceinline__ Moments shfl_down_moments(Moments m, int o) {
-  Moments r;
-  r.mean = __shfl_down_sync(0xFFFFFFFFu, m.mean, o);
-  r.m2 = __shfl_down_sync(0xFFFFFFFFu, m.m2, o);
-  r.n = __shfl_down_sync(0xFFFFFFFFu, m.n, o);
-  return r;
-}
-
-// Per-unit record of the forward statistics partials (16 bytes).
+// ------------------------------------------------------ group statistics
+// Per-unit record of the forward statistics (16 bytes): the unit's mean as the
+// unevaluated pair m1 + cn (m1 = sum/n in fp32, cn = sum(x - m1)/n), its M2 =
+// sum((x - mean)^2) and its element count.
 struct Part {
-  float mean, m2;
-  int n, pad;
+  float m1, m2;
+  int n;
+  float cn;
 };
 
-// Fixed-shape combine of `cnt` unit partials by one CTA: thread t merges its
-// contiguous slice in order, a shfl_down tree merges each warp into lane 0, and
-// thread 0 merges the warp results in warp order.  Result valid in thread 0.
-__device__ __forceinline__ Moments combine_parts(const Part* parts, int64_t cnt, Moments* sh) {
+// Merge of the unit partials of one group (the parallel-variance combine of
+// Chan, Golub & LeVeque in its shifted-sum form): with the shift K = the first
+// unit's mean and d_u = mean_u - K,
+//   mean = K + (sum n_u d_u) / M,   M2 = sum (M2_u + n_u d_u^2) - (sum n_u d_u)^2 / M.
+// The merge runs in fp64 (the per-element accumulation is fp32): the group
+// mean then keeps the digits an fp32 mean of a large-offset group loses, which
+// the normalize uses as a hi/lo pair.  Fixed shape: thread t sums its
+// contiguous slice in order, a shfl_down tree sums each warp into lane 0, and
+// thread 0 adds the warp sums in warp order.  Result valid in thread 0.
+struct GroupMoments {
+  double mean, m2;
+};
+
+__device__ __forceinline__ double dadd(double a, double b) { return __dadd_rn(a, b); }
+__device__ __forceinline__ double dmul(double a, double b) { return __dmul_rn(a, b); }
+
+__device__ __forceinline__ GroupMoments combine_parts(const Part* parts, int64_t cnt, int64_t M, double2* sh) {
+  const float4 r0 = __ldcg(reinterpret_cast<const float4*>(parts));
+  const double K = dadd((double)r0.x, (double)r0.w);
   const int64_t per = (cnt + kThreads - 1) / kThreads;
   int64_t lo = (int64_t)threadIdx.x * per, hi = lo + per;
   if (hi > cnt) hi = cnt;
-  Moments m = {0.f, 0.f, 0};
+  double S = 0.0, Q = 0.0;
   for (int64_t i = lo; i < hi; ++i) {
     const float4 r = __ldcg(reinterpret_cast<const float4*>(parts + i));
-    Moments b = {r.x, r.y, (int64_t)__float_as_int(r.z)};
-    m = chan_merge(m, b);
+    const int n = __float_as_int(r.z);
+    if (n == 0) continue;
+    const double d = dadd(dadd((double)r.x, -K), (double)r.w);
+    const double nd = dmul((double)n, d);
+    S = dadd(S, nd);
+    Q = dadd(Q, dadd((double)r.y, dmul(nd, d)));
   }
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    Moments b = shfl_down_moments(m, o);
-    if (lane + o < 32) m = chan_merge(m, b);
+    const double a = __shfl_down_sync(0xFFFFFFFFu, S, o);
+    const double b = __shfl_down_sync(0xFFFFFFFFu, Q, o);
+    if (lane + o < 32) { S = dadd(S, a); Q = dadd(Q, b); }
   }
-  if (lane == 0) sh[threadIdx.x >> 5] = m;
+  if (lane == 0) sh[threadIdx.x >> 5] = make_double2(S, Q);
   __syncthreads();
+  GroupMoments g = {0.0, 0.0};
   if (threadIdx.x == 0) {
-    m = sh[0];
-    for (int i = 1; i < kWarps; ++i) m = chan_merge(m, sh[i]);
+    S = sh[0].x;
+    Q = sh[0].y;
+    for (int i = 1; i < kWarps; ++i) { S = dadd(S, sh[i].x); Q = dadd(Q, sh[i].y); }
+    const double sm = __ddiv_rn(S, (double)M);
+    g.mean = dadd(K, sm);
+    g.m2 = dadd(Q, -dmul(S, sm));
+    if (g.m2 < 0.0) g.m2 = 0.0;  // rounding only; NaN is kept
   }
   __syncthreads();
-  return m;
+  return g;
 }
 
 // ---------------------------------------------------------- unit loaders

@@ -23,7 +23,7 @@ namespace gn3d {
 
 struct FwdWs {
   Part* parts;      // [units]
-  float2* stats;    // [NG] (mean, rstd)
+  float4* stats;    // [NG] (mean hi, mean lo, rstd, 0)
   unsigned* cnt;    // [NG] arrivals per group
 };
 
@@ -35,11 +35,12 @@ struct BwdWs {
 };
 
 // Corrected two-pass moments of one unit held in registers: m1 = sum/n, then
-// c = sum(x - m1), q = sum((x - m1)^2); mean = m1 + c/n, M2 = q - c*c/n (the
-// correction term keeps M2 exact to first order in the error of m1).
+// c = sum(x - m1), q = sum((x - m1)^2); the unit mean is m1 + c/n (kept as the
+// pair) and M2 = q - c*c/n (the correction term keeps M2 exact to first order
+// in the error of m1).
 template <class T>
-__device__ __forceinline__ Moments unit_moments(const UnitRegs<T>& u, int n, float2* red) {
-  Moments m = {0.f, 0.f, 0};
+__device__ __forceinline__ Part unit_moments(const UnitRegs<T>& u, int n, float2* red) {
+  Part m = {0.f, 0.f, 0, 0.f};
   if (n == 0) return m;
   float s = 0.f;
 #pragma unroll
@@ -68,24 +69,27 @@ __device__ __forceinline__ Moments unit_moments(const UnitRegs<T>& u, int n, flo
     q = ffma(d, d, q);
   }
   const float2 t = block_sum2(c, q, red);
-  const float cn = __fdiv_rn(t.x, fn);
-  m.mean = fadd(m1, cn);
-  m.m2 = fsub(t.y, fmul(t.x, cn));
+  m.m1 = m1;
+  m.cn = __fdiv_rn(t.x, fn);
+  m.m2 = fsub(t.y, fmul(t.x, m.cn));
   if (m.m2 < 0.f) m.m2 = 0.f;  // rounding only; NaN is kept
   m.n = n;
   return m;
 }
 
-// Finalize of one group from its unit partials: mean, rstd = 1/sqrt(M2/M + eps).
+// Finalize of one group from its unit partials: mean, rstd = 1/sqrt(M2/M + eps)
+// (fp64, rounded once to fp32); the workspace keeps the mean as a hi/lo fp32 pair.
 __device__ __forceinline__ void finalize_group(const Plan& p, int64_t ng, const Part* parts, float eps,
-                                               float2* stats, float* mean_out, float* rstd_out,
-                                               Moments* sh) {
-  const Moments m = combine_parts(parts + ng * p.upg, p.upg, sh);
+                                               float4* stats, float* mean_out, float* rstd_out,
+                                               double2* sh) {
+  const GroupMoments m = combine_parts(parts + ng * p.upg, p.upg, p.M, sh);
   if (threadIdx.x == 0) {
-    const float var = __fdiv_rn(m.m2, (float)p.M);
-    const float r = __frsqrt_rn(fadd(var, eps));
-    stats[ng] = make_float2(m.mean, r);
-    if (mean_out) mean_out[ng] = m.mean;
+    const double var = __ddiv_rn(m.m2, (double)p.M);
+    const float r = (float)__drcp_rn(__dsqrt_rn(dadd(var, (double)eps)));
+    const float hi = (float)m.mean;
+    const float lo = (float)dadd(m.mean, -(double)hi);
+    stats[ng] = make_float4(hi, lo, r, 0.f);
+    if (mean_out) mean_out[ng] = hi;
     if (rstd_out) rstd_out[ng] = r;
   }
 }
@@ -94,16 +98,16 @@ template <class TI>
 __global__ void __launch_bounds__(kThreads) k_fwd_stats(const TI* __restrict__ x, Plan p, FwdWs ws,
                                                         float eps, float* mean_out, float* rstd_out) {
   __shared__ float2 red[kWarps];
-  __shared__ Moments msh[kWarps];
+  __shared__ double2 msh[kWarps];
   __shared__ int s_last;
   for (int64_t u = blockIdx.x; u < p.units; u += gridDim.x) {
     const URange q = unit_range(p, u);
     UnitRegs<TI> r;
     r.load(x, q);
-    const Moments m = unit_moments(r, q.n, red);
+    const Part m = unit_moments(r, q.n, red);
     const int64_t ng = q.row / p.Cg;
     if (threadIdx.x == 0) {
-      ws.parts[u] = Part{m.mean, m.m2, (int)m.n, 0};
+      ws.parts[u] = m;
       __threadfence();
       s_last = atomicAdd(&ws.cnt[ng], 1u) == (unsigned)(p.upg - 1);
     }
@@ -118,15 +122,15 @@ __global__ void __launch_bounds__(kThreads) k_fwd_stats(const TI* __restrict__ x
 
 template <class TI, class TO>
 __global__ void __launch_bounds__(kThreads) k_fwd_norm(const TI* __restrict__ x, TO* __restrict__ y, Plan p,
-                                                       const float2* __restrict__ stats,
+                                                       const float4* __restrict__ stats,
                                                        const float* __restrict__ gamma,
                                                        const float* __restrict__ beta) {
   for (int64_t i = blockIdx.x; i < p.units; i += gridDim.x) {
     const int64_t u = p.units - 1 - i;
     const URange q = unit_range(p, u);
     const int64_t c = q.row % p.C, ng = q.row / p.Cg;
-    const float2 st = stats[ng];
-    const float sc = gamma ? fmul(st.y, gamma[c]) : st.y;
+    const float4 st = stats[ng];
+    const float sc = gamma ? fmul(st.z, gamma[c]) : st.z;
     const float sh = beta ? beta[c] : 0.f;
     const int64_t nv = (q.b1 - q.b0) / kVec;
     float v[kVecPerThread][8];
@@ -140,13 +144,13 @@ __global__ void __launch_bounds__(kThreads) k_fwd_norm(const TI* __restrict__ x,
       const int64_t j = threadIdx.x + (int64_t)k * kThreads;
       if (j < nv) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) v[k][e] = ffma(fsub(v[k][e], st.x), sc, sh);
+        for (int e = 0; e < 8; ++e) v[k][e] = ffma(fsub(fsub(v[k][e], st.x), st.y), sc, sh);
         IO<TO>::store8(y + q.b0 + j * kVec, v[k]);
       }
     }
     if ((int)threadIdx.x < scalar_count(q)) {
       const int64_t idx = scalar_index(q, threadIdx.x);
-      IO<TO>::store1(y + idx, ffma(fsub(IO<TI>::load1(x + idx), st.x), sc, sh));
+      IO<TO>::store1(y + idx, ffma(fsub(fsub(IO<TI>::load1(x + idx), st.x), st.y), sc, sh));
     }
   }
 }
