@@ -312,6 +312,7 @@ def run_gpu(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     build.build()
+    gn.gn3d_debug_set(gn.DEBUG_PATH, {"auto": 0, "streaming": 1, "fused": 2}[args.path])
     site = synth.WORKLOADS[args.workload].sites[0]
     vol = Volume(site, dev, pinned=True)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -364,7 +365,8 @@ def run_gpu(args):
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": args.workload, "N": site.N, "C": site.C, "D": site.D, "H": site.H,
                        "W": site.W, "G": site.G, "eps": site.eps, "parallelism": f"replicas x{ws}",
-                       "min_bytes_per_step": fb + bb, "l2": "flushed between steps (256 MiB write)"},
+                       "min_bytes_per_step": fb + bb, "l2": "flushed between steps (256 MiB write)",
+                       "path": args.path},
             "pct_of_8TBs": round(100 * value / ws / NOMINAL_HBM_GBS, 2),
             "pct_of_measured_copy": round(100 * value / ws / peak, 2),
             "fwd": {"ms": round(fwd_ms, 4), "gbs": round(fwd_gbs, 1)},
@@ -425,6 +427,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--impl", default="gn3d", choices=["gn3d", "reference"])
     ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--path", default="auto", choices=["auto", "streaming", "fused"],
+                    help="launch form (results are bit-identical; for A/B timing)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps

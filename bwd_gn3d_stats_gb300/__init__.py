@@ -147,3 +147,16 @@ def backward(dy, x, mean, rstd, gamma, G: int):
                   _dtype_code(x.dtype), dx.data_ptr(), dgamma.data_ptr(), dbeta.data_ptr(),
                   torch.cuda.current_stream(x.device).cuda_stream)
     return dx, dgamma, dbeta
+
+
+# ------------------------------------------------------------ testing hooks
+
+DEBUG_PATH, DEBUG_SPIN_LIMIT, DEBUG_FORCE_TIMEOUT, DEBUG_LAG, DEBUG_STASH, DEBUG_RING = range(6)
+PATH_AUTO, PATH_STREAMING, PATH_FUSED = 0, 1, 2
+
+
+def gn3d_debug_set(what: int, value: int):
+    L = lib()
+    L.gn3d_debug_set.argtypes = [ctypes.c_int, ctypes.c_longlong]
+    L.gn3d_debug_set.restype = ctypes.c_int
+    _check(L.gn3d_debug_set(what, value))

@@ -1,5 +1,10 @@
 // gn3d.cu -- libgn3d's C ABI: argument checks, the launch plan, per-call scratch
-// and the kernel launches for GroupNorm forward and backward (see include/gn3d.h).
+// and the kernel launches for GroupNorm forward and backward (include/gn3d.h).
+//
+// Two launch forms run the same units with the same arithmetic (bit-identical
+// results): the persistent cooperative kernels (gn3d_fused.cuh), used by
+// default, and the streaming kernels (gn3d_kernels.cuh), selectable through
+// gn3d_debug_set for cross-checks and A/B timing.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdio.h>
@@ -9,14 +14,29 @@
 #include <string>
 
 #include "../../include/gn3d.h"
+#include "gn3d_fused.cuh"
 #include "gn3d_kernels.cuh"
 
 namespace gn3d {
+
+// Device status word: bounded waits that give up record GN3D_ERR_TIMEOUT here.
+__device__ uint32_t g_status_word;
+
 namespace {
 
 thread_local std::string g_detail;
 thread_local std::string g_msg;
 std::atomic<uint64_t> g_launches{0};
+
+// testing / tuning hooks (gn3d_debug_set)
+std::atomic<long long> g_hook_path{0};     // 0 auto (fused), 1 streaming kernels, 2 fused kernels
+std::atomic<long long> g_hook_spin{0};     // 0 default poll budget
+std::atomic<long long> g_hook_timeout{0};  // 1: the next fused launch waits on a flag nothing sets
+std::atomic<long long> g_hook_lag{-1};     // -1 auto
+std::atomic<long long> g_hook_stash{-1};   // -1 auto
+std::atomic<long long> g_hook_ring{-1};    // -1 auto
+
+constexpr unsigned long long kDefaultSpin = 1ull << 26;  // ~4 s of polls at 64 ns sleeps
 
 int cuda_fail(cudaError_t e, const char* what) {
   g_detail = std::string(what) + ": " + cudaGetErrorString(e);
@@ -28,30 +48,50 @@ int arg_fail(const char* what) {
   return GN3D_ERR_INVALID_ARG;
 }
 
-#define GN3D_CUDA(call, what)                      \
-  do {                                             \
-    cudaError_t e_ = (call);                       \
+#define GN3D_CUDA(call, what)                          \
+  do {                                                 \
+    cudaError_t e_ = (call);                           \
     if (e_ != cudaSuccess) return cuda_fail(e_, what); \
   } while (0)
 
-// Per-device facts, read once.
+// Per-device facts and objects, created once.
 struct DevInfo {
   bool ready = false;
   int sms = 0;
+  int l2_bytes = 0;
+  int smem_optin = 0;
+  cudaMemPool_t pool = nullptr;
+  uint32_t* status = nullptr;
+  uint32_t attr_set = 0;  // kernels whose max dynamic shared memory was raised
 };
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 DevInfo g_dev[kMaxDevices];
 
-int device_info(int dev, DevInfo* out) {
+int device_info(int dev, DevInfo** out) {
   if (dev < 0 || dev >= kMaxDevices) return arg_fail("device ordinal out of range");
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_dev[dev].ready) {
-    GN3D_CUDA(cudaDeviceGetAttribute(&g_dev[dev].sms, cudaDevAttrMultiProcessorCount, dev),
-              "cudaDeviceGetAttribute");
-    g_dev[dev].ready = true;
+  DevInfo& d = g_dev[dev];
+  if (!d.ready) {
+    GN3D_CUDA(cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev), "device attribute");
+    GN3D_CUDA(cudaDeviceGetAttribute(&d.l2_bytes, cudaDevAttrL2CacheSize, dev), "device attribute");
+    GN3D_CUDA(cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev),
+              "device attribute");
+    // A pool of our own for the per-call scratch: the default pool trims
+    // freed memory at every synchronization, which makes the next call remap.
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    GN3D_CUDA(cudaMemPoolCreate(&d.pool, &props), "cudaMemPoolCreate");
+    uint64_t keep = 64ull << 20;
+    GN3D_CUDA(cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep), "pool attribute");
+    void* sym = nullptr;
+    GN3D_CUDA(cudaGetSymbolAddress(&sym, g_status_word), "cudaGetSymbolAddress");
+    d.status = static_cast<uint32_t*>(sym);
+    d.ready = true;
   }
-  *out = g_dev[dev];
+  *out = &d;
   return GN3D_OK;
 }
 
@@ -66,8 +106,7 @@ int check_ptr(const void* p, int dev, const char* name) {
   }
   if (a.type == cudaMemoryTypeManaged) return GN3D_OK;
   if (a.type == cudaMemoryTypeDevice && a.device == dev) return GN3D_OK;
-  g_detail = std::string(name) + (a.type == cudaMemoryTypeDevice ? ": on another device"
-                                                                   : ": not device memory");
+  g_detail = std::string(name) + (a.type == cudaMemoryTypeDevice ? ": on another device" : ": not device memory");
   return GN3D_ERR_DEVICE;
 }
 
@@ -77,10 +116,9 @@ int check_shape(int64_t N, int64_t C, int64_t D, int64_t H, int64_t W, int64_t G
   if (N < 0 || C < 0 || D < 0 || H < 0 || W < 0) return arg_fail("negative dimension");
   if (G <= 0) return arg_fail("G must be >= 1");
   if (C % G != 0) return arg_fail("C must be divisible by G");
-  // D*H*W and N*C*D*H*W must fit int64
   const double total = (double)N * (double)C * (double)D * (double)H * (double)W;
-  if (total > 9.0e18) return arg_fail("tensor too large");
-  if (N * (C / G) * D * H * W == 1 && C > 0)
+  if (total > 4.0e18) return arg_fail("tensor too large");
+  if (C > 0 && N * (C / G) * D * H * W == 1)
     return arg_fail("expected more than 1 value per group (N*(C/G)*D*H*W == 1)");
   return GN3D_OK;
 }
@@ -91,74 +129,151 @@ int grid_for(const DevInfo& di, int64_t units, int per_sm) {
   return (int)(g < 1 ? 1 : g);
 }
 
-template <class T>
-T* carve(char*& cur, int64_t count) {
-  T* p = reinterpret_cast<T*>(cur);
-  cur += ((count * (int64_t)sizeof(T) + 255) / 256) * 256;
-  return p;
+// Scratch carved out of one stream-ordered allocation, 256-byte aligned pieces.
+struct Scratch {
+  void* base = nullptr;
+  char* cur = nullptr;
+  template <class T>
+  T* take(int64_t count) {
+    T* p = reinterpret_cast<T*>(cur);
+    cur += ((count * (int64_t)sizeof(T) + 255) / 256) * 256;
+    return p;
+  }
+};
+
+int64_t rup(int64_t b) { return ((b + 255) / 256) * 256; }
+
+bool use_fused() { return g_hook_path.load() != 1; }
+
+unsigned long long spin_budget() {
+  const long long s = g_hook_spin.load();
+  return s > 0 ? (unsigned long long)s : kDefaultSpin;
+}
+
+// Slots of the persistent kernels: stream ring + two stash areas in shared memory.
+FusedCfg fused_cfg(const DevInfo& di, int slot_bytes, int64_t group_bytes) {
+  FusedCfg c;
+  const int budget = di.smem_optin - 4096;  // static shared memory of the kernel
+  int n = budget / (slot_bytes + 8);
+  if (n > kMaxSlots) n = kMaxSlots;
+  c.ring = n >= 4 ? 4 : (n >= 2 ? 2 : 1);
+  if (slot_bytes > 32768 && n >= 3) c.ring = 2;
+  c.stash = (n - c.ring) / 2;
+  // lag 1 keeps two groups in flight: only when both fit well inside L2
+  c.lag = (3 * group_bytes <= (int64_t)di.l2_bytes) ? 1 : 0;
+  const long long hr = g_hook_ring.load(), hs = g_hook_stash.load(), hl = g_hook_lag.load();
+  if (hr >= 1 && hr <= n) c.ring = (int)hr;
+  if (hs >= 0) c.stash = (int)hs;
+  if (c.ring + 2 * c.stash > n) c.stash = (n - c.ring) / 2;
+  if (hl >= 0) c.lag = hl ? 1 : 0;
+  c.force_timeout = g_hook_timeout.exchange(0) != 0;
+  c.spin = spin_budget();
+  return c;
+}
+
+int raise_smem(const void* func, DevInfo& di, uint32_t bit) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!(di.attr_set & bit)) {
+    GN3D_CUDA(cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, di.smem_optin),
+              "cudaFuncSetAttribute");
+    di.attr_set |= bit;
+  }
+  return GN3D_OK;
 }
 
 // --------------------------------------------------------------- forward
 template <class TI, class TO>
-int launch_forward(const void* x, const float* gamma, const float* beta, const Plan& p, float eps,
-                   void* y, float* mean, float* rstd, cudaStream_t st, const DevInfo& di) {
-  const int64_t bytes = 256 * 4 + p.units * (int64_t)sizeof(Part) + p.NG * (int64_t)(sizeof(float4) + sizeof(unsigned));
-  void* ws = nullptr;
-  GN3D_CUDA(cudaMallocAsync(&ws, (size_t)bytes, st), "cudaMallocAsync(workspace)");
-  char* cur = static_cast<char*>(ws);
+int launch_forward(const void* x, const float* gamma, const float* beta, const Plan& p, float eps, void* y,
+                   float* mean, float* rstd, cudaStream_t st, DevInfo& di) {
+  const bool fused = use_fused();
+  const int64_t nsync = p.NG + 1 + p.NG + 2;  // cnt, ready, abort, never
+  const int64_t bytes = rup(p.units * (int64_t)sizeof(Part)) + rup(p.NG * (int64_t)sizeof(float4)) +
+                        rup(nsync * (int64_t)sizeof(uint32_t));
+  Scratch s;
+  GN3D_CUDA(cudaMallocFromPoolAsync(&s.base, (size_t)bytes, di.pool, st), "scratch allocation");
+  s.cur = static_cast<char*>(s.base);
   FwdWs w;
-  w.cnt = carve<unsigned>(cur, p.NG);
-  w.stats = carve<float4>(cur, p.NG);
-  w.parts = carve<Part>(cur, p.units);
-  cudaError_t e = cudaMemsetAsync(w.cnt, 0, (size_t)p.NG * sizeof(unsigned), st);
-  if (e == cudaSuccess) {
+  uint32_t* sync = s.take<uint32_t>(nsync);
+  w.cnt = sync;
+  w.stats = s.take<float4>(p.NG);
+  w.parts = s.take<Part>(p.units);
+  cudaError_t e = cudaMemsetAsync(sync, 0, (size_t)nsync * sizeof(uint32_t), st);
+  const TI* xp = static_cast<const TI*>(x);
+  TO* yp = static_cast<TO*>(y);
+  if (e == cudaSuccess && fused) {
+    const int slot = kUnitElems * (int)sizeof(TI);
+    FusedCfg cfg = fused_cfg(di, slot, p.M * (int64_t)sizeof(TI));
+    FusedSync fs{sync, sync + p.NG + 1, sync + 2 * p.NG + 1, sync + 2 * p.NG + 2, di.status};
+    const int smem = (cfg.ring + 2 * cfg.stash) * (slot + 8);
+    auto k = k_fwd_fused<TI, TO>;
+    const uint32_t bit = (sizeof(TI) == 2 ? 1u : 4u) << (sizeof(TO) == 2 ? 0 : 1);
+    int rc = raise_smem((const void*)k, di, bit);
+    if (rc) { cudaFreeAsync(s.base, st); return rc; }
+    void* args[] = {(void*)&xp, (void*)&yp, (void*)&p, (void*)&w, (void*)&cfg, (void*)&fs, (void*)&eps,
+                    (void*)&gamma, (void*)&beta, (void*)&mean, (void*)&rstd};
+    g_launches += 1;
+    e = cudaLaunchCooperativeKernel((const void*)k, dim3(di.sms), dim3(kThreads), args, (size_t)smem, st);
+  } else if (e == cudaSuccess) {
     g_launches += 2;
-    k_fwd_stats<TI><<<grid_for(di, p.units, 8), kThreads, 0, st>>>(static_cast<const TI*>(x), p, w, eps,
-                                                                     mean, rstd);
+    k_fwd_stats<TI><<<grid_for(di, p.units, 4), kThreads, 0, st>>>(xp, p, w, eps, mean, rstd);
     e = cudaGetLastError();
+    if (e == cudaSuccess) {
+      k_fwd_norm<TI, TO><<<grid_for(di, p.units, 4), kThreads, 0, st>>>(xp, yp, p, w.stats, gamma, beta);
+      e = cudaGetLastError();
+    }
   }
-  if (e == cudaSuccess) {
-    k_fwd_norm<TI, TO><<<grid_for(di, p.units, 8), kThreads, 0, st>>>(
-        static_cast<const TI*>(x), static_cast<TO*>(y), p, w.stats, gamma, beta);
-    e = cudaGetLastError();
-  }
-  cudaError_t ef = cudaFreeAsync(ws, st);
+  cudaError_t ef = cudaFreeAsync(s.base, st);
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
-  if (ef != cudaSuccess) return cuda_fail(ef, "cudaFreeAsync(workspace)");
+  if (ef != cudaSuccess) return cuda_fail(ef, "scratch free");
   return GN3D_OK;
 }
 
 // -------------------------------------------------------------- backward
 template <class T>
-int launch_backward(const void* dy, const void* x, const float* mean, const float* rstd,
-                    const float* gamma, const Plan& p, void* dx, float* dgamma, float* dbeta,
-                    cudaStream_t st, const DevInfo& di) {
-  const int64_t bytes = 256 * 5 + p.units * (int64_t)sizeof(float2) + p.NC * (int64_t)sizeof(float2) +
-                        p.NG * (int64_t)sizeof(float2) + (p.NG + 1) * (int64_t)sizeof(unsigned);
-  void* ws = nullptr;
-  GN3D_CUDA(cudaMallocAsync(&ws, (size_t)bytes, st), "cudaMallocAsync(workspace)");
-  char* cur = static_cast<char*>(ws);
+int launch_backward(const void* dy, const void* x, const float* mean, const float* rstd, const float* gamma,
+                    const Plan& p, void* dx, float* dgamma, float* dbeta, cudaStream_t st, DevInfo& di) {
+  const bool fused = use_fused();
+  const int64_t nsync = p.NG + 1 + p.NG + 2;
+  const int64_t bytes = rup(p.units * (int64_t)sizeof(float2)) + rup(p.NC * (int64_t)sizeof(float2)) +
+                        rup(p.NG * (int64_t)sizeof(float2)) + rup(nsync * (int64_t)sizeof(uint32_t));
+  Scratch s;
+  GN3D_CUDA(cudaMallocFromPoolAsync(&s.base, (size_t)bytes, di.pool, st), "scratch allocation");
+  s.cur = static_cast<char*>(s.base);
   BwdWs w;
-  w.cnt = carve<unsigned>(cur, p.NG + 1);
-  w.coef = carve<float2>(cur, p.NG);
-  w.rows = carve<float2>(cur, p.NC);
-  w.parts = carve<float2>(cur, p.units);
-  cudaError_t e = cudaMemsetAsync(w.cnt, 0, (size_t)(p.NG + 1) * sizeof(unsigned), st);
-  if (e == cudaSuccess) {
+  uint32_t* sync = s.take<uint32_t>(nsync);
+  w.cnt = sync;
+  w.coef = s.take<float2>(p.NG);
+  w.rows = s.take<float2>(p.NC);
+  w.parts = s.take<float2>(p.units);
+  cudaError_t e = cudaMemsetAsync(sync, 0, (size_t)nsync * sizeof(uint32_t), st);
+  const T* dyp = static_cast<const T*>(dy);
+  const T* xp = static_cast<const T*>(x);
+  T* dxp = static_cast<T*>(dx);
+  if (e == cudaSuccess && fused) {
+    const int slot = 2 * kUnitElems * (int)sizeof(T);
+    FusedCfg cfg = fused_cfg(di, slot, 2 * p.M * (int64_t)sizeof(T));
+    FusedSync fs{sync, sync + p.NG + 1, sync + 2 * p.NG + 1, sync + 2 * p.NG + 2, di.status};
+    const int smem = (cfg.ring + 2 * cfg.stash) * (slot + 8);
+    auto k = k_bwd_fused<T>;
+    int rc = raise_smem((const void*)k, di, sizeof(T) == 2 ? 16u : 32u);
+    if (rc) { cudaFreeAsync(s.base, st); return rc; }
+    void* args[] = {(void*)&dyp, (void*)&xp, (void*)&dxp, (void*)&p, (void*)&mean, (void*)&rstd, (void*)&gamma,
+                    (void*)&w, (void*)&cfg, (void*)&fs, (void*)&dgamma, (void*)&dbeta};
+    g_launches += 1;
+    e = cudaLaunchCooperativeKernel((const void*)k, dim3(di.sms), dim3(kThreads), args, (size_t)smem, st);
+  } else if (e == cudaSuccess) {
     g_launches += 2;
-    k_bwd_reduce<T><<<grid_for(di, p.units, 6), kThreads, 0, st>>>(
-        static_cast<const T*>(dy), static_cast<const T*>(x), p, mean, rstd, gamma, w, dgamma, dbeta);
+    k_bwd_reduce<T><<<grid_for(di, p.units, 3), kThreads, 0, st>>>(dyp, xp, p, mean, rstd, gamma, w, dgamma,
+                                                                     dbeta);
     e = cudaGetLastError();
+    if (e == cudaSuccess) {
+      k_bwd_dx<T><<<grid_for(di, p.units, 3), kThreads, 0, st>>>(dyp, xp, dxp, p, mean, rstd, gamma, w.coef);
+      e = cudaGetLastError();
+    }
   }
-  if (e == cudaSuccess) {
-    k_bwd_dx<T><<<grid_for(di, p.units, 6), kThreads, 0, st>>>(
-        static_cast<const T*>(dy), static_cast<const T*>(x), static_cast<T*>(dx), p, mean, rstd, gamma,
-        w.coef);
-    e = cudaGetLastError();
-  }
-  cudaError_t ef = cudaFreeAsync(ws, st);
+  cudaError_t ef = cudaFreeAsync(s.base, st);
   if (e != cudaSuccess) return cuda_fail(e, "backward launch");
-  if (ef != cudaSuccess) return cuda_fail(ef, "cudaFreeAsync(workspace)");
+  if (ef != cudaSuccess) return cuda_fail(ef, "scratch free");
   return GN3D_OK;
 }
 
@@ -181,7 +296,7 @@ extern "C" int gn3d_forward(const void* x, const float* gamma, const float* beta
   const int64_t numel = p.NC * p.S;
   int dev = 0;
   GN3D_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
-  DevInfo di;
+  DevInfo* di = nullptr;
   if ((rc = device_info(dev, &di))) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (numel > 0) {
@@ -207,18 +322,17 @@ extern "C" int gn3d_forward(const void* x, const float* gamma, const float* beta
   }
   using bf = __nv_bfloat16;
   if (in_dtype == GN3D_BF16 && out_dtype == GN3D_BF16)
-    return launch_forward<bf, bf>(x, gamma, beta, p, feps, y, mean, rstd, st, di);
+    return launch_forward<bf, bf>(x, gamma, beta, p, feps, y, mean, rstd, st, *di);
   if (in_dtype == GN3D_BF16 && out_dtype == GN3D_F32)
-    return launch_forward<bf, float>(x, gamma, beta, p, feps, y, mean, rstd, st, di);
+    return launch_forward<bf, float>(x, gamma, beta, p, feps, y, mean, rstd, st, *di);
   if (in_dtype == GN3D_F32 && out_dtype == GN3D_BF16)
-    return launch_forward<float, bf>(x, gamma, beta, p, feps, y, mean, rstd, st, di);
-  return launch_forward<float, float>(x, gamma, beta, p, feps, y, mean, rstd, st, di);
+    return launch_forward<float, bf>(x, gamma, beta, p, feps, y, mean, rstd, st, *di);
+  return launch_forward<float, float>(x, gamma, beta, p, feps, y, mean, rstd, st, *di);
 }
 
 extern "C" int gn3d_backward(const void* dy, const void* x, const float* mean, const float* rstd,
                              const float* gamma, int64_t N, int64_t C, int64_t D, int64_t H, int64_t W,
-                             int64_t G, gn3d_dtype dtype, void* dx, float* dgamma, float* dbeta,
-                             void* stream) {
+                             int64_t G, gn3d_dtype dtype, void* dx, float* dgamma, float* dbeta, void* stream) {
   int rc = check_shape(N, C, D, H, W, G);
   if (rc) return rc;
   if (!valid_dtype(dtype)) return arg_fail("unsupported dtype");
@@ -226,7 +340,7 @@ extern "C" int gn3d_backward(const void* dy, const void* x, const float* mean, c
   const int64_t numel = p.NC * p.S;
   int dev = 0;
   GN3D_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
-  DevInfo di;
+  DevInfo* di = nullptr;
   if ((rc = device_info(dev, &di))) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (C > 0) {
@@ -245,13 +359,57 @@ extern "C" int gn3d_backward(const void* dy, const void* x, const float* mean, c
       (rc = check_ptr(mean, dev, "mean")) || (rc = check_ptr(rstd, dev, "rstd")))
     return rc;
   if (dtype == GN3D_BF16)
-    return launch_backward<__nv_bfloat16>(dy, x, mean, rstd, gamma, p, dx, dgamma, dbeta, st, di);
-  return launch_backward<float>(dy, x, mean, rstd, gamma, p, dx, dgamma, dbeta, st, di);
+    return launch_backward<__nv_bfloat16>(dy, x, mean, rstd, gamma, p, dx, dgamma, dbeta, st, *di);
+  return launch_backward<float>(dy, x, mean, rstd, gamma, p, dx, dgamma, dbeta, st, *di);
 }
 
 extern "C" int gn3d_stream_status(void* stream) {
-  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return cuda_fail(e, "stream");
+  int dev = 0;
+  GN3D_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  DevInfo* di = nullptr;
+  int rc = device_info(dev, &di);
+  if (rc) return rc;
+  uint32_t word = 0;
+  GN3D_CUDA(cudaMemcpy(&word, di->status, sizeof(word), cudaMemcpyDeviceToHost), "status read");
+  if (word != 0) {
+    const uint32_t zero = 0;
+    GN3D_CUDA(cudaMemcpy(di->status, &zero, sizeof(zero), cudaMemcpyHostToDevice), "status clear");
+    return (int)word;
+  }
+  return GN3D_OK;
+}
+
+extern "C" int gn3d_debug_set(int what, long long value) {
+  switch (what) {
+    case GN3D_DEBUG_PATH:
+      if (value < 0 || value > 2) return arg_fail("path: 0, 1 or 2");
+      g_hook_path = value;
+      break;
+    case GN3D_DEBUG_SPIN_LIMIT:
+      if (value < 0) return arg_fail("spin limit >= 0");
+      g_hook_spin = value;
+      break;
+    case GN3D_DEBUG_FORCE_TIMEOUT:
+      g_hook_timeout = value ? 1 : 0;
+      break;
+    case GN3D_DEBUG_LAG:
+      if (value < -1 || value > 1) return arg_fail("lag: -1, 0 or 1");
+      g_hook_lag = value;
+      break;
+    case GN3D_DEBUG_STASH:
+      if (value < -1 || value > 13) return arg_fail("stash: -1 .. 13");
+      g_hook_stash = value;
+      break;
+    case GN3D_DEBUG_RING:
+      if (value < -1 || value > 8 || value == 0) return arg_fail("ring: -1, 1 .. 8");
+      g_hook_ring = value;
+      break;
+    default:
+      return arg_fail("unknown debug setting");
+  }
   return GN3D_OK;
 }
 
@@ -268,4 +426,4 @@ extern "C" const char* gn3d_error_string(int status) {
 
 extern "C" uint64_t gn3d_launch_count(void) { return g_launches.load(); }
 
-extern "C" const char* gn3d_version(void) { return "gn3d 0.1.0 sm_103a"; }
+extern "C" const char* gn3d_version(void) { return "gn3d 0.2.0 sm_103a"; }

@@ -23,9 +23,9 @@ namespace gn3d {
 
 constexpr int kVec = 8;             // elements per vector
 constexpr int kUnitElems = 8192;    // body elements per unit (multiple of kVec)
-constexpr int kThreads = 256;       // threads per CTA of the unit kernels
+constexpr int kThreads = 512;       // threads per CTA of the unit kernels
 constexpr int kWarps = kThreads / 32;
-constexpr int kVecPerThread = kUnitElems / kVec / kThreads;  // 4
+constexpr int kVecPerThread = kUnitElems / kVec / kThreads;  // 2
 constexpr int kMaxScalars = 14;     // head + tail elements of one unit, at most
 
 struct Plan {

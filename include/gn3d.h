@@ -111,7 +111,36 @@ const char* gn3d_error_string(int status);
  * region).  Memory-set and copy operations are not counted. */
 uint64_t gn3d_launch_count(void);
 
-/* Library version, e.g. "gn3d 0.1.0 sm_103a". */
+/*
+ * Testing and tuning hooks (process-wide, not thread-scoped; not needed for
+ * normal use -- every setting defaults to automatic).  None of them changes a
+ * result bit: both launch forms run the same units and reduction trees.
+ *   GN3D_DEBUG_PATH          0 automatic (persistent kernels), 1 streaming
+ *                            kernels (two launches per direction), 2 persistent.
+ *   GN3D_DEBUG_SPIN_LIMIT    poll budget of every bounded device-side wait
+ *                            (0 = default, about four seconds).
+ *   GN3D_DEBUG_FORCE_TIMEOUT 1: the next persistent launch waits for a flag that
+ *                            nothing sets, so its bounded wait runs out and
+ *                            gn3d_stream_status reports GN3D_ERR_TIMEOUT (tests
+ *                            the failure path without a fault or a hang).
+ *   GN3D_DEBUG_LAG           -1 automatic, 0 or 1: groups of lookahead between
+ *                            the statistics pass and the elementwise pass.
+ *   GN3D_DEBUG_STASH         -1 automatic, else shared-memory stash slots per
+ *                            group parity.
+ *   GN3D_DEBUG_RING          -1 automatic, else bulk-copy stream slots.
+ * Returns GN3D_OK or GN3D_ERR_INVALID_ARG for an unknown setting or value.
+ */
+enum {
+  GN3D_DEBUG_PATH = 0,
+  GN3D_DEBUG_SPIN_LIMIT = 1,
+  GN3D_DEBUG_FORCE_TIMEOUT = 2,
+  GN3D_DEBUG_LAG = 3,
+  GN3D_DEBUG_STASH = 4,
+  GN3D_DEBUG_RING = 5
+};
+int gn3d_debug_set(int what, long long value);
+
+/* Library version, e.g. "gn3d 0.2.0 sm_103a". */
 const char* gn3d_version(void);
 
 #ifdef __cplusplus

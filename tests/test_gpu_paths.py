@@ -1,0 +1,91 @@
+"""The two launch forms (persistent cooperative kernels and streaming kernels)
+and every tuning setting give bit-identical results; the bounded-wait failure
+path reports GN3D_ERR_TIMEOUT and leaves the library usable."""
+import numpy as np
+import pytest
+
+import bwd_gn3d_stats_gb300 as gn
+from bwd_gn3d_stats_gb300 import synth
+
+from .gpu_util import device_inputs, run_backward, run_forward, to_np, torch
+
+pytestmark = pytest.mark.gpu
+
+SETTINGS = [gn.DEBUG_PATH, gn.DEBUG_LAG, gn.DEBUG_STASH, gn.DEBUG_RING, gn.DEBUG_SPIN_LIMIT]
+DEFAULTS = {gn.DEBUG_PATH: 0, gn.DEBUG_LAG: -1, gn.DEBUG_STASH: -1, gn.DEBUG_RING: -1, gn.DEBUG_SPIN_LIMIT: 0}
+
+
+@pytest.fixture(autouse=True)
+def _reset():
+    from bwd_gn3d_stats_gb300 import build
+
+    build.build()
+    yield
+    for k, v in DEFAULTS.items():
+        gn.gn3d_debug_set(k, v)
+
+
+def run_all(site, d):
+    y, mean, rstd = run_forward(site, d["x"], d["gamma"], d["beta"])
+    dx, dg, db = run_backward(site, d["dy"], d["x"], mean, rstd, d["gamma"])
+    torch().cuda.synchronize()
+    return [to_np(t) for t in (y, mean, rstd, dx, dg, db)]
+
+
+def same(a, b):
+    return all(np.array_equal(u.view(np.uint8), v.view(np.uint8)) for u, v in zip(a, b))
+
+
+SHAPES = [
+    (1, 32, 40, 40, 40, 8, synth.BF16),
+    (2, 8, 5, 6, 7, 4, synth.BF16),
+    (1, 48, 13, 11, 9, 8, synth.BF16),
+    (2, 6, 1, 1, 1, 6, synth.F32),
+    (1, 16, 24, 24, 24, 2, synth.F32),
+    (1, 512, 8, 8, 8, 8, synth.BF16),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s[:6])) + "_" + s[6])
+def test_fused_and_streaming_bit_identical(shape):
+    site = synth.Site(*shape)
+    d = device_inputs(synth.make_inputs(site, seed=11))
+    gn.gn3d_debug_set(gn.DEBUG_PATH, gn.PATH_FUSED)
+    a = run_all(site, d)
+    gn.gn3d_debug_set(gn.DEBUG_PATH, gn.PATH_STREAMING)
+    b = run_all(site, d)
+    assert same(a, b)
+
+
+@pytest.mark.parametrize("knob,values", [(gn.DEBUG_LAG, [0, 1]), (gn.DEBUG_STASH, [0, 1, 3]),
+                                         (gn.DEBUG_RING, [1, 2, 3])])
+def test_tuning_does_not_move_a_bit(knob, values):
+    site = synth.Site(1, 32, 36, 36, 36, 8, synth.BF16)
+    d = device_inputs(synth.make_inputs(site, seed=12))
+    ref = run_all(site, d)
+    for v in values:
+        gn.gn3d_debug_set(knob, v)
+        assert same(ref, run_all(site, d)), f"setting {knob}={v} changed the result"
+
+
+def test_bounded_wait_timeout_reports_and_recovers():
+    site = synth.Site(1, 8, 24, 24, 24, 4, synth.BF16)
+    d = device_inputs(synth.make_inputs(site, seed=13))
+    ref = run_all(site, d)
+    st = torch().cuda.current_stream().cuda_stream
+    gn.gn3d_debug_set(gn.DEBUG_SPIN_LIMIT, 20000)
+    gn.gn3d_debug_set(gn.DEBUG_FORCE_TIMEOUT, 1)
+    run_forward(site, d["x"], d["gamma"], d["beta"])
+    L = gn.lib()
+    assert L.gn3d_stream_status(st) == gn.ERR_TIMEOUT
+    assert L.gn3d_stream_status(st) == gn.OK  # read-and-clear
+    gn.gn3d_debug_set(gn.DEBUG_SPIN_LIMIT, 0)
+    assert same(ref, run_all(site, d))
+
+
+def test_launch_count_one_kernel_per_direction():
+    site = synth.Site(1, 8, 16, 16, 16, 4, synth.BF16)
+    d = device_inputs(synth.make_inputs(site, seed=14))
+    n0 = gn.gn3d_launch_count()
+    run_all(site, d)
+    assert gn.gn3d_launch_count() - n0 == 2
