@@ -62,7 +62,7 @@ struct DevInfo {
   int smem_optin = 0;
   cudaMemPool_t pool = nullptr;
   uint32_t* status = nullptr;
-  uint32_t attr_set = 0;  // kernels whose max dynamic shared memory was raised
+  int attr_smem[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // dynamic shared memory raised to, per kernel
 };
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
@@ -153,7 +153,7 @@ unsigned long long spin_budget() {
 // Slots of the persistent kernels: stream ring + two stash areas in shared memory.
 FusedCfg fused_cfg(const DevInfo& di, int slot_bytes, int64_t group_bytes) {
   FusedCfg c;
-  const int budget = di.smem_optin - 4096;  // static shared memory of the kernel
+  const int budget = di.smem_optin - 4096;  // leaves room for the kernels' static shared memory
   int n = budget / (slot_bytes + 8);
   if (n > kMaxSlots) n = kMaxSlots;
   c.ring = n >= 4 ? 4 : (n >= 2 ? 2 : 1);
@@ -171,12 +171,12 @@ FusedCfg fused_cfg(const DevInfo& di, int slot_bytes, int64_t group_bytes) {
   return c;
 }
 
-int raise_smem(const void* func, DevInfo& di, uint32_t bit) {
+int raise_smem(const void* func, int bytes, DevInfo& di, int which) {
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!(di.attr_set & bit)) {
-    GN3D_CUDA(cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, di.smem_optin),
+  if (di.attr_smem[which] < bytes) {
+    GN3D_CUDA(cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes),
               "cudaFuncSetAttribute");
-    di.attr_set |= bit;
+    di.attr_smem[which] = bytes;
   }
   return GN3D_OK;
 }
@@ -206,8 +206,8 @@ int launch_forward(const void* x, const float* gamma, const float* beta, const P
     FusedSync fs{sync, sync + p.NG + 1, sync + 2 * p.NG + 1, sync + 2 * p.NG + 2, di.status};
     const int smem = (cfg.ring + 2 * cfg.stash) * (slot + 8);
     auto k = k_fwd_fused<TI, TO>;
-    const uint32_t bit = (sizeof(TI) == 2 ? 1u : 4u) << (sizeof(TO) == 2 ? 0 : 1);
-    int rc = raise_smem((const void*)k, di, bit);
+    const int which = (sizeof(TI) == 2 ? 0 : 2) + (sizeof(TO) == 2 ? 0 : 1);
+    int rc = raise_smem((const void*)k, smem, di, which);
     if (rc) { cudaFreeAsync(s.base, st); return rc; }
     void* args[] = {(void*)&xp, (void*)&yp, (void*)&p, (void*)&w, (void*)&cfg, (void*)&fs, (void*)&eps,
                     (void*)&gamma, (void*)&beta, (void*)&mean, (void*)&rstd};
@@ -255,7 +255,7 @@ int launch_backward(const void* dy, const void* x, const float* mean, const floa
     FusedSync fs{sync, sync + p.NG + 1, sync + 2 * p.NG + 1, sync + 2 * p.NG + 2, di.status};
     const int smem = (cfg.ring + 2 * cfg.stash) * (slot + 8);
     auto k = k_bwd_fused<T>;
-    int rc = raise_smem((const void*)k, di, sizeof(T) == 2 ? 16u : 32u);
+    int rc = raise_smem((const void*)k, smem, di, sizeof(T) == 2 ? 4 : 5);
     if (rc) { cudaFreeAsync(s.base, st); return rc; }
     void* args[] = {(void*)&dyp, (void*)&xp, (void*)&dxp, (void*)&p, (void*)&mean, (void*)&rstd, (void*)&gamma,
                     (void*)&w, (void*)&cfg, (void*)&fs, (void*)&dgamma, (void*)&dbeta};
