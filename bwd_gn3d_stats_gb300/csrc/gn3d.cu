@@ -60,6 +60,7 @@ struct DevInfo {
   int sms = 0;
   int l2_bytes = 0;
   int smem_optin = 0;
+  int smem_per_sm = 0;
   cudaMemPool_t pool = nullptr;
   uint32_t* status = nullptr;
   int attr_smem[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // dynamic shared memory raised to, per kernel
@@ -76,6 +77,8 @@ int device_info(int dev, DevInfo** out) {
     GN3D_CUDA(cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev), "device attribute");
     GN3D_CUDA(cudaDeviceGetAttribute(&d.l2_bytes, cudaDevAttrL2CacheSize, dev), "device attribute");
     GN3D_CUDA(cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev),
+              "device attribute");
+    GN3D_CUDA(cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev),
               "device attribute");
     // A pool of our own for the per-call scratch: the default pool trims
     // freed memory at every synchronization, which makes the next call remap.
@@ -153,7 +156,10 @@ unsigned long long spin_budget() {
 // Slots of the persistent kernels: stream ring + two stash areas in shared memory.
 FusedCfg fused_cfg(const DevInfo& di, int slot_bytes, int64_t group_bytes) {
   FusedCfg c;
-  const int budget = di.smem_optin - 4096;  // leaves room for the kernels' static shared memory
+  // kFusedCtasPerSm CTAs share an SM's shared memory; each also holds ~1 KB of
+  // static shared memory and the system's 1 KB per-CTA reservation.
+  int budget = di.smem_per_sm / kFusedCtasPerSm - 3072;
+  if (budget > di.smem_optin - 2048) budget = di.smem_optin - 2048;
   int n = budget / (slot_bytes + 8);
   if (n > kMaxSlots) n = kMaxSlots;
   c.ring = n >= 4 ? 4 : (n >= 2 ? 2 : 1);
@@ -178,6 +184,19 @@ int raise_smem(const void* func, int bytes, DevInfo& di, int which) {
               "cudaFuncSetAttribute");
     di.attr_smem[which] = bytes;
   }
+  return GN3D_OK;
+}
+
+// Grid of a persistent launch: every CTA must be resident at once.
+int coop_grid(const void* func, int smem, const DevInfo& di, int* grid) {
+  int per_sm = 0;
+  GN3D_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, func, kThreads, (size_t)smem), "occupancy");
+  if (per_sm < 1) {
+    g_detail = "persistent kernel does not fit on an SM";
+    return GN3D_ERR_CUDA;
+  }
+  if (per_sm > kFusedCtasPerSm) per_sm = kFusedCtasPerSm;
+  *grid = di.sms * per_sm;
   return GN3D_OK;
 }
 
@@ -211,8 +230,11 @@ int launch_forward(const void* x, const float* gamma, const float* beta, const P
     if (rc) { cudaFreeAsync(s.base, st); return rc; }
     void* args[] = {(void*)&xp, (void*)&yp, (void*)&p, (void*)&w, (void*)&cfg, (void*)&fs, (void*)&eps,
                     (void*)&gamma, (void*)&beta, (void*)&mean, (void*)&rstd};
+    int grid = 0;
+    rc = coop_grid((const void*)k, smem, di, &grid);
+    if (rc) { cudaFreeAsync(s.base, st); return rc; }
     g_launches += 1;
-    e = cudaLaunchCooperativeKernel((const void*)k, dim3(di.sms), dim3(kThreads), args, (size_t)smem, st);
+    e = cudaLaunchCooperativeKernel((const void*)k, dim3(grid), dim3(kThreads), args, (size_t)smem, st);
   } else if (e == cudaSuccess) {
     g_launches += 2;
     k_fwd_stats<TI><<<grid_for(di, p.units, 4), kThreads, 0, st>>>(xp, p, w, eps, mean, rstd);
@@ -259,8 +281,11 @@ int launch_backward(const void* dy, const void* x, const float* mean, const floa
     if (rc) { cudaFreeAsync(s.base, st); return rc; }
     void* args[] = {(void*)&dyp, (void*)&xp, (void*)&dxp, (void*)&p, (void*)&mean, (void*)&rstd, (void*)&gamma,
                     (void*)&w, (void*)&cfg, (void*)&fs, (void*)&dgamma, (void*)&dbeta};
+    int grid = 0;
+    rc = coop_grid((const void*)k, smem, di, &grid);
+    if (rc) { cudaFreeAsync(s.base, st); return rc; }
     g_launches += 1;
-    e = cudaLaunchCooperativeKernel((const void*)k, dim3(di.sms), dim3(kThreads), args, (size_t)smem, st);
+    e = cudaLaunchCooperativeKernel((const void*)k, dim3(grid), dim3(kThreads), args, (size_t)smem, st);
   } else if (e == cudaSuccess) {
     g_launches += 2;
     k_bwd_reduce<T><<<grid_for(di, p.units, 3), kThreads, 0, st>>>(dyp, xp, p, mean, rstd, gamma, w, dgamma,

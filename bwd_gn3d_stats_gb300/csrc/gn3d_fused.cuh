@@ -37,6 +37,7 @@
 namespace gn3d {
 
 constexpr int kMaxSlots = 30;
+constexpr int kFusedCtasPerSm = 2;
 constexpr uint32_t kStatusTimeout = 4;  // GN3D_ERR_TIMEOUT
 
 struct FusedCfg {
@@ -56,8 +57,12 @@ struct FusedSync {
 };
 
 // ------------------------------------------------------------ scheduling
+// CTA pid of P owns the units u = pid (mod P); inside group g these are
+// first(g), first(g) + P, ...  Phases: STAT(g) in increasing unit order, NORM(g)
+// in decreasing order; the stashed units are the last `stash` of each group.
 struct Sched {
-  int64_t P, pid, NG, upg;
+  int64_t P, pid, NG, upg, R;
+  int64_t qP, rP;  // P / R and P % R: stepping u by P moves (row, k) by these
   int stash, lag;
 
   __device__ __forceinline__ int64_t first(int64_t g) const {
@@ -66,13 +71,9 @@ struct Sched {
     if (off < 0) off += P;
     return base + off;
   }
-  __device__ __forceinline__ int64_t count(int64_t g) const {
-    const int64_t u0 = first(g), end = (g + 1) * upg;
+  __device__ __forceinline__ int64_t count_from(int64_t g, int64_t u0) const {
+    const int64_t end = (g + 1) * upg;
     return u0 < end ? (end - 1 - u0) / P + 1 : 0;
-  }
-  __device__ __forceinline__ int64_t stashed(int64_t g) const {
-    const int64_t n = count(g);
-    return n < stash ? n : stash;
   }
   // phase k -> (kind, group); false when k names no phase (STAT beyond the last group)
   __device__ __forceinline__ bool phase(int64_t k, int& kind, int64_t& g) const {
@@ -97,15 +98,18 @@ enum { kStat = 0, kNorm = 1, kEnd = 2 };
 
 struct Task {
   int kind;
-  int64_t g, j, u;
-  bool stashed;
+  int64_t g, u, row, kr;
+  bool stashed, last_in_phase;
   int sidx;  // stash slot within the group's parity area
 };
 
+// Position in the task sequence.  Per phase it costs a few divisions; per task
+// it only adds or subtracts, so thread 0 can run it ahead cheaply.
 struct TaskIt {
-  int64_t k, idx, n;
+  int64_t k, idx, n, ns, u0;
   int kind;
   int64_t g;
+  int64_t u, row, kr;
 
   __device__ __forceinline__ void seek(const Sched& s) {
     for (;; ++k) {
@@ -113,23 +117,40 @@ struct TaskIt {
       int kd;
       int64_t gg;
       if (!s.phase(k, kd, gg)) continue;
-      const int64_t c = s.count(gg);
-      if (c > 0) { kind = kd; g = gg; n = c; idx = 0; return; }
+      const int64_t f = s.first(gg);
+      const int64_t c = s.count_from(gg, f);
+      if (c > 0) {
+        kind = kd; g = gg; n = c; idx = 0; u0 = f;
+        ns = c < s.stash ? c : s.stash;
+        u = kind == kStat ? f : f + (c - 1) * s.P;
+        row = u / s.R;
+        kr = u - row * s.R;
+        return;
+      }
     }
   }
   __device__ __forceinline__ void start(const Sched& s) { k = 0; seek(s); }
   __device__ __forceinline__ void next(const Sched& s) {
-    if (++idx >= n) { ++k; seek(s); }
+    if (++idx >= n) { ++k; seek(s); return; }
+    if (kind == kStat) {
+      u += s.P; row += s.qP; kr += s.rP;
+      if (kr >= s.R) { kr -= s.R; ++row; }
+    } else {
+      u -= s.P; row -= s.qP; kr -= s.rP;
+      if (kr < 0) { kr += s.R; --row; }
+    }
   }
-  __device__ __forceinline__ Task cur(const Sched& s) const {
+  __device__ __forceinline__ Task cur() const {
     Task t;
     t.kind = kind;
     t.g = g;
-    t.j = kind == kStat ? idx : n - 1 - idx;
-    t.u = s.first(g) + t.j * s.P;
-    const int64_t ns = s.stashed(g);
-    t.stashed = t.j >= n - ns;
-    t.sidx = (int)(t.j - (n - ns));
+    t.u = u;
+    t.row = row;
+    t.kr = kr;
+    const int64_t j = kind == kStat ? idx : n - 1 - idx;
+    t.stashed = j >= n - ns;
+    t.sidx = (int)(j - (n - ns));
+    t.last_in_phase = idx == n - 1;
     return t;
   }
 };
@@ -145,18 +166,26 @@ __device__ __forceinline__ bool wait_ready(const uint32_t* flag, const FusedSync
   while (ld_acquire(flag) == 0) {
     if (ld_relaxed(fs.abort) != 0) return false;
     if (++it > spin) return false;
-    __nanosleep(64);
+    __nanosleep(32);
   }
   return true;
 }
 
+// Row -> channel, in 32 bits when the row index allows it.
+__device__ __forceinline__ int64_t channel_of(int64_t row, int64_t C) {
+  if (row < 0x7FFFFFFF && C < 0x7FFFFFFF) return (int64_t)((uint32_t)row % (uint32_t)C);
+  return row % C;
+}
+
 // ------------------------------------------------------------- the kernel
 // Op supplies the direction-specific parts:
-//   kTensors                     tensors per unit in a slot (1: x; 2: x then dy)
-//   src(t)                       base pointer of tensor t
-//   stat(slot, q, u, g, ...)     statistics of one unit (all threads)
-//   prepare(g)                   load group g's published statistics (all threads)
-//   norm(slot, q)                elementwise pass of one unit (all threads)
+//   kTensors                          tensors per unit in a slot (1: x; 2: x then dy)
+//   src(t)                            base pointer of tensor t
+//   stat(slot, q, u, g, arrive, n)    statistics of one unit (all threads); when
+//                                     `arrive`, also the CTA's arrival for group g
+//                                     with its n units (and the group finalize if last)
+//   prepare(g)                        load group g's published statistics (all threads)
+//   norm(slot, q)                     elementwise pass of one unit (all threads)
 template <class Op>
 __device__ __forceinline__ void run_fused(Op& op, const Plan& p, const FusedCfg& cfg, const FusedSync& fs) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -172,6 +201,9 @@ __device__ __forceinline__ void run_fused(Op& op, const Plan& p, const FusedCfg&
   s.pid = blockIdx.x;
   s.NG = p.NG;
   s.upg = p.upg;
+  s.R = p.R;
+  s.qP = s.P / s.R;
+  s.rP = s.P - s.qP * s.R;
   s.stash = cfg.stash;
   s.lag = cfg.lag;
 
@@ -198,7 +230,7 @@ __device__ __forceinline__ void run_fused(Op& op, const Plan& p, const FusedCfg&
     // ---- producer: issue bulk copies ahead while their slots are free
     if (threadIdx.x == 0) {
       while (pt.kind != kEnd) {
-        const Task t = pt.cur(s);
+        const Task t = pt.cur();
         int slot;
         if (t.stashed) {
           if (t.kind == kNorm) { pt.next(s); continue; }     // data stays from STAT
@@ -208,7 +240,7 @@ __device__ __forceinline__ void run_fused(Op& op, const Plan& p, const FusedCfg&
           if (lp >= lc + (uint64_t)cfg.ring) break;          // ring full
           slot = (int)(lp % (uint64_t)cfg.ring);
         }
-        const URange q = unit_range(p, t.u);
+        const URange q = unit_range_rk(p, t.row, t.kr);
         const uint32_t bytes = (uint32_t)((q.b1 - q.b0) * (int64_t)sizeof(T));
         unsigned char* dst = smem + (size_t)slot * kSlotBytes;
         fence_proxy_async_smem();
@@ -225,8 +257,8 @@ __device__ __forceinline__ void run_fused(Op& op, const Plan& p, const FusedCfg&
     }
 
     // ---- consumer
-    const Task t = ct.cur(s);
-    const URange q = unit_range(p, t.u);
+    const Task t = ct.cur();
+    const URange q = unit_range_rk(p, t.row, t.kr);
     if (t.kind == kNorm && t.g != norm_group) {
       if (threadIdx.x == 0) {
         const uint32_t* flag = forced ? fs.never : fs.ready + t.g;
@@ -256,8 +288,8 @@ __device__ __forceinline__ void run_fused(Op& op, const Plan& p, const FusedCfg&
       if (s_fail) break;
     }
     const unsigned char* data = smem + (size_t)slot * kSlotBytes;
-    if (t.kind == kStat) op.stat(data, q, t.u, t.g);
-    else op.norm(data, q);
+    if (t.kind == kStat) op.stat(data, q, t.u, t.g, t.last_in_phase, ct.n);
+    else op.norm(data, q, channel_of(t.row, p.C));
     __syncthreads();  // every thread is done with the slot
     if (!t.stashed) ++lc;
     else if (t.kind == kStat) stash_par ^= 1u << (slot - cfg.ring);
@@ -315,15 +347,19 @@ struct FwdOp {
     r.s = r.sok ? IO<TI>::load1(x + scalar_index(q, threadIdx.x)) : 0.f;
   }
 
-  __device__ __forceinline__ void stat(const unsigned char* slot, const URange& q, int64_t u, int64_t g) {
+  __device__ __forceinline__ void stat(const unsigned char* slot, const URange& q, int64_t u, int64_t g,
+                                      bool arrive, int64_t n) {
     UnitRegs<TI> r;
     load_regs(slot, q, r);
     const Part m = unit_moments(r, q.n, red);
     if (threadIdx.x == 0) {
       ws.parts[u] = m;
-      __threadfence();
-      *s_last = atomicAdd(&fs.cnt[g], 1u) == (unsigned)(p.upg - 1);
+      if (arrive) {
+        __threadfence();
+        *s_last = atomicAdd(&fs.cnt[g], (unsigned)n) + (unsigned)n == (unsigned)p.upg;
+      }
     }
+    if (!arrive) return;
     __syncthreads();
     if (*s_last) {
       __threadfence();
@@ -337,8 +373,7 @@ struct FwdOp {
 
   __device__ __forceinline__ void prepare(int64_t g) { st = __ldcg(ws.stats + g); }
 
-  __device__ __forceinline__ void norm(const unsigned char* slot, const URange& q) {
-    const int64_t c = q.row % p.C;
+  __device__ __forceinline__ void norm(const unsigned char* slot, const URange& q, int64_t c) {
     const float sc = gamma ? fmul(st.z, gamma[c]) : st.z;
     const float sh = beta ? beta[c] : 0.f;
     const TI* sp = reinterpret_cast<const TI*>(slot);
@@ -362,7 +397,7 @@ struct FwdOp {
 };
 
 template <class TI, class TO>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, kFusedCtasPerSm)
     k_fwd_fused(const TI* __restrict__ x, TO* __restrict__ y, Plan p, FwdWs ws, FusedCfg cfg, FusedSync fs,
                 float eps, const float* __restrict__ gamma, const float* __restrict__ beta, float* mean_out,
                 float* rstd_out) {
@@ -423,15 +458,19 @@ struct BwdOp {
     }
   }
 
-  __device__ __forceinline__ void stat(const unsigned char* slot, const URange& q, int64_t u, int64_t g) {
+  __device__ __forceinline__ void stat(const unsigned char* slot, const URange& q, int64_t u, int64_t g,
+                                      bool arrive, int64_t n) {
     UnitRegs<T> rx, rd;
     load_pair(slot, q, rx, rd);
     const float2 sums = unit_bwd_sums(rd, rx, mean[g], red);
     if (threadIdx.x == 0) {
       ws.parts[u] = sums;
-      __threadfence();
-      s_flags[0] = atomicAdd(&fs.cnt[g], 1u) == (unsigned)(p.upg - 1);
+      if (arrive) {
+        __threadfence();
+        s_flags[0] = atomicAdd(&fs.cnt[g], (unsigned)n) + (unsigned)n == (unsigned)p.upg;
+      }
     }
+    if (!arrive) return;
     __syncthreads();
     if (s_flags[0]) {
       __threadfence();
@@ -458,8 +497,7 @@ struct BwdOp {
     b = ab.y;
   }
 
-  __device__ __forceinline__ void norm(const unsigned char* slot, const URange& q) {
-    const int64_t c = q.row % p.C;
+  __device__ __forceinline__ void norm(const unsigned char* slot, const URange& q, int64_t c) {
     const float gm = gamma ? gamma[c] : 1.f;
     const T* sx = reinterpret_cast<const T*>(slot);
     const T* sd = sx + kUnitElems;
@@ -490,7 +528,7 @@ struct BwdOp {
 };
 
 template <class T>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, kFusedCtasPerSm)
     k_bwd_fused(const T* __restrict__ dy, const T* __restrict__ x, T* __restrict__ dx, Plan p,
                 const float* __restrict__ mean, const float* __restrict__ rstd, const float* __restrict__ gamma,
                 BwdWs ws, FusedCfg cfg, FusedSync fs, float* dgamma, float* dbeta) {

@@ -23,9 +23,9 @@ namespace gn3d {
 
 constexpr int kVec = 8;             // elements per vector
 constexpr int kUnitElems = 8192;    // body elements per unit (multiple of kVec)
-constexpr int kThreads = 512;       // threads per CTA of the unit kernels
+constexpr int kThreads = 256;       // threads per CTA of the unit kernels
 constexpr int kWarps = kThreads / 32;
-constexpr int kVecPerThread = kUnitElems / kVec / kThreads;  // 2
+constexpr int kVecPerThread = kUnitElems / kVec / kThreads;  // 4
 constexpr int kMaxScalars = 14;     // head + tail elements of one unit, at most
 
 struct Plan {
@@ -61,9 +61,9 @@ struct URange {
   int n;            // element count
 };
 
-__host__ __device__ inline URange unit_range(const Plan& p, int64_t u) {
+// Unit k of row `row` (u = row * R + k).
+__host__ __device__ inline URange unit_range_rk(const Plan& p, int64_t row, int64_t k) {
   URange q;
-  const int64_t row = u / p.R, k = u - row * p.R;
   const int64_t r0 = row * p.S, r1 = r0 + p.S;
   const int64_t bl = (r0 + kVec - 1) & ~(int64_t)(kVec - 1);
   const int64_t bh = r1 & ~(int64_t)(kVec - 1);
@@ -81,6 +81,11 @@ __host__ __device__ inline URange unit_range(const Plan& p, int64_t u) {
   }
   q.n = (int)((q.h1 - q.h0) + (q.b1 - q.b0) + (q.t1 - q.t0));
   return q;
+}
+
+__host__ __device__ inline URange unit_range(const Plan& p, int64_t u) {
+  const int64_t row = u / p.R;
+  return unit_range_rk(p, row, u - row * p.R);
 }
 
 // Flat index of scalar number s (0 <= s < head+tail) of a unit: head first, then tail.
