@@ -151,7 +151,7 @@ def backward(dy, x, mean, rstd, gamma, G: int):
 
 # ------------------------------------------------------------ testing hooks
 
-DEBUG_PATH, DEBUG_SPIN_LIMIT, DEBUG_FORCE_TIMEOUT, DEBUG_LAG, DEBUG_STASH, DEBUG_RING = range(6)
+DEBUG_PATH, DEBUG_SPIN_LIMIT, DEBUG_FORCE_TIMEOUT, DEBUG_LAG, DEBUG_SLOTS = range(5)
 PATH_AUTO, PATH_STREAMING, PATH_FUSED = 0, 1, 2
 
 

@@ -33,8 +33,7 @@ std::atomic<long long> g_hook_path{0};     // 0 auto (fused), 1 streaming kernel
 std::atomic<long long> g_hook_spin{0};     // 0 default poll budget
 std::atomic<long long> g_hook_timeout{0};  // 1: the next fused launch waits on a flag nothing sets
 std::atomic<long long> g_hook_lag{-1};     // -1 auto
-std::atomic<long long> g_hook_stash{-1};   // -1 auto
-std::atomic<long long> g_hook_ring{-1};    // -1 auto
+std::atomic<long long> g_hook_slots{-1};   // -1 auto
 
 constexpr unsigned long long kDefaultSpin = 1ull << 26;  // ~4 s of polls at 64 ns sleeps
 
@@ -153,24 +152,16 @@ unsigned long long spin_budget() {
   return s > 0 ? (unsigned long long)s : kDefaultSpin;
 }
 
-// Slots of the persistent kernels: stream ring + two stash areas in shared memory.
+// Shared-memory slots of a persistent launch (one CTA per SM) and its schedule.
 FusedCfg fused_cfg(const DevInfo& di, int slot_bytes, int64_t group_bytes) {
   FusedCfg c;
-  // kFusedCtasPerSm CTAs share an SM's shared memory; each also holds ~1 KB of
-  // static shared memory and the system's 1 KB per-CTA reservation.
-  int budget = di.smem_per_sm / kFusedCtasPerSm - 3072;
-  if (budget > di.smem_optin - 2048) budget = di.smem_optin - 2048;
-  int n = budget / (slot_bytes + 8);
+  int n = (di.smem_optin - 2048) / (slot_bytes + 16);  // 2 KB: the kernel's static shared memory
   if (n > kMaxSlots) n = kMaxSlots;
-  c.ring = n >= 4 ? 4 : (n >= 2 ? 2 : 1);
-  if (slot_bytes > 32768 && n >= 3) c.ring = 2;
-  c.stash = (n - c.ring) / 2;
+  const long long hs = g_hook_slots.load(), hl = g_hook_lag.load();
+  if (hs >= 1 && hs < n) n = (int)hs;
+  c.slots = n;
   // lag 1 keeps two groups in flight: only when both fit well inside L2
   c.lag = (3 * group_bytes <= (int64_t)di.l2_bytes) ? 1 : 0;
-  const long long hr = g_hook_ring.load(), hs = g_hook_stash.load(), hl = g_hook_lag.load();
-  if (hr >= 1 && hr <= n) c.ring = (int)hr;
-  if (hs >= 0) c.stash = (int)hs;
-  if (c.ring + 2 * c.stash > n) c.stash = (n - c.ring) / 2;
   if (hl >= 0) c.lag = hl ? 1 : 0;
   c.force_timeout = g_hook_timeout.exchange(0) != 0;
   c.spin = spin_budget();
@@ -187,16 +178,16 @@ int raise_smem(const void* func, int bytes, DevInfo& di, int which) {
   return GN3D_OK;
 }
 
-// Grid of a persistent launch: every CTA must be resident at once.
+// Grid of a persistent launch: one CTA per SM, all resident at once.
 int coop_grid(const void* func, int smem, const DevInfo& di, int* grid) {
   int per_sm = 0;
-  GN3D_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, func, kThreads, (size_t)smem), "occupancy");
+  GN3D_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, func, kFusedThreads, (size_t)smem),
+            "occupancy");
   if (per_sm < 1) {
     g_detail = "persistent kernel does not fit on an SM";
     return GN3D_ERR_CUDA;
   }
-  if (per_sm > kFusedCtasPerSm) per_sm = kFusedCtasPerSm;
-  *grid = di.sms * per_sm;
+  *grid = di.sms;
   return GN3D_OK;
 }
 
@@ -205,42 +196,47 @@ template <class TI, class TO>
 int launch_forward(const void* x, const float* gamma, const float* beta, const Plan& p, float eps, void* y,
                    float* mean, float* rstd, cudaStream_t st, DevInfo& di) {
   const bool fused = use_fused();
-  const int64_t nsync = p.NG + 1 + p.NG + 2;  // cnt, ready, abort, never
-  const int64_t bytes = rup(p.units * (int64_t)sizeof(Part)) + rup(p.NG * (int64_t)sizeof(float4)) +
-                        rup(nsync * (int64_t)sizeof(uint32_t));
+  const int64_t nblk = p.NC * p.nb;
+  const int64_t nsync = nblk + 2 * p.NG + 2;  // bcnt, gcnt, ready, abort, never
+  const int64_t bytes = rup(nsync * 4) + rup(p.units * (int64_t)sizeof(Part)) +
+                        rup(nblk * (int64_t)sizeof(Part)) + rup(p.NG * (int64_t)sizeof(float4));
   Scratch s;
   GN3D_CUDA(cudaMallocFromPoolAsync(&s.base, (size_t)bytes, di.pool, st), "scratch allocation");
   s.cur = static_cast<char*>(s.base);
-  FwdWs w;
   uint32_t* sync = s.take<uint32_t>(nsync);
-  w.cnt = sync;
-  w.stats = s.take<float4>(p.NG);
+  FwdWs w;
+  w.bcnt = sync;
+  w.gcnt = sync + nblk;
+  w.ready = sync + nblk + p.NG;
   w.parts = s.take<Part>(p.units);
+  w.bparts = s.take<Part>(nblk);
+  w.stats = s.take<float4>(p.NG);
+  FusedSync fs{sync + nblk + 2 * p.NG, sync + nblk + 2 * p.NG + 1, di.status};
   cudaError_t e = cudaMemsetAsync(sync, 0, (size_t)nsync * sizeof(uint32_t), st);
   const TI* xp = static_cast<const TI*>(x);
   TO* yp = static_cast<TO*>(y);
   if (e == cudaSuccess && fused) {
     const int slot = kUnitElems * (int)sizeof(TI);
     FusedCfg cfg = fused_cfg(di, slot, p.M * (int64_t)sizeof(TI));
-    FusedSync fs{sync, sync + p.NG + 1, sync + 2 * p.NG + 1, sync + 2 * p.NG + 2, di.status};
-    const int smem = (cfg.ring + 2 * cfg.stash) * (slot + 8);
+    const int smem = cfg.slots * (slot + 16);
     auto k = k_fwd_fused<TI, TO>;
     const int which = (sizeof(TI) == 2 ? 0 : 2) + (sizeof(TO) == 2 ? 0 : 1);
     int rc = raise_smem((const void*)k, smem, di, which);
+    int grid = 0;
+    if (!rc) rc = coop_grid((const void*)k, smem, di, &grid);
     if (rc) { cudaFreeAsync(s.base, st); return rc; }
     void* args[] = {(void*)&xp, (void*)&yp, (void*)&p, (void*)&w, (void*)&cfg, (void*)&fs, (void*)&eps,
                     (void*)&gamma, (void*)&beta, (void*)&mean, (void*)&rstd};
-    int grid = 0;
-    rc = coop_grid((const void*)k, smem, di, &grid);
-    if (rc) { cudaFreeAsync(s.base, st); return rc; }
     g_launches += 1;
-    e = cudaLaunchCooperativeKernel((const void*)k, dim3(grid), dim3(kThreads), args, (size_t)smem, st);
+    e = cudaLaunchCooperativeKernel((const void*)k, dim3(grid), dim3(kFusedThreads), args, (size_t)smem, st);
   } else if (e == cudaSuccess) {
+    const int64_t warps_needed = (p.units + kStreamWarps - 1) / kStreamWarps;
     g_launches += 2;
-    k_fwd_stats<TI><<<grid_for(di, p.units, 4), kThreads, 0, st>>>(xp, p, w, eps, mean, rstd);
+    k_fwd_stats<TI><<<grid_for(di, warps_needed, 8), 32 * kStreamWarps, 0, st>>>(xp, p, w, eps, mean, rstd);
     e = cudaGetLastError();
     if (e == cudaSuccess) {
-      k_fwd_norm<TI, TO><<<grid_for(di, p.units, 4), kThreads, 0, st>>>(xp, yp, p, w.stats, gamma, beta);
+      k_fwd_norm<TI, TO><<<grid_for(di, warps_needed, 8), 32 * kStreamWarps, 0, st>>>(xp, yp, p, w.stats, gamma,
+                                                                                      beta);
       e = cudaGetLastError();
     }
   }
@@ -255,18 +251,25 @@ template <class T>
 int launch_backward(const void* dy, const void* x, const float* mean, const float* rstd, const float* gamma,
                     const Plan& p, void* dx, float* dgamma, float* dbeta, cudaStream_t st, DevInfo& di) {
   const bool fused = use_fused();
-  const int64_t nsync = p.NG + 1 + p.NG + 2;
-  const int64_t bytes = rup(p.units * (int64_t)sizeof(float2)) + rup(p.NC * (int64_t)sizeof(float2)) +
-                        rup(p.NG * (int64_t)sizeof(float2)) + rup(nsync * (int64_t)sizeof(uint32_t));
+  const int64_t nblk = p.NC * p.nb;
+  const int64_t nsync = nblk + 2 * p.NG + 3;  // bcnt, gcnt, ready, done, abort, never
+  const int64_t bytes = rup(nsync * 4) + rup(p.units * (int64_t)sizeof(float2)) +
+                        rup(nblk * (int64_t)sizeof(float2)) + rup(p.NC * (int64_t)sizeof(float2)) +
+                        rup(p.NG * (int64_t)sizeof(float2));
   Scratch s;
   GN3D_CUDA(cudaMallocFromPoolAsync(&s.base, (size_t)bytes, di.pool, st), "scratch allocation");
   s.cur = static_cast<char*>(s.base);
-  BwdWs w;
   uint32_t* sync = s.take<uint32_t>(nsync);
-  w.cnt = sync;
-  w.coef = s.take<float2>(p.NG);
-  w.rows = s.take<float2>(p.NC);
+  BwdWs w;
+  w.bcnt = sync;
+  w.gcnt = sync + nblk;
+  w.ready = sync + nblk + p.NG;
+  w.done = sync + nblk + 2 * p.NG;
   w.parts = s.take<float2>(p.units);
+  w.bparts = s.take<float2>(nblk);
+  w.rows = s.take<float2>(p.NC);
+  w.coef = s.take<float2>(p.NG);
+  FusedSync fs{sync + nblk + 2 * p.NG + 1, sync + nblk + 2 * p.NG + 2, di.status};
   cudaError_t e = cudaMemsetAsync(sync, 0, (size_t)nsync * sizeof(uint32_t), st);
   const T* dyp = static_cast<const T*>(dy);
   const T* xp = static_cast<const T*>(x);
@@ -274,25 +277,25 @@ int launch_backward(const void* dy, const void* x, const float* mean, const floa
   if (e == cudaSuccess && fused) {
     const int slot = 2 * kUnitElems * (int)sizeof(T);
     FusedCfg cfg = fused_cfg(di, slot, 2 * p.M * (int64_t)sizeof(T));
-    FusedSync fs{sync, sync + p.NG + 1, sync + 2 * p.NG + 1, sync + 2 * p.NG + 2, di.status};
-    const int smem = (cfg.ring + 2 * cfg.stash) * (slot + 8);
+    const int smem = cfg.slots * (slot + 16);
     auto k = k_bwd_fused<T>;
     int rc = raise_smem((const void*)k, smem, di, sizeof(T) == 2 ? 4 : 5);
+    int grid = 0;
+    if (!rc) rc = coop_grid((const void*)k, smem, di, &grid);
     if (rc) { cudaFreeAsync(s.base, st); return rc; }
     void* args[] = {(void*)&dyp, (void*)&xp, (void*)&dxp, (void*)&p, (void*)&mean, (void*)&rstd, (void*)&gamma,
                     (void*)&w, (void*)&cfg, (void*)&fs, (void*)&dgamma, (void*)&dbeta};
-    int grid = 0;
-    rc = coop_grid((const void*)k, smem, di, &grid);
-    if (rc) { cudaFreeAsync(s.base, st); return rc; }
     g_launches += 1;
-    e = cudaLaunchCooperativeKernel((const void*)k, dim3(grid), dim3(kThreads), args, (size_t)smem, st);
+    e = cudaLaunchCooperativeKernel((const void*)k, dim3(grid), dim3(kFusedThreads), args, (size_t)smem, st);
   } else if (e == cudaSuccess) {
+    const int64_t warps_needed = (p.units + kStreamWarps - 1) / kStreamWarps;
     g_launches += 2;
-    k_bwd_reduce<T><<<grid_for(di, p.units, 3), kThreads, 0, st>>>(dyp, xp, p, mean, rstd, gamma, w, dgamma,
-                                                                     dbeta);
+    k_bwd_reduce<T><<<grid_for(di, warps_needed, 8), 32 * kStreamWarps, 0, st>>>(dyp, xp, p, mean, rstd, gamma,
+                                                                                   w, dgamma, dbeta);
     e = cudaGetLastError();
     if (e == cudaSuccess) {
-      k_bwd_dx<T><<<grid_for(di, p.units, 3), kThreads, 0, st>>>(dyp, xp, dxp, p, mean, rstd, gamma, w.coef);
+      k_bwd_dx<T><<<grid_for(di, warps_needed, 8), 32 * kStreamWarps, 0, st>>>(dyp, xp, dxp, p, mean, rstd,
+                                                                                gamma, w.coef);
       e = cudaGetLastError();
     }
   }
@@ -424,13 +427,9 @@ extern "C" int gn3d_debug_set(int what, long long value) {
       if (value < -1 || value > 1) return arg_fail("lag: -1, 0 or 1");
       g_hook_lag = value;
       break;
-    case GN3D_DEBUG_STASH:
-      if (value < -1 || value > 13) return arg_fail("stash: -1 .. 13");
-      g_hook_stash = value;
-      break;
-    case GN3D_DEBUG_RING:
-      if (value < -1 || value > 8 || value == 0) return arg_fail("ring: -1, 1 .. 8");
-      g_hook_ring = value;
+    case GN3D_DEBUG_SLOTS:
+      if (value < -1 || value == 0 || value > 48) return arg_fail("slots: -1, 1 .. 48");
+      g_hook_slots = value;
       break;
     default:
       return arg_fail("unknown debug setting");
@@ -451,4 +450,4 @@ extern "C" const char* gn3d_error_string(int status) {
 
 extern "C" uint64_t gn3d_launch_count(void) { return g_launches.load(); }
 
-extern "C" const char* gn3d_version(void) { return "gn3d 0.2.0 sm_103a"; }
+extern "C" const char* gn3d_version(void) { return "gn3d 0.3.0 sm_103a"; }

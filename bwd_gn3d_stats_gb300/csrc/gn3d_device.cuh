@@ -1,12 +1,17 @@
-// gn3d_device.cuh -- device building blocks shared by the GroupNorm kernels:
-// vector loads/stores, fixed-order block reductions, the group merge of the
-// per-unit statistics.
+// gn3d_device.cuh -- the GroupNorm arithmetic, shared by both launch forms:
+// vector I/O, warp reductions, the per-unit statistics, the block and group
+// merges, and the elementwise passes.
 //
 // Every floating-point operation that feeds a statistic or an output is written
 // with an explicit round-to-nearest intrinsic (__fadd_rn, __fmul_rn, __fmaf_rn,
 // ...).  The compiler never contracts or reorders those, so the arithmetic --
 // and the bits -- are the same in every template instantiation (bf16 or fp32
-// input, bf16 or fp32 output) and in every kernel variant that uses them.
+// input, bf16 or fp32 output) and in both launch forms.
+//
+// Completion across warps and CTAs uses integer counters with acquire/release
+// semantics (never float atomics): the warp that brings a block's counter to
+// its size merges the block, and the warp that completes a group's last block
+// merges the group and publishes it with a release store on the group's flag.
 #pragma once
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -20,10 +25,13 @@ __device__ __forceinline__ float fsub(float a, float b) { return __fsub_rn(a, b)
 __device__ __forceinline__ float fmul(float a, float b) { return __fmul_rn(a, b); }
 __device__ __forceinline__ float ffma(float a, float b, float c) { return __fmaf_rn(a, b, c); }
 
+constexpr unsigned kFull = 0xFFFFFFFFu;
+
 // ------------------------------------------------------------- element I/O
 // A "vector" is 8 consecutive elements starting at a flat index that is a
 // multiple of 8; with a 16-byte aligned base this is one 16-byte access for
-// bf16 and two for fp32.
+// bf16 and two for fp32.  load8 takes a generic pointer (shared memory in the
+// persistent kernels, global memory in the streaming ones).
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -48,9 +56,7 @@ template <> struct IO<__nv_bfloat16> {
     r.x = pack2(v[0], v[1]); r.y = pack2(v[2], v[3]); r.z = pack2(v[4], v[5]); r.w = pack2(v[6], v[7]);
     __stcs(reinterpret_cast<uint4*>(p), r);
   }
-  static __device__ __forceinline__ void store1(__nv_bfloat16* p, float v) {
-    *p = __float2bfloat16_rn(v);
-  }
+  static __device__ __forceinline__ void store1(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
 };
 
 template <> struct IO<float> {
@@ -67,121 +73,401 @@ template <> struct IO<float> {
   static __device__ __forceinline__ void store1(float* p, float v) { *p = v; }
 };
 
-// ------------------------------------------------------ block reductions
-// Sum of (a, b) over the CTA in a fixed order: an xor butterfly inside each warp
-// (every lane ends with the same bits, since IEEE addition is commutative), then
-// the warp totals added in warp order.  Every thread returns the total.
-
-__device__ __forceinline__ float2 block_sum2(float a, float b, float2* sh) {
+// -------------------------------------------------------- warp reductions
+// xor butterfly: every lane ends with the same bits (IEEE addition commutes).
+__device__ __forceinline__ float warp_sum(float a) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    a = fadd(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
-    b = fadd(b, __shfl_xor_sync(0xFFFFFFFFu, b, o));
-  }
-  const int w = threadIdx.x >> 5;
-  if ((threadIdx.x & 31) == 0) sh[w] = make_float2(a, b);
-  __syncthreads();
-  float2 r = sh[0];
-#pragma unroll
-  for (int i = 1; i < kWarps; ++i) {
-    r.x = fadd(r.x, sh[i].x);
-    r.y = fadd(r.y, sh[i].y);
-  }
-  __syncthreads();
-  return r;
+  for (int o = 16; o > 0; o >>= 1) a = fadd(a, __shfl_xor_sync(kFull, a, o));
+  return a;
 }
 
-// ------------------------------------------------------ group statistics
-// Per-unit record of the forward statistics (16 bytes): the unit's mean as the
-// unevaluated pair m1 + cn (m1 = sum/n in fp32, cn = sum(x - m1)/n), its M2 =
-// sum((x - mean)^2) and its element count.
+__device__ __forceinline__ float2 warp_sum2(float a, float b) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a = fadd(a, __shfl_xor_sync(kFull, a, o));
+    b = fadd(b, __shfl_xor_sync(kFull, b, o));
+  }
+  return make_float2(a, b);
+}
+
+// The fixed meeting tree of a lane's 8 running sums.
+__device__ __forceinline__ float tree8(const float c[8]) {
+  return fadd(fadd(fadd(c[0], c[1]), fadd(c[2], c[3])), fadd(fadd(c[4], c[5]), fadd(c[6], c[7])));
+}
+
+// -------------------------------------------------- acquire/release words
+__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Lane 0 adds one arrival to *ctr; every lane learns whether it was the last of
+// `total`.  The release half orders lane 0's earlier stores before the arrival,
+// the acquire half (with the __syncwarp) orders the warp's later loads after it.
+__device__ __forceinline__ bool warp_arrive_last(uint32_t* ctr, uint32_t total) {
+  uint32_t old = 0;
+  if ((threadIdx.x & 31) == 0) old = atom_add_acq_rel(ctr, 1u);
+  old = __shfl_sync(kFull, old, 0);
+  __syncwarp();
+  return old + 1u == total;
+}
+
+// ------------------------------------------------------------- moments
+// Moments of a set of elements: the mean as the unevaluated pair m1 + cn, M2 =
+// sum((x - mean)^2), and the count (16 bytes, one per unit, block and group).
 struct Part {
   float m1, m2;
   int n;
   float cn;
 };
 
-// Merge of the unit partials of one group (the parallel-variance combine of
-// Chan, Golub & LeVeque in its shifted-sum form): with the shift K = the first
-// unit's mean and d_u = mean_u - K,
-//   mean = K + (sum n_u d_u) / M,   M2 = sum (M2_u + n_u d_u^2) - (sum n_u d_u)^2 / M.
-// The merge runs in fp64 (the per-element accumulation is fp32): the group
-// mean then keeps the digits an fp32 mean of a large-offset group loses, which
-// the normalize uses as a hi/lo pair.  Fixed shape: thread t sums its
-// contiguous slice in order, a shfl_down tree sums each warp into lane 0, and
-// thread 0 adds the warp sums in warp order.  Result valid in thread 0.
-struct GroupMoments {
-  double mean, m2;
-};
-
-__device__ __forceinline__ double dadd(double a, double b) { return __dadd_rn(a, b); }
-__device__ __forceinline__ double dmul(double a, double b) { return __dmul_rn(a, b); }
-
-__device__ __forceinline__ GroupMoments combine_parts(const Part* parts, int64_t cnt, int64_t M, double2* sh) {
-  const float4 r0 = __ldcg(reinterpret_cast<const float4*>(parts));
-  const double K = dadd((double)r0.x, (double)r0.w);
-  const int64_t per = (cnt + kThreads - 1) / kThreads;
-  int64_t lo = (int64_t)threadIdx.x * per, hi = lo + per;
-  if (hi > cnt) hi = cnt;
-  double S = 0.0, Q = 0.0;
-  for (int64_t i = lo; i < hi; ++i) {
-    const float4 r = __ldcg(reinterpret_cast<const float4*>(parts + i));
-    const int n = __float_as_int(r.z);
-    if (n == 0) continue;
-    const double d = dadd(dadd((double)r.x, -K), (double)r.w);
-    const double nd = dmul((double)n, d);
-    S = dadd(S, nd);
-    Q = dadd(Q, dadd((double)r.y, dmul(nd, d)));
-  }
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const double a = __shfl_down_sync(0xFFFFFFFFu, S, o);
-    const double b = __shfl_down_sync(0xFFFFFFFFu, Q, o);
-    if (lane + o < 32) { S = dadd(S, a); Q = dadd(Q, b); }
-  }
-  if (lane == 0) sh[threadIdx.x >> 5] = make_double2(S, Q);
-  __syncthreads();
-  GroupMoments g = {0.0, 0.0};
-  if (threadIdx.x == 0) {
-    S = sh[0].x;
-    Q = sh[0].y;
-    for (int i = 1; i < kWarps; ++i) { S = dadd(S, sh[i].x); Q = dadd(Q, sh[i].y); }
-    const double sm = __ddiv_rn(S, (double)M);
-    g.mean = dadd(K, sm);
-    g.m2 = dadd(Q, -dmul(S, sm));
-    if (g.m2 < 0.0) g.m2 = 0.0;  // rounding only; NaN is kept
-  }
-  __syncthreads();
-  return g;
-}
-
-// ---------------------------------------------------------- unit loaders
-// Loads one unit into registers: kVecPerThread vectors per thread (vector j of
-// the body goes to thread j % kThreads, slot j / kThreads) plus at most one
-// head/tail scalar (scalar s goes to thread s).  Absent values are 0 and flagged.
+// Corrected two-pass moments of one unit, by one warp: m1 = sum/n, then
+// c = sum(x - m1), q = sum((x - m1)^2); mean = m1 + c/n, M2 = q - c*(c/n) (the
+// correction term keeps M2 exact to first order in the error of m1; ScaFFold
+// PR #93: a corrected two-pass per tile, merged with Chan's formula).
+// `body` points at vector 0 of the unit's body (nv vectors); scalars come from x.
 template <class T>
-struct UnitRegs {
-  float v[kVecPerThread][8];
-  bool vok[kVecPerThread];
-  float s;
-  bool sok;
-
-  __device__ __forceinline__ void load(const T* __restrict__ p, const URange& q) {
-    const int64_t nv = (q.b1 - q.b0) / kVec;
+__device__ __forceinline__ Part unit_moments(const T* body, int nv, const T* __restrict__ x, const URange& q) {
+  Part m = {0.f, 0.f, 0, 0.f};
+  if (q.n == 0) return m;
+  const int lane = threadIdx.x & 31;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+  for (int i = 0; i < kVecPerLane; ++i) {
+    const int j = lane + 32 * i;
+    if (j < nv) {
+      float v[8];
+      IO<T>::load8(body + (int64_t)j * kVec, v);
 #pragma unroll
-    for (int i = 0; i < kVecPerThread; ++i) {
-      const int64_t j = threadIdx.x + (int64_t)i * kThreads;
-      vok[i] = j < nv;
-      if (vok[i]) IO<T>::load8(p + q.b0 + j * kVec, v[i]);
-      else {
+      for (int e = 0; e < 8; ++e) acc[e] = fadd(acc[e], v[e]);
+    }
+  }
+  float s = tree8(acc);
+  const bool hs = lane < scalar_count(q);
+  const float sv = hs ? IO<T>::load1(x + scalar_index(q, lane)) : 0.f;
+  if (hs) s = fadd(s, sv);
+  const float fn = (float)q.n;
+  const float m1 = __fdiv_rn(warp_sum(s), fn);
+  float c[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float qq[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+  for (int i = 0; i < kVecPerLane; ++i) {
+    const int j = lane + 32 * i;
+    if (j < nv) {
+      float v[8];
+      IO<T>::load8(body + (int64_t)j * kVec, v);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) v[i][e] = 0.f;
+      for (int e = 0; e < 8; ++e) {
+        const float d = fsub(v[e], m1);
+        c[e] = fadd(c[e], d);
+        qq[e] = ffma(d, d, qq[e]);
       }
     }
-    sok = (int)threadIdx.x < scalar_count(q);
-    s = sok ? IO<T>::load1(p + scalar_index(q, threadIdx.x)) : 0.f;
   }
+  float cs = tree8(c), qs = tree8(qq);
+  if (hs) {
+    const float d = fsub(sv, m1);
+    cs = fadd(cs, d);
+    qs = ffma(d, d, qs);
+  }
+  const float2 t = warp_sum2(cs, qs);
+  m.m1 = m1;
+  m.cn = __fdiv_rn(t.x, fn);
+  m.m2 = fsub(t.y, fmul(t.x, m.cn));
+  if (m.m2 < 0.f) m.m2 = 0.f;  // rounding only; NaN is kept
+  m.n = q.n;
+  return m;
+}
+
+// Shifted-sum merge (the parallel-variance combine of Chan, Golub & LeVeque):
+// with the shift K and d_i = mean_i - K,  S = sum n_i d_i,  Q = sum (M2_i + n_i d_i^2);
+// the union has mean K + S/n and M2 = Q - S*(S/n).
+__device__ __forceinline__ void shifted_terms(const Part& a, float K, float& S, float& Q) {
+  if (a.n == 0) { S = 0.f; Q = 0.f; return; }
+  const float d = fadd(fsub(a.m1, K), a.cn);
+  const float nd = fmul((float)a.n, d);
+  S = nd;
+  Q = fadd(a.m2, fmul(nd, d));
+}
+
+__device__ __forceinline__ Part finish_merge(float K, float S, float Q, int64_t n) {
+  Part r;
+  r.m1 = K;
+  r.n = (int)n;
+  const float fn = (float)n;
+  r.cn = __fdiv_rn(S, fn);
+  r.m2 = fsub(Q, fmul(S, r.cn));
+  if (r.m2 < 0.f) r.m2 = 0.f;
+  return r;
+}
+
+__device__ __forceinline__ Part ldcg_part(const Part* p) {
+  const float4 r = __ldcg(reinterpret_cast<const float4*>(p));
+  return Part{r.x, r.y, __float_as_int(r.z), r.w};
+}
+
+// Block merge of `bsz` unit partials (one per lane), by one warp.
+__device__ __forceinline__ Part merge_block(const Part* units, int bsz) {
+  const int lane = threadIdx.x & 31;
+  const Part a = lane < bsz ? ldcg_part(units + lane) : Part{0.f, 0.f, 0, 0.f};
+  const float K = __shfl_sync(kFull, fadd(a.m1, a.cn), 0);
+  float S, Q;
+  shifted_terms(a, K, S, Q);
+  const float2 t = warp_sum2(S, Q);
+  int n = a.n;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(kFull, n, o);
+  return finish_merge(K, t.x, t.y, n);
+}
+
+// Group merge of its Cg*nb block partials (contiguous), by one warp: lane l takes
+// blocks l, l+32, ... in order, then the butterfly.  Returns (mean hi, mean lo,
+// rstd) with mean = hi + lo and rstd = 1/sqrt(M2/M + eps).
+__device__ __forceinline__ float4 merge_group(const Part* blocks, int64_t nblk, int64_t M, float eps) {
+  const int lane = threadIdx.x & 31;
+  const Part b0 = ldcg_part(blocks);
+  const float K = fadd(b0.m1, b0.cn);
+  float S = 0.f, Q = 0.f;
+  for (int64_t i = lane; i < nblk; i += 32) {
+    float s, q;
+    shifted_terms(ldcg_part(blocks + i), K, s, q);
+    S = fadd(S, s);
+    Q = fadd(Q, q);
+  }
+  const float2 t = warp_sum2(S, Q);
+  const Part g = finish_merge(K, t.x, t.y, M);
+  const float var = __fdiv_rn(g.m2, (float)M);
+  return make_float4(g.m1, g.cn, __frsqrt_rn(fadd(var, eps)), 0.f);
+}
+
+// --------------------------------------------------------------- forward
+struct FwdWs {
+  Part* parts;      // [units]
+  Part* bparts;     // [NC * nb]
+  float4* stats;    // [NG] (mean hi, mean lo, rstd, 0)
+  uint32_t* bcnt;   // [NC * nb] unit arrivals per block
+  uint32_t* gcnt;   // [NG] block arrivals per group
+  uint32_t* ready;  // [NG] 1 once stats[g] is published
 };
+
+// STAT of one forward unit, by one warp: unit moments, then the block and group
+// merges if this warp completes them.
+template <class T>
+__device__ __forceinline__ void fwd_stat(const Plan& p, const FwdWs& ws, const T* body, const T* __restrict__ x,
+                                         const URange& q, int64_t u, int64_t kr, float eps, float* mean_out,
+                                         float* rstd_out) {
+  const Part m = unit_moments(body, (int)((q.b1 - q.b0) / kVec), x, q);
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) ws.parts[u] = m;
+  const int64_t blk = block_of(p, q.row, kr), kb = kr / kBlockUnits;
+  if (!warp_arrive_last(ws.bcnt + blk, (uint32_t)block_size(p, kb))) return;
+  const Part b = merge_block(ws.parts + q.row * p.R + kb * kBlockUnits, block_size(p, kb));
+  if (lane == 0) ws.bparts[blk] = b;
+  const int64_t g = q.row / p.Cg;
+  if (!warp_arrive_last(ws.gcnt + g, (uint32_t)(p.Cg * p.nb))) return;
+  const float4 st = merge_group(ws.bparts + g * p.Cg * p.nb, p.Cg * p.nb, p.M, eps);
+  if (lane == 0) {
+    ws.stats[g] = st;
+    if (mean_out) mean_out[g] = fadd(st.x, st.y);
+    if (rstd_out) rstd_out[g] = st.z;
+    st_release(ws.ready + g, 1u);
+  }
+}
+
+// NORM of one forward unit, by one warp: y = (x - hi)*sc + (beta - lo*sc), sc = rstd*gamma.
+template <class TI, class TO>
+__device__ __forceinline__ void fwd_norm(const TI* body, const TI* __restrict__ x, TO* __restrict__ y,
+                                         const URange& q, float4 st, float gam, float bet) {
+  const int lane = threadIdx.x & 31;
+  const float sc = fmul(st.z, gam);
+  const float sh = ffma(-st.y, sc, bet);
+  const int nv = (int)((q.b1 - q.b0) / kVec);
+#pragma unroll 4
+  for (int i = 0; i < kVecPerLane; ++i) {
+    const int j = lane + 32 * i;
+    if (j < nv) {
+      float v[8];
+      IO<TI>::load8(body + (int64_t)j * kVec, v);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] = ffma(fsub(v[e], st.x), sc, sh);
+      IO<TO>::store8(y + q.b0 + (int64_t)j * kVec, v);
+    }
+  }
+  if (lane < scalar_count(q)) {
+    const int64_t idx = scalar_index(q, lane);
+    IO<TO>::store1(y + idx, ffma(fsub(IO<TI>::load1(x + idx), st.x), sc, sh));
+  }
+}
+
+// -------------------------------------------------------------- backward
+struct BwdWs {
+  float2* parts;    // [units] (S1, S2)
+  float2* bparts;   // [NC * nb]
+  float2* rows;     // [NC] per-row (S1, S2)
+  float2* coef;     // [NG] (a, b)
+  uint32_t* bcnt;   // [NC * nb]
+  uint32_t* gcnt;   // [NG]
+  uint32_t* ready;  // [NG]
+  uint32_t* done;   // [1] groups finalized
+};
+
+// S1 = sum dy, S2 = sum dy*(x - mean) of one unit, by one warp.
+template <class T>
+__device__ __forceinline__ float2 unit_bwd_sums(const T* xb, const T* db, int nv, const T* __restrict__ x,
+                                                const T* __restrict__ dy, const URange& q, float mu) {
+  const int lane = threadIdx.x & 31;
+  float a1[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float a2[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+  for (int i = 0; i < kVecPerLane; ++i) {
+    const int j = lane + 32 * i;
+    if (j < nv) {
+      float vx[8], vd[8];
+      IO<T>::load8(xb + (int64_t)j * kVec, vx);
+      IO<T>::load8(db + (int64_t)j * kVec, vd);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        a1[e] = fadd(a1[e], vd[e]);
+        a2[e] = ffma(vd[e], fsub(vx[e], mu), a2[e]);
+      }
+    }
+  }
+  float s1 = tree8(a1), s2 = tree8(a2);
+  if (lane < scalar_count(q)) {
+    const int64_t idx = scalar_index(q, lane);
+    const float d = IO<T>::load1(dy + idx);
+    s1 = fadd(s1, d);
+    s2 = ffma(d, fsub(IO<T>::load1(x + idx), mu), s2);
+  }
+  return warp_sum2(s1, s2);
+}
+
+// Group finalize of the backward, by one warp: per-row totals of the block sums
+// (lane l takes blocks l, l+32, ... of the row, then the butterfly), then
+// A = sum_c gamma_c*S1_c and B = rstd * sum_c gamma_c*S2_c in channel order;
+// a = A/M and b = B/M.
+__device__ __forceinline__ void bwd_group(const Plan& p, const BwdWs& ws, int64_t g, const float* rstd,
+                                          const float* gamma) {
+  const int lane = threadIdx.x & 31;
+  float A = 0.f, B = 0.f;
+  for (int64_t cl = 0; cl < p.Cg; ++cl) {
+    const int64_t row = g * p.Cg + cl;
+    const float2* bp = ws.bparts + row * p.nb;
+    float s1 = 0.f, s2 = 0.f;
+    for (int64_t i = lane; i < p.nb; i += 32) {
+      const float2 v = __ldcg(bp + i);
+      s1 = fadd(s1, v.x);
+      s2 = fadd(s2, v.y);
+    }
+    const float2 t = warp_sum2(s1, s2);
+    if (lane == 0) ws.rows[row] = t;
+    const float gm = gamma ? gamma[(g % p.G) * p.Cg + cl] : 1.f;
+    A = fadd(A, fmul(gm, t.x));
+    B = fadd(B, fmul(gm, t.y));
+  }
+  B = fmul(rstd[g], B);
+  if (lane == 0) {
+    const float fM = (float)p.M;
+    ws.coef[g] = make_float2(__fdiv_rn(A, fM), __fdiv_rn(B, fM));
+  }
+}
+
+// dgamma_c = sum_n rstd[n,g] * S2[n,c], dbeta_c = sum_n S1[n,c], in n order, by one warp.
+__device__ __forceinline__ void bwd_param_grads(const Plan& p, const float* rstd, const float2* rows,
+                                                float* dgamma, float* dbeta) {
+  for (int64_t c = threadIdx.x & 31; c < p.C; c += 32) {
+    const int64_t g = c / p.Cg;
+    float dg = 0.f, db = 0.f;
+    for (int64_t n = 0; n < p.N; ++n) {
+      const float2 rs = __ldcg(rows + n * p.C + c);
+      dg = fadd(dg, fmul(rstd[n * p.G + g], rs.y));
+      db = fadd(db, rs.x);
+    }
+    if (dgamma) dgamma[c] = dg;
+    if (dbeta) dbeta[c] = db;
+  }
+}
+
+// STAT of one backward unit, by one warp.
+template <class T>
+__device__ __forceinline__ void bwd_stat(const Plan& p, const BwdWs& ws, const T* xb, const T* db,
+                                         const T* __restrict__ x, const T* __restrict__ dy, const URange& q,
+                                         int64_t u, int64_t kr, const float* mean, const float* rstd,
+                                         const float* gamma, float* dgamma, float* dbeta) {
+  const int64_t g = q.row / p.Cg;
+  const float2 s = unit_bwd_sums(xb, db, (int)((q.b1 - q.b0) / kVec), x, dy, q, mean[g]);
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) ws.parts[u] = s;
+  const int64_t blk = block_of(p, q.row, kr), kb = kr / kBlockUnits;
+  const int bsz = block_size(p, kb);
+  if (!warp_arrive_last(ws.bcnt + blk, (uint32_t)bsz)) return;
+  const float2 v = lane < bsz ? __ldcg(ws.parts + q.row * p.R + kb * kBlockUnits + lane) : make_float2(0.f, 0.f);
+  const float2 t = warp_sum2(v.x, v.y);
+  if (lane == 0) ws.bparts[blk] = t;
+  if (!warp_arrive_last(ws.gcnt + g, (uint32_t)(p.Cg * p.nb))) return;
+  bwd_group(p, ws, g, rstd, gamma);
+  if (lane == 0) st_release(ws.ready + g, 1u);
+  if (!warp_arrive_last(ws.done, (uint32_t)p.NG)) return;
+  bwd_param_grads(p, rstd, ws.rows, dgamma, dbeta);
+}
+
+// Per-group coefficients of dx = dy*p1 - (x - mean)*p2 - p3, with p1 = rstd*gamma,
+// p2 = rstd^2 * b, p3 = rstd * a  (= rstd*((dy*gamma - a) - xhat*b)).
+struct DxCoef {
+  float mu, r, a, b;
+  bool single;  // one element per group: dx is exactly 0
+};
+
+// NORM of one backward unit, by one warp.
+template <class T>
+__device__ __forceinline__ void bwd_norm(const T* xb, const T* db, const T* __restrict__ x,
+                                         const T* __restrict__ dy, T* __restrict__ dx, const URange& q,
+                                         const DxCoef& k, float gam) {
+  const int lane = threadIdx.x & 31;
+  const float p1 = k.single ? 0.f : fmul(k.r, gam);
+  const float p2 = k.single ? 0.f : fmul(fmul(k.r, k.r), k.b);
+  const float p3 = k.single ? 0.f : fmul(k.r, k.a);
+  const int nv = (int)((q.b1 - q.b0) / kVec);
+#pragma unroll 4
+  for (int i = 0; i < kVecPerLane; ++i) {
+    const int j = lane + 32 * i;
+    if (j < nv) {
+      float vx[8], vd[8];
+      IO<T>::load8(xb + (int64_t)j * kVec, vx);
+      IO<T>::load8(db + (int64_t)j * kVec, vd);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) vd[e] = ffma(vd[e], p1, ffma(-p2, fsub(vx[e], k.mu), -p3));
+      IO<T>::store8(dx + q.b0 + (int64_t)j * kVec, vd);
+    }
+  }
+  if (lane < scalar_count(q)) {
+    const int64_t idx = scalar_index(q, lane);
+    const float d = IO<T>::load1(dy + idx);
+    IO<T>::store1(dx + idx, ffma(d, p1, ffma(-p2, fsub(IO<T>::load1(x + idx), k.mu), -p3)));
+  }
+}
+
+// Row -> channel, in 32 bits when the indices allow it.
+__device__ __forceinline__ int64_t channel_of(int64_t row, int64_t C) {
+  if (row < 0x7FFFFFFF && C < 0x7FFFFFFF) return (int64_t)((uint32_t)row % (uint32_t)C);
+  return row % C;
+}
 
 }  // namespace gn3d

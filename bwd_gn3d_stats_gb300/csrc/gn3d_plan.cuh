@@ -16,16 +16,24 @@
 // 7 after it (the tail) to unit R-1; a row too short to hold an aligned 8-block
 // is all head.  Groups are Cg = C/G consecutive rows, so group (n, g) owns the
 // Cg*R consecutive units starting at ((n*C + g*Cg) * R).
+//
+// Reduction tree.  One warp reduces one unit: lane l takes body vectors l,
+// l+32, l+64, ... and keeps one running sum per vector position (8 chains), the
+// chains meet in a fixed pairwise tree, the lane's head/tail scalar (scalar l)
+// is added, and an xor butterfly sums the lanes.  Within a row, units form
+// blocks of kBlockUnits consecutive units (the last block of a row may be
+// shorter); a block's unit partials are merged one per lane with the same
+// butterfly.  A group merges its blocks row by row in a fixed order.
 #pragma once
 #include <stdint.h>
 
 namespace gn3d {
 
 constexpr int kVec = 8;             // elements per vector
-constexpr int kUnitElems = 8192;    // body elements per unit (multiple of kVec)
-constexpr int kThreads = 256;       // threads per CTA of the unit kernels
-constexpr int kWarps = kThreads / 32;
-constexpr int kVecPerThread = kUnitElems / kVec / kThreads;  // 4
+constexpr int kUnitElems = 4096;    // body elements per unit (multiple of kVec)
+constexpr int kUnitVecs = kUnitElems / kVec;  // 512
+constexpr int kVecPerLane = kUnitVecs / 32;   // 16
+constexpr int kBlockUnits = 32;     // units per merge block (one per lane)
 constexpr int kMaxScalars = 14;     // head + tail elements of one unit, at most
 
 struct Plan {
@@ -35,6 +43,7 @@ struct Plan {
   int64_t NG;     // N * G groups
   int64_t NC;     // N * C rows
   int64_t R;      // units per row
+  int64_t nb;     // merge blocks per row = ceil(R / kBlockUnits)
   int64_t upg;    // units per group = Cg * R
   int64_t units;  // total units = NC * R
 };
@@ -47,6 +56,7 @@ inline Plan make_plan(int64_t N, int64_t C, int64_t S, int64_t G) {
   p.NG = N * G;
   p.NC = N * C;
   p.R = S > 0 ? (S + kUnitElems - 1) / kUnitElems : 0;
+  p.nb = (p.R + kBlockUnits - 1) / kBlockUnits;
   p.upg = p.Cg * p.R;
   p.units = p.NC * p.R;
   return p;
@@ -96,6 +106,16 @@ __host__ __device__ inline int64_t scalar_index(const URange& q, int s) {
 
 __host__ __device__ inline int scalar_count(const URange& q) {
   return (int)((q.h1 - q.h0) + (q.t1 - q.t0));
+}
+
+// Merge block of unit (row, k): block id row * nb + k / kBlockUnits, and its size.
+__host__ __device__ inline int64_t block_of(const Plan& p, int64_t row, int64_t k) {
+  return row * p.nb + k / kBlockUnits;
+}
+
+__host__ __device__ inline int block_size(const Plan& p, int64_t kb) {
+  const int64_t first = kb * kBlockUnits, rest = p.R - first;
+  return (int)(rest < kBlockUnits ? rest : kBlockUnits);
 }
 
 }  // namespace gn3d

@@ -125,9 +125,8 @@ uint64_t gn3d_launch_count(void);
  *                            the failure path without a fault or a hang).
  *   GN3D_DEBUG_LAG           -1 automatic, 0 or 1: groups of lookahead between
  *                            the statistics pass and the elementwise pass.
- *   GN3D_DEBUG_STASH         -1 automatic, else shared-memory stash slots per
- *                            group parity.
- *   GN3D_DEBUG_RING          -1 automatic, else bulk-copy stream slots.
+ *   GN3D_DEBUG_SLOTS         -1 automatic, else the number of shared-memory
+ *                            slots of the persistent kernels (at most what fits).
  * Returns GN3D_OK or GN3D_ERR_INVALID_ARG for an unknown setting or value.
  */
 enum {
@@ -135,12 +134,11 @@ enum {
   GN3D_DEBUG_SPIN_LIMIT = 1,
   GN3D_DEBUG_FORCE_TIMEOUT = 2,
   GN3D_DEBUG_LAG = 3,
-  GN3D_DEBUG_STASH = 4,
-  GN3D_DEBUG_RING = 5
+  GN3D_DEBUG_SLOTS = 4
 };
 int gn3d_debug_set(int what, long long value);
 
-/* Library version, e.g. "gn3d 0.2.0 sm_103a". */
+/* Library version, e.g. "gn3d 0.3.0 sm_103a". */
 const char* gn3d_version(void);
 
 #ifdef __cplusplus

@@ -11,8 +11,7 @@ from .gpu_util import device_inputs, run_backward, run_forward, to_np, torch
 
 pytestmark = pytest.mark.gpu
 
-SETTINGS = [gn.DEBUG_PATH, gn.DEBUG_LAG, gn.DEBUG_STASH, gn.DEBUG_RING, gn.DEBUG_SPIN_LIMIT]
-DEFAULTS = {gn.DEBUG_PATH: 0, gn.DEBUG_LAG: -1, gn.DEBUG_STASH: -1, gn.DEBUG_RING: -1, gn.DEBUG_SPIN_LIMIT: 0}
+DEFAULTS = {gn.DEBUG_PATH: 0, gn.DEBUG_LAG: -1, gn.DEBUG_SLOTS: -1, gn.DEBUG_SPIN_LIMIT: 0}
 
 
 @pytest.fixture(autouse=True)
@@ -57,8 +56,7 @@ def test_fused_and_streaming_bit_identical(shape):
     assert same(a, b)
 
 
-@pytest.mark.parametrize("knob,values", [(gn.DEBUG_LAG, [0, 1]), (gn.DEBUG_STASH, [0, 1, 3]),
-                                         (gn.DEBUG_RING, [1, 2, 3])])
+@pytest.mark.parametrize("knob,values", [(gn.DEBUG_LAG, [0, 1]), (gn.DEBUG_SLOTS, [1, 2, 3, 9])])
 def test_tuning_does_not_move_a_bit(knob, values):
     site = synth.Site(1, 32, 36, 36, 36, 8, synth.BF16)
     d = device_inputs(synth.make_inputs(site, seed=12))
