@@ -134,6 +134,17 @@ __device__ __forceinline__ bool wait_ready(const uint32_t* flag, const FusedSync
   return true;
 }
 
+// Bounded wait until a slot carries the given task tag (all lanes poll).
+__device__ __forceinline__ bool wait_tag(const volatile unsigned long long* tag, unsigned long long want,
+                                         unsigned long long spin, const volatile int* stop) {
+  for (unsigned long long it = 0; it < spin; ++it) {
+    if (*tag == want) return true;
+    if (*stop) return false;
+    __nanosleep(20);
+  }
+  return false;
+}
+
 // ------------------------------------------------------------- the kernel
 // Op supplies the direction-specific parts:
 //   Elem, kTensors              element type; tensors per slot (1: x; 2: x then dy)
@@ -153,6 +164,11 @@ __device__ __forceinline__ void run_fused(Op& op, const Plan& p, const FusedCfg&
   uint64_t* empty = full + nslots;
   __shared__ volatile int s_fail;
   __shared__ uint32_t s_issued[kMaxSlots];  // bulk copies issued per slot (producer)
+  // Task loaded (or being loaded) into each slot, plus one.  Several consumer
+  // warps share a slot's mbarrier; a warp first waits until its own task is the
+  // slot's current one -- which implies the previous round has completed -- so
+  // its parity wait cannot be satisfied by an older phase of the same parity.
+  __shared__ volatile unsigned long long s_tag[kMaxSlots];
 
   Sched s;
   s.P = gridDim.x;
@@ -169,6 +185,7 @@ __device__ __forceinline__ void run_fused(Op& op, const Plan& p, const FusedCfg&
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
       s_issued[i] = 0;
+      s_tag[i] = 0;
     }
     fence_mbar_init();
     s_fail = 0;
@@ -196,6 +213,7 @@ __device__ __forceinline__ void run_fused(Op& op, const Plan& p, const FusedCfg&
         const uint32_t bytes = (uint32_t)((q.b1 - q.b0) * (int64_t)sizeof(T));
         unsigned char* dst = smem + (size_t)slot * kSlotBytes;
         fence_proxy_async_smem();
+        s_tag[slot] = i + 1;
         mbar_arrive_expect_tx(&full[slot], bytes * Op::kTensors);
         if (bytes) {
 #pragma unroll
@@ -230,7 +248,8 @@ __device__ __forceinline__ void run_fused(Op& op, const Plan& p, const FusedCfg&
         op.prepare(it.g);
         norm_group = it.g;
       }
-      if (!mbar_wait(&full[slot], (uint32_t)(round & 1u), cfg.spin, &s_fail)) {
+      if (!wait_tag(&s_tag[slot], i + 1, cfg.spin, &s_fail) ||
+          !mbar_wait(&full[slot], (uint32_t)(round & 1u), cfg.spin, &s_fail)) {
         s_fail = 1;
         break;
       }
