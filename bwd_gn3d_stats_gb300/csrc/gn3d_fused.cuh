@@ -205,10 +205,7 @@ __device__ __forceinline__ void run_fused(Op& op, const Plan& p, const FusedCfg&
           s_fail = 1;
           break;
         }
-        if (ld_relaxed(fs.abort) != 0) {
-          s_fail = 1;
-          break;
-        }
+        if (s_fail) break;  // a consumer warp gave up (only shared memory is polled here)
         const URange q = unit_range_rk(p, it.row, it.kr);
         const uint32_t bytes = (uint32_t)((q.b1 - q.b0) * (int64_t)sizeof(T));
         unsigned char* dst = smem + (size_t)slot * kSlotBytes;
