@@ -153,13 +153,15 @@ unsigned long long spin_budget() {
 }
 
 // Shared-memory slots of a persistent launch (one CTA per SM) and its schedule.
-FusedCfg fused_cfg(const DevInfo& di, int slot_bytes, int64_t group_bytes) {
+// Dynamic shared memory: slots, two mbarriers per slot, slots + 2 block records.
+FusedCfg fused_cfg(const DevInfo& di, int slot_bytes, int rec_bytes, int64_t group_bytes) {
   FusedCfg c;
-  int n = (di.smem_optin - 2048) / (slot_bytes + 16);  // 2 KB: the kernel's static shared memory
+  int n = (di.smem_optin - 2048 - 2 * rec_bytes) / (slot_bytes + 16 + rec_bytes);  // 2 KB: static smem
   if (n > kMaxSlots) n = kMaxSlots;
   const long long hs = g_hook_slots.load(), hl = g_hook_lag.load();
   if (hs >= 1 && hs < n) n = (int)hs;
   c.slots = n;
+  c.recs = n + 2;
   // lag 1 keeps two groups in flight: only when both fit well inside L2
   c.lag = (3 * group_bytes <= (int64_t)di.l2_bytes) ? 1 : 0;
   if (hl >= 0) c.lag = hl ? 1 : 0;
@@ -217,8 +219,9 @@ int launch_forward(const void* x, const float* gamma, const float* beta, const P
   TO* yp = static_cast<TO*>(y);
   if (e == cudaSuccess && fused) {
     const int slot = kUnitElems * (int)sizeof(TI);
-    FusedCfg cfg = fused_cfg(di, slot, p.M * (int64_t)sizeof(TI));
-    const int smem = cfg.slots * (slot + 16);
+    const int rec = (int)sizeof(BlockRec<Part>);
+    FusedCfg cfg = fused_cfg(di, slot, rec, p.M * (int64_t)sizeof(TI));
+    const int smem = cfg.slots * (slot + 16) + cfg.recs * rec;
     auto k = k_fwd_fused<TI, TO>;
     const int which = (sizeof(TI) == 2 ? 0 : 2) + (sizeof(TO) == 2 ? 0 : 1);
     int rc = raise_smem((const void*)k, smem, di, which);
@@ -276,8 +279,9 @@ int launch_backward(const void* dy, const void* x, const float* mean, const floa
   T* dxp = static_cast<T*>(dx);
   if (e == cudaSuccess && fused) {
     const int slot = 2 * kUnitElems * (int)sizeof(T);
-    FusedCfg cfg = fused_cfg(di, slot, 2 * p.M * (int64_t)sizeof(T));
-    const int smem = cfg.slots * (slot + 16);
+    const int rec = (int)sizeof(BlockRec<float2>);
+    FusedCfg cfg = fused_cfg(di, slot, rec, 2 * p.M * (int64_t)sizeof(T));
+    const int smem = cfg.slots * (slot + 16) + cfg.recs * rec;
     auto k = k_bwd_fused<T>;
     int rc = raise_smem((const void*)k, smem, di, sizeof(T) == 2 ? 4 : 5);
     int grid = 0;

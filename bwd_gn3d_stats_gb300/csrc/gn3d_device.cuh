@@ -223,10 +223,9 @@ __device__ __forceinline__ Part ldcg_part(const Part* p) {
   return Part{r.x, r.y, __float_as_int(r.z), r.w};
 }
 
-// Block merge of `bsz` unit partials (one per lane), by one warp.
-__device__ __forceinline__ Part merge_block(const Part* units, int bsz) {
-  const int lane = threadIdx.x & 31;
-  const Part a = lane < bsz ? ldcg_part(units + lane) : Part{0.f, 0.f, 0, 0.f};
+// Block merge of a block's unit partials, by one warp: lane l holds unit l's
+// partial (lanes past the block's size hold an empty one).
+__device__ __forceinline__ Part merge_block(const Part a) {
   const float K = __shfl_sync(kFull, fadd(a.m1, a.cn), 0);
   float S, Q;
   shifted_terms(a, K, S, Q);
@@ -267,20 +266,13 @@ struct FwdWs {
   uint32_t* ready;  // [NG] 1 once stats[g] is published
 };
 
-// STAT of one forward unit, by one warp: unit moments, then the block and group
-// merges if this warp completes them.
-template <class T>
-__device__ __forceinline__ void fwd_stat(const Plan& p, const FwdWs& ws, const T* body, const T* __restrict__ x,
-                                         const URange& q, int64_t u, int64_t kr, float eps, float* mean_out,
-                                         float* rstd_out) {
-  const Part m = unit_moments(body, (int)((q.b1 - q.b0) / kVec), x, q);
+// A completed forward block, by one warp: publish its partial, arrive on the
+// group, and merge and publish the group if this completes it.
+__device__ __forceinline__ void fwd_block_done(const Plan& p, const FwdWs& ws, int64_t blk, const Part& b,
+                                               float eps, float* mean_out, float* rstd_out) {
   const int lane = threadIdx.x & 31;
-  if (lane == 0) ws.parts[u] = m;
-  const int64_t blk = block_of(p, q.row, kr), kb = kr / kBlockUnits;
-  if (!warp_arrive_last(ws.bcnt + blk, (uint32_t)block_size(p, kb))) return;
-  const Part b = merge_block(ws.parts + q.row * p.R + kb * kBlockUnits, block_size(p, kb));
   if (lane == 0) ws.bparts[blk] = b;
-  const int64_t g = q.row / p.Cg;
+  const int64_t g = (blk / p.nb) / p.Cg;
   if (!warp_arrive_last(ws.gcnt + g, (uint32_t)(p.Cg * p.nb))) return;
   const float4 st = merge_group(ws.bparts + g * p.Cg * p.nb, p.Cg * p.nb, p.M, eps);
   if (lane == 0) {
@@ -289,6 +281,22 @@ __device__ __forceinline__ void fwd_stat(const Plan& p, const FwdWs& ws, const T
     if (rstd_out) rstd_out[g] = st.z;
     st_release(ws.ready + g, 1u);
   }
+}
+
+// STAT of one forward unit through global memory (streaming form), by one warp:
+// unit moments; the warp that completes the unit's block merges it.
+template <class T>
+__device__ __forceinline__ void fwd_stat_global(const Plan& p, const FwdWs& ws, const T* body,
+                                                const T* __restrict__ x, const URange& q, int64_t u, int64_t kr,
+                                                float eps, float* mean_out, float* rstd_out) {
+  const Part m = unit_moments(body, (int)((q.b1 - q.b0) / kVec), x, q);
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) ws.parts[u] = m;
+  const int64_t blk = block_of(p, q.row, kr), kb = kr / kBlockUnits;
+  const int bsz = block_size(p, kb);
+  if (!warp_arrive_last(ws.bcnt + blk, (uint32_t)bsz)) return;
+  const Part a = lane < bsz ? ldcg_part(ws.parts + q.row * p.R + kb * kBlockUnits + lane) : Part{0.f, 0.f, 0, 0.f};
+  fwd_block_done(p, ws, blk, merge_block(a), eps, mean_out, rstd_out);
 }
 
 // NORM of one forward unit, by one warp: y = (x - hi)*sc + (beta - lo*sc), sc = rstd*gamma.
@@ -405,27 +413,38 @@ __device__ __forceinline__ void bwd_param_grads(const Plan& p, const float* rstd
   }
 }
 
-// STAT of one backward unit, by one warp.
+// A completed backward block, by one warp (lane l holds unit l's sums): the
+// block sums, the group arrival, and the group and parameter-gradient merges
+// if this completes them.
+__device__ __forceinline__ void bwd_block_done(const Plan& p, const BwdWs& ws, int64_t blk, float2 v,
+                                               const float* rstd, const float* gamma, float* dgamma,
+                                               float* dbeta) {
+  const int lane = threadIdx.x & 31;
+  const float2 t = warp_sum2(v.x, v.y);
+  if (lane == 0) ws.bparts[blk] = t;
+  const int64_t g = (blk / p.nb) / p.Cg;
+  if (!warp_arrive_last(ws.gcnt + g, (uint32_t)(p.Cg * p.nb))) return;
+  bwd_group(p, ws, g, rstd, gamma);
+  if (lane == 0) st_release(ws.ready + g, 1u);
+  if (!warp_arrive_last(ws.done, (uint32_t)p.NG)) return;
+  bwd_param_grads(p, rstd, ws.rows, dgamma, dbeta);
+}
+
+// STAT of one backward unit through global memory (streaming form), by one warp.
 template <class T>
-__device__ __forceinline__ void bwd_stat(const Plan& p, const BwdWs& ws, const T* xb, const T* db,
-                                         const T* __restrict__ x, const T* __restrict__ dy, const URange& q,
-                                         int64_t u, int64_t kr, const float* mean, const float* rstd,
-                                         const float* gamma, float* dgamma, float* dbeta) {
-  const int64_t g = q.row / p.Cg;
-  const float2 s = unit_bwd_sums(xb, db, (int)((q.b1 - q.b0) / kVec), x, dy, q, mean[g]);
+__device__ __forceinline__ void bwd_stat_global(const Plan& p, const BwdWs& ws, const T* xb, const T* db,
+                                                const T* __restrict__ x, const T* __restrict__ dy,
+                                                const URange& q, int64_t u, int64_t kr, const float* mean,
+                                                const float* rstd, const float* gamma, float* dgamma,
+                                                float* dbeta) {
+  const float2 s = unit_bwd_sums(xb, db, (int)((q.b1 - q.b0) / kVec), x, dy, q, mean[q.row / p.Cg]);
   const int lane = threadIdx.x & 31;
   if (lane == 0) ws.parts[u] = s;
   const int64_t blk = block_of(p, q.row, kr), kb = kr / kBlockUnits;
   const int bsz = block_size(p, kb);
   if (!warp_arrive_last(ws.bcnt + blk, (uint32_t)bsz)) return;
   const float2 v = lane < bsz ? __ldcg(ws.parts + q.row * p.R + kb * kBlockUnits + lane) : make_float2(0.f, 0.f);
-  const float2 t = warp_sum2(v.x, v.y);
-  if (lane == 0) ws.bparts[blk] = t;
-  if (!warp_arrive_last(ws.gcnt + g, (uint32_t)(p.Cg * p.nb))) return;
-  bwd_group(p, ws, g, rstd, gamma);
-  if (lane == 0) st_release(ws.ready + g, 1u);
-  if (!warp_arrive_last(ws.done, (uint32_t)p.NG)) return;
-  bwd_param_grads(p, rstd, ws.rows, dgamma, dbeta);
+  bwd_block_done(p, ws, blk, v, rstd, gamma, dgamma, dbeta);
 }
 
 // Per-group coefficients of dx = dy*p1 - (x - mean)*p2 - p3, with p1 = rstd*gamma,

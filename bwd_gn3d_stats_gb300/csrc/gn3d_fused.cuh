@@ -1,13 +1,16 @@
 // gn3d_fused.cuh -- persistent, warp-specialized forward and backward kernels.
 //
-// One CTA per SM: kConsumerWarps consumer warps and one producer warp.  The CTA
-// walks its share of the plan's units (u = CTA id mod the grid) in group order
-// as a sequence of tasks:
-//   STAT(g): statistics of the CTA's units of group g (fwd_stat / bwd_stat); the
-//            warp that completes a block or a group merges it, and the group's
-//            merge ends with a release store on its ready flag.
-//   NORM(g): the elementwise pass over the same units (y or dx), last unit first,
-//            once group g is ready.
+// One CTA per SM: kConsumerWarps consumer warps and one producer warp.  CTA p
+// owns the merge blocks b = p (mod the grid) -- each block is up to 16
+// consecutive units of one row -- and walks them in group order as a sequence
+// of unit tasks:
+//   STAT(g): statistics of the CTA's units of group g.  A unit's partial goes to
+//            a block record in shared memory; the warp that completes the block
+//            merges it there, publishes the block partial and arrives on the
+//            group; the warp that completes the group merges and publishes it
+//            with a release store on the group's ready flag.
+//   NORM(g): the elementwise pass over the same units (y or dx), in reverse
+//            order, once group g is ready.
 // Order: STAT(0) STAT(1) NORM(0) STAT(2) NORM(1) ... (lag 1: the wait for a
 // group's statistics hides behind the next group's statistics pass while two
 // groups fit in L2), or STAT(0) NORM(0) STAT(1) ... (lag 0, for groups too large
@@ -17,15 +20,17 @@
 // 1-D bulk copy (the TMA engine) into slot i mod nslots, on that slot's "full"
 // mbarrier; the consumer warp releases the slot on its "empty" mbarrier.  The
 // consumers never synchronize as a block: each unit is one warp's work, with
-// warp shuffles only.  (The ScaFFold GroupNorm kernels are split-group Triton
-// programs; this is that split-group reduction re-cut for sm_103a.)
+// warp shuffles only, and only one global arrival is made per 16 units.  (The
+// ScaFFold GroupNorm kernels are split-group Triton programs; this is that
+// split-group reduction re-cut for sm_103a.)  Both launch forms use the same
+// units, merge blocks and arithmetic, so their results are bit-identical.
 //
 // Deadlock freedom: all CTAs are co-resident (cooperative launch).  A STAT(h)
 // task precedes every NORM(h) task in each CTA's sequence and waits only for
-// its own bulk copy, whose slot is released by an earlier task of lower group;
-// so the lowest group anyone waits for always completes.  Every wait is still
-// bounded: on timeout the CTA records GN3D_ERR_TIMEOUT, raises the abort word
-// (which the other CTAs' waits watch), drains its own bulk copies and returns.
+// its own bulk copy, whose slot is released by an earlier task; so the lowest
+// group anyone waits for always completes.  Every wait is still bounded: on
+// timeout the CTA records GN3D_ERR_TIMEOUT, raises the abort word (which the
+// other CTAs' waits watch), drains its own bulk copies and returns.
 #pragma once
 #include "gn3d_device.cuh"
 #include "gn3d_sync.cuh"
@@ -39,6 +44,7 @@ constexpr uint32_t kStatusTimeout = 4;  // GN3D_ERR_TIMEOUT
 
 struct FusedCfg {
   int slots;                // shared-memory slots (>= 1)
+  int recs;                 // block records (> slots: see record reuse below)
   int lag;                  // 0 or 1
   int force_timeout;        // testing hook: the first group wait targets a word nothing sets
   unsigned long long spin;  // poll budget of every bounded wait
@@ -50,21 +56,32 @@ struct FusedSync {
   uint32_t* status;  // device status word (GN3D_ERR_TIMEOUT on a timeout)
 };
 
+// Shared-memory record of one block in its STAT phase: the unit partials and
+// an arrival count.  Records are reused round-robin over the CTA's STAT blocks;
+// a block's tasks all finish before the task of block j + recs can start,
+// because the producer only loads task i after task i - nslots has finished
+// and recs > nslots.
+template <class PartT>
+struct BlockRec {
+  PartT part[kBlockUnits];
+  int cnt;
+};
+
 // ------------------------------------------------------------ scheduling
 struct Sched {
-  int64_t P, pid, NG, upg, R;
-  int64_t qP, rP;  // P / R and P % R: stepping u by P moves (row, k) by these
+  int64_t P, pid, NG, nbg, nb, R;  // nbg = merge blocks per group
+  const Plan* plan;
   int lag;
 
   __device__ __forceinline__ int64_t first(int64_t g) const {
-    const int64_t base = g * upg;
+    const int64_t base = g * nbg;
     int64_t off = (pid - base % P) % P;
     if (off < 0) off += P;
     return base + off;
   }
-  __device__ __forceinline__ int64_t count_from(int64_t g, int64_t u0) const {
-    const int64_t end = (g + 1) * upg;
-    return u0 < end ? (end - 1 - u0) / P + 1 : 0;
+  __device__ __forceinline__ int64_t count_from(int64_t g, int64_t b0) const {
+    const int64_t end = (g + 1) * nbg;
+    return b0 < end ? (end - 1 - b0) / P + 1 : 0;
   }
   // phase k -> (kind, group); false when k names no phase (STAT beyond the last group)
   __device__ __forceinline__ bool phase(int64_t k, int& kind, int64_t& g) const {
@@ -86,13 +103,26 @@ struct Sched {
 
 enum { kStat = 0, kNorm = 1, kEnd = 2 };
 
-// Position in the task sequence: a few divisions per phase, only additions per task.
+// Position in the task sequence: a few divisions per block, only additions per unit.
 struct TaskIt {
-  int64_t k, idx, n;
+  int64_t k;
   int kind;
   int64_t g;
-  int64_t u, row, kr;
+  int64_t fb, nblk, bi;  // phase: first block, block count, block index
+  int64_t b, row, kb;    // current block
+  int bsz, ui;           // its unit count; units done in it
+  int64_t kr;            // current unit within its row
+  int64_t sblk;          // STAT blocks finished before this one (record sequence)
 
+  __device__ __forceinline__ void set_block(const Sched& s) {
+    const int64_t j = kind == kStat ? bi : nblk - 1 - bi;
+    b = fb + j * s.P;
+    row = b / s.nb;
+    kb = b - row * s.nb;
+    bsz = block_size(*s.plan, kb);
+    ui = 0;
+    kr = kb * kBlockUnits + (kind == kStat ? 0 : bsz - 1);
+  }
   __device__ __forceinline__ void seek(const Sched& s) {
     for (;; ++k) {
       if (k > s.last_phase()) { kind = kEnd; return; }
@@ -102,24 +132,19 @@ struct TaskIt {
       const int64_t f = s.first(gg);
       const int64_t c = s.count_from(gg, f);
       if (c > 0) {
-        kind = kd; g = gg; n = c; idx = 0;
-        u = kind == kStat ? f : f + (c - 1) * s.P;
-        row = u / s.R;
-        kr = u - row * s.R;
+        kind = kd; g = gg; fb = f; nblk = c; bi = 0;
+        set_block(s);
         return;
       }
     }
   }
-  __device__ __forceinline__ void start(const Sched& s) { k = 0; seek(s); }
+  __device__ __forceinline__ void start(const Sched& s) { k = 0; sblk = 0; seek(s); }
   __device__ __forceinline__ void next(const Sched& s) {
-    if (++idx >= n) { ++k; seek(s); return; }
-    if (kind == kStat) {
-      u += s.P; row += s.qP; kr += s.rP;
-      if (kr >= s.R) { kr -= s.R; ++row; }
-    } else {
-      u -= s.P; row -= s.qP; kr -= s.rP;
-      if (kr < 0) { kr += s.R; --row; }
-    }
+    if (++ui < bsz) { kr += kind == kStat ? 1 : -1; return; }
+    if (kind == kStat) ++sblk;
+    if (++bi < nblk) { set_block(s); return; }
+    ++k;
+    seek(s);
   }
 };
 
@@ -147,21 +172,24 @@ __device__ __forceinline__ bool wait_tag(const volatile unsigned long long* tag,
 
 // ------------------------------------------------------------- the kernel
 // Op supplies the direction-specific parts:
-//   Elem, kTensors              element type; tensors per slot (1: x; 2: x then dy)
-//   src(t)                      base pointer of tensor t
+//   Elem, PartT, kTensors       element type; unit partial type; tensors per slot
+//   src(t)                      base pointer of tensor t (0: x, 1: dy)
 //   ready(g)                    the group's ready flag
-//   stat(slot, q, u, kr)        STAT of one unit (one warp)
+//   unit(slot, q)               the unit's partial (one warp)
+//   block_done(blk, a)          a completed block, lane l holding unit l's partial
 //   prepare(g)                  load group g's published statistics (one warp)
 //   norm(slot, q, row)          NORM of one unit (one warp)
 template <class Op>
 __device__ __forceinline__ void run_fused(Op& op, const Plan& p, const FusedCfg& cfg, const FusedSync& fs) {
   extern __shared__ __align__(128) unsigned char smem[];
   using T = typename Op::Elem;
+  using PartT = typename Op::PartT;
   constexpr int kTensorBytes = kUnitElems * (int)sizeof(T);
   constexpr int kSlotBytes = Op::kTensors * kTensorBytes;
   const int nslots = cfg.slots;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)nslots * kSlotBytes);
   uint64_t* empty = full + nslots;
+  BlockRec<PartT>* recs = reinterpret_cast<BlockRec<PartT>*>(empty + nslots);
   __shared__ volatile int s_fail;
   __shared__ uint32_t s_issued[kMaxSlots];  // bulk copies issued per slot (producer)
   // Task loaded (or being loaded) into each slot, plus one.  Several consumer
@@ -174,10 +202,10 @@ __device__ __forceinline__ void run_fused(Op& op, const Plan& p, const FusedCfg&
   s.P = gridDim.x;
   s.pid = blockIdx.x;
   s.NG = p.NG;
-  s.upg = p.upg;
+  s.nbg = p.Cg * p.nb;
+  s.nb = p.nb;
   s.R = p.R;
-  s.qP = s.P / s.R;
-  s.rP = s.P - s.qP * s.R;
+  s.plan = &p;
   s.lag = cfg.lag;
 
   if (threadIdx.x == 0) {
@@ -190,6 +218,7 @@ __device__ __forceinline__ void run_fused(Op& op, const Plan& p, const FusedCfg&
     fence_mbar_init();
     s_fail = 0;
   }
+  for (int i = threadIdx.x; i < cfg.recs; i += blockDim.x) recs[i].cnt = 0;
   __syncthreads();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -251,8 +280,27 @@ __device__ __forceinline__ void run_fused(Op& op, const Plan& p, const FusedCfg&
         break;
       }
       const unsigned char* data = smem + (size_t)slot * kSlotBytes;
-      if (it.kind == kStat) op.stat(data, q, it.u, it.kr);
-      else op.norm(data, q, it.row);
+      if (it.kind == kStat) {
+        const PartT v = op.unit(data, q);
+        BlockRec<PartT>& rec = recs[it.sblk % cfg.recs];
+        int last = 0;
+        if (lane == 0) {
+          rec.part[it.kr - it.kb * kBlockUnits] = v;
+          __threadfence_block();  // the partial before the arrival
+          last = atomicAdd(&rec.cnt, 1) == it.bsz - 1;
+          if (last) __threadfence_block();  // the other warps' partials after it
+        }
+        __syncwarp();
+        last = __shfl_sync(kFull, last, 0);
+        if (last) {
+          const PartT a = lane < it.bsz ? rec.part[lane] : PartT{};
+          __syncwarp();
+          if (lane == 0) rec.cnt = 0;
+          op.block_done(it.b, a);
+        }
+      } else {
+        op.norm(data, q, it.row);
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);
       for (int w = 0; w < kConsumerWarps && it.kind != kEnd; ++w) it.next(s);
@@ -274,6 +322,7 @@ __device__ __forceinline__ void run_fused(Op& op, const Plan& p, const FusedCfg&
 template <class TI, class TO>
 struct FwdOp {
   using Elem = TI;
+  using PartT = Part;
   static constexpr int kTensors = 1;
   const TI* x;
   TO* y;
@@ -288,8 +337,11 @@ struct FwdOp {
 
   __device__ __forceinline__ const TI* src(int) const { return x; }
   __device__ __forceinline__ const uint32_t* ready(int64_t g) const { return ws.ready + g; }
-  __device__ __forceinline__ void stat(const unsigned char* slot, const URange& q, int64_t u, int64_t kr) {
-    fwd_stat<TI>(p, ws, reinterpret_cast<const TI*>(slot), x, q, u, kr, eps, mean_out, rstd_out);
+  __device__ __forceinline__ Part unit(const unsigned char* slot, const URange& q) const {
+    return unit_moments(reinterpret_cast<const TI*>(slot), (int)((q.b1 - q.b0) / kVec), x, q);
+  }
+  __device__ __forceinline__ void block_done(int64_t blk, const Part& a) {
+    fwd_block_done(p, ws, blk, merge_block(a), eps, mean_out, rstd_out);
   }
   __device__ __forceinline__ void prepare(int64_t g) { st = __ldcg(ws.stats + g); }
   __device__ __forceinline__ void norm(const unsigned char* slot, const URange& q, int64_t row) {
@@ -312,6 +364,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 template <class T>
 struct BwdOp {
   using Elem = T;
+  using PartT = float2;
   static constexpr int kTensors = 2;  // slot: x body, then dy body
   const T* dy;
   const T* x;
@@ -327,9 +380,12 @@ struct BwdOp {
 
   __device__ __forceinline__ const T* src(int t) const { return t == 0 ? x : dy; }
   __device__ __forceinline__ const uint32_t* ready(int64_t g) const { return ws.ready + g; }
-  __device__ __forceinline__ void stat(const unsigned char* slot, const URange& q, int64_t u, int64_t kr) {
+  __device__ __forceinline__ float2 unit(const unsigned char* slot, const URange& q) const {
     const T* xb = reinterpret_cast<const T*>(slot);
-    bwd_stat<T>(p, ws, xb, xb + kUnitElems, x, dy, q, u, kr, mean, rstd, gamma, dgamma, dbeta);
+    return unit_bwd_sums(xb, xb + kUnitElems, (int)((q.b1 - q.b0) / kVec), x, dy, q, mean[q.row / p.Cg]);
+  }
+  __device__ __forceinline__ void block_done(int64_t blk, const float2& a) {
+    bwd_block_done(p, ws, blk, a, rstd, gamma, dgamma, dbeta);
   }
   __device__ __forceinline__ void prepare(int64_t g) {
     const float2 ab = __ldcg(ws.coef + g);

@@ -32,7 +32,7 @@ __global__ void __launch_bounds__(32 * kStreamWarps)
   for (int64_t u = warp_global(); u < p.units; u += nw) {
     const int64_t row = u / p.R, kr = u - row * p.R;
     const URange q = unit_range_rk(p, row, kr);
-    fwd_stat<TI>(p, ws, x + q.b0, x, q, u, kr, eps, mean_out, rstd_out);
+    fwd_stat_global<TI>(p, ws, x + q.b0, x, q, u, kr, eps, mean_out, rstd_out);
   }
 }
 
@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(32 * kStreamWarps)
   for (int64_t u = warp_global(); u < p.units; u += nw) {
     const int64_t row = u / p.R, kr = u - row * p.R;
     const URange q = unit_range_rk(p, row, kr);
-    bwd_stat<T>(p, ws, x + q.b0, dy + q.b0, x, dy, q, u, kr, mean, rstd, gamma, dgamma, dbeta);
+    bwd_stat_global<T>(p, ws, x + q.b0, dy + q.b0, x, dy, q, u, kr, mean, rstd, gamma, dgamma, dbeta);
   }
 }
 

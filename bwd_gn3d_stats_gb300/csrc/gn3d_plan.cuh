@@ -33,7 +33,7 @@ constexpr int kVec = 8;             // elements per vector
 constexpr int kUnitElems = 4096;    // body elements per unit (multiple of kVec)
 constexpr int kUnitVecs = kUnitElems / kVec;  // 512
 constexpr int kVecPerLane = kUnitVecs / 32;   // 16
-constexpr int kBlockUnits = 32;     // units per merge block (one per lane)
+constexpr int kBlockUnits = 16;     // units per merge block (one per lane; <= 32)
 constexpr int kMaxScalars = 14;     // head + tail elements of one unit, at most
 
 struct Plan {
