@@ -432,7 +432,7 @@ extern "C" int gn3d_debug_set(int what, long long value) {
       g_hook_lag = value;
       break;
     case GN3D_DEBUG_SLOTS:
-      if (value < -1 || value == 0 || value > 48) return arg_fail("slots: -1, 1 .. 48");
+      if (value < -1 || value == 0 || value > 32) return arg_fail("slots: -1, 1 .. 32");
       g_hook_slots = value;
       break;
     default:

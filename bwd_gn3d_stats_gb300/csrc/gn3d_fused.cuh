@@ -18,7 +18,8 @@
 //
 // The producer warp moves each task's unit body global -> shared memory with a
 // 1-D bulk copy (the TMA engine) into slot i mod nslots, on that slot's "full"
-// mbarrier; the consumer warp releases the slot on its "empty" mbarrier.  The
+// mbarrier (lane l of the producer warp serves slot l); the consumer warp
+// releases the slot on its "empty" mbarrier.  The
 // consumers never synchronize as a block: each unit is one warp's work, with
 // warp shuffles only, and only one global arrival is made per 16 units.  (The
 // ScaFFold GroupNorm kernels are split-group Triton programs; this is that
@@ -37,9 +38,9 @@
 
 namespace gn3d {
 
-constexpr int kConsumerWarps = 8;
+constexpr int kConsumerWarps = 16;
 constexpr int kFusedThreads = 32 * (kConsumerWarps + 1);
-constexpr int kMaxSlots = 48;
+constexpr int kMaxSlots = 32;  // one producer lane per slot
 constexpr uint32_t kStatusTimeout = 4;  // GN3D_ERR_TIMEOUT
 
 struct FusedCfg {
@@ -224,12 +225,15 @@ __device__ __forceinline__ void run_fused(Op& op, const Plan& p, const FusedCfg&
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp == kConsumerWarps) {
     // ---------------------------------------------------------- producer
-    if (lane == 0) {
+    // Lane l owns slot l: it loads tasks l, l + nslots, l + 2*nslots, ... each
+    // once the slot's previous task has been released, so the lanes issue their
+    // bulk copies independently of one another.
+    if (lane < nslots) {
+      const int slot = lane;
       TaskIt it;
       it.start(s);
-      for (uint64_t i = 0; it.kind != kEnd; ++i) {
-        const int slot = (int)(i % (uint64_t)nslots);
-        const uint64_t round = i / (uint64_t)nslots;
+      for (int w = 0; w < slot && it.kind != kEnd; ++w) it.next(s);
+      for (uint64_t round = 0; it.kind != kEnd; ++round) {
         if (round > 0 && !mbar_wait(&empty[slot], (uint32_t)((round - 1) & 1u), cfg.spin, &s_fail)) {
           s_fail = 1;
           break;
@@ -239,15 +243,15 @@ __device__ __forceinline__ void run_fused(Op& op, const Plan& p, const FusedCfg&
         const uint32_t bytes = (uint32_t)((q.b1 - q.b0) * (int64_t)sizeof(T));
         unsigned char* dst = smem + (size_t)slot * kSlotBytes;
         fence_proxy_async_smem();
-        s_tag[slot] = i + 1;
+        s_tag[slot] = round * (uint64_t)nslots + (uint64_t)slot + 1;
         mbar_arrive_expect_tx(&full[slot], bytes * Op::kTensors);
         if (bytes) {
 #pragma unroll
           for (int tn = 0; tn < Op::kTensors; ++tn)
             bulk_g2s(dst + tn * kTensorBytes, op.src(tn) + q.b0, bytes, &full[slot]);
         }
-        ++s_issued[slot];
-        it.next(s);
+        s_issued[slot] = (uint32_t)round + 1;
+        for (int w = 0; w < nslots && it.kind != kEnd; ++w) it.next(s);
       }
     }
   } else {
