@@ -147,6 +147,20 @@ struct TaskIt {
     ++k;
     seek(s);
   }
+  // n steps of next(), skipping whole blocks at a time.
+  __device__ __forceinline__ void advance(const Sched& s, int n) {
+    while (n > 0 && kind != kEnd) {
+      const int rest = bsz - ui;  // units left in this block, the current one included
+      if (n < rest) {
+        ui += n;
+        kr += kind == kStat ? n : -n;
+        return;
+      }
+      n -= rest;
+      ui = bsz - 1;
+      next(s);  // leaves the block
+    }
+  }
 };
 
 // Bounded wait for a group's ready flag (one lane); watches the abort word.
@@ -232,7 +246,7 @@ __device__ __forceinline__ void run_fused(Op& op, const Plan& p, const FusedCfg&
       const int slot = lane;
       TaskIt it;
       it.start(s);
-      for (int w = 0; w < slot && it.kind != kEnd; ++w) it.next(s);
+      it.advance(s, slot);
       for (uint64_t round = 0; it.kind != kEnd; ++round) {
         if (round > 0 && !mbar_wait(&empty[slot], (uint32_t)((round - 1) & 1u), cfg.spin, &s_fail)) {
           s_fail = 1;
@@ -251,14 +265,14 @@ __device__ __forceinline__ void run_fused(Op& op, const Plan& p, const FusedCfg&
             bulk_g2s(dst + tn * kTensorBytes, op.src(tn) + q.b0, bytes, &full[slot]);
         }
         s_issued[slot] = (uint32_t)round + 1;
-        for (int w = 0; w < nslots && it.kind != kEnd; ++w) it.next(s);
+        it.advance(s, nslots);
       }
     }
   } else {
     // --------------------------------------------------------- consumers
     TaskIt it;
     it.start(s);
-    for (int w = 0; w < warp && it.kind != kEnd; ++w) it.next(s);
+    it.advance(s, warp);
     int64_t norm_group = -1;
     bool forced = cfg.force_timeout != 0;
     for (uint64_t i = warp; it.kind != kEnd; i += kConsumerWarps) {
@@ -307,7 +321,7 @@ __device__ __forceinline__ void run_fused(Op& op, const Plan& p, const FusedCfg&
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);
-      for (int w = 0; w < kConsumerWarps && it.kind != kEnd; ++w) it.next(s);
+      it.advance(s, kConsumerWarps);
     }
   }
 
