@@ -160,3 +160,13 @@ def gn3d_debug_set(what: int, value: int):
     L.gn3d_debug_set.argtypes = [ctypes.c_int, ctypes.c_longlong]
     L.gn3d_debug_set.restype = ctypes.c_int
     _check(L.gn3d_debug_set(what, value))
+
+
+def gn3d_forward_noalloc(x, gamma, beta, N, C, D, H, W, G, eps, in_dtype, out_dtype, y, mean, rstd, stream):
+    """The allocation-free forward (C entry point gn3d_forward_noalloc)."""
+    L = lib()
+    i64, vp, dbl, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_double, ctypes.c_int
+    L.gn3d_forward_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, dbl, ci, ci, vp, vp, vp, vp]
+    L.gn3d_forward_noalloc.restype = ci
+    _check(L.gn3d_forward_noalloc(x, gamma, beta, N, C, D, H, W, G, eps, in_dtype, out_dtype, y, mean, rstd,
+                                  stream))

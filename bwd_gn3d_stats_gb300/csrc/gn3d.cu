@@ -311,6 +311,98 @@ int launch_backward(const void* dy, const void* x, const float* mean, const floa
 
 bool valid_dtype(int d) { return d == GN3D_F32 || d == GN3D_BF16; }
 
+// ------------------------------------------------- allocation-free forward
+// Scratch of gn3d_forward_noalloc: one fixed area in the module's global memory,
+// present on every device that loads the library, for as long as it is loaded.
+// Host code never touches it by name: the name is only a host-side handle, so
+// its device address is looked up once per device (cudaGetSymbolAddress, with
+// that device current) and passed to the kernel.
+constexpr size_t kNoAllocScratchBytes = 8u << 20;  // 8 MiB
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+struct NoAllocDev {
+  bool ready = false;
+  unsigned char* scratch = nullptr;  // device address of g_noalloc_scratch
+  uint32_t* status = nullptr;        // device address of the status word
+  DevInfo facts;                     // SM count, L2 and shared-memory sizes (no pool)
+  int attr_smem[4] = {0, 0, 0, 0};
+};
+NoAllocDev g_noalloc[kMaxDevices];
+
+int noalloc_setup(int dev, NoAllocDev** out) {
+  if (dev < 0 || dev >= kMaxDevices) return arg_fail("device ordinal out of range");
+  std::lock_guard<std::mutex> lk(g_mu);
+  NoAllocDev& d = g_noalloc[dev];
+  if (!d.ready) {
+    GN3D_CUDA(cudaDeviceGetAttribute(&d.facts.sms, cudaDevAttrMultiProcessorCount, dev), "device attribute");
+    GN3D_CUDA(cudaDeviceGetAttribute(&d.facts.l2_bytes, cudaDevAttrL2CacheSize, dev), "device attribute");
+    GN3D_CUDA(cudaDeviceGetAttribute(&d.facts.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev),
+              "device attribute");
+    void* sym = nullptr;
+    GN3D_CUDA(cudaGetSymbolAddress(&sym, g_noalloc_scratch), "cudaGetSymbolAddress(scratch)");
+    d.scratch = static_cast<unsigned char*>(sym);
+    GN3D_CUDA(cudaGetSymbolAddress(&sym, g_status_word), "cudaGetSymbolAddress(status)");
+    d.status = static_cast<uint32_t*>(sym);
+    d.ready = true;
+  }
+  *out = &d;
+  return GN3D_OK;
+}
+
+// The forward's scratch layout (sync words, unit partials, block partials, group
+// statistics) laid over the static area; the same layout gn3d_forward allocates.
+int64_t noalloc_bytes(const Plan& p) {
+  const int64_t nblk = p.NC * p.nb;
+  return rup((nblk + 2 * p.NG + 2) * 4) + rup(p.units * (int64_t)sizeof(Part)) +
+         rup(nblk * (int64_t)sizeof(Part)) + rup(p.NG * (int64_t)sizeof(float4));
+}
+
+template <class TI, class TO>
+int launch_forward_noalloc(const void* x, const float* gamma, const float* beta, const Plan& p, float eps,
+                           void* y, float* mean, float* rstd, cudaStream_t st, NoAllocDev& nd) {
+  const int64_t nblk = p.NC * p.nb;
+  const int64_t nsync = nblk + 2 * p.NG + 2;
+  Scratch s;
+  s.base = nd.scratch;
+  s.cur = reinterpret_cast<char*>(nd.scratch);
+  uint32_t* sync = s.take<uint32_t>(nsync);
+  FwdWs w;
+  w.bcnt = sync;
+  w.gcnt = sync + nblk;
+  w.ready = sync + nblk + p.NG;
+  w.parts = s.take<Part>(p.units);
+  w.bparts = s.take<Part>(nblk);
+  w.stats = s.take<float4>(p.NG);
+  FusedSync fs{sync + nblk + 2 * p.NG, sync + nblk + 2 * p.NG + 1, nd.status};
+  // the area keeps the previous call's contents: the counters and flags start at zero
+  GN3D_CUDA(cudaMemsetAsync(sync, 0, (size_t)nsync * sizeof(uint32_t), st), "memset");
+  const int slot = kUnitElems * (int)sizeof(TI);
+  const int rec = (int)sizeof(BlockRec<Part>);
+  FusedCfg cfg = fused_cfg(nd.facts, slot, rec, p.M * (int64_t)sizeof(TI));
+  const int smem = cfg.slots * (slot + 16) + cfg.recs * rec;
+  auto k = k_fwd_fused<TI, TO>;
+  const int which = (sizeof(TI) == 2 ? 0 : 2) + (sizeof(TO) == 2 ? 0 : 1);
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (nd.attr_smem[which] < smem) {
+      GN3D_CUDA(cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem),
+                "cudaFuncSetAttribute");
+      nd.attr_smem[which] = smem;
+    }
+  }
+  int grid = 0;
+  int rc = coop_grid((const void*)k, smem, nd.facts, &grid);
+  if (rc) return rc;
+  const TI* xp = static_cast<const TI*>(x);
+  TO* yp = static_cast<TO*>(y);
+  void* args[] = {(void*)&xp, (void*)&yp, (void*)&p, (void*)&w, (void*)&cfg, (void*)&fs, (void*)&eps,
+                  (void*)&gamma, (void*)&beta, (void*)&mean, (void*)&rstd};
+  g_launches += 1;
+  GN3D_CUDA(cudaLaunchCooperativeKernel((const void*)k, dim3(grid), dim3(kFusedThreads), args, (size_t)smem, st),
+            "forward launch");
+  return GN3D_OK;
+}
+
 }  // namespace
 }  // namespace gn3d
 
@@ -360,6 +452,47 @@ extern "C" int gn3d_forward(const void* x, const float* gamma, const float* beta
   if (in_dtype == GN3D_F32 && out_dtype == GN3D_BF16)
     return launch_forward<float, bf>(x, gamma, beta, p, feps, y, mean, rstd, st, *di);
   return launch_forward<float, float>(x, gamma, beta, p, feps, y, mean, rstd, st, *di);
+}
+
+// The forward without any allocation: the same kernel as gn3d_forward, with its
+// scratch in the library's static device area (see include/gn3d.h).
+extern "C" int gn3d_forward_noalloc(const void* x, const float* gamma, const float* beta, int64_t N, int64_t C,
+                                    int64_t D, int64_t H, int64_t W, int64_t G, double eps, gn3d_dtype in_dtype,
+                                    gn3d_dtype out_dtype, void* y, float* mean, float* rstd, void* stream) {
+  int rc = check_shape(N, C, D, H, W, G);
+  if (rc) return rc;
+  if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype)) return arg_fail("unsupported dtype");
+  if (!(eps >= 0.0) || !isfinite(eps)) return arg_fail("eps must be finite and >= 0");
+  const float feps = (float)eps;
+  const Plan p = make_plan(N, C, D * H * W, G);
+  const int64_t numel = p.NC * p.S;
+  if (numel == 0) return arg_fail("gn3d_forward_noalloc needs a non-empty tensor");
+  const int64_t need = noalloc_bytes(p);
+  if (need > (int64_t)kNoAllocScratchBytes) {
+    g_detail = "gn3d_forward_noalloc: this shape needs " + std::to_string(need) +
+               " bytes of scratch; the static area holds " + std::to_string(kNoAllocScratchBytes);
+    return GN3D_ERR_INVALID_ARG;
+  }
+  int dev = 0;
+  GN3D_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  NoAllocDev* nd = nullptr;
+  if ((rc = noalloc_setup(dev, &nd))) return rc;
+  if (!x || !y) return arg_fail("x and y are required");
+  if (!aligned16(x) || !aligned16(y)) return arg_fail("x and y must be 16-byte aligned");
+  if ((rc = check_ptr(x, dev, "x")) || (rc = check_ptr(y, dev, "y"))) return rc;
+  if (mean && (rc = check_ptr(mean, dev, "mean"))) return rc;
+  if (rstd && (rc = check_ptr(rstd, dev, "rstd"))) return rc;
+  if (gamma && (rc = check_ptr(gamma, dev, "gamma"))) return rc;
+  if (beta && (rc = check_ptr(beta, dev, "beta"))) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  using bf = __nv_bfloat16;
+  if (in_dtype == GN3D_BF16 && out_dtype == GN3D_BF16)
+    return launch_forward_noalloc<bf, bf>(x, gamma, beta, p, feps, y, mean, rstd, st, *nd);
+  if (in_dtype == GN3D_BF16 && out_dtype == GN3D_F32)
+    return launch_forward_noalloc<bf, float>(x, gamma, beta, p, feps, y, mean, rstd, st, *nd);
+  if (in_dtype == GN3D_F32 && out_dtype == GN3D_BF16)
+    return launch_forward_noalloc<float, bf>(x, gamma, beta, p, feps, y, mean, rstd, st, *nd);
+  return launch_forward_noalloc<float, float>(x, gamma, beta, p, feps, y, mean, rstd, st, *nd);
 }
 
 extern "C" int gn3d_backward(const void* dy, const void* x, const float* mean, const float* rstd,

@@ -83,6 +83,33 @@ int gn3d_forward(const void* x, const float* gamma, const float* beta, int64_t N
                  gn3d_dtype out_dtype, void* y, float* mean, float* rstd, void* stream);
 
 /*
+ * GroupNorm forward that allocates nothing.  The pages have no counterpart of
+ * this entry point; it exists for callers that must not allocate device memory
+ * during the call -- for example code running under a fixed memory budget, or
+ * inside another allocator's critical section, where cudaMalloc (which may
+ * synchronize the device) or a stream-ordered pool allocation is not allowed.
+ *
+ * Same arguments, results and errors as gn3d_forward, computed by the same
+ * kernel, except:
+ *   - Scratch comes from a static area of 8 MiB inside the library's device
+ *     code, which every GPU that loads the library holds until the process
+ *     exits.  The scratch is about 17 bytes per 4096 elements of each (n, c)
+ *     row, so up to about 2 billion elements fit when rows are long, fewer
+ *     when D*H*W is small.  A shape whose scratch would not fit is rejected
+ *     with GN3D_ERR_INVALID_ARG, and gn3d_error_string says how many bytes it
+ *     needed.  Empty tensors are rejected too.
+ *   - The first call on a device looks up the area's device address; make that
+ *     first call before any stream capture.
+ *   - All calls share the one area (each call clears the counters it needs), so
+ *     calls that can overlap on the GPU -- on different streams, or from
+ *     different threads -- race and give wrong results.  Serialize them.
+ * No cudaMalloc, cudaFree or memory-pool call is made.
+ */
+int gn3d_forward_noalloc(const void* x, const float* gamma, const float* beta, int64_t N, int64_t C,
+                         int64_t D, int64_t H, int64_t W, int64_t G, double eps, gn3d_dtype in_dtype,
+                         gn3d_dtype out_dtype, void* y, float* mean, float* rstd, void* stream);
+
+/*
  * GroupNorm backward at the forward's saved statistics.
  *   dy, x  [N,C,D,H,W] dtype, read only.
  *   mean, rstd  [N*G] fp32 as written by gn3d_forward for the same x, G, eps.
