@@ -138,23 +138,83 @@ struct Part {
   float cn;
 };
 
+// --------------------------------------------------------- body readers
+// Where a unit's body vectors come from: shared memory (a bulk-copied slot, read
+// with explicit ld.shared) or global memory.  A vector is kRaw 16-byte words.
+__device__ __forceinline__ uint32_t shared_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+struct FromShared {
+  static __device__ __forceinline__ uint4 word(const void* p) {
+    uint4 r;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "r"(shared_addr(p)));
+    return r;
+  }
+};
+
+struct FromGlobal {
+  static __device__ __forceinline__ uint4 word(const void* p) { return *reinterpret_cast<const uint4*>(p); }
+};
+
+template <class T> struct Vec;
+
+template <> struct Vec<__nv_bfloat16> {
+  static constexpr int kRaw = 1;
+  template <class Src>
+  static __device__ __forceinline__ void load(const __nv_bfloat16* p, uint4 r[kRaw]) { r[0] = Src::word(p); }
+  static __device__ __forceinline__ void unpack(const uint4 r[kRaw], float v[8]) {
+    v[0] = bf16_lo(r[0].x); v[1] = bf16_hi(r[0].x); v[2] = bf16_lo(r[0].y); v[3] = bf16_hi(r[0].y);
+    v[4] = bf16_lo(r[0].z); v[5] = bf16_hi(r[0].z); v[6] = bf16_lo(r[0].w); v[7] = bf16_hi(r[0].w);
+  }
+};
+
+template <> struct Vec<float> {
+  static constexpr int kRaw = 2;
+  template <class Src>
+  static __device__ __forceinline__ void load(const float* p, uint4 r[kRaw]) {
+    r[0] = Src::word(p);
+    r[1] = Src::word(p + 4);
+  }
+  static __device__ __forceinline__ void unpack(const uint4 r[kRaw], float v[8]) {
+    v[0] = __uint_as_float(r[0].x); v[1] = __uint_as_float(r[0].y);
+    v[2] = __uint_as_float(r[0].z); v[3] = __uint_as_float(r[0].w);
+    v[4] = __uint_as_float(r[1].x); v[5] = __uint_as_float(r[1].y);
+    v[6] = __uint_as_float(r[1].z); v[7] = __uint_as_float(r[1].w);
+  }
+};
+
+template <class T, class Src>
+__device__ __forceinline__ void load_vec(const T* body, int j, float v[8]) {
+  uint4 r[Vec<T>::kRaw];
+  Vec<T>::template load<Src>(body + j * kVec, r);
+  Vec<T>::unpack(r, v);
+}
+
 // Corrected two-pass moments of one unit, by one warp: m1 = sum/n, then
 // c = sum(x - m1), q = sum((x - m1)^2); mean = m1 + c/n, M2 = q - c*(c/n) (the
 // correction term keeps M2 exact to first order in the error of m1; ScaFFold
 // PR #93: a corrected two-pass per tile, merged with Chan's formula).
 // `body` points at vector 0 of the unit's body (nv vectors); scalars come from x.
-template <class T>
+// bf16 bodies stay in registers (packed) between the passes; fp32 ones are read twice.
+template <class T, class Src>
 __device__ __forceinline__ Part unit_moments(const T* body, int nv, const T* __restrict__ x, const URange& q) {
   Part m = {0.f, 0.f, 0, 0.f};
   if (q.n == 0) return m;
   const int lane = threadIdx.x & 31;
+  constexpr bool kHold = Vec<T>::kRaw == 1;
+  uint4 raw[kHold ? kVecPerLane : 1][Vec<T>::kRaw];
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
+#pragma unroll
   for (int i = 0; i < kVecPerLane; ++i) {
     const int j = lane + 32 * i;
     if (j < nv) {
       float v[8];
-      IO<T>::load8(body + (int64_t)j * kVec, v);
+      uint4* r = raw[kHold ? i : 0];
+      Vec<T>::template load<Src>(body + j * kVec, r);
+      Vec<T>::unpack(r, v);
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc[e] = fadd(acc[e], v[e]);
     }
@@ -167,12 +227,14 @@ __device__ __forceinline__ Part unit_moments(const T* body, int nv, const T* __r
   const float m1 = __fdiv_rn(warp_sum(s), fn);
   float c[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   float qq[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
+#pragma unroll
   for (int i = 0; i < kVecPerLane; ++i) {
     const int j = lane + 32 * i;
     if (j < nv) {
       float v[8];
-      IO<T>::load8(body + (int64_t)j * kVec, v);
+      uint4* r = raw[kHold ? i : 0];
+      if (!kHold) Vec<T>::template load<Src>(body + j * kVec, r);
+      Vec<T>::unpack(r, v);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const float d = fsub(v[e], m1);
@@ -289,7 +351,7 @@ template <class T>
 __device__ __forceinline__ void fwd_stat_global(const Plan& p, const FwdWs& ws, const T* body,
                                                 const T* __restrict__ x, const URange& q, int64_t u, int64_t kr,
                                                 float eps, float* mean_out, float* rstd_out) {
-  const Part m = unit_moments(body, (int)((q.b1 - q.b0) / kVec), x, q);
+  const Part m = unit_moments<T, FromGlobal>(body, (int)((q.b1 - q.b0) / kVec), x, q);
   const int lane = threadIdx.x & 31;
   if (lane == 0) ws.parts[u] = m;
   const int64_t blk = block_of(p, q.row, kr), kb = kr / kBlockUnits;
@@ -300,7 +362,7 @@ __device__ __forceinline__ void fwd_stat_global(const Plan& p, const FwdWs& ws, 
 }
 
 // NORM of one forward unit, by one warp: y = (x - hi)*sc + (beta - lo*sc), sc = rstd*gamma.
-template <class TI, class TO>
+template <class TI, class TO, class Src>
 __device__ __forceinline__ void fwd_norm(const TI* body, const TI* __restrict__ x, TO* __restrict__ y,
                                          const URange& q, float4 st, float gam, float bet) {
   const int lane = threadIdx.x & 31;
@@ -312,7 +374,7 @@ __device__ __forceinline__ void fwd_norm(const TI* body, const TI* __restrict__ 
     const int j = lane + 32 * i;
     if (j < nv) {
       float v[8];
-      IO<TI>::load8(body + (int64_t)j * kVec, v);
+      load_vec<TI, Src>(body, j, v);
 #pragma unroll
       for (int e = 0; e < 8; ++e) v[e] = ffma(fsub(v[e], st.x), sc, sh);
       IO<TO>::store8(y + q.b0 + (int64_t)j * kVec, v);
@@ -337,7 +399,7 @@ struct BwdWs {
 };
 
 // S1 = sum dy, S2 = sum dy*(x - mean) of one unit, by one warp.
-template <class T>
+template <class T, class Src>
 __device__ __forceinline__ float2 unit_bwd_sums(const T* xb, const T* db, int nv, const T* __restrict__ x,
                                                 const T* __restrict__ dy, const URange& q, float mu) {
   const int lane = threadIdx.x & 31;
@@ -348,8 +410,8 @@ __device__ __forceinline__ float2 unit_bwd_sums(const T* xb, const T* db, int nv
     const int j = lane + 32 * i;
     if (j < nv) {
       float vx[8], vd[8];
-      IO<T>::load8(xb + (int64_t)j * kVec, vx);
-      IO<T>::load8(db + (int64_t)j * kVec, vd);
+      load_vec<T, Src>(xb, j, vx);
+      load_vec<T, Src>(db, j, vd);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         a1[e] = fadd(a1[e], vd[e]);
@@ -437,7 +499,7 @@ __device__ __forceinline__ void bwd_stat_global(const Plan& p, const BwdWs& ws, 
                                                 const URange& q, int64_t u, int64_t kr, const float* mean,
                                                 const float* rstd, const float* gamma, float* dgamma,
                                                 float* dbeta) {
-  const float2 s = unit_bwd_sums(xb, db, (int)((q.b1 - q.b0) / kVec), x, dy, q, mean[q.row / p.Cg]);
+  const float2 s = unit_bwd_sums<T, FromGlobal>(xb, db, (int)((q.b1 - q.b0) / kVec), x, dy, q, mean[q.row / p.Cg]);
   const int lane = threadIdx.x & 31;
   if (lane == 0) ws.parts[u] = s;
   const int64_t blk = block_of(p, q.row, kr), kb = kr / kBlockUnits;
@@ -455,7 +517,7 @@ struct DxCoef {
 };
 
 // NORM of one backward unit, by one warp.
-template <class T>
+template <class T, class Src>
 __device__ __forceinline__ void bwd_norm(const T* xb, const T* db, const T* __restrict__ x,
                                          const T* __restrict__ dy, T* __restrict__ dx, const URange& q,
                                          const DxCoef& k, float gam) {
@@ -469,8 +531,8 @@ __device__ __forceinline__ void bwd_norm(const T* xb, const T* db, const T* __re
     const int j = lane + 32 * i;
     if (j < nv) {
       float vx[8], vd[8];
-      IO<T>::load8(xb + (int64_t)j * kVec, vx);
-      IO<T>::load8(db + (int64_t)j * kVec, vd);
+      load_vec<T, Src>(xb, j, vx);
+      load_vec<T, Src>(db, j, vd);
 #pragma unroll
       for (int e = 0; e < 8; ++e) vd[e] = ffma(vd[e], p1, ffma(-p2, fsub(vx[e], k.mu), -p3));
       IO<T>::store8(dx + q.b0 + (int64_t)j * kVec, vd);

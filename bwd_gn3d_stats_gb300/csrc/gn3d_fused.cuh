@@ -356,7 +356,7 @@ struct FwdOp {
   __device__ __forceinline__ const TI* src(int) const { return x; }
   __device__ __forceinline__ const uint32_t* ready(int64_t g) const { return ws.ready + g; }
   __device__ __forceinline__ Part unit(const unsigned char* slot, const URange& q) const {
-    return unit_moments(reinterpret_cast<const TI*>(slot), (int)((q.b1 - q.b0) / kVec), x, q);
+    return unit_moments<TI, FromShared>(reinterpret_cast<const TI*>(slot), (int)((q.b1 - q.b0) / kVec), x, q);
   }
   __device__ __forceinline__ void block_done(int64_t blk, const Part& a) {
     fwd_block_done(p, ws, blk, merge_block(a), eps, mean_out, rstd_out);
@@ -364,7 +364,7 @@ struct FwdOp {
   __device__ __forceinline__ void prepare(int64_t g) { st = __ldcg(ws.stats + g); }
   __device__ __forceinline__ void norm(const unsigned char* slot, const URange& q, int64_t row) {
     const int64_t c = channel_of(row, p.C);
-    fwd_norm<TI, TO>(reinterpret_cast<const TI*>(slot), x, y, q, st, gamma ? gamma[c] : 1.f,
+    fwd_norm<TI, TO, FromShared>(reinterpret_cast<const TI*>(slot), x, y, q, st, gamma ? gamma[c] : 1.f,
                      beta ? beta[c] : 0.f);
   }
 };
@@ -400,7 +400,8 @@ struct BwdOp {
   __device__ __forceinline__ const uint32_t* ready(int64_t g) const { return ws.ready + g; }
   __device__ __forceinline__ float2 unit(const unsigned char* slot, const URange& q) const {
     const T* xb = reinterpret_cast<const T*>(slot);
-    return unit_bwd_sums(xb, xb + kUnitElems, (int)((q.b1 - q.b0) / kVec), x, dy, q, mean[q.row / p.Cg]);
+    return unit_bwd_sums<T, FromShared>(xb, xb + kUnitElems, (int)((q.b1 - q.b0) / kVec), x, dy, q,
+                                        mean[q.row / p.Cg]);
   }
   __device__ __forceinline__ void block_done(int64_t blk, const float2& a) {
     bwd_block_done(p, ws, blk, a, rstd, gamma, dgamma, dbeta);
@@ -412,7 +413,7 @@ struct BwdOp {
   __device__ __forceinline__ void norm(const unsigned char* slot, const URange& q, int64_t row) {
     const T* xb = reinterpret_cast<const T*>(slot);
     const int64_t c = channel_of(row, p.C);
-    bwd_norm<T>(xb, xb + kUnitElems, x, dy, dx, q, k, gamma ? gamma[c] : 1.f);
+    bwd_norm<T, FromShared>(xb, xb + kUnitElems, x, dy, dx, q, k, gamma ? gamma[c] : 1.f);
   }
 };
 
