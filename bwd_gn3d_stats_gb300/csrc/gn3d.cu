@@ -162,9 +162,15 @@ FusedCfg fused_cfg(const DevInfo& di, int slot_bytes, int rec_bytes, int64_t gro
   if (hs >= 1 && hs < n) n = (int)hs;
   c.slots = n;
   c.recs = n + 2;
-  // lag 1 keeps two groups in flight: only when both fit well inside L2
-  c.lag = (3 * group_bytes <= (int64_t)di.l2_bytes) ? 1 : 0;
-  if (hl >= 0) c.lag = hl ? 1 : 0;
+  // Lag: as many groups of lookahead as leave each group's second read in L2
+  // (lag + 1 groups resident, with room for the writes), at least one -- a
+  // lookahead of one group beats stalling at every group boundary even when a
+  // group alone outgrows L2.
+  int64_t lag = group_bytes > 0 ? (int64_t)di.l2_bytes / (2 * group_bytes) - 1 : kMaxLag;
+  if (lag < 1) lag = 1;
+  if (lag > kMaxLag) lag = kMaxLag;
+  c.lag = (int)lag;
+  if (hl >= 0) c.lag = (int)hl;
   c.force_timeout = g_hook_timeout.exchange(0) != 0;
   c.spin = spin_budget();
   return c;
@@ -561,7 +567,7 @@ extern "C" int gn3d_debug_set(int what, long long value) {
       g_hook_timeout = value ? 1 : 0;
       break;
     case GN3D_DEBUG_LAG:
-      if (value < -1 || value > 1) return arg_fail("lag: -1, 0 or 1");
+      if (value < -1 || value > kMaxLag) return arg_fail("lag: -1 .. 8");
       g_hook_lag = value;
       break;
     case GN3D_DEBUG_SLOTS:

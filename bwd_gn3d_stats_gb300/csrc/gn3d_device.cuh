@@ -139,20 +139,12 @@ struct Part {
 };
 
 // --------------------------------------------------------- body readers
-// Where a unit's body vectors come from: shared memory (a bulk-copied slot, read
-// with explicit ld.shared) or global memory.  A vector is kRaw 16-byte words.
-__device__ __forceinline__ uint32_t shared_addr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
+// Where a unit's body vectors come from: a bulk-copied shared-memory slot or
+// global memory.  A vector is kRaw 16-byte words.  Shared-memory reads are plain
+// loads: the compiler schedules them freely, and the "memory" clobber of the
+// mbarrier wait keeps them after the copy has landed.
 struct FromShared {
-  static __device__ __forceinline__ uint4 word(const void* p) {
-    uint4 r;
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "r"(shared_addr(p)));
-    return r;
-  }
+  static __device__ __forceinline__ uint4 word(const void* p) { return *reinterpret_cast<const uint4*>(p); }
 };
 
 struct FromGlobal {

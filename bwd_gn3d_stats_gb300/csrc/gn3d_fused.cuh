@@ -11,10 +11,11 @@
 //            with a release store on the group's ready flag.
 //   NORM(g): the elementwise pass over the same units (y or dx), in reverse
 //            order, once group g is ready.
-// Order: STAT(0) STAT(1) NORM(0) STAT(2) NORM(1) ... (lag 1: the wait for a
-// group's statistics hides behind the next group's statistics pass while two
-// groups fit in L2), or STAT(0) NORM(0) STAT(1) ... (lag 0, for groups too large
-// for two to fit in L2).  Task i goes to consumer warp i mod kConsumerWarps.
+// Order, with a lag of L groups: STAT(0) .. STAT(L-1), then STAT(L) NORM(0)
+// STAT(L+1) NORM(1) ..., then the last L NORMs.  The wait for a group's
+// statistics hides behind the next L groups' statistics passes while L+1
+// groups stay resident in L2 for their second read.  Task i goes to consumer
+// warp i mod kConsumerWarps.
 //
 // The producer warp moves each task's unit body global -> shared memory with a
 // 1-D bulk copy (the TMA engine) into slot i mod nslots, on that slot's "full"
@@ -42,11 +43,12 @@ constexpr int kConsumerWarps = 16;
 constexpr int kFusedThreads = 32 * (kConsumerWarps + 1);
 constexpr int kMaxSlots = 32;  // one producer lane per slot
 constexpr uint32_t kStatusTimeout = 4;  // GN3D_ERR_TIMEOUT
+constexpr int kMaxLag = 8;
 
 struct FusedCfg {
   int slots;                // shared-memory slots (>= 1)
   int recs;                 // block records (> slots: see record reuse below)
-  int lag;                  // 0 or 1
+  int lag;                  // groups of lookahead between the two passes (0 .. kMaxLag)
   int force_timeout;        // testing hook: the first group wait targets a word nothing sets
   unsigned long long spin;  // poll budget of every bounded wait
 };
@@ -84,22 +86,26 @@ struct Sched {
     const int64_t end = (g + 1) * nbg;
     return b0 < end ? (end - 1 - b0) / P + 1 : 0;
   }
-  // phase k -> (kind, group); false when k names no phase (STAT beyond the last group)
+  // Phase k (0 <= k < 2*NG) -> (kind, group), with L = min(lag, NG):
+  //   STAT(0) .. STAT(L-1), then STAT(L) NORM(0) STAT(L+1) NORM(1) ..., then the
+  //   last L NORMs.  NORM(h) always follows STAT(h') for every h' <= h + L.
   __device__ __forceinline__ bool phase(int64_t k, int& kind, int64_t& g) const {
-    if (lag == 0) {
-      kind = (int)(k & 1);
-      g = k >> 1;
-    } else if (k == 0) {
-      kind = 0;
-      g = 0;
+    const int64_t L = lag < NG ? lag : NG;
+    if (k < L) {
+      kind = kStatPhase;
+      g = k;
+    } else if (k >= 2 * NG - L) {
+      kind = kNormPhase;
+      g = k - NG;
     } else {
-      const int64_t m = k - 1;
-      kind = (m & 1) ? 1 : 0;
-      g = (m & 1) ? (m >> 1) : (m >> 1) + 1;
+      const int64_t m = k - L;
+      kind = (m & 1) ? kNormPhase : kStatPhase;
+      g = (m & 1) ? (m - 1) >> 1 : L + (m >> 1);
     }
-    return g < NG;
+    return true;
   }
-  __device__ __forceinline__ int64_t last_phase() const { return lag == 0 ? 2 * NG - 1 : 2 * NG; }
+  __device__ __forceinline__ int64_t last_phase() const { return 2 * NG - 1; }
+  static constexpr int kStatPhase = 0, kNormPhase = 1;
 };
 
 enum { kStat = 0, kNorm = 1, kEnd = 2 };

@@ -150,8 +150,8 @@ uint64_t gn3d_launch_count(void);
  *                            nothing sets, so its bounded wait runs out and
  *                            gn3d_stream_status reports GN3D_ERR_TIMEOUT (tests
  *                            the failure path without a fault or a hang).
- *   GN3D_DEBUG_LAG           -1 automatic, 0 or 1: groups of lookahead between
- *                            the statistics pass and the elementwise pass.
+ *   GN3D_DEBUG_LAG           -1 automatic, else 0 .. 8: groups of lookahead
+ *                            between the statistics pass and the elementwise pass.
  *   GN3D_DEBUG_SLOTS         -1 automatic, else the number of shared-memory
  *                            slots of the persistent kernels (at most what fits).
  * Returns GN3D_OK or GN3D_ERR_INVALID_ARG for an unknown setting or value.
