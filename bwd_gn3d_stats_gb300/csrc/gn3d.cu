@@ -187,9 +187,9 @@ int raise_smem(const void* func, int bytes, DevInfo& di, int which) {
 }
 
 // Grid of a persistent launch: one CTA per SM, all resident at once.
-int coop_grid(const void* func, int smem, const DevInfo& di, int* grid) {
+int coop_grid(const void* func, int threads, int smem, const DevInfo& di, int* grid) {
   int per_sm = 0;
-  GN3D_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, func, kFusedThreads, (size_t)smem),
+  GN3D_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, func, threads, (size_t)smem),
             "occupancy");
   if (per_sm < 1) {
     g_detail = "persistent kernel does not fit on an SM";
@@ -231,13 +231,14 @@ int launch_forward(const void* x, const float* gamma, const float* beta, const P
     auto k = k_fwd_fused<TI, TO>;
     const int which = (sizeof(TI) == 2 ? 0 : 2) + (sizeof(TO) == 2 ? 0 : 1);
     int rc = raise_smem((const void*)k, smem, di, which);
+    const int threads = 32 * (FwdPolicy<TI>::kWarps + 1);
     int grid = 0;
-    if (!rc) rc = coop_grid((const void*)k, smem, di, &grid);
+    if (!rc) rc = coop_grid((const void*)k, threads, smem, di, &grid);
     if (rc) { cudaFreeAsync(s.base, st); return rc; }
     void* args[] = {(void*)&xp, (void*)&yp, (void*)&p, (void*)&w, (void*)&cfg, (void*)&fs, (void*)&eps,
                     (void*)&gamma, (void*)&beta, (void*)&mean, (void*)&rstd};
     g_launches += 1;
-    e = cudaLaunchCooperativeKernel((const void*)k, dim3(grid), dim3(kFusedThreads), args, (size_t)smem, st);
+    e = cudaLaunchCooperativeKernel((const void*)k, dim3(grid), dim3(threads), args, (size_t)smem, st);
   } else if (e == cudaSuccess) {
     const int64_t warps_needed = (p.units + kStreamWarps - 1) / kStreamWarps;
     g_launches += 2;
@@ -290,13 +291,14 @@ int launch_backward(const void* dy, const void* x, const float* mean, const floa
     const int smem = cfg.slots * (slot + 16) + cfg.recs * rec;
     auto k = k_bwd_fused<T>;
     int rc = raise_smem((const void*)k, smem, di, sizeof(T) == 2 ? 4 : 5);
+    const int threads = 32 * (BwdPolicy<T>::kWarps + 1);
     int grid = 0;
-    if (!rc) rc = coop_grid((const void*)k, smem, di, &grid);
+    if (!rc) rc = coop_grid((const void*)k, threads, smem, di, &grid);
     if (rc) { cudaFreeAsync(s.base, st); return rc; }
     void* args[] = {(void*)&dyp, (void*)&xp, (void*)&dxp, (void*)&p, (void*)&mean, (void*)&rstd, (void*)&gamma,
                     (void*)&w, (void*)&cfg, (void*)&fs, (void*)&dgamma, (void*)&dbeta};
     g_launches += 1;
-    e = cudaLaunchCooperativeKernel((const void*)k, dim3(grid), dim3(kFusedThreads), args, (size_t)smem, st);
+    e = cudaLaunchCooperativeKernel((const void*)k, dim3(grid), dim3(threads), args, (size_t)smem, st);
   } else if (e == cudaSuccess) {
     const int64_t warps_needed = (p.units + kStreamWarps - 1) / kStreamWarps;
     g_launches += 2;
@@ -396,15 +398,16 @@ int launch_forward_noalloc(const void* x, const float* gamma, const float* beta,
       nd.attr_smem[which] = smem;
     }
   }
+  const int threads = 32 * (FwdPolicy<TI>::kWarps + 1);
   int grid = 0;
-  int rc = coop_grid((const void*)k, smem, nd.facts, &grid);
+  int rc = coop_grid((const void*)k, threads, smem, nd.facts, &grid);
   if (rc) return rc;
   const TI* xp = static_cast<const TI*>(x);
   TO* yp = static_cast<TO*>(y);
   void* args[] = {(void*)&xp, (void*)&yp, (void*)&p, (void*)&w, (void*)&cfg, (void*)&fs, (void*)&eps,
                   (void*)&gamma, (void*)&beta, (void*)&mean, (void*)&rstd};
   g_launches += 1;
-  GN3D_CUDA(cudaLaunchCooperativeKernel((const void*)k, dim3(grid), dim3(kFusedThreads), args, (size_t)smem, st),
+  GN3D_CUDA(cudaLaunchCooperativeKernel((const void*)k, dim3(grid), dim3(threads), args, (size_t)smem, st),
             "forward launch");
   return GN3D_OK;
 }

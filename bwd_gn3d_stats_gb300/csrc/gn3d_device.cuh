@@ -185,28 +185,54 @@ __device__ __forceinline__ void load_vec(const T* body, int j, float v[8]) {
   Vec<T>::unpack(r, v);
 }
 
+// ------------------------------------------------------------ unit views
+// A unit's body as one warp sees it: lane l owns vectors l, l+32, ..., l+480.
+// RegView holds the lane's vectors in registers (loaded once, from shared or
+// global memory); MemView reads them from memory on every access.  Both give
+// the same values in the same order, so every function below does the same
+// arithmetic whichever view it is handed.
+template <class T>
+struct RegView {
+  uint4 w[kVecPerLane][Vec<T>::kRaw];
+  int nv;
+  template <class Src>
+  __device__ __forceinline__ void load(const T* body, int nv_) {
+    nv = nv_;
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int i = 0; i < kVecPerLane; ++i)
+      if (lane + 32 * i < nv) Vec<T>::template load<Src>(body + (lane + 32 * i) * kVec, w[i]);
+  }
+  __device__ __forceinline__ bool has(int i) const { return (int)(threadIdx.x & 31) + 32 * i < nv; }
+  __device__ __forceinline__ void get(int i, float v[8]) const { Vec<T>::unpack(w[i], v); }
+};
+
+template <class T, class Src>
+struct MemView {
+  const T* body;
+  int nv;
+  __device__ __forceinline__ bool has(int i) const { return (int)(threadIdx.x & 31) + 32 * i < nv; }
+  __device__ __forceinline__ void get(int i, float v[8]) const {
+    load_vec<T, Src>(body, (int)(threadIdx.x & 31) + 32 * i, v);
+  }
+};
+
 // Corrected two-pass moments of one unit, by one warp: m1 = sum/n, then
 // c = sum(x - m1), q = sum((x - m1)^2); mean = m1 + c/n, M2 = q - c*(c/n) (the
 // correction term keeps M2 exact to first order in the error of m1; ScaFFold
 // PR #93: a corrected two-pass per tile, merged with Chan's formula).
-// `body` points at vector 0 of the unit's body (nv vectors); scalars come from x.
-// bf16 bodies stay in registers (packed) between the passes; fp32 ones are read twice.
-template <class T, class Src>
-__device__ __forceinline__ Part unit_moments(const T* body, int nv, const T* __restrict__ x, const URange& q) {
+// Scalars (head/tail) come from x.
+template <class T, class View>
+__device__ __forceinline__ Part unit_moments(const View& u, const T* __restrict__ x, const URange& q) {
   Part m = {0.f, 0.f, 0, 0.f};
   if (q.n == 0) return m;
   const int lane = threadIdx.x & 31;
-  constexpr bool kHold = Vec<T>::kRaw == 1;
-  uint4 raw[kHold ? kVecPerLane : 1][Vec<T>::kRaw];
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int i = 0; i < kVecPerLane; ++i) {
-    const int j = lane + 32 * i;
-    if (j < nv) {
+    if (u.has(i)) {
       float v[8];
-      uint4* r = raw[kHold ? i : 0];
-      Vec<T>::template load<Src>(body + j * kVec, r);
-      Vec<T>::unpack(r, v);
+      u.get(i, v);
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc[e] = fadd(acc[e], v[e]);
     }
@@ -221,12 +247,9 @@ __device__ __forceinline__ Part unit_moments(const T* body, int nv, const T* __r
   float qq[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int i = 0; i < kVecPerLane; ++i) {
-    const int j = lane + 32 * i;
-    if (j < nv) {
+    if (u.has(i)) {
       float v[8];
-      uint4* r = raw[kHold ? i : 0];
-      if (!kHold) Vec<T>::template load<Src>(body + j * kVec, r);
-      Vec<T>::unpack(r, v);
+      u.get(i, v);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const float d = fsub(v[e], m1);
@@ -343,7 +366,14 @@ template <class T>
 __device__ __forceinline__ void fwd_stat_global(const Plan& p, const FwdWs& ws, const T* body,
                                                 const T* __restrict__ x, const URange& q, int64_t u, int64_t kr,
                                                 float eps, float* mean_out, float* rstd_out) {
-  const Part m = unit_moments<T, FromGlobal>(body, (int)((q.b1 - q.b0) / kVec), x, q);
+  Part m;
+  if (Vec<T>::kRaw == 1) {  // bf16: read the unit once, keep it in registers for both passes
+    RegView<T> v;
+    v.template load<FromGlobal>(body, (int)((q.b1 - q.b0) / kVec));
+    m = unit_moments<T>(v, x, q);
+  } else {
+    m = unit_moments<T>(MemView<T, FromGlobal>{body, (int)((q.b1 - q.b0) / kVec)}, x, q);
+  }
   const int lane = threadIdx.x & 31;
   if (lane == 0) ws.parts[u] = m;
   const int64_t blk = block_of(p, q.row, kr), kb = kr / kBlockUnits;
@@ -354,22 +384,20 @@ __device__ __forceinline__ void fwd_stat_global(const Plan& p, const FwdWs& ws, 
 }
 
 // NORM of one forward unit, by one warp: y = (x - hi)*sc + (beta - lo*sc), sc = rstd*gamma.
-template <class TI, class TO, class Src>
-__device__ __forceinline__ void fwd_norm(const TI* body, const TI* __restrict__ x, TO* __restrict__ y,
+template <class TI, class TO, class View>
+__device__ __forceinline__ void fwd_norm(const View& u, const TI* __restrict__ x, TO* __restrict__ y,
                                          const URange& q, float4 st, float gam, float bet) {
   const int lane = threadIdx.x & 31;
   const float sc = fmul(st.z, gam);
   const float sh = ffma(-st.y, sc, bet);
-  const int nv = (int)((q.b1 - q.b0) / kVec);
-#pragma unroll 4
+#pragma unroll
   for (int i = 0; i < kVecPerLane; ++i) {
-    const int j = lane + 32 * i;
-    if (j < nv) {
+    if (u.has(i)) {
       float v[8];
-      load_vec<TI, Src>(body, j, v);
+      u.get(i, v);
 #pragma unroll
       for (int e = 0; e < 8; ++e) v[e] = ffma(fsub(v[e], st.x), sc, sh);
-      IO<TO>::store8(y + q.b0 + (int64_t)j * kVec, v);
+      IO<TO>::store8(y + q.b0 + (int64_t)(lane + 32 * i) * kVec, v);
     }
   }
   if (lane < scalar_count(q)) {
@@ -391,19 +419,18 @@ struct BwdWs {
 };
 
 // S1 = sum dy, S2 = sum dy*(x - mean) of one unit, by one warp.
-template <class T, class Src>
-__device__ __forceinline__ float2 unit_bwd_sums(const T* xb, const T* db, int nv, const T* __restrict__ x,
+template <class T, class View>
+__device__ __forceinline__ float2 unit_bwd_sums(const View& ux, const View& ud, const T* __restrict__ x,
                                                 const T* __restrict__ dy, const URange& q, float mu) {
   const int lane = threadIdx.x & 31;
   float a1[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   float a2[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
+#pragma unroll
   for (int i = 0; i < kVecPerLane; ++i) {
-    const int j = lane + 32 * i;
-    if (j < nv) {
+    if (ux.has(i)) {
       float vx[8], vd[8];
-      load_vec<T, Src>(xb, j, vx);
-      load_vec<T, Src>(db, j, vd);
+      ux.get(i, vx);
+      ud.get(i, vd);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         a1[e] = fadd(a1[e], vd[e]);
@@ -491,7 +518,9 @@ __device__ __forceinline__ void bwd_stat_global(const Plan& p, const BwdWs& ws, 
                                                 const URange& q, int64_t u, int64_t kr, const float* mean,
                                                 const float* rstd, const float* gamma, float* dgamma,
                                                 float* dbeta) {
-  const float2 s = unit_bwd_sums<T, FromGlobal>(xb, db, (int)((q.b1 - q.b0) / kVec), x, dy, q, mean[q.row / p.Cg]);
+  const int nv = (int)((q.b1 - q.b0) / kVec);
+  const float2 s = unit_bwd_sums<T>(MemView<T, FromGlobal>{xb, nv}, MemView<T, FromGlobal>{db, nv}, x, dy, q,
+                                    mean[q.row / p.Cg]);
   const int lane = threadIdx.x & 31;
   if (lane == 0) ws.parts[u] = s;
   const int64_t blk = block_of(p, q.row, kr), kb = kr / kBlockUnits;
@@ -509,25 +538,23 @@ struct DxCoef {
 };
 
 // NORM of one backward unit, by one warp.
-template <class T, class Src>
-__device__ __forceinline__ void bwd_norm(const T* xb, const T* db, const T* __restrict__ x,
+template <class T, class View>
+__device__ __forceinline__ void bwd_norm(const View& ux, const View& ud, const T* __restrict__ x,
                                          const T* __restrict__ dy, T* __restrict__ dx, const URange& q,
                                          const DxCoef& k, float gam) {
   const int lane = threadIdx.x & 31;
   const float p1 = k.single ? 0.f : fmul(k.r, gam);
   const float p2 = k.single ? 0.f : fmul(fmul(k.r, k.r), k.b);
   const float p3 = k.single ? 0.f : fmul(k.r, k.a);
-  const int nv = (int)((q.b1 - q.b0) / kVec);
-#pragma unroll 4
+#pragma unroll
   for (int i = 0; i < kVecPerLane; ++i) {
-    const int j = lane + 32 * i;
-    if (j < nv) {
+    if (ux.has(i)) {
       float vx[8], vd[8];
-      load_vec<T, Src>(xb, j, vx);
-      load_vec<T, Src>(db, j, vd);
+      ux.get(i, vx);
+      ud.get(i, vd);
 #pragma unroll
       for (int e = 0; e < 8; ++e) vd[e] = ffma(vd[e], p1, ffma(-p2, fsub(vx[e], k.mu), -p3));
-      IO<T>::store8(dx + q.b0 + (int64_t)j * kVec, vd);
+      IO<T>::store8(dx + q.b0 + (int64_t)(lane + 32 * i) * kVec, vd);
     }
   }
   if (lane < scalar_count(q)) {

@@ -39,8 +39,6 @@
 
 namespace gn3d {
 
-constexpr int kConsumerWarps = 16;
-constexpr int kFusedThreads = 32 * (kConsumerWarps + 1);
 constexpr int kMaxSlots = 32;  // one producer lane per slot
 constexpr uint32_t kStatusTimeout = 4;  // GN3D_ERR_TIMEOUT
 constexpr int kMaxLag = 8;
@@ -59,15 +57,17 @@ struct FusedSync {
   uint32_t* status;  // device status word (GN3D_ERR_TIMEOUT on a timeout)
 };
 
-// Shared-memory record of one block in its STAT phase: the unit partials and
-// an arrival count.  Records are reused round-robin over the CTA's STAT blocks;
-// a block's tasks all finish before the task of block j + recs can start,
-// because the producer only loads task i after task i - nslots has finished
-// and recs > nslots.
+// Shared-memory record of one block in its STAT phase: the unit partials, an
+// arrival count, and the sequence number of the CTA's STAT block allowed to
+// use it next.  Records are reused round-robin over the CTA's STAT blocks
+// (block j uses record j mod recs); a warp writes into a record only once the
+// previous block there has been merged (next == j), which in practice it always
+// has -- recs exceeds the slots, so block j + recs starts long after block j.
 template <class PartT>
 struct BlockRec {
   PartT part[kBlockUnits];
   int cnt;
+  long long next;
 };
 
 // ------------------------------------------------------------ scheduling
@@ -194,17 +194,23 @@ __device__ __forceinline__ bool wait_tag(const volatile unsigned long long* tag,
 // ------------------------------------------------------------- the kernel
 // Op supplies the direction-specific parts:
 //   Elem, PartT, kTensors       element type; unit partial type; tensors per slot
+//   kWarps                      consumer warps (the producer warp comes after them)
+//   kEarly, Held                Held is what a warp keeps of a unit: its body in
+//                               registers (kEarly: the slot is released as soon as
+//                               the registers are loaded) or a view of the slot
 //   src(t)                      base pointer of tensor t (0: x, 1: dy)
 //   ready(g)                    the group's ready flag
-//   unit(slot, q)               the unit's partial (one warp)
+//   hold(h, slot, q)            take the unit from its slot
+//   unit(h, q)                  the unit's partial (one warp)
 //   block_done(blk, a)          a completed block, lane l holding unit l's partial
 //   prepare(g)                  load group g's published statistics (one warp)
-//   norm(slot, q, row)          NORM of one unit (one warp)
+//   norm(h, q, row)             NORM of one unit (one warp)
 template <class Op>
 __device__ __forceinline__ void run_fused(Op& op, const Plan& p, const FusedCfg& cfg, const FusedSync& fs) {
   extern __shared__ __align__(128) unsigned char smem[];
   using T = typename Op::Elem;
   using PartT = typename Op::PartT;
+  constexpr int kConsumerWarps = Op::kWarps;
   constexpr int kTensorBytes = kUnitElems * (int)sizeof(T);
   constexpr int kSlotBytes = Op::kTensors * kTensorBytes;
   const int nslots = cfg.slots;
@@ -239,7 +245,10 @@ __device__ __forceinline__ void run_fused(Op& op, const Plan& p, const FusedCfg&
     fence_mbar_init();
     s_fail = 0;
   }
-  for (int i = threadIdx.x; i < cfg.recs; i += blockDim.x) recs[i].cnt = 0;
+  for (int i = threadIdx.x; i < cfg.recs; i += blockDim.x) {
+    recs[i].cnt = 0;
+    recs[i].next = i;
+  }
   __syncthreads();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -304,29 +313,51 @@ __device__ __forceinline__ void run_fused(Op& op, const Plan& p, const FusedCfg&
         break;
       }
       const unsigned char* data = smem + (size_t)slot * kSlotBytes;
+      typename Op::Held h;
+      op.hold(h, data, q);
+      if (Op::kEarly) {  // the unit is in registers: hand the slot back before computing
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+      }
       if (it.kind == kStat) {
-        const PartT v = op.unit(data, q);
+        const PartT v = op.unit(h, q);
         BlockRec<PartT>& rec = recs[it.sblk % cfg.recs];
-        int last = 0;
+        int last = 0, ok = 1;
         if (lane == 0) {
-          rec.part[it.kr - it.kb * kBlockUnits] = v;
-          __threadfence_block();  // the partial before the arrival
-          last = atomicAdd(&rec.cnt, 1) == it.bsz - 1;
-          if (last) __threadfence_block();  // the other warps' partials after it
+          // the record's previous block must have been merged (bounded wait)
+          const volatile long long* next = &rec.next;
+          for (unsigned long long w = 0; *next != it.sblk; ++w)
+            if (w > cfg.spin || s_fail) { ok = 0; break; }
+          if (ok) {
+            rec.part[it.kr - it.kb * kBlockUnits] = v;
+            __threadfence_block();  // the partial before the arrival
+            last = atomicAdd(&rec.cnt, 1) == it.bsz - 1;
+            if (last) __threadfence_block();  // the other warps' partials after it
+          }
         }
         __syncwarp();
+        if (!__shfl_sync(kFull, ok, 0)) {
+          s_fail = 1;
+          break;
+        }
         last = __shfl_sync(kFull, last, 0);
         if (last) {
           const PartT a = lane < it.bsz ? rec.part[lane] : PartT{};
           __syncwarp();
-          if (lane == 0) rec.cnt = 0;
+          if (lane == 0) {
+            rec.cnt = 0;
+            __threadfence_block();
+            *(volatile long long*)&rec.next = it.sblk + cfg.recs;  // the record is free
+          }
           op.block_done(it.b, a);
         }
       } else {
-        op.norm(data, q, it.row);
+        op.norm(h, q, it.row);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[slot]);
+      if (!Op::kEarly) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+      }
       it.advance(s, kConsumerWarps);
     }
   }
@@ -343,11 +374,26 @@ __device__ __forceinline__ void run_fused(Op& op, const Plan& p, const FusedCfg&
 }
 
 // ------------------------------------------------------------- forward op
+// bf16 units (8 KB) are loaded into registers and their slot released at once,
+// with 15 consumer warps; fp32 units stay in their slot, with 7.  With the
+// producer warp the CTA is 16 or 8 warps, so every thread keeps 128 or 255
+// registers (register files are allocated in 4-warp steps).
+template <class T> struct FwdPolicy {
+  static constexpr bool kEarly = Vec<T>::kRaw == 1;
+  static constexpr int kWarps = kEarly ? 15 : 7;
+};
+
 template <class TI, class TO>
 struct FwdOp {
   using Elem = TI;
   using PartT = Part;
   static constexpr int kTensors = 1;
+  static constexpr int kWarps = FwdPolicy<TI>::kWarps;
+  static constexpr bool kEarly = FwdPolicy<TI>::kEarly;
+  struct Held {
+    RegView<TI> r;                 // kEarly
+    MemView<TI, FromShared> m;     // otherwise
+  };
   const TI* x;
   TO* y;
   Plan p;
@@ -361,22 +407,28 @@ struct FwdOp {
 
   __device__ __forceinline__ const TI* src(int) const { return x; }
   __device__ __forceinline__ const uint32_t* ready(int64_t g) const { return ws.ready + g; }
-  __device__ __forceinline__ Part unit(const unsigned char* slot, const URange& q) const {
-    return unit_moments<TI, FromShared>(reinterpret_cast<const TI*>(slot), (int)((q.b1 - q.b0) / kVec), x, q);
+  __device__ __forceinline__ void hold(Held& h, const unsigned char* slot, const URange& q) const {
+    const int nv = (int)((q.b1 - q.b0) / kVec);
+    if (kEarly) h.r.template load<FromShared>(reinterpret_cast<const TI*>(slot), nv);
+    else h.m = MemView<TI, FromShared>{reinterpret_cast<const TI*>(slot), nv};
+  }
+  __device__ __forceinline__ Part unit(const Held& h, const URange& q) const {
+    return kEarly ? unit_moments<TI>(h.r, x, q) : unit_moments<TI>(h.m, x, q);
   }
   __device__ __forceinline__ void block_done(int64_t blk, const Part& a) {
     fwd_block_done(p, ws, blk, merge_block(a), eps, mean_out, rstd_out);
   }
   __device__ __forceinline__ void prepare(int64_t g) { st = __ldcg(ws.stats + g); }
-  __device__ __forceinline__ void norm(const unsigned char* slot, const URange& q, int64_t row) {
+  __device__ __forceinline__ void norm(const Held& h, const URange& q, int64_t row) {
     const int64_t c = channel_of(row, p.C);
-    fwd_norm<TI, TO, FromShared>(reinterpret_cast<const TI*>(slot), x, y, q, st, gamma ? gamma[c] : 1.f,
-                     beta ? beta[c] : 0.f);
+    const float gm = gamma ? gamma[c] : 1.f, bt = beta ? beta[c] : 0.f;
+    if (kEarly) fwd_norm<TI, TO>(h.r, x, y, q, st, gm, bt);
+    else fwd_norm<TI, TO>(h.m, x, y, q, st, gm, bt);
   }
 };
 
 template <class TI, class TO>
-__global__ void __launch_bounds__(kFusedThreads, 1)
+__global__ void __launch_bounds__(32 * (FwdPolicy<TI>::kWarps + 1), 1)
     k_fwd_fused(const TI* __restrict__ x, TO* __restrict__ y, Plan p, FwdWs ws, FusedCfg cfg, FusedSync fs,
                 float eps, const float* __restrict__ gamma, const float* __restrict__ beta, float* mean_out,
                 float* rstd_out) {
@@ -385,11 +437,25 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 }
 
 // ------------------------------------------------------------ backward op
+// bf16 units (x and dy, 16 KB) go to registers (128 per lane) and release their
+// slot at once, with 7 consumer warps (8 with the producer: 255 registers per
+// thread); fp32 units stay in their slot.
+template <class T> struct BwdPolicy {
+  static constexpr bool kEarly = Vec<T>::kRaw == 1;
+  static constexpr int kWarps = 7;
+};
+
 template <class T>
 struct BwdOp {
   using Elem = T;
   using PartT = float2;
   static constexpr int kTensors = 2;  // slot: x body, then dy body
+  static constexpr int kWarps = BwdPolicy<T>::kWarps;
+  static constexpr bool kEarly = BwdPolicy<T>::kEarly;
+  struct Held {
+    RegView<T> rx, rd;                // kEarly
+    MemView<T, FromShared> mx, md;    // otherwise
+  };
   const T* dy;
   const T* x;
   T* dx;
@@ -404,10 +470,20 @@ struct BwdOp {
 
   __device__ __forceinline__ const T* src(int t) const { return t == 0 ? x : dy; }
   __device__ __forceinline__ const uint32_t* ready(int64_t g) const { return ws.ready + g; }
-  __device__ __forceinline__ float2 unit(const unsigned char* slot, const URange& q) const {
+  __device__ __forceinline__ void hold(Held& h, const unsigned char* slot, const URange& q) const {
     const T* xb = reinterpret_cast<const T*>(slot);
-    return unit_bwd_sums<T, FromShared>(xb, xb + kUnitElems, (int)((q.b1 - q.b0) / kVec), x, dy, q,
-                                        mean[q.row / p.Cg]);
+    const int nv = (int)((q.b1 - q.b0) / kVec);
+    if (kEarly) {
+      h.rx.template load<FromShared>(xb, nv);
+      h.rd.template load<FromShared>(xb + kUnitElems, nv);
+    } else {
+      h.mx = MemView<T, FromShared>{xb, nv};
+      h.md = MemView<T, FromShared>{xb + kUnitElems, nv};
+    }
+  }
+  __device__ __forceinline__ float2 unit(const Held& h, const URange& q) const {
+    const float mu = mean[q.row / p.Cg];
+    return kEarly ? unit_bwd_sums<T>(h.rx, h.rd, x, dy, q, mu) : unit_bwd_sums<T>(h.mx, h.md, x, dy, q, mu);
   }
   __device__ __forceinline__ void block_done(int64_t blk, const float2& a) {
     bwd_block_done(p, ws, blk, a, rstd, gamma, dgamma, dbeta);
@@ -416,15 +492,16 @@ struct BwdOp {
     const float2 ab = __ldcg(ws.coef + g);
     k = DxCoef{mean[g], rstd[g], ab.x, ab.y, p.M == 1};
   }
-  __device__ __forceinline__ void norm(const unsigned char* slot, const URange& q, int64_t row) {
-    const T* xb = reinterpret_cast<const T*>(slot);
+  __device__ __forceinline__ void norm(const Held& h, const URange& q, int64_t row) {
     const int64_t c = channel_of(row, p.C);
-    bwd_norm<T, FromShared>(xb, xb + kUnitElems, x, dy, dx, q, k, gamma ? gamma[c] : 1.f);
+    const float gm = gamma ? gamma[c] : 1.f;
+    if (kEarly) bwd_norm<T>(h.rx, h.rd, x, dy, dx, q, k, gm);
+    else bwd_norm<T>(h.mx, h.md, x, dy, dx, q, k, gm);
   }
 };
 
 template <class T>
-__global__ void __launch_bounds__(kFusedThreads, 1)
+__global__ void __launch_bounds__(32 * (BwdPolicy<T>::kWarps + 1), 1)
     k_bwd_fused(const T* __restrict__ dy, const T* __restrict__ x, T* __restrict__ dx, Plan p,
                 const float* __restrict__ mean, const float* __restrict__ rstd, const float* __restrict__ gamma,
                 BwdWs ws, FusedCfg cfg, FusedSync fs, float* dgamma, float* dbeta) {

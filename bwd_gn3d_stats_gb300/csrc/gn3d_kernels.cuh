@@ -46,7 +46,8 @@ __global__ void __launch_bounds__(32 * kStreamWarps)
     const int64_t row = u / p.R;
     const URange q = unit_range_rk(p, row, u - row * p.R);
     const int64_t c = channel_of(row, p.C), g = row / p.Cg;
-    fwd_norm<TI, TO, FromGlobal>(x + q.b0, x, y, q, __ldcg(stats + g), gamma ? gamma[c] : 1.f, beta ? beta[c] : 0.f);
+    const MemView<TI, FromGlobal> v{x + q.b0, (int)((q.b1 - q.b0) / kVec)};
+    fwd_norm<TI, TO>(v, x, y, q, __ldcg(stats + g), gamma ? gamma[c] : 1.f, beta ? beta[c] : 0.f);
   }
 }
 
@@ -76,7 +77,9 @@ __global__ void __launch_bounds__(32 * kStreamWarps)
     const int64_t c = channel_of(row, p.C), g = row / p.Cg;
     const float2 ab = __ldcg(coef + g);
     const DxCoef k{mean[g], rstd[g], ab.x, ab.y, p.M == 1};
-    bwd_norm<T, FromGlobal>(x + q.b0, dy + q.b0, x, dy, dx, q, k, gamma ? gamma[c] : 1.f);
+    const int nv = (int)((q.b1 - q.b0) / kVec);
+    bwd_norm<T>(MemView<T, FromGlobal>{x + q.b0, nv}, MemView<T, FromGlobal>{dy + q.b0, nv}, x, dy, dx, q, k,
+                gamma ? gamma[c] : 1.f);
   }
 }
 
