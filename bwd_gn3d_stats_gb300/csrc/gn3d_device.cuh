@@ -151,8 +151,53 @@ struct FromGlobal {
   static __device__ __forceinline__ uint4 word(const void* p) { return *reinterpret_cast<const uint4*>(p); }
 };
 
+// ----------------------------------------------------------- fp32 pairs
+// Two fp32 values in one 64-bit register pair, for the paired fp32
+// instructions of sm_100-class GPUs (add/sub/mul/fma .rn.f32x2).  Each half is
+// rounded exactly as the scalar instruction would round it, so pair code gives
+// the same bits as the scalar code it replaces -- at half the instructions.
+typedef unsigned long long f2;
+
+__device__ __forceinline__ f2 f2_of(float lo, float hi) {
+  f2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ f2 f2_bits(uint32_t lo, uint32_t hi) {
+  f2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+__device__ __forceinline__ float f2_lo(f2 a) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a));
+  return lo;
+}
+__device__ __forceinline__ float f2_hi(f2 a) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a));
+  return hi;
+}
+__device__ __forceinline__ f2 f2_splat(float a) { return f2_of(a, a); }
+__device__ __forceinline__ f2 f2add(f2 a, f2 b) {
+  f2 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2 f2sub(f2 a, f2 b) {
+  f2 d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2 f2fma(f2 a, f2 b, f2 c) {
+  f2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
 template <class T> struct Vec;
 
+// A vector of 8 elements as 4 pairs: pair k holds elements 2k and 2k+1.
 template <> struct Vec<__nv_bfloat16> {
   static constexpr int kRaw = 1;
   template <class Src>
@@ -160,6 +205,12 @@ template <> struct Vec<__nv_bfloat16> {
   static __device__ __forceinline__ void unpack(const uint4 r[kRaw], float v[8]) {
     v[0] = bf16_lo(r[0].x); v[1] = bf16_hi(r[0].x); v[2] = bf16_lo(r[0].y); v[3] = bf16_hi(r[0].y);
     v[4] = bf16_lo(r[0].z); v[5] = bf16_hi(r[0].z); v[6] = bf16_lo(r[0].w); v[7] = bf16_hi(r[0].w);
+  }
+  static __device__ __forceinline__ void pairs(const uint4 r[kRaw], f2 p[4]) {
+    p[0] = f2_of(bf16_lo(r[0].x), bf16_hi(r[0].x));
+    p[1] = f2_of(bf16_lo(r[0].y), bf16_hi(r[0].y));
+    p[2] = f2_of(bf16_lo(r[0].z), bf16_hi(r[0].z));
+    p[3] = f2_of(bf16_lo(r[0].w), bf16_hi(r[0].w));
   }
 };
 
@@ -176,7 +227,40 @@ template <> struct Vec<float> {
     v[4] = __uint_as_float(r[1].x); v[5] = __uint_as_float(r[1].y);
     v[6] = __uint_as_float(r[1].z); v[7] = __uint_as_float(r[1].w);
   }
+  static __device__ __forceinline__ void pairs(const uint4 r[kRaw], f2 p[4]) {
+    p[0] = f2_bits(r[0].x, r[0].y);
+    p[1] = f2_bits(r[0].z, r[0].w);
+    p[2] = f2_bits(r[1].x, r[1].y);
+    p[3] = f2_bits(r[1].z, r[1].w);
+  }
 };
+
+// Store of 8 results given as 4 pairs (one rounding to the output type, RNE).
+template <class T>
+__device__ __forceinline__ void store8p(T* p, const f2 v[4]);
+
+template <>
+__device__ __forceinline__ void store8p<__nv_bfloat16>(__nv_bfloat16* p, const f2 v[4]) {
+  uint4 r;
+  r.x = IO<__nv_bfloat16>::pack2(f2_lo(v[0]), f2_hi(v[0]));
+  r.y = IO<__nv_bfloat16>::pack2(f2_lo(v[1]), f2_hi(v[1]));
+  r.z = IO<__nv_bfloat16>::pack2(f2_lo(v[2]), f2_hi(v[2]));
+  r.w = IO<__nv_bfloat16>::pack2(f2_lo(v[3]), f2_hi(v[3]));
+  __stcs(reinterpret_cast<uint4*>(p), r);
+}
+
+template <>
+__device__ __forceinline__ void store8p<float>(float* p, const f2 v[4]) {
+  __stcs(reinterpret_cast<float4*>(p), make_float4(f2_lo(v[0]), f2_hi(v[0]), f2_lo(v[1]), f2_hi(v[1])));
+  __stcs(reinterpret_cast<float4*>(p + 4), make_float4(f2_lo(v[2]), f2_hi(v[2]), f2_lo(v[3]), f2_hi(v[3])));
+}
+
+// The 8 running sums of a lane, kept as 4 pairs, meeting in the fixed tree.
+__device__ __forceinline__ float tree8p(const f2 a[4]) {
+  const float c[8] = {f2_lo(a[0]), f2_hi(a[0]), f2_lo(a[1]), f2_hi(a[1]),
+                      f2_lo(a[2]), f2_hi(a[2]), f2_lo(a[3]), f2_hi(a[3])};
+  return fadd(fadd(fadd(c[0], c[1]), fadd(c[2], c[3])), fadd(fadd(c[4], c[5]), fadd(c[6], c[7])));
+}
 
 template <class T, class Src>
 __device__ __forceinline__ void load_vec(const T* body, int j, float v[8]) {
@@ -204,7 +288,7 @@ struct RegView {
       if (lane + 32 * i < nv) Vec<T>::template load<Src>(body + (lane + 32 * i) * kVec, w[i]);
   }
   __device__ __forceinline__ bool has(int i) const { return (int)(threadIdx.x & 31) + 32 * i < nv; }
-  __device__ __forceinline__ void get(int i, float v[8]) const { Vec<T>::unpack(w[i], v); }
+  __device__ __forceinline__ void get(int i, f2 p[4]) const { Vec<T>::pairs(w[i], p); }
 };
 
 template <class T, class Src>
@@ -212,8 +296,10 @@ struct MemView {
   const T* body;
   int nv;
   __device__ __forceinline__ bool has(int i) const { return (int)(threadIdx.x & 31) + 32 * i < nv; }
-  __device__ __forceinline__ void get(int i, float v[8]) const {
-    load_vec<T, Src>(body, (int)(threadIdx.x & 31) + 32 * i, v);
+  __device__ __forceinline__ void get(int i, f2 p[4]) const {
+    uint4 r[Vec<T>::kRaw];
+    Vec<T>::template load<Src>(body + ((int)(threadIdx.x & 31) + 32 * i) * kVec, r);
+    Vec<T>::pairs(r, p);
   }
 };
 
@@ -227,38 +313,40 @@ __device__ __forceinline__ Part unit_moments(const View& u, const T* __restrict_
   Part m = {0.f, 0.f, 0, 0.f};
   if (q.n == 0) return m;
   const int lane = threadIdx.x & 31;
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  const f2 z2 = f2_splat(0.f);
+  f2 acc[4] = {z2, z2, z2, z2};
 #pragma unroll
   for (int i = 0; i < kVecPerLane; ++i) {
     if (u.has(i)) {
-      float v[8];
+      f2 v[4];
       u.get(i, v);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] = fadd(acc[e], v[e]);
+      for (int k = 0; k < 4; ++k) acc[k] = f2add(acc[k], v[k]);
     }
   }
-  float s = tree8(acc);
+  float s = tree8p(acc);
   const bool hs = lane < scalar_count(q);
   const float sv = hs ? IO<T>::load1(x + scalar_index(q, lane)) : 0.f;
   if (hs) s = fadd(s, sv);
   const float fn = (float)q.n;
   const float m1 = __fdiv_rn(warp_sum(s), fn);
-  float c[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  float qq[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  const f2 m12 = f2_splat(m1);
+  f2 c[4] = {z2, z2, z2, z2};
+  f2 qq[4] = {z2, z2, z2, z2};
 #pragma unroll
   for (int i = 0; i < kVecPerLane; ++i) {
     if (u.has(i)) {
-      float v[8];
+      f2 v[4];
       u.get(i, v);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float d = fsub(v[e], m1);
-        c[e] = fadd(c[e], d);
-        qq[e] = ffma(d, d, qq[e]);
+      for (int k = 0; k < 4; ++k) {
+        const f2 d = f2sub(v[k], m12);
+        c[k] = f2add(c[k], d);
+        qq[k] = f2fma(d, d, qq[k]);
       }
     }
   }
-  float cs = tree8(c), qs = tree8(qq);
+  float cs = tree8p(c), qs = tree8p(qq);
   if (hs) {
     const float d = fsub(sv, m1);
     cs = fadd(cs, d);
@@ -390,14 +478,15 @@ __device__ __forceinline__ void fwd_norm(const View& u, const TI* __restrict__ x
   const int lane = threadIdx.x & 31;
   const float sc = fmul(st.z, gam);
   const float sh = ffma(-st.y, sc, bet);
+  const f2 hi2 = f2_splat(st.x), sc2 = f2_splat(sc), sh2 = f2_splat(sh);
 #pragma unroll
   for (int i = 0; i < kVecPerLane; ++i) {
     if (u.has(i)) {
-      float v[8];
+      f2 v[4];
       u.get(i, v);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) v[e] = ffma(fsub(v[e], st.x), sc, sh);
-      IO<TO>::store8(y + q.b0 + (int64_t)(lane + 32 * i) * kVec, v);
+      for (int k = 0; k < 4; ++k) v[k] = f2fma(f2sub(v[k], hi2), sc2, sh2);
+      store8p<TO>(y + q.b0 + (int64_t)(lane + 32 * i) * kVec, v);
     }
   }
   if (lane < scalar_count(q)) {
@@ -423,22 +512,23 @@ template <class T, class View>
 __device__ __forceinline__ float2 unit_bwd_sums(const View& ux, const View& ud, const T* __restrict__ x,
                                                 const T* __restrict__ dy, const URange& q, float mu) {
   const int lane = threadIdx.x & 31;
-  float a1[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  float a2[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  const f2 z2 = f2_splat(0.f), mu2 = f2_splat(mu);
+  f2 a1[4] = {z2, z2, z2, z2};
+  f2 a2[4] = {z2, z2, z2, z2};
 #pragma unroll
   for (int i = 0; i < kVecPerLane; ++i) {
     if (ux.has(i)) {
-      float vx[8], vd[8];
+      f2 vx[4], vd[4];
       ux.get(i, vx);
       ud.get(i, vd);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        a1[e] = fadd(a1[e], vd[e]);
-        a2[e] = ffma(vd[e], fsub(vx[e], mu), a2[e]);
+      for (int k = 0; k < 4; ++k) {
+        a1[k] = f2add(a1[k], vd[k]);
+        a2[k] = f2fma(vd[k], f2sub(vx[k], mu2), a2[k]);
       }
     }
   }
-  float s1 = tree8(a1), s2 = tree8(a2);
+  float s1 = tree8p(a1), s2 = tree8p(a2);
   if (lane < scalar_count(q)) {
     const int64_t idx = scalar_index(q, lane);
     const float d = IO<T>::load1(dy + idx);
@@ -546,15 +636,16 @@ __device__ __forceinline__ void bwd_norm(const View& ux, const View& ud, const T
   const float p1 = k.single ? 0.f : fmul(k.r, gam);
   const float p2 = k.single ? 0.f : fmul(fmul(k.r, k.r), k.b);
   const float p3 = k.single ? 0.f : fmul(k.r, k.a);
+  const f2 p12 = f2_splat(p1), np22 = f2_splat(-p2), np32 = f2_splat(-p3), mu2 = f2_splat(k.mu);
 #pragma unroll
   for (int i = 0; i < kVecPerLane; ++i) {
     if (ux.has(i)) {
-      float vx[8], vd[8];
+      f2 vx[4], vd[4];
       ux.get(i, vx);
       ud.get(i, vd);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) vd[e] = ffma(vd[e], p1, ffma(-p2, fsub(vx[e], k.mu), -p3));
-      IO<T>::store8(dx + q.b0 + (int64_t)(lane + 32 * i) * kVec, vd);
+      for (int e = 0; e < 4; ++e) vd[e] = f2fma(vd[e], p12, f2fma(np22, f2sub(vx[e], mu2), np32));
+      store8p<T>(dx + q.b0 + (int64_t)(lane + 32 * i) * kVec, vd);
     }
   }
   if (lane < scalar_count(q)) {
