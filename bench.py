@@ -169,9 +169,16 @@ class Volume:
                          self.dgamma.data_ptr(), self.dbeta.data_ptr(), st)
 
 
-def time_device(vols, steps, warmup, flush, stream):
-    """Per-step device time (ms) of fwd+bwd over all sites, plus fwd/bwd split."""
+def time_device(vols, steps, warmup, flush, stream, kernel_timing=False):
+    """Per-step device time (ms) of fwd+bwd over all sites, plus fwd/bwd split.
+
+    All steps are enqueued before the one synchronize, so host-side launch work
+    overlaps the device and never shows as idle time between the events.  With
+    kernel_timing the library brackets each of its kernel launches in the timed
+    steps with events too (gn3d_kernel_time)."""
     import torch
+
+    import bwd_gn3d_stats_gb300 as gn
 
     st = stream.cuda_stream
     with torch.cuda.stream(stream):
@@ -180,7 +187,9 @@ def time_device(vols, steps, warmup, flush, stream):
                 v.fwd(st)
                 v.bwd(st)
         stream.synchronize()
-        tot, tf, tb = [], [], []
+        if kernel_timing:
+            gn.gn3d_debug_set(gn.DEBUG_TIMING, 1)
+        evs = []
         for _ in range(steps):
             flush.fill_(1)
             ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * len(vols) + 1)]
@@ -190,11 +199,29 @@ def time_device(vols, steps, warmup, flush, stream):
                 ev[2 * i + 1].record(stream)
                 v.bwd(st)
                 ev[2 * i + 2].record(stream)
-            stream.synchronize()
+            evs.append(ev)
+        stream.synchronize()
+        kernels = {}
+        if kernel_timing:
+            for name in gn.KERNELS:
+                ms, n = gn.gn3d_kernel_time(name)
+                if n:
+                    kernels[name] = {"launches": n, "ms_per_launch": ms / n}
+            gn.gn3d_debug_set(gn.DEBUG_TIMING, 0)
+        tot, tf, tb = [], [], []
+        for ev in evs:
             tot.append(ev[0].elapsed_time(ev[-1]))
             tf.append(sum(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(len(vols))))
             tb.append(sum(ev[2 * i + 1].elapsed_time(ev[2 * i + 2]) for i in range(len(vols))))
+    if kernel_timing:
+        return tot, tf, tb, kernels
     return tot, tf, tb
+
+
+# Algorithmic HBM bytes per launch of each kernel, in tensors of the volume's
+# size: what it must read and write at least (re-reads from L2 are not counted).
+KERNEL_TENSORS = {"k_fwd_fused": 2, "k_fwd_stats": 1, "k_fwd_norm": 2,
+                  "k_bwd_fused": 3, "k_bwd_reduce": 2, "k_bwd_dx": 3}
 
 
 def time_e2e(vol, steps, warmup, stream):
@@ -322,7 +349,7 @@ def run_gpu(args):
     torch.cuda.synchronize()
     with ClockSampler(local) as cs:
         t0 = time.perf_counter()
-        tot, tf, tb = time_device([vol], args.steps, args.warmup, flush, stream)
+        tot, tf, tb, kernels = time_device([vol], args.steps, args.warmup, flush, stream, kernel_timing=True)
         barrier(ws)
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
@@ -335,7 +362,15 @@ def run_gpu(args):
     e2e_ms, h2d, d2h = time_e2e(vol, max(2, args.steps // 2), 1, stream)
     e2e_ms = max_over_ranks(e2e_ms, ws, dev)
     peak, peak_kind = peaks()
-    # dominant kernel: the backward (one gn3d_backward call per step)
+    # dominant kernel: the one with the largest share of the timed steps' kernel time
+    tensor_bytes = site.numel * site.elem_bytes
+    kinfo = {}
+    for name, k in kernels.items():
+        kinfo[name] = {"launches": k["launches"], "us_per_launch": round(k["ms_per_launch"] * 1e3, 2),
+                       "algorithmic_bytes": KERNEL_TENSORS[name] * tensor_bytes,
+                       "gbs": round(KERNEL_TENSORS[name] * tensor_bytes / (k["ms_per_launch"] * 1e-3) / 1e9, 1)}
+    dom = max(kernels, key=lambda n: kernels[n]["ms_per_launch"] * kernels[n]["launches"])
+    dom_gbs = kinfo[dom]["gbs"]
     bwd_ms = sum(tb) / len(tb)
     fwd_ms = sum(tf) / len(tf)
     bwd_gbs = bb / (bwd_ms * 1e-3) / 1e9
@@ -371,9 +406,11 @@ def run_gpu(args):
             "pct_of_measured_copy": round(100 * value / ws / peak, 2),
             "fwd": {"ms": round(fwd_ms, 4), "gbs": round(fwd_gbs, 1)},
             "bwd": {"ms": round(bwd_ms, 4), "gbs": round(bwd_gbs, 1)},
-            "roofline": {"bound": "hbm", "kernel": "gn3d_backward", "achieved": round(bwd_gbs, 1),
-                         "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                         "frac": round(bwd_gbs / peak, 4), "traffic": traffic_for("gn3d_backward", args.workload)},
+            "roofline": {"bound": "hbm", "kernel": dom, "achieved": dom_gbs, "peak": peak, "peak_kind": peak_kind,
+                         "unit": "GB/s", "frac": round(dom_gbs / peak, 4),
+                         "algorithmic_bytes_per_launch": kinfo[dom]["algorithmic_bytes"],
+                         "traffic": traffic_for(dom, args.workload)},
+            "kernels": kinfo,
             "e2e": {"value": round(ws * (fb + bb) / (e2e_ms * 1e-3) / 1e9, 1), "unit": UNIT,
                     "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": int(launches),

@@ -151,7 +151,7 @@ def backward(dy, x, mean, rstd, gamma, G: int):
 
 # ------------------------------------------------------------ testing hooks
 
-DEBUG_PATH, DEBUG_SPIN_LIMIT, DEBUG_FORCE_TIMEOUT, DEBUG_LAG, DEBUG_SLOTS = range(5)
+DEBUG_PATH, DEBUG_SPIN_LIMIT, DEBUG_FORCE_TIMEOUT, DEBUG_LAG, DEBUG_SLOTS, DEBUG_TIMING = range(6)
 PATH_AUTO, PATH_STREAMING, PATH_FUSED = 0, 1, 2
 
 
@@ -160,6 +160,20 @@ def gn3d_debug_set(what: int, value: int):
     L.gn3d_debug_set.argtypes = [ctypes.c_int, ctypes.c_longlong]
     L.gn3d_debug_set.restype = ctypes.c_int
     _check(L.gn3d_debug_set(what, value))
+
+
+KERNELS = ("k_fwd_fused", "k_bwd_fused", "k_fwd_stats", "k_fwd_norm", "k_bwd_reduce", "k_bwd_dx")
+
+
+def gn3d_kernel_time(name: str):
+    """(total milliseconds, launches) of one kernel since timing was switched on
+    with gn3d_debug_set(DEBUG_TIMING, 1) (C entry point gn3d_kernel_time)."""
+    L = lib()
+    L.gn3d_kernel_time.argtypes = [ctypes.c_char_p, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_uint64)]
+    L.gn3d_kernel_time.restype = ctypes.c_int
+    ms, n = ctypes.c_double(0.0), ctypes.c_uint64(0)
+    _check(L.gn3d_kernel_time(name.encode(), ctypes.byref(ms), ctypes.byref(n)))
+    return ms.value, n.value
 
 
 def gn3d_forward_noalloc(x, gamma, beta, N, C, D, H, W, G, eps, in_dtype, out_dtype, y, mean, rstd, stream):

@@ -12,6 +12,7 @@
 #include <atomic>
 #include <mutex>
 #include <string>
+#include <vector>
 
 #include "../../include/gn3d.h"
 #include "gn3d_fused.cuh"
@@ -62,7 +63,7 @@ struct DevInfo {
   int smem_per_sm = 0;
   cudaMemPool_t pool = nullptr;
   uint32_t* status = nullptr;
-  int attr_smem[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // dynamic shared memory raised to, per kernel
+  int attr_smem[10] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0};  // dynamic shared memory raised to, per kernel
 };
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
@@ -144,6 +145,44 @@ struct Scratch {
 };
 
 int64_t rup(int64_t b) { return ((b + 255) / 256) * 256; }
+
+// ------------------------------------------------------------ kernel timing
+// While timing is on (GN3D_DEBUG_TIMING), each kernel launch is bracketed by two
+// CUDA events on its stream; gn3d_kernel_time resolves them per kernel.
+enum { KK_FWD_FUSED, KK_BWD_FUSED, KK_FWD_STATS, KK_FWD_NORM, KK_BWD_REDUCE, KK_BWD_DX, KK_COUNT };
+const char* const kKernelNames[KK_COUNT] = {"k_fwd_fused", "k_bwd_fused", "k_fwd_stats",
+                                            "k_fwd_norm",  "k_bwd_reduce", "k_bwd_dx"};
+std::atomic<int> g_timing{0};
+std::mutex g_tmu;
+struct TimedLaunch {
+  int kind;
+  cudaEvent_t a, b;
+};
+std::vector<TimedLaunch> g_timed;
+double g_kernel_ms[KK_COUNT];
+uint64_t g_kernel_n[KK_COUNT];
+
+struct LaunchTimer {
+  int kind;
+  cudaStream_t st;
+  cudaEvent_t a = nullptr;
+  LaunchTimer(int k, cudaStream_t s) : kind(k), st(s) {
+    if (!g_timing.load()) return;
+    if (cudaEventCreate(&a) != cudaSuccess || cudaEventRecord(a, st) != cudaSuccess) a = nullptr;
+  }
+  void done() {
+    if (!a) return;
+    cudaEvent_t b = nullptr;
+    if (cudaEventCreate(&b) == cudaSuccess && cudaEventRecord(b, st) == cudaSuccess) {
+      std::lock_guard<std::mutex> lk(g_tmu);
+      g_timed.push_back(TimedLaunch{kind, a, b});
+    } else {
+      cudaEventDestroy(a);
+      if (b) cudaEventDestroy(b);
+    }
+    a = nullptr;
+  }
+};
 
 bool use_fused() { return g_hook_path.load() != 1; }
 
@@ -238,15 +277,27 @@ int launch_forward(const void* x, const float* gamma, const float* beta, const P
     void* args[] = {(void*)&xp, (void*)&yp, (void*)&p, (void*)&w, (void*)&cfg, (void*)&fs, (void*)&eps,
                     (void*)&gamma, (void*)&beta, (void*)&mean, (void*)&rstd};
     g_launches += 1;
+    LaunchTimer tm(KK_FWD_FUSED, st);
     e = cudaLaunchCooperativeKernel((const void*)k, dim3(grid), dim3(threads), args, (size_t)smem, st);
+    tm.done();
   } else if (e == cudaSuccess) {
+    using Shape = FwdStatShape<TI>;
+    const int smem = Shape::kWarps * WarpRing<TI, 1, Shape::kSlots>::kWarpBytes;
+    auto ks = k_fwd_stats<TI>;
+    int rc = raise_smem((const void*)ks, smem, di, sizeof(TI) == 2 ? 6 : 7);
+    if (rc) { cudaFreeAsync(s.base, st); return rc; }
+    const int sgrid = grid_for(di, (nblk + Shape::kWarps - 1) / Shape::kWarps, 1);
     const int64_t warps_needed = (p.units + kStreamWarps - 1) / kStreamWarps;
     g_launches += 2;
-    k_fwd_stats<TI><<<grid_for(di, warps_needed, 8), 32 * kStreamWarps, 0, st>>>(xp, p, w, eps, mean, rstd);
+    LaunchTimer t1(KK_FWD_STATS, st);
+    ks<<<sgrid, 32 * Shape::kWarps, smem, st>>>(xp, p, w, eps, mean, rstd, spin_budget(), di.status);
+    t1.done();
     e = cudaGetLastError();
     if (e == cudaSuccess) {
+      LaunchTimer t2(KK_FWD_NORM, st);
       k_fwd_norm<TI, TO><<<grid_for(di, warps_needed, 8), 32 * kStreamWarps, 0, st>>>(xp, yp, p, w.stats, gamma,
                                                                                       beta);
+      t2.done();
       e = cudaGetLastError();
     }
   }
@@ -298,16 +349,28 @@ int launch_backward(const void* dy, const void* x, const float* mean, const floa
     void* args[] = {(void*)&dyp, (void*)&xp, (void*)&dxp, (void*)&p, (void*)&mean, (void*)&rstd, (void*)&gamma,
                     (void*)&w, (void*)&cfg, (void*)&fs, (void*)&dgamma, (void*)&dbeta};
     g_launches += 1;
+    LaunchTimer tm(KK_BWD_FUSED, st);
     e = cudaLaunchCooperativeKernel((const void*)k, dim3(grid), dim3(threads), args, (size_t)smem, st);
+    tm.done();
   } else if (e == cudaSuccess) {
+    using Shape = BwdRedShape<T>;
+    const int smem = Shape::kWarps * WarpRing<T, 2, Shape::kSlots>::kWarpBytes;
+    auto kr = k_bwd_reduce<T>;
+    int rc = raise_smem((const void*)kr, smem, di, sizeof(T) == 2 ? 8 : 9);
+    if (rc) { cudaFreeAsync(s.base, st); return rc; }
+    const int rgrid = grid_for(di, (nblk + Shape::kWarps - 1) / Shape::kWarps, 1);
     const int64_t warps_needed = (p.units + kStreamWarps - 1) / kStreamWarps;
     g_launches += 2;
-    k_bwd_reduce<T><<<grid_for(di, warps_needed, 8), 32 * kStreamWarps, 0, st>>>(dyp, xp, p, mean, rstd, gamma,
-                                                                                   w, dgamma, dbeta);
+    LaunchTimer t1(KK_BWD_REDUCE, st);
+    kr<<<rgrid, 32 * Shape::kWarps, smem, st>>>(dyp, xp, p, mean, rstd, gamma, w, dgamma, dbeta, spin_budget(),
+                                               di.status);
+    t1.done();
     e = cudaGetLastError();
     if (e == cudaSuccess) {
+      LaunchTimer t2(KK_BWD_DX, st);
       k_bwd_dx<T><<<grid_for(di, warps_needed, 8), 32 * kStreamWarps, 0, st>>>(dyp, xp, dxp, p, mean, rstd,
                                                                                 gamma, w.coef);
+      t2.done();
       e = cudaGetLastError();
     }
   }
@@ -577,6 +640,23 @@ extern "C" int gn3d_debug_set(int what, long long value) {
       if (value < -1 || value == 0 || value > 32) return arg_fail("slots: -1, 1 .. 32");
       g_hook_slots = value;
       break;
+    case GN3D_DEBUG_TIMING: {
+      if (value != 0 && value != 1) return arg_fail("timing: 0 or 1");
+      std::lock_guard<std::mutex> lk(g_tmu);
+      if (value) {
+        for (TimedLaunch& t : g_timed) {
+          cudaEventDestroy(t.a);
+          cudaEventDestroy(t.b);
+        }
+        g_timed.clear();
+        for (int k = 0; k < KK_COUNT; ++k) {
+          g_kernel_ms[k] = 0.0;
+          g_kernel_n[k] = 0;
+        }
+      }
+      g_timing = (int)value;
+      break;
+    }
     default:
       return arg_fail("unknown debug setting");
   }
@@ -595,5 +675,33 @@ extern "C" const char* gn3d_error_string(int status) {
 }
 
 extern "C" uint64_t gn3d_launch_count(void) { return g_launches.load(); }
+
+extern "C" int gn3d_kernel_time(const char* name, double* ms, uint64_t* launches) {
+  if (!name || !ms || !launches) return arg_fail("gn3d_kernel_time: NULL argument");
+  int kind = -1;
+  for (int k = 0; k < KK_COUNT; ++k)
+    if (std::string(name) == kKernelNames[k]) kind = k;
+  if (kind < 0) return arg_fail("gn3d_kernel_time: unknown kernel name");
+  std::lock_guard<std::mutex> lk(g_tmu);
+  cudaError_t err = cudaSuccess;
+  for (TimedLaunch& t : g_timed) {
+    float e = 0.f;
+    cudaError_t r = cudaEventSynchronize(t.b);
+    if (r == cudaSuccess) r = cudaEventElapsedTime(&e, t.a, t.b);
+    if (r == cudaSuccess) {
+      g_kernel_ms[t.kind] += e;
+      g_kernel_n[t.kind] += 1;
+    } else if (err == cudaSuccess) {
+      err = r;
+    }
+    cudaEventDestroy(t.a);
+    cudaEventDestroy(t.b);
+  }
+  g_timed.clear();
+  if (err != cudaSuccess) return cuda_fail(err, "kernel timing events");
+  *ms = g_kernel_ms[kind];
+  *launches = g_kernel_n[kind];
+  return GN3D_OK;
+}
 
 extern "C" const char* gn3d_version(void) { return "gn3d 0.3.0 sm_103a"; }

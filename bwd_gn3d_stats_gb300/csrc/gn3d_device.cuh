@@ -169,13 +169,13 @@ __device__ __forceinline__ f2 f2_bits(uint32_t lo, uint32_t hi) {
   return r;
 }
 __device__ __forceinline__ float f2_lo(f2 a) {
-  float lo, hi;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a));
+  float lo;
+  asm("{\n .reg .f32 t;\n mov.b64 {%0, t}, %1;\n}" : "=f"(lo) : "l"(a));
   return lo;
 }
 __device__ __forceinline__ float f2_hi(f2 a) {
-  float lo, hi;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a));
+  float hi;
+  asm("{\n .reg .f32 t;\n mov.b64 {t, %0}, %1;\n}" : "=f"(hi) : "l"(a));
   return hi;
 }
 __device__ __forceinline__ f2 f2_splat(float a) { return f2_of(a, a); }

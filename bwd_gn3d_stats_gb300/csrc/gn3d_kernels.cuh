@@ -3,19 +3,24 @@
 // Forward  (ScaFFold PR #93 "Optimize GroupNorm": split-group statistics, a
 //           corrected two-pass per tile merged with Chan's formula, then a
 //           normalize that rounds once on the store, PR #105):
-//   k_fwd_stats : each warp takes units in turn (fwd_stat); the warp that
-//                 completes a block or a group merges it.
-//   k_fwd_norm  : each warp normalizes units, last unit first, so the tail of
-//                 the statistics pass is re-read from L2.
+//   k_fwd_stats : each warp owns whole merge blocks (up to 16 consecutive units
+//                 of a row) and streams their bodies through a private ring of
+//                 shared-memory slots filled by 1-D bulk copies (the TMA
+//                 engine), so several units per warp are always in flight; it
+//                 merges each block in registers and the warp that completes a
+//                 group merges the group.
+//   k_fwd_norm  : each warp normalizes units, last unit first, so the part of x
+//                 the statistics pass read last is re-read from L2.
 // Backward (the same PR's _bwd_finalize/_dwdb_reduce/_dx split):
-//   k_bwd_reduce: S1 = sum dy, S2 = sum dy*(x - mean) per unit; group and
-//                 parameter-gradient merges by the completing warps.
+//   k_bwd_reduce: S1 = sum dy, S2 = sum dy*(x - mean) per unit, through the same
+//                 kind of ring; group and parameter-gradient merges by the
+//                 completing warps.
 //   k_bwd_dx    : dx per unit, last unit first.
-// These read unit bodies straight from global memory and use exactly the
-// arithmetic of the persistent kernels (gn3d_device.cuh), so the two launch
-// forms give bit-identical results.
+// These use exactly the units, merge blocks and arithmetic of the persistent
+// kernels (gn3d_device.cuh), so the two launch forms give bit-identical results.
 #pragma once
 #include "gn3d_device.cuh"
+#include "gn3d_sync.cuh"
 
 namespace gn3d {
 
@@ -25,15 +30,157 @@ __device__ __forceinline__ int64_t warp_global() {
   return (int64_t)blockIdx.x * kStreamWarps + (threadIdx.x >> 5);
 }
 
-template <class TI>
-__global__ void __launch_bounds__(32 * kStreamWarps)
-    k_fwd_stats(const TI* __restrict__ x, Plan p, FwdWs ws, float eps, float* mean_out, float* rstd_out) {
-  const int64_t nw = (int64_t)gridDim.x * kStreamWarps;
-  for (int64_t u = warp_global(); u < p.units; u += nw) {
-    const int64_t row = u / p.R, kr = u - row * p.R;
-    const URange q = unit_range_rk(p, row, kr);
-    fwd_stat_global<TI>(p, ws, x + q.b0, x, q, u, kr, eps, mean_out, rstd_out);
+// ---------------------------------------------------------- block rings
+// Warp w of CTA c walks merge blocks b = w*grid + c, then b + warps*grid, ...
+// (every SM gets an equal share of each part of the tensor), unit by unit.
+struct BlockWalk {
+  int64_t b, row, kb;  // current block, its row and index in the row
+  int bsz, ui;         // its unit count; the current unit in it
+  bool end;
+  __device__ __forceinline__ void set(const Plan& p, int64_t b_, int64_t nblk) {
+    b = b_;
+    end = b >= nblk;
+    if (!end) {
+      row = b / p.nb;
+      kb = b - row * p.nb;
+      bsz = block_size(p, kb);
+      ui = 0;
+    }
   }
+  __device__ __forceinline__ void next(const Plan& p, int64_t stride, int64_t nblk) {
+    if (++ui >= bsz) set(p, b + stride, nblk);
+  }
+  __device__ __forceinline__ int64_t k() const { return kb * kBlockUnits + ui; }
+};
+
+// A warp's private ring: kSlots slots of kTensors unit bodies each, one "full"
+// mbarrier per slot.  Lane 0 issues the bulk copies; the warp reads a slot only
+// after its barrier phase completed, and refills it only after every lane's
+// reads of it (a __syncwarp, then the proxy fence) -- no other warp touches it.
+template <class T, int kTensors, int kSlots>
+struct WarpRing {
+  static constexpr int kTensorBytes = kUnitElems * (int)sizeof(T);
+  static constexpr int kSlotBytes = kTensors * kTensorBytes;
+  // a warp's region: its slots, then its barriers, rounded up so that every
+  // warp's slots start on a 128-byte boundary (bulk copies need 16)
+  static constexpr int kWarpBytes = (kSlots * (kSlotBytes + 8) + 127) / 128 * 128;
+  static_assert(kSlotBytes % 128 == 0 && kTensorBytes % 16 == 0, "slot alignment");
+  static_assert((kSlots * kSlotBytes) % 8 == 0, "mbarrier alignment");
+  unsigned char* data;   // kSlots * kSlotBytes
+  uint64_t* bar;         // kSlots
+  int64_t issued = 0;    // copies issued
+  int64_t taken = 0;     // slots consumed
+
+  __device__ __forceinline__ void init(unsigned char* base) {
+    data = base;
+    bar = reinterpret_cast<uint64_t*>(base + (size_t)kSlots * kSlotBytes);
+    if ((threadIdx.x & 31) == 0) {
+      for (int i = 0; i < kSlots; ++i) mbar_init(&bar[i], 1);
+      fence_mbar_init();
+    }
+    __syncwarp();
+  }
+  // Issue the body of unit q into the next slot (all lanes call; lane 0 copies).
+  __device__ __forceinline__ void issue(const URange& q, const T* const* src) {
+    const int slot = (int)(issued % kSlots);
+    if ((threadIdx.x & 31) == 0) {
+      const uint32_t bytes = (uint32_t)((q.b1 - q.b0) * (int64_t)sizeof(T));
+      unsigned char* dst = data + (size_t)slot * kSlotBytes;
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(&bar[slot], bytes * kTensors);
+      if (bytes) {
+#pragma unroll
+        for (int t = 0; t < kTensors; ++t) bulk_g2s(dst + t * kTensorBytes, src[t] + q.b0, bytes, &bar[slot]);
+      }
+    }
+    ++issued;
+  }
+  // Wait (bounded) for the next slot's copy; returns its data or nullptr.
+  __device__ __forceinline__ const unsigned char* take(unsigned long long spin) {
+    const int slot = (int)(taken % kSlots);
+    if (!mbar_wait_bounded(&bar[slot], (uint32_t)((taken / kSlots) & 1), spin)) return nullptr;
+    ++taken;
+    return data + (size_t)slot * kSlotBytes;
+  }
+  // Wait (bounded) for every copy still in flight, after a failure.
+  __device__ __forceinline__ void drain(unsigned long long spin) {
+    for (int64_t t = taken; t < issued; ++t)
+      mbar_wait_bounded(&bar[t % kSlots], (uint32_t)((t / kSlots) & 1), spin);
+  }
+};
+
+__device__ __forceinline__ void record_timeout(uint32_t* status) {
+  if ((threadIdx.x & 31) == 0) atomicExch(status, 4u);  // GN3D_ERR_TIMEOUT
+}
+
+// Ring shapes per kernel and dtype: warps per CTA and slots per warp, one CTA
+// per SM, every ring in 192 KB of shared memory.
+template <class T> struct FwdStatShape {
+  static constexpr int kWarps = sizeof(T) == 2 ? 8 : 4;
+  static constexpr int kSlots = 3;
+};
+template <class T> struct BwdRedShape {
+  static constexpr int kWarps = sizeof(T) == 2 ? 4 : 3;
+  static constexpr int kSlots = sizeof(T) == 2 ? 3 : 2;
+};
+
+template <class TI>
+__global__ void __launch_bounds__(32 * FwdStatShape<TI>::kWarps, 1)
+    k_fwd_stats(const TI* __restrict__ x, Plan p, FwdWs ws, float eps, float* mean_out, float* rstd_out,
+                unsigned long long spin, uint32_t* status) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  using Shape = FwdStatShape<TI>;
+  using Ring = WarpRing<TI, 1, Shape::kSlots>;
+  constexpr bool kRegs = Vec<TI>::kRaw == 1;  // bf16: the unit goes to registers, the slot is refilled at once
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  Ring ring;
+  ring.init(smem + (size_t)warp * Ring::kWarpBytes);
+  const int64_t nblk = p.NC * p.nb, stride = (int64_t)gridDim.x * Shape::kWarps;
+  const int64_t first = (int64_t)warp * gridDim.x + blockIdx.x;
+  const TI* src[1] = {x};
+  BlockWalk ld, cu;
+  ld.set(p, first, nblk);
+  cu = ld;
+  for (int i = 0; i < Shape::kSlots && !ld.end; ++i) {
+    ring.issue(unit_range_rk(p, ld.row, ld.k()), src);
+    ld.next(p, stride, nblk);
+  }
+  Part a{0.f, 0.f, 0, 0.f};  // lane l: the partial of unit l of the current block
+  while (!cu.end) {
+    const unsigned char* slot = ring.take(spin);
+    if (!slot) {
+      record_timeout(status);
+      break;
+    }
+    const URange q = unit_range_rk(p, cu.row, cu.k());
+    const int nv = (int)((q.b1 - q.b0) / kVec);
+    Part m;
+    if (kRegs) {
+      RegView<TI> v;
+      v.template load<FromShared>(reinterpret_cast<const TI*>(slot), nv);
+      __syncwarp();
+      if (!ld.end) {
+        ring.issue(unit_range_rk(p, ld.row, ld.k()), src);
+        ld.next(p, stride, nblk);
+      }
+      m = unit_moments<TI>(v, x, q);
+    } else {
+      m = unit_moments<TI>(MemView<TI, FromShared>{reinterpret_cast<const TI*>(slot), nv}, x, q);
+      __syncwarp();
+      if (!ld.end) {
+        ring.issue(unit_range_rk(p, ld.row, ld.k()), src);
+        ld.next(p, stride, nblk);
+      }
+    }
+    if (lane == cu.ui) a = m;
+    if (cu.ui == cu.bsz - 1) {
+      fwd_block_done(p, ws, cu.b, merge_block(lane < cu.bsz ? a : Part{0.f, 0.f, 0, 0.f}), eps, mean_out,
+                     rstd_out);
+      a = Part{0.f, 0.f, 0, 0.f};
+    }
+    cu.next(p, stride, nblk);
+  }
+  ring.drain(spin);
 }
 
 template <class TI, class TO>
@@ -52,16 +199,52 @@ __global__ void __launch_bounds__(32 * kStreamWarps)
 }
 
 template <class T>
-__global__ void __launch_bounds__(32 * kStreamWarps)
+__global__ void __launch_bounds__(32 * BwdRedShape<T>::kWarps, 1)
     k_bwd_reduce(const T* __restrict__ dy, const T* __restrict__ x, Plan p, const float* __restrict__ mean,
                  const float* __restrict__ rstd, const float* __restrict__ gamma, BwdWs ws, float* dgamma,
-                 float* dbeta) {
-  const int64_t nw = (int64_t)gridDim.x * kStreamWarps;
-  for (int64_t u = warp_global(); u < p.units; u += nw) {
-    const int64_t row = u / p.R, kr = u - row * p.R;
-    const URange q = unit_range_rk(p, row, kr);
-    bwd_stat_global<T>(p, ws, x + q.b0, dy + q.b0, x, dy, q, u, kr, mean, rstd, gamma, dgamma, dbeta);
+                 float* dbeta, unsigned long long spin, uint32_t* status) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  using Shape = BwdRedShape<T>;
+  using Ring = WarpRing<T, 2, Shape::kSlots>;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  Ring ring;
+  ring.init(smem + (size_t)warp * Ring::kWarpBytes);
+  const int64_t nblk = p.NC * p.nb, stride = (int64_t)gridDim.x * Shape::kWarps;
+  const int64_t first = (int64_t)warp * gridDim.x + blockIdx.x;
+  const T* src[2] = {x, dy};
+  BlockWalk ld, cu;
+  ld.set(p, first, nblk);
+  cu = ld;
+  for (int i = 0; i < Shape::kSlots && !ld.end; ++i) {
+    ring.issue(unit_range_rk(p, ld.row, ld.k()), src);
+    ld.next(p, stride, nblk);
   }
+  float2 a = make_float2(0.f, 0.f);  // lane l: the sums of unit l of the current block
+  while (!cu.end) {
+    const unsigned char* slot = ring.take(spin);
+    if (!slot) {
+      record_timeout(status);
+      break;
+    }
+    const URange q = unit_range_rk(p, cu.row, cu.k());
+    const int nv = (int)((q.b1 - q.b0) / kVec);
+    const T* xs = reinterpret_cast<const T*>(slot);
+    const T* ds = reinterpret_cast<const T*>(slot + Ring::kTensorBytes);
+    const float2 v = unit_bwd_sums<T>(MemView<T, FromShared>{xs, nv}, MemView<T, FromShared>{ds, nv}, x, dy, q,
+                                      mean[q.row / p.Cg]);
+    __syncwarp();
+    if (!ld.end) {
+      ring.issue(unit_range_rk(p, ld.row, ld.k()), src);
+      ld.next(p, stride, nblk);
+    }
+    if (lane == cu.ui) a = v;
+    if (cu.ui == cu.bsz - 1) {
+      bwd_block_done(p, ws, cu.b, lane < cu.bsz ? a : make_float2(0.f, 0.f), rstd, gamma, dgamma, dbeta);
+      a = make_float2(0.f, 0.f);
+    }
+    cu.next(p, stride, nblk);
+  }
+  ring.drain(spin);
 }
 
 template <class T>

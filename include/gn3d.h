@@ -154,6 +154,9 @@ uint64_t gn3d_launch_count(void);
  *                            between the statistics pass and the elementwise pass.
  *   GN3D_DEBUG_SLOTS         -1 automatic, else the number of shared-memory
  *                            slots of the persistent kernels (at most what fits).
+ *   GN3D_DEBUG_TIMING        1 clears the per-kernel times and starts recording
+ *                            them: every kernel launch is bracketed by two CUDA
+ *                            events on its stream (see gn3d_kernel_time); 0 stops.
  * Returns GN3D_OK or GN3D_ERR_INVALID_ARG for an unknown setting or value.
  */
 enum {
@@ -161,9 +164,20 @@ enum {
   GN3D_DEBUG_SPIN_LIMIT = 1,
   GN3D_DEBUG_FORCE_TIMEOUT = 2,
   GN3D_DEBUG_LAG = 3,
-  GN3D_DEBUG_SLOTS = 4
+  GN3D_DEBUG_SLOTS = 4,
+  GN3D_DEBUG_TIMING = 5
 };
 int gn3d_debug_set(int what, long long value);
+
+/*
+ * Device time of one kernel, summed over the launches recorded since
+ * GN3D_DEBUG_TIMING was last set to 1.  `name` is one of "k_fwd_fused",
+ * "k_bwd_fused", "k_fwd_stats", "k_fwd_norm", "k_bwd_reduce", "k_bwd_dx".
+ * Waits for the recorded events (host-blocking), then writes the total
+ * milliseconds to *ms and the launch count to *launches.  Returns GN3D_OK,
+ * GN3D_ERR_INVALID_ARG (NULL argument, unknown name) or GN3D_ERR_CUDA.
+ */
+int gn3d_kernel_time(const char* name, double* ms, uint64_t* launches);
 
 /* Library version, e.g. "gn3d 0.3.0 sm_103a". */
 const char* gn3d_version(void);

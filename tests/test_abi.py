@@ -156,3 +156,17 @@ def test_gpu_torch_level_wrappers():
     assert torch.equal(y32.to(torch.bfloat16), y)
     dx, dg, db = gn.backward(torch.ones_like(x), x, mean, rstd, g, 4)
     assert dx.dtype == torch.bfloat16 and dg.shape == (8,)
+
+
+def test_kernel_timing_hooks_without_launches(L):
+    # starting a timing window clears it; nothing launched -> zero time, zero launches
+    gn.gn3d_debug_set(gn.DEBUG_TIMING, 1)
+    try:
+        for name in gn.KERNELS:
+            assert gn.gn3d_kernel_time(name) == (0.0, 0)
+        with pytest.raises(gn.GN3DError):
+            gn.gn3d_kernel_time("k_not_a_kernel")
+        with pytest.raises(gn.GN3DError):
+            gn.gn3d_debug_set(gn.DEBUG_TIMING, 2)
+    finally:
+        gn.gn3d_debug_set(gn.DEBUG_TIMING, 0)
