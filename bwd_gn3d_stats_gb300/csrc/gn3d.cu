@@ -63,7 +63,7 @@ struct DevInfo {
   int smem_per_sm = 0;
   cudaMemPool_t pool = nullptr;
   uint32_t* status = nullptr;
-  int attr_smem[10] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0};  // dynamic shared memory raised to, per kernel
+  std::vector<std::pair<const void*, int>> attr_smem;  // dynamic shared memory raised to, per kernel
 };
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
@@ -215,13 +215,19 @@ FusedCfg fused_cfg(const DevInfo& di, int slot_bytes, int rec_bytes, int64_t gro
   return c;
 }
 
-int raise_smem(const void* func, int bytes, DevInfo& di, int which) {
+int raise_smem(const void* func, int bytes, DevInfo& di) {
   std::lock_guard<std::mutex> lk(g_mu);
-  if (di.attr_smem[which] < bytes) {
-    GN3D_CUDA(cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes),
-              "cudaFuncSetAttribute");
-    di.attr_smem[which] = bytes;
+  for (auto& e : di.attr_smem) {
+    if (e.first != func) continue;
+    if (e.second < bytes) {
+      GN3D_CUDA(cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes),
+                "cudaFuncSetAttribute");
+      e.second = bytes;
+    }
+    return GN3D_OK;
   }
+  GN3D_CUDA(cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes), "cudaFuncSetAttribute");
+  di.attr_smem.emplace_back(func, bytes);
   return GN3D_OK;
 }
 
@@ -268,8 +274,7 @@ int launch_forward(const void* x, const float* gamma, const float* beta, const P
     FusedCfg cfg = fused_cfg(di, slot, rec, p.M * (int64_t)sizeof(TI));
     const int smem = cfg.slots * (slot + 16) + cfg.recs * rec;
     auto k = k_fwd_fused<TI, TO>;
-    const int which = (sizeof(TI) == 2 ? 0 : 2) + (sizeof(TO) == 2 ? 0 : 1);
-    int rc = raise_smem((const void*)k, smem, di, which);
+    int rc = raise_smem((const void*)k, smem, di);
     const int threads = 32 * (FwdPolicy<TI>::kWarps + 1);
     int grid = 0;
     if (!rc) rc = coop_grid((const void*)k, threads, smem, di, &grid);
@@ -283,8 +288,9 @@ int launch_forward(const void* x, const float* gamma, const float* beta, const P
   } else if (e == cudaSuccess) {
     using Shape = FwdStatShape<TI>;
     const int smem = Shape::kWarps * WarpRing<TI, 1, Shape::kSlots>::kWarpBytes;
-    auto ks = k_fwd_stats<TI>;
-    int rc = raise_smem((const void*)ks, smem, di, sizeof(TI) == 2 ? 6 : 7);
+    const bool full = plan_all_full(p);
+    auto ks = full ? k_fwd_stats<TI, true> : k_fwd_stats<TI, false>;
+    int rc = raise_smem((const void*)ks, smem, di);
     if (rc) { cudaFreeAsync(s.base, st); return rc; }
     const int sgrid = grid_for(di, (nblk + Shape::kWarps - 1) / Shape::kWarps, 1);
     const int64_t warps_needed = (p.units + kStreamWarps - 1) / kStreamWarps;
@@ -295,8 +301,8 @@ int launch_forward(const void* x, const float* gamma, const float* beta, const P
     e = cudaGetLastError();
     if (e == cudaSuccess) {
       LaunchTimer t2(KK_FWD_NORM, st);
-      k_fwd_norm<TI, TO><<<grid_for(di, warps_needed, 8), 32 * kStreamWarps, 0, st>>>(xp, yp, p, w.stats, gamma,
-                                                                                      beta);
+      auto kn = full ? k_fwd_norm<TI, TO, true> : k_fwd_norm<TI, TO, false>;
+      kn<<<grid_for(di, warps_needed, 8), 32 * kStreamWarps, 0, st>>>(xp, yp, p, w.stats, gamma, beta);
       t2.done();
       e = cudaGetLastError();
     }
@@ -341,7 +347,7 @@ int launch_backward(const void* dy, const void* x, const float* mean, const floa
     FusedCfg cfg = fused_cfg(di, slot, rec, 2 * p.M * (int64_t)sizeof(T));
     const int smem = cfg.slots * (slot + 16) + cfg.recs * rec;
     auto k = k_bwd_fused<T>;
-    int rc = raise_smem((const void*)k, smem, di, sizeof(T) == 2 ? 4 : 5);
+    int rc = raise_smem((const void*)k, smem, di);
     const int threads = 32 * (BwdPolicy<T>::kWarps + 1);
     int grid = 0;
     if (!rc) rc = coop_grid((const void*)k, threads, smem, di, &grid);
@@ -355,8 +361,9 @@ int launch_backward(const void* dy, const void* x, const float* mean, const floa
   } else if (e == cudaSuccess) {
     using Shape = BwdRedShape<T>;
     const int smem = Shape::kWarps * WarpRing<T, 2, Shape::kSlots>::kWarpBytes;
-    auto kr = k_bwd_reduce<T>;
-    int rc = raise_smem((const void*)kr, smem, di, sizeof(T) == 2 ? 8 : 9);
+    const bool full = plan_all_full(p);
+    auto kr = full ? k_bwd_reduce<T, true> : k_bwd_reduce<T, false>;
+    int rc = raise_smem((const void*)kr, smem, di);
     if (rc) { cudaFreeAsync(s.base, st); return rc; }
     const int rgrid = grid_for(di, (nblk + Shape::kWarps - 1) / Shape::kWarps, 1);
     const int64_t warps_needed = (p.units + kStreamWarps - 1) / kStreamWarps;
@@ -368,8 +375,8 @@ int launch_backward(const void* dy, const void* x, const float* mean, const floa
     e = cudaGetLastError();
     if (e == cudaSuccess) {
       LaunchTimer t2(KK_BWD_DX, st);
-      k_bwd_dx<T><<<grid_for(di, warps_needed, 8), 32 * kStreamWarps, 0, st>>>(dyp, xp, dxp, p, mean, rstd,
-                                                                                gamma, w.coef);
+      auto kd = full ? k_bwd_dx<T, true> : k_bwd_dx<T, false>;
+      kd<<<grid_for(di, warps_needed, 8), 32 * kStreamWarps, 0, st>>>(dyp, xp, dxp, p, mean, rstd, gamma, w.coef);
       t2.done();
       e = cudaGetLastError();
     }

@@ -195,6 +195,16 @@ __device__ __forceinline__ f2 f2fma(f2 a, f2 b, f2 c) {
   return d;
 }
 
+// (lo - k, hi - k) for the two bf16 halves of w, as an fp32 pair.
+__device__ __forceinline__ f2 bf16_pair_minus(uint32_t w, float k) {
+  f2 d;
+  asm("{\n .reg .b16 l, h;\n .reg .f32 dl, dh;\n mov.b32 {l, h}, %1;\n sub.rn.f32.bf16 dl, l, %2;\n"
+      " sub.rn.f32.bf16 dh, h, %2;\n mov.b64 %0, {dl, dh};\n}"
+      : "=l"(d)
+      : "r"(w), "f"(k));
+  return d;
+}
+
 template <class T> struct Vec;
 
 // A vector of 8 elements as 4 pairs: pair k holds elements 2k and 2k+1.
@@ -211,6 +221,14 @@ template <> struct Vec<__nv_bfloat16> {
     p[1] = f2_of(bf16_lo(r[0].y), bf16_hi(r[0].y));
     p[2] = f2_of(bf16_lo(r[0].z), bf16_hi(r[0].z));
     p[3] = f2_of(bf16_lo(r[0].w), bf16_hi(r[0].w));
+  }
+  // x - k as pairs: one mixed-precision subtraction per element (bf16 operand,
+  // fp32 result, rounded once -- the same value as converting x first).
+  static __device__ __forceinline__ void diff(const uint4 r[kRaw], float k, f2 d[4]) {
+    d[0] = bf16_pair_minus(r[0].x, k);
+    d[1] = bf16_pair_minus(r[0].y, k);
+    d[2] = bf16_pair_minus(r[0].z, k);
+    d[3] = bf16_pair_minus(r[0].w, k);
   }
 };
 
@@ -232,6 +250,13 @@ template <> struct Vec<float> {
     p[1] = f2_bits(r[0].z, r[0].w);
     p[2] = f2_bits(r[1].x, r[1].y);
     p[3] = f2_bits(r[1].z, r[1].w);
+  }
+  static __device__ __forceinline__ void diff(const uint4 r[kRaw], float k, f2 d[4]) {
+    f2 p[4];
+    pairs(r, p);
+    const f2 k2 = f2_splat(k);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) d[e] = f2sub(p[e], k2);
   }
 };
 
@@ -287,8 +312,17 @@ struct RegView {
     for (int i = 0; i < kVecPerLane; ++i)
       if (lane + 32 * i < nv) Vec<T>::template load<Src>(body + (lane + 32 * i) * kVec, w[i]);
   }
+  // all 16 vectors present (a full unit)
+  template <class Src>
+  __device__ __forceinline__ void load_full(const T* body) {
+    nv = kUnitVecs;
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int i = 0; i < kVecPerLane; ++i) Vec<T>::template load<Src>(body + (lane + 32 * i) * kVec, w[i]);
+  }
   __device__ __forceinline__ bool has(int i) const { return (int)(threadIdx.x & 31) + 32 * i < nv; }
   __device__ __forceinline__ void get(int i, f2 p[4]) const { Vec<T>::pairs(w[i], p); }
+  __device__ __forceinline__ void diff(int i, float k, f2 d[4]) const { Vec<T>::diff(w[i], k, d); }
 };
 
 template <class T, class Src>
@@ -301,65 +335,12 @@ struct MemView {
     Vec<T>::template load<Src>(body + ((int)(threadIdx.x & 31) + 32 * i) * kVec, r);
     Vec<T>::pairs(r, p);
   }
+  __device__ __forceinline__ void diff(int i, float k, f2 d[4]) const {
+    uint4 r[Vec<T>::kRaw];
+    Vec<T>::template load<Src>(body + ((int)(threadIdx.x & 31) + 32 * i) * kVec, r);
+    Vec<T>::diff(r, k, d);
+  }
 };
-
-// Corrected two-pass moments of one unit, by one warp: m1 = sum/n, then
-// c = sum(x - m1), q = sum((x - m1)^2); mean = m1 + c/n, M2 = q - c*(c/n) (the
-// correction term keeps M2 exact to first order in the error of m1; ScaFFold
-// PR #93: a corrected two-pass per tile, merged with Chan's formula).
-// Scalars (head/tail) come from x.
-template <class T, class View>
-__device__ __forceinline__ Part unit_moments(const View& u, const T* __restrict__ x, const URange& q) {
-  Part m = {0.f, 0.f, 0, 0.f};
-  if (q.n == 0) return m;
-  const int lane = threadIdx.x & 31;
-  const f2 z2 = f2_splat(0.f);
-  f2 acc[4] = {z2, z2, z2, z2};
-#pragma unroll
-  for (int i = 0; i < kVecPerLane; ++i) {
-    if (u.has(i)) {
-      f2 v[4];
-      u.get(i, v);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) acc[k] = f2add(acc[k], v[k]);
-    }
-  }
-  float s = tree8p(acc);
-  const bool hs = lane < scalar_count(q);
-  const float sv = hs ? IO<T>::load1(x + scalar_index(q, lane)) : 0.f;
-  if (hs) s = fadd(s, sv);
-  const float fn = (float)q.n;
-  const float m1 = __fdiv_rn(warp_sum(s), fn);
-  const f2 m12 = f2_splat(m1);
-  f2 c[4] = {z2, z2, z2, z2};
-  f2 qq[4] = {z2, z2, z2, z2};
-#pragma unroll
-  for (int i = 0; i < kVecPerLane; ++i) {
-    if (u.has(i)) {
-      f2 v[4];
-      u.get(i, v);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const f2 d = f2sub(v[k], m12);
-        c[k] = f2add(c[k], d);
-        qq[k] = f2fma(d, d, qq[k]);
-      }
-    }
-  }
-  float cs = tree8p(c), qs = tree8p(qq);
-  if (hs) {
-    const float d = fsub(sv, m1);
-    cs = fadd(cs, d);
-    qs = ffma(d, d, qs);
-  }
-  const float2 t = warp_sum2(cs, qs);
-  m.m1 = m1;
-  m.cn = __fdiv_rn(t.x, fn);
-  m.m2 = fsub(t.y, fmul(t.x, m.cn));
-  if (m.m2 < 0.f) m.m2 = 0.f;  // rounding only; NaN is kept
-  m.n = q.n;
-  return m;
-}
 
 // Shifted-sum merge (the parallel-variance combine of Chan, Golub & LeVeque):
 // with the shift K and d_i = mean_i - K,  S = sum n_i d_i,  Q = sum (M2_i + n_i d_i^2);
@@ -383,6 +364,9 @@ __device__ __forceinline__ Part finish_merge(float K, float S, float Q, int64_t 
   return r;
 }
 
+// Loads issued together by the lane-strided merges (their sums keep lane order).
+constexpr int kMergeBatch = 8;
+
 __device__ __forceinline__ Part ldcg_part(const Part* p) {
   const float4 r = __ldcg(reinterpret_cast<const float4*>(p));
   return Part{r.x, r.y, __float_as_int(r.z), r.w};
@@ -401,6 +385,15 @@ __device__ __forceinline__ Part merge_block(const Part a) {
   return finish_merge(K, t.x, t.y, n);
 }
 
+// Merge of the 32 lanes' partials of one unit (total count n), by one warp.
+__device__ __forceinline__ Part merge_lanes(const Part a, int n) {
+  const float K = __shfl_sync(kFull, fadd(a.m1, a.cn), 0);
+  float S, Q;
+  shifted_terms(a, K, S, Q);
+  const float2 t = warp_sum2(S, Q);
+  return finish_merge(K, t.x, t.y, n);
+}
+
 // Group merge of its Cg*nb block partials (contiguous), by one warp: lane l takes
 // blocks l, l+32, ... in order, then the butterfly.  Returns (mean hi, mean lo,
 // rstd) with mean = hi + lo and rstd = 1/sqrt(M2/M + eps).
@@ -409,16 +402,99 @@ __device__ __forceinline__ float4 merge_group(const Part* blocks, int64_t nblk, 
   const Part b0 = ldcg_part(blocks);
   const float K = fadd(b0.m1, b0.cn);
   float S = 0.f, Q = 0.f;
-  for (int64_t i = lane; i < nblk; i += 32) {
-    float s, q;
-    shifted_terms(ldcg_part(blocks + i), K, s, q);
-    S = fadd(S, s);
-    Q = fadd(Q, q);
+  // loads in batches of kMergeBatch (independent), sums in the same order
+  for (int64_t i0 = lane; i0 < nblk; i0 += 32 * kMergeBatch) {
+    Part v[kMergeBatch];
+#pragma unroll
+    for (int j = 0; j < kMergeBatch; ++j)
+      if (i0 + 32 * j < nblk) v[j] = ldcg_part(blocks + i0 + 32 * j);
+#pragma unroll
+    for (int j = 0; j < kMergeBatch; ++j) {
+      if (i0 + 32 * j < nblk) {
+        float s, q;
+        shifted_terms(v[j], K, s, q);
+        S = fadd(S, s);
+        Q = fadd(Q, q);
+      }
+    }
   }
   const float2 t = warp_sum2(S, Q);
   const Part g = finish_merge(K, t.x, t.y, M);
   const float var = __fdiv_rn(g.m2, (float)M);
   return make_float4(g.m1, g.cn, __frsqrt_rn(fadd(var, eps)), 0.f);
+}
+
+// Moments of one unit, by one warp, in one pass over its elements.  Lane l
+// first takes a pilot mean K_l of its first kPilotVecs vectors, then sums
+// d = x - K_l and d^2 over all its elements: its partial is n_l, mean
+// K_l + c/n_l (kept as the pair K_l, c/n_l) and M2 = q - c*(c/n_l).  The
+// lanes' partials then merge with the shifted-sum formula below, shifted by
+// lane 0's mean.  Shifting by the mean of a quarter of the lane's elements
+// bounds the cancellation of the one pass: by Cauchy-Schwarz,
+// sum d^2 <= (n_l / pilot) * M2 = 4 * M2 (ScaFFold PR #93 keeps per-tile
+// partials merged with Chan's formula; this is that merge one level down).
+// kFull: a unit of 4096 body elements and no head or tail scalars, every lane
+// full -- the same arithmetic as the general path, without its checks.
+constexpr int kPilotVecs = 4;
+
+template <bool kFull, class T, class View>
+__device__ __forceinline__ Part unit_moments(const View& u, const T* __restrict__ x, const URange& q) {
+  if (!kFull && q.n == 0) return Part{0.f, 0.f, 0, 0.f};
+  const int lane = threadIdx.x & 31;
+  const f2 z2 = f2_splat(0.f);
+  f2 pa[4] = {z2, z2, z2, z2};
+  int npv = 0;
+#pragma unroll
+  for (int i = 0; i < kPilotVecs; ++i) {
+    if (kFull || u.has(i)) {
+      f2 v[4];
+      u.get(i, v);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) pa[k] = f2add(pa[k], v[k]);
+      ++npv;
+    }
+  }
+  const bool hs = !kFull && lane < scalar_count(q);
+  const float sv = hs ? IO<T>::load1(x + scalar_index(q, lane)) : 0.f;
+  // the shift: the pilot mean (an exact power-of-two scaling when the lane is full),
+  // else the lane's scalar, else 0 for an empty lane
+  float K;
+  if (kFull) K = fmul(tree8p(pa), 1.f / (float)(kVec * kPilotVecs));
+  else K = npv > 0 ? __fdiv_rn(tree8p(pa), (float)(kVec * npv)) : sv;
+  f2 c[4] = {z2, z2, z2, z2};
+  f2 qq[4] = {z2, z2, z2, z2};
+  int nvl = 0;
+#pragma unroll
+  for (int i = 0; i < kVecPerLane; ++i) {
+    if (kFull || u.has(i)) {
+      f2 d[4];
+      u.diff(i, K, d);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        c[k] = f2add(c[k], d[k]);
+        qq[k] = f2fma(d[k], d[k], qq[k]);
+      }
+      ++nvl;
+    }
+  }
+  float cs = tree8p(c), qs = tree8p(qq);
+  if (hs) {
+    const float d = fsub(sv, K);
+    cs = fadd(cs, d);
+    qs = ffma(d, d, qs);
+  }
+  Part lp;
+  lp.m1 = K;
+  if (kFull) {
+    lp.n = kVec * kVecPerLane;
+    lp.cn = fmul(cs, 1.f / (float)(kVec * kVecPerLane));
+  } else {
+    lp.n = kVec * nvl + (hs ? 1 : 0);
+    lp.cn = lp.n > 0 ? __fdiv_rn(cs, (float)lp.n) : 0.f;
+  }
+  lp.m2 = fsub(qs, fmul(cs, lp.cn));
+  if (lp.m2 < 0.f) lp.m2 = 0.f;  // rounding only; NaN is kept
+  return merge_lanes(lp, kFull ? kUnitElems : q.n);
 }
 
 // --------------------------------------------------------------- forward
@@ -448,48 +524,25 @@ __device__ __forceinline__ void fwd_block_done(const Plan& p, const FwdWs& ws, i
   }
 }
 
-// STAT of one forward unit through global memory (streaming form), by one warp:
-// unit moments; the warp that completes the unit's block merges it.
-template <class T>
-__device__ __forceinline__ void fwd_stat_global(const Plan& p, const FwdWs& ws, const T* body,
-                                                const T* __restrict__ x, const URange& q, int64_t u, int64_t kr,
-                                                float eps, float* mean_out, float* rstd_out) {
-  Part m;
-  if (Vec<T>::kRaw == 1) {  // bf16: read the unit once, keep it in registers for both passes
-    RegView<T> v;
-    v.template load<FromGlobal>(body, (int)((q.b1 - q.b0) / kVec));
-    m = unit_moments<T>(v, x, q);
-  } else {
-    m = unit_moments<T>(MemView<T, FromGlobal>{body, (int)((q.b1 - q.b0) / kVec)}, x, q);
-  }
-  const int lane = threadIdx.x & 31;
-  if (lane == 0) ws.parts[u] = m;
-  const int64_t blk = block_of(p, q.row, kr), kb = kr / kBlockUnits;
-  const int bsz = block_size(p, kb);
-  if (!warp_arrive_last(ws.bcnt + blk, (uint32_t)bsz)) return;
-  const Part a = lane < bsz ? ldcg_part(ws.parts + q.row * p.R + kb * kBlockUnits + lane) : Part{0.f, 0.f, 0, 0.f};
-  fwd_block_done(p, ws, blk, merge_block(a), eps, mean_out, rstd_out);
-}
-
 // NORM of one forward unit, by one warp: y = (x - hi)*sc + (beta - lo*sc), sc = rstd*gamma.
-template <class TI, class TO, class View>
+template <bool kFull, class TI, class TO, class View>
 __device__ __forceinline__ void fwd_norm(const View& u, const TI* __restrict__ x, TO* __restrict__ y,
                                          const URange& q, float4 st, float gam, float bet) {
   const int lane = threadIdx.x & 31;
   const float sc = fmul(st.z, gam);
   const float sh = ffma(-st.y, sc, bet);
-  const f2 hi2 = f2_splat(st.x), sc2 = f2_splat(sc), sh2 = f2_splat(sh);
+  const f2 sc2 = f2_splat(sc), sh2 = f2_splat(sh);
 #pragma unroll
   for (int i = 0; i < kVecPerLane; ++i) {
-    if (u.has(i)) {
+    if (kFull || u.has(i)) {
       f2 v[4];
-      u.get(i, v);
+      u.diff(i, st.x, v);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) v[k] = f2fma(f2sub(v[k], hi2), sc2, sh2);
+      for (int k = 0; k < 4; ++k) v[k] = f2fma(v[k], sc2, sh2);
       store8p<TO>(y + q.b0 + (int64_t)(lane + 32 * i) * kVec, v);
     }
   }
-  if (lane < scalar_count(q)) {
+  if (!kFull && lane < scalar_count(q)) {
     const int64_t idx = scalar_index(q, lane);
     IO<TO>::store1(y + idx, ffma(fsub(IO<TI>::load1(x + idx), st.x), sc, sh));
   }
@@ -508,28 +561,28 @@ struct BwdWs {
 };
 
 // S1 = sum dy, S2 = sum dy*(x - mean) of one unit, by one warp.
-template <class T, class View>
+template <bool kFull, class T, class View>
 __device__ __forceinline__ float2 unit_bwd_sums(const View& ux, const View& ud, const T* __restrict__ x,
                                                 const T* __restrict__ dy, const URange& q, float mu) {
   const int lane = threadIdx.x & 31;
-  const f2 z2 = f2_splat(0.f), mu2 = f2_splat(mu);
+  const f2 z2 = f2_splat(0.f);
   f2 a1[4] = {z2, z2, z2, z2};
   f2 a2[4] = {z2, z2, z2, z2};
 #pragma unroll
   for (int i = 0; i < kVecPerLane; ++i) {
-    if (ux.has(i)) {
-      f2 vx[4], vd[4];
-      ux.get(i, vx);
+    if (kFull || ux.has(i)) {
+      f2 xm[4], vd[4];
+      ux.diff(i, mu, xm);
       ud.get(i, vd);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         a1[k] = f2add(a1[k], vd[k]);
-        a2[k] = f2fma(vd[k], f2sub(vx[k], mu2), a2[k]);
+        a2[k] = f2fma(vd[k], xm[k], a2[k]);
       }
     }
   }
   float s1 = tree8p(a1), s2 = tree8p(a2);
-  if (lane < scalar_count(q)) {
+  if (!kFull && lane < scalar_count(q)) {
     const int64_t idx = scalar_index(q, lane);
     const float d = IO<T>::load1(dy + idx);
     s1 = fadd(s1, d);
@@ -550,10 +603,18 @@ __device__ __forceinline__ void bwd_group(const Plan& p, const BwdWs& ws, int64_
     const int64_t row = g * p.Cg + cl;
     const float2* bp = ws.bparts + row * p.nb;
     float s1 = 0.f, s2 = 0.f;
-    for (int64_t i = lane; i < p.nb; i += 32) {
-      const float2 v = __ldcg(bp + i);
-      s1 = fadd(s1, v.x);
-      s2 = fadd(s2, v.y);
+    for (int64_t i0 = lane; i0 < p.nb; i0 += 32 * kMergeBatch) {
+      float2 v[kMergeBatch];
+#pragma unroll
+      for (int j = 0; j < kMergeBatch; ++j)
+        if (i0 + 32 * j < p.nb) v[j] = __ldcg(bp + i0 + 32 * j);
+#pragma unroll
+      for (int j = 0; j < kMergeBatch; ++j) {
+        if (i0 + 32 * j < p.nb) {
+          s1 = fadd(s1, v[j].x);
+          s2 = fadd(s2, v[j].y);
+        }
+      }
     }
     const float2 t = warp_sum2(s1, s2);
     if (lane == 0) ws.rows[row] = t;
@@ -574,10 +635,23 @@ __device__ __forceinline__ void bwd_param_grads(const Plan& p, const float* rstd
   for (int64_t c = threadIdx.x & 31; c < p.C; c += 32) {
     const int64_t g = c / p.Cg;
     float dg = 0.f, db = 0.f;
-    for (int64_t n = 0; n < p.N; ++n) {
-      const float2 rs = __ldcg(rows + n * p.C + c);
-      dg = fadd(dg, fmul(rstd[n * p.G + g], rs.y));
-      db = fadd(db, rs.x);
+    for (int64_t n0 = 0; n0 < p.N; n0 += kMergeBatch) {
+      float2 rs[kMergeBatch];
+      float r[kMergeBatch];
+#pragma unroll
+      for (int j = 0; j < kMergeBatch; ++j) {
+        if (n0 + j < p.N) {
+          rs[j] = __ldcg(rows + (n0 + j) * p.C + c);
+          r[j] = rstd[(n0 + j) * p.G + g];
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kMergeBatch; ++j) {
+        if (n0 + j < p.N) {
+          dg = fadd(dg, fmul(r[j], rs[j].y));
+          db = fadd(db, rs[j].x);
+        }
+      }
     }
     if (dgamma) dgamma[c] = dg;
     if (dbeta) dbeta[c] = db;
@@ -601,25 +675,6 @@ __device__ __forceinline__ void bwd_block_done(const Plan& p, const BwdWs& ws, i
   bwd_param_grads(p, rstd, ws.rows, dgamma, dbeta);
 }
 
-// STAT of one backward unit through global memory (streaming form), by one warp.
-template <class T>
-__device__ __forceinline__ void bwd_stat_global(const Plan& p, const BwdWs& ws, const T* xb, const T* db,
-                                                const T* __restrict__ x, const T* __restrict__ dy,
-                                                const URange& q, int64_t u, int64_t kr, const float* mean,
-                                                const float* rstd, const float* gamma, float* dgamma,
-                                                float* dbeta) {
-  const int nv = (int)((q.b1 - q.b0) / kVec);
-  const float2 s = unit_bwd_sums<T>(MemView<T, FromGlobal>{xb, nv}, MemView<T, FromGlobal>{db, nv}, x, dy, q,
-                                    mean[q.row / p.Cg]);
-  const int lane = threadIdx.x & 31;
-  if (lane == 0) ws.parts[u] = s;
-  const int64_t blk = block_of(p, q.row, kr), kb = kr / kBlockUnits;
-  const int bsz = block_size(p, kb);
-  if (!warp_arrive_last(ws.bcnt + blk, (uint32_t)bsz)) return;
-  const float2 v = lane < bsz ? __ldcg(ws.parts + q.row * p.R + kb * kBlockUnits + lane) : make_float2(0.f, 0.f);
-  bwd_block_done(p, ws, blk, v, rstd, gamma, dgamma, dbeta);
-}
-
 // Per-group coefficients of dx = dy*p1 - (x - mean)*p2 - p3, with p1 = rstd*gamma,
 // p2 = rstd^2 * b, p3 = rstd * a  (= rstd*((dy*gamma - a) - xhat*b)).
 struct DxCoef {
@@ -628,7 +683,7 @@ struct DxCoef {
 };
 
 // NORM of one backward unit, by one warp.
-template <class T, class View>
+template <bool kFull, class T, class View>
 __device__ __forceinline__ void bwd_norm(const View& ux, const View& ud, const T* __restrict__ x,
                                          const T* __restrict__ dy, T* __restrict__ dx, const URange& q,
                                          const DxCoef& k, float gam) {
@@ -636,19 +691,19 @@ __device__ __forceinline__ void bwd_norm(const View& ux, const View& ud, const T
   const float p1 = k.single ? 0.f : fmul(k.r, gam);
   const float p2 = k.single ? 0.f : fmul(fmul(k.r, k.r), k.b);
   const float p3 = k.single ? 0.f : fmul(k.r, k.a);
-  const f2 p12 = f2_splat(p1), np22 = f2_splat(-p2), np32 = f2_splat(-p3), mu2 = f2_splat(k.mu);
+  const f2 p12 = f2_splat(p1), np22 = f2_splat(-p2), np32 = f2_splat(-p3);
 #pragma unroll
   for (int i = 0; i < kVecPerLane; ++i) {
-    if (ux.has(i)) {
-      f2 vx[4], vd[4];
-      ux.get(i, vx);
+    if (kFull || ux.has(i)) {
+      f2 xm[4], vd[4];
+      ux.diff(i, k.mu, xm);
       ud.get(i, vd);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) vd[e] = f2fma(vd[e], p12, f2fma(np22, f2sub(vx[e], mu2), np32));
+      for (int e = 0; e < 4; ++e) vd[e] = f2fma(vd[e], p12, f2fma(np22, xm[e], np32));
       store8p<T>(dx + q.b0 + (int64_t)(lane + 32 * i) * kVec, vd);
     }
   }
-  if (lane < scalar_count(q)) {
+  if (!kFull && lane < scalar_count(q)) {
     const int64_t idx = scalar_index(q, lane);
     const float d = IO<T>::load1(dy + idx);
     IO<T>::store1(dx + idx, ffma(d, p1, ffma(-p2, fsub(IO<T>::load1(x + idx), k.mu), -p3)));

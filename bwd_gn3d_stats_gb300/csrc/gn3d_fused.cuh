@@ -375,12 +375,12 @@ __device__ __forceinline__ void run_fused(Op& op, const Plan& p, const FusedCfg&
 
 // ------------------------------------------------------------- forward op
 // bf16 units (8 KB) are loaded into registers and their slot released at once,
-// with 15 consumer warps; fp32 units stay in their slot, with 7.  With the
-// producer warp the CTA is 16 or 8 warps, so every thread keeps 128 or 255
+// with 11 consumer warps; fp32 units stay in their slot, with 7.  With the
+// producer warp the CTA is 12 or 8 warps, so every thread keeps 168 or 255
 // registers (register files are allocated in 4-warp steps).
 template <class T> struct FwdPolicy {
   static constexpr bool kEarly = Vec<T>::kRaw == 1;
-  static constexpr int kWarps = kEarly ? 15 : 7;
+  static constexpr int kWarps = kEarly ? 11 : 7;
 };
 
 template <class TI, class TO>
@@ -413,7 +413,7 @@ struct FwdOp {
     else h.m = MemView<TI, FromShared>{reinterpret_cast<const TI*>(slot), nv};
   }
   __device__ __forceinline__ Part unit(const Held& h, const URange& q) const {
-    return kEarly ? unit_moments<TI>(h.r, x, q) : unit_moments<TI>(h.m, x, q);
+    return kEarly ? unit_moments<false, TI>(h.r, x, q) : unit_moments<false, TI>(h.m, x, q);
   }
   __device__ __forceinline__ void block_done(int64_t blk, const Part& a) {
     fwd_block_done(p, ws, blk, merge_block(a), eps, mean_out, rstd_out);
@@ -422,8 +422,8 @@ struct FwdOp {
   __device__ __forceinline__ void norm(const Held& h, const URange& q, int64_t row) {
     const int64_t c = channel_of(row, p.C);
     const float gm = gamma ? gamma[c] : 1.f, bt = beta ? beta[c] : 0.f;
-    if (kEarly) fwd_norm<TI, TO>(h.r, x, y, q, st, gm, bt);
-    else fwd_norm<TI, TO>(h.m, x, y, q, st, gm, bt);
+    if (kEarly) fwd_norm<false, TI, TO>(h.r, x, y, q, st, gm, bt);
+    else fwd_norm<false, TI, TO>(h.m, x, y, q, st, gm, bt);
   }
 };
 
@@ -483,7 +483,8 @@ struct BwdOp {
   }
   __device__ __forceinline__ float2 unit(const Held& h, const URange& q) const {
     const float mu = mean[q.row / p.Cg];
-    return kEarly ? unit_bwd_sums<T>(h.rx, h.rd, x, dy, q, mu) : unit_bwd_sums<T>(h.mx, h.md, x, dy, q, mu);
+    return kEarly ? unit_bwd_sums<false, T>(h.rx, h.rd, x, dy, q, mu)
+                  : unit_bwd_sums<false, T>(h.mx, h.md, x, dy, q, mu);
   }
   __device__ __forceinline__ void block_done(int64_t blk, const float2& a) {
     bwd_block_done(p, ws, blk, a, rstd, gamma, dgamma, dbeta);
@@ -495,8 +496,8 @@ struct BwdOp {
   __device__ __forceinline__ void norm(const Held& h, const URange& q, int64_t row) {
     const int64_t c = channel_of(row, p.C);
     const float gm = gamma ? gamma[c] : 1.f;
-    if (kEarly) bwd_norm<T>(h.rx, h.rd, x, dy, dx, q, k, gm);
-    else bwd_norm<T>(h.mx, h.md, x, dy, dx, q, k, gm);
+    if (kEarly) bwd_norm<false, T>(h.rx, h.rd, x, dy, dx, q, k, gm);
+    else bwd_norm<false, T>(h.mx, h.md, x, dy, dx, q, k, gm);
   }
 };
 

@@ -109,6 +109,12 @@ struct WarpRing {
   }
 };
 
+// Unit k of a row: the general range, or its closed form when every unit is full.
+template <bool kFull>
+__device__ __forceinline__ URange urange(const Plan& p, int64_t row, int64_t k) {
+  return kFull ? full_range(p, row, k) : unit_range_rk(p, row, k);
+}
+
 __device__ __forceinline__ void record_timeout(uint32_t* status) {
   if ((threadIdx.x & 31) == 0) atomicExch(status, 4u);  // GN3D_ERR_TIMEOUT
 }
@@ -124,7 +130,7 @@ template <class T> struct BwdRedShape {
   static constexpr int kSlots = sizeof(T) == 2 ? 3 : 2;
 };
 
-template <class TI>
+template <class TI, bool kFull>
 __global__ void __launch_bounds__(32 * FwdStatShape<TI>::kWarps, 1)
     k_fwd_stats(const TI* __restrict__ x, Plan p, FwdWs ws, float eps, float* mean_out, float* rstd_out,
                 unsigned long long spin, uint32_t* status) {
@@ -142,7 +148,7 @@ __global__ void __launch_bounds__(32 * FwdStatShape<TI>::kWarps, 1)
   ld.set(p, first, nblk);
   cu = ld;
   for (int i = 0; i < Shape::kSlots && !ld.end; ++i) {
-    ring.issue(unit_range_rk(p, ld.row, ld.k()), src);
+    ring.issue(urange<kFull>(p, ld.row, ld.k()), src);
     ld.next(p, stride, nblk);
   }
   Part a{0.f, 0.f, 0, 0.f};  // lane l: the partial of unit l of the current block
@@ -152,23 +158,24 @@ __global__ void __launch_bounds__(32 * FwdStatShape<TI>::kWarps, 1)
       record_timeout(status);
       break;
     }
-    const URange q = unit_range_rk(p, cu.row, cu.k());
+    const URange q = urange<kFull>(p, cu.row, cu.k());
     const int nv = (int)((q.b1 - q.b0) / kVec);
     Part m;
     if (kRegs) {
       RegView<TI> v;
-      v.template load<FromShared>(reinterpret_cast<const TI*>(slot), nv);
+      if (kFull) v.template load_full<FromShared>(reinterpret_cast<const TI*>(slot));
+      else v.template load<FromShared>(reinterpret_cast<const TI*>(slot), nv);
       __syncwarp();
       if (!ld.end) {
-        ring.issue(unit_range_rk(p, ld.row, ld.k()), src);
+        ring.issue(urange<kFull>(p, ld.row, ld.k()), src);
         ld.next(p, stride, nblk);
       }
-      m = unit_moments<TI>(v, x, q);
+      m = unit_moments<kFull, TI>(v, x, q);
     } else {
-      m = unit_moments<TI>(MemView<TI, FromShared>{reinterpret_cast<const TI*>(slot), nv}, x, q);
+      m = unit_moments<kFull, TI>(MemView<TI, FromShared>{reinterpret_cast<const TI*>(slot), nv}, x, q);
       __syncwarp();
       if (!ld.end) {
-        ring.issue(unit_range_rk(p, ld.row, ld.k()), src);
+        ring.issue(urange<kFull>(p, ld.row, ld.k()), src);
         ld.next(p, stride, nblk);
       }
     }
@@ -183,7 +190,7 @@ __global__ void __launch_bounds__(32 * FwdStatShape<TI>::kWarps, 1)
   ring.drain(spin);
 }
 
-template <class TI, class TO>
+template <class TI, class TO, bool kFull>
 __global__ void __launch_bounds__(32 * kStreamWarps)
     k_fwd_norm(const TI* __restrict__ x, TO* __restrict__ y, Plan p, const float4* __restrict__ stats,
                const float* __restrict__ gamma, const float* __restrict__ beta) {
@@ -191,14 +198,14 @@ __global__ void __launch_bounds__(32 * kStreamWarps)
   for (int64_t i = warp_global(); i < p.units; i += nw) {
     const int64_t u = p.units - 1 - i;
     const int64_t row = u / p.R;
-    const URange q = unit_range_rk(p, row, u - row * p.R);
+    const URange q = urange<kFull>(p, row, u - row * p.R);
     const int64_t c = channel_of(row, p.C), g = row / p.Cg;
     const MemView<TI, FromGlobal> v{x + q.b0, (int)((q.b1 - q.b0) / kVec)};
-    fwd_norm<TI, TO>(v, x, y, q, __ldcg(stats + g), gamma ? gamma[c] : 1.f, beta ? beta[c] : 0.f);
+    fwd_norm<kFull, TI, TO>(v, x, y, q, __ldcg(stats + g), gamma ? gamma[c] : 1.f, beta ? beta[c] : 0.f);
   }
 }
 
-template <class T>
+template <class T, bool kFull>
 __global__ void __launch_bounds__(32 * BwdRedShape<T>::kWarps, 1)
     k_bwd_reduce(const T* __restrict__ dy, const T* __restrict__ x, Plan p, const float* __restrict__ mean,
                  const float* __restrict__ rstd, const float* __restrict__ gamma, BwdWs ws, float* dgamma,
@@ -216,7 +223,7 @@ __global__ void __launch_bounds__(32 * BwdRedShape<T>::kWarps, 1)
   ld.set(p, first, nblk);
   cu = ld;
   for (int i = 0; i < Shape::kSlots && !ld.end; ++i) {
-    ring.issue(unit_range_rk(p, ld.row, ld.k()), src);
+    ring.issue(urange<kFull>(p, ld.row, ld.k()), src);
     ld.next(p, stride, nblk);
   }
   float2 a = make_float2(0.f, 0.f);  // lane l: the sums of unit l of the current block
@@ -226,15 +233,15 @@ __global__ void __launch_bounds__(32 * BwdRedShape<T>::kWarps, 1)
       record_timeout(status);
       break;
     }
-    const URange q = unit_range_rk(p, cu.row, cu.k());
+    const URange q = urange<kFull>(p, cu.row, cu.k());
     const int nv = (int)((q.b1 - q.b0) / kVec);
     const T* xs = reinterpret_cast<const T*>(slot);
     const T* ds = reinterpret_cast<const T*>(slot + Ring::kTensorBytes);
-    const float2 v = unit_bwd_sums<T>(MemView<T, FromShared>{xs, nv}, MemView<T, FromShared>{ds, nv}, x, dy, q,
+    const float2 v = unit_bwd_sums<kFull, T>(MemView<T, FromShared>{xs, nv}, MemView<T, FromShared>{ds, nv}, x, dy, q,
                                       mean[q.row / p.Cg]);
     __syncwarp();
     if (!ld.end) {
-      ring.issue(unit_range_rk(p, ld.row, ld.k()), src);
+      ring.issue(urange<kFull>(p, ld.row, ld.k()), src);
       ld.next(p, stride, nblk);
     }
     if (lane == cu.ui) a = v;
@@ -247,7 +254,7 @@ __global__ void __launch_bounds__(32 * BwdRedShape<T>::kWarps, 1)
   ring.drain(spin);
 }
 
-template <class T>
+template <class T, bool kFull>
 __global__ void __launch_bounds__(32 * kStreamWarps)
     k_bwd_dx(const T* __restrict__ dy, const T* __restrict__ x, T* __restrict__ dx, Plan p,
              const float* __restrict__ mean, const float* __restrict__ rstd, const float* __restrict__ gamma,
@@ -256,13 +263,13 @@ __global__ void __launch_bounds__(32 * kStreamWarps)
   for (int64_t i = warp_global(); i < p.units; i += nw) {
     const int64_t u = p.units - 1 - i;
     const int64_t row = u / p.R;
-    const URange q = unit_range_rk(p, row, u - row * p.R);
+    const URange q = urange<kFull>(p, row, u - row * p.R);
     const int64_t c = channel_of(row, p.C), g = row / p.Cg;
     const float2 ab = __ldcg(coef + g);
     const DxCoef k{mean[g], rstd[g], ab.x, ab.y, p.M == 1};
     const int nv = (int)((q.b1 - q.b0) / kVec);
-    bwd_norm<T>(MemView<T, FromGlobal>{x + q.b0, nv}, MemView<T, FromGlobal>{dy + q.b0, nv}, x, dy, dx, q, k,
-                gamma ? gamma[c] : 1.f);
+    bwd_norm<kFull, T>(MemView<T, FromGlobal>{x + q.b0, nv}, MemView<T, FromGlobal>{dy + q.b0, nv}, x, dy, dx, q,
+                       k, gamma ? gamma[c] : 1.f);
   }
 }
 

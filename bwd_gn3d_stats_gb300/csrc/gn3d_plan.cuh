@@ -98,6 +98,27 @@ __host__ __device__ inline URange unit_range(const Plan& p, int64_t u) {
   return unit_range_rk(p, row, u - row * p.R);
 }
 
+// A unit whose 4096 elements are all body (no head or tail scalars).
+__host__ __device__ inline bool unit_is_full(const URange& q) {
+  return q.n == kUnitElems && q.b1 - q.b0 == kUnitElems;
+}
+
+// Every unit of the plan is full: rows are whole multiples of kUnitElems, so
+// every row also starts on a vector boundary.
+__host__ __device__ inline bool plan_all_full(const Plan& p) { return p.S > 0 && p.S % kUnitElems == 0; }
+
+// Unit k of row `row` when plan_all_full (the same range unit_range_rk gives).
+__host__ __device__ inline URange full_range(const Plan& p, int64_t row, int64_t k) {
+  URange q;
+  q.row = row;
+  q.b0 = row * p.S + k * (int64_t)kUnitElems;
+  q.b1 = q.b0 + kUnitElems;
+  q.h0 = q.h1 = row * p.S;
+  q.t0 = q.t1 = row * p.S + p.S;
+  q.n = kUnitElems;
+  return q;
+}
+
 // Flat index of scalar number s (0 <= s < head+tail) of a unit: head first, then tail.
 __host__ __device__ inline int64_t scalar_index(const URange& q, int s) {
   const int64_t nh = q.h1 - q.h0;
