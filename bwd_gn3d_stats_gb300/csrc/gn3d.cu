@@ -30,7 +30,7 @@ thread_local std::string g_msg;
 std::atomic<uint64_t> g_launches{0};
 
 // testing / tuning hooks (gn3d_debug_set)
-std::atomic<long long> g_hook_path{0};     // 0 auto (fused), 1 streaming kernels, 2 fused kernels
+std::atomic<long long> g_hook_path{0};     // 0 auto (streaming), 1 streaming kernels, 2 fused kernels
 std::atomic<long long> g_hook_spin{0};     // 0 default poll budget
 std::atomic<long long> g_hook_timeout{0};  // 1: the next fused launch waits on a flag nothing sets
 std::atomic<long long> g_hook_lag{-1};     // -1 auto
@@ -64,6 +64,7 @@ struct DevInfo {
   cudaMemPool_t pool = nullptr;
   uint32_t* status = nullptr;
   std::vector<std::pair<const void*, int>> attr_smem;  // dynamic shared memory raised to, per kernel
+  std::vector<cudaEvent_t> free_events;                // timing events of this device, for reuse
 };
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
@@ -156,35 +157,55 @@ std::atomic<int> g_timing{0};
 std::mutex g_tmu;
 struct TimedLaunch {
   int kind;
+  DevInfo* dev;  // owner of the events
   cudaEvent_t a, b;
 };
 std::vector<TimedLaunch> g_timed;
 double g_kernel_ms[KK_COUNT];
 uint64_t g_kernel_n[KK_COUNT];
 
+// An event of this device: a recycled one, else a new one (timing only).
+cudaEvent_t take_event(DevInfo& di) {
+  {
+    std::lock_guard<std::mutex> lk(g_tmu);
+    if (!di.free_events.empty()) {
+      cudaEvent_t e = di.free_events.back();
+      di.free_events.pop_back();
+      return e;
+    }
+  }
+  cudaEvent_t e = nullptr;
+  return cudaEventCreate(&e) == cudaSuccess ? e : nullptr;
+}
+
 struct LaunchTimer {
   int kind;
   cudaStream_t st;
+  DevInfo& di;
   cudaEvent_t a = nullptr;
-  LaunchTimer(int k, cudaStream_t s) : kind(k), st(s) {
+  LaunchTimer(int k, cudaStream_t s, DevInfo& d) : kind(k), st(s), di(d) {
     if (!g_timing.load()) return;
-    if (cudaEventCreate(&a) != cudaSuccess || cudaEventRecord(a, st) != cudaSuccess) a = nullptr;
+    a = take_event(di);
+    if (a && cudaEventRecord(a, st) != cudaSuccess) {
+      cudaEventDestroy(a);
+      a = nullptr;
+    }
   }
   void done() {
     if (!a) return;
-    cudaEvent_t b = nullptr;
-    if (cudaEventCreate(&b) == cudaSuccess && cudaEventRecord(b, st) == cudaSuccess) {
-      std::lock_guard<std::mutex> lk(g_tmu);
-      g_timed.push_back(TimedLaunch{kind, a, b});
+    cudaEvent_t b = take_event(di);
+    std::lock_guard<std::mutex> lk(g_tmu);
+    if (b && cudaEventRecord(b, st) == cudaSuccess) {
+      g_timed.push_back(TimedLaunch{kind, &di, a, b});
     } else {
-      cudaEventDestroy(a);
-      if (b) cudaEventDestroy(b);
+      di.free_events.push_back(a);
+      if (b) di.free_events.push_back(b);
     }
     a = nullptr;
   }
 };
 
-bool use_fused() { return g_hook_path.load() != 1; }
+bool use_fused() { return g_hook_path.load() == 2; }
 
 unsigned long long spin_budget() {
   const long long s = g_hook_spin.load();
@@ -282,7 +303,7 @@ int launch_forward(const void* x, const float* gamma, const float* beta, const P
     void* args[] = {(void*)&xp, (void*)&yp, (void*)&p, (void*)&w, (void*)&cfg, (void*)&fs, (void*)&eps,
                     (void*)&gamma, (void*)&beta, (void*)&mean, (void*)&rstd};
     g_launches += 1;
-    LaunchTimer tm(KK_FWD_FUSED, st);
+    LaunchTimer tm(KK_FWD_FUSED, st, di);
     e = cudaLaunchCooperativeKernel((const void*)k, dim3(grid), dim3(threads), args, (size_t)smem, st);
     tm.done();
   } else if (e == cudaSuccess) {
@@ -292,17 +313,18 @@ int launch_forward(const void* x, const float* gamma, const float* beta, const P
     auto ks = full ? k_fwd_stats<TI, true> : k_fwd_stats<TI, false>;
     int rc = raise_smem((const void*)ks, smem, di);
     if (rc) { cudaFreeAsync(s.base, st); return rc; }
-    const int sgrid = grid_for(di, (nblk + Shape::kWarps - 1) / Shape::kWarps, 1);
-    const int64_t warps_needed = (p.units + kStreamWarps - 1) / kStreamWarps;
+    // one CTA per SM (fewer only when there are fewer blocks than SMs): warp w of
+    // CTA c owns blocks w*grid + c, ..., so every SM takes a share
+    const int sgrid = grid_for(di, nblk, 1);
     g_launches += 2;
-    LaunchTimer t1(KK_FWD_STATS, st);
+    LaunchTimer t1(KK_FWD_STATS, st, di);
     ks<<<sgrid, 32 * Shape::kWarps, smem, st>>>(xp, p, w, eps, mean, rstd, spin_budget(), di.status);
     t1.done();
     e = cudaGetLastError();
     if (e == cudaSuccess) {
-      LaunchTimer t2(KK_FWD_NORM, st);
+      LaunchTimer t2(KK_FWD_NORM, st, di);
       auto kn = full ? k_fwd_norm<TI, TO, true> : k_fwd_norm<TI, TO, false>;
-      kn<<<grid_for(di, warps_needed, 8), 32 * kStreamWarps, 0, st>>>(xp, yp, p, w.stats, gamma, beta);
+      kn<<<sgrid, 32 * kElemWarps, 0, st>>>(xp, yp, p, w.stats, gamma, beta);
       t2.done();
       e = cudaGetLastError();
     }
@@ -355,28 +377,27 @@ int launch_backward(const void* dy, const void* x, const float* mean, const floa
     void* args[] = {(void*)&dyp, (void*)&xp, (void*)&dxp, (void*)&p, (void*)&mean, (void*)&rstd, (void*)&gamma,
                     (void*)&w, (void*)&cfg, (void*)&fs, (void*)&dgamma, (void*)&dbeta};
     g_launches += 1;
-    LaunchTimer tm(KK_BWD_FUSED, st);
+    LaunchTimer tm(KK_BWD_FUSED, st, di);
     e = cudaLaunchCooperativeKernel((const void*)k, dim3(grid), dim3(threads), args, (size_t)smem, st);
     tm.done();
   } else if (e == cudaSuccess) {
     using Shape = BwdRedShape<T>;
-    const int smem = Shape::kWarps * WarpRing<T, 2, Shape::kSlots>::kWarpBytes;
+    const int smem = Shape::kWarps * WarpRing<T, 2, Shape::kSlots, Shape::kElems>::kWarpBytes;
     const bool full = plan_all_full(p);
     auto kr = full ? k_bwd_reduce<T, true> : k_bwd_reduce<T, false>;
     int rc = raise_smem((const void*)kr, smem, di);
     if (rc) { cudaFreeAsync(s.base, st); return rc; }
-    const int rgrid = grid_for(di, (nblk + Shape::kWarps - 1) / Shape::kWarps, 1);
-    const int64_t warps_needed = (p.units + kStreamWarps - 1) / kStreamWarps;
+    const int rgrid = grid_for(di, nblk, 1);
     g_launches += 2;
-    LaunchTimer t1(KK_BWD_REDUCE, st);
+    LaunchTimer t1(KK_BWD_REDUCE, st, di);
     kr<<<rgrid, 32 * Shape::kWarps, smem, st>>>(dyp, xp, p, mean, rstd, gamma, w, dgamma, dbeta, spin_budget(),
                                                di.status);
     t1.done();
     e = cudaGetLastError();
     if (e == cudaSuccess) {
-      LaunchTimer t2(KK_BWD_DX, st);
+      LaunchTimer t2(KK_BWD_DX, st, di);
       auto kd = full ? k_bwd_dx<T, true> : k_bwd_dx<T, false>;
-      kd<<<grid_for(di, warps_needed, 8), 32 * kStreamWarps, 0, st>>>(dyp, xp, dxp, p, mean, rstd, gamma, w.coef);
+      kd<<<rgrid, 32 * kElemWarps, 0, st>>>(dyp, xp, dxp, p, mean, rstd, gamma, w.coef);
       t2.done();
       e = cudaGetLastError();
     }
@@ -652,8 +673,8 @@ extern "C" int gn3d_debug_set(int what, long long value) {
       std::lock_guard<std::mutex> lk(g_tmu);
       if (value) {
         for (TimedLaunch& t : g_timed) {
-          cudaEventDestroy(t.a);
-          cudaEventDestroy(t.b);
+          t.dev->free_events.push_back(t.a);
+          t.dev->free_events.push_back(t.b);
         }
         g_timed.clear();
         for (int k = 0; k < KK_COUNT; ++k) {
@@ -701,8 +722,8 @@ extern "C" int gn3d_kernel_time(const char* name, double* ms, uint64_t* launches
     } else if (err == cudaSuccess) {
       err = r;
     }
-    cudaEventDestroy(t.a);
-    cudaEventDestroy(t.b);
+    t.dev->free_events.push_back(t.a);
+    t.dev->free_events.push_back(t.b);
   }
   g_timed.clear();
   if (err != cudaSuccess) return cuda_fail(err, "kernel timing events");

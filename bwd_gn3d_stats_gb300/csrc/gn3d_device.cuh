@@ -560,17 +560,16 @@ struct BwdWs {
   uint32_t* done;   // [1] groups finalized
 };
 
-// S1 = sum dy, S2 = sum dy*(x - mean) of one unit, by one warp.
+// S1 = sum dy, S2 = sum dy*(x - mean) of one unit, by one warp, in two steps:
+// bwd_accum adds the lane's vectors i0 <= i < i1 to its running sums (a unit's
+// body may arrive in parts), bwd_finish meets the sums in the fixed tree, adds
+// the lane's scalar and sums the lanes.
 template <bool kFull, class T, class View>
-__device__ __forceinline__ float2 unit_bwd_sums(const View& ux, const View& ud, const T* __restrict__ x,
-                                                const T* __restrict__ dy, const URange& q, float mu) {
-  const int lane = threadIdx.x & 31;
-  const f2 z2 = f2_splat(0.f);
-  f2 a1[4] = {z2, z2, z2, z2};
-  f2 a2[4] = {z2, z2, z2, z2};
+__device__ __forceinline__ void bwd_accum(const View& ux, const View& ud, int i0, int i1, float mu, f2 a1[4],
+                                          f2 a2[4]) {
 #pragma unroll
   for (int i = 0; i < kVecPerLane; ++i) {
-    if (kFull || ux.has(i)) {
+    if (i >= i0 && i < i1 && (kFull || ux.has(i))) {
       f2 xm[4], vd[4];
       ux.diff(i, mu, xm);
       ud.get(i, vd);
@@ -581,6 +580,12 @@ __device__ __forceinline__ float2 unit_bwd_sums(const View& ux, const View& ud, 
       }
     }
   }
+}
+
+template <bool kFull, class T>
+__device__ __forceinline__ float2 bwd_finish(const f2 a1[4], const f2 a2[4], const T* __restrict__ x,
+                                             const T* __restrict__ dy, const URange& q, float mu) {
+  const int lane = threadIdx.x & 31;
   float s1 = tree8p(a1), s2 = tree8p(a2);
   if (!kFull && lane < scalar_count(q)) {
     const int64_t idx = scalar_index(q, lane);
@@ -589,6 +594,16 @@ __device__ __forceinline__ float2 unit_bwd_sums(const View& ux, const View& ud, 
     s2 = ffma(d, fsub(IO<T>::load1(x + idx), mu), s2);
   }
   return warp_sum2(s1, s2);
+}
+
+template <bool kFull, class T, class View>
+__device__ __forceinline__ float2 unit_bwd_sums(const View& ux, const View& ud, const T* __restrict__ x,
+                                                const T* __restrict__ dy, const URange& q, float mu) {
+  const f2 z2 = f2_splat(0.f);
+  f2 a1[4] = {z2, z2, z2, z2};
+  f2 a2[4] = {z2, z2, z2, z2};
+  bwd_accum<kFull, T>(ux, ud, 0, kVecPerLane, mu, a1, a2);
+  return bwd_finish<kFull, T>(a1, a2, x, dy, q, mu);
 }
 
 // Group finalize of the backward, by one warp: per-row totals of the block sums

@@ -89,8 +89,9 @@ int gn3d_forward(const void* x, const float* gamma, const float* beta, int64_t N
  * inside another allocator's critical section, where cudaMalloc (which may
  * synchronize the device) or a stream-ordered pool allocation is not allowed.
  *
- * Same arguments, results and errors as gn3d_forward, computed by the same
- * kernel, except:
+ * Same arguments, results and errors as gn3d_forward (computed by the
+ * persistent forward kernel, whose results are bit-identical to the streaming
+ * kernels'), except:
  *   - Scratch comes from a static area of 8 MiB inside the library's device
  *     code, which every GPU that loads the library holds until the process
  *     exits.  The scratch is about 17 bytes per 4096 elements of each (n, c)
@@ -142,8 +143,9 @@ uint64_t gn3d_launch_count(void);
  * Testing and tuning hooks (process-wide, not thread-scoped; not needed for
  * normal use -- every setting defaults to automatic).  None of them changes a
  * result bit: both launch forms run the same units and reduction trees.
- *   GN3D_DEBUG_PATH          0 automatic (persistent kernels), 1 streaming
- *                            kernels (two launches per direction), 2 persistent.
+ *   GN3D_DEBUG_PATH          0 automatic (the streaming kernels: two launches
+ *                            per direction), 1 streaming, 2 persistent (one
+ *                            cooperative launch per direction).
  *   GN3D_DEBUG_SPIN_LIMIT    poll budget of every bounded device-side wait
  *                            (0 = default, about four seconds).
  *   GN3D_DEBUG_FORCE_TIMEOUT 1: the next persistent launch waits for a flag that

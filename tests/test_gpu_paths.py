@@ -42,6 +42,10 @@ SHAPES = [
     (2, 6, 1, 1, 1, 6, synth.F32),
     (1, 16, 24, 24, 24, 2, synth.F32),
     (1, 512, 8, 8, 8, 8, synth.BF16),
+    # rows of whole 4096-element units: the streaming kernels' full-unit variants
+    # against the persistent kernels' general path
+    (1, 16, 16, 16, 32, 4, synth.BF16),
+    (2, 8, 16, 16, 16, 2, synth.F32),
 ]
 
 
@@ -60,6 +64,7 @@ def test_fused_and_streaming_bit_identical(shape):
 def test_tuning_does_not_move_a_bit(knob, values):
     site = synth.Site(1, 32, 36, 36, 36, 8, synth.BF16)
     d = device_inputs(synth.make_inputs(site, seed=12))
+    gn.gn3d_debug_set(gn.DEBUG_PATH, gn.PATH_FUSED)  # lag and slots shape the persistent kernels
     ref = run_all(site, d)
     for v in values:
         gn.gn3d_debug_set(knob, v)
@@ -71,6 +76,7 @@ def test_bounded_wait_timeout_reports_and_recovers():
     d = device_inputs(synth.make_inputs(site, seed=13))
     ref = run_all(site, d)
     st = torch().cuda.current_stream().cuda_stream
+    gn.gn3d_debug_set(gn.DEBUG_PATH, gn.PATH_FUSED)  # the forced wait is in the persistent kernels
     gn.gn3d_debug_set(gn.DEBUG_SPIN_LIMIT, 20000)
     gn.gn3d_debug_set(gn.DEBUG_FORCE_TIMEOUT, 1)
     run_forward(site, d["x"], d["gamma"], d["beta"])
@@ -81,9 +87,11 @@ def test_bounded_wait_timeout_reports_and_recovers():
     assert same(ref, run_all(site, d))
 
 
-def test_launch_count_one_kernel_per_direction():
+@pytest.mark.parametrize("path,launches", [(gn.PATH_AUTO, 4), (gn.PATH_STREAMING, 4), (gn.PATH_FUSED, 2)])
+def test_launch_count(path, launches):
     site = synth.Site(1, 8, 16, 16, 16, 4, synth.BF16)
     d = device_inputs(synth.make_inputs(site, seed=14))
+    gn.gn3d_debug_set(gn.DEBUG_PATH, path)
     n0 = gn.gn3d_launch_count()
     run_all(site, d)
-    assert gn.gn3d_launch_count() - n0 == 2
+    assert gn.gn3d_launch_count() - n0 == launches
