@@ -252,6 +252,24 @@ int raise_smem(const void* func, int bytes, DevInfo& di) {
   return GN3D_OK;
 }
 
+// Launch of a kernel that may start before the previous kernel on the stream
+// has finished (programmatic dependent launch); it waits in-kernel (pdl_wait)
+// before reading that kernel's results.
+template <class... KArgs, class... Args>
+cudaError_t launch_dependent(void (*k)(KArgs...), int grid, int threads, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, args...);
+}
+
 // Grid of a persistent launch: one CTA per SM, all resident at once.
 int coop_grid(const void* func, int threads, int smem, const DevInfo& di, int* grid) {
   int per_sm = 0;
@@ -324,9 +342,8 @@ int launch_forward(const void* x, const float* gamma, const float* beta, const P
     if (e == cudaSuccess) {
       LaunchTimer t2(KK_FWD_NORM, st, di);
       auto kn = full ? k_fwd_norm<TI, TO, true> : k_fwd_norm<TI, TO, false>;
-      kn<<<sgrid, 32 * kElemWarps, 0, st>>>(xp, yp, p, w.stats, gamma, beta);
+      e = launch_dependent(kn, sgrid, 32 * kElemWarps, st, xp, yp, p, (const float4*)w.stats, gamma, beta);
       t2.done();
-      e = cudaGetLastError();
     }
   }
   cudaError_t ef = cudaFreeAsync(s.base, st);
@@ -397,9 +414,9 @@ int launch_backward(const void* dy, const void* x, const float* mean, const floa
     if (e == cudaSuccess) {
       LaunchTimer t2(KK_BWD_DX, st, di);
       auto kd = full ? k_bwd_dx<T, true> : k_bwd_dx<T, false>;
-      kd<<<rgrid, 32 * kElemWarps, 0, st>>>(dyp, xp, dxp, p, mean, rstd, gamma, w.coef);
+      e = launch_dependent(kd, rgrid, 32 * kElemWarps, st, dyp, xp, dxp, p, mean, rstd, gamma,
+                           (const float2*)w.coef);
       t2.done();
-      e = cudaGetLastError();
     }
   }
   cudaError_t ef = cudaFreeAsync(s.base, st);

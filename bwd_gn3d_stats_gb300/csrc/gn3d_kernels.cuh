@@ -155,6 +155,7 @@ __global__ void __launch_bounds__(32 * FwdStatShape<TI>::kWarps, 1)
   using Ring = WarpRing<TI, 1, Shape::kSlots>;
   constexpr bool kRegs = Vec<TI>::kRaw == 1;  // bf16: the unit goes to registers, the slot is refilled at once
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_launch_dependents();  // the normalize kernel may take SMs as this one leaves them
   Ring ring;
   ring.init(smem + (size_t)warp * Ring::kWarpBytes);
   const int64_t nblk = p.NC * p.nb, stride = (int64_t)gridDim.x * Shape::kWarps;
@@ -234,9 +235,27 @@ __global__ void __launch_bounds__(32 * kElemWarps, 1)
     k_fwd_norm(const TI* __restrict__ x, TO* __restrict__ y, Plan p, const float4* __restrict__ stats,
                const float* __restrict__ gamma, const float* __restrict__ beta) {
   using Own = OwnedBlocks<FwdStatShape<TI>::kWarps>;
+  constexpr bool kRegs = Vec<TI>::kRaw == 1;  // bf16: all 16 loads in flight before any use
   const Own own;
   const int64_t nblk = p.NC * p.nb;
-  for (int64_t b = own.last(nblk); b >= own.b0; b -= own.stride) {
+  // The warp's first unit is read before the statistics kernel has finished
+  // (x is not written there); everything the statistics kernel writes is read
+  // after pdl_wait.
+  RegView<TI> v;
+  bool pre = false;
+  const int64_t b_first = own.last(nblk);
+  if (kRegs && b_first >= own.b0) {
+    const int64_t row = b_first / p.nb, kb = b_first - row * p.nb;
+    const int ui = block_size(p, kb) - 1 - own.share;
+    if (ui >= 0) {
+      const URange q = urange<kFull>(p, row, kb * kBlockUnits + ui);
+      if (kFull) v.template load_full<FromGlobal>(x + q.b0);
+      else v.template load<FromGlobal>(x + q.b0, (int)((q.b1 - q.b0) / kVec));
+      pre = true;
+    }
+  }
+  pdl_wait();
+  for (int64_t b = b_first; b >= own.b0; b -= own.stride) {
     const int64_t row = b / p.nb, kb = b - row * p.nb;
     const int bsz = block_size(p, kb);
     const int64_t c = channel_of(row, p.C), g = row / p.Cg;
@@ -245,10 +264,12 @@ __global__ void __launch_bounds__(32 * kElemWarps, 1)
     for (int ui = bsz - 1 - own.share; ui >= 0; ui -= Own::kSplit) {
       const URange q = urange<kFull>(p, row, kb * kBlockUnits + ui);
       const int nv = (int)((q.b1 - q.b0) / kVec);
-      if (Vec<TI>::kRaw == 1) {  // bf16: all 16 loads in flight before any use
-        RegView<TI> v;
-        if (kFull) v.template load_full<FromGlobal>(x + q.b0);
-        else v.template load<FromGlobal>(x + q.b0, nv);
+      if (kRegs) {
+        if (!pre) {
+          if (kFull) v.template load_full<FromGlobal>(x + q.b0);
+          else v.template load<FromGlobal>(x + q.b0, nv);
+        }
+        pre = false;
         fwd_norm<kFull, TI, TO>(v, x, y, q, st, gm, bt);
       } else {
         fwd_norm<kFull, TI, TO>(MemView<TI, FromGlobal>{x + q.b0, nv}, x, y, q, st, gm, bt);
@@ -267,6 +288,7 @@ __global__ void __launch_bounds__(32 * BwdRedShape<T>::kWarps, 1)
   using Ring = WarpRing<T, 2, Shape::kSlots, Shape::kElems>;
   constexpr int kParts = Ring::kParts, kPartVecs = kVecPerLane / kParts;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_launch_dependents();  // the dx kernel may take SMs as this one leaves them
   Ring ring;
   ring.init(smem + (size_t)warp * Ring::kWarpBytes);
   const int64_t nblk = p.NC * p.nb, stride = (int64_t)gridDim.x * Shape::kWarps;
@@ -329,6 +351,7 @@ __global__ void __launch_bounds__(32 * kElemWarps, 1)
   using Own = OwnedBlocks<BwdRedShape<T>::kWarps>;
   const Own own;
   const int64_t nblk = p.NC * p.nb;
+  pdl_wait();  // the reduction kernel's coefficients
   for (int64_t b = own.last(nblk); b >= own.b0; b -= own.stride) {
     const int64_t row = b / p.nb, kb = b - row * p.nb;
     const int bsz = block_size(p, kb);
