@@ -61,9 +61,16 @@ def _load():
                                                  dp, dp, dp]
             lib.gn3d_oracle_backward_at.argtypes = [vp, vp, ctypes.c_int, dp, dp, fp, i64, i64, i64, i64,
                                                     vp, i64, dp, dp, dp]
+            lib.gn3d_oracle_backward_relu.argtypes = [vp, vp, vp, ctypes.c_int, dp, dp, fp, i64, i64, i64, i64,
+                                                      dp, dp, dp]
+            lib.gn3d_oracle_backward_relu_at.argtypes = [vp, vp, vp, ctypes.c_int, dp, dp, fp, i64, i64, i64,
+                                                         i64, vp, i64, dp, dp, dp]
+            lib.gn3d_oracle_relu.argtypes = [dp, i64, dp]
+            lib.gn3d_oracle_relu.restype = None
             lib.gn3d_oracle_round_bf16.argtypes = [dp, i64, vp]
             lib.gn3d_oracle_round_f32.argtypes = [dp, i64, fp]
-            for f in ("stats", "forward", "forward_at", "backward", "backward_at"):
+            for f in ("stats", "forward", "forward_at", "backward", "backward_at", "backward_relu",
+                      "backward_relu_at"):
                 getattr(lib, "gn3d_oracle_" + f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -148,6 +155,49 @@ def backward_at(dy, x, mean, rstd, gamma, N, C, S, G, idx):
     _check(_load().gn3d_oracle_backward_at(_ptr(dyr), _ptr(xr), dt, _ptr(mean), _ptr(rstd), _ptr(g),
                                            N, C, S, G, _ptr(idx), idx.size, _ptr(dx), _ptr(dgamma),
                                            _ptr(dbeta)))
+    return dx, dgamma, dbeta
+
+
+def relu(v):
+    """F.relu on output values already rounded to the output type (as fp64):
+    out = (v < 0) ? +0 : v -- the fused ReLU's forward, applied after the rounding."""
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    out = np.empty(v.shape)
+    _load().gn3d_oracle_relu(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+def backward_relu(dy, x, out, mean, rstd, gamma, N, C, S, G, want_dx=True):
+    """Backward of relu(GroupNorm(x)) at given statistics; `out` is the forward's
+    result in x's dtype (float32, or uint16 bf16 bits)."""
+    xr, dt = _raw(x)
+    dyr, dt2 = _raw(dy)
+    outr, dt3 = _raw(out)
+    if not dt == dt2 == dt3:
+        raise TypeError("dy, x and out must share a dtype")
+    g = _params(gamma)
+    mean = np.ascontiguousarray(mean, dtype=np.float64)
+    rstd = np.ascontiguousarray(rstd, dtype=np.float64)
+    dx = np.empty(N * C * S) if want_dx else None
+    dgamma, dbeta = np.empty(C), np.empty(C)
+    _check(_load().gn3d_oracle_backward_relu(_ptr(dyr), _ptr(xr), _ptr(outr), dt, _ptr(mean), _ptr(rstd),
+                                             _ptr(g), N, C, S, G, _ptr(dx), _ptr(dgamma), _ptr(dbeta)))
+    return dx, dgamma, dbeta
+
+
+def backward_relu_at(dy, x, out, mean, rstd, gamma, N, C, S, G, idx):
+    xr, dt = _raw(x)
+    dyr, _ = _raw(dy)
+    outr, _ = _raw(out)
+    g = _params(gamma)
+    idx = np.ascontiguousarray(idx, dtype=np.int64)
+    mean = np.ascontiguousarray(mean, dtype=np.float64)
+    rstd = np.ascontiguousarray(rstd, dtype=np.float64)
+    dx = np.empty(idx.size)
+    dgamma, dbeta = np.empty(C), np.empty(C)
+    _check(_load().gn3d_oracle_backward_relu_at(_ptr(dyr), _ptr(xr), _ptr(outr), dt, _ptr(mean), _ptr(rstd),
+                                                _ptr(g), N, C, S, G, _ptr(idx), idx.size, _ptr(dx),
+                                                _ptr(dgamma), _ptr(dbeta)))
     return dx, dgamma, dbeta
 
 

@@ -26,6 +26,14 @@
  *   dx = rstd * (g - a - xhat * b)
  *   dgamma_c = sum_{n, spatial} dy * xhat,   dbeta_c = sum_{n, spatial} dy
  *
+ * The fused ReLU (the ScaFFold GroupNorm pages: FastGroupNorm's activation
+ * argument, and the fix that makes it bit-identical to unfused GroupNorm then
+ * F.relu on NaN, both infinities and -0.0) is, forward, F.relu of the rounded
+ * output: out = (v < 0) ? +0 : v on v = y rounded to the output type -- NaN,
+ * +Inf and -0.0 pass, -Inf and negatives become +0 -- and, backward, torch's
+ * threshold_backward on the forward's result: the gradient reaching GroupNorm
+ * is dy where the result is not <= 0 (a NaN result passes it) and 0 elsewhere.
+ *
  * Every sum is a Neumaier-compensated fp64 sum (Neumaier 1974), so results are
  * the exact values to well below the GPU's fp32 error.  Inputs arrive as the
  * raw bytes the GPU sees (fp32 or bf16), widened exactly to fp64 here.  eps is
@@ -165,8 +173,17 @@ int gn3d_oracle_forward_at(const void* x, int dtype, const float* gamma, const f
 
 /* Group sums a = mean(g), b = mean(g*xhat) per (n,g), and per-(n,c) partial
  * dgamma/dbeta sums, all at the given statistics. */
-static void bwd_sums(const void* dy, const void* x, int dtype, const double* mean, const double* rstd,
-                     const float* gamma, int64_t N, int64_t C, int64_t S, int64_t G,
+/* The gradient arriving at GroupNorm at element i: dy, or -- behind the fused
+ * ReLU -- 0 where the forward's result `gate` is <= 0 (NaN compares false, so
+ * a NaN result passes the gradient). */
+static double grad_in(const void* dy, const void* gate, int dtype, int64_t i) {
+  const double d = widen(dy, dtype, i);
+  if (gate && widen(gate, dtype, i) <= 0.0) return 0.0;
+  return d;
+}
+
+static void bwd_sums(const void* dy, const void* gate, const void* x, int dtype, const double* mean,
+                     const double* rstd, const float* gamma, int64_t N, int64_t C, int64_t S, int64_t G,
                      double* a, double* b, double* dg_nc, double* db_nc) {
   const int64_t Cg = C / G, M = Cg * S;
 #pragma omp parallel for schedule(dynamic, 1)
@@ -179,7 +196,7 @@ static void bwd_sums(const void* dy, const void* x, int dtype, const double* mea
       nsum sdy = {0, 0}, sdyx = {0, 0};
       for (int64_t s = 0; s < S; ++s) {
         const int64_t i = nc * S + s;
-        const double d = widen(dy, dtype, i);
+        const double d = grad_in(dy, gate, dtype, i);
         const double xh = (widen(x, dtype, i) - mean[ng]) * rstd[ng];
         nsum_add(&sg, d * gam);
         nsum_add(&sgx, d * gam * xh);
@@ -212,9 +229,7 @@ static void reduce_params(const double* dg_nc, const double* db_nc, int64_t N, i
   }
 }
 
-/* Backward at given statistics (fp64 [N*G]).  dx: [N*C*S] fp64 or NULL;
- * dgamma/dbeta: [C] fp64 or NULL. */
-int gn3d_oracle_backward(const void* dy, const void* x, int dtype, const double* mean,
+static int backward_impl(const void* dy, const void* gate, const void* x, int dtype, const double* mean,
                          const double* rstd, const float* gamma, int64_t N, int64_t C, int64_t S,
                          int64_t G, double* dx, double* dgamma, double* dbeta) {
   if (check_shape(N, C, S, G)) return ORC_EINVAL;
@@ -224,7 +239,7 @@ int gn3d_oracle_backward(const void* dy, const void* x, int dtype, const double*
   double* dg = (double*)malloc(sizeof(double) * (size_t)(NC + 1));
   double* db = (double*)malloc(sizeof(double) * (size_t)(NC + 1));
   if (!a || !b || !dg || !db) { free(a); free(b); free(dg); free(db); return ORC_EINVAL; }
-  bwd_sums(dy, x, dtype, mean, rstd, gamma, N, C, S, G, a, b, dg, db);
+  bwd_sums(dy, gate, x, dtype, mean, rstd, gamma, N, C, S, G, a, b, dg, db);
   if (dx) {
 #pragma omp parallel for schedule(static)
     for (int64_t nc = 0; nc < NC; ++nc) {
@@ -232,7 +247,7 @@ int gn3d_oracle_backward(const void* dy, const void* x, int dtype, const double*
       const double gam = param(gamma, c, 1.0);
       for (int64_t s = 0; s < S; ++s) {
         const int64_t i = nc * S + s;
-        dx[i] = dx_of(widen(dy, dtype, i), widen(x, dtype, i), mean[ng], rstd[ng], gam, a[ng], b[ng]);
+        dx[i] = dx_of(grad_in(dy, gate, dtype, i), widen(x, dtype, i), mean[ng], rstd[ng], gam, a[ng], b[ng]);
       }
     }
   }
@@ -241,8 +256,23 @@ int gn3d_oracle_backward(const void* dy, const void* x, int dtype, const double*
   return ORC_OK;
 }
 
-/* Backward: dx at k flat indices only, dgamma/dbeta in full. */
-int gn3d_oracle_backward_at(const void* dy, const void* x, int dtype, const double* mean,
+/* Backward at given statistics (fp64 [N*G]).  dx: [N*C*S] fp64 or NULL;
+ * dgamma/dbeta: [C] fp64 or NULL. */
+int gn3d_oracle_backward(const void* dy, const void* x, int dtype, const double* mean,
+                         const double* rstd, const float* gamma, int64_t N, int64_t C, int64_t S,
+                         int64_t G, double* dx, double* dgamma, double* dbeta) {
+  return backward_impl(dy, NULL, x, dtype, mean, rstd, gamma, N, C, S, G, dx, dgamma, dbeta);
+}
+
+/* Backward of relu(GroupNorm(x)): `out` is the forward's result (x's dtype). */
+int gn3d_oracle_backward_relu(const void* dy, const void* x, const void* out, int dtype, const double* mean,
+                              const double* rstd, const float* gamma, int64_t N, int64_t C, int64_t S,
+                              int64_t G, double* dx, double* dgamma, double* dbeta) {
+  if (!out) return ORC_EINVAL;
+  return backward_impl(dy, out, x, dtype, mean, rstd, gamma, N, C, S, G, dx, dgamma, dbeta);
+}
+
+static int backward_at_impl(const void* dy, const void* gate, const void* x, int dtype, const double* mean,
                             const double* rstd, const float* gamma, int64_t N, int64_t C,
                             int64_t S, int64_t G, const int64_t* idx, int64_t k, double* dx,
                             double* dgamma, double* dbeta) {
@@ -253,18 +283,42 @@ int gn3d_oracle_backward_at(const void* dy, const void* x, int dtype, const doub
   double* dg = (double*)malloc(sizeof(double) * (size_t)(NC + 1));
   double* db = (double*)malloc(sizeof(double) * (size_t)(NC + 1));
   if (!a || !b || !dg || !db) { free(a); free(b); free(dg); free(db); return ORC_EINVAL; }
-  bwd_sums(dy, x, dtype, mean, rstd, gamma, N, C, S, G, a, b, dg, db);
+  bwd_sums(dy, gate, x, dtype, mean, rstd, gamma, N, C, S, G, a, b, dg, db);
   int st = ORC_OK;
   for (int64_t j = 0; j < k; ++j) {
     const int64_t i = idx[j];
     if (i < 0 || i >= L) { st = ORC_EINVAL; break; }
     const int64_t nc = i / S, n = nc / C, c = nc % C, ng = n * G + c / Cg;
-    dx[j] = dx_of(widen(dy, dtype, i), widen(x, dtype, i), mean[ng], rstd[ng],
+    dx[j] = dx_of(grad_in(dy, gate, dtype, i), widen(x, dtype, i), mean[ng], rstd[ng],
                   param(gamma, c, 1.0), a[ng], b[ng]);
   }
   reduce_params(dg, db, N, C, dgamma, dbeta);
   free(a); free(b); free(dg); free(db);
   return st;
+}
+
+/* Backward: dx at k flat indices only, dgamma/dbeta in full. */
+int gn3d_oracle_backward_at(const void* dy, const void* x, int dtype, const double* mean,
+                            const double* rstd, const float* gamma, int64_t N, int64_t C,
+                            int64_t S, int64_t G, const int64_t* idx, int64_t k, double* dx,
+                            double* dgamma, double* dbeta) {
+  return backward_at_impl(dy, NULL, x, dtype, mean, rstd, gamma, N, C, S, G, idx, k, dx, dgamma, dbeta);
+}
+
+int gn3d_oracle_backward_relu_at(const void* dy, const void* x, const void* out, int dtype, const double* mean,
+                                 const double* rstd, const float* gamma, int64_t N, int64_t C, int64_t S,
+                                 int64_t G, const int64_t* idx, int64_t k, double* dx, double* dgamma,
+                                 double* dbeta) {
+  if (!out) return ORC_EINVAL;
+  return backward_at_impl(dy, out, x, dtype, mean, rstd, gamma, N, C, S, G, idx, k, dx, dgamma, dbeta);
+}
+
+/* ------------------------------------------------------------- fused ReLU */
+
+/* F.relu on values already rounded to the output type (widened to fp64):
+ * out = (v < 0) ? +0 : v (NaN, +Inf and -0.0 pass; -Inf and negatives become +0). */
+void gn3d_oracle_relu(const double* v, int64_t n, double* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = (v[i] < 0.0) ? 0.0 : v[i];
 }
 
 /* -------------------------------------------------------- output rounding */

@@ -327,3 +327,86 @@ def test_round_bf16_agrees_with_torch_on_fp32_values(orc):
 def test_round_f32(orc):
     v = np.array([1.0 + 2 ** -24, 1.0 + 3 * 2 ** -24, 0.1])
     assert np.array_equal(orc.round_f32(v), np.array([1.0, 1.0 + 2 ** -22, 0.1], dtype=np.float32))
+
+
+# ------------------------------------------------------------ fused ReLU
+
+def _vals(strs):
+    return np.array([float(s) for s in strs])
+
+
+def test_relu_special_values_are_the_pages(orc):
+    f = GOLD["fused_relu_forward_special_values"]
+    out, want = orc.relu(_vals(f["in"])), _vals(f["out"])
+    assert np.array_equal(np.isnan(out), np.isnan(want))
+    ok = ~np.isnan(want)
+    assert np.array_equal(out[ok], want[ok])
+    assert np.array_equal(np.signbit(out[ok]), np.signbit(want[ok]))  # -0.0 stays -0.0, -inf -> +0
+
+
+def test_relu_matches_torch_relu_bitwise(orc):
+    rng = np.random.default_rng(30)
+    v = np.concatenate([_vals(["nan", "inf", "-inf", "-0.0", "0.0", "5e-324", "-5e-324"]),
+                        rng.standard_normal(1000), -np.abs(rng.standard_normal(100)) * 1e-30])
+    want = torch.relu(torch.from_numpy(v)).numpy()
+    assert np.array_equal(orc.relu(v).view(np.uint64), want.view(np.uint64))
+
+
+def test_backward_relu_gate_is_the_pages(orc):
+    f = GOLD["fused_relu_backward_gate"]
+    N, C, S, G = 1, 2, 3, 1
+    rng = np.random.default_rng(31)
+    x = rng.standard_normal(N * C * S).astype(np.float32)
+    gamma = np.array([1.25, 0.75], dtype=np.float32)
+    dy = rng.standard_normal(N * C * S).astype(np.float32)
+    out = _vals(f["result"]).astype(np.float32)
+    _, mean, rstd = orc.forward(x, gamma, None, N, C, S, G, 1e-5)
+    got = orc.backward_relu(dy, x, out, mean, rstd, gamma, N, C, S, G)
+    gated = np.where(np.array(f["passes"]), dy, np.float32(0)).astype(np.float32)
+    want = orc.backward(gated, x, mean, rstd, gamma, N, C, S, G)
+    for a, b in zip(got, want):
+        assert np.array_equal(a, b)
+
+
+def test_backward_relu_matches_torch_autograd(orc):
+    site = synth.Site(2, 12, 3, 4, 5, 3, synth.F32)
+    inp = synth.make_inputs(site, seed=32)
+    N, C, S, G = site.N, site.C, site.S, site.G
+    y64, mean, rstd = orc.forward(inp["x"], inp["gamma"], inp["beta"], N, C, S, G, site.eps)
+    out = orc.relu(orc.round_f32(y64).astype(np.float64)).astype(np.float32)
+    dx, dgamma, dbeta = orc.backward_relu(inp["dy"], inp["x"], out, mean, rstd, inp["gamma"], N, C, S, G)
+    xt = torch.from_numpy(inp["x"].astype(np.float64)).reshape(N, C, S).requires_grad_()
+    gt = torch.from_numpy(inp["gamma"].astype(np.float64)).requires_grad_()
+    bt = torch.from_numpy(inp["beta"].astype(np.float64)).requires_grad_()
+    yt = F.relu(F.group_norm(xt, G, gt, bt, EPS32))
+    assert np.allclose(out, yt.detach().reshape(-1).numpy(), rtol=1e-6, atol=1e-7)
+    yt.backward(torch.from_numpy(inp["dy"].astype(np.float64)).reshape(N, C, S))
+    assert np.allclose(dx, xt.grad.reshape(-1).numpy(), rtol=1e-10, atol=1e-12)
+    assert np.allclose(dgamma, gt.grad.numpy(), rtol=1e-10, atol=1e-10)
+    assert np.allclose(dbeta, bt.grad.numpy(), rtol=1e-10, atol=1e-10)
+
+
+def test_backward_relu_matches_finite_differences(orc):
+    N, C, S, G = 1, 4, 8, 2
+    rng = np.random.default_rng(33)
+    h = 2.0 ** -14
+    x = (rng.integers(-512, 512, N * C * S) / 256.0).astype(np.float32)
+    gamma = (rng.integers(128, 384, C) / 256.0).astype(np.float32)
+    beta = (rng.integers(-32, 32, C) / 256.0).astype(np.float32)
+    w = rng.standard_normal(N * C * S).astype(np.float32)
+    eps = 1e-3
+    y64, mean, rstd = orc.forward(x, gamma, beta, N, C, S, G, eps)
+    assert np.min(np.abs(y64)) > 1e-3  # ~10x what a step of h moves y: each difference sees one side of the kink
+    out = orc.relu(orc.round_f32(y64).astype(np.float64)).astype(np.float32)
+    dx, _, _ = orc.backward_relu(w, x, out, mean, rstd, gamma, N, C, S, G)
+
+    def L(xx):
+        yy, _, _ = orc.forward(xx, gamma, beta, N, C, S, G, eps)
+        return float(np.dot(w.astype(np.float64), orc.relu(yy)))
+    gx = np.empty(x.size)
+    for i in range(x.size):
+        xp, xm = x.copy(), x.copy()
+        xp[i] += np.float32(h)
+        xm[i] -= np.float32(h)
+        gx[i] = (L(xp) - L(xm)) / (2 * h)
+    assert np.max(np.abs(dx - gx)) <= 1e-7 * np.max(np.abs(gx))
