@@ -53,6 +53,11 @@ def lib():
             L.gn3d_forward.restype = ci
             L.gn3d_backward.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, ci, vp, vp, vp, vp]
             L.gn3d_backward.restype = ci
+            L.gn3d_forward_relu.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, dbl, ci, ci, vp, vp, vp, vp]
+            L.gn3d_forward_relu.restype = ci
+            L.gn3d_backward_relu.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, ci, vp, vp, vp,
+                                             vp]
+            L.gn3d_backward_relu.restype = ci
             L.gn3d_stream_status.argtypes = [vp]
             L.gn3d_stream_status.restype = ci
             L.gn3d_error_string.argtypes = [ci]
@@ -79,6 +84,16 @@ def gn3d_forward(x, gamma, beta, N, C, D, H, W, G, eps, in_dtype, out_dtype, y, 
 
 def gn3d_backward(dy, x, mean, rstd, gamma, N, C, D, H, W, G, dtype, dx, dgamma, dbeta, stream):
     _check(lib().gn3d_backward(dy, x, mean, rstd, gamma, N, C, D, H, W, G, dtype, dx, dgamma, dbeta, stream))
+
+
+def gn3d_forward_relu(x, gamma, beta, N, C, D, H, W, G, eps, in_dtype, out_dtype, out, mean, rstd, stream):
+    _check(lib().gn3d_forward_relu(x, gamma, beta, N, C, D, H, W, G, eps, in_dtype, out_dtype, out, mean, rstd,
+                                   stream))
+
+
+def gn3d_backward_relu(dy, x, out, mean, rstd, gamma, N, C, D, H, W, G, dtype, dx, dgamma, dbeta, stream):
+    _check(lib().gn3d_backward_relu(dy, x, out, mean, rstd, gamma, N, C, D, H, W, G, dtype, dx, dgamma, dbeta,
+                                    stream))
 
 
 def gn3d_stream_status(stream):
@@ -117,8 +132,9 @@ def _shape5(x):
     return tuple(int(s) for s in x.shape)
 
 
-def forward(x, gamma, beta, G: int, eps: float = 1e-5, out_dtype=None):
-    """y, mean, rstd = GroupNorm(x) on x's device; y has out_dtype (default x.dtype)."""
+def forward(x, gamma, beta, G: int, eps: float = 1e-5, out_dtype=None, relu: bool = False):
+    """y, mean, rstd = GroupNorm(x) on x's device -- followed by the fused ReLU
+    when relu is set; y has out_dtype (default x.dtype)."""
     import torch
 
     N, C, D, H, W = _shape5(x)
@@ -126,26 +142,36 @@ def forward(x, gamma, beta, G: int, eps: float = 1e-5, out_dtype=None):
     y = torch.empty((N, C, D, H, W), dtype=out_dtype, device=x.device)
     mean = torch.empty((N, G), dtype=torch.float32, device=x.device)
     rstd = torch.empty((N, G), dtype=torch.float32, device=x.device)
-    gn3d_forward(x.data_ptr(), _ptr(gamma), _ptr(beta), N, C, D, H, W, G, float(eps), _dtype_code(x.dtype),
-                 _dtype_code(out_dtype), y.data_ptr(), mean.data_ptr(), rstd.data_ptr(),
-                 torch.cuda.current_stream(x.device).cuda_stream)
+    fn = gn3d_forward_relu if relu else gn3d_forward
+    fn(x.data_ptr(), _ptr(gamma), _ptr(beta), N, C, D, H, W, G, float(eps), _dtype_code(x.dtype),
+       _dtype_code(out_dtype), y.data_ptr(), mean.data_ptr(), rstd.data_ptr(),
+       torch.cuda.current_stream(x.device).cuda_stream)
     return y, mean, rstd
 
 
-def backward(dy, x, mean, rstd, gamma, G: int):
-    """dx, dgamma, dbeta of GroupNorm at the saved (mean, rstd)."""
+def backward(dy, x, mean, rstd, gamma, G: int, out=None):
+    """dx, dgamma, dbeta of GroupNorm at the saved (mean, rstd); with `out` (the
+    fused ReLU forward's result, x's dtype) the backward of relu(GroupNorm(x))."""
     import torch
 
     N, C, D, H, W = _shape5(x)
     if dy.shape != x.shape or dy.dtype != x.dtype:
         raise ValueError("dy must match x in shape and dtype")
+    if out is not None and (out.shape != x.shape or out.dtype != x.dtype):
+        raise ValueError("out must match x in shape and dtype")
     dy = dy.contiguous()
     dx = torch.empty_like(x)
     dgamma = torch.empty((C,), dtype=torch.float32, device=x.device)
     dbeta = torch.empty((C,), dtype=torch.float32, device=x.device)
-    gn3d_backward(dy.data_ptr(), x.data_ptr(), mean.data_ptr(), rstd.data_ptr(), _ptr(gamma), N, C, D, H, W, G,
-                  _dtype_code(x.dtype), dx.data_ptr(), dgamma.data_ptr(), dbeta.data_ptr(),
-                  torch.cuda.current_stream(x.device).cuda_stream)
+    st = torch.cuda.current_stream(x.device).cuda_stream
+    if out is None:
+        gn3d_backward(dy.data_ptr(), x.data_ptr(), mean.data_ptr(), rstd.data_ptr(), _ptr(gamma), N, C, D, H, W, G,
+                      _dtype_code(x.dtype), dx.data_ptr(), dgamma.data_ptr(), dbeta.data_ptr(), st)
+    else:
+        out = out.contiguous()
+        gn3d_backward_relu(dy.data_ptr(), x.data_ptr(), out.data_ptr(), mean.data_ptr(), rstd.data_ptr(),
+                           _ptr(gamma), N, C, D, H, W, G, _dtype_code(x.dtype), dx.data_ptr(), dgamma.data_ptr(),
+                           dbeta.data_ptr(), st)
     return dx, dgamma, dbeta
 
 

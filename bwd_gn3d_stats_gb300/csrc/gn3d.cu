@@ -286,8 +286,8 @@ int coop_grid(const void* func, int threads, int smem, const DevInfo& di, int* g
 // --------------------------------------------------------------- forward
 template <class TI, class TO>
 int launch_forward(const void* x, const float* gamma, const float* beta, const Plan& p, float eps, void* y,
-                   float* mean, float* rstd, cudaStream_t st, DevInfo& di) {
-  const bool fused = use_fused();
+                   float* mean, float* rstd, cudaStream_t st, DevInfo& di, bool relu) {
+  const bool fused = use_fused() && !relu;  // the fused ReLU runs in the streaming kernels
   const int64_t nblk = p.NC * p.nb;
   const int64_t nsync = nblk + 2 * p.NG + 2;  // bcnt, gcnt, ready, abort, never
   const int64_t bytes = rup(nsync * 4) + rup(p.units * (int64_t)sizeof(Part)) +
@@ -341,7 +341,8 @@ int launch_forward(const void* x, const float* gamma, const float* beta, const P
     e = cudaGetLastError();
     if (e == cudaSuccess) {
       LaunchTimer t2(KK_FWD_NORM, st, di);
-      auto kn = full ? k_fwd_norm<TI, TO, true> : k_fwd_norm<TI, TO, false>;
+      auto kn = full ? (relu ? k_fwd_norm<TI, TO, true, true> : k_fwd_norm<TI, TO, true, false>)
+                     : (relu ? k_fwd_norm<TI, TO, false, true> : k_fwd_norm<TI, TO, false, false>);
       e = launch_dependent(kn, sgrid, 32 * kElemWarps, st, xp, yp, p, (const float4*)w.stats, gamma, beta);
       t2.done();
     }
@@ -353,10 +354,41 @@ int launch_forward(const void* x, const float* gamma, const float* beta, const P
 }
 
 // -------------------------------------------------------------- backward
+// The streaming backward launches; kRelu: behind a fused ReLU, dy gated by the
+// forward's result `res`.
+template <class T, bool kRelu>
+cudaError_t launch_backward_streaming(const T* dyp, const T* xp, const T* resp, T* dxp, const Plan& p,
+                                      const float* mean, const float* rstd, const float* gamma, BwdWs& w,
+                                      float* dgamma, float* dbeta, cudaStream_t st, DevInfo& di, int* rc) {
+  using Shape = BwdRedShape<T, kRelu>;
+  const int64_t nblk = p.NC * p.nb;
+  const int smem = Shape::kWarps * WarpRing<T, Shape::kTensors, Shape::kSlots, Shape::kElems>::kWarpBytes;
+  const bool full = plan_all_full(p);
+  auto kr = full ? k_bwd_reduce<T, true, kRelu> : k_bwd_reduce<T, false, kRelu>;
+  *rc = raise_smem((const void*)kr, smem, di);
+  if (*rc) return cudaSuccess;
+  const int rgrid = grid_for(di, nblk, 1);
+  g_launches += 2;
+  LaunchTimer t1(KK_BWD_REDUCE, st, di);
+  kr<<<rgrid, 32 * Shape::kWarps, smem, st>>>(dyp, xp, resp, p, mean, rstd, gamma, w, dgamma, dbeta,
+                                             spin_budget(), di.status);
+  t1.done();
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) {
+    LaunchTimer t2(KK_BWD_DX, st, di);
+    auto kd = full ? k_bwd_dx<T, true, kRelu> : k_bwd_dx<T, false, kRelu>;
+    e = launch_dependent(kd, rgrid, 32 * kElemWarps, st, dyp, xp, resp, dxp, p, mean, rstd, gamma,
+                         (const float2*)w.coef);
+    t2.done();
+  }
+  return e;
+}
+
 template <class T>
-int launch_backward(const void* dy, const void* x, const float* mean, const float* rstd, const float* gamma,
-                    const Plan& p, void* dx, float* dgamma, float* dbeta, cudaStream_t st, DevInfo& di) {
-  const bool fused = use_fused();
+int launch_backward(const void* dy, const void* x, const void* res, const float* mean, const float* rstd,
+                    const float* gamma, const Plan& p, void* dx, float* dgamma, float* dbeta, cudaStream_t st,
+                    DevInfo& di) {
+  const bool fused = use_fused() && !res;  // the fused ReLU's gate runs in the streaming kernels
   const int64_t nblk = p.NC * p.nb;
   const int64_t nsync = nblk + 2 * p.NG + 3;  // bcnt, gcnt, ready, done, abort, never
   const int64_t bytes = rup(nsync * 4) + rup(p.units * (int64_t)sizeof(float2)) +
@@ -398,26 +430,13 @@ int launch_backward(const void* dy, const void* x, const float* mean, const floa
     e = cudaLaunchCooperativeKernel((const void*)k, dim3(grid), dim3(threads), args, (size_t)smem, st);
     tm.done();
   } else if (e == cudaSuccess) {
-    using Shape = BwdRedShape<T>;
-    const int smem = Shape::kWarps * WarpRing<T, 2, Shape::kSlots, Shape::kElems>::kWarpBytes;
-    const bool full = plan_all_full(p);
-    auto kr = full ? k_bwd_reduce<T, true> : k_bwd_reduce<T, false>;
-    int rc = raise_smem((const void*)kr, smem, di);
+    int rc = GN3D_OK;
+    const T* resp = static_cast<const T*>(res);
+    e = res ? launch_backward_streaming<T, true>(dyp, xp, resp, dxp, p, mean, rstd, gamma, w, dgamma, dbeta, st,
+                                                 di, &rc)
+            : launch_backward_streaming<T, false>(dyp, xp, nullptr, dxp, p, mean, rstd, gamma, w, dgamma, dbeta,
+                                                  st, di, &rc);
     if (rc) { cudaFreeAsync(s.base, st); return rc; }
-    const int rgrid = grid_for(di, nblk, 1);
-    g_launches += 2;
-    LaunchTimer t1(KK_BWD_REDUCE, st, di);
-    kr<<<rgrid, 32 * Shape::kWarps, smem, st>>>(dyp, xp, p, mean, rstd, gamma, w, dgamma, dbeta, spin_budget(),
-                                               di.status);
-    t1.done();
-    e = cudaGetLastError();
-    if (e == cudaSuccess) {
-      LaunchTimer t2(KK_BWD_DX, st, di);
-      auto kd = full ? k_bwd_dx<T, true> : k_bwd_dx<T, false>;
-      e = launch_dependent(kd, rgrid, 32 * kElemWarps, st, dyp, xp, dxp, p, mean, rstd, gamma,
-                           (const float2*)w.coef);
-      t2.done();
-    }
   }
   cudaError_t ef = cudaFreeAsync(s.base, st);
   if (e != cudaSuccess) return cuda_fail(e, "backward launch");
@@ -525,9 +544,10 @@ int launch_forward_noalloc(const void* x, const float* gamma, const float* beta,
 
 using namespace gn3d;
 
-extern "C" int gn3d_forward(const void* x, const float* gamma, const float* beta, int64_t N, int64_t C,
-                            int64_t D, int64_t H, int64_t W, int64_t G, double eps, gn3d_dtype in_dtype,
-                            gn3d_dtype out_dtype, void* y, float* mean, float* rstd, void* stream) {
+namespace {
+int forward_impl(const void* x, const float* gamma, const float* beta, int64_t N, int64_t C, int64_t D, int64_t H,
+                 int64_t W, int64_t G, double eps, gn3d_dtype in_dtype, gn3d_dtype out_dtype, void* y, float* mean,
+                 float* rstd, void* stream, bool relu) {
   int rc = check_shape(N, C, D, H, W, G);
   if (rc) return rc;
   if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype)) return arg_fail("unsupported dtype");
@@ -563,12 +583,64 @@ extern "C" int gn3d_forward(const void* x, const float* gamma, const float* beta
   }
   using bf = __nv_bfloat16;
   if (in_dtype == GN3D_BF16 && out_dtype == GN3D_BF16)
-    return launch_forward<bf, bf>(x, gamma, beta, p, feps, y, mean, rstd, st, *di);
+    return launch_forward<bf, bf>(x, gamma, beta, p, feps, y, mean, rstd, st, *di, relu);
   if (in_dtype == GN3D_BF16 && out_dtype == GN3D_F32)
-    return launch_forward<bf, float>(x, gamma, beta, p, feps, y, mean, rstd, st, *di);
+    return launch_forward<bf, float>(x, gamma, beta, p, feps, y, mean, rstd, st, *di, relu);
   if (in_dtype == GN3D_F32 && out_dtype == GN3D_BF16)
-    return launch_forward<float, bf>(x, gamma, beta, p, feps, y, mean, rstd, st, *di);
-  return launch_forward<float, float>(x, gamma, beta, p, feps, y, mean, rstd, st, *di);
+    return launch_forward<float, bf>(x, gamma, beta, p, feps, y, mean, rstd, st, *di, relu);
+  return launch_forward<float, float>(x, gamma, beta, p, feps, y, mean, rstd, st, *di, relu);
+}
+
+int backward_impl(const void* dy, const void* x, const void* res, const float* mean, const float* rstd,
+                  const float* gamma, int64_t N, int64_t C, int64_t D, int64_t H, int64_t W, int64_t G,
+                  gn3d_dtype dtype, void* dx, float* dgamma, float* dbeta, void* stream, bool relu) {
+  int rc = check_shape(N, C, D, H, W, G);
+  if (rc) return rc;
+  if (!valid_dtype(dtype)) return arg_fail("unsupported dtype");
+  const Plan p = make_plan(N, C, D * H * W, G);
+  const int64_t numel = p.NC * p.S;
+  int dev = 0;
+  GN3D_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  DevInfo* di = nullptr;
+  if ((rc = device_info(dev, &di))) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (C > 0) {
+    if (gamma && (rc = check_ptr(gamma, dev, "gamma"))) return rc;
+    if (dgamma && (rc = check_ptr(dgamma, dev, "dgamma"))) return rc;
+    if (dbeta && (rc = check_ptr(dbeta, dev, "dbeta"))) return rc;
+  }
+  if (numel == 0) {
+    if (dgamma && C > 0) GN3D_CUDA(cudaMemsetAsync(dgamma, 0, (size_t)C * sizeof(float), st), "memset");
+    if (dbeta && C > 0) GN3D_CUDA(cudaMemsetAsync(dbeta, 0, (size_t)C * sizeof(float), st), "memset");
+    return GN3D_OK;
+  }
+  if (!dy || !x || !dx || !mean || !rstd) return arg_fail("dy, x, dx, mean and rstd are required");
+  if (!aligned16(dy) || !aligned16(x) || !aligned16(dx)) return arg_fail("dy, x and dx must be 16-byte aligned");
+  if ((rc = check_ptr(dy, dev, "dy")) || (rc = check_ptr(x, dev, "x")) || (rc = check_ptr(dx, dev, "dx")) ||
+      (rc = check_ptr(mean, dev, "mean")) || (rc = check_ptr(rstd, dev, "rstd")))
+    return rc;
+  if (relu) {
+    if (!res) return arg_fail("out (the forward's result) is required");
+    if (!aligned16(res)) return arg_fail("out must be 16-byte aligned");
+    if ((rc = check_ptr(res, dev, "out"))) return rc;
+  }
+  if (dtype == GN3D_BF16)
+    return launch_backward<__nv_bfloat16>(dy, x, relu ? res : nullptr, mean, rstd, gamma, p, dx, dgamma, dbeta,
+                                          st, *di);
+  return launch_backward<float>(dy, x, relu ? res : nullptr, mean, rstd, gamma, p, dx, dgamma, dbeta, st, *di);
+}
+}  // namespace
+
+extern "C" int gn3d_forward(const void* x, const float* gamma, const float* beta, int64_t N, int64_t C,
+                            int64_t D, int64_t H, int64_t W, int64_t G, double eps, gn3d_dtype in_dtype,
+                            gn3d_dtype out_dtype, void* y, float* mean, float* rstd, void* stream) {
+  return forward_impl(x, gamma, beta, N, C, D, H, W, G, eps, in_dtype, out_dtype, y, mean, rstd, stream, false);
+}
+
+extern "C" int gn3d_forward_relu(const void* x, const float* gamma, const float* beta, int64_t N, int64_t C,
+                                 int64_t D, int64_t H, int64_t W, int64_t G, double eps, gn3d_dtype in_dtype,
+                                 gn3d_dtype out_dtype, void* out, float* mean, float* rstd, void* stream) {
+  return forward_impl(x, gamma, beta, N, C, D, H, W, G, eps, in_dtype, out_dtype, out, mean, rstd, stream, true);
 }
 
 // The forward without any allocation: the same kernel as gn3d_forward, with its
@@ -615,34 +687,15 @@ extern "C" int gn3d_forward_noalloc(const void* x, const float* gamma, const flo
 extern "C" int gn3d_backward(const void* dy, const void* x, const float* mean, const float* rstd,
                              const float* gamma, int64_t N, int64_t C, int64_t D, int64_t H, int64_t W,
                              int64_t G, gn3d_dtype dtype, void* dx, float* dgamma, float* dbeta, void* stream) {
-  int rc = check_shape(N, C, D, H, W, G);
-  if (rc) return rc;
-  if (!valid_dtype(dtype)) return arg_fail("unsupported dtype");
-  const Plan p = make_plan(N, C, D * H * W, G);
-  const int64_t numel = p.NC * p.S;
-  int dev = 0;
-  GN3D_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
-  DevInfo* di = nullptr;
-  if ((rc = device_info(dev, &di))) return rc;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (C > 0) {
-    if (gamma && (rc = check_ptr(gamma, dev, "gamma"))) return rc;
-    if (dgamma && (rc = check_ptr(dgamma, dev, "dgamma"))) return rc;
-    if (dbeta && (rc = check_ptr(dbeta, dev, "dbeta"))) return rc;
-  }
-  if (numel == 0) {
-    if (dgamma && C > 0) GN3D_CUDA(cudaMemsetAsync(dgamma, 0, (size_t)C * sizeof(float), st), "memset");
-    if (dbeta && C > 0) GN3D_CUDA(cudaMemsetAsync(dbeta, 0, (size_t)C * sizeof(float), st), "memset");
-    return GN3D_OK;
-  }
-  if (!dy || !x || !dx || !mean || !rstd) return arg_fail("dy, x, dx, mean and rstd are required");
-  if (!aligned16(dy) || !aligned16(x) || !aligned16(dx)) return arg_fail("dy, x and dx must be 16-byte aligned");
-  if ((rc = check_ptr(dy, dev, "dy")) || (rc = check_ptr(x, dev, "x")) || (rc = check_ptr(dx, dev, "dx")) ||
-      (rc = check_ptr(mean, dev, "mean")) || (rc = check_ptr(rstd, dev, "rstd")))
-    return rc;
-  if (dtype == GN3D_BF16)
-    return launch_backward<__nv_bfloat16>(dy, x, mean, rstd, gamma, p, dx, dgamma, dbeta, st, *di);
-  return launch_backward<float>(dy, x, mean, rstd, gamma, p, dx, dgamma, dbeta, st, *di);
+  return backward_impl(dy, x, nullptr, mean, rstd, gamma, N, C, D, H, W, G, dtype, dx, dgamma, dbeta, stream,
+                       false);
+}
+
+extern "C" int gn3d_backward_relu(const void* dy, const void* x, const void* out, const float* mean,
+                                  const float* rstd, const float* gamma, int64_t N, int64_t C, int64_t D,
+                                  int64_t H, int64_t W, int64_t G, gn3d_dtype dtype, void* dx, float* dgamma,
+                                  float* dbeta, void* stream) {
+  return backward_impl(dy, x, out, mean, rstd, gamma, N, C, D, H, W, G, dtype, dx, dgamma, dbeta, stream, true);
 }
 
 extern "C" int gn3d_stream_status(void* stream) {

@@ -195,6 +195,13 @@ __device__ __forceinline__ f2 f2fma(f2 a, f2 b, f2 c) {
   return d;
 }
 
+// 0xFFFF in each 16-bit half of w that holds a bf16 value <= 0 (NaN: 0).
+__device__ __forceinline__ uint32_t bf16x2_le0(uint32_t w) {
+  uint32_t m;
+  asm("set.le.u32.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(w), "r"(0u));
+  return m;
+}
+
 // (lo - k, hi - k) for the two bf16 halves of w, as an fp32 pair.
 __device__ __forceinline__ f2 bf16_pair_minus(uint32_t w, float k) {
   f2 d;
@@ -230,6 +237,14 @@ template <> struct Vec<__nv_bfloat16> {
     d[2] = bf16_pair_minus(r[0].z, k);
     d[3] = bf16_pair_minus(r[0].w, k);
   }
+  // Zero the elements of d where the result o is <= 0 (ordered compare: a NaN
+  // result keeps its gradient) -- threshold_backward's gate, two halves at once.
+  static __device__ __forceinline__ void gate(const uint4 o[kRaw], uint4 d[kRaw]) {
+    d[0].x &= ~bf16x2_le0(o[0].x);
+    d[0].y &= ~bf16x2_le0(o[0].y);
+    d[0].z &= ~bf16x2_le0(o[0].z);
+    d[0].w &= ~bf16x2_le0(o[0].w);
+  }
 };
 
 template <> struct Vec<float> {
@@ -257,6 +272,15 @@ template <> struct Vec<float> {
     const f2 k2 = f2_splat(k);
 #pragma unroll
     for (int e = 0; e < 4; ++e) d[e] = f2sub(p[e], k2);
+  }
+  static __device__ __forceinline__ void gate(const uint4 o[kRaw], uint4 d[kRaw]) {
+#pragma unroll
+    for (int t = 0; t < kRaw; ++t) {
+      d[t].x = __uint_as_float(o[t].x) <= 0.f ? 0u : d[t].x;
+      d[t].y = __uint_as_float(o[t].y) <= 0.f ? 0u : d[t].y;
+      d[t].z = __uint_as_float(o[t].z) <= 0.f ? 0u : d[t].z;
+      d[t].w = __uint_as_float(o[t].w) <= 0.f ? 0u : d[t].w;
+    }
   }
 };
 
@@ -424,6 +448,25 @@ __device__ __forceinline__ float4 merge_group(const Part* blocks, int64_t nblk, 
   return make_float4(g.m1, g.cn, __frsqrt_rn(fadd(var, eps)), 0.f);
 }
 
+// The gradient arriving at GroupNorm behind a fused ReLU: dy read from `body`,
+// zeroed where the forward's result (read from `res`, laid out like dy) is
+// <= 0 -- torch's threshold_backward on the saved result.
+template <class T, class Src>
+struct GatedView {
+  const T* body;
+  const T* res;
+  int nv;
+  __device__ __forceinline__ bool has(int i) const { return (int)(threadIdx.x & 31) + 32 * i < nv; }
+  __device__ __forceinline__ void get(int i, f2 p[4]) const {
+    const int v = (int)(threadIdx.x & 31) + 32 * i;
+    uint4 d[Vec<T>::kRaw], o[Vec<T>::kRaw];
+    Vec<T>::template load<Src>(body + v * kVec, d);
+    Vec<T>::template load<Src>(res + v * kVec, o);
+    Vec<T>::gate(o, d);
+    Vec<T>::pairs(d, p);
+  }
+};
+
 // Moments of one unit, by one warp, in one pass over its elements.  Lane l
 // first takes a pilot mean K_l of its first kPilotVecs vectors, then sums
 // d = x - K_l and d^2 over all its elements: its partial is n_l, mean
@@ -525,7 +568,21 @@ __device__ __forceinline__ void fwd_block_done(const Plan& p, const FwdWs& ws, i
 }
 
 // NORM of one forward unit, by one warp: y = (x - hi)*sc + (beta - lo*sc), sc = rstd*gamma.
-template <bool kFull, class TI, class TO, class View>
+// The fused ReLU of the forward: F.relu of the value the store will round to,
+// computed before the store.  Rounding to TO and then v < 0 ? +0 : v keeps -0.0
+// for the values that round to -0.0 (below half the smallest bf16 subnormal,
+// 2^-134, in magnitude) and gives +0 for every other negative.
+template <class TO> struct OutRelu;
+template <> struct OutRelu<float> {
+  static __device__ __forceinline__ float apply(float v) { return v < 0.f ? 0.f : v; }
+};
+template <> struct OutRelu<__nv_bfloat16> {
+  static __device__ __forceinline__ float apply(float v) {
+    return v < 0.f ? (v >= -0x1p-134f ? -0.f : 0.f) : v;
+  }
+};
+
+template <bool kFull, class TI, class TO, class View, bool kRelu = false>
 __device__ __forceinline__ void fwd_norm(const View& u, const TI* __restrict__ x, TO* __restrict__ y,
                                          const URange& q, float4 st, float gam, float bet) {
   const int lane = threadIdx.x & 31;
@@ -538,13 +595,17 @@ __device__ __forceinline__ void fwd_norm(const View& u, const TI* __restrict__ x
       f2 v[4];
       u.diff(i, st.x, v);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) v[k] = f2fma(v[k], sc2, sh2);
+      for (int k = 0; k < 4; ++k) {
+        v[k] = f2fma(v[k], sc2, sh2);
+        if (kRelu) v[k] = f2_of(OutRelu<TO>::apply(f2_lo(v[k])), OutRelu<TO>::apply(f2_hi(v[k])));
+      }
       store8p<TO>(y + q.b0 + (int64_t)(lane + 32 * i) * kVec, v);
     }
   }
   if (!kFull && lane < scalar_count(q)) {
     const int64_t idx = scalar_index(q, lane);
-    IO<TO>::store1(y + idx, ffma(fsub(IO<TI>::load1(x + idx), st.x), sc, sh));
+    const float r = ffma(fsub(IO<TI>::load1(x + idx), st.x), sc, sh);
+    IO<TO>::store1(y + idx, kRelu ? OutRelu<TO>::apply(r) : r);
   }
 }
 
@@ -564,8 +625,8 @@ struct BwdWs {
 // bwd_accum adds the lane's vectors i0 <= i < i1 to its running sums (a unit's
 // body may arrive in parts), bwd_finish meets the sums in the fixed tree, adds
 // the lane's scalar and sums the lanes.
-template <bool kFull, class T, class View>
-__device__ __forceinline__ void bwd_accum(const View& ux, const View& ud, int i0, int i1, float mu, f2 a1[4],
+template <bool kFull, class T, class XView, class DView>
+__device__ __forceinline__ void bwd_accum(const XView& ux, const DView& ud, int i0, int i1, float mu, f2 a1[4],
                                           f2 a2[4]) {
 #pragma unroll
   for (int i = 0; i < kVecPerLane; ++i) {
@@ -582,14 +643,23 @@ __device__ __forceinline__ void bwd_accum(const View& ux, const View& ud, int i0
   }
 }
 
+// The gradient at scalar element idx: dy, zeroed behind a fused ReLU (res !=
+// nullptr) where the forward's result is <= 0.
+template <class T>
+__device__ __forceinline__ float grad_at(const T* __restrict__ dy, const T* __restrict__ res, int64_t idx) {
+  const float d = IO<T>::load1(dy + idx);
+  return res && IO<T>::load1(res + idx) <= 0.f ? 0.f : d;
+}
+
 template <bool kFull, class T>
 __device__ __forceinline__ float2 bwd_finish(const f2 a1[4], const f2 a2[4], const T* __restrict__ x,
-                                             const T* __restrict__ dy, const URange& q, float mu) {
+                                             const T* __restrict__ dy, const URange& q, float mu,
+                                             const T* __restrict__ res = nullptr) {
   const int lane = threadIdx.x & 31;
   float s1 = tree8p(a1), s2 = tree8p(a2);
   if (!kFull && lane < scalar_count(q)) {
     const int64_t idx = scalar_index(q, lane);
-    const float d = IO<T>::load1(dy + idx);
+    const float d = grad_at(dy, res, idx);
     s1 = fadd(s1, d);
     s2 = ffma(d, fsub(IO<T>::load1(x + idx), mu), s2);
   }
@@ -698,10 +768,10 @@ struct DxCoef {
 };
 
 // NORM of one backward unit, by one warp.
-template <bool kFull, class T, class View>
-__device__ __forceinline__ void bwd_norm(const View& ux, const View& ud, const T* __restrict__ x,
+template <bool kFull, class T, class XView, class DView>
+__device__ __forceinline__ void bwd_norm(const XView& ux, const DView& ud, const T* __restrict__ x,
                                          const T* __restrict__ dy, T* __restrict__ dx, const URange& q,
-                                         const DxCoef& k, float gam) {
+                                         const DxCoef& k, float gam, const T* __restrict__ res = nullptr) {
   const int lane = threadIdx.x & 31;
   const float p1 = k.single ? 0.f : fmul(k.r, gam);
   const float p2 = k.single ? 0.f : fmul(fmul(k.r, k.r), k.b);
@@ -720,7 +790,7 @@ __device__ __forceinline__ void bwd_norm(const View& ux, const View& ud, const T
   }
   if (!kFull && lane < scalar_count(q)) {
     const int64_t idx = scalar_index(q, lane);
-    const float d = IO<T>::load1(dy + idx);
+    const float d = grad_at(dy, res, idx);
     IO<T>::store1(dx + idx, ffma(d, p1, ffma(-p2, fsub(IO<T>::load1(x + idx), k.mu), -p3)));
   }
 }

@@ -140,10 +140,13 @@ template <class T> struct FwdStatShape {
   static constexpr int kWarps = sizeof(T) == 2 ? 8 : 4;
   static constexpr int kSlots = 3;
 };
-template <class T> struct BwdRedShape {  // x and dy of one 8 KB part per slot
+template <class T, bool kRelu = false> struct BwdRedShape {
+  // a slot: 4 KB of each of x and dy (8 KB), or -- behind a fused ReLU, with the
+  // forward's result as a third tensor -- 2 KB of each (6 KB, four slots)
   static constexpr int kWarps = 8;
-  static constexpr int kSlots = 3;
-  static constexpr int kElems = 4096 / (int)sizeof(T);
+  static constexpr int kSlots = kRelu ? 4 : 3;
+  static constexpr int kTensors = kRelu ? 3 : 2;
+  static constexpr int kElems = (kRelu ? 2048 : 4096) / (int)sizeof(T);
 };
 
 template <class TI, bool kFull>
@@ -230,7 +233,7 @@ struct OwnedBlocks {
   }
 };
 
-template <class TI, class TO, bool kFull>
+template <class TI, class TO, bool kFull, bool kRelu>
 __global__ void __launch_bounds__(32 * kElemWarps, 1)
     k_fwd_norm(const TI* __restrict__ x, TO* __restrict__ y, Plan p, const float4* __restrict__ stats,
                const float* __restrict__ gamma, const float* __restrict__ beta) {
@@ -270,22 +273,23 @@ __global__ void __launch_bounds__(32 * kElemWarps, 1)
           else v.template load<FromGlobal>(x + q.b0, nv);
         }
         pre = false;
-        fwd_norm<kFull, TI, TO>(v, x, y, q, st, gm, bt);
+        fwd_norm<kFull, TI, TO, RegView<TI>, kRelu>(v, x, y, q, st, gm, bt);
       } else {
-        fwd_norm<kFull, TI, TO>(MemView<TI, FromGlobal>{x + q.b0, nv}, x, y, q, st, gm, bt);
+        fwd_norm<kFull, TI, TO, MemView<TI, FromGlobal>, kRelu>(MemView<TI, FromGlobal>{x + q.b0, nv}, x, y, q, st,
+                                                                gm, bt);
       }
     }
   }
 }
 
-template <class T, bool kFull>
-__global__ void __launch_bounds__(32 * BwdRedShape<T>::kWarps, 1)
-    k_bwd_reduce(const T* __restrict__ dy, const T* __restrict__ x, Plan p, const float* __restrict__ mean,
-                 const float* __restrict__ rstd, const float* __restrict__ gamma, BwdWs ws, float* dgamma,
-                 float* dbeta, unsigned long long spin, uint32_t* status) {
+template <class T, bool kFull, bool kRelu>
+__global__ void __launch_bounds__(32 * BwdRedShape<T, kRelu>::kWarps, 1)
+    k_bwd_reduce(const T* __restrict__ dy, const T* __restrict__ x, const T* __restrict__ res, Plan p,
+                 const float* __restrict__ mean, const float* __restrict__ rstd, const float* __restrict__ gamma,
+                 BwdWs ws, float* dgamma, float* dbeta, unsigned long long spin, uint32_t* status) {
   extern __shared__ __align__(128) unsigned char smem[];
-  using Shape = BwdRedShape<T>;
-  using Ring = WarpRing<T, 2, Shape::kSlots, Shape::kElems>;
+  using Shape = BwdRedShape<T, kRelu>;
+  using Ring = WarpRing<T, Shape::kTensors, Shape::kSlots, Shape::kElems>;
   constexpr int kParts = Ring::kParts, kPartVecs = kVecPerLane / kParts;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_launch_dependents();  // the dx kernel may take SMs as this one leaves them
@@ -293,7 +297,7 @@ __global__ void __launch_bounds__(32 * BwdRedShape<T>::kWarps, 1)
   ring.init(smem + (size_t)warp * Ring::kWarpBytes);
   const int64_t nblk = p.NC * p.nb, stride = (int64_t)gridDim.x * Shape::kWarps;
   const int64_t first = (int64_t)warp * gridDim.x + blockIdx.x;
-  const T* src[2] = {x, dy};
+  const T* src[3] = {x, dy, res};
   PartWalk ld;
   ld.w.set(p, first, nblk);
   BlockWalk cu = ld.w;
@@ -320,8 +324,14 @@ __global__ void __launch_bounds__(32 * BwdRedShape<T>::kWarps, 1)
       // views placed so that vector i of the unit is read from this part's slot
       const T* xs = reinterpret_cast<const T*>(slot) - (size_t)part * Shape::kElems;
       const T* ds = reinterpret_cast<const T*>(slot + Ring::kTensorBytes) - (size_t)part * Shape::kElems;
-      bwd_accum<kFull, T>(MemView<T, FromShared>{xs, nv}, MemView<T, FromShared>{ds, nv}, part * kPartVecs,
-                          (part + 1) * kPartVecs, mu, a1, a2);
+      if constexpr (kRelu) {
+        const T* rs = reinterpret_cast<const T*>(slot + 2 * Ring::kTensorBytes) - (size_t)part * Shape::kElems;
+        bwd_accum<kFull, T>(MemView<T, FromShared>{xs, nv}, GatedView<T, FromShared>{ds, rs, nv},
+                            part * kPartVecs, (part + 1) * kPartVecs, mu, a1, a2);
+      } else {
+        bwd_accum<kFull, T>(MemView<T, FromShared>{xs, nv}, MemView<T, FromShared>{ds, nv}, part * kPartVecs,
+                            (part + 1) * kPartVecs, mu, a1, a2);
+      }
       __syncwarp();
       if (!ld.w.end) {
         ring.issue(urange<kFull>(p, ld.w.row, ld.w.k()), ld.part, src);
@@ -332,7 +342,7 @@ __global__ void __launch_bounds__(32 * BwdRedShape<T>::kWarps, 1)
       record_timeout(status);
       break;
     }
-    const float2 v = bwd_finish<kFull, T>(a1, a2, x, dy, q, mu);
+    const float2 v = bwd_finish<kFull, T>(a1, a2, x, dy, q, mu, kRelu ? res : nullptr);
     if (lane == cu.ui) a = v;
     if (cu.ui == cu.bsz - 1) {
       bwd_block_done(p, ws, cu.b, lane < cu.bsz ? a : make_float2(0.f, 0.f), rstd, gamma, dgamma, dbeta);
@@ -343,12 +353,12 @@ __global__ void __launch_bounds__(32 * BwdRedShape<T>::kWarps, 1)
   ring.drain(spin);
 }
 
-template <class T, bool kFull>
+template <class T, bool kFull, bool kRelu>
 __global__ void __launch_bounds__(32 * kElemWarps, 1)
-    k_bwd_dx(const T* __restrict__ dy, const T* __restrict__ x, T* __restrict__ dx, Plan p,
-             const float* __restrict__ mean, const float* __restrict__ rstd, const float* __restrict__ gamma,
-             const float2* __restrict__ coef) {
-  using Own = OwnedBlocks<BwdRedShape<T>::kWarps>;
+    k_bwd_dx(const T* __restrict__ dy, const T* __restrict__ x, const T* __restrict__ res, T* __restrict__ dx,
+             Plan p, const float* __restrict__ mean, const float* __restrict__ rstd,
+             const float* __restrict__ gamma, const float2* __restrict__ coef) {
+  using Own = OwnedBlocks<BwdRedShape<T, kRelu>::kWarps>;
   const Own own;
   const int64_t nblk = p.NC * p.nb;
   pdl_wait();  // the reduction kernel's coefficients
@@ -362,8 +372,13 @@ __global__ void __launch_bounds__(32 * kElemWarps, 1)
     for (int ui = bsz - 1 - own.share; ui >= 0; ui -= Own::kSplit) {
       const URange q = urange<kFull>(p, row, kb * kBlockUnits + ui);
       const int nv = (int)((q.b1 - q.b0) / kVec);
-      bwd_norm<kFull, T>(MemView<T, FromGlobal>{x + q.b0, nv}, MemView<T, FromGlobal>{dy + q.b0, nv}, x, dy, dx,
-                         q, k, gm);
+      if constexpr (kRelu) {
+        bwd_norm<kFull, T>(MemView<T, FromGlobal>{x + q.b0, nv}, GatedView<T, FromGlobal>{dy + q.b0, res + q.b0, nv},
+                           x, dy, dx, q, k, gm, res);
+      } else {
+        bwd_norm<kFull, T>(MemView<T, FromGlobal>{x + q.b0, nv}, MemView<T, FromGlobal>{dy + q.b0, nv}, x, dy,
+                           dx, q, k, gm);
+      }
     }
   }
 }

@@ -125,6 +125,36 @@ int gn3d_backward(const void* dy, const void* x, const float* mean, const float*
                   void* stream);
 
 /*
+ * GroupNorm followed by ReLU, the ReLU fused into the store (the ScaFFold
+ * GroupNorm pages move the ReLU that follows every GroupNorm of the UNet inside
+ * it: FastGroupNorm's activation argument).  Same arguments, errors, mean and
+ * rstd as gn3d_forward; `out` receives F.relu of the rounded GroupNorm result,
+ *   out = v < 0 ? +0 : v,   v = y rounded once to out_dtype,
+ * so NaN, +Inf and -0.0 pass and -Inf and every other negative become +0: bit
+ * for bit gn3d_forward followed by F.relu on its output (the pages' fix makes the
+ * fused ReLU match F.relu on NaN, both infinities and -0.0).  Always runs the
+ * streaming kernels (GN3D_DEBUG_PATH 2 does not apply to it).
+ */
+int gn3d_forward_relu(const void* x, const float* gamma, const float* beta, int64_t N, int64_t C,
+                      int64_t D, int64_t H, int64_t W, int64_t G, double eps, gn3d_dtype in_dtype,
+                      gn3d_dtype out_dtype, void* out, float* mean, float* rstd, void* stream);
+
+/*
+ * Backward of relu(GroupNorm(x)).
+ *   out  [N,C,D,H,W] dtype (the dtype of x, dy and dx), read only: the
+ *        forward's result (gn3d_forward_relu's out).  The gradient reaching
+ *        GroupNorm is torch's threshold_backward on it: dy where out is not <= 0
+ *        (a NaN result passes the gradient, as the pages' fix requires), 0 where
+ *        out <= 0 (either zero included).
+ * Everything else as gn3d_backward; the results are bit for bit gn3d_backward's
+ * on that gated dy.  dx must not overlap out.  Always runs the streaming kernels.
+ */
+int gn3d_backward_relu(const void* dy, const void* x, const void* out, const float* mean,
+                       const float* rstd, const float* gamma, int64_t N, int64_t C, int64_t D,
+                       int64_t H, int64_t W, int64_t G, gn3d_dtype dtype, void* dx, float* dgamma,
+                       float* dbeta, void* stream);
+
+/*
  * Synchronizes `stream`, then returns and clears the device-side error word
  * that bounded waits inside the kernels set (GN3D_ERR_TIMEOUT), or
  * GN3D_ERR_CUDA if the stream reports a CUDA error, else GN3D_OK.
