@@ -1,0 +1,88 @@
+"""The torch front end on the GPU: the module and its autograd give exactly the
+C ABI's results, load nn.GroupNorm's state dict, and agree with torch's own
+fp32 GroupNorm (and ReLU) within fp32 rounding."""
+import numpy as np
+import pytest
+
+import bwd_gn3d_stats_gb300 as gn
+from bwd_gn3d_stats_gb300 import synth
+
+from .gpu_util import to_np, torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from bwd_gn3d_stats_gb300 import build
+
+    build.build()
+
+
+def same(u, v):
+    return np.array_equal(to_np(u), to_np(v))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("affine", [True, False])
+@pytest.mark.parametrize("relu", [False, True])
+def test_module_is_the_c_abi(dtype, affine, relu):
+    from bwd_gn3d_stats_gb300.nn import GroupNorm3d
+
+    t = torch()
+    tdt = t.bfloat16 if dtype == "bf16" else t.float32
+    gen = t.Generator(device="cuda").manual_seed(5)
+    N, C, D, H, W, G = 2, 16, 9, 10, 11, 4
+    x = t.randn(N, C, D, H, W, device="cuda", generator=gen).to(tdt)
+    dy = t.randn(N, C, D, H, W, device="cuda", generator=gen).to(tdt)
+    m = GroupNorm3d(G, C, affine=affine, activation="relu" if relu else None).cuda()
+    if affine:
+        with t.no_grad():
+            m.weight.uniform_(0.5, 1.5, generator=gen)
+            m.bias.normal_(0, 0.3, generator=gen)
+    xr = x.clone().requires_grad_()
+    y = m(xr)
+    y.backward(dy)
+    w = m.weight.detach() if affine else None
+    b = m.bias.detach() if affine else None
+    y0, mean, rstd = gn.forward(x, w, b, G, 1e-5, relu=relu)
+    dx0, dg0, db0 = gn.backward(dy, x, mean, rstd, w, G, out=y0 if relu else None)
+    assert y.dtype == tdt and same(y, y0)
+    assert same(xr.grad, dx0)
+    if affine:
+        assert same(m.weight.grad, dg0) and same(m.bias.grad, db0)
+
+
+def test_module_loads_nn_groupnorm_and_matches_it():
+    from bwd_gn3d_stats_gb300.nn import GroupNorm3d
+
+    t = torch()
+    gen = t.Generator(device="cuda").manual_seed(6)
+    ref = t.nn.GroupNorm(8, 32).cuda()
+    with t.no_grad():
+        ref.weight.uniform_(0.5, 1.5, generator=gen)
+        ref.bias.normal_(0, 0.3, generator=gen)
+    ours = GroupNorm3d(8, 32, activation="relu").cuda()
+    ours.load_state_dict(ref.state_dict())
+    x = t.randn(2, 32, 12, 12, 12, device="cuda", generator=gen)
+    dy = t.randn(2, 32, 12, 12, 12, device="cuda", generator=gen)
+    x1, x2 = x.clone().requires_grad_(), x.clone().requires_grad_()
+    y1 = ours(x1)
+    y2 = t.relu(ref(x2))
+    y1.backward(dy)
+    y2.backward(dy)
+    assert t.allclose(y1, y2, rtol=1e-5, atol=1e-5)
+    assert t.allclose(x1.grad, x2.grad, rtol=1e-4, atol=1e-5)
+    assert t.allclose(ours.weight.grad, ref.weight.grad, rtol=1e-4, atol=1e-3)
+    assert t.allclose(ours.bias.grad, ref.bias.grad, rtol=1e-4, atol=1e-3)
+
+
+def test_relu_needs_matching_out_dtype():
+    from bwd_gn3d_stats_gb300.nn import group_norm_3d
+
+    t = torch()
+    x = t.randn(1, 8, 4, 4, 4, device="cuda").to(t.bfloat16)
+    with pytest.raises(ValueError):
+        group_norm_3d(x, 4, out_dtype=t.float32, relu=True)
+    y = group_norm_3d(x, 4, out_dtype=t.float32)  # without the ReLU any pair is allowed
+    assert y.dtype == t.float32
