@@ -35,6 +35,7 @@ UNIT = "GB/s"
 NOMINAL_HBM_GBS = 8000.0
 DEFAULT_WORKLOAD = "bf16_1x32x128^3_G8"
 SECONDARY = ["bf16_1x32x256^3_G8"]
+UNET = "bf16_unet_stack_G8"  # the UNet's GroupNorm sites, reported per site and rolled up
 FLUSH_BYTES = 256 << 20
 
 
@@ -329,6 +330,30 @@ def barrier(ws):
         dist.barrier()
 
 
+def unet_rollup(dev, flush, stream, ws):
+    """Per-site device time of the UNet site stack (each distinct shape timed once,
+    counted as often as the stack holds it) and the stack's effective GB/s."""
+    import torch
+
+    distinct = {}
+    for s in synth.WORKLOADS[UNET].sites:
+        distinct.setdefault(s.name(), [s, 0])[1] += 1
+    sites, tot_bytes, tot_ms = [], 0, 0.0
+    for name, (s2, count) in distinct.items():
+        v2 = Volume(s2, dev, pinned=False)
+        t2, _, _ = time_device([v2], 5, 3, flush, stream)
+        ms2 = max_over_ranks(sum(t2) / len(t2), ws, dev)
+        fb, bb = s2.min_bytes()
+        sites.append({"site": name, "count": count, "us_per_step": round(ms2 * 1e3, 2),
+                      "gbs": round(ws * (fb + bb) / (ms2 * 1e-3) / 1e9, 1)})
+        tot_bytes += count * (fb + bb)
+        tot_ms += count * ms2
+        del v2
+        torch.cuda.empty_cache()
+    return {"value": round(ws * tot_bytes / (tot_ms * 1e-3) / 1e9, 1), "ms_per_stack": round(tot_ms, 4),
+            "min_bytes_per_stack": tot_bytes, "sites": sites}
+
+
 def run_gpu(args):
     import torch
 
@@ -393,6 +418,7 @@ def run_gpu(args):
                                "fwd_gbs": round(f2b / (sum(f2) / len(f2) * 1e-3) / 1e9, 1),
                                "bwd_gbs": round(b2b / (sum(b2) / len(b2) * 1e-3) / 1e9, 1)}
             del v2
+        secondary[UNET] = unet_rollup(dev, flush, stream, ws)
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         v, cores, sample = cpu_oracle_sample(site)

@@ -684,7 +684,31 @@ __device__ __forceinline__ void bwd_group(const Plan& p, const BwdWs& ws, int64_
                                           const float* gamma) {
   const int lane = threadIdx.x & 31;
   float A = 0.f, B = 0.f;
-  for (int64_t cl = 0; cl < p.Cg; ++cl) {
+  // rows of at most 32 blocks: each lane holds one block of a row, so the loads
+  // of kMergeBatch rows go out together (a group of many short rows would
+  // otherwise wait out one L2 round trip per row); the sums are the same
+  for (int64_t cl0 = 0; p.nb <= 32 && cl0 < p.Cg; cl0 += kMergeBatch) {
+    float2 v[kMergeBatch];
+    float gm[kMergeBatch];
+#pragma unroll
+    for (int j = 0; j < kMergeBatch; ++j) {
+      const int64_t cl = cl0 + j, row = g * p.Cg + cl;
+      v[j] = cl < p.Cg && lane < p.nb ? __ldcg(ws.bparts + row * p.nb + lane) : make_float2(0.f, 0.f);
+      gm[j] = cl < p.Cg && gamma ? gamma[(g % p.G) * p.Cg + cl] : 1.f;
+    }
+#pragma unroll
+    for (int j = 0; j < kMergeBatch; ++j) {
+      const int64_t cl = cl0 + j;
+      if (cl >= p.Cg) break;
+      const float s1 = lane < p.nb ? fadd(0.f, v[j].x) : 0.f;
+      const float s2 = lane < p.nb ? fadd(0.f, v[j].y) : 0.f;
+      const float2 t = warp_sum2(s1, s2);
+      if (lane == 0) ws.rows[g * p.Cg + cl] = t;
+      A = fadd(A, fmul(gm[j], t.x));
+      B = fadd(B, fmul(gm[j], t.y));
+    }
+  }
+  for (int64_t cl = 0; p.nb > 32 && cl < p.Cg; ++cl) {
     const int64_t row = g * p.Cg + cl;
     const float2* bp = ws.bparts + row * p.nb;
     float s1 = 0.f, s2 = 0.f;
@@ -717,7 +741,28 @@ __device__ __forceinline__ void bwd_group(const Plan& p, const BwdWs& ws, int64_
 // dgamma_c = sum_n rstd[n,g] * S2[n,c], dbeta_c = sum_n S1[n,c], in n order, by one warp.
 __device__ __forceinline__ void bwd_param_grads(const Plan& p, const float* rstd, const float2* rows,
                                                 float* dgamma, float* dbeta) {
-  for (int64_t c = threadIdx.x & 31; c < p.C; c += 32) {
+  // one sample: the loads of kMergeBatch channels per lane go out together
+  for (int64_t c0 = threadIdx.x & 31; p.N == 1 && c0 < p.C; c0 += 32 * kMergeBatch) {
+    float2 rs[kMergeBatch];
+    float r[kMergeBatch];
+#pragma unroll
+    for (int k = 0; k < kMergeBatch; ++k) {
+      const int64_t c = c0 + 32 * k;
+      if (c < p.C) {
+        rs[k] = __ldcg(rows + c);
+        r[k] = rstd[c / p.Cg];
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kMergeBatch; ++k) {
+      const int64_t c = c0 + 32 * k;
+      if (c >= p.C) break;
+      const float dg = fadd(0.f, fmul(r[k], rs[k].y)), db = fadd(0.f, rs[k].x);
+      if (dgamma) dgamma[c] = dg;
+      if (dbeta) dbeta[c] = db;
+    }
+  }
+  for (int64_t c = threadIdx.x & 31; p.N > 1 && c < p.C; c += 32) {
     const int64_t g = c / p.Cg;
     float dg = 0.f, db = 0.f;
     for (int64_t n0 = 0; n0 < p.N; n0 += kMergeBatch) {
