@@ -47,22 +47,26 @@ def peaks():
     return 6800.0, "fallback"
 
 
-def source_sha():
+# The device sources of the streaming kernels (what a traffic figure depends on).
+KERNEL_SOURCES = ["gn3d_plan.cuh", "gn3d_device.cuh", "gn3d_sync.cuh", "gn3d_kernels.cuh"]
+
+
+def source_sha(files=None):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bwd_gn3d_stats_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in sorted(files or KERNEL_SOURCES):
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
 def traffic_for(kernel: str, workload: str):
-    """DRAM bytes per launch from a committed ncu summary, if taken on the current sources."""
+    """DRAM bytes per launch from a committed ncu summary, if taken on the current kernel sources."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
     e = d.get(kernel, {}).get(workload)
-    if not e or e.get("source_sha") != source_sha():
+    if not e or e.get("source_sha") != source_sha(e.get("sources")):
         return None
     return e.get("dram_bytes_per_launch")
 
