@@ -10,7 +10,8 @@ Two levels:
     handle) and raise ``GN3DError`` on a non-zero status.
   * ``forward`` / ``backward`` take torch CUDA tensors, allocate the outputs
     with torch and pass torch's current stream.  torch is used for device
-    memory and streams only.
+    memory and streams only.  ``forward_ndhwc`` / ``backward_ndhwc`` do the same
+    for channels_last_3d tensors (the C entry points ``gn3d_*_ndhwc*``).
 """
 from __future__ import annotations
 
@@ -58,6 +59,14 @@ def lib():
             L.gn3d_backward_relu.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, ci, vp, vp, vp,
                                              vp]
             L.gn3d_backward_relu.restype = ci
+            for name in ("gn3d_forward_ndhwc", "gn3d_forward_ndhwc_relu"):
+                getattr(L, name).argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, dbl, ci, ci, vp, vp, vp, vp]
+                getattr(L, name).restype = ci
+            L.gn3d_backward_ndhwc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, ci, vp, vp, vp, vp]
+            L.gn3d_backward_ndhwc.restype = ci
+            L.gn3d_backward_ndhwc_relu.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, ci, vp, vp,
+                                                   vp, vp]
+            L.gn3d_backward_ndhwc_relu.restype = ci
             L.gn3d_stream_status.argtypes = [vp]
             L.gn3d_stream_status.restype = ci
             L.gn3d_error_string.argtypes = [ci]
@@ -96,6 +105,25 @@ def gn3d_backward_relu(dy, x, out, mean, rstd, gamma, N, C, D, H, W, G, dtype, d
                                     stream))
 
 
+def gn3d_forward_ndhwc(x, gamma, beta, N, C, D, H, W, G, eps, in_dtype, out_dtype, y, mean, rstd, stream):
+    _check(lib().gn3d_forward_ndhwc(x, gamma, beta, N, C, D, H, W, G, eps, in_dtype, out_dtype, y, mean, rstd,
+                                    stream))
+
+
+def gn3d_forward_ndhwc_relu(x, gamma, beta, N, C, D, H, W, G, eps, in_dtype, out_dtype, out, mean, rstd, stream):
+    _check(lib().gn3d_forward_ndhwc_relu(x, gamma, beta, N, C, D, H, W, G, eps, in_dtype, out_dtype, out, mean,
+                                         rstd, stream))
+
+
+def gn3d_backward_ndhwc(dy, x, mean, rstd, gamma, N, C, D, H, W, G, dtype, dx, dgamma, dbeta, stream):
+    _check(lib().gn3d_backward_ndhwc(dy, x, mean, rstd, gamma, N, C, D, H, W, G, dtype, dx, dgamma, dbeta, stream))
+
+
+def gn3d_backward_ndhwc_relu(dy, x, out, mean, rstd, gamma, N, C, D, H, W, G, dtype, dx, dgamma, dbeta, stream):
+    _check(lib().gn3d_backward_ndhwc_relu(dy, x, out, mean, rstd, gamma, N, C, D, H, W, G, dtype, dx, dgamma,
+                                          dbeta, stream))
+
+
 def gn3d_stream_status(stream):
     _check(lib().gn3d_stream_status(stream))
 
@@ -130,6 +158,65 @@ def _shape5(x):
     if not x.is_contiguous():
         raise ValueError("libgn3d takes contiguous NCDHW tensors")
     return tuple(int(s) for s in x.shape)
+
+
+def _shape5_cl(x):
+    import torch
+
+    if x.dim() != 5:
+        raise ValueError("expected an [N, C, D, H, W] tensor")
+    if not x.is_contiguous(memory_format=torch.channels_last_3d):
+        raise ValueError("the NDHWC entry points take channels_last_3d tensors")
+    return tuple(int(s) for s in x.shape)
+
+
+def is_ndhwc(x) -> bool:
+    """x is stored channels-last (channels_last_3d) and not plain NCDHW-contiguous."""
+    import torch
+
+    return x.dim() == 5 and not x.is_contiguous() and x.is_contiguous(memory_format=torch.channels_last_3d)
+
+
+def forward_ndhwc(x, gamma, beta, G: int, eps: float = 1e-5, out_dtype=None, relu: bool = False):
+    """forward() for a channels_last_3d x: y (channels_last_3d), mean, rstd."""
+    import torch
+
+    N, C, D, H, W = _shape5_cl(x)
+    out_dtype = x.dtype if out_dtype is None else out_dtype
+    y = torch.empty((N, C, D, H, W), dtype=out_dtype, device=x.device, memory_format=torch.channels_last_3d)
+    mean = torch.empty((N, G), dtype=torch.float32, device=x.device)
+    rstd = torch.empty((N, G), dtype=torch.float32, device=x.device)
+    fn = gn3d_forward_ndhwc_relu if relu else gn3d_forward_ndhwc
+    fn(x.data_ptr(), _ptr(gamma), _ptr(beta), N, C, D, H, W, G, float(eps), _dtype_code(x.dtype),
+       _dtype_code(out_dtype), y.data_ptr(), mean.data_ptr(), rstd.data_ptr(),
+       torch.cuda.current_stream(x.device).cuda_stream)
+    return y, mean, rstd
+
+
+def backward_ndhwc(dy, x, mean, rstd, gamma, G: int, out=None):
+    """backward() for channels_last_3d tensors: dx (channels_last_3d), dgamma, dbeta."""
+    import torch
+
+    N, C, D, H, W = _shape5_cl(x)
+    if dy.shape != x.shape or dy.dtype != x.dtype:
+        raise ValueError("dy must match x in shape and dtype")
+    if out is not None and (out.shape != x.shape or out.dtype != x.dtype):
+        raise ValueError("out must match x in shape and dtype")
+    cl = torch.channels_last_3d
+    dy = dy.contiguous(memory_format=cl)
+    dx = torch.empty((N, C, D, H, W), dtype=x.dtype, device=x.device, memory_format=cl)
+    dgamma = torch.empty((C,), dtype=torch.float32, device=x.device)
+    dbeta = torch.empty((C,), dtype=torch.float32, device=x.device)
+    st = torch.cuda.current_stream(x.device).cuda_stream
+    if out is None:
+        gn3d_backward_ndhwc(dy.data_ptr(), x.data_ptr(), mean.data_ptr(), rstd.data_ptr(), _ptr(gamma), N, C, D, H,
+                            W, G, _dtype_code(x.dtype), dx.data_ptr(), dgamma.data_ptr(), dbeta.data_ptr(), st)
+    else:
+        out = out.contiguous(memory_format=cl)
+        gn3d_backward_ndhwc_relu(dy.data_ptr(), x.data_ptr(), out.data_ptr(), mean.data_ptr(), rstd.data_ptr(),
+                                 _ptr(gamma), N, C, D, H, W, G, _dtype_code(x.dtype), dx.data_ptr(),
+                                 dgamma.data_ptr(), dbeta.data_ptr(), st)
+    return dx, dgamma, dbeta
 
 
 def forward(x, gamma, beta, G: int, eps: float = 1e-5, out_dtype=None, relu: bool = False):
@@ -188,7 +275,8 @@ def gn3d_debug_set(what: int, value: int):
     _check(L.gn3d_debug_set(what, value))
 
 
-KERNELS = ("k_fwd_fused", "k_bwd_fused", "k_fwd_stats", "k_fwd_norm", "k_bwd_reduce", "k_bwd_dx")
+KERNELS = ("k_fwd_fused", "k_bwd_fused", "k_fwd_stats", "k_fwd_norm", "k_bwd_reduce", "k_bwd_dx",
+           "k_ndhwc_stats", "k_ndhwc_norm", "k_ndhwc_reduce", "k_ndhwc_dx")
 
 
 def gn3d_kernel_time(name: str):

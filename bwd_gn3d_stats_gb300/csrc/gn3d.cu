@@ -17,6 +17,7 @@
 #include "../../include/gn3d.h"
 #include "gn3d_fused.cuh"
 #include "gn3d_kernels.cuh"
+#include "gn3d_ndhwc.cuh"
 
 namespace gn3d {
 
@@ -150,9 +151,13 @@ int64_t rup(int64_t b) { return ((b + 255) / 256) * 256; }
 // ------------------------------------------------------------ kernel timing
 // While timing is on (GN3D_DEBUG_TIMING), each kernel launch is bracketed by two
 // CUDA events on its stream; gn3d_kernel_time resolves them per kernel.
-enum { KK_FWD_FUSED, KK_BWD_FUSED, KK_FWD_STATS, KK_FWD_NORM, KK_BWD_REDUCE, KK_BWD_DX, KK_COUNT };
-const char* const kKernelNames[KK_COUNT] = {"k_fwd_fused", "k_bwd_fused", "k_fwd_stats",
-                                            "k_fwd_norm",  "k_bwd_reduce", "k_bwd_dx"};
+enum {
+  KK_FWD_FUSED, KK_BWD_FUSED, KK_FWD_STATS, KK_FWD_NORM, KK_BWD_REDUCE, KK_BWD_DX,
+  KK_N_STATS, KK_N_NORM, KK_N_REDUCE, KK_N_DX, KK_COUNT
+};
+const char* const kKernelNames[KK_COUNT] = {"k_fwd_fused",   "k_bwd_fused",  "k_fwd_stats",    "k_fwd_norm",
+                                            "k_bwd_reduce",  "k_bwd_dx",     "k_ndhwc_stats",  "k_ndhwc_norm",
+                                            "k_ndhwc_reduce", "k_ndhwc_dx"};
 std::atomic<int> g_timing{0};
 std::mutex g_tmu;
 struct TimedLaunch {
@@ -444,6 +449,101 @@ int launch_backward(const void* dy, const void* x, const void* res, const float*
   return GN3D_OK;
 }
 
+// ---------------------------------------------------- channels-last (NDHWC)
+// Statistics then normalize (dependent launch), and reduction then dx, each pair
+// on one grid of min(SMs, units) CTAs (gn3d_ndhwc.cuh).
+template <class TI, class TO>
+int launch_forward_ndhwc(const void* x, const float* gamma, const float* beta, const NPlan& p, float eps, void* y,
+                         float* mean, float* rstd, cudaStream_t st, DevInfo& di, bool relu) {
+  const int64_t nsync = p.nblk + 1;  // block counters, finished CTAs
+  const int64_t bytes = rup(nsync * 4) + rup(p.rows * p.P * p.R * (int64_t)sizeof(Part)) +
+                        rup(p.rows * p.P * p.nb * (int64_t)sizeof(Part)) + rup(p.NG * (int64_t)sizeof(float4));
+  Scratch s;
+  GN3D_CUDA(cudaMallocFromPoolAsync(&s.base, (size_t)bytes, di.pool, st), "scratch allocation");
+  s.cur = static_cast<char*>(s.base);
+  uint32_t* sync = s.take<uint32_t>(nsync);
+  NFwdWs w;
+  w.bcnt = sync;
+  w.done = sync + p.nblk;
+  w.upart = s.take<Part>(p.rows * p.P * p.R);
+  w.bpart = s.take<Part>(p.rows * p.P * p.nb);
+  w.stats = s.take<float4>(p.NG);
+  cudaError_t e = cudaMemsetAsync(sync, 0, (size_t)nsync * sizeof(uint32_t), st);
+  const TI* xp = static_cast<const TI*>(x);
+  TO* yp = static_cast<TO*>(y);
+  const int smem = kNRedWarps * kNSpan * kNVec * (int)sizeof(Part);  // per warp: one unit's channel partials
+  auto ks = k_ndhwc_stats<TI>;
+  int rc = raise_smem((const void*)ks, smem, di);
+  if (rc) { cudaFreeAsync(s.base, st); return rc; }
+  const int grid = grid_for(di, p.units, 1);
+  if (e == cudaSuccess) {
+    g_launches += 2;
+    LaunchTimer t1(KK_N_STATS, st, di);
+    ks<<<grid, 32 * kNRedWarps, smem, st>>>(xp, p, w, eps, mean, rstd);
+    t1.done();
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) {
+    LaunchTimer t2(KK_N_NORM, st, di);
+    auto kn = relu ? k_ndhwc_norm<TI, TO, true> : k_ndhwc_norm<TI, TO, false>;
+    e = launch_dependent(kn, grid, 32 * kNElemWarps, st, xp, yp, p, (const float4*)w.stats, gamma, beta);
+    t2.done();
+  }
+  cudaError_t ef = cudaFreeAsync(s.base, st);
+  if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+  if (ef != cudaSuccess) return cuda_fail(ef, "scratch free");
+  return GN3D_OK;
+}
+
+template <class T>
+int launch_backward_ndhwc(const void* dy, const void* x, const void* res, const float* mean, const float* rstd,
+                          const float* gamma, const NPlan& p, void* dx, float* dgamma, float* dbeta, cudaStream_t st,
+                          DevInfo& di) {
+  const int64_t nsync = p.nblk + 1;
+  const int64_t NC = p.N * p.C;
+  const int64_t bytes = rup(nsync * 4) + rup(NC * p.R * (int64_t)sizeof(float2)) +
+                        rup(NC * p.nb * (int64_t)sizeof(float2)) + rup(NC * (int64_t)sizeof(float2)) +
+                        rup(p.NG * (int64_t)sizeof(float2));
+  Scratch s;
+  GN3D_CUDA(cudaMallocFromPoolAsync(&s.base, (size_t)bytes, di.pool, st), "scratch allocation");
+  s.cur = static_cast<char*>(s.base);
+  uint32_t* sync = s.take<uint32_t>(nsync);
+  NBwdWs w;
+  w.bcnt = sync;
+  w.done = sync + p.nblk;
+  w.usum = s.take<float2>(NC * p.R);
+  w.bsum = s.take<float2>(NC * p.nb);
+  w.rows = s.take<float2>(NC);
+  w.coef = s.take<float2>(p.NG);
+  cudaError_t e = cudaMemsetAsync(sync, 0, (size_t)nsync * sizeof(uint32_t), st);
+  const T* dyp = static_cast<const T*>(dy);
+  const T* xp = static_cast<const T*>(x);
+  const T* resp = static_cast<const T*>(res);
+  T* dxp = static_cast<T*>(dx);
+  const int grid = grid_for(di, p.units, 1);
+  if (e == cudaSuccess) {
+    g_launches += 2;
+    LaunchTimer t1(KK_N_REDUCE, st, di);
+    if (res)
+      k_ndhwc_reduce<T, true><<<grid, 32 * kNRedWarps, 0, st>>>(dyp, xp, resp, p, mean, rstd, gamma, w, dgamma, dbeta);
+    else
+      k_ndhwc_reduce<T, false><<<grid, 32 * kNRedWarps, 0, st>>>(dyp, xp, nullptr, p, mean, rstd, gamma, w, dgamma,
+                                                              dbeta);
+    t1.done();
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) {
+    LaunchTimer t2(KK_N_DX, st, di);
+    auto kd = res ? k_ndhwc_dx<T, true> : k_ndhwc_dx<T, false>;
+    e = launch_dependent(kd, grid, 32 * kNElemWarps, st, dyp, xp, resp, dxp, p, mean, rstd, gamma, (const float2*)w.coef);
+    t2.done();
+  }
+  cudaError_t ef = cudaFreeAsync(s.base, st);
+  if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+  if (ef != cudaSuccess) return cuda_fail(ef, "scratch free");
+  return GN3D_OK;
+}
+
 bool valid_dtype(int d) { return d == GN3D_F32 || d == GN3D_BF16; }
 
 // ------------------------------------------------- allocation-free forward
@@ -547,9 +647,10 @@ using namespace gn3d;
 namespace {
 int forward_impl(const void* x, const float* gamma, const float* beta, int64_t N, int64_t C, int64_t D, int64_t H,
                  int64_t W, int64_t G, double eps, gn3d_dtype in_dtype, gn3d_dtype out_dtype, void* y, float* mean,
-                 float* rstd, void* stream, bool relu) {
+                 float* rstd, void* stream, bool relu, bool ndhwc = false) {
   int rc = check_shape(N, C, D, H, W, G);
   if (rc) return rc;
+  if (ndhwc && C % kNVec != 0 && N * D * H * W > 0) return arg_fail("the NDHWC layout needs C % 8 == 0");
   if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype)) return arg_fail("unsupported dtype");
   if (!(eps >= 0.0) || !isfinite(eps)) return arg_fail("eps must be finite and >= 0");
   const float feps = (float)eps;
@@ -582,6 +683,16 @@ int forward_impl(const void* x, const float* gamma, const float* beta, int64_t N
     return GN3D_OK;
   }
   using bf = __nv_bfloat16;
+  if (ndhwc) {
+    const NPlan np = make_nplan(N, C, D * H * W, G);
+    if (in_dtype == GN3D_BF16 && out_dtype == GN3D_BF16)
+      return launch_forward_ndhwc<bf, bf>(x, gamma, beta, np, feps, y, mean, rstd, st, *di, relu);
+    if (in_dtype == GN3D_BF16 && out_dtype == GN3D_F32)
+      return launch_forward_ndhwc<bf, float>(x, gamma, beta, np, feps, y, mean, rstd, st, *di, relu);
+    if (in_dtype == GN3D_F32 && out_dtype == GN3D_BF16)
+      return launch_forward_ndhwc<float, bf>(x, gamma, beta, np, feps, y, mean, rstd, st, *di, relu);
+    return launch_forward_ndhwc<float, float>(x, gamma, beta, np, feps, y, mean, rstd, st, *di, relu);
+  }
   if (in_dtype == GN3D_BF16 && out_dtype == GN3D_BF16)
     return launch_forward<bf, bf>(x, gamma, beta, p, feps, y, mean, rstd, st, *di, relu);
   if (in_dtype == GN3D_BF16 && out_dtype == GN3D_F32)
@@ -593,9 +704,11 @@ int forward_impl(const void* x, const float* gamma, const float* beta, int64_t N
 
 int backward_impl(const void* dy, const void* x, const void* res, const float* mean, const float* rstd,
                   const float* gamma, int64_t N, int64_t C, int64_t D, int64_t H, int64_t W, int64_t G,
-                  gn3d_dtype dtype, void* dx, float* dgamma, float* dbeta, void* stream, bool relu) {
+                  gn3d_dtype dtype, void* dx, float* dgamma, float* dbeta, void* stream, bool relu,
+                  bool ndhwc = false) {
   int rc = check_shape(N, C, D, H, W, G);
   if (rc) return rc;
+  if (ndhwc && C % kNVec != 0 && N * D * H * W > 0) return arg_fail("the NDHWC layout needs C % 8 == 0");
   if (!valid_dtype(dtype)) return arg_fail("unsupported dtype");
   const Plan p = make_plan(N, C, D * H * W, G);
   const int64_t numel = p.NC * p.S;
@@ -623,6 +736,14 @@ int backward_impl(const void* dy, const void* x, const void* res, const float* m
     if (!res) return arg_fail("out (the forward's result) is required");
     if (!aligned16(res)) return arg_fail("out must be 16-byte aligned");
     if ((rc = check_ptr(res, dev, "out"))) return rc;
+  }
+  if (ndhwc) {
+    const NPlan np = make_nplan(N, C, D * H * W, G);
+    if (dtype == GN3D_BF16)
+      return launch_backward_ndhwc<__nv_bfloat16>(dy, x, relu ? res : nullptr, mean, rstd, gamma, np, dx, dgamma,
+                                                  dbeta, st, *di);
+    return launch_backward_ndhwc<float>(dy, x, relu ? res : nullptr, mean, rstd, gamma, np, dx, dgamma, dbeta, st,
+                                        *di);
   }
   if (dtype == GN3D_BF16)
     return launch_backward<__nv_bfloat16>(dy, x, relu ? res : nullptr, mean, rstd, gamma, p, dx, dgamma, dbeta,
@@ -696,6 +817,32 @@ extern "C" int gn3d_backward_relu(const void* dy, const void* x, const void* out
                                   int64_t H, int64_t W, int64_t G, gn3d_dtype dtype, void* dx, float* dgamma,
                                   float* dbeta, void* stream) {
   return backward_impl(dy, x, out, mean, rstd, gamma, N, C, D, H, W, G, dtype, dx, dgamma, dbeta, stream, true);
+}
+
+extern "C" int gn3d_forward_ndhwc(const void* x, const float* gamma, const float* beta, int64_t N, int64_t C,
+                                  int64_t D, int64_t H, int64_t W, int64_t G, double eps, gn3d_dtype in_dtype,
+                                  gn3d_dtype out_dtype, void* y, float* mean, float* rstd, void* stream) {
+  return forward_impl(x, gamma, beta, N, C, D, H, W, G, eps, in_dtype, out_dtype, y, mean, rstd, stream, false, true);
+}
+
+extern "C" int gn3d_forward_ndhwc_relu(const void* x, const float* gamma, const float* beta, int64_t N, int64_t C,
+                                       int64_t D, int64_t H, int64_t W, int64_t G, double eps, gn3d_dtype in_dtype,
+                                       gn3d_dtype out_dtype, void* out, float* mean, float* rstd, void* stream) {
+  return forward_impl(x, gamma, beta, N, C, D, H, W, G, eps, in_dtype, out_dtype, out, mean, rstd, stream, true, true);
+}
+
+extern "C" int gn3d_backward_ndhwc(const void* dy, const void* x, const float* mean, const float* rstd,
+                                   const float* gamma, int64_t N, int64_t C, int64_t D, int64_t H, int64_t W,
+                                   int64_t G, gn3d_dtype dtype, void* dx, float* dgamma, float* dbeta, void* stream) {
+  return backward_impl(dy, x, nullptr, mean, rstd, gamma, N, C, D, H, W, G, dtype, dx, dgamma, dbeta, stream, false,
+                       true);
+}
+
+extern "C" int gn3d_backward_ndhwc_relu(const void* dy, const void* x, const void* out, const float* mean,
+                                        const float* rstd, const float* gamma, int64_t N, int64_t C, int64_t D,
+                                        int64_t H, int64_t W, int64_t G, gn3d_dtype dtype, void* dx, float* dgamma,
+                                        float* dbeta, void* stream) {
+  return backward_impl(dy, x, out, mean, rstd, gamma, N, C, D, H, W, G, dtype, dx, dgamma, dbeta, stream, true, true);
 }
 
 extern "C" int gn3d_stream_status(void* stream) {

@@ -1,0 +1,132 @@
+// gn3d_ndhwc_plan.cuh -- the launch plan of the channels-last (NDHWC) kernels:
+// channel ranges, units, merge blocks and pieces, as pure functions of the
+// shape (N, C, S = D*H*W, G).  Nothing here depends on the dtype or on the GPU,
+// so neither does any reduction order.  Host and device share these functions.
+#pragma once
+#include <stdint.h>
+
+#ifndef __CUDACC__
+#define __host__
+#define __device__
+#endif
+
+namespace gn3d {
+
+constexpr int kNVec = 8;     // elements per vector: 8 channels of one position
+constexpr int kNSpan = 32;   // vectors per channel range (256 channels)
+constexpr int kNSteps = 64;  // steps (vectors per lane) per unit
+constexpr int kNChunk = 16;  // steps of a lane's first chunk (pilot-shifted)
+constexpr int kNPilot = 4;   // steps of the pilot mean
+constexpr int kNRedWarps = 8;    // warps per CTA of the statistics and reduction kernels
+constexpr int kNElemWarps = 16;  // warps per CTA of the normalize and dx kernels
+
+struct NPlan {
+  int64_t N, C, S, G, Cg, NG, M;
+  int64_t V;      // vectors per position (C / 8)
+  int64_t nr;     // channel ranges
+  int64_t Pu;     // positions per unit
+  int64_t R;      // units per row
+  int64_t B;      // units per merge block
+  int64_t nb;     // merge blocks per row
+  int64_t P;      // pieces (groups met) per range, the most of any range
+  int64_t rows;   // N * nr
+  int64_t units;  // rows * R
+  int64_t nblk;   // rows * nb
+};
+
+// Range r: vectors [32r, 32r + vr), channels [c0, c1), groups g0 .. g1.
+struct NRange {
+  int vr, lp, lw;
+  int64_t c0, c1, g0, g1;
+};
+
+__host__ __device__ inline NRange n_range(const NPlan& p, int64_t r) {
+  NRange q;
+  const int64_t v = p.V - r * kNSpan;
+  q.vr = (int)(v < kNSpan ? v : kNSpan);
+  q.lp = 32 / q.vr;
+  q.lw = q.lp * q.vr;
+  q.c0 = r * kNSpan * kNVec;
+  q.c1 = q.c0 + (int64_t)kNVec * q.vr;
+  q.g0 = q.c0 / p.Cg;
+  q.g1 = (q.c1 - 1) / p.Cg;
+  return q;
+}
+
+inline NPlan make_nplan(int64_t N, int64_t C, int64_t S, int64_t G) {
+  NPlan p;
+  p.N = N; p.C = C; p.S = S; p.G = G;
+  p.Cg = C / G;
+  p.NG = N * G;
+  p.M = p.Cg * S;
+  p.V = C / kNVec;
+  p.nr = (p.V + kNSpan - 1) / kNSpan;
+  const int64_t v0 = p.V < kNSpan ? p.V : kNSpan;
+  p.Pu = (int64_t)kNSteps * (32 / v0);
+  p.R = S > 0 ? (S + p.Pu - 1) / p.Pu : 0;
+  // about 1024 channel-units per block (B * channels of range 0), 4 .. 32 units
+  int64_t b = 32;
+  while (b > 4 && b * kNVec * v0 > 1024) b >>= 1;
+  p.B = b;
+  p.nb = (p.R + p.B - 1) / p.B;
+  p.P = 0;
+  for (int64_t r = 0; r < p.nr; ++r) {
+    const NRange q = n_range(p, r);
+    if (q.g1 - q.g0 + 1 > p.P) p.P = q.g1 - q.g0 + 1;
+  }
+  p.rows = N * p.nr;
+  p.units = p.rows * p.R;
+  p.nblk = p.rows * p.nb;
+  return p;
+}
+
+// One unit as the calling lane sees it.
+struct NUnit {
+  int64_t row, k, n, r;
+  NRange rg;
+  int m, b;          // the lane's position in the step and its vector in the range
+  int64_t u0, len;   // first position of the unit and its positions
+  int cnt;           // vectors this lane reads
+  int64_t off;       // element offset of the lane's first vector
+  int64_t step;      // elements between the lane's consecutive vectors (lp * C)
+};
+
+__host__ __device__ inline NUnit n_unit(const NPlan& p, int64_t u, int lane) {
+  NUnit q;
+  q.row = u / p.R;
+  q.k = u - q.row * p.R;
+  q.n = q.row / p.nr;
+  q.r = q.row - q.n * p.nr;
+  q.rg = n_range(p, q.r);
+  q.m = lane / q.rg.vr;
+  q.b = lane - q.m * q.rg.vr;
+  q.u0 = q.k * p.Pu;
+  q.len = p.S - q.u0 < p.Pu ? p.S - q.u0 : p.Pu;
+  const bool active = lane < q.rg.lw && q.len > q.m;
+  q.cnt = active ? (int)((q.len - q.m + q.rg.lp - 1) / q.rg.lp) : 0;
+  q.off = (q.n * p.S + q.u0 + q.m) * p.C + q.rg.c0 + (int64_t)kNVec * q.b;
+  q.step = (int64_t)q.rg.lp * p.C;
+  return q;
+}
+
+// Channels [c0, c1) of piece j (group g0 + j) of a range, relative to the range.
+__host__ __device__ inline void n_piece(const NPlan& p, const NRange& rg, int64_t j, int64_t& c0, int64_t& c1) {
+  const int64_t g = rg.g0 + j;
+  const int64_t a = g * p.Cg, e = a + p.Cg;
+  c0 = (a > rg.c0 ? a : rg.c0) - rg.c0;
+  c1 = (e < rg.c1 ? e : rg.c1) - rg.c0;
+}
+
+// Units of block kb of a row.
+__host__ __device__ inline int n_block_size(const NPlan& p, int64_t kb) {
+  const int64_t rest = p.R - kb * p.B;
+  return (int)(rest < p.B ? rest : p.B);
+}
+
+// Positions covered by block kb of a row.
+__host__ __device__ inline int64_t n_block_positions(const NPlan& p, int64_t kb) {
+  const int64_t a = kb * p.B * p.Pu, e = a + p.B * p.Pu;
+  return (e < p.S ? e : p.S) - a;
+}
+
+}  // namespace gn3d

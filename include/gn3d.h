@@ -2,6 +2,9 @@
  * gn3d.h -- C ABI of libgn3d: GroupNorm forward and backward over contiguous
  * NCDHW volumes on an NVIDIA GB300 (sm_103a).
  *
+ * (The entry points named *_ndhwc take the channels-last layout instead; see
+ * their declaration below.)
+ *
  * Operation (ScaFFold PR #93 "Optimize GroupNorm": a drop-in for torch's
  * nn.GroupNorm, same weight and bias; PR #105 "Preserve GroupNorm dtype":
  * statistics accumulated in fp32, the normalized value computed in fp32, only
@@ -155,6 +158,45 @@ int gn3d_backward_relu(const void* dy, const void* x, const void* out, const flo
                        float* dbeta, void* stream);
 
 /*
+ * Channels-last (NDHWC) layout: the same four operations on tensors stored as
+ * x[n][d][h][w][c] -- the channels_last_3d memory format of an [N,C,D,H,W]
+ * tensor, as channels-last convolutions produce it (the ScaFFold GroupNorm
+ * pages' Triton kernel reads channels-last activations: a dense run of
+ * positions x C channels viewed as (G, C/G); their layout-tax measurements show
+ * a layout conversion around GroupNorm costing more than GroupNorm itself).
+ * Element (n, c, d, h, w) is at offset ((n*D + d)*H + h)*W + w)*C + c; group
+ * (n, g) is channels g*C/G .. (g+1)*C/G - 1 of every position of sample n.
+ *   - Same arguments, formulas, dtypes, ownership, empty-tensor handling and
+ *     errors as gn3d_forward / gn3d_forward_relu / gn3d_backward /
+ *     gn3d_backward_relu; y, dx, out and dy use the same NDHWC layout as x, and
+ *     mean, rstd ([N*G]), gamma, beta, dgamma, dbeta ([C]) are unchanged.
+ *   - C must be a multiple of 8 (a 16-byte vector then holds 8 channels of one
+ *     position); otherwise GN3D_ERR_INVALID_ARG.
+ *   - Deterministic (a fixed reduction order chosen from the shape alone; no
+ *     float atomics).  The order differs from the NCDHW entry points', so the
+ *     two layouts agree to rounding, not bit for bit.
+ *   - Always the streaming kernels (k_ndhwc_stats + k_ndhwc_norm forward,
+ *     k_ndhwc_reduce + k_ndhwc_dx backward); GN3D_DEBUG_PATH does not apply.
+ */
+int gn3d_forward_ndhwc(const void* x, const float* gamma, const float* beta, int64_t N, int64_t C,
+                       int64_t D, int64_t H, int64_t W, int64_t G, double eps, gn3d_dtype in_dtype,
+                       gn3d_dtype out_dtype, void* y, float* mean, float* rstd, void* stream);
+
+int gn3d_forward_ndhwc_relu(const void* x, const float* gamma, const float* beta, int64_t N, int64_t C,
+                            int64_t D, int64_t H, int64_t W, int64_t G, double eps, gn3d_dtype in_dtype,
+                            gn3d_dtype out_dtype, void* out, float* mean, float* rstd, void* stream);
+
+int gn3d_backward_ndhwc(const void* dy, const void* x, const float* mean, const float* rstd,
+                        const float* gamma, int64_t N, int64_t C, int64_t D, int64_t H, int64_t W,
+                        int64_t G, gn3d_dtype dtype, void* dx, float* dgamma, float* dbeta,
+                        void* stream);
+
+int gn3d_backward_ndhwc_relu(const void* dy, const void* x, const void* out, const float* mean,
+                             const float* rstd, const float* gamma, int64_t N, int64_t C, int64_t D,
+                             int64_t H, int64_t W, int64_t G, gn3d_dtype dtype, void* dx, float* dgamma,
+                             float* dbeta, void* stream);
+
+/*
  * Synchronizes `stream`, then returns and clears the device-side error word
  * that bounded waits inside the kernels set (GN3D_ERR_TIMEOUT), or
  * GN3D_ERR_CUDA if the stream reports a CUDA error, else GN3D_OK.
@@ -204,7 +246,8 @@ int gn3d_debug_set(int what, long long value);
 /*
  * Device time of one kernel, summed over the launches recorded since
  * GN3D_DEBUG_TIMING was last set to 1.  `name` is one of "k_fwd_fused",
- * "k_bwd_fused", "k_fwd_stats", "k_fwd_norm", "k_bwd_reduce", "k_bwd_dx".
+ * "k_bwd_fused", "k_fwd_stats", "k_fwd_norm", "k_bwd_reduce", "k_bwd_dx",
+ * "k_ndhwc_stats", "k_ndhwc_norm", "k_ndhwc_reduce", "k_ndhwc_dx".
  * Waits for the recorded events (host-blocking), then writes the total
  * milliseconds to *ms and the launch count to *launches.  Returns GN3D_OK,
  * GN3D_ERR_INVALID_ARG (NULL argument, unknown name) or GN3D_ERR_CUDA.

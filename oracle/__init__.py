@@ -14,6 +14,11 @@ Functions (all cite the ScaFFold pages' GroupNorm definition; see the C file):
   backward_at(..., idx)                        -> dx64 at indices, dgamma, dbeta
   round_bf16(v64) -> uint16 bit patterns (RNE straight from fp64)
   round_f32(v64)  -> float32 (RNE)
+Channels-last (NDHWC) tensors: the same GroupNorm of the same logical tensor,
+only stored position-major (element (n, c, s) at flat index (n*S + s)*C + c).
+  ndhwc_to_ncdhw(a, N, C, S) / ncdhw_to_ndhwc(a, N, C, S)  -> the layout change
+  ndhwc_index(idx, N, C, S)  -> NCDHW flat indices of NDHWC flat indices
+  forward_ndhwc / backward_ndhwc / backward_relu_ndhwc  -> as above, NDHWC in/out
 """
 from __future__ import annotations
 
@@ -213,3 +218,47 @@ def round_f32(v):
     out = np.empty(v.shape, dtype=np.float32)
     _load().gn3d_oracle_round_f32(_ptr(v), v.size, _ptr(out))
     return out
+
+
+# ------------------------------------------------------- channels-last layout
+# GroupNorm is defined on the logical tensor [N, C, D, H, W]; a channels-last
+# (NDHWC) tensor is the same tensor stored position-major.  These adapters only
+# move elements between the two storage orders and call the functions above.
+
+def ndhwc_to_ncdhw(a, N, C, S):
+    """Flat NDHWC storage -> flat NCDHW storage (same values, same dtype)."""
+    return np.ascontiguousarray(np.asarray(a).reshape(N, S, C).transpose(0, 2, 1)).reshape(-1)
+
+
+def ncdhw_to_ndhwc(a, N, C, S):
+    """Flat NCDHW storage -> flat NDHWC storage."""
+    return np.ascontiguousarray(np.asarray(a).reshape(N, C, S).transpose(0, 2, 1)).reshape(-1)
+
+
+def ndhwc_index(idx, N, C, S):
+    """NCDHW flat index of each NDHWC flat index: (n*S + s)*C + c -> (n*C + c)*S + s."""
+    idx = np.asarray(idx, dtype=np.int64)
+    c = idx % C
+    ns = idx // C
+    n, s_ = ns // S, ns % S
+    return (n * C + c) * S + s_
+
+
+def forward_ndhwc(x, gamma, beta, N, C, S, G, eps):
+    """y64 (NDHWC), mean, rstd of GroupNorm of an NDHWC tensor."""
+    y, mean, rstd = forward(ndhwc_to_ncdhw(x, N, C, S), gamma, beta, N, C, S, G, eps)
+    return ncdhw_to_ndhwc(y, N, C, S), mean, rstd
+
+
+def backward_ndhwc(dy, x, mean, rstd, gamma, N, C, S, G, want_dx=True):
+    """dx64 (NDHWC), dgamma, dbeta of GroupNorm of an NDHWC tensor."""
+    dx, dgamma, dbeta = backward(ndhwc_to_ncdhw(dy, N, C, S), ndhwc_to_ncdhw(x, N, C, S), mean, rstd, gamma, N,
+                                 C, S, G, want_dx)
+    return (ncdhw_to_ndhwc(dx, N, C, S) if want_dx else None), dgamma, dbeta
+
+
+def backward_relu_ndhwc(dy, x, out, mean, rstd, gamma, N, C, S, G, want_dx=True):
+    """Backward of relu(GroupNorm(x)) for NDHWC tensors (out: the forward's result, NDHWC)."""
+    dx, dgamma, dbeta = backward_relu(ndhwc_to_ncdhw(dy, N, C, S), ndhwc_to_ncdhw(x, N, C, S),
+                                      ndhwc_to_ncdhw(out, N, C, S), mean, rstd, gamma, N, C, S, G, want_dx)
+    return (ncdhw_to_ndhwc(dx, N, C, S) if want_dx else None), dgamma, dbeta

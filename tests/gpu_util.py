@@ -86,3 +86,36 @@ def run_backward_relu(site: synth.Site, dy, x, out, mean, rstd, gamma):
                           site.G, code(site.dtype), dx.data_ptr(), dgamma.data_ptr(), dbeta.data_ptr(),
                           t.cuda.current_stream().cuda_stream)
     return dx, dgamma, dbeta
+
+
+# ------------------------------------------------ channels-last (NDHWC) runs
+# Inputs and outputs are flat NDHWC storage (element (n, c, s) at (n*S + s)*C + c).
+
+def run_forward_ndhwc(site: synth.Site, x, gamma, beta, out_dtype: str | None = None, relu: bool = False):
+    t = torch()
+    out_dtype = out_dtype or site.dtype
+    y = t.empty(site.numel, dtype=t.bfloat16 if out_dtype == synth.BF16 else t.float32, device=x.device)
+    mean = t.empty(site.N * site.G, dtype=t.float32, device=x.device)
+    rstd = t.empty(site.N * site.G, dtype=t.float32, device=x.device)
+    fn = gn.gn3d_forward_ndhwc_relu if relu else gn.gn3d_forward_ndhwc
+    fn(x.data_ptr(), None if gamma is None else gamma.data_ptr(), None if beta is None else beta.data_ptr(),
+       site.N, site.C, site.D, site.H, site.W, site.G, site.eps, code(site.dtype), code(out_dtype), y.data_ptr(),
+       mean.data_ptr(), rstd.data_ptr(), t.cuda.current_stream().cuda_stream)
+    return y, mean, rstd
+
+
+def run_backward_ndhwc(site: synth.Site, dy, x, mean, rstd, gamma, out=None):
+    t = torch()
+    dx = t.empty_like(x)
+    dgamma = t.empty(site.C, dtype=t.float32, device=x.device)
+    dbeta = t.empty(site.C, dtype=t.float32, device=x.device)
+    g = None if gamma is None else gamma.data_ptr()
+    st = t.cuda.current_stream().cuda_stream
+    args = (site.N, site.C, site.D, site.H, site.W, site.G, code(site.dtype), dx.data_ptr(), dgamma.data_ptr(),
+            dbeta.data_ptr(), st)
+    if out is None:
+        gn.gn3d_backward_ndhwc(dy.data_ptr(), x.data_ptr(), mean.data_ptr(), rstd.data_ptr(), g, *args)
+    else:
+        gn.gn3d_backward_ndhwc_relu(dy.data_ptr(), x.data_ptr(), out.data_ptr(), mean.data_ptr(), rstd.data_ptr(),
+                                    g, *args)
+    return dx, dgamma, dbeta

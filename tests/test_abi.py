@@ -76,6 +76,31 @@ def test_invalid_shapes_rejected(L, shape):
     assert rc == gn.ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("shape", BAD_SHAPES)
+def test_invalid_shapes_rejected_ndhwc(L, shape):
+    s = shape
+    rc = L.gn3d_forward_ndhwc(None, None, None, s["N"], s["C"], s["D"], s["H"], s["W"], s["G"], 1e-5, gn.BF16,
+                              gn.BF16, None, None, None, None)
+    assert rc == gn.ERR_INVALID_ARG
+    rc = L.gn3d_backward_ndhwc(None, None, None, None, None, s["N"], s["C"], s["D"], s["H"], s["W"], s["G"], gn.BF16,
+                               None, None, None, None)
+    assert rc == gn.ERR_INVALID_ARG
+
+
+def test_ndhwc_needs_channels_multiple_of_8(L):
+    rc = L.gn3d_forward_ndhwc(None, None, None, 1, 12, 2, 2, 2, 4, 1e-5, gn.BF16, gn.BF16, None, None, None, None)
+    assert rc == gn.ERR_INVALID_ARG
+    assert "C % 8" in L.gn3d_error_string(rc).decode()
+    rc = L.gn3d_forward_ndhwc_relu(None, None, None, 1, 12, 2, 2, 2, 4, 1e-5, gn.BF16, gn.BF16, None, None, None,
+                                   None)
+    assert rc == gn.ERR_INVALID_ARG
+    rc = L.gn3d_backward_ndhwc(None, None, None, None, None, 1, 20, 2, 2, 2, 5, gn.F32, None, None, None, None)
+    assert rc == gn.ERR_INVALID_ARG
+    rc = L.gn3d_backward_ndhwc_relu(None, None, None, None, None, None, 1, 20, 2, 2, 2, 5, gn.F32, None, None, None,
+                                    None)
+    assert rc == gn.ERR_INVALID_ARG
+
+
 def test_invalid_dtype_and_eps_rejected(L):
     assert L.gn3d_forward(None, None, None, 1, 4, 2, 2, 2, 2, 1e-5, 7, gn.BF16, None, None, None, None) == 1
     assert L.gn3d_forward(None, None, None, 1, 4, 2, 2, 2, 2, -1.0, gn.BF16, gn.BF16, None, None, None, None) == 1

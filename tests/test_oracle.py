@@ -410,3 +410,67 @@ def test_backward_relu_matches_finite_differences(orc):
         xm[i] -= np.float32(h)
         gx[i] = (L(xp) - L(xm)) / (2 * h)
     assert np.max(np.abs(dx - gx)) <= 1e-7 * np.max(np.abs(gx))
+
+
+# ------------------------------------------------------ channels-last layout
+
+def test_ndhwc_layout_brute_force(orc):
+    """The NDHWC adapters read element (n, c, s) at flat index (n*S + s)*C + c:
+    group statistics and y recomputed here by loops over that index formula
+    (a transposed reading would mix positions into channels and fail)."""
+    rng = np.random.default_rng(30)
+    N, C, S, G = 2, 6, 5, 3
+    Cg = C // G
+    xcl = (rng.standard_normal(N * S * C) + np.arange(N * S * C) % C).astype(np.float32)  # channel-dependent means
+    gamma = rng.uniform(0.5, 1.5, C).astype(np.float32)
+    beta = rng.standard_normal(C).astype(np.float32)
+    y, mean, rstd = orc.forward_ndhwc(xcl, gamma, beta, N, C, S, G, 1e-5)
+    for n in range(N):
+        for g in range(G):
+            vals = [float(xcl[(n * S + s) * C + c]) for s in range(S) for c in range(g * Cg, (g + 1) * Cg)]
+            mu = sum(vals) / len(vals)
+            var = sum((v - mu) ** 2 for v in vals) / len(vals)
+            assert abs(mean[n * G + g] - mu) < 1e-12
+            assert abs(rstd[n * G + g] - 1.0 / np.sqrt(var + EPS32)) < 1e-10
+            for s in range(S):
+                for c in range(g * Cg, (g + 1) * Cg):
+                    i = (n * S + s) * C + c
+                    ref = (float(xcl[i]) - mu) / np.sqrt(var + EPS32) * float(gamma[c]) + float(beta[c])
+                    assert abs(y[i] - ref) < 1e-10
+
+
+def test_ndhwc_matches_torch_channels_last_float64(orc):
+    """Forward and backward against torch's float64 CPU GroupNorm run on a
+    channels_last_3d tensor (torch's own channels-last kernel) and its autograd."""
+    rng = np.random.default_rng(31)
+    N, C, D, H, W, G = 2, 16, 3, 4, 5, 4
+    S = D * H * W
+    x, gamma, beta, dy = rand_case(rng, N, C, S, G, scale=2.0, offset=0.5)
+    xt = torch.from_numpy(x.astype(np.float64)).reshape(N, C, D, H, W).contiguous(
+        memory_format=torch.channels_last_3d).requires_grad_(True)
+    gt = torch.from_numpy(gamma.astype(np.float64)).requires_grad_(True)
+    bt = torch.from_numpy(beta.astype(np.float64)).requires_grad_(True)
+    yt = F.group_norm(xt, G, gt, bt, EPS32)
+    dyt = torch.from_numpy(dy.astype(np.float64)).reshape(N, C, D, H, W).contiguous(
+        memory_format=torch.channels_last_3d)
+    yt.backward(dyt)
+    # channels-last storage of everything (torch keeps the memory format)
+    xcl = orc.ncdhw_to_ndhwc(x, N, C, S)
+    dycl = orc.ncdhw_to_ndhwc(dy, N, C, S)
+    y, mean, rstd = orc.forward_ndhwc(xcl, gamma, beta, N, C, S, G, EPS32)
+    ycl_t = yt.detach().permute(0, 2, 3, 4, 1).reshape(-1).numpy()
+    assert np.allclose(y, ycl_t, rtol=1e-12, atol=1e-12)
+    dx, dgamma, dbeta = orc.backward_ndhwc(dycl, xcl, mean, rstd, gamma, N, C, S, G)
+    assert np.allclose(dx, xt.grad.permute(0, 2, 3, 4, 1).reshape(-1).numpy(), rtol=1e-10, atol=1e-12)
+    assert np.allclose(dgamma, gt.grad.numpy(), rtol=1e-10, atol=1e-12)
+    assert np.allclose(dbeta, bt.grad.numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_ndhwc_index_and_permutations_agree(orc):
+    rng = np.random.default_rng(32)
+    N, C, S = 3, 8, 7
+    a = rng.standard_normal(N * C * S)
+    cl = orc.ncdhw_to_ndhwc(a, N, C, S)
+    assert np.array_equal(orc.ndhwc_to_ncdhw(cl, N, C, S), a)
+    idx = np.arange(N * C * S)
+    assert np.array_equal(a[orc.ndhwc_index(idx, N, C, S)], cl)
