@@ -276,7 +276,8 @@ def gn3d_debug_set(what: int, value: int):
 
 
 KERNELS = ("k_fwd_fused", "k_bwd_fused", "k_fwd_stats", "k_fwd_norm", "k_bwd_reduce", "k_bwd_dx",
-           "k_ndhwc_stats", "k_ndhwc_norm", "k_ndhwc_reduce", "k_ndhwc_dx")
+           "k_ndhwc_stats", "k_ndhwc_stats_final", "k_ndhwc_norm", "k_ndhwc_reduce", "k_ndhwc_reduce_final",
+           "k_ndhwc_dx")
 
 
 def gn3d_kernel_time(name: str):

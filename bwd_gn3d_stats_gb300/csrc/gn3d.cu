@@ -153,11 +153,12 @@ int64_t rup(int64_t b) { return ((b + 255) / 256) * 256; }
 // CUDA events on its stream; gn3d_kernel_time resolves them per kernel.
 enum {
   KK_FWD_FUSED, KK_BWD_FUSED, KK_FWD_STATS, KK_FWD_NORM, KK_BWD_REDUCE, KK_BWD_DX,
-  KK_N_STATS, KK_N_NORM, KK_N_REDUCE, KK_N_DX, KK_COUNT
+  KK_N_STATS, KK_N_STATS_FINAL, KK_N_NORM, KK_N_REDUCE, KK_N_REDUCE_FINAL, KK_N_DX, KK_COUNT
 };
-const char* const kKernelNames[KK_COUNT] = {"k_fwd_fused",   "k_bwd_fused",  "k_fwd_stats",    "k_fwd_norm",
-                                            "k_bwd_reduce",  "k_bwd_dx",     "k_ndhwc_stats",  "k_ndhwc_norm",
-                                            "k_ndhwc_reduce", "k_ndhwc_dx"};
+const char* const kKernelNames[KK_COUNT] = {
+    "k_fwd_fused",   "k_bwd_fused",         "k_fwd_stats",  "k_fwd_norm",     "k_bwd_reduce",
+    "k_bwd_dx",      "k_ndhwc_stats",       "k_ndhwc_stats_final", "k_ndhwc_norm", "k_ndhwc_reduce",
+    "k_ndhwc_reduce_final", "k_ndhwc_dx"};
 std::atomic<int> g_timing{0};
 std::mutex g_tmu;
 struct TimedLaunch {
@@ -450,44 +451,54 @@ int launch_backward(const void* dy, const void* x, const void* res, const float*
 }
 
 // ---------------------------------------------------- channels-last (NDHWC)
-// Statistics then normalize (dependent launch), and reduction then dx, each pair
-// on one grid of min(SMs, units) CTAs (gn3d_ndhwc.cuh).
+// Three dependent launches per direction (gn3d_ndhwc.cuh): the streaming
+// reduction on min(SMs, units) CTAs, the finalize (one CTA per group / per row),
+// then the elementwise pass on the reduction's grid.
 template <class TI, class TO>
 int launch_forward_ndhwc(const void* x, const float* gamma, const float* beta, const NPlan& p, float eps, void* y,
                          float* mean, float* rstd, cudaStream_t st, DevInfo& di, bool relu) {
-  const int64_t nsync = p.nblk + 1;  // block counters, finished CTAs
-  const int64_t bytes = rup(nsync * 4) + rup(p.rows * p.P * p.R * (int64_t)sizeof(Part)) +
-                        rup(p.rows * p.P * p.nb * (int64_t)sizeof(Part)) + rup(p.NG * (int64_t)sizeof(float4));
+  const int64_t tasks = p.NG * n_fin_maxr(p) * n_fin_nkc(p);  // finalize chunks
+  const int64_t bytes = rup(p.NG * 4) + rup(p.rows * p.P * p.R * (int64_t)sizeof(Part)) +
+                        rup(tasks * (int64_t)sizeof(Part)) + rup(p.NG * (int64_t)sizeof(float4));
   Scratch s;
   GN3D_CUDA(cudaMallocFromPoolAsync(&s.base, (size_t)bytes, di.pool, st), "scratch allocation");
   s.cur = static_cast<char*>(s.base);
-  uint32_t* sync = s.take<uint32_t>(nsync);
   NFwdWs w;
-  w.bcnt = sync;
-  w.done = sync + p.nblk;
+  w.gcnt = s.take<uint32_t>(p.NG);
   w.upart = s.take<Part>(p.rows * p.P * p.R);
-  w.bpart = s.take<Part>(p.rows * p.P * p.nb);
+  w.fpart = s.take<Part>(tasks);
   w.stats = s.take<float4>(p.NG);
-  cudaError_t e = cudaMemsetAsync(sync, 0, (size_t)nsync * sizeof(uint32_t), st);
   const TI* xp = static_cast<const TI*>(x);
   TO* yp = static_cast<TO*>(y);
-  const int smem = kNRedWarps * kNSpan * kNVec * (int)sizeof(Part);  // per warp: one unit's channel partials
-  auto ks = k_ndhwc_stats<TI>;
-  int rc = raise_smem((const void*)ks, smem, di);
+  // one channel range: the bulk-copy ring kernel; else the direct one (per warp:
+  // one unit's channel partials in shared memory, plus the ring's slots)
+  const bool ring = p.nr == 1;
+  const int smem = ring ? NStatRing<TI>::kSmem : kNRedWarps * kNSpan * kNVec * (int)sizeof(Part);
+  const void* kfn = ring ? (const void*)k_ndhwc_stats_ring<TI> : (const void*)k_ndhwc_stats<TI>;
+  int rc = raise_smem(kfn, smem, di);
   if (rc) { cudaFreeAsync(s.base, st); return rc; }
   const int grid = grid_for(di, p.units, 1);
+  cudaError_t e = cudaMemsetAsync(w.gcnt, 0, (size_t)p.NG * sizeof(uint32_t), st);
   if (e == cudaSuccess) {
-    g_launches += 2;
+    g_launches += 3;
     LaunchTimer t1(KK_N_STATS, st, di);
-    ks<<<grid, 32 * kNRedWarps, smem, st>>>(xp, p, w, eps, mean, rstd);
+    if (ring)
+      k_ndhwc_stats_ring<TI><<<grid, 32 * kNRedWarps, smem, st>>>(xp, p, w, spin_budget(), di.status);
+    else
+      k_ndhwc_stats<TI><<<grid, 32 * kNRedWarps, smem, st>>>(xp, p, w);
     t1.done();
     e = cudaGetLastError();
   }
   if (e == cudaSuccess) {
-    LaunchTimer t2(KK_N_NORM, st, di);
+    LaunchTimer t2(KK_N_STATS_FINAL, st, di);
+    e = launch_dependent(k_ndhwc_stats_final, grid_for(di, tasks, 4), kNFinThreads, st, p, w, eps, mean, rstd);
+    t2.done();
+  }
+  if (e == cudaSuccess) {
+    LaunchTimer t3(KK_N_NORM, st, di);
     auto kn = relu ? k_ndhwc_norm<TI, TO, true> : k_ndhwc_norm<TI, TO, false>;
     e = launch_dependent(kn, grid, 32 * kNElemWarps, st, xp, yp, p, (const float4*)w.stats, gamma, beta);
-    t2.done();
+    t3.done();
   }
   cudaError_t ef = cudaFreeAsync(s.base, st);
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
@@ -499,20 +510,20 @@ template <class T>
 int launch_backward_ndhwc(const void* dy, const void* x, const void* res, const float* mean, const float* rstd,
                           const float* gamma, const NPlan& p, void* dx, float* dgamma, float* dbeta, cudaStream_t st,
                           DevInfo& di) {
-  const int64_t nsync = p.nblk + 1;
-  const int64_t NC = p.N * p.C;
+  const int64_t NC = p.N * p.C, tasks = NC * n_fin_nkc(p);
+  const int64_t nsync = NC + 1;  // chunks done per row, rows done
   const int64_t bytes = rup(nsync * 4) + rup(NC * p.R * (int64_t)sizeof(float2)) +
-                        rup(NC * p.nb * (int64_t)sizeof(float2)) + rup(NC * (int64_t)sizeof(float2)) +
+                        rup(tasks * (int64_t)sizeof(float2)) + rup(NC * (int64_t)sizeof(float2)) +
                         rup(p.NG * (int64_t)sizeof(float2));
   Scratch s;
   GN3D_CUDA(cudaMallocFromPoolAsync(&s.base, (size_t)bytes, di.pool, st), "scratch allocation");
   s.cur = static_cast<char*>(s.base);
-  uint32_t* sync = s.take<uint32_t>(nsync);
   NBwdWs w;
-  w.bcnt = sync;
-  w.done = sync + p.nblk;
+  uint32_t* sync = s.take<uint32_t>(nsync);
+  w.rcnt = sync;
+  w.done = sync + NC;
   w.usum = s.take<float2>(NC * p.R);
-  w.bsum = s.take<float2>(NC * p.nb);
+  w.rpart = s.take<float2>(tasks);
   w.rows = s.take<float2>(NC);
   w.coef = s.take<float2>(p.NG);
   cudaError_t e = cudaMemsetAsync(sync, 0, (size_t)nsync * sizeof(uint32_t), st);
@@ -521,22 +532,41 @@ int launch_backward_ndhwc(const void* dy, const void* x, const void* res, const 
   const T* resp = static_cast<const T*>(res);
   T* dxp = static_cast<T*>(dx);
   const int grid = grid_for(di, p.units, 1);
+  const bool ring = p.nr == 1;  // one channel range: the bulk-copy ring kernel
+  if (ring) {
+    const int smem = res ? NRedRing<T, true>::kSmem : NRedRing<T, false>::kSmem;
+    int rc = raise_smem(res ? (const void*)k_ndhwc_reduce_ring<T, true> : (const void*)k_ndhwc_reduce_ring<T, false>,
+                        smem, di);
+    if (rc) { cudaFreeAsync(s.base, st); return rc; }
+  }
   if (e == cudaSuccess) {
-    g_launches += 2;
+    g_launches += 3;
     LaunchTimer t1(KK_N_REDUCE, st, di);
-    if (res)
-      k_ndhwc_reduce<T, true><<<grid, 32 * kNRedWarps, 0, st>>>(dyp, xp, resp, p, mean, rstd, gamma, w, dgamma, dbeta);
+    const unsigned long long spin = spin_budget();
+    if (ring && res)
+      k_ndhwc_reduce_ring<T, true><<<grid, 32 * kNRedWarps, NRedRing<T, true>::kSmem, st>>>(dyp, xp, resp, p, mean, w,
+                                                                                            spin, di.status);
+    else if (ring)
+      k_ndhwc_reduce_ring<T, false><<<grid, 32 * kNRedWarps, NRedRing<T, false>::kSmem, st>>>(dyp, xp, nullptr, p,
+                                                                                              mean, w, spin, di.status);
+    else if (res)
+      k_ndhwc_reduce<T, true><<<grid, 32 * kNRedWarps, 0, st>>>(dyp, xp, resp, p, mean, w);
     else
-      k_ndhwc_reduce<T, false><<<grid, 32 * kNRedWarps, 0, st>>>(dyp, xp, nullptr, p, mean, rstd, gamma, w, dgamma,
-                                                              dbeta);
+      k_ndhwc_reduce<T, false><<<grid, 32 * kNRedWarps, 0, st>>>(dyp, xp, nullptr, p, mean, w);
     t1.done();
     e = cudaGetLastError();
   }
   if (e == cudaSuccess) {
-    LaunchTimer t2(KK_N_DX, st, di);
+    LaunchTimer t2(KK_N_REDUCE_FINAL, st, di);
+    e = launch_dependent(k_ndhwc_reduce_final, grid_for(di, tasks, 4), kNFinThreads, st, p, w, rstd, gamma, dgamma,
+                         dbeta);
+    t2.done();
+  }
+  if (e == cudaSuccess) {
+    LaunchTimer t3(KK_N_DX, st, di);
     auto kd = res ? k_ndhwc_dx<T, true> : k_ndhwc_dx<T, false>;
     e = launch_dependent(kd, grid, 32 * kNElemWarps, st, dyp, xp, resp, dxp, p, mean, rstd, gamma, (const float2*)w.coef);
-    t2.done();
+    t3.done();
   }
   cudaError_t ef = cudaFreeAsync(s.base, st);
   if (e != cudaSuccess) return cuda_fail(e, "backward launch");

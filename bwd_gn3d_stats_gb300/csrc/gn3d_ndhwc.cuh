@@ -15,15 +15,17 @@
 // slice when vr = 32) and each lane keeps the same 8 channels throughout
 // (lanes >= lp*vr idle).
 //
-// Units, blocks, groups.  Row (n, r) -- sample n, range r -- is cut into units of
+// Units and groups.  Row (n, r) -- sample n, range r -- is cut into units of
 // Pu = kNSteps * lp0 positions (lp0: the lp of range 0, the widest), one warp
-// per unit, at most kNSteps vectors per lane.  B consecutive units of a row form
-// a merge block.  Statistics merge in a fixed tree that depends on the shape
-// alone: lane -> channel (the lp lanes of a channel, pairwise) -> piece (the
-// channels of one group inside the range) per unit -> piece per block (the
-// warp that completes the block) -> group (the last CTA to finish).  The
-// backward keeps per-channel sums (the weight gradient needs them): unit ->
-// block -> row (n, c) -> group coefficients and parameter gradients.
+// per unit, at most kNSteps vectors per lane.  Statistics merge in a fixed tree
+// that depends on the shape alone: lane -> channel (the lp lanes of a channel,
+// pairwise) -> piece (the channels of one group inside the range), per unit,
+// in the streaming kernel; the pieces -> group in a finalize kernel, one CTA per
+// group.  The backward keeps per-channel sums (the weight gradient needs them):
+// unit -> row (n, c), one CTA per row -> group coefficients and parameter
+// gradients.  The streaming kernels only store their unit results: a round trip
+// to L2 (an arrival counter, a merge's loads) costs microseconds while the
+// stream saturates DRAM, and a warp that waits for one falls behind.
 //
 // Every floating-point step uses the round-to-nearest intrinsics of
 // gn3d_device.cuh, so the result bits depend on the shape only.
@@ -36,20 +38,19 @@ namespace gn3d {
 
 // ------------------------------------------------------------- workspaces
 struct NFwdWs {
-  Part* upart;     // [rows][P][R]  unit pieces
-  Part* bpart;     // [rows][P][nb] block pieces
-  float4* stats;   // [NG] (mean hi, mean lo, rstd, 0)
-  uint32_t* bcnt;  // [nblk] unit arrivals per block
-  uint32_t* done;  // [1] CTAs finished
+  Part* upart;     // [rows][P][R]       unit pieces
+  Part* fpart;     // [NG][maxr * nkc]   finalize chunk partials
+  uint32_t* gcnt;  // [NG]               finalize chunks done per group
+  float4* stats;   // [NG]               (mean hi, mean lo, rstd, 0)
 };
 
 struct NBwdWs {
-  float2* usum;    // [N*C][R]  unit sums per channel (S1, S2)
-  float2* bsum;    // [N*C][nb] block sums per channel
-  float2* rows;    // [N*C]     row totals
-  float2* coef;    // [NG]      (a, b)
-  uint32_t* bcnt;  // [nblk]
-  uint32_t* done;  // [1]
+  float2* usum;    // [N*C][R]    unit sums per channel (S1, S2)
+  float2* rpart;   // [N*C][nkc]  finalize chunk sums
+  uint32_t* rcnt;  // [N*C]       finalize chunks done per row
+  float2* rows;    // [N*C]       row totals
+  float2* coef;    // [NG]        (a, b)
+  uint32_t* done;  // [1]         rows finished
 };
 
 // ------------------------------------------------------------- lane sums
@@ -58,9 +59,9 @@ struct NBwdWs {
 template <class T, bool kRelu = false> struct NBatch {
   static constexpr int kRaw = Vec<T>::kRaw;
   static constexpr int kStats = 16 / kRaw;
-  static constexpr int kNorm = 8 / kRaw;
+  static constexpr int kNorm = 16 / kRaw;
   static constexpr int kReduce = (kRelu ? 4 : 8) / kRaw;
-  static constexpr int kDx = (kRelu ? 2 : 4) / kRaw;
+  static constexpr int kDx = (kRelu ? 4 : 8) / kRaw;
 };
 
 // (v - k) for the 8 elements of a vector as pairs, each pair with its own shift.
@@ -79,121 +80,139 @@ __device__ __forceinline__ float n_slot(const f2 a[4], int s) { return s & 1 ? f
 // vectors); the rest by the first chunk's mean.  With shift K and d = x - K,
 // a chunk's sums c = sum d, q = sum d^2 give M2 = q - c*(c/n); a shift that is
 // the mean of a quarter of the chunk keeps q <= 5 M2 (Cauchy-Schwarz), and the
-// second chunk, shifted by the mean of the first 16 of its up to 64 elements,
-// the same bound (ScaFFold PR #93: per-tile corrected two-pass partials merged
+// rest, shifted by the mean of the first 16 of the lane's up to kNSteps
+// elements, q <= (kNSteps / 16 + 1) M2 (ScaFFold PR #93: per-tile corrected two-pass partials merged
 // with Chan's formula; here the pass is one, the correction its shift).
-// Returns the 8 slot partials as (m1, cn, m2) pairs and the count.
+// The vectors arrive in batches of kB consecutive steps (kB divides kNChunk),
+// from global memory or from a shared-memory slot; the arithmetic is the same.
 template <class T>
-__device__ __forceinline__ int n_lane_moments(const T* __restrict__ x, const NUnit& q, f2 m1[4], f2 cn[4],
-                                              f2 m2[4]) {
-  constexpr int kB = NBatch<T>::kStats, kRaw = Vec<T>::kRaw;
-  const f2 z2 = f2_splat(0.f);
-  const T* base = x + q.off;
-  const int cnt = q.cnt;
-  const int nA = cnt < kNChunk ? cnt : kNChunk;
-  f2 K[4] = {z2, z2, z2, z2}, c[4] = {z2, z2, z2, z2}, s2[4] = {z2, z2, z2, z2};
+struct NMoments {
+  f2 K[4], c[4], s2[4];  // the current chunk: shift and sums
+  f2 m1[4], cn[4], m2[4];  // the first chunk's partial, then the lane's (pairs of channels)
+  int nA = 0;
+
+  // Steps t0 .. t0 + nv - 1 of the lane (nv >= 1), w[t] holding step t0 + t.
+  template <int kB>
+  __device__ __forceinline__ void batch(const uint4 (&w)[kB][Vec<T>::kRaw], int t0, int nv, int cnt) {
+    static_assert(kNChunk % kB == 0 && kB >= kNPilot, "batches inside chunks, the pilot in the first");
+    const f2 z2 = f2_splat(0.f);
+    if (t0 == 0) {
+      f2 pa[4] = {z2, z2, z2, z2};
 #pragma unroll
-  for (int t0 = 0; t0 < kNChunk; t0 += kB) {
-    if (t0 < nA) {
-      uint4 w[kB][kRaw];
+      for (int t = 0; t < kNPilot; ++t) {
+        if (t < nv) {
+          f2 v[4];
+          Vec<T>::pairs(w[t], v);
 #pragma unroll
-      for (int t = 0; t < kB; ++t)
-        if (t0 + t < nA) Vec<T>::template load<FromGlobal>(base + (int64_t)(t0 + t) * q.step, w[t]);
-      if (t0 == 0) {
-        f2 pa[4] = {z2, z2, z2, z2};
-#pragma unroll
-        for (int t = 0; t < kNPilot; ++t) {
-          if (t < nA) {
-            f2 v[4];
-            Vec<T>::pairs(w[t], v);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) pa[e] = f2add(pa[e], v[e]);
-          }
+          for (int e = 0; e < 4; ++e) pa[e] = f2add(pa[e], v[e]);
         }
-        const int np = nA < kNPilot ? nA : kNPilot;
-        const f2 inv = f2_splat(np == kNPilot ? 1.f / (float)kNPilot : __frcp_rn((float)np));
-#pragma unroll
-        for (int e = 0; e < 4; ++e) K[e] = f2fma(pa[e], inv, z2);
       }
+      const int np = nv < kNPilot ? nv : kNPilot;
+      const f2 inv = f2_splat(np == kNPilot ? 1.f / (float)kNPilot : __frcp_rn((float)np));
 #pragma unroll
-      for (int t = 0; t < kB; ++t) {
-        if (t0 + t < nA) {
-          f2 d[4];
-          n_diff<T>(w[t], K, d);
+      for (int e = 0; e < 4; ++e) {
+        K[e] = f2fma(pa[e], inv, z2);
+        c[e] = z2;
+        s2[e] = z2;
+      }
+    }
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            c[e] = f2add(c[e], d[e]);
-            s2[e] = f2fma(d[e], d[e], s2[e]);
-          }
+    for (int t = 0; t < kB; ++t) {
+      if (t < nv) {
+        f2 d[4];
+        n_diff<T>(w[t], K, d);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          c[e] = f2add(c[e], d[e]);
+          s2[e] = f2fma(d[e], d[e], s2[e]);
         }
       }
     }
-  }
-  if (nA == 0) {
+    // the first chunk ends with step min(cnt, kNChunk) - 1: its partial, and the
+    // rest's shift (its mean)
+    const int endA = cnt < kNChunk ? cnt : kNChunk;
+    if (t0 < kNChunk && t0 + nv >= endA) {
+      nA = endA;
+      const f2 invA = f2_splat(nA == kNChunk ? 1.f / (float)kNChunk : __frcp_rn((float)nA));
 #pragma unroll
-    for (int e = 0; e < 4; ++e) m1[e] = cn[e] = m2[e] = z2;
-    return 0;
-  }
-  // the first chunk's partial
-  const f2 invA = f2_splat(nA == kNChunk ? 1.f / (float)kNChunk : __frcp_rn((float)nA));
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    m1[e] = K[e];
-    cn[e] = f2fma(c[e], invA, z2);
-    m2[e] = f2sub(s2[e], f2fma(c[e], cn[e], z2));
-  }
-  if (cnt > nA) {
-    // the rest, shifted by the first chunk's mean
-    f2 K2[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      K2[e] = f2add(m1[e], cn[e]);
-      c[e] = z2;
-      s2[e] = z2;
-    }
-    for (int t0 = kNChunk; t0 < cnt; t0 += kB) {
-      uint4 w[kB][kRaw];
-#pragma unroll
-      for (int t = 0; t < kB; ++t)
-        if (t0 + t < cnt) Vec<T>::template load<FromGlobal>(base + (int64_t)(t0 + t) * q.step, w[t]);
-#pragma unroll
-      for (int t = 0; t < kB; ++t) {
-        if (t0 + t < cnt) {
-          f2 d[4];
-          n_diff<T>(w[t], K2, d);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            c[e] = f2add(c[e], d[e]);
-            s2[e] = f2fma(d[e], d[e], s2[e]);
-          }
-        }
+      for (int e = 0; e < 4; ++e) {
+        m1[e] = K[e];
+        cn[e] = f2fma(c[e], invA, z2);
+        m2[e] = f2sub(s2[e], f2fma(c[e], cn[e], z2));
+        K[e] = f2add(m1[e], cn[e]);
+        c[e] = z2;
+        s2[e] = z2;
       }
     }
-    // merge: the first chunk's terms about K2, plus the rest's sums
+  }
+
+  // After every step: the lane's partial of each channel in (m1, cn, m2); count cnt.
+  __device__ __forceinline__ void finish(int cnt) {
+    const f2 z2 = f2_splat(0.f);
+    if (cnt == 0) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) m1[e] = cn[e] = m2[e] = z2;
+      return;
+    }
+    if (cnt == nA) return;
+    // merge: the first chunk's terms about the rest's shift K, plus the rest's sums
     const f2 fa = f2_splat((float)nA);
     const f2 inv = f2_splat(cnt == kNSteps ? 1.f / (float)kNSteps : __frcp_rn((float)cnt));
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const f2 d = f2add(f2sub(m1[e], K2[e]), cn[e]);
+      const f2 d = f2add(f2sub(m1[e], K[e]), cn[e]);
       const f2 nd = f2fma(fa, d, z2);
       const f2 S = f2add(nd, c[e]);
       const f2 Q = f2add(f2fma(nd, d, m2[e]), s2[e]);
-      m1[e] = K2[e];
+      m1[e] = K[e];
       cn[e] = f2fma(S, inv, z2);
       m2[e] = f2sub(Q, f2fma(S, cn[e], z2));
     }
   }
-  return cnt;
+};
+
+// The direct form: the lane's vectors read from global memory, kB at a time.
+template <class T>
+__device__ __forceinline__ void n_lane_moments(const T* __restrict__ x, const NUnit& q, NMoments<T>& mom) {
+  constexpr int kB = NBatch<T>::kStats, kRaw = Vec<T>::kRaw;
+  const T* base = x + q.off;
+  for (int t0 = 0; t0 < q.cnt; t0 += kB) {
+    const int nv = q.cnt - t0 < kB ? q.cnt - t0 : kB;
+    uint4 w[kB][kRaw];
+#pragma unroll
+    for (int t = 0; t < kB; ++t)
+      if (t < nv) Vec<T>::template load<FromGlobal>(base + (int64_t)(t0 + t) * q.step, w[t]);
+    mom.batch(w, t0, nv, q.cnt);
+  }
+  mom.finish(q.cnt);
 }
 
-// Sum over the lp lanes that share a vector b (lane m*vr + b), pairwise over m;
-// the totals land in the m = 0 lanes.  All 32 lanes call.
-__device__ __forceinline__ float n_msum(float v, const NRange& rg, int m) {
+// Sums over the lp lanes that share a vector b (lane m*vr + b), pairwise over
+// m, of kV values at once (the shuffles of one level issue together); the
+// totals land in the m = 0 lanes.  All 32 lanes call.
+template <int kV>
+__device__ __forceinline__ void n_msum(float (&v)[kV], const NRange& rg, int m) {
   for (int s = 1; s < rg.lp; s <<= 1) {
-    const float o = __shfl_down_sync(kFull, v, s * rg.vr);
-    if ((m & (2 * s - 1)) == 0 && m + s < rg.lp) v = fadd(v, o);
+    float o[kV];
+#pragma unroll
+    for (int i = 0; i < kV; ++i) o[i] = __shfl_down_sync(kFull, v[i], s * rg.vr);
+    if ((m & (2 * s - 1)) == 0 && m + s < rg.lp) {
+#pragma unroll
+      for (int i = 0; i < kV; ++i) v[i] = fadd(v[i], o[i]);
+    }
   }
-  return v;
+}
+
+// The merged partial from shift K and sums S, Q over n elements, with inv = 1/n
+// (rounded; exact when n is a power of two).
+__device__ __forceinline__ Part n_finish(float K, float S, float Q, int n, float inv) {
+  Part r;
+  r.m1 = K;
+  r.n = n;
+  r.cn = fmul(S, inv);
+  r.m2 = fsub(Q, fmul(S, r.cn));
+  if (r.m2 < 0.f) r.m2 = 0.f;
+  return r;
 }
 
 __device__ __forceinline__ float n_shifted_s(float m1, float cn, int n, float K, float& Q, float m2) {
@@ -274,102 +293,6 @@ __device__ __forceinline__ void n_unit_pieces(const NPlan& p, const NUnit& q, co
   }
 }
 
-// Sum over the B lanes of a segment (lanes cl*B .. cl*B + B - 1, B a power of
-// two): an xor butterfly inside the segment, every lane ends with the total.
-__device__ __forceinline__ float n_segsum(float v, int B) {
-  for (int o = B >> 1; o > 0; o >>= 1) v = fadd(v, __shfl_xor_sync(kFull, v, o));
-  return v;
-}
-
-// Block kb of row `row` is complete: merge each piece's unit partials into
-// bpart, by one warp.  The warp works as 32/B segments of B lanes, one piece
-// per segment, lane kk of a segment holding unit kk of the block.
-__device__ __forceinline__ void n_fwd_block(const NPlan& p, const NFwdWs& ws, int64_t row, int64_t kb) {
-  const int lane = threadIdx.x & 31, B = (int)p.B, per = 32 / B, cl = lane / B, kk = lane - cl * B;
-  const NRange rg = n_range(p, row % p.nr);
-  const int64_t np = rg.g1 - rg.g0 + 1;
-  const int bsz = n_block_size(p, kb);
-  const int64_t pos = n_block_positions(p, kb);
-  for (int64_t j0 = 0; j0 < np; j0 += (int64_t)per * kMergeBatch) {
-    Part v[kMergeBatch];
-#pragma unroll
-    for (int t = 0; t < kMergeBatch; ++t) {
-      const int64_t j = j0 + (int64_t)t * per + cl;
-      v[t] = j < np && kk < bsz ? ldcg_part(ws.upart + ((row * p.P + j) * p.R + kb * p.B + kk))
-                                : Part{0.f, 0.f, 0, 0.f};
-    }
-#pragma unroll
-    for (int t = 0; t < kMergeBatch; ++t) {
-      if (j0 + (int64_t)t * per >= np) break;
-      const int64_t j = j0 + (int64_t)t * per + cl;
-      const float K = __shfl_sync(kFull, fadd(v[t].m1, v[t].cn), cl * B);
-      float S, Q;
-      shifted_terms(v[t], K, S, Q);
-      S = n_segsum(S, B);
-      Q = n_segsum(Q, B);
-      if (kk == 0 && j < np) {
-        int64_t c0, c1;
-        n_piece(p, rg, j, c0, c1);
-        ws.bpart[(row * p.P + j) * p.nb + kb] = finish_merge(K, S, Q, pos * (c1 - c0));
-      }
-    }
-  }
-}
-
-// Group gi = n*G + g from its block pieces (every range the group meets, block
-// by block), by one warp: lane l takes parts l, l+32, ... in order.
-__device__ __forceinline__ void n_fwd_group(const NPlan& p, const NFwdWs& ws, int64_t gi, float eps, float* mean_out,
-                                            float* rstd_out) {
-  const int lane = threadIdx.x & 31;
-  const int64_t n = gi / p.G, g = gi - n * p.G;
-  const int64_t r_lo = (g * p.Cg) / (kNSpan * kVec), r_hi = ((g + 1) * p.Cg - 1) / (kNSpan * kVec);
-  const int64_t total = (r_hi - r_lo + 1) * p.nb;
-  auto at = [&](int64_t i) {
-    const int64_t r = r_lo + i / p.nb, kb = i - (i / p.nb) * p.nb;
-    const int64_t j = g - n_range(p, r).g0;
-    return ws.bpart + ((n * p.nr + r) * p.P + j) * p.nb + kb;
-  };
-  const Part b0 = ldcg_part(at(0));
-  const float K = fadd(b0.m1, b0.cn);
-  float S = 0.f, Q = 0.f;
-  for (int64_t i0 = lane; i0 < total; i0 += 32 * kMergeBatch) {
-    Part v[kMergeBatch];
-#pragma unroll
-    for (int t = 0; t < kMergeBatch; ++t)
-      if (i0 + 32 * t < total) v[t] = ldcg_part(at(i0 + 32 * t));
-#pragma unroll
-    for (int t = 0; t < kMergeBatch; ++t) {
-      if (i0 + 32 * t < total) {
-        float s, q;
-        shifted_terms(v[t], K, s, q);
-        S = fadd(S, s);
-        Q = fadd(Q, q);
-      }
-    }
-  }
-  const float2 tq = warp_sum2(S, Q);
-  const Part gp = finish_merge(K, tq.x, tq.y, p.M);
-  const float rs = __frsqrt_rn(fadd(__fdiv_rn(gp.m2, (float)p.M), eps));
-  if (lane == 0) {
-    ws.stats[gi] = make_float4(gp.m1, gp.cn, rs, 0.f);
-    if (mean_out) mean_out[gi] = fadd(gp.m1, gp.cn);
-    if (rstd_out) rstd_out[gi] = rs;
-  }
-}
-
-// Everything this CTA wrote is published; true in the last CTA to finish, which
-// then sees every other CTA's results.
-__device__ __forceinline__ bool n_last_cta(uint32_t* done) {
-  __shared__ uint32_t last;
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) last = atom_add_acq_rel(done, 1u) + 1u == gridDim.x ? 1u : 0u;
-  __syncthreads();
-  const bool l = last != 0;
-  if (l) __threadfence();
-  return l;
-}
-
 // Reduction warp w = warp*grid + cta takes units w, w + W, w + 2W, ... (W =
 // grid * kNRedWarps).  An elementwise warp takes the units of reduction warp
 // warp % kNRedWarps of the same CTA, last first, every kSplit-th: what that
@@ -392,9 +315,37 @@ struct NOwned {
   __device__ __forceinline__ void next() { t -= kSplit; }
 };
 
+// A unit's lane partials -> channel partials (the lp lanes of each channel,
+// shifted by the m = 0 lane's mean, summed pairwise) -> pieces, stored to upart.
+// Nothing waits here: the finalize kernel merges the pieces once every unit is
+// done, so the streaming warps never stop for a round trip to L2.
+template <class T>
+__device__ __forceinline__ void n_stats_unit_done(const NPlan& p, const NFwdWs& ws, const NUnit& q,
+                                                  const NMoments<T>& mom, Part* sp) {
+  const int lane = threadIdx.x & 31;
+  float K[8], v[16];  // v: S of the 8 channels, then Q
+#pragma unroll
+  for (int sl = 0; sl < 8; ++sl) K[sl] = __shfl_sync(kFull, fadd(n_slot(mom.m1, sl), n_slot(mom.cn, sl)), q.b);
+#pragma unroll
+  for (int sl = 0; sl < 8; ++sl) {
+    const float a2 = n_slot(mom.m2, sl);
+    v[sl] = n_shifted_s(n_slot(mom.m1, sl), n_slot(mom.cn, sl), q.cnt, K[sl], v[8 + sl], a2 < 0.f ? 0.f : a2);
+  }
+  n_msum(v, q.rg, q.m);
+  if (q.m == 0 && lane < q.rg.vr) {
+    const float inv = __frcp_rn((float)q.len);
+#pragma unroll
+    for (int sl = 0; sl < 8; ++sl) sp[kVec * q.b + sl] = n_finish(K[sl], v[sl], v[8 + sl], (int)q.len, inv);
+  }
+  __syncwarp();
+  n_unit_pieces(p, q, sp, ws.upart);
+  __syncwarp();  // sp is rewritten by the next unit
+}
+
+// The direct statistics kernel (any channel count).
 template <class T>
 __global__ void __launch_bounds__(32 * kNRedWarps, 1)
-    k_ndhwc_stats(const T* __restrict__ x, NPlan p, NFwdWs ws, float eps, float* mean_out, float* rstd_out) {
+    k_ndhwc_stats(const T* __restrict__ x, NPlan p, NFwdWs ws) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   Part* sp = reinterpret_cast<Part*>(smem) + (size_t)warp * (kNSpan * kVec);
@@ -402,29 +353,277 @@ __global__ void __launch_bounds__(32 * kNRedWarps, 1)
   const int64_t W = (int64_t)gridDim.x * kNRedWarps;
   for (int64_t u = n_first_unit(); u < p.units; u += W) {
     const NUnit q = n_unit(p, u, lane);
-    f2 m1[4], cn[4], m2[4];
-    const int cnt = n_lane_moments<T>(x, q, m1, cn, m2);
-    // the lp lanes of each channel: shift by the m = 0 lane's mean, sum pairwise
-#pragma unroll
-    for (int sl = 0; sl < 8; ++sl) {
-      const float a1 = n_slot(m1, sl), ac = n_slot(cn, sl), a2 = n_slot(m2, sl);
-      const float K = __shfl_sync(kFull, fadd(a1, ac), q.b);
-      float Q;
-      float S = n_shifted_s(a1, ac, cnt, K, Q, a2 < 0.f ? 0.f : a2);
-      S = n_msum(S, q.rg, q.m);
-      Q = n_msum(Q, q.rg, q.m);
-      if (q.m == 0 && lane < q.rg.vr) sp[kVec * q.b + sl] = finish_merge(K, S, Q, q.len);
+    NMoments<T> mom;
+    n_lane_moments<T>(x, q, mom);
+    n_stats_unit_done<T>(p, ws, q, mom, sp);
+  }
+}
+
+// A bounded wait gave up: GN3D_ERR_TIMEOUT in the device status word.
+__device__ __forceinline__ void n_record_timeout(uint32_t* status) {
+  if ((threadIdx.x & 31) == 0) atomicExch(status, 4u);
+}
+
+// ---------------------------------------------------------- bulk-copy rings
+// With one channel range (C <= 256) a unit is one contiguous span: len*C
+// elements, step i the 8*lw elements from i*8*lw on (lane l < lw holding
+// vector l of the step).  The ring kernels stream the spans of the warp's units
+// through a warp-private ring of kSlots shared-memory slots, kPS steps per
+// slot, filled by 1-D bulk copies (the TMA engine) issued by lane 0, so several
+// parts of a warp's units are in flight at every moment.
+template <class T, int kTensors, int kSlots, int kPS>
+struct NRing {
+  static constexpr int kTensorBytes = kPS * kNSpan * kVec * (int)sizeof(T);
+  static constexpr int kSlotBytes = kTensors * kTensorBytes;
+  static constexpr int kWarpBytes = (kSlots * (kSlotBytes + 8) + 127) / 128 * 128;
+  static_assert(kTensorBytes % 128 == 0 && kSlotBytes % 8 == 0, "slot alignment");
+  unsigned char* data;
+  uint64_t* bar;
+  int64_t issued = 0, taken = 0;
+
+  __device__ __forceinline__ void init(unsigned char* base) {
+    data = base;
+    bar = reinterpret_cast<uint64_t*>(base + (size_t)kSlots * kSlotBytes);
+    if ((threadIdx.x & 31) == 0) {
+      for (int i = 0; i < kSlots; ++i) mbar_init(&bar[i], 1);
+      fence_mbar_init();
     }
     __syncwarp();
-    n_unit_pieces(p, q, sp, ws.upart);
-    // the pieces (written by several lanes) are published before lane 0's arrival
-    __threadfence();
-    __syncwarp();
-    const int64_t kb = q.k / p.B;
-    if (warp_arrive_last(ws.bcnt + q.row * p.nb + kb, (uint32_t)n_block_size(p, kb))) n_fwd_block(p, ws, q.row, kb);
   }
-  if (!n_last_cta(ws.done)) return;
-  for (int64_t gi = warp; gi < p.NG; gi += kNRedWarps) n_fwd_group(p, ws, gi, eps, mean_out, rstd_out);
+  // Copy elements [e0, e0 + n) of each tensor into the next slot (all lanes call;
+  // lane 0 copies).  e0 and n are multiples of 8 (16-byte aligned, 16-byte sizes).
+  __device__ __forceinline__ void issue(const T* const* src, int64_t e0, int64_t n) {
+    const int slot = (int)(issued % kSlots);
+    if ((threadIdx.x & 31) == 0) {
+      const uint32_t bytes = (uint32_t)(n * (int64_t)sizeof(T));
+      unsigned char* dst = data + (size_t)slot * kSlotBytes;
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(&bar[slot], bytes * kTensors);
+#pragma unroll
+      for (int t = 0; t < kTensors; ++t) bulk_g2s(dst + t * kTensorBytes, src[t] + e0, bytes, &bar[slot]);
+    }
+    ++issued;
+  }
+  // Wait (bounded) for the next slot; its data, or nullptr in every lane.
+  __device__ __forceinline__ const unsigned char* take(unsigned long long spin) {
+    const int slot = (int)(taken % kSlots);
+    const bool ok = __all_sync(kFull, mbar_wait_bounded(&bar[slot], (uint32_t)((taken / kSlots) & 1), spin));
+    if (!ok) return nullptr;
+    ++taken;
+    return data + (size_t)slot * kSlotBytes;
+  }
+  __device__ __forceinline__ void drain(unsigned long long spin) {
+    for (int64_t t = taken; t < issued; ++t)
+      mbar_wait_bounded(&bar[t % kSlots], (uint32_t)((t / kSlots) & 1), spin);
+  }
+};
+
+// Steps of unit u (one range: lp positions per step).
+__device__ __forceinline__ int n_unit_steps(const NPlan& p, const NRange& rg, int64_t u) {
+  const int64_t k = u % p.R, len = p.S - k * p.Pu < p.Pu ? p.S - k * p.Pu : p.Pu;
+  return (int)((len + rg.lp - 1) / rg.lp);
+}
+
+// The loader of a ring: part `part` of unit u, over the warp's units.
+template <int kPS>
+struct NLoader {
+  int64_t u;
+  int part;
+  template <class Ring, class T>
+  __device__ __forceinline__ void issue_next(const NPlan& p, const NRange& rg, int64_t W, Ring& ring,
+                                             const T* const* src) {
+    if (u >= p.units) return;
+    const int64_t k = u % p.R, n = u / p.R;
+    const int64_t len = p.S - k * p.Pu < p.Pu ? p.S - k * p.Pu : p.Pu;
+    const int64_t span = (int64_t)kPS * kVec * rg.lw, total = len * p.C;
+    const int64_t e0 = (n * p.S + k * p.Pu) * p.C + part * span;
+    const int64_t rest = total - part * span;
+    ring.issue(src, e0, rest < span ? rest : span);
+    if ((int64_t)(part + 1) * span >= total) {
+      part = 0;
+      u += W;
+    } else {
+      ++part;
+    }
+  }
+};
+
+template <class T> struct NStatRing {
+  static constexpr int kSlots = 3;
+  static constexpr int kPS = NBatch<T>::kStats;  // 8 KB slots
+  using Ring = NRing<T, 1, kSlots, kPS>;
+  static constexpr int kSmem = kNRedWarps * (Ring::kWarpBytes + kNSpan * kVec * (int)sizeof(Part));
+};
+
+// The ring statistics kernel (one channel range).
+template <class T>
+__global__ void __launch_bounds__(32 * kNRedWarps, 1)
+    k_ndhwc_stats_ring(const T* __restrict__ x, NPlan p, NFwdWs ws, unsigned long long spin, uint32_t* status) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  using Sh = NStatRing<T>;
+  constexpr int kPS = Sh::kPS, kRaw = Vec<T>::kRaw;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  typename Sh::Ring ring;
+  ring.init(smem + (size_t)warp * Sh::Ring::kWarpBytes);
+  Part* sp = reinterpret_cast<Part*>(smem + (size_t)kNRedWarps * Sh::Ring::kWarpBytes) + (size_t)warp * (kNSpan * kVec);
+  pdl_launch_dependents();
+  const int64_t W = (int64_t)gridDim.x * kNRedWarps;
+  const NRange rg = n_range(p, 0);
+  const T* src[1] = {x};
+  NLoader<kPS> ld{n_first_unit(), 0};
+  for (int i = 0; i < Sh::kSlots; ++i) ld.issue_next(p, rg, W, ring, src);
+  bool failed = false;
+  for (int64_t u = n_first_unit(); u < p.units && !failed; u += W) {
+    const NUnit q = n_unit(p, u, lane);
+    const int steps = n_unit_steps(p, rg, u);
+    NMoments<T> mom;
+    for (int t0 = 0; t0 < steps; t0 += kPS) {
+      const unsigned char* slot = ring.take(spin);
+      if (!slot) {
+        failed = true;
+        break;
+      }
+      const T* sb = reinterpret_cast<const T*>(slot) + kVec * lane;
+      const int nv = q.cnt - t0 < kPS ? q.cnt - t0 : kPS;
+      uint4 w[kPS][kRaw];
+#pragma unroll
+      for (int t = 0; t < kPS; ++t)
+        if (t < nv) Vec<T>::template load<FromShared>(sb + t * kVec * rg.lw, w[t]);
+      __syncwarp();
+      ld.issue_next(p, rg, W, ring, src);
+      if (nv > 0) mom.batch(w, t0, nv, q.cnt);
+    }
+    if (failed) break;
+    mom.finish(q.cnt);
+    n_stats_unit_done<T>(p, ws, q, mom, sp);
+  }
+  if (failed) n_record_timeout(status);
+  ring.drain(spin);
+}
+
+// ------------------------------------------------------ forward finalize
+// The unit pieces of group gi = n*G + g (range by range, unit by unit) are cut
+// into chunks of kNFinChunk units; one CTA of kNFinThreads threads merges a
+// chunk (thread t takes units t, t + kNFinThreads, ... in order, then the
+// warps' butterflies, then the warps in order) and the CTA that completes a
+// group merges its chunk partials in order.  Every merge is the shifted-sum
+// merge with the shift = the mean of the first part merged.  Chunk boundaries
+// depend on the shape only.
+constexpr int kNFinThreads = 256;
+constexpr int64_t kNFinChunk = 4096;
+
+// Ranges a group can meet (the most of any group) and chunks per range.
+__host__ __device__ inline int64_t n_fin_maxr(const NPlan& p) {
+  int64_t m = 1;
+  for (int64_t g = 0; g < p.G; ++g) {
+    const int64_t r = ((g + 1) * p.Cg - 1) / (kNSpan * kVec) - (g * p.Cg) / (kNSpan * kVec) + 1;
+    if (r > m) m = r;
+  }
+  return m;
+}
+__host__ __device__ inline int64_t n_fin_nkc(const NPlan& p) { return (p.R + kNFinChunk - 1) / kNFinChunk; }
+
+__device__ __forceinline__ float2 n_cta_sum2(float a, float b) {
+  __shared__ float2 part[kNFinThreads / 32];
+  const float2 t = warp_sum2(a, b);
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = t;
+  __syncthreads();
+  float2 r = part[0];
+  for (int w = 1; w < kNFinThreads / 32; ++w) r = make_float2(fadd(r.x, part[w].x), fadd(r.y, part[w].y));
+  __syncthreads();  // part is reused by the next call
+  return r;
+}
+
+// Thread 0 adds the CTA's arrival on *ctr after the CTA's stores; every thread
+// learns whether it was the last of `total` (and then sees the others' stores).
+__device__ __forceinline__ bool n_cta_arrive_last(uint32_t* ctr, uint32_t total) {
+  __shared__ uint32_t last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = atom_add_acq_rel(ctr, 1u) + 1u == total ? 1u : 0u;
+  __syncthreads();
+  const bool l = last != 0;
+  if (l) __threadfence();
+  __syncthreads();  // last is reused by the next call
+  return l;
+}
+
+__global__ void __launch_bounds__(kNFinThreads)
+    k_ndhwc_stats_final(NPlan p, NFwdWs ws, float eps, float* mean_out, float* rstd_out) {
+  pdl_launch_dependents();
+  pdl_wait();  // the statistics kernel's unit pieces
+  const int64_t maxr = n_fin_maxr(p), nkc = n_fin_nkc(p), per = maxr * nkc;
+  for (int64_t t = blockIdx.x; t < p.NG * per; t += gridDim.x) {
+    const int64_t gi = t / per, rem = t - gi * per, ri = rem / nkc, kc = rem - ri * nkc;
+    const int64_t n = gi / p.G, g = gi - n * p.G;
+    const int64_t r = (g * p.Cg) / (kNSpan * kVec) + ri, r_hi = ((g + 1) * p.Cg - 1) / (kNSpan * kVec);
+    Part part{0.f, 0.f, 0, 0.f};
+    if (r <= r_hi) {
+      const NRange rg = n_range(p, r);
+      const int64_t j = g - rg.g0;
+      int64_t c0, c1;
+      n_piece(p, rg, j, c0, c1);
+      const Part* base = ws.upart + ((n * p.nr + r) * p.P + j) * p.R;
+      const int64_t k0 = kc * kNFinChunk, k1 = k0 + kNFinChunk < p.R ? k0 + kNFinChunk : p.R;
+      const Part b0 = ldcg_part(base + k0);
+      const float K = fadd(b0.m1, b0.cn);
+      float S = 0.f, Q = 0.f;
+      constexpr int kBatch = 16, kPer = (int)(kNFinChunk / kNFinThreads);
+#pragma unroll
+      for (int i0 = 0; i0 < kPer; i0 += kBatch) {
+        Part v[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+          const int64_t k = k0 + threadIdx.x + (int64_t)(i0 + i) * kNFinThreads;
+          if (k < k1) v[i] = ldcg_part(base + k);
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+          if (k0 + threadIdx.x + (int64_t)(i0 + i) * kNFinThreads < k1) {
+            float s1, q1;
+            shifted_terms(v[i], K, s1, q1);
+            S = fadd(S, s1);
+            Q = fadd(Q, q1);
+          }
+        }
+      }
+      const float2 tq = n_cta_sum2(S, Q);
+      const int64_t pos = (k1 * p.Pu < p.S ? k1 * p.Pu : p.S) - k0 * p.Pu;
+      part = finish_merge(K, tq.x, tq.y, pos * (c1 - c0));
+    }
+    if (per == 1) {  // one chunk: it is the group
+      if (threadIdx.x == 0) {
+        const float rs = __frsqrt_rn(fadd(__fdiv_rn(part.m2, (float)p.M), eps));
+        ws.stats[gi] = make_float4(part.m1, part.cn, rs, 0.f);
+        if (mean_out) mean_out[gi] = fadd(part.m1, part.cn);
+        if (rstd_out) rstd_out[gi] = rs;
+      }
+      continue;
+    }
+    if (threadIdx.x == 0) ws.fpart[t] = part;
+    if (!n_cta_arrive_last(ws.gcnt + gi, (uint32_t)per)) continue;
+    if (threadIdx.x < 32) {
+      // the group's chunk partials in order (the first one is never empty)
+      const Part* fp = ws.fpart + gi * per;
+      const Part a0 = ldcg_part(fp);
+      const float K = fadd(a0.m1, a0.cn);
+      float S = 0.f, Q = 0.f;
+      for (int64_t i = threadIdx.x; i < per; i += 32) {
+        float s1, q1;
+        shifted_terms(ldcg_part(fp + i), K, s1, q1);
+        S = fadd(S, s1);
+        Q = fadd(Q, q1);
+      }
+      const float2 tq = warp_sum2(S, Q);
+      if (threadIdx.x == 0) {
+        const Part gp = finish_merge(K, tq.x, tq.y, p.M);
+        const float rs = __frsqrt_rn(fadd(__fdiv_rn(gp.m2, (float)p.M), eps));
+        ws.stats[gi] = make_float4(gp.m1, gp.cn, rs, 0.f);
+        if (mean_out) mean_out[gi] = fadd(gp.m1, gp.cn);
+        if (rstd_out) rstd_out[gi] = rs;
+      }
+    }
+  }
 }
 
 // ------------------------------------------------------------- normalize
@@ -436,11 +635,25 @@ __global__ void __launch_bounds__(32 * kNElemWarps, 1)
                  const float* __restrict__ gamma, const float* __restrict__ beta) {
   constexpr int kB = NBatch<TI>::kNorm, kRaw = Vec<TI>::kRaw;
   const int lane = threadIdx.x & 31;
+  NOwned own(p);
+  // the first batch of the first unit is loaded before the statistics are
+  // complete (x is not written there); everything else after pdl_wait
+  uint4 w[kB][kRaw];
+  bool pre = false;
+  if (own.more()) {
+    const NUnit q = n_unit(p, own.unit(), lane);
+#pragma unroll
+    for (int t = 0; t < kB; ++t)
+      if (t < q.cnt) Vec<TI>::template load<FromGlobal>(x + q.off + (int64_t)t * q.step, w[t]);
+    pre = true;
+  }
   pdl_wait();
-  for (NOwned own(p); own.more(); own.next()) {
-    const int64_t u = own.unit();
-    const NUnit q = n_unit(p, u, lane);
-    if (q.cnt == 0) continue;
+  for (; own.more(); own.next()) {
+    const NUnit q = n_unit(p, own.unit(), lane);
+    if (q.cnt == 0) {
+      pre = false;
+      continue;
+    }
     f2 hi[4], sc[4], sh[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -461,10 +674,12 @@ __global__ void __launch_bounds__(32 * kNElemWarps, 1)
     const TI* xb = x + q.off;
     TO* yb = y + q.off;
     for (int t0 = 0; t0 < q.cnt; t0 += kB) {
-      uint4 w[kB][kRaw];
+      if (!pre) {
 #pragma unroll
-      for (int t = 0; t < kB; ++t)
-        if (t0 + t < q.cnt) Vec<TI>::template load<FromGlobal>(xb + (int64_t)(t0 + t) * q.step, w[t]);
+        for (int t = 0; t < kB; ++t)
+          if (t0 + t < q.cnt) Vec<TI>::template load<FromGlobal>(xb + (int64_t)(t0 + t) * q.step, w[t]);
+      }
+      pre = false;
 #pragma unroll
       for (int t = 0; t < kB; ++t) {
         if (t0 + t < q.cnt) {
@@ -494,110 +709,110 @@ __device__ __forceinline__ void n_grad(const T* dy, const T* res, int64_t o, uin
   }
 }
 
-// Block kb of row `row` is complete: per channel of the range, the sum of its
-// unit sums, by one warp working as 32/B segments (one channel per segment,
-// lane kk holding unit kk of the block).
-__device__ __forceinline__ void n_bwd_block(const NPlan& p, const NBwdWs& ws, int64_t row, int64_t kb) {
-  const int lane = threadIdx.x & 31, B = (int)p.B, per = 32 / B, cl = lane / B, kk = lane - cl * B;
-  const int64_t n = row / p.nr;
-  const NRange rg = n_range(p, row - n * p.nr);
-  const int bsz = n_block_size(p, kb);
-  for (int64_t c0 = rg.c0; c0 < rg.c1; c0 += (int64_t)per * kMergeBatch) {
-    float2 v[kMergeBatch];
+// S1 += dy, S2 += dy*(x - mean) over a batch of nv steps (wx: x, wd: the gradient).
+template <class T, int kB>
+__device__ __forceinline__ void n_bwd_batch(const uint4 (&wx)[kB][Vec<T>::kRaw], const uint4 (&wd)[kB][Vec<T>::kRaw],
+                                            int nv, const f2 mu[4], f2 a1[4], f2 a2[4]) {
 #pragma unroll
-    for (int t = 0; t < kMergeBatch; ++t) {
-      const int64_t c = c0 + (int64_t)t * per + cl;
-      v[t] = c < rg.c1 && kk < bsz ? __ldcg(ws.usum + (n * p.C + c) * p.R + kb * p.B + kk) : make_float2(0.f, 0.f);
-    }
+  for (int t = 0; t < kB; ++t) {
+    if (t < nv) {
+      f2 xm[4], vd[4];
+      n_diff<T>(wx[t], mu, xm);
+      Vec<T>::pairs(wd[t], vd);
 #pragma unroll
-    for (int t = 0; t < kMergeBatch; ++t) {
-      if (c0 + (int64_t)t * per >= rg.c1) break;
-      const int64_t c = c0 + (int64_t)t * per + cl;
-      const float s1 = n_segsum(v[t].x, B), s2 = n_segsum(v[t].y, B);
-      if (kk == 0 && c < rg.c1) ws.bsum[(n * p.C + c) * p.nb + kb] = make_float2(s1, s2);
+      for (int e = 0; e < 4; ++e) {
+        a1[e] = f2add(a1[e], vd[e]);
+        a2[e] = f2fma(vd[e], xm[e], a2[e]);
+      }
     }
   }
 }
 
-template <class T, bool kRelu>
-__global__ void __launch_bounds__(32 * kNRedWarps, 1)
-    k_ndhwc_reduce(const T* __restrict__ dy, const T* __restrict__ x, const T* __restrict__ res, NPlan p,
-                   const float* __restrict__ mean, const float* __restrict__ rstd, const float* __restrict__ gamma,
-                   NBwdWs ws, float* dgamma, float* dbeta) {
-  constexpr int kB = NBatch<T, kRelu>::kReduce, kRaw = Vec<T>::kRaw;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+// The lane's 8 group means (pairs of channels).
+template <class T>
+__device__ __forceinline__ void n_lane_means(const NPlan& p, const NUnit& q, const float* __restrict__ mean,
+                                             f2 mu[4]) {
+  const float* mg = mean + q.n * p.G;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int64_t c = q.rg.c0 + kVec * q.b + 2 * e;
+    mu[e] = q.cnt ? f2_of(mg[c / p.Cg], mg[(c + 1) / p.Cg]) : f2_splat(0.f);
+  }
+}
+
+// A unit's lane sums -> channel sums (pairwise over the lp lanes of a channel),
+// stored to usum (the finalize kernel sums them).
+__device__ __forceinline__ void n_reduce_unit_done(const NPlan& p, const NBwdWs& ws, const NUnit& q, const f2 a1[4],
+                                                   const f2 a2[4]) {
+  const int lane = threadIdx.x & 31;
+  float v[16];  // S1 of the 8 channels, then S2
+#pragma unroll
+  for (int sl = 0; sl < 8; ++sl) {
+    v[sl] = n_slot(a1, sl);
+    v[8 + sl] = n_slot(a2, sl);
+  }
+  n_msum(v, q.rg, q.m);
+  if (q.m == 0 && lane < q.rg.vr) {
+#pragma unroll
+    for (int sl = 0; sl < 8; ++sl)
+      ws.usum[(q.n * p.C + q.rg.c0 + kVec * q.b + sl) * p.R + q.k] = make_float2(v[sl], v[8 + sl]);
+  }
+}
+
+// ----------------------------------------------------- backward finalize
+// Row (n, c): its unit sums cut into chunks of kNFinChunk units; one CTA sums a
+// chunk (thread t takes units t, t + kNFinThreads, ... in order, then the warps'
+// butterflies, then the warps in order); the CTA that completes a row adds its
+// chunk sums in order (S1, S2 of the row); the CTA that completes the last row
+// forms the group coefficients, A = sum_c gamma_c*S1_c and
+// B = rstd * sum_c gamma_c*S2_c in channel order (a = A/M, b = B/M), and
+// dgamma_c = sum_n rstd[n,g]*S2[n,c], dbeta_c = sum_n S1[n,c] in n order.
+__global__ void __launch_bounds__(kNFinThreads)
+    k_ndhwc_reduce_final(NPlan p, NBwdWs ws, const float* __restrict__ rstd, const float* __restrict__ gamma,
+                         float* dgamma, float* dbeta) {
   pdl_launch_dependents();
-  const int64_t W = (int64_t)gridDim.x * kNRedWarps;
-  const f2 z2 = f2_splat(0.f);
-  for (int64_t u = n_first_unit(); u < p.units; u += W) {
-    const NUnit q = n_unit(p, u, lane);
-    f2 mu[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int64_t c = q.rg.c0 + kVec * q.b + 2 * e;
-      const float* mg = mean + q.n * p.G;
-      mu[e] = q.cnt ? f2_of(mg[c / p.Cg], mg[(c + 1) / p.Cg]) : z2;
-    }
-    f2 a1[4] = {z2, z2, z2, z2}, a2[4] = {z2, z2, z2, z2};
-    for (int t0 = 0; t0 < q.cnt; t0 += kB) {
-      uint4 wx[kB][kRaw], wd[kB][kRaw];
-#pragma unroll
-      for (int t = 0; t < kB; ++t) {
-        if (t0 + t < q.cnt) {
-          const int64_t o = q.off + (int64_t)(t0 + t) * q.step;
-          Vec<T>::template load<FromGlobal>(x + o, wx[t]);
-          n_grad<T, kRelu>(dy, res, o, wd[t]);
-        }
-      }
-#pragma unroll
-      for (int t = 0; t < kB; ++t) {
-        if (t0 + t < q.cnt) {
-          f2 xm[4], vd[4];
-          n_diff<T>(wx[t], mu, xm);
-          Vec<T>::pairs(wd[t], vd);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            a1[e] = f2add(a1[e], vd[e]);
-            a2[e] = f2fma(vd[e], xm[e], a2[e]);
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int sl = 0; sl < 8; ++sl) {
-      const float s1 = n_msum(n_slot(a1, sl), q.rg, q.m), s2 = n_msum(n_slot(a2, sl), q.rg, q.m);
-      if (q.m == 0 && lane < q.rg.vr)
-        ws.usum[(q.n * p.C + q.rg.c0 + kVec * q.b + sl) * p.R + q.k] = make_float2(s1, s2);
-    }
-    __threadfence();
-    __syncwarp();
-    const int64_t kb = q.k / p.B;
-    if (warp_arrive_last(ws.bcnt + q.row * p.nb + kb, (uint32_t)n_block_size(p, kb))) n_bwd_block(p, ws, q.row, kb);
-  }
-  if (!n_last_cta(ws.done)) return;
-  // row totals (n, c): warp per row, lane l takes blocks l, l+32, ...
-  for (int64_t rc = warp; rc < p.N * p.C; rc += kNRedWarps) {
-    const float2* bp = ws.bsum + rc * p.nb;
+  pdl_wait();  // the reduction kernel's unit sums
+  const int64_t nkc = n_fin_nkc(p), NC = p.N * p.C;
+  bool last_row = false;
+  for (int64_t t = blockIdx.x; t < NC * nkc; t += gridDim.x) {
+    const int64_t rc = t / nkc, kc = t - rc * nkc;
+    const float2* us = ws.usum + rc * p.R;
+    const int64_t k0 = kc * kNFinChunk, k1 = k0 + kNFinChunk < p.R ? k0 + kNFinChunk : p.R;
     float s1 = 0.f, s2 = 0.f;
-    for (int64_t i0 = lane; i0 < p.nb; i0 += 32 * kMergeBatch) {
-      float2 v[kMergeBatch];
+    constexpr int kPer = (int)(kNFinChunk / kNFinThreads);
+    float2 v[kPer];
 #pragma unroll
-      for (int t = 0; t < kMergeBatch; ++t)
-        if (i0 + 32 * t < p.nb) v[t] = __ldcg(bp + i0 + 32 * t);
+    for (int i = 0; i < kPer; ++i) {
+      const int64_t k = k0 + threadIdx.x + (int64_t)i * kNFinThreads;
+      if (k < k1) v[i] = __ldcg(us + k);
+    }
 #pragma unroll
-      for (int t = 0; t < kMergeBatch; ++t) {
-        if (i0 + 32 * t < p.nb) {
-          s1 = fadd(s1, v[t].x);
-          s2 = fadd(s2, v[t].y);
-        }
+    for (int i = 0; i < kPer; ++i) {
+      if (k0 + threadIdx.x + (int64_t)i * kNFinThreads < k1) {
+        s1 = fadd(s1, v[i].x);
+        s2 = fadd(s2, v[i].y);
       }
     }
-    const float2 t = warp_sum2(s1, s2);
-    if (lane == 0) ws.rows[rc] = t;
+    const float2 sum = n_cta_sum2(s1, s2);
+    if (nkc == 1) {  // one chunk: it is the row
+      if (threadIdx.x == 0) ws.rows[rc] = sum;
+    } else {
+      if (threadIdx.x == 0) ws.rpart[t] = sum;
+      if (!n_cta_arrive_last(ws.rcnt + rc, (uint32_t)nkc)) continue;
+    }
+    if (nkc > 1 && threadIdx.x < 32) {
+      float a1 = 0.f, a2 = 0.f;
+      for (int64_t i = threadIdx.x; i < nkc; i += 32) {
+        const float2 v = __ldcg(ws.rpart + rc * nkc + i);
+        a1 = fadd(a1, v.x);
+        a2 = fadd(a2, v.y);
+      }
+      const float2 row = warp_sum2(a1, a2);
+      if (threadIdx.x == 0) ws.rows[rc] = row;
+    }
+    if (n_cta_arrive_last(ws.done, (uint32_t)NC)) last_row = true;
   }
-  __syncthreads();
-  // group coefficients: A = sum_c gamma_c*S1_c and B = rstd * sum_c gamma_c*S2_c
-  // in channel order; a = A/M, b = B/M
+  if (!last_row) return;
   for (int64_t gi = threadIdx.x; gi < p.NG; gi += blockDim.x) {
     const int64_t n = gi / p.G, g = gi - n * p.G;
     float A = 0.f, Bs = 0.f;
@@ -612,7 +827,6 @@ __global__ void __launch_bounds__(32 * kNRedWarps, 1)
     const float fM = (float)p.M;
     ws.coef[gi] = make_float2(__fdiv_rn(A, fM), __fdiv_rn(Bs, fM));
   }
-  // dgamma_c = sum_n rstd[n,g]*S2[n,c], dbeta_c = sum_n S1[n,c], in n order
   for (int64_t c = threadIdx.x; c < p.C; c += blockDim.x) {
     const int64_t g = c / p.Cg;
     float dg = 0.f, db = 0.f;
@@ -626,6 +840,106 @@ __global__ void __launch_bounds__(32 * kNRedWarps, 1)
   }
 }
 
+// The direct reduction kernel (any channel count).
+template <class T, bool kRelu>
+__global__ void __launch_bounds__(32 * kNRedWarps, 1)
+    k_ndhwc_reduce(const T* __restrict__ dy, const T* __restrict__ x, const T* __restrict__ res, NPlan p,
+                   const float* __restrict__ mean, NBwdWs ws) {
+  constexpr int kB = NBatch<T, kRelu>::kReduce, kRaw = Vec<T>::kRaw;
+  const int lane = threadIdx.x & 31;
+  pdl_launch_dependents();
+  const int64_t W = (int64_t)gridDim.x * kNRedWarps;
+  const f2 z2 = f2_splat(0.f);
+  for (int64_t u = n_first_unit(); u < p.units; u += W) {
+    const NUnit q = n_unit(p, u, lane);
+    f2 mu[4];
+    n_lane_means<T>(p, q, mean, mu);
+    f2 a1[4] = {z2, z2, z2, z2}, a2[4] = {z2, z2, z2, z2};
+    for (int t0 = 0; t0 < q.cnt; t0 += kB) {
+      const int nv = q.cnt - t0 < kB ? q.cnt - t0 : kB;
+      uint4 wx[kB][kRaw], wd[kB][kRaw];
+#pragma unroll
+      for (int t = 0; t < kB; ++t) {
+        if (t < nv) {
+          const int64_t o = q.off + (int64_t)(t0 + t) * q.step;
+          Vec<T>::template load<FromGlobal>(x + o, wx[t]);
+          n_grad<T, kRelu>(dy, res, o, wd[t]);
+        }
+      }
+      n_bwd_batch<T>(wx, wd, nv, mu, a1, a2);
+    }
+    n_reduce_unit_done(p, ws, q, a1, a2);
+  }
+}
+
+template <class T, bool kRelu> struct NRedRing {
+  static constexpr int kSlots = kRelu ? 4 : 3;
+  static constexpr int kTensors = kRelu ? 3 : 2;
+  static constexpr int kPS = NBatch<T, kRelu>::kReduce;  // 4 KB (2 KB behind a ReLU) of each tensor per slot
+  using Ring = NRing<T, kTensors, kSlots, kPS>;
+  static constexpr int kSmem = kNRedWarps * Ring::kWarpBytes;
+};
+
+// The ring reduction kernel (one channel range).
+template <class T, bool kRelu>
+__global__ void __launch_bounds__(32 * kNRedWarps, 1)
+    k_ndhwc_reduce_ring(const T* __restrict__ dy, const T* __restrict__ x, const T* __restrict__ res, NPlan p,
+                        const float* __restrict__ mean, NBwdWs ws, unsigned long long spin, uint32_t* status) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  using Sh = NRedRing<T, kRelu>;
+  using Ring = typename Sh::Ring;
+  constexpr int kPS = Sh::kPS, kRaw = Vec<T>::kRaw;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  Ring ring;
+  ring.init(smem + (size_t)warp * Ring::kWarpBytes);
+  pdl_launch_dependents();
+  const int64_t W = (int64_t)gridDim.x * kNRedWarps;
+  const NRange rg = n_range(p, 0);
+  const T* src[3] = {x, dy, res};
+  NLoader<kPS> ld{n_first_unit(), 0};
+  for (int i = 0; i < Sh::kSlots; ++i) ld.issue_next(p, rg, W, ring, src);
+  const f2 z2 = f2_splat(0.f);
+  bool failed = false;
+  for (int64_t u = n_first_unit(); u < p.units && !failed; u += W) {
+    const NUnit q = n_unit(p, u, lane);
+    const int steps = n_unit_steps(p, rg, u);
+    f2 mu[4];
+    n_lane_means<T>(p, q, mean, mu);
+    f2 a1[4] = {z2, z2, z2, z2}, a2[4] = {z2, z2, z2, z2};
+    for (int t0 = 0; t0 < steps; t0 += kPS) {
+      const unsigned char* slot = ring.take(spin);
+      if (!slot) {
+        failed = true;
+        break;
+      }
+      const int nv = q.cnt - t0 < kPS ? q.cnt - t0 : kPS;
+      const T* xs = reinterpret_cast<const T*>(slot) + kVec * lane;
+      const T* ds = reinterpret_cast<const T*>(slot + Ring::kTensorBytes) + kVec * lane;
+      uint4 wx[kPS][kRaw], wd[kPS][kRaw];
+#pragma unroll
+      for (int t = 0; t < kPS; ++t) {
+        if (t < nv) {
+          Vec<T>::template load<FromShared>(xs + t * kVec * rg.lw, wx[t]);
+          Vec<T>::template load<FromShared>(ds + t * kVec * rg.lw, wd[t]);
+          if constexpr (kRelu) {
+            const T* rs = reinterpret_cast<const T*>(slot + 2 * Ring::kTensorBytes) + kVec * lane;
+            uint4 o[kRaw];
+            Vec<T>::template load<FromShared>(rs + t * kVec * rg.lw, o);
+            Vec<T>::gate(o, wd[t]);
+          }
+        }
+      }
+      __syncwarp();
+      ld.issue_next(p, rg, W, ring, src);
+      n_bwd_batch<T>(wx, wd, nv, mu, a1, a2);
+    }
+    if (failed) break;
+    n_reduce_unit_done(p, ws, q, a1, a2);
+  }
+  if (failed) n_record_timeout(status);
+  ring.drain(spin);
+}
+
 // dx = dy*p1 - (x - mean)*p2 - p3 per channel, with p1 = rstd*gamma,
 // p2 = rstd^2 * b, p3 = rstd * a (a single-element group has dx = 0).
 template <class T, bool kRelu>
@@ -635,12 +949,31 @@ __global__ void __launch_bounds__(32 * kNElemWarps, 1)
                const float* __restrict__ gamma, const float2* __restrict__ coef) {
   constexpr int kB = NBatch<T, kRelu>::kDx, kRaw = Vec<T>::kRaw;
   const int lane = threadIdx.x & 31;
+  NOwned own(p);
+  // the first batch is loaded before the coefficients exist (x, dy and the
+  // forward's result are inputs); the coefficients after pdl_wait
+  uint4 wx[kB][kRaw], wd[kB][kRaw];
+  bool pre = false;
+  if (own.more()) {
+    const NUnit q = n_unit(p, own.unit(), lane);
+#pragma unroll
+    for (int t = 0; t < kB; ++t) {
+      if (t < q.cnt) {
+        const int64_t o = q.off + (int64_t)t * q.step;
+        Vec<T>::template load<FromGlobal>(x + o, wx[t]);
+        n_grad<T, kRelu>(dy, res, o, wd[t]);
+      }
+    }
+    pre = true;
+  }
   pdl_wait();
   const bool single = p.M == 1;
-  for (NOwned own(p); own.more(); own.next()) {
-    const int64_t u = own.unit();
-    const NUnit q = n_unit(p, u, lane);
-    if (q.cnt == 0) continue;
+  for (; own.more(); own.next()) {
+    const NUnit q = n_unit(p, own.unit(), lane);
+    if (q.cnt == 0) {
+      pre = false;
+      continue;
+    }
     f2 mu[4], p1[4], np2[4], np3[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -662,15 +995,17 @@ __global__ void __launch_bounds__(32 * kNElemWarps, 1)
       np3[e] = f2_of(a[3][0], a[3][1]);
     }
     for (int t0 = 0; t0 < q.cnt; t0 += kB) {
-      uint4 wx[kB][kRaw], wd[kB][kRaw];
+      if (!pre) {
 #pragma unroll
-      for (int t = 0; t < kB; ++t) {
-        if (t0 + t < q.cnt) {
-          const int64_t o = q.off + (int64_t)(t0 + t) * q.step;
-          Vec<T>::template load<FromGlobal>(x + o, wx[t]);
-          n_grad<T, kRelu>(dy, res, o, wd[t]);
+        for (int t = 0; t < kB; ++t) {
+          if (t0 + t < q.cnt) {
+            const int64_t o = q.off + (int64_t)(t0 + t) * q.step;
+            Vec<T>::template load<FromGlobal>(x + o, wx[t]);
+            n_grad<T, kRelu>(dy, res, o, wd[t]);
+          }
         }
       }
+      pre = false;
 #pragma unroll
       for (int t = 0; t < kB; ++t) {
         if (t0 + t < q.cnt) {

@@ -26,12 +26,9 @@ struct NPlan {
   int64_t nr;     // channel ranges
   int64_t Pu;     // positions per unit
   int64_t R;      // units per row
-  int64_t B;      // units per merge block
-  int64_t nb;     // merge blocks per row
   int64_t P;      // pieces (groups met) per range, the most of any range
   int64_t rows;   // N * nr
   int64_t units;  // rows * R
-  int64_t nblk;   // rows * nb
 };
 
 // Range r: vectors [32r, 32r + vr), channels [c0, c1), groups g0 .. g1.
@@ -64,11 +61,6 @@ inline NPlan make_nplan(int64_t N, int64_t C, int64_t S, int64_t G) {
   const int64_t v0 = p.V < kNSpan ? p.V : kNSpan;
   p.Pu = (int64_t)kNSteps * (32 / v0);
   p.R = S > 0 ? (S + p.Pu - 1) / p.Pu : 0;
-  // about 1024 channel-units per block (B * channels of range 0), 4 .. 32 units
-  int64_t b = 32;
-  while (b > 4 && b * kNVec * v0 > 1024) b >>= 1;
-  p.B = b;
-  p.nb = (p.R + p.B - 1) / p.B;
   p.P = 0;
   for (int64_t r = 0; r < p.nr; ++r) {
     const NRange q = n_range(p, r);
@@ -76,7 +68,6 @@ inline NPlan make_nplan(int64_t N, int64_t C, int64_t S, int64_t G) {
   }
   p.rows = N * p.nr;
   p.units = p.rows * p.R;
-  p.nblk = p.rows * p.nb;
   return p;
 }
 
@@ -115,18 +106,6 @@ __host__ __device__ inline void n_piece(const NPlan& p, const NRange& rg, int64_
   const int64_t a = g * p.Cg, e = a + p.Cg;
   c0 = (a > rg.c0 ? a : rg.c0) - rg.c0;
   c1 = (e < rg.c1 ? e : rg.c1) - rg.c0;
-}
-
-// Units of block kb of a row.
-__host__ __device__ inline int n_block_size(const NPlan& p, int64_t kb) {
-  const int64_t rest = p.R - kb * p.B;
-  return (int)(rest < p.B ? rest : p.B);
-}
-
-// Positions covered by block kb of a row.
-__host__ __device__ inline int64_t n_block_positions(const NPlan& p, int64_t kb) {
-  const int64_t a = kb * p.B * p.Pu, e = a + p.B * p.Pu;
-  return (e < p.S ? e : p.S) - a;
 }
 
 }  // namespace gn3d

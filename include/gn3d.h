@@ -175,8 +175,9 @@ int gn3d_backward_relu(const void* dy, const void* x, const void* out, const flo
  *   - Deterministic (a fixed reduction order chosen from the shape alone; no
  *     float atomics).  The order differs from the NCDHW entry points', so the
  *     two layouts agree to rounding, not bit for bit.
- *   - Always the streaming kernels (k_ndhwc_stats + k_ndhwc_norm forward,
- *     k_ndhwc_reduce + k_ndhwc_dx backward); GN3D_DEBUG_PATH does not apply.
+ *   - Three kernels per direction: k_ndhwc_stats, k_ndhwc_stats_final,
+ *     k_ndhwc_norm forward; k_ndhwc_reduce, k_ndhwc_reduce_final, k_ndhwc_dx
+ *     backward.  GN3D_DEBUG_PATH does not apply.
  */
 int gn3d_forward_ndhwc(const void* x, const float* gamma, const float* beta, int64_t N, int64_t C,
                        int64_t D, int64_t H, int64_t W, int64_t G, double eps, gn3d_dtype in_dtype,
@@ -247,7 +248,8 @@ int gn3d_debug_set(int what, long long value);
  * Device time of one kernel, summed over the launches recorded since
  * GN3D_DEBUG_TIMING was last set to 1.  `name` is one of "k_fwd_fused",
  * "k_bwd_fused", "k_fwd_stats", "k_fwd_norm", "k_bwd_reduce", "k_bwd_dx",
- * "k_ndhwc_stats", "k_ndhwc_norm", "k_ndhwc_reduce", "k_ndhwc_dx".
+ * "k_ndhwc_stats", "k_ndhwc_stats_final", "k_ndhwc_norm", "k_ndhwc_reduce",
+ * "k_ndhwc_reduce_final", "k_ndhwc_dx".
  * Waits for the recorded events (host-blocking), then writes the total
  * milliseconds to *ms and the launch count to *launches.  Returns GN3D_OK,
  * GN3D_ERR_INVALID_ARG (NULL argument, unknown name) or GN3D_ERR_CUDA.
