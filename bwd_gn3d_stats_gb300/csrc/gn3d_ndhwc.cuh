@@ -648,15 +648,18 @@ __global__ void __launch_bounds__(32 * kNElemWarps, 1)
     pre = true;
   }
   pdl_wait();
+  f2 hi[4], sc[4], sh[4];
+  int64_t have = -1;  // the row (n, r) whose coefficients are loaded
   for (; own.more(); own.next()) {
     const NUnit q = n_unit(p, own.unit(), lane);
     if (q.cnt == 0) {
       pre = false;
       continue;
     }
-    f2 hi[4], sc[4], sh[4];
+    // a warp's units mostly share the row: the coefficients are reloaded only
+    // when it changes
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
+    for (int e = 0; e < 4 && have != q.row; ++e) {
       float h[2], a[2], b[2];
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
@@ -671,6 +674,7 @@ __global__ void __launch_bounds__(32 * kNElemWarps, 1)
       sc[e] = f2_of(a[0], a[1]);
       sh[e] = f2_of(b[0], b[1]);
     }
+    have = q.row;
     const TI* xb = x + q.off;
     TO* yb = y + q.off;
     for (int t0 = 0; t0 < q.cnt; t0 += kB) {
@@ -850,10 +854,14 @@ __global__ void __launch_bounds__(32 * kNRedWarps, 1)
   pdl_launch_dependents();
   const int64_t W = (int64_t)gridDim.x * kNRedWarps;
   const f2 z2 = f2_splat(0.f);
+  f2 mu[4];
+  int64_t have = -1;  // the row (n, r) whose means are loaded
   for (int64_t u = n_first_unit(); u < p.units; u += W) {
     const NUnit q = n_unit(p, u, lane);
-    f2 mu[4];
-    n_lane_means<T>(p, q, mean, mu);
+    if (have != q.row && q.cnt) {
+      n_lane_means<T>(p, q, mean, mu);
+      have = q.row;
+    }
     f2 a1[4] = {z2, z2, z2, z2}, a2[4] = {z2, z2, z2, z2};
     for (int t0 = 0; t0 < q.cnt; t0 += kB) {
       const int nv = q.cnt - t0 < kB ? q.cnt - t0 : kB;
@@ -900,11 +908,15 @@ __global__ void __launch_bounds__(32 * kNRedWarps, 1)
   for (int i = 0; i < Sh::kSlots; ++i) ld.issue_next(p, rg, W, ring, src);
   const f2 z2 = f2_splat(0.f);
   bool failed = false;
+  f2 mu[4];
+  int64_t have = -1;  // the row (n, r) whose means are loaded
   for (int64_t u = n_first_unit(); u < p.units && !failed; u += W) {
     const NUnit q = n_unit(p, u, lane);
     const int steps = n_unit_steps(p, rg, u);
-    f2 mu[4];
-    n_lane_means<T>(p, q, mean, mu);
+    if (have != q.row && q.cnt) {
+      n_lane_means<T>(p, q, mean, mu);
+      have = q.row;
+    }
     f2 a1[4] = {z2, z2, z2, z2}, a2[4] = {z2, z2, z2, z2};
     for (int t0 = 0; t0 < steps; t0 += kPS) {
       const unsigned char* slot = ring.take(spin);
@@ -968,15 +980,16 @@ __global__ void __launch_bounds__(32 * kNElemWarps, 1)
   }
   pdl_wait();
   const bool single = p.M == 1;
+  f2 mu[4], p1[4], np2[4], np3[4];
+  int64_t have = -1;  // the row (n, r) whose coefficients are loaded
   for (; own.more(); own.next()) {
     const NUnit q = n_unit(p, own.unit(), lane);
     if (q.cnt == 0) {
       pre = false;
       continue;
     }
-    f2 mu[4], p1[4], np2[4], np3[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
+    for (int e = 0; e < 4 && have != q.row; ++e) {
       float a[4][2];
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
@@ -994,6 +1007,7 @@ __global__ void __launch_bounds__(32 * kNElemWarps, 1)
       np2[e] = f2_of(a[2][0], a[2][1]);
       np3[e] = f2_of(a[3][0], a[3][1]);
     }
+    have = q.row;
     for (int t0 = 0; t0 < q.cnt; t0 += kB) {
       if (!pre) {
 #pragma unroll
