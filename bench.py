@@ -126,11 +126,15 @@ class ClockSampler:
 class Volume:
     """Device (and pinned host) buffers of one workload site."""
 
-    def __init__(self, site: synth.Site, dev, pinned: bool):
+    def __init__(self, site: synth.Site, dev, pinned: bool, layout: str = "ncdhw"):
         import torch
 
         self.site = site
+        self.layout = layout
         inp = synth.make_inputs(site, seed=0)
+        if layout == "ndhwc":  # the same logical tensors stored channels-last
+            for k in ("x", "dy"):
+                inp[k] = np.ascontiguousarray(inp[k].reshape(site.N, site.C, site.S).transpose(0, 2, 1)).reshape(-1)
         dt = torch.bfloat16 if site.dtype == synth.BF16 else torch.float32
 
         def host(a):
@@ -161,17 +165,18 @@ class Volume:
 
         s = self.site
         c = gn.BF16 if s.dtype == synth.BF16 else gn.F32
-        gn.gn3d_forward(self.x.data_ptr(), self.gamma.data_ptr(), self.beta.data_ptr(), s.N, s.C, s.D, s.H, s.W,
-                        s.G, s.eps, c, c, self.y.data_ptr(), self.mean.data_ptr(), self.rstd.data_ptr(), st)
+        fn = gn.gn3d_forward_ndhwc if self.layout == "ndhwc" else gn.gn3d_forward
+        fn(self.x.data_ptr(), self.gamma.data_ptr(), self.beta.data_ptr(), s.N, s.C, s.D, s.H, s.W, s.G, s.eps, c, c,
+           self.y.data_ptr(), self.mean.data_ptr(), self.rstd.data_ptr(), st)
 
     def bwd(self, st):
         import bwd_gn3d_stats_gb300 as gn
 
         s = self.site
         c = gn.BF16 if s.dtype == synth.BF16 else gn.F32
-        gn.gn3d_backward(self.dy.data_ptr(), self.x.data_ptr(), self.mean.data_ptr(), self.rstd.data_ptr(),
-                         self.gamma.data_ptr(), s.N, s.C, s.D, s.H, s.W, s.G, c, self.dx.data_ptr(),
-                         self.dgamma.data_ptr(), self.dbeta.data_ptr(), st)
+        fn = gn.gn3d_backward_ndhwc if self.layout == "ndhwc" else gn.gn3d_backward
+        fn(self.dy.data_ptr(), self.x.data_ptr(), self.mean.data_ptr(), self.rstd.data_ptr(), self.gamma.data_ptr(),
+           s.N, s.C, s.D, s.H, s.W, s.G, c, self.dx.data_ptr(), self.dgamma.data_ptr(), self.dbeta.data_ptr(), st)
 
 
 def time_device(vols, steps, warmup, flush, stream, kernel_timing=False):
@@ -226,7 +231,9 @@ def time_device(vols, steps, warmup, flush, stream, kernel_timing=False):
 # Algorithmic HBM bytes per launch of each kernel, in tensors of the volume's
 # size: what it must read and write at least (re-reads from L2 are not counted).
 KERNEL_TENSORS = {"k_fwd_fused": 2, "k_fwd_stats": 1, "k_fwd_norm": 2,
-                  "k_bwd_fused": 3, "k_bwd_reduce": 2, "k_bwd_dx": 3}
+                  "k_bwd_fused": 3, "k_bwd_reduce": 2, "k_bwd_dx": 3,
+                  "k_ndhwc_stats": 1, "k_ndhwc_stats_final": 0, "k_ndhwc_norm": 2,
+                  "k_ndhwc_reduce": 2, "k_ndhwc_reduce_final": 0, "k_ndhwc_dx": 3}
 
 
 def time_e2e(vol, steps, warmup, stream):
@@ -358,6 +365,29 @@ def unet_rollup(dev, flush, stream, ws):
             "min_bytes_per_stack": tot_bytes, "sites": sites}
 
 
+def ndhwc_line(site, dev, flush, stream, ws, steps):
+    """The same workload stored channels-last (NDHWC entry points): GB/s and the
+    per-kernel device times of its six kernels."""
+    import torch
+
+    v = Volume(site, dev, pinned=False, layout="ndhwc")
+    t, f, b = time_device([v], steps, 3, flush, stream)
+    ms = max_over_ranks(sum(t) / len(t), ws, dev)
+    _, _, _, kern = time_device([v], steps, 1, flush, stream, kernel_timing=True)
+    fb, bb = site.min_bytes()
+    tb = site.numel * site.elem_bytes
+    out = {"value": round(ws * (fb + bb) / (ms * 1e-3) / 1e9, 1), "unit": UNIT, "ms_per_step": round(ms, 4),
+           "layout": "NDHWC (channels_last_3d)",
+           "fwd_gbs": round(fb / (sum(f) / len(f) * 1e-3) / 1e9, 1),
+           "bwd_gbs": round(bb / (sum(b) / len(b) * 1e-3) / 1e9, 1),
+           "kernels": {k: {"us_per_launch": round(d["ms_per_launch"] * 1e3, 2),
+                           "gbs": (round(KERNEL_TENSORS[k] * tb / (d["ms_per_launch"] * 1e-3) / 1e9, 1)
+                                   if KERNEL_TENSORS[k] else None)} for k, d in kern.items()}}
+    del v
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_gpu(args):
     import torch
 
@@ -370,7 +400,7 @@ def run_gpu(args):
     build.build()
     gn.gn3d_debug_set(gn.DEBUG_PATH, {"auto": 0, "streaming": 1, "fused": 2}[args.path])
     site = synth.WORKLOADS[args.workload].sites[0]
-    vol = Volume(site, dev, pinned=True)
+    vol = Volume(site, dev, pinned=True, layout=args.layout)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(dev)
     launches0 = gn.gn3d_launch_count()
@@ -423,6 +453,8 @@ def run_gpu(args):
                                "bwd_gbs": round(b2b / (sum(b2) / len(b2) * 1e-3) / 1e9, 1)}
             del v2
         secondary[UNET] = unet_rollup(dev, flush, stream, ws)
+        if args.layout == "ncdhw":
+            secondary[args.workload + "_ndhwc"] = ndhwc_line(site, dev, flush, stream, ws, args.steps)
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         v, cores, sample = cpu_oracle_sample(site)
@@ -435,7 +467,7 @@ def run_gpu(args):
             "config": {"workload": args.workload, "N": site.N, "C": site.C, "D": site.D, "H": site.H,
                        "W": site.W, "G": site.G, "eps": site.eps, "parallelism": f"replicas x{ws}",
                        "min_bytes_per_step": fb + bb, "l2": "flushed between steps (256 MiB write)",
-                       "path": args.path},
+                       "path": args.path, "layout": args.layout},
             "pct_of_8TBs": round(100 * value / ws / NOMINAL_HBM_GBS, 2),
             "pct_of_measured_copy": round(100 * value / ws / peak, 2),
             "fwd": {"ms": round(fwd_ms, 4), "gbs": round(fwd_gbs, 1)},
@@ -499,6 +531,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--impl", default="gn3d", choices=["gn3d", "reference"])
     ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--layout", choices=["ncdhw", "ndhwc"], default="ncdhw",
+                    help="storage of the timed volume: NCDHW (default) or channels-last NDHWC")
     ap.add_argument("--path", default="auto", choices=["auto", "streaming", "fused"],
                     help="launch form (results are bit-identical; for A/B timing)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

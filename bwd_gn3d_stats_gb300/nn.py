@@ -7,16 +7,25 @@ GroupNorm dtype" fixes the output dtype policy (the input's dtype unless asked
 otherwise); the GroupNorm pages' FastGroupNorm takes an activation argument
 that fuses the following ReLU (gn3d_forward_relu / gn3d_backward_relu).
 
+Memory format: a channels_last_3d input (as channels-last convolutions
+produce it) runs the NDHWC entry points and gives a channels_last_3d output,
+with no layout conversion; any other input runs the NCDHW entry points on its
+contiguous form.  The NDHWC kernels need C % 8 == 0; other channel counts take
+the NCDHW path.
+
 Every computation runs in libgn3d's kernels: this file only allocates outputs,
-saves what the backward needs and converts the incoming gradient to x's dtype.
-There is no CPU path -- a CPU tensor raises.
+saves what the backward needs and converts the incoming gradient to x's dtype
+and layout.  There is no CPU path -- a CPU tensor raises.
 """
 from __future__ import annotations
 
 import torch
 
 from . import backward as _backward
+from . import backward_ndhwc as _backward_ndhwc
 from . import forward as _forward
+from . import forward_ndhwc as _forward_ndhwc
+from . import is_ndhwc as _is_ndhwc
 
 
 def _check_input(x: torch.Tensor):
@@ -38,12 +47,16 @@ class GroupNorm3dFunction(torch.autograd.Function):
         if relu and out_dtype != x.dtype:
             raise ValueError("the fused ReLU's backward gates on the forward's result in x's dtype: "
                              "out_dtype must equal x.dtype when relu is set")
-        x = x.contiguous()
+        ndhwc = _is_ndhwc(x) and x.shape[1] % 8 == 0
+        if not ndhwc:
+            x = x.contiguous()
         w = None if weight is None else weight.detach().float().contiguous()
         b = None if bias is None else bias.detach().float().contiguous()
-        y, mean, rstd = _forward(x, w, b, num_groups, eps, out_dtype, relu)
+        fwd = _forward_ndhwc if ndhwc else _forward
+        y, mean, rstd = fwd(x, w, b, num_groups, eps, out_dtype, relu)
         ctx.num_groups = num_groups
         ctx.relu = relu
+        ctx.ndhwc = ndhwc
         ctx.weight_dtype = None if weight is None else weight.dtype
         ctx.bias_dtype = None if bias is None else bias.dtype
         ctx.save_for_backward(x, w, mean, rstd, y if relu else None)
@@ -52,8 +65,12 @@ class GroupNorm3dFunction(torch.autograd.Function):
     @staticmethod
     def backward(ctx, dy):
         x, w, mean, rstd, y = ctx.saved_tensors
-        dy = dy.to(x.dtype).contiguous()
-        dx, dgamma, dbeta = _backward(dy, x, mean, rstd, w, ctx.num_groups, out=y if ctx.relu else None)
+        if ctx.ndhwc:
+            dy = dy.to(x.dtype).contiguous(memory_format=torch.channels_last_3d)
+            dx, dgamma, dbeta = _backward_ndhwc(dy, x, mean, rstd, w, ctx.num_groups, out=y if ctx.relu else None)
+        else:
+            dy = dy.to(x.dtype).contiguous()
+            dx, dgamma, dbeta = _backward(dy, x, mean, rstd, w, ctx.num_groups, out=y if ctx.relu else None)
         gw = dgamma.to(ctx.weight_dtype) if ctx.weight_dtype is not None and ctx.needs_input_grad[1] else None
         gb = dbeta.to(ctx.bias_dtype) if ctx.bias_dtype is not None and ctx.needs_input_grad[2] else None
         return dx, gw, gb, None, None, None, None
@@ -61,12 +78,14 @@ class GroupNorm3dFunction(torch.autograd.Function):
 
 def group_norm_3d(x, num_groups: int, weight=None, bias=None, eps: float = 1e-5, out_dtype=None,
                   relu: bool = False):
-    """Functional form: GroupNorm over an NCDHW CUDA tensor (then ReLU when relu is set)."""
+    """Functional form: GroupNorm over an [N, C, D, H, W] CUDA tensor, NCDHW or
+    channels_last_3d (then ReLU when relu is set)."""
     return GroupNorm3dFunction.apply(x, weight, bias, num_groups, eps, out_dtype, relu)
 
 
 class GroupNorm3d(torch.nn.Module):
-    """Drop-in for torch.nn.GroupNorm on NCDHW volumes, computed by libgn3d.
+    """Drop-in for torch.nn.GroupNorm on [N, C, D, H, W] volumes (NCDHW or
+    channels_last_3d), computed by libgn3d.
 
     Same constructor arguments, parameters ("weight", "bias") and state-dict keys
     as nn.GroupNorm, plus:

@@ -86,3 +86,55 @@ def test_relu_needs_matching_out_dtype():
         group_norm_3d(x, 4, out_dtype=t.float32, relu=True)
     y = group_norm_3d(x, 4, out_dtype=t.float32)  # without the ReLU any pair is allowed
     assert y.dtype == t.float32
+
+
+@pytest.mark.parametrize("relu", [False, True])
+def test_channels_last_module_runs_ndhwc(relu):
+    """A channels_last_3d input runs the NDHWC kernels (bit for bit the C ABI's
+    NDHWC entry points), keeps its memory format in y and dx, and agrees with
+    the NCDHW path to rounding."""
+    from bwd_gn3d_stats_gb300.nn import GroupNorm3d
+
+    t = torch()
+    cl = t.channels_last_3d
+    gen = t.Generator(device="cuda").manual_seed(7)
+    N, C, D, H, W, G = 2, 32, 10, 11, 12, 8
+    x = t.randn(N, C, D, H, W, device="cuda", generator=gen).to(t.bfloat16).contiguous(memory_format=cl)
+    dy = t.randn(N, C, D, H, W, device="cuda", generator=gen).to(t.bfloat16).contiguous(memory_format=cl)
+    m = GroupNorm3d(G, C, activation="relu" if relu else None).cuda()
+    with t.no_grad():
+        m.weight.uniform_(0.5, 1.5, generator=gen)
+        m.bias.normal_(0, 0.3, generator=gen)
+    xr = x.clone().requires_grad_()
+    y = m(xr)
+    y.backward(dy)
+    assert y.is_contiguous(memory_format=cl) and not y.is_contiguous()
+    assert xr.grad.is_contiguous(memory_format=cl)
+    w, b = m.weight.detach(), m.bias.detach()
+    n0 = gn.gn3d_launch_count()
+    y0, mean, rstd = gn.forward_ndhwc(x, w, b, G, 1e-5, relu=relu)
+    dx0, dg0, db0 = gn.backward_ndhwc(dy, x, mean, rstd, w, G, out=y0 if relu else None)
+    assert gn.gn3d_launch_count() - n0 == 6  # three kernels per direction
+    assert t.equal(y.view(t.int16), y0.view(t.int16)) and t.equal(xr.grad.view(t.int16), dx0.view(t.int16))
+    assert t.equal(m.weight.grad, dg0) and t.equal(m.bias.grad, db0)
+    # the NCDHW path on the same logical tensor
+    m2 = GroupNorm3d(G, C, activation="relu" if relu else None).cuda()
+    m2.load_state_dict(m.state_dict())
+    x2 = x.contiguous().requires_grad_()
+    y2 = m2(x2)
+    y2.backward(dy.contiguous())
+    d = (y.float() - y2.float()).abs().max().item()
+    assert d <= 2 ** -6 * max(1.0, y2.float().abs().max().item())
+    assert t.allclose(m.weight.grad, m2.weight.grad, rtol=1e-4, atol=1e-3)
+
+
+def test_channels_last_with_c_not_multiple_of_8_takes_ncdhw():
+    from bwd_gn3d_stats_gb300.nn import GroupNorm3d
+
+    t = torch()
+    gen = t.Generator(device="cuda").manual_seed(8)
+    x = t.randn(1, 12, 6, 6, 6, device="cuda", generator=gen).contiguous(memory_format=t.channels_last_3d)
+    m = GroupNorm3d(3, 12).cuda()
+    y = m(x)
+    ref = t.nn.functional.group_norm(x.contiguous(), 3, m.weight, m.bias, 1e-5)
+    assert t.allclose(y, ref, rtol=1e-5, atol=1e-5)
