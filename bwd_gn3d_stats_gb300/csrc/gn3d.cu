@@ -458,13 +458,14 @@ template <class TI, class TO>
 int launch_forward_ndhwc(const void* x, const float* gamma, const float* beta, const NPlan& p, float eps, void* y,
                          float* mean, float* rstd, cudaStream_t st, DevInfo& di, bool relu) {
   const int64_t tasks = p.NG * n_fin_maxr(p) * n_fin_nkc(p);  // finalize chunks
-  const int64_t bytes = rup(p.NG * 4) + rup(p.rows * p.P * p.R * (int64_t)sizeof(Part)) +
+  const int64_t bytes = rup((p.NG + 1) * 4) + rup(p.rows * p.P * p.R * (int64_t)sizeof(Part)) +
                         rup(tasks * (int64_t)sizeof(Part)) + rup(p.NG * (int64_t)sizeof(float4));
   Scratch s;
   GN3D_CUDA(cudaMallocFromPoolAsync(&s.base, (size_t)bytes, di.pool, st), "scratch allocation");
   s.cur = static_cast<char*>(s.base);
   NFwdWs w;
-  w.gcnt = s.take<uint32_t>(p.NG);
+  w.gcnt = s.take<uint32_t>(p.NG + 1);
+  w.never = w.gcnt + p.NG;
   w.upart = s.take<Part>(p.rows * p.P * p.R);
   w.fpart = s.take<Part>(tasks);
   w.stats = s.take<float4>(p.NG);
@@ -478,12 +479,13 @@ int launch_forward_ndhwc(const void* x, const float* gamma, const float* beta, c
   int rc = raise_smem(kfn, smem, di);
   if (rc) { cudaFreeAsync(s.base, st); return rc; }
   const int grid = grid_for(di, p.units, 1);
-  cudaError_t e = cudaMemsetAsync(w.gcnt, 0, (size_t)p.NG * sizeof(uint32_t), st);
+  cudaError_t e = cudaMemsetAsync(w.gcnt, 0, (size_t)(p.NG + 1) * sizeof(uint32_t), st);
   if (e == cudaSuccess) {
     g_launches += 3;
     LaunchTimer t1(KK_N_STATS, st, di);
     if (ring)
-      k_ndhwc_stats_ring<TI><<<grid, 32 * kNRedWarps, smem, st>>>(xp, p, w, spin_budget(), di.status);
+      k_ndhwc_stats_ring<TI><<<grid, 32 * kNRedWarps, smem, st>>>(xp, p, w, spin_budget(), di.status,
+                                                                  g_hook_timeout.exchange(0) != 0 ? 1 : 0);
     else
       k_ndhwc_stats<TI><<<grid, 32 * kNRedWarps, smem, st>>>(xp, p, w);
     t1.done();

@@ -369,7 +369,7 @@ __device__ __forceinline__ void run_fused(Op& op, const Plan& p, const FusedCfg&
     // drain this CTA's bulk copies in flight: wait for the last issued phase of every slot
     const volatile int no_stop = 0;
     for (int i = 0; i < nslots; ++i)
-      if (s_issued[i] > 0) mbar_wait(&full[i], (s_issued[i] - 1) & 1u, cfg.spin, &no_stop);
+      if (s_issued[i] > 0) mbar_wait(&full[i], (s_issued[i] - 1) & 1u, kDrainPolls, &no_stop);
   }
 }
 

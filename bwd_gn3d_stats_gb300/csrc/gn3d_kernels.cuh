@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(32 * FwdStatShape<TI>::kWarps, 1)
     }
     cu.next(p, stride, nblk);
   }
-  ring.drain(spin);
+  ring.drain(kDrainPolls);
 }
 
 // Elementwise passes: 16 warps per CTA, on the reduction kernel's grid.  Warp w
@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(32 * BwdRedShape<T, kRelu>::kWarps, 1)
     }
     cu.next(p, stride, nblk);
   }
-  ring.drain(spin);
+  ring.drain(kDrainPolls);
 }
 
 template <class T, bool kFull, bool kRelu>

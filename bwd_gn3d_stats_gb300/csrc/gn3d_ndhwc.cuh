@@ -38,6 +38,7 @@ namespace gn3d {
 
 // ------------------------------------------------------------- workspaces
 struct NFwdWs {
+  uint32_t* never; // [1] zero, never set (the forced-timeout test waits on it)
   Part* upart;     // [rows][P][R]       unit pieces
   Part* fpart;     // [NG][maxr * nkc]   finalize chunk partials
   uint32_t* gcnt;  // [NG]               finalize chunks done per group
@@ -64,13 +65,32 @@ template <class T, bool kRelu = false> struct NBatch {
   static constexpr int kDx = (kRelu ? 4 : 8) / kRaw;
 };
 
+// (lo - k.lo, hi - k.hi) for the two bf16 halves of w: one mixed-precision
+// subtraction per element (bf16 operand, fp32 shift and result, rounded once --
+// the value of widening first).
+__device__ __forceinline__ f2 n_bf16_pair_minus(uint32_t w, f2 k) {
+  f2 d;
+  asm("{\n .reg .b16 l, h;\n .reg .f32 kl, kh, dl, dh;\n mov.b32 {l, h}, %1;\n mov.b64 {kl, kh}, %2;\n"
+      " sub.rn.f32.bf16 dl, l, kl;\n sub.rn.f32.bf16 dh, h, kh;\n mov.b64 %0, {dl, dh};\n}"
+      : "=l"(d)
+      : "r"(w), "l"(k));
+  return d;
+}
+
 // (v - k) for the 8 elements of a vector as pairs, each pair with its own shift.
 template <class T>
 __device__ __forceinline__ void n_diff(const uint4 r[Vec<T>::kRaw], const f2 k[4], f2 d[4]) {
-  f2 v[4];
-  Vec<T>::pairs(r, v);
+  if constexpr (Vec<T>::kRaw == 1) {
+    d[0] = n_bf16_pair_minus(r[0].x, k[0]);
+    d[1] = n_bf16_pair_minus(r[0].y, k[1]);
+    d[2] = n_bf16_pair_minus(r[0].z, k[2]);
+    d[3] = n_bf16_pair_minus(r[0].w, k[3]);
+  } else {
+    f2 v[4];
+    Vec<T>::pairs(r, v);
 #pragma unroll
-  for (int e = 0; e < 4; ++e) d[e] = f2sub(v[e], k[e]);
+    for (int e = 0; e < 4; ++e) d[e] = f2sub(v[e], k[e]);
+  }
 }
 
 __device__ __forceinline__ float n_slot(const f2 a[4], int s) { return s & 1 ? f2_hi(a[s >> 1]) : f2_lo(a[s >> 1]); }
@@ -88,6 +108,7 @@ __device__ __forceinline__ float n_slot(const f2 a[4], int s) { return s & 1 ? f
 template <class T>
 struct NMoments {
   f2 K[4], c[4], s2[4];  // the current chunk: shift and sums
+  f2 c1[4], q1[4];       // second set of sums (odd steps), added to c, s2 at a chunk's end
   f2 m1[4], cn[4], m2[4];  // the first chunk's partial, then the lane's (pairs of channels)
   int nA = 0;
 
@@ -112,10 +133,10 @@ struct NMoments {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         K[e] = f2fma(pa[e], inv, z2);
-        c[e] = z2;
-        s2[e] = z2;
+        c[e] = s2[e] = c1[e] = q1[e] = z2;
       }
     }
+    // even steps into (c, s2), odd steps into (c1, q1): two chains per sum
 #pragma unroll
     for (int t = 0; t < kB; ++t) {
       if (t < nv) {
@@ -123,8 +144,13 @@ struct NMoments {
         n_diff<T>(w[t], K, d);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          c[e] = f2add(c[e], d[e]);
-          s2[e] = f2fma(d[e], d[e], s2[e]);
+          if (t & 1) {
+            c1[e] = f2add(c1[e], d[e]);
+            q1[e] = f2fma(d[e], d[e], q1[e]);
+          } else {
+            c[e] = f2add(c[e], d[e]);
+            s2[e] = f2fma(d[e], d[e], s2[e]);
+          }
         }
       }
     }
@@ -133,6 +159,11 @@ struct NMoments {
     const int endA = cnt < kNChunk ? cnt : kNChunk;
     if (t0 < kNChunk && t0 + nv >= endA) {
       nA = endA;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        c[e] = f2add(c[e], c1[e]);
+        s2[e] = f2add(s2[e], q1[e]);
+      }
       const f2 invA = f2_splat(nA == kNChunk ? 1.f / (float)kNChunk : __frcp_rn((float)nA));
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -140,8 +171,7 @@ struct NMoments {
         cn[e] = f2fma(c[e], invA, z2);
         m2[e] = f2sub(s2[e], f2fma(c[e], cn[e], z2));
         K[e] = f2add(m1[e], cn[e]);
-        c[e] = z2;
-        s2[e] = z2;
+        c[e] = s2[e] = c1[e] = q1[e] = z2;
       }
     }
   }
@@ -155,6 +185,11 @@ struct NMoments {
       return;
     }
     if (cnt == nA) return;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      c[e] = f2add(c[e], c1[e]);
+      s2[e] = f2add(s2[e], q1[e]);
+    }
     // merge: the first chunk's terms about the rest's shift K, plus the rest's sums
     const f2 fa = f2_splat((float)nA);
     const f2 inv = f2_splat(cnt == kNSteps ? 1.f / (float)kNSteps : __frcp_rn((float)cnt));
@@ -458,7 +493,8 @@ template <class T> struct NStatRing {
 // The ring statistics kernel (one channel range).
 template <class T>
 __global__ void __launch_bounds__(32 * kNRedWarps, 1)
-    k_ndhwc_stats_ring(const T* __restrict__ x, NPlan p, NFwdWs ws, unsigned long long spin, uint32_t* status) {
+    k_ndhwc_stats_ring(const T* __restrict__ x, NPlan p, NFwdWs ws, unsigned long long spin, uint32_t* status,
+                       int force_timeout) {
   extern __shared__ __align__(128) unsigned char smem[];
   using Sh = NStatRing<T>;
   constexpr int kPS = Sh::kPS, kRaw = Vec<T>::kRaw;
@@ -473,6 +509,11 @@ __global__ void __launch_bounds__(32 * kNRedWarps, 1)
   NLoader<kPS> ld{n_first_unit(), 0};
   for (int i = 0; i < Sh::kSlots; ++i) ld.issue_next(p, rg, W, ring, src);
   bool failed = false;
+  if (force_timeout) {  // testing: a bounded wait on a word nothing sets, with copies in flight
+    unsigned long long i = 0;
+    while (i < spin && ld_acquire(ws.never) == 0u) ++i;
+    failed = ld_acquire(ws.never) == 0u;
+  }
   for (int64_t u = n_first_unit(); u < p.units && !failed; u += W) {
     const NUnit q = n_unit(p, u, lane);
     const int steps = n_unit_steps(p, rg, u);
@@ -498,7 +539,7 @@ __global__ void __launch_bounds__(32 * kNRedWarps, 1)
     n_stats_unit_done<T>(p, ws, q, mom, sp);
   }
   if (failed) n_record_timeout(status);
-  ring.drain(spin);
+  ring.drain(kDrainPolls);
 }
 
 // ------------------------------------------------------ forward finalize
@@ -714,9 +755,11 @@ __device__ __forceinline__ void n_grad(const T* dy, const T* res, int64_t o, uin
 }
 
 // S1 += dy, S2 += dy*(x - mean) over a batch of nv steps (wx: x, wd: the gradient).
+// Even steps go to (a1, a2), odd steps to (b1, b2): two chains per sum; the
+// caller adds the two sets when the unit is done.
 template <class T, int kB>
 __device__ __forceinline__ void n_bwd_batch(const uint4 (&wx)[kB][Vec<T>::kRaw], const uint4 (&wd)[kB][Vec<T>::kRaw],
-                                            int nv, const f2 mu[4], f2 a1[4], f2 a2[4]) {
+                                            int nv, const f2 mu[4], f2 a1[4], f2 a2[4], f2 b1[4], f2 b2[4]) {
 #pragma unroll
   for (int t = 0; t < kB; ++t) {
     if (t < nv) {
@@ -725,8 +768,13 @@ __device__ __forceinline__ void n_bwd_batch(const uint4 (&wx)[kB][Vec<T>::kRaw],
       Vec<T>::pairs(wd[t], vd);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        a1[e] = f2add(a1[e], vd[e]);
-        a2[e] = f2fma(vd[e], xm[e], a2[e]);
+        if (t & 1) {
+          b1[e] = f2add(b1[e], vd[e]);
+          b2[e] = f2fma(vd[e], xm[e], b2[e]);
+        } else {
+          a1[e] = f2add(a1[e], vd[e]);
+          a2[e] = f2fma(vd[e], xm[e], a2[e]);
+        }
       }
     }
   }
@@ -862,7 +910,7 @@ __global__ void __launch_bounds__(32 * kNRedWarps, 1)
       n_lane_means<T>(p, q, mean, mu);
       have = q.row;
     }
-    f2 a1[4] = {z2, z2, z2, z2}, a2[4] = {z2, z2, z2, z2};
+    f2 a1[4] = {z2, z2, z2, z2}, a2[4] = {z2, z2, z2, z2}, b1[4] = {z2, z2, z2, z2}, b2[4] = {z2, z2, z2, z2};
     for (int t0 = 0; t0 < q.cnt; t0 += kB) {
       const int nv = q.cnt - t0 < kB ? q.cnt - t0 : kB;
       uint4 wx[kB][kRaw], wd[kB][kRaw];
@@ -874,7 +922,12 @@ __global__ void __launch_bounds__(32 * kNRedWarps, 1)
           n_grad<T, kRelu>(dy, res, o, wd[t]);
         }
       }
-      n_bwd_batch<T>(wx, wd, nv, mu, a1, a2);
+      n_bwd_batch<T>(wx, wd, nv, mu, a1, a2, b1, b2);
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      a1[e] = f2add(a1[e], b1[e]);
+      a2[e] = f2add(a2[e], b2[e]);
     }
     n_reduce_unit_done(p, ws, q, a1, a2);
   }
@@ -917,7 +970,7 @@ __global__ void __launch_bounds__(32 * kNRedWarps, 1)
       n_lane_means<T>(p, q, mean, mu);
       have = q.row;
     }
-    f2 a1[4] = {z2, z2, z2, z2}, a2[4] = {z2, z2, z2, z2};
+    f2 a1[4] = {z2, z2, z2, z2}, a2[4] = {z2, z2, z2, z2}, b1[4] = {z2, z2, z2, z2}, b2[4] = {z2, z2, z2, z2};
     for (int t0 = 0; t0 < steps; t0 += kPS) {
       const unsigned char* slot = ring.take(spin);
       if (!slot) {
@@ -943,13 +996,18 @@ __global__ void __launch_bounds__(32 * kNRedWarps, 1)
       }
       __syncwarp();
       ld.issue_next(p, rg, W, ring, src);
-      n_bwd_batch<T>(wx, wd, nv, mu, a1, a2);
+      n_bwd_batch<T>(wx, wd, nv, mu, a1, a2, b1, b2);
     }
     if (failed) break;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      a1[e] = f2add(a1[e], b1[e]);
+      a2[e] = f2add(a2[e], b2[e]);
+    }
     n_reduce_unit_done(p, ws, q, a1, a2);
   }
   if (failed) n_record_timeout(status);
-  ring.drain(spin);
+  ring.drain(kDrainPolls);
 }
 
 // dx = dy*p1 - (x - mean)*p2 - p3 per channel, with p1 = rstd*gamma,

@@ -10,6 +10,11 @@
 
 namespace gn3d {
 
+// Poll budget of the drain after a failed wait: the bulk copies a CTA has in
+// flight always complete, and a CTA must not exit before they land in its
+// shared memory, so the drain never uses the caller's (possibly tiny) budget.
+constexpr unsigned long long kDrainPolls = 1ull << 26;
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

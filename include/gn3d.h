@@ -220,11 +220,16 @@ uint64_t gn3d_launch_count(void);
  *                            per direction), 1 streaming, 2 persistent (one
  *                            cooperative launch per direction).
  *   GN3D_DEBUG_SPIN_LIMIT    poll budget of every bounded device-side wait
- *                            (0 = default, about four seconds).
- *   GN3D_DEBUG_FORCE_TIMEOUT 1: the next persistent launch waits for a flag that
- *                            nothing sets, so its bounded wait runs out and
- *                            gn3d_stream_status reports GN3D_ERR_TIMEOUT (tests
- *                            the failure path without a fault or a hang).
+ *                            (0 = default, about four seconds).  A kernel
+ *                            whose wait gave up still waits for its own bulk
+ *                            copies in flight with the default budget before
+ *                            it exits.
+ *   GN3D_DEBUG_FORCE_TIMEOUT 1: the next persistent launch (or the next
+ *                            channels-last statistics launch with C <= 256)
+ *                            waits for a flag that nothing sets, so its bounded
+ *                            wait runs out and gn3d_stream_status reports
+ *                            GN3D_ERR_TIMEOUT (tests the failure path without a
+ *                            fault or a hang).
  *   GN3D_DEBUG_LAG           -1 automatic, else 0 .. 8: groups of lookahead
  *                            between the statistics pass and the elementwise pass.
  *   GN3D_DEBUG_SLOTS         -1 automatic, else the number of shared-memory

@@ -205,3 +205,30 @@ def test_ndhwc_full_size_sampled():
     l2 = np.sqrt(N * S * 1.0) * np.ones(C)
     assert np.all(parity.check_reduction(to_np(dgamma).astype(np.float64), dg64, l2))
     assert np.all(parity.check_reduction(to_np(dbeta).astype(np.float64), db64, l2))
+
+
+def test_ndhwc_bounded_wait_timeout_reports_and_recovers():
+    """The channels-last statistics kernel's bounded wait: a forced wait on a
+    word nothing sets gives up, the kernel drains its bulk copies and exits,
+    gn3d_stream_status reports GN3D_ERR_TIMEOUT once, and the next calls are
+    correct again."""
+    import bwd_gn3d_stats_gb300 as gn
+
+    site = synth.Site(1, 32, 16, 16, 16, 8, synth.BF16)
+    inp = synth.make_inputs(site, seed=18)
+    ref = run_cl(site, inp)
+    d = cl_inputs(site, inp)
+    st = torch().cuda.current_stream().cuda_stream
+    L = gn.lib()
+    try:
+        gn.gn3d_debug_set(gn.DEBUG_SPIN_LIMIT, 20000)
+        gn.gn3d_debug_set(gn.DEBUG_FORCE_TIMEOUT, 1)
+        run_forward_ndhwc(site, d["x"], d["gamma"], d["beta"])
+        assert L.gn3d_stream_status(st) == gn.ERR_TIMEOUT
+        assert L.gn3d_stream_status(st) == gn.OK  # read and cleared
+    finally:
+        gn.gn3d_debug_set(gn.DEBUG_FORCE_TIMEOUT, 0)
+        gn.gn3d_debug_set(gn.DEBUG_SPIN_LIMIT, 0)
+    again = run_cl(site, inp)
+    for a, b in zip(ref, again):
+        assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
