@@ -365,7 +365,7 @@ def unet_rollup(dev, flush, stream, ws):
             "min_bytes_per_stack": tot_bytes, "sites": sites}
 
 
-def ndhwc_line(site, dev, flush, stream, ws, steps):
+def ndhwc_line(site, wname, dev, flush, stream, ws, steps):
     """The same workload stored channels-last (NDHWC entry points): GB/s and the
     per-kernel device times of its six kernels."""
     import torch
@@ -383,6 +383,14 @@ def ndhwc_line(site, dev, flush, stream, ws, steps):
            "kernels": {k: {"us_per_launch": round(d["ms_per_launch"] * 1e3, 2),
                            "gbs": (round(KERNEL_TENSORS[k] * tb / (d["ms_per_launch"] * 1e-3) / 1e9, 1)
                                    if KERNEL_TENSORS[k] else None)} for k, d in kern.items()}}
+    if kern:
+        peak, peak_kind = peaks()
+        dom = max(kern, key=lambda k: kern[k]["ms_per_launch"] * kern[k]["launches"])
+        dgbs = KERNEL_TENSORS[dom] * tb / (kern[dom]["ms_per_launch"] * 1e-3) / 1e9
+        out["roofline"] = {"bound": "hbm", "kernel": dom, "achieved": round(dgbs, 1), "peak": peak,
+                           "peak_kind": peak_kind, "unit": "GB/s", "frac": round(dgbs / peak, 4),
+                           "algorithmic_bytes_per_launch": KERNEL_TENSORS[dom] * tb,
+                           "traffic": traffic_for(dom, wname + "_ndhwc")}
     del v
     torch.cuda.empty_cache()
     return out
@@ -454,7 +462,7 @@ def run_gpu(args):
             del v2
         secondary[UNET] = unet_rollup(dev, flush, stream, ws)
         if args.layout == "ncdhw":
-            secondary[args.workload + "_ndhwc"] = ndhwc_line(site, dev, flush, stream, ws, args.steps)
+            secondary[args.workload + "_ndhwc"] = ndhwc_line(site, args.workload, dev, flush, stream, ws, args.steps)
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         v, cores, sample = cpu_oracle_sample(site)
