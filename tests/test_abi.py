@@ -195,3 +195,37 @@ def test_kernel_timing_hooks_without_launches(L):
             gn.gn3d_debug_set(gn.DEBUG_TIMING, 2)
     finally:
         gn.gn3d_debug_set(gn.DEBUG_TIMING, 0)
+
+
+@pytest.mark.gpu
+def test_gpu_ndhwc_empty_tensors_and_pointer_checks(L):
+    """The channels-last entry points share the argument checks and the empty-
+    tensor results: zero-size volumes give mean 0, rstd 1/sqrt(eps) and zero
+    parameter gradients; misaligned or host pointers are rejected."""
+    import torch
+
+    st = torch.cuda.current_stream().cuda_stream
+    mean = torch.full((2 * 4,), 7.0, device="cuda")
+    rstd = torch.full((2 * 4,), 7.0, device="cuda")
+    x = torch.empty(0, device="cuda")
+    rc = L.gn3d_forward_ndhwc(x.data_ptr(), None, None, 2, 8, 0, 5, 5, 4, 1e-5, gn.F32, gn.F32, x.data_ptr(),
+                              mean.data_ptr(), rstd.data_ptr(), st)
+    assert rc == gn.OK
+    assert torch.all(mean == 0) and torch.allclose(rstd, torch.full_like(rstd, 1e-5 ** -0.5))
+    dg = torch.full((8,), 3.0, device="cuda")
+    db = torch.full((8,), 3.0, device="cuda")
+    rc = L.gn3d_backward_ndhwc(x.data_ptr(), x.data_ptr(), mean.data_ptr(), rstd.data_ptr(), None, 2, 8, 0, 5, 5, 4,
+                               gn.F32, x.data_ptr(), dg.data_ptr(), db.data_ptr(), st)
+    assert rc == gn.OK
+    torch.cuda.synchronize()
+    assert torch.all(dg == 0) and torch.all(db == 0)
+    xb = torch.zeros(64 * 8, dtype=torch.bfloat16, device="cuda")
+    yb = torch.empty_like(xb)
+    rc = L.gn3d_forward_ndhwc(xb.data_ptr() + 2, None, None, 1, 8, 1, 1, 63, 2, 1e-5, gn.BF16, gn.BF16,
+                              yb.data_ptr(), None, None, st)
+    assert rc == gn.ERR_INVALID_ARG
+    h = np.zeros(64 * 8, dtype=np.uint16)
+    rc = L.gn3d_forward_ndhwc(xb.data_ptr(), None, None, 1, 8, 1, 1, 64, 2, 1e-5, gn.BF16, gn.BF16, h.ctypes.data,
+                              None, None, st)
+    assert rc == gn.ERR_DEVICE
+    assert L.gn3d_stream_status(st) == gn.OK

@@ -232,3 +232,38 @@ def test_ndhwc_bounded_wait_timeout_reports_and_recovers():
     again = run_cl(site, inp)
     for a, b in zip(ref, again):
         assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
+
+
+def test_ndhwc_two_level_finalize_sampled():
+    """A shape whose rows hold more than one finalize chunk (256 channels: units
+    of 64 positions, 66^3 positions -> 4493 units per row, two chunks), so both
+    finalize kernels take their two-level path: complete statistics and
+    parameter gradients, and a seeded sample of y and dx, against the oracle."""
+    site = synth.Site(1, 256, 66, 66, 66, 8, synth.BF16)
+    inp = synth.make_inputs(site, seed=19)
+    N, C, S, G = site.N, site.C, site.S, site.G
+    d = cl_inputs(site, inp)
+    y, mean, rstd = run_forward_ndhwc(site, d["x"], d["gamma"], d["beta"])
+    dx, dgamma, dbeta = run_backward_ndhwc(site, d["dy"], d["x"], mean, rstd, d["gamma"])
+    torch().cuda.synchronize()
+    mg, rg = to_np(mean).astype(np.float64), to_np(rstd).astype(np.float64)
+    m64, r64 = stats_check(site, inp, mg, rg)
+    rng = np.random.default_rng(9)
+    icl = np.unique(np.concatenate([rng.integers(0, site.numel, 100_000), np.arange(64),
+                                    site.numel - 1 - np.arange(64)]))
+    inc = oracle.ndhwc_index(icl, N, C, S)
+    y64 = oracle.forward_at(inp["x"], inp["gamma"], inp["beta"], N, C, S, G, m64, r64, inc)
+    xv = synth.bits_to_f32(inp["x"])[inc].astype(np.float64)
+    dyv = synth.bits_to_f32(inp["dy"])[inc].astype(np.float64)
+    ng = (inc // S) // (C // G)
+    c = (inc // S) % C
+    tg = (np.abs(xv) + np.abs(m64[ng])) * r64[ng] * np.abs(inp["gamma"][c]) + np.abs(inp["beta"][c])
+    check_out(site.dtype, to_np(y)[icl], y64, tg, "y(sampled)")
+    dx64, dg64, db64 = oracle.backward_at(inp["dy"], inp["x"], mg, rg, inp["gamma"], N, C, S, G, inc)
+    td = rg[ng] * (np.abs(dyv) * np.abs(inp["gamma"][c]) + 1.0 + (np.abs(xv) + np.abs(mg[ng])) * rg[ng])
+    check_out(site.dtype, to_np(dx)[icl], dx64, td, "dx(sampled)")
+    xf = synth.bits_to_f32(inp["x"]).astype(np.float64)
+    dyf = synth.bits_to_f32(inp["dy"]).astype(np.float64)
+    l2g, l2b = param_l2(dyf, xf, mg, rg, N, C, S, G)
+    assert np.all(parity.check_reduction(to_np(dgamma).astype(np.float64), dg64, l2g))
+    assert np.all(parity.check_reduction(to_np(dbeta).astype(np.float64), db64, l2b))
