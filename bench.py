@@ -237,39 +237,72 @@ KERNEL_TENSORS = {"k_fwd_fused": 2, "k_fwd_stats": 1, "k_fwd_norm": 2,
 
 
 def time_e2e(vol, steps, warmup, stream):
-    """Per-step time with the host<->device copies: H2D x, dy from pinned memory;
-    fwd; bwd; D2H y, dx, mean, rstd, dgamma, dbeta to pinned memory."""
+    """Per-step time with the host<->device copies inside the timed region, every
+    step: H2D x, dy from pinned memory; fwd; bwd; D2H y, dx, mean, rstd, dgamma,
+    dbeta to pinned memory.  The copies run as a user would pipeline them: H2D on
+    one copy stream, D2H on another, compute on `stream`, with two device buffer
+    sets so that step i+1's inputs arrive while step i computes and step i's
+    results leave (events order every use of a buffer set)."""
+    import copy
+
     import torch
 
-    st = stream.cuda_stream
     s = vol.site
+    h2d, d2h = torch.cuda.Stream(stream.device), torch.cuda.Stream(stream.device)
+    v2 = copy.copy(vol)  # same host buffers and parameters, own device buffers
+    for name in ("x", "dy", "y", "dx", "mean", "rstd", "dgamma", "dbeta"):
+        setattr(v2, name, torch.empty_like(getattr(vol, name)))
+    sets = [vol, v2]
+    free = [None, None]  # event: the set's results have left the device
 
-    def step():
-        vol.x.copy_(vol.h_x, non_blocking=True)
-        vol.dy.copy_(vol.h_dy, non_blocking=True)
-        vol.fwd(st)
-        vol.bwd(st)
-        vol.h_y.copy_(vol.y, non_blocking=True)
-        vol.h_dx.copy_(vol.dx, non_blocking=True)
-        k = 0
-        for t in (vol.mean, vol.rstd, vol.dgamma, vol.dbeta):
-            vol.h_small[k:k + t.numel()].copy_(t, non_blocking=True)
-            k += t.numel()
+    def step(i):
+        v = sets[i % 2]
+        ev = lambda: torch.cuda.Event()  # noqa: E731
+        with torch.cuda.stream(h2d):
+            if free[i % 2] is not None:
+                h2d.wait_event(free[i % 2])
+            v.x.copy_(v.h_x, non_blocking=True)
+            ex = ev()
+            ex.record(h2d)
+            v.dy.copy_(v.h_dy, non_blocking=True)
+            edy = ev()
+            edy.record(h2d)
+        stream.wait_event(ex)
+        v.fwd(stream.cuda_stream)
+        efwd = ev()
+        efwd.record(stream)
+        stream.wait_event(edy)
+        v.bwd(stream.cuda_stream)
+        ebwd = ev()
+        ebwd.record(stream)
+        with torch.cuda.stream(d2h):
+            d2h.wait_event(efwd)
+            v.h_y.copy_(v.y, non_blocking=True)
+            d2h.wait_event(ebwd)
+            v.h_dx.copy_(v.dx, non_blocking=True)
+            k = 0
+            for t in (v.mean, v.rstd, v.dgamma, v.dbeta):
+                v.h_small[k:k + t.numel()].copy_(t, non_blocking=True)
+                k += t.numel()
+            free[i % 2] = ev()
+            free[i % 2].record(d2h)
 
-    with torch.cuda.stream(stream):
-        for _ in range(warmup):
-            step()
-        stream.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(steps):
-            step()
-        b.record(stream)
-        stream.synchronize()
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize(stream.device)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    h2d.wait_event(a)
+    d2h.wait_event(a)
+    for i in range(steps):
+        step(i)
+    stream.wait_event(free[(steps - 1) % 2])
+    b.record(stream)
+    torch.cuda.synchronize(stream.device)
     eb = s.numel * s.elem_bytes
-    h2d = 2 * eb + 2 * s.C * 4
-    d2h = 2 * eb + (2 * s.C + 2 * s.N * s.G) * 4
-    return a.elapsed_time(b) / steps, h2d, d2h
+    h2d_b = 2 * eb  # x, dy (gamma and beta stay on the device)
+    d2h_b = 2 * eb + (2 * s.C + 2 * s.N * s.G) * 4  # y, dx, mean, rstd, dgamma, dbeta
+    return a.elapsed_time(b) / steps, h2d_b, d2h_b
 
 
 def oracle_sample_site(site: synth.Site):
@@ -341,7 +374,7 @@ def barrier(ws):
         dist.barrier()
 
 
-def unet_rollup(dev, flush, stream, ws):
+def unet_rollup(dev, flush, stream, ws, layout="ncdhw"):
     """Per-site device time of the UNet site stack (each distinct shape timed once,
     counted as often as the stack holds it) and the stack's effective GB/s."""
     import torch
@@ -351,7 +384,7 @@ def unet_rollup(dev, flush, stream, ws):
         distinct.setdefault(s.name(), [s, 0])[1] += 1
     sites, tot_bytes, tot_ms = [], 0, 0.0
     for name, (s2, count) in distinct.items():
-        v2 = Volume(s2, dev, pinned=False)
+        v2 = Volume(s2, dev, pinned=False, layout=layout)
         t2, _, _ = time_device([v2], 5, 3, flush, stream)
         ms2 = max_over_ranks(sum(t2) / len(t2), ws, dev)
         fb, bb = s2.min_bytes()
@@ -463,6 +496,7 @@ def run_gpu(args):
         secondary[UNET] = unet_rollup(dev, flush, stream, ws)
         if args.layout == "ncdhw":
             secondary[args.workload + "_ndhwc"] = ndhwc_line(site, args.workload, dev, flush, stream, ws, args.steps)
+            secondary[UNET + "_ndhwc"] = unet_rollup(dev, flush, stream, ws, layout="ndhwc")
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         v, cores, sample = cpu_oracle_sample(site)
