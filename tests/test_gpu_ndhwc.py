@@ -129,16 +129,20 @@ def test_ndhwc_deterministic():
             assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
 
 
-def test_ndhwc_relu_is_relu_of_forward():
+@pytest.mark.parametrize("shape", [(1, 32, 12, 12, 12, 8, synth.BF16), (2, 16, 6, 7, 8, 4, synth.F32),
+                                   (1, 512, 4, 4, 5, 8, synth.BF16)],
+                         ids=["bf16_ring", "f32_ring", "bf16_two_ranges"])
+def test_ndhwc_relu_is_relu_of_forward(shape):
     """The fused ReLU forward is bit for bit F.relu of the plain forward; its
     backward matches the oracle's backward of relu(GroupNorm) at the saved statistics."""
-    site = synth.Site(1, 32, 12, 12, 12, 8, synth.BF16)
+    site = synth.Site(*shape)
     inp = synth.make_inputs(site, seed=16)
     t = torch()
     d = cl_inputs(site, inp)
     y, m, r = run_forward_ndhwc(site, d["x"], d["gamma"], d["beta"])
     yr, mr, rr = run_forward_ndhwc(site, d["x"], d["gamma"], d["beta"], relu=True)
-    assert t.equal(t.nn.functional.relu(y).view(t.int16), yr.view(t.int16))
+    iv = t.int16 if site.dtype == synth.BF16 else t.int32
+    assert t.equal(t.nn.functional.relu(y).view(iv), yr.view(iv))
     assert t.equal(m, mr) and t.equal(r, rr)
     dx, dg, db = run_backward_ndhwc(site, d["dy"], d["x"], mr, rr, d["gamma"], out=yr)
     t.cuda.synchronize()
