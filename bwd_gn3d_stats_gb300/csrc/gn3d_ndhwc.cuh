@@ -1,5 +1,7 @@
-// gn3d_ndhwc.cuh -- GroupNorm over channels-last (NDHWC) volumes: the plan and
-// the four streaming kernels (statistics, normalize, backward reduction, dx).
+// gn3d_ndhwc.cuh -- GroupNorm over channels-last (NDHWC) volumes: six kernels,
+// three per direction (streaming statistics, finalize, normalize; streaming
+// reduction, finalize, dx), chained by dependent launches.  The plan is in
+// gn3d_ndhwc_plan.cuh.
 //
 // Layout.  x[n][s][c], s = (d*H + h)*W + w -- the channels_last_3d memory
 // format of an NCDHW tensor (ScaFFold's Triton GroupNorm reads channels-last
@@ -20,10 +22,13 @@
 // per unit, at most kNSteps vectors per lane.  Statistics merge in a fixed tree
 // that depends on the shape alone: lane -> channel (the lp lanes of a channel,
 // pairwise) -> piece (the channels of one group inside the range), per unit,
-// in the streaming kernel; the pieces -> group in a finalize kernel, one CTA per
-// group.  The backward keeps per-channel sums (the weight gradient needs them):
-// unit -> row (n, c), one CTA per row -> group coefficients and parameter
-// gradients.  The streaming kernels only store their unit results: a round trip
+// in the streaming kernel; the pieces -> group in the finalize kernel, one CTA
+// per chunk of kNFinChunk units, then the chunk partials in order.  The
+// backward keeps per-channel sums (the weight gradient needs them): unit -> row
+// (n, c) the same way -> group coefficients and parameter gradients.  With one
+// channel range (C <= 256) the streaming kernels read through warp-private
+// rings of bulk copies; otherwise with vector loads.  They only store their
+// unit results: a round trip
 // to L2 (an arrival counter, a merge's loads) costs microseconds while the
 // stream saturates DRAM, and a warp that waits for one falls behind.
 //
