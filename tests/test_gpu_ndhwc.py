@@ -180,10 +180,14 @@ def test_ndhwc_agrees_with_ncdhw():
     assert np.allclose(db_cl, to_np(db), rtol=1e-4, atol=1e-3)
 
 
-def test_ndhwc_full_size_sampled():
-    """The 1x32x128^3 bf16 volume, channels-last: complete statistics and
-    parameter gradients, and a seeded sample of y and dx, against the oracle."""
-    site = synth.WORKLOADS["bf16_1x32x128^3_G8"].sites[0]
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["bf16_1x32x128^3_G8", "bf16_2x64x96^3_G32", "bf16_2x64x96^3_G32_offset1e3",
+                                  "bf16_1x32x256^3_G8"])
+def test_ndhwc_full_size_sampled(name):
+    """The bench volumes stored channels-last (including the 1e3 mean-offset
+    cancellation probe): complete statistics and parameter gradients, and a
+    seeded sample of y and dx, against the oracle."""
+    site = synth.WORKLOADS[name].sites[0]
     inp = synth.make_inputs(site, seed=0)
     N, C, S, G = site.N, site.C, site.S, site.G
     d = cl_inputs(site, inp)
