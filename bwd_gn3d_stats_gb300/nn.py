@@ -28,6 +28,15 @@ from . import forward_ndhwc as _forward_ndhwc
 from . import is_ndhwc as _is_ndhwc
 
 
+def _aligned(t: torch.Tensor, memory_format=torch.contiguous_format) -> torch.Tensor:
+    """t in the given memory format, starting on a 16-byte boundary (the C ABI's
+    vector loads need it; a view with an odd storage offset is copied)."""
+    t = t.contiguous(memory_format=memory_format)
+    if t.data_ptr() % 16:
+        t = t.clone(memory_format=memory_format)
+    return t
+
+
 def _check_input(x: torch.Tensor):
     if not x.is_cuda:
         raise RuntimeError("libgn3d runs on CUDA tensors only (there is no CPU path)")
@@ -48,8 +57,7 @@ class GroupNorm3dFunction(torch.autograd.Function):
             raise ValueError("the fused ReLU's backward gates on the forward's result in x's dtype: "
                              "out_dtype must equal x.dtype when relu is set")
         ndhwc = _is_ndhwc(x) and x.shape[1] % 8 == 0
-        if not ndhwc:
-            x = x.contiguous()
+        x = _aligned(x, torch.channels_last_3d if ndhwc else torch.contiguous_format)
         w = None if weight is None else weight.detach().float().contiguous()
         b = None if bias is None else bias.detach().float().contiguous()
         fwd = _forward_ndhwc if ndhwc else _forward
@@ -66,10 +74,10 @@ class GroupNorm3dFunction(torch.autograd.Function):
     def backward(ctx, dy):
         x, w, mean, rstd, y = ctx.saved_tensors
         if ctx.ndhwc:
-            dy = dy.to(x.dtype).contiguous(memory_format=torch.channels_last_3d)
+            dy = _aligned(dy.to(x.dtype), torch.channels_last_3d)
             dx, dgamma, dbeta = _backward_ndhwc(dy, x, mean, rstd, w, ctx.num_groups, out=y if ctx.relu else None)
         else:
-            dy = dy.to(x.dtype).contiguous()
+            dy = _aligned(dy.to(x.dtype))
             dx, dgamma, dbeta = _backward(dy, x, mean, rstd, w, ctx.num_groups, out=y if ctx.relu else None)
         gw = dgamma.to(ctx.weight_dtype) if ctx.weight_dtype is not None and ctx.needs_input_grad[1] else None
         gb = dbeta.to(ctx.bias_dtype) if ctx.bias_dtype is not None and ctx.needs_input_grad[2] else None

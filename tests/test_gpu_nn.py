@@ -138,3 +138,27 @@ def test_channels_last_with_c_not_multiple_of_8_takes_ncdhw():
     y = m(x)
     ref = t.nn.functional.group_norm(x.contiguous(), 3, m.weight, m.bias, 1e-5)
     assert t.allclose(y, ref, rtol=1e-5, atol=1e-5)
+
+
+def test_misaligned_views_are_handled():
+    """Views whose storage offset breaks 16-byte alignment (the C ABI rejects
+    those pointers) still run: the front end copies them to an aligned buffer."""
+    from bwd_gn3d_stats_gb300.nn import group_norm_3d
+
+    t = torch()
+    gen = t.Generator(device="cuda").manual_seed(9)
+    base = t.randn(1 + 2 * 16 * 6 * 6 * 6, device="cuda", generator=gen).to(t.bfloat16)
+    x = base[1:].view(2, 16, 6, 6, 6)  # 2-byte offset
+    assert x.data_ptr() % 16 != 0
+    w = t.rand(16, device="cuda", generator=gen) + 0.5
+    b = t.randn(16, device="cuda", generator=gen)
+    y = group_norm_3d(x, 4, w, b)
+    y_ref = group_norm_3d(x.clone(), 4, w, b)
+    assert t.equal(y.view(t.int16), y_ref.view(t.int16))
+    dyb = t.randn(1 + y.numel(), device="cuda", generator=gen).to(t.bfloat16)
+    dy = dyb[1:].view_as(y)
+    xr2 = x.clone().requires_grad_()
+    group_norm_3d(xr2, 4, w, b).backward(dy)
+    xr3 = x.clone().requires_grad_()
+    group_norm_3d(xr3, 4, w, b).backward(dy.clone())
+    assert t.equal(xr2.grad.view(t.int16), xr3.grad.view(t.int16))
