@@ -429,6 +429,61 @@ def ndhwc_line(site, wname, dev, flush, stream, ws, steps):
     return out
 
 
+def relu_line(site, dev, flush, stream, ws, steps):
+    """GroupNorm + ReLU, fused (gn3d_forward_relu / gn3d_backward_relu) against
+    the unfused sequence a caller would otherwise run: gn3d_forward, torch's
+    relu, torch's threshold_backward on the incoming gradient, gn3d_backward."""
+    import torch
+
+    import bwd_gn3d_stats_gb300 as gn
+
+    v = Volume(site, dev, pinned=False)
+    out = torch.empty_like(v.y)
+    s = site
+    c = gn.BF16 if s.dtype == synth.BF16 else gn.F32
+    st = stream.cuda_stream
+
+    def fused():
+        gn.gn3d_forward_relu(v.x.data_ptr(), v.gamma.data_ptr(), v.beta.data_ptr(), s.N, s.C, s.D, s.H, s.W, s.G,
+                             s.eps, c, c, out.data_ptr(), v.mean.data_ptr(), v.rstd.data_ptr(), st)
+        gn.gn3d_backward_relu(v.dy.data_ptr(), v.x.data_ptr(), out.data_ptr(), v.mean.data_ptr(), v.rstd.data_ptr(),
+                              v.gamma.data_ptr(), s.N, s.C, s.D, s.H, s.W, s.G, c, v.dx.data_ptr(),
+                              v.dgamma.data_ptr(), v.dbeta.data_ptr(), st)
+
+    def unfused():
+        v.fwd(st)
+        r = torch.relu(v.y)
+        g = torch.ops.aten.threshold_backward(v.dy, r, 0)
+        gn.gn3d_backward(g.data_ptr(), v.x.data_ptr(), v.mean.data_ptr(), v.rstd.data_ptr(), v.gamma.data_ptr(),
+                         s.N, s.C, s.D, s.H, s.W, s.G, c, v.dx.data_ptr(), v.dgamma.data_ptr(), v.dbeta.data_ptr(),
+                         st)
+
+    res = {}
+    with torch.cuda.stream(stream):
+        for name, fn in (("fused", fused), ("unfused", unfused)):
+            for _ in range(3):
+                fn()
+            stream.synchronize()
+            evs = []
+            for _ in range(steps):
+                flush.fill_(1)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                evs.append((a, b))
+            stream.synchronize()
+            res[name] = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs) / steps, ws, dev)
+    tb = site.numel * site.elem_bytes
+    fused_bytes = 6 * tb  # x -> out forward; x, dy, out -> dx backward
+    del v, out
+    torch.cuda.empty_cache()
+    return {"value": round(ws * fused_bytes / (res["fused"] * 1e-3) / 1e9, 1), "unit": UNIT,
+            "bytes": "x, out forward; x, dy, out, dx backward",
+            "fused_ms_per_step": round(res["fused"], 4), "unfused_ms_per_step": round(res["unfused"], 4),
+            "unfused_over_fused": round(res["unfused"] / res["fused"], 3)}
+
+
 def run_gpu(args):
     import torch
 
@@ -495,6 +550,7 @@ def run_gpu(args):
             del v2
         secondary[UNET] = unet_rollup(dev, flush, stream, ws)
         if args.layout == "ncdhw":
+            secondary[args.workload + "_relu"] = relu_line(site, dev, flush, stream, ws, args.steps)
             secondary[args.workload + "_ndhwc"] = ndhwc_line(site, args.workload, dev, flush, stream, ws, args.steps)
             secondary[UNET + "_ndhwc"] = unet_rollup(dev, flush, stream, ws, layout="ndhwc")
     cpu = None
