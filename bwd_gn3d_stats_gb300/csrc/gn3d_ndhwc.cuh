@@ -459,12 +459,7 @@ struct NRing {
 };
 
 // Steps of unit u (one range: lp positions per step).
-__device__ __forceinline__ int n_unit_steps(const NPlan& p, const NRange& rg, int64_t u) {
-  const int64_t k = u % p.R, len = p.S - k * p.Pu < p.Pu ? p.S - k * p.Pu : p.Pu;
-  return (int)((len + rg.lp - 1) / rg.lp);
-}
-
-// The loader of a ring: part `part` of unit u, over the warp's units.
+// The loader of a ring: part `part` of unit u (n_ring_part), over the warp's units.
 template <int kPS>
 struct NLoader {
   int64_t u;
@@ -473,13 +468,10 @@ struct NLoader {
   __device__ __forceinline__ void issue_next(const NPlan& p, const NRange& rg, int64_t W, Ring& ring,
                                              const T* const* src) {
     if (u >= p.units) return;
-    const int64_t k = u % p.R, n = u / p.R;
-    const int64_t len = p.S - k * p.Pu < p.Pu ? p.S - k * p.Pu : p.Pu;
-    const int64_t span = (int64_t)kPS * kVec * rg.lw, total = len * p.C;
-    const int64_t e0 = (n * p.S + k * p.Pu) * p.C + part * span;
-    const int64_t rest = total - part * span;
-    ring.issue(src, e0, rest < span ? rest : span);
-    if ((int64_t)(part + 1) * span >= total) {
+    int64_t e0, n;
+    const bool last = n_ring_part(p, rg, u, part, kPS, e0, n);
+    ring.issue(src, e0, n);
+    if (last) {
       part = 0;
       u += W;
     } else {

@@ -108,4 +108,24 @@ __host__ __device__ inline void n_piece(const NPlan& p, const NRange& rg, int64_
   c1 = (e < rg.c1 ? e : rg.c1) - rg.c0;
 }
 
+// Ring form (one channel range, so a unit is one contiguous span of len*C
+// elements and step i its 8*lw elements from i*8*lw on): the steps of unit u,
+// and part `part` of kPS steps -- elements [e0, e0 + n) -- returning whether it
+// is the unit's last part.
+__host__ __device__ inline int n_unit_steps(const NPlan& p, const NRange& rg, int64_t u) {
+  const int64_t k = u % p.R, len = p.S - k * p.Pu < p.Pu ? p.S - k * p.Pu : p.Pu;
+  return (int)((len + rg.lp - 1) / rg.lp);
+}
+
+__host__ __device__ inline bool n_ring_part(const NPlan& p, const NRange& rg, int64_t u, int part, int kPS,
+                                            int64_t& e0, int64_t& n) {
+  const int64_t k = u % p.R, s = u / p.R;
+  const int64_t len = p.S - k * p.Pu < p.Pu ? p.S - k * p.Pu : p.Pu;
+  const int64_t span = (int64_t)kPS * kNVec * rg.lw, total = len * p.C;
+  e0 = (s * p.S + k * p.Pu) * p.C + part * span;
+  const int64_t rest = total - part * span;
+  n = rest < span ? rest : span;
+  return (int64_t)(part + 1) * span >= total;
+}
+
 }  // namespace gn3d
