@@ -39,15 +39,22 @@ _lock = threading.Lock()
 _lib = None
 
 
+def compile_source(src: str, out: str) -> str:
+    """gcc -> shared library, with the oracle's flags (OpenMP, no FMA contraction,
+    IEEE math).  The tests also use it to build deliberately broken copies."""
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
+           src, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
 def build(force: bool = False) -> str:
-    """Compile the oracle with gcc (OpenMP, no FMA contraction, IEEE math)."""
+    """Compile the oracle (once; again when the source is newer)."""
     os.makedirs(_BUILD, exist_ok=True)
     if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
-        tmp = _SO + f".tmp{os.getpid()}"
-        cmd = ["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
-               "-fno-fast-math", _SRC, "-o", tmp, "-lm"]
-        subprocess.run(cmd, check=True)
-        os.replace(tmp, _SO)
+        compile_source(_SRC, _SO)
     return _SO
 
 
@@ -55,7 +62,9 @@ def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
+            # GN3D_ORACLE_LIB: a library built from a modified copy of the source
+            # (tests/test_oracle_mutants.py checks that the pins reject such copies)
+            lib = ctypes.CDLL(os.environ.get("GN3D_ORACLE_LIB") or build())
             i64, vp, dp, fp = ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
             lib.gn3d_oracle_stats.argtypes = [vp, ctypes.c_int, i64, i64, i64, i64, ctypes.c_double, dp, dp, dp]
             lib.gn3d_oracle_forward.argtypes = [vp, ctypes.c_int, fp, fp, i64, i64, i64, i64,

@@ -1,0 +1,115 @@
+"""The oracle's pins reject plausible mistakes.
+
+Each mutant is a copy of oracle/gn3d_oracle.c with one plausible mistake: a
+dropped term, a wrong sign, index, divisor or rounding step. It is compiled
+into a temporary library, and tests/test_oracle.py runs against it in a child
+process (GN3D_ORACLE_LIB); every mutant must make a pin fail.  The
+channels-last adapters are mutated in-process, with a transposed reshape or a
+wrong index map, and their pins must fail too.  The real oracle source is
+never modified.
+"""
+import os
+import subprocess
+import sys
+import types
+
+import numpy as np
+import pytest
+
+import oracle
+
+from . import test_oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "gn3d_oracle.c")
+
+MUTANTS = {
+    "eps_outside_sqrt": ("rstd[ng] = 1.0 / sqrt(v + e);", "rstd[ng] = 1.0 / sqrt(v) + e;"),
+    "unbiased_variance": ("const double v = M ? nsum_val(&s2) / (double)M : 0.0;",
+                          "const double v = M > 1 ? nsum_val(&s2) / (double)(M - 1) : 0.0;"),
+    "eps_not_fp32": ("static double eps_as_used(double eps) { return (double)(float)eps; }",
+                     "static double eps_as_used(double eps) { return eps; }"),
+    "beta_sign": ("return (xv - mu) * r * gam + bet;", "return (xv - mu) * r * gam - bet;"),
+    "gamma_index": ("const double gam = param(gamma, c, 1.0), bet = param(beta, c, 0.0);",
+                    "const double gam = param(gamma, c / Cg, 1.0), bet = param(beta, c, 0.0);"),
+    "dx_drop_a": ("return r * (dyv * gam - a - xh * b);", "return r * (dyv * gam - xh * b);"),
+    "dx_drop_b": ("return r * (dyv * gam - a - xh * b);", "return r * (dyv * gam - a);"),
+    "dx_sign_b": ("return r * (dyv * gam - a - xh * b);", "return r * (dyv * gam - a + xh * b);"),
+    "dgamma_without_xhat": ("nsum_add(&sdyx, d * xh);", "nsum_add(&sdyx, d);"),
+    "b_without_gamma": ("nsum_add(&sgx, d * gam * xh);", "nsum_add(&sgx, d * xh);"),
+    "bf16_widening": ("<< 16;", "<< 15;"),
+    "bf16_rounding_position": ("int q = e - 8;", "int q = e - 9;"),
+    "group_base": ("const int64_t base = ng * M;", "const int64_t base = ng * S;"),
+    "relu_minus_zero": ("out[i] = (v[i] < 0.0) ? 0.0 : v[i];", "out[i] = (v[i] <= 0.0) ? 0.0 : v[i];"),
+    "relu_gate_strict": ("if (gate && widen(gate, dtype, i) <= 0.0) return 0.0;",
+                         "if (gate && widen(gate, dtype, i) < 0.0) return 0.0;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_reject_mutant(name, tmp_path):
+    a, b = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(a) == 1, f"mutation anchor for {name} not found once"
+    msrc = tmp_path / "gn3d_oracle.c"
+    msrc.write_text(src.replace(a, b))
+    lib = oracle.compile_source(str(msrc), str(tmp_path / "libgn3d_oracle_mutant.so"))
+    env = dict(os.environ, GN3D_ORACLE_LIB=lib)
+    r = subprocess.run([sys.executable, "-m", "pytest", "tests/test_oracle.py", "-x", "-q", "-p", "no:cacheprovider"],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-1500:]}"
+    assert " failed" in r.stdout, f"mutant {name} did not fail a pin (collection or build error?):\n{r.stdout[-1500:]}"
+
+
+def _mutated_oracle(**overrides):
+    m = types.SimpleNamespace(**{k: getattr(oracle, k) for k in dir(oracle) if not k.startswith("__")})
+    for k, v in overrides.items():
+        setattr(m, k, v)
+    return m
+
+
+def _wrong_to_ncdhw(a, N, C, S):
+    return np.ascontiguousarray(np.asarray(a).reshape(N, C, S)).reshape(-1)  # no transpose
+
+
+def _wrong_to_ndhwc(a, N, C, S):
+    return np.ascontiguousarray(np.asarray(a).reshape(N, S, C)).reshape(-1)  # no transpose
+
+
+def _fwd_with(to_ncdhw, to_ndhwc):
+    def forward_ndhwc(x, gamma, beta, N, C, S, G, eps):
+        y, mean, rstd = oracle.forward(to_ncdhw(x, N, C, S), gamma, beta, N, C, S, G, eps)
+        return to_ndhwc(y, N, C, S), mean, rstd
+    return forward_ndhwc
+
+
+def _bwd_with(to_ncdhw, to_ndhwc):
+    def backward_ndhwc(dy, x, mean, rstd, gamma, N, C, S, G, want_dx=True):
+        dx, dg, db = oracle.backward(to_ncdhw(dy, N, C, S), to_ncdhw(x, N, C, S), mean, rstd, gamma, N, C, S, G,
+                                     want_dx)
+        return (to_ndhwc(dx, N, C, S) if want_dx else None), dg, db
+    return backward_ndhwc
+
+
+def test_channels_last_pins_reject_mutants():
+    mutants = {
+        "untransposed_input": _mutated_oracle(forward_ndhwc=_fwd_with(_wrong_to_ncdhw, oracle.ncdhw_to_ndhwc),
+                                              backward_ndhwc=_bwd_with(_wrong_to_ncdhw, oracle.ncdhw_to_ndhwc),
+                                              ndhwc_to_ncdhw=_wrong_to_ncdhw),
+        "untransposed_output": _mutated_oracle(forward_ndhwc=_fwd_with(oracle.ndhwc_to_ncdhw, _wrong_to_ndhwc),
+                                               backward_ndhwc=_bwd_with(oracle.ndhwc_to_ncdhw, _wrong_to_ndhwc),
+                                               ncdhw_to_ndhwc=_wrong_to_ndhwc),
+        "index_map_swapped": _mutated_oracle(
+            ndhwc_index=lambda idx, N, C, S: (np.asarray(idx) % S) * C + np.asarray(idx) // S),
+    }
+    pins = [test_oracle.test_ndhwc_layout_brute_force, test_oracle.test_ndhwc_matches_torch_channels_last_float64,
+            test_oracle.test_ndhwc_index_and_permutations_agree]
+    for name, orc in mutants.items():
+        caught = False
+        for pin in pins:
+            try:
+                pin(orc)
+            except (AssertionError, ValueError, IndexError):
+                caught = True
+                break
+        assert caught, f"channels-last mutant {name} survived the pins"
