@@ -39,7 +39,9 @@
  *     `stream`; results are ready when the stream reaches the call.
  *   - Ownership: the caller owns every buffer; the library keeps no pointer
  *     after a call returns.  Per-call scratch is allocated and freed
- *     stream-ordered on `stream` (cudaMallocAsync / cudaFreeAsync).
+ *     stream-ordered on `stream` (cudaMallocAsync / cudaFreeAsync), so calls
+ *     can be captured into a CUDA graph and replayed (make one call on the
+ *     device first, outside the capture).
  *   - Return value: GN3D_OK, or an error code below; on error nothing has been
  *     enqueued.  gn3d_error_string() describes the code and, for
  *     GN3D_ERR_CUDA, the CUDA error of the calling thread's last failure.
