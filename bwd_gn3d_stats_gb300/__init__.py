@@ -264,7 +264,7 @@ def backward(dy, x, mean, rstd, gamma, G: int, out=None):
 
 # ------------------------------------------------------------ testing hooks
 
-DEBUG_PATH, DEBUG_SPIN_LIMIT, DEBUG_FORCE_TIMEOUT, DEBUG_LAG, DEBUG_SLOTS, DEBUG_TIMING = range(6)
+DEBUG_PATH, DEBUG_SPIN_LIMIT, DEBUG_FORCE_TIMEOUT, DEBUG_LAG, DEBUG_SLOTS, DEBUG_TIMING, DEBUG_SHARES = range(7)
 PATH_AUTO, PATH_STREAMING, PATH_FUSED = 0, 1, 2
 
 

@@ -36,6 +36,7 @@ std::atomic<long long> g_hook_spin{0};     // 0 default poll budget
 std::atomic<long long> g_hook_timeout{0};  // 1: the next fused launch waits on a flag nothing sets
 std::atomic<long long> g_hook_lag{-1};     // -1 auto
 std::atomic<long long> g_hook_slots{-1};   // -1 auto
+std::atomic<int> g_hook_shares{-1};        // -1 auto, 0 strided blocks, 1 unit shares
 
 constexpr unsigned long long kDefaultSpin = 1ull << 26;  // ~4 s of polls at 64 ns sleeps
 
@@ -132,6 +133,13 @@ int grid_for(const DevInfo& di, int64_t units, int per_sm) {
   int64_t g = (int64_t)di.sms * per_sm;
   if (g > units) g = units;
   return (int)(g < 1 ? 1 : g);
+}
+
+// Strided blocks or unit shares for the NCDHW streaming kernels' nw warps
+// (placement only).
+bool unit_shares(const Plan& p, int64_t nw) {
+  const int h = g_hook_shares.load();
+  return h < 0 ? use_unit_shares(p, nw) : h == 1;
 }
 
 // Scratch carved out of one stream-ordered allocation, 256-byte aligned pieces.
@@ -290,6 +298,17 @@ int coop_grid(const void* func, int threads, int smem, const DevInfo& di, int* g
 }
 
 // --------------------------------------------------------------- forward
+// The normalize kernel for a plan: full units or not, fused ReLU or not, layout.
+template <class TI, class TO>
+auto norm_kernel(bool full, bool relu, bool cut) {
+  using K = decltype(&k_fwd_norm<TI, TO, true, true, true>);
+  const K ks[8] = {k_fwd_norm<TI, TO, false, false, false>, k_fwd_norm<TI, TO, false, false, true>,
+                   k_fwd_norm<TI, TO, false, true, false>,  k_fwd_norm<TI, TO, false, true, true>,
+                   k_fwd_norm<TI, TO, true, false, false>,  k_fwd_norm<TI, TO, true, false, true>,
+                   k_fwd_norm<TI, TO, true, true, false>,   k_fwd_norm<TI, TO, true, true, true>};
+  return ks[(full ? 4 : 0) + (relu ? 2 : 0) + (cut ? 1 : 0)];
+}
+
 template <class TI, class TO>
 int launch_forward(const void* x, const float* gamma, const float* beta, const Plan& p, float eps, void* y,
                    float* mean, float* rstd, cudaStream_t st, DevInfo& di, bool relu) {
@@ -334,12 +353,14 @@ int launch_forward(const void* x, const float* gamma, const float* beta, const P
     using Shape = FwdStatShape<TI>;
     const int smem = Shape::kWarps * WarpRing<TI, 1, Shape::kSlots>::kWarpBytes;
     const bool full = plan_all_full(p);
-    auto ks = full ? k_fwd_stats<TI, true> : k_fwd_stats<TI, false>;
+    // one CTA per SM (fewer only when there are fewer units than SMs), every SM
+    // an equal part of the work in either layout
+    const int sgrid = grid_for(di, p.units, 1);
+    const bool cut = unit_shares(p, (int64_t)sgrid * Shape::kWarps);
+    auto ks = full ? (cut ? k_fwd_stats<TI, true, true> : k_fwd_stats<TI, true, false>)
+                   : (cut ? k_fwd_stats<TI, false, true> : k_fwd_stats<TI, false, false>);
     int rc = raise_smem((const void*)ks, smem, di);
     if (rc) { cudaFreeAsync(s.base, st); return rc; }
-    // one CTA per SM (fewer only when there are fewer blocks than SMs): warp w of
-    // CTA c owns blocks w*grid + c, ..., so every SM takes a share
-    const int sgrid = grid_for(di, nblk, 1);
     g_launches += 2;
     LaunchTimer t1(KK_FWD_STATS, st, di);
     ks<<<sgrid, 32 * Shape::kWarps, smem, st>>>(xp, p, w, eps, mean, rstd, spin_budget(), di.status);
@@ -347,8 +368,7 @@ int launch_forward(const void* x, const float* gamma, const float* beta, const P
     e = cudaGetLastError();
     if (e == cudaSuccess) {
       LaunchTimer t2(KK_FWD_NORM, st, di);
-      auto kn = full ? (relu ? k_fwd_norm<TI, TO, true, true> : k_fwd_norm<TI, TO, true, false>)
-                     : (relu ? k_fwd_norm<TI, TO, false, true> : k_fwd_norm<TI, TO, false, false>);
+      auto kn = norm_kernel<TI, TO>(full, relu, cut);
       e = launch_dependent(kn, sgrid, 32 * kElemWarps, st, xp, yp, p, (const float4*)w.stats, gamma, beta);
       t2.done();
     }
@@ -367,13 +387,14 @@ cudaError_t launch_backward_streaming(const T* dyp, const T* xp, const T* resp, 
                                       const float* mean, const float* rstd, const float* gamma, BwdWs& w,
                                       float* dgamma, float* dbeta, cudaStream_t st, DevInfo& di, int* rc) {
   using Shape = BwdRedShape<T, kRelu>;
-  const int64_t nblk = p.NC * p.nb;
   const int smem = Shape::kWarps * WarpRing<T, Shape::kTensors, Shape::kSlots, Shape::kElems>::kWarpBytes;
   const bool full = plan_all_full(p);
-  auto kr = full ? k_bwd_reduce<T, true, kRelu> : k_bwd_reduce<T, false, kRelu>;
+  const int rgrid = grid_for(di, p.units, 1);
+  const bool cut = unit_shares(p, (int64_t)rgrid * Shape::kWarps);
+  auto kr = full ? (cut ? k_bwd_reduce<T, true, kRelu, true> : k_bwd_reduce<T, true, kRelu, false>)
+                 : (cut ? k_bwd_reduce<T, false, kRelu, true> : k_bwd_reduce<T, false, kRelu, false>);
   *rc = raise_smem((const void*)kr, smem, di);
   if (*rc) return cudaSuccess;
-  const int rgrid = grid_for(di, nblk, 1);
   g_launches += 2;
   LaunchTimer t1(KK_BWD_REDUCE, st, di);
   kr<<<rgrid, 32 * Shape::kWarps, smem, st>>>(dyp, xp, resp, p, mean, rstd, gamma, w, dgamma, dbeta,
@@ -382,7 +403,8 @@ cudaError_t launch_backward_streaming(const T* dyp, const T* xp, const T* resp, 
   cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) {
     LaunchTimer t2(KK_BWD_DX, st, di);
-    auto kd = full ? k_bwd_dx<T, true, kRelu> : k_bwd_dx<T, false, kRelu>;
+    auto kd = full ? (cut ? k_bwd_dx<T, true, kRelu, true> : k_bwd_dx<T, true, kRelu, false>)
+                   : (cut ? k_bwd_dx<T, false, kRelu, true> : k_bwd_dx<T, false, kRelu, false>);
     e = launch_dependent(kd, rgrid, 32 * kElemWarps, st, dyp, xp, resp, dxp, p, mean, rstd, gamma,
                          (const float2*)w.coef);
     t2.done();
@@ -934,6 +956,10 @@ extern "C" int gn3d_debug_set(int what, long long value) {
       g_timing = (int)value;
       break;
     }
+    case GN3D_DEBUG_SHARES:
+      if (value < -1 || value > 1) return arg_fail("shares: -1, 0 or 1");
+      g_hook_shares = (int)value;
+      break;
     default:
       return arg_fail("unknown debug setting");
   }

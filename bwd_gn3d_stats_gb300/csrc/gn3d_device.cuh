@@ -396,6 +396,32 @@ __device__ __forceinline__ Part ldcg_part(const Part* p) {
   return Part{r.x, r.y, __float_as_int(r.z), r.w};
 }
 
+__device__ __forceinline__ void stcg_unit(Part* p, const Part& a) {
+  __stcg(reinterpret_cast<float4*>(p), make_float4(a.m1, a.m2, __int_as_float(a.n), a.cn));
+}
+__device__ __forceinline__ void stcg_unit(float2* p, float2 a) { __stcg(p, a); }
+__device__ __forceinline__ Part ldcg_unit(const Part* p) { return ldcg_part(p); }
+__device__ __forceinline__ float2 ldcg_unit(const float2* p) { return __ldcg(p); }
+
+// A merge block cut between two warps' shares, by one warp: lanes lo..hi hold
+// the results of units lo..hi of the block (unit i in lane i).  They publish
+// them to parts[lane] and add hi-lo+1 arrivals to *ctr; true in the warp whose
+// arrivals complete the block's bsz units, which then reads all of parts back
+// (ldcg_unit) and merges the block exactly as a warp holding it whole would.
+template <class V>
+__device__ __forceinline__ bool split_block_arrive(V* parts, uint32_t* ctr, int lo, int hi, int bsz, const V& a) {
+  const int lane = threadIdx.x & 31;
+  if (lane >= lo && lane <= hi) stcg_unit(parts + lane, a);
+  __threadfence();  // every lane's publication before lane 0's arrival
+  __syncwarp();
+  const uint32_t n = (uint32_t)(hi - lo + 1);
+  uint32_t old = 0;
+  if (lane == 0) old = atom_add_acq_rel(ctr, n);
+  old = __shfl_sync(kFull, old, 0);
+  __syncwarp();
+  return old + n == (uint32_t)bsz;
+}
+
 // Block merge of a block's unit partials, by one warp: lane l holds unit l's
 // partial (lanes past the block's size hold an empty one).
 __device__ __forceinline__ Part merge_block(const Part a) {
@@ -480,8 +506,18 @@ struct GatedView {
 // full -- the same arithmetic as the general path, without its checks.
 constexpr int kPilotVecs = 4;
 
+// The lane's head or tail scalar of a general unit, 0 where it has none.  The
+// streaming reduction kernels load it a unit ahead: read where it is used, its
+// DRAM latency would stall the warp once per unit.
+template <bool kFull, class T>
+__device__ __forceinline__ float unit_scalar(const T* __restrict__ x, const URange& q) {
+  const int lane = threadIdx.x & 31;
+  return !kFull && lane < scalar_count(q) ? IO<T>::load1(x + scalar_index(q, lane)) : 0.f;
+}
+
+// sv: the lane's scalar, as unit_scalar gives it.
 template <bool kFull, class T, class View>
-__device__ __forceinline__ Part unit_moments(const View& u, const T* __restrict__ x, const URange& q) {
+__device__ __forceinline__ Part unit_moments_sv(const View& u, float sv, const URange& q) {
   if (!kFull && q.n == 0) return Part{0.f, 0.f, 0, 0.f};
   const int lane = threadIdx.x & 31;
   const f2 z2 = f2_splat(0.f);
@@ -498,7 +534,6 @@ __device__ __forceinline__ Part unit_moments(const View& u, const T* __restrict_
     }
   }
   const bool hs = !kFull && lane < scalar_count(q);
-  const float sv = hs ? IO<T>::load1(x + scalar_index(q, lane)) : 0.f;
   // the shift: the pilot mean (an exact power-of-two scaling when the lane is full),
   // else the lane's scalar, else 0 for an empty lane
   float K;
@@ -538,6 +573,11 @@ __device__ __forceinline__ Part unit_moments(const View& u, const T* __restrict_
   lp.m2 = fsub(qs, fmul(cs, lp.cn));
   if (lp.m2 < 0.f) lp.m2 = 0.f;  // rounding only; NaN is kept
   return merge_lanes(lp, kFull ? kUnitElems : q.n);
+}
+
+template <bool kFull, class T, class View>
+__device__ __forceinline__ Part unit_moments(const View& u, const T* __restrict__ x, const URange& q) {
+  return unit_moments_sv<kFull, T>(u, unit_scalar<kFull, T>(x, q), q);
 }
 
 // --------------------------------------------------------------- forward
@@ -651,19 +691,37 @@ __device__ __forceinline__ float grad_at(const T* __restrict__ dy, const T* __re
   return res && IO<T>::load1(res + idx) <= 0.f ? 0.f : d;
 }
 
+// The lane's scalar of a general unit for the backward sums: its gradient and
+// its x (zeros where it has none), loaded a unit ahead by the reduction kernel.
+struct BwdScalar {
+  float d, x;
+};
+template <bool kFull, class T>
+__device__ __forceinline__ BwdScalar bwd_scalar(const T* __restrict__ x, const T* __restrict__ dy,
+                                                const T* __restrict__ res, const URange& q) {
+  const int lane = threadIdx.x & 31;
+  if (kFull || lane >= scalar_count(q)) return BwdScalar{0.f, 0.f};
+  const int64_t idx = scalar_index(q, lane);
+  return BwdScalar{grad_at(dy, res, idx), IO<T>::load1(x + idx)};
+}
+
+template <bool kFull>
+__device__ __forceinline__ float2 bwd_finish_sv(const f2 a1[4], const f2 a2[4], BwdScalar sc, const URange& q,
+                                                float mu) {
+  const int lane = threadIdx.x & 31;
+  float s1 = tree8p(a1), s2 = tree8p(a2);
+  if (!kFull && lane < scalar_count(q)) {
+    s1 = fadd(s1, sc.d);
+    s2 = ffma(sc.d, fsub(sc.x, mu), s2);
+  }
+  return warp_sum2(s1, s2);
+}
+
 template <bool kFull, class T>
 __device__ __forceinline__ float2 bwd_finish(const f2 a1[4], const f2 a2[4], const T* __restrict__ x,
                                              const T* __restrict__ dy, const URange& q, float mu,
                                              const T* __restrict__ res = nullptr) {
-  const int lane = threadIdx.x & 31;
-  float s1 = tree8p(a1), s2 = tree8p(a2);
-  if (!kFull && lane < scalar_count(q)) {
-    const int64_t idx = scalar_index(q, lane);
-    const float d = grad_at(dy, res, idx);
-    s1 = fadd(s1, d);
-    s2 = ffma(d, fsub(IO<T>::load1(x + idx), mu), s2);
-  }
-  return warp_sum2(s1, s2);
+  return bwd_finish_sv<kFull>(a1, a2, bwd_scalar<kFull, T>(x, dy, res, q), q, mu);
 }
 
 template <bool kFull, class T, class View>
@@ -838,6 +896,58 @@ __device__ __forceinline__ void bwd_norm(const XView& ux, const DView& ud, const
     const float d = grad_at(dy, res, idx);
     IO<T>::store1(dx + idx, ffma(d, p1, ffma(-p2, fsub(IO<T>::load1(x + idx), k.mu), -p3)));
   }
+}
+
+// bwd_norm of a general unit read from global memory, with the loads of kB
+// vectors of each tensor issued together before any of them is used: where
+// every vector is behind its own bounds check, the compiler otherwise keeps
+// each vector's loads after the previous vector's store, one DRAM round trip
+// per vector.  The same arithmetic as bwd_norm, element for element.
+template <class T, bool kRelu, int kB>
+__device__ __forceinline__ void bwd_norm_staged(const T* __restrict__ x, const T* __restrict__ dy,
+                                                const T* __restrict__ res, T* __restrict__ dx, const URange& q,
+                                                const DxCoef& k, float gam) {
+  static_assert(kVecPerLane % kB == 0, "whole batches");
+  constexpr int kR = Vec<T>::kRaw;
+  const int lane = threadIdx.x & 31;
+  const int nv = (int)((q.b1 - q.b0) / kVec);
+  const float p1 = k.single ? 0.f : fmul(k.r, gam);
+  const float p2 = k.single ? 0.f : fmul(fmul(k.r, k.r), k.b);
+  const float p3 = k.single ? 0.f : fmul(k.r, k.a);
+  const f2 p12 = f2_splat(p1), np22 = f2_splat(-p2), np32 = f2_splat(-p3);
+  // the scalar first: its loads overlap the body's
+  const bool hs = lane < scalar_count(q);
+  const int64_t sidx = hs ? scalar_index(q, lane) : 0;
+  const float sd = hs ? grad_at(dy, kRelu ? res : nullptr, sidx) : 0.f;
+  const float sx = hs ? IO<T>::load1(x + sidx) : 0.f;
+#pragma unroll
+  for (int i0 = 0; i0 < kVecPerLane; i0 += kB) {
+    if (lane + 32 * i0 >= nv) break;
+    uint4 rx[kB][kR], rd[kB][kR], rr[kRelu ? kB : 1][kR];
+#pragma unroll
+    for (int j = 0; j < kB; ++j) {
+      const int v = lane + 32 * (i0 + j);
+      if (v < nv) {
+        Vec<T>::template load<FromGlobal>(x + q.b0 + (int64_t)v * kVec, rx[j]);
+        Vec<T>::template load<FromGlobal>(dy + q.b0 + (int64_t)v * kVec, rd[j]);
+        if constexpr (kRelu) Vec<T>::template load<FromGlobal>(res + q.b0 + (int64_t)v * kVec, rr[j]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kB; ++j) {
+      const int v = lane + 32 * (i0 + j);
+      if (v < nv) {
+        f2 xm[4], vd[4];
+        Vec<T>::diff(rx[j], k.mu, xm);
+        if constexpr (kRelu) Vec<T>::gate(rr[j], rd[j]);
+        Vec<T>::pairs(rd[j], vd);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) vd[e] = f2fma(vd[e], p12, f2fma(np22, xm[e], np32));
+        store8p<T>(dx + q.b0 + (int64_t)v * kVec, vd);
+      }
+    }
+  }
+  if (hs) IO<T>::store1(dx + sidx, ffma(sd, p1, ffma(-p2, fsub(sx, k.mu), -p3)));
 }
 
 // Row -> channel, in 32 bits when the indices allow it.

@@ -3,21 +3,22 @@
 // Forward  (ScaFFold PR #93 "Optimize GroupNorm": split-group statistics, a
 //           corrected two-pass per tile merged with Chan's formula, then a
 //           normalize that rounds once on the store, PR #105):
-//   k_fwd_stats : each warp owns whole merge blocks (up to 16 consecutive units
-//                 of a row) and streams their bodies through a private ring of
+//   k_fwd_stats : each warp takes an equal share of consecutive units
+//                 (UnitWalk) and streams their bodies through a private ring of
 //                 shared-memory slots filled by 1-D bulk copies (the TMA
 //                 engine), so several units per warp are always in flight; it
-//                 merges each block in registers and the warp that completes a
-//                 group merges the group.
-//   k_fwd_norm  : normalizes the blocks each statistics warp owned, on the same
-//                 CTA index (so, for identical launches, the same SM), last
-//                 block and last unit first: what that SM read last is read
-//                 again first, while it is still in L2.
+//                 merges each merge block it holds whole in registers, a block
+//                 cut between two shares is merged by the warp completing it,
+//                 and the warp that completes a group merges the group.
+//   k_fwd_norm  : normalizes the units of each statistics warp's share, on the
+//                 same CTA index (so, for identical launches, the same SM), last
+//                 unit first: what that SM read last is read again first, while
+//                 it is still in L2.
 // Backward (the same PR's _bwd_finalize/_dwdb_reduce/_dx split):
 //   k_bwd_reduce: S1 = sum dy, S2 = sum dy*(x - mean) per unit, through the same
 //                 kind of ring; group and parameter-gradient merges by the
 //                 completing warps.
-//   k_bwd_dx    : dx over the reduction warps' blocks, the same way.
+//   k_bwd_dx    : dx over the reduction warps' shares, the same way.
 // These use exactly the units, merge blocks and arithmetic of the persistent
 // kernels (gn3d_device.cuh), so the two launch forms give bit-identical results.
 #pragma once
@@ -26,28 +27,14 @@
 
 namespace gn3d {
 
-// ---------------------------------------------------------- block rings
-// Warp w of CTA c walks merge blocks b = w*grid + c, then b + warps*grid, ...
-// (every SM gets an equal share of each part of the tensor), unit by unit.
-struct BlockWalk {
-  int64_t b, row, kb;  // current block, its row and index in the row
-  int bsz, ui;         // its unit count; the current unit in it
-  bool end;
-  __device__ __forceinline__ void set(const Plan& p, int64_t b_, int64_t nblk) {
-    b = b_;
-    end = b >= nblk;
-    if (!end) {
-      row = b / p.nb;
-      kb = b - row * p.nb;
-      bsz = block_size(p, kb);
-      ui = 0;
-    }
-  }
-  __device__ __forceinline__ void next(const Plan& p, int64_t stride, int64_t nblk) {
-    if (++ui >= bsz) set(p, b + stride, nblk);
-  }
-  __device__ __forceinline__ int64_t k() const { return kb * kBlockUnits + ui; }
-};
+// ---------------------------------------------------------- unit rings
+// The worker index of warp w of CTA c, of grid*warps: in unit shares c*warps +
+// w (each CTA a run of consecutive shares), in strided blocks w*grid + c (every
+// CTA blocks from all over the tensor); either way every SM gets an equal part.
+template <int kWarps>
+__device__ __forceinline__ int64_t worker_index(bool cut, int warp) {
+  return cut ? (int64_t)blockIdx.x * kWarps + warp : (int64_t)warp * gridDim.x + blockIdx.x;
+}
 
 // A warp's private ring: kSlots slots, each holding kElems consecutive body
 // elements of each of kTensors tensors (a whole unit, or one of its
@@ -115,12 +102,12 @@ struct WarpRing {
 
 // The load-ahead position of a ring: a block walk plus the part of the unit.
 struct PartWalk {
-  BlockWalk w;
+  UnitWalk w;
   int part = 0;
-  __device__ __forceinline__ void next(const Plan& p, int64_t stride, int64_t nblk, int parts) {
+  __device__ __forceinline__ void next(const Plan& p, int parts) {
     if (++part < parts) return;
     part = 0;
-    w.next(p, stride, nblk);
+    w.next(p);
   }
 };
 
@@ -149,7 +136,7 @@ template <class T, bool kRelu = false> struct BwdRedShape {
   static constexpr int kElems = (kRelu ? 2048 : 4096) / (int)sizeof(T);
 };
 
-template <class TI, bool kFull>
+template <class TI, bool kFull, bool kCut>
 __global__ void __launch_bounds__(32 * FwdStatShape<TI>::kWarps, 1)
     k_fwd_stats(const TI* __restrict__ x, Plan p, FwdWs ws, float eps, float* mean_out, float* rstd_out,
                 unsigned long long spin, uint32_t* status) {
@@ -161,25 +148,31 @@ __global__ void __launch_bounds__(32 * FwdStatShape<TI>::kWarps, 1)
   pdl_launch_dependents();  // the normalize kernel may take SMs as this one leaves them
   Ring ring;
   ring.init(smem + (size_t)warp * Ring::kWarpBytes);
-  const int64_t nblk = p.NC * p.nb, stride = (int64_t)gridDim.x * Shape::kWarps;
-  const int64_t first = (int64_t)warp * gridDim.x + blockIdx.x;
   const TI* src[1] = {x};
-  BlockWalk ld, cu;
-  ld.set(p, first, nblk);
+  UnitWalk ld, cu;
+  ld.set(p, worker_index<Shape::kWarps>(kCut, warp), (int64_t)gridDim.x * Shape::kWarps, kCut);
   cu = ld;
   for (int i = 0; i < Shape::kSlots && !ld.end; ++i) {
-    ring.issue(urange<kFull>(p, ld.row, ld.k()), 0, src);
-    ld.next(p, stride, nblk);
+    ring.issue(urange<kFull>(p, ld.row, ld.k), 0, src);
+    ld.next(p);
   }
-  Part a{0.f, 0.f, 0, 0.f};  // lane l: the partial of unit l of the current block
+  const Part empty{0.f, 0.f, 0, 0.f};
+  Part a = empty;  // lane l: the partial of unit l of the current block
+  float sv = cu.end ? 0.f : unit_scalar<kFull, TI>(x, urange<kFull>(p, cu.row, cu.k));
   while (!cu.end) {
+    const URange q = urange<kFull>(p, cu.row, cu.k);
+    const int nv = (int)((q.b1 - q.b0) / kVec);
+    float sv_next = 0.f;  // the next unit's scalar, in flight while this unit is summed
+    if (!kFull) {
+      UnitWalk nx = cu;
+      nx.next(p);
+      if (!nx.end) sv_next = unit_scalar<kFull, TI>(x, urange<kFull>(p, nx.row, nx.k));
+    }
     const unsigned char* slot = ring.take(spin);
     if (!slot) {
       record_timeout(status);
       break;
     }
-    const URange q = urange<kFull>(p, cu.row, cu.k());
-    const int nv = (int)((q.b1 - q.b0) / kVec);
     Part m;
     if (kRegs) {
       RegView<TI> v;
@@ -187,102 +180,103 @@ __global__ void __launch_bounds__(32 * FwdStatShape<TI>::kWarps, 1)
       else v.template load<FromShared>(reinterpret_cast<const TI*>(slot), nv);
       __syncwarp();
       if (!ld.end) {
-        ring.issue(urange<kFull>(p, ld.row, ld.k()), 0, src);
-        ld.next(p, stride, nblk);
+        ring.issue(urange<kFull>(p, ld.row, ld.k), 0, src);
+        ld.next(p);
       }
-      m = unit_moments<kFull, TI>(v, x, q);
+      m = unit_moments_sv<kFull, TI>(v, sv, q);
     } else {
-      m = unit_moments<kFull, TI>(MemView<TI, FromShared>{reinterpret_cast<const TI*>(slot), nv}, x, q);
+      m = unit_moments_sv<kFull, TI>(MemView<TI, FromShared>{reinterpret_cast<const TI*>(slot), nv}, sv, q);
       __syncwarp();
       if (!ld.end) {
-        ring.issue(urange<kFull>(p, ld.row, ld.k()), 0, src);
-        ld.next(p, stride, nblk);
+        ring.issue(urange<kFull>(p, ld.row, ld.k), 0, src);
+        ld.next(p);
       }
     }
-    if (lane == cu.ui) a = m;
-    if (cu.ui == cu.bsz - 1) {
-      fwd_block_done(p, ws, cu.b, merge_block(lane < cu.bsz ? a : Part{0.f, 0.f, 0, 0.f}), eps, mean_out,
-                     rstd_out);
-      a = Part{0.f, 0.f, 0, 0.f};
+    const int ui = cu.ui(), bsz = block_size(p, cu.kb());
+    if (lane == ui) a = m;
+    if (ui == bsz - 1 || (kCut && cu.u + 1 == cu.u1)) {  // the block, or this warp's part of it, is done
+      const int64_t blk = cu.row * p.nb + cu.kb();
+      bool merge = ui == bsz - 1;
+      Part v = lane < bsz ? a : empty;
+      if constexpr (kCut) {
+        const int64_t ub = cu.u - ui;
+        const int lo = ub >= cu.u0 ? 0 : (int)(cu.u0 - ub);
+        if (lo > 0 || ui < bsz - 1) {  // a cut block: the warp completing it merges it
+          merge = split_block_arrive(ws.parts + ub, ws.bcnt + blk, lo, ui, bsz, a);
+          if (merge) v = lane < bsz ? ldcg_unit(ws.parts + ub + lane) : empty;
+        }
+      }
+      if (merge) fwd_block_done(p, ws, blk, merge_block(v), eps, mean_out, rstd_out);
+      a = empty;
     }
-    cu.next(p, stride, nblk);
+    sv = sv_next;
+    cu.next(p);
   }
   ring.drain(kDrainPolls);
 }
 
 // Elementwise passes: 16 warps per CTA, on the reduction kernel's grid.  Warp w
-// takes the blocks of reduction warp w % kOwners of the same CTA, from its last
-// block back to its first, and in each block every (16 / kOwners)-th unit from
-// the last one down.  Placement only decides what is found in L2, never a result.
+// takes the units of reduction warp w % kOwners of the same CTA, every
+// (16 / kOwners)-th, in the reverse of that warp's order (UnitWalkDown): what a
+// reduction warp read last is read again first, while it is still in L2.
+// Placement only decides what is found in L2, never a result.
 constexpr int kElemWarps = 16;
 
-template <int kOwners>
-struct OwnedBlocks {
-  static constexpr int kSplit = kElemWarps / kOwners;
-  int64_t b0, stride;
-  int share;
-  __device__ __forceinline__ OwnedBlocks() {
-    const int warp = threadIdx.x >> 5;
-    stride = (int64_t)gridDim.x * kOwners;
-    b0 = (int64_t)(warp % kOwners) * gridDim.x + blockIdx.x;
-    share = warp / kOwners;
-  }
-  // the owner's last block, or -1
-  __device__ __forceinline__ int64_t last(int64_t nblk) const {
-    return b0 < nblk ? b0 + (nblk - 1 - b0) / stride * stride : -1;
-  }
-};
+template <int kOwners, bool kCut>
+__device__ __forceinline__ UnitWalkDown owned_units(const Plan& p) {
+  const int warp = threadIdx.x >> 5;
+  UnitWalkDown w;
+  w.set(p, worker_index<kOwners>(kCut, warp % kOwners), (int64_t)gridDim.x * kOwners, kCut, warp / kOwners,
+        kElemWarps / kOwners);
+  return w;
+}
 
-template <class TI, class TO, bool kFull, bool kRelu>
+template <class TI, class TO, bool kFull, bool kRelu, bool kCut>
 __global__ void __launch_bounds__(32 * kElemWarps, 1)
     k_fwd_norm(const TI* __restrict__ x, TO* __restrict__ y, Plan p, const float4* __restrict__ stats,
                const float* __restrict__ gamma, const float* __restrict__ beta) {
-  using Own = OwnedBlocks<FwdStatShape<TI>::kWarps>;
   constexpr bool kRegs = Vec<TI>::kRaw == 1;  // bf16: all 16 loads in flight before any use
-  const Own own;
-  const int64_t nblk = p.NC * p.nb;
+  UnitWalkDown w = owned_units<FwdStatShape<TI>::kWarps, kCut>(p);
   // The warp's first unit is read before the statistics kernel has finished
   // (x is not written there); everything the statistics kernel writes is read
   // after pdl_wait.
   RegView<TI> v;
   bool pre = false;
-  const int64_t b_first = own.last(nblk);
-  if (kRegs && b_first >= own.b0) {
-    const int64_t row = b_first / p.nb, kb = b_first - row * p.nb;
-    const int ui = block_size(p, kb) - 1 - own.share;
-    if (ui >= 0) {
-      const URange q = urange<kFull>(p, row, kb * kBlockUnits + ui);
-      if (kFull) v.template load_full<FromGlobal>(x + q.b0);
-      else v.template load<FromGlobal>(x + q.b0, (int)((q.b1 - q.b0) / kVec));
-      pre = true;
-    }
+  if (kRegs && !w.end()) {
+    const URange q = urange<kFull>(p, w.row, w.k);
+    if (kFull) v.template load_full<FromGlobal>(x + q.b0);
+    else v.template load<FromGlobal>(x + q.b0, (int)((q.b1 - q.b0) / kVec));
+    pre = true;
   }
   pdl_wait();
-  for (int64_t b = b_first; b >= own.b0; b -= own.stride) {
-    const int64_t row = b / p.nb, kb = b - row * p.nb;
-    const int bsz = block_size(p, kb);
-    const int64_t c = channel_of(row, p.C), g = row / p.Cg;
-    const float4 st = __ldcg(stats + g);
-    const float gm = gamma ? gamma[c] : 1.f, bt = beta ? beta[c] : 0.f;
-    for (int ui = bsz - 1 - own.share; ui >= 0; ui -= Own::kSplit) {
-      const URange q = urange<kFull>(p, row, kb * kBlockUnits + ui);
-      const int nv = (int)((q.b1 - q.b0) / kVec);
-      if (kRegs) {
-        if (!pre) {
-          if (kFull) v.template load_full<FromGlobal>(x + q.b0);
-          else v.template load<FromGlobal>(x + q.b0, nv);
-        }
-        pre = false;
-        fwd_norm<kFull, TI, TO, RegView<TI>, kRelu>(v, x, y, q, st, gm, bt);
-      } else {
-        fwd_norm<kFull, TI, TO, MemView<TI, FromGlobal>, kRelu>(MemView<TI, FromGlobal>{x + q.b0, nv}, x, y, q, st,
-                                                                gm, bt);
+  int64_t row = -1;
+  float4 st;
+  float gm = 1.f, bt = 0.f;
+  for (; !w.end(); w.next(p)) {
+    if (w.row != row) {  // the row's coefficients
+      row = w.row;
+      const int64_t c = channel_of(row, p.C);
+      st = __ldcg(stats + row / p.Cg);
+      gm = gamma ? gamma[c] : 1.f;
+      bt = beta ? beta[c] : 0.f;
+    }
+    const URange q = urange<kFull>(p, w.row, w.k);
+    const int nv = (int)((q.b1 - q.b0) / kVec);
+    if (kRegs) {
+      if (!pre) {
+        if (kFull) v.template load_full<FromGlobal>(x + q.b0);
+        else v.template load<FromGlobal>(x + q.b0, nv);
       }
+      pre = false;
+      fwd_norm<kFull, TI, TO, RegView<TI>, kRelu>(v, x, y, q, st, gm, bt);
+    } else {
+      fwd_norm<kFull, TI, TO, MemView<TI, FromGlobal>, kRelu>(MemView<TI, FromGlobal>{x + q.b0, nv}, x, y, q, st, gm,
+                                                              bt);
     }
   }
 }
 
-template <class T, bool kFull, bool kRelu>
+template <class T, bool kFull, bool kRelu, bool kCut>
 __global__ void __launch_bounds__(32 * BwdRedShape<T, kRelu>::kWarps, 1)
     k_bwd_reduce(const T* __restrict__ dy, const T* __restrict__ x, const T* __restrict__ res, Plan p,
                  const float* __restrict__ mean, const float* __restrict__ rstd, const float* __restrict__ gamma,
@@ -295,22 +289,29 @@ __global__ void __launch_bounds__(32 * BwdRedShape<T, kRelu>::kWarps, 1)
   pdl_launch_dependents();  // the dx kernel may take SMs as this one leaves them
   Ring ring;
   ring.init(smem + (size_t)warp * Ring::kWarpBytes);
-  const int64_t nblk = p.NC * p.nb, stride = (int64_t)gridDim.x * Shape::kWarps;
-  const int64_t first = (int64_t)warp * gridDim.x + blockIdx.x;
   const T* src[3] = {x, dy, res};
   PartWalk ld;
-  ld.w.set(p, first, nblk);
-  BlockWalk cu = ld.w;
+  ld.w.set(p, worker_index<Shape::kWarps>(kCut, warp), (int64_t)gridDim.x * Shape::kWarps, kCut);
+  UnitWalk cu = ld.w;
   for (int i = 0; i < Shape::kSlots && !ld.w.end; ++i) {
-    ring.issue(urange<kFull>(p, ld.w.row, ld.w.k()), ld.part, src);
-    ld.next(p, stride, nblk, kParts);
+    ring.issue(urange<kFull>(p, ld.w.row, ld.w.k), ld.part, src);
+    ld.next(p, kParts);
   }
-  float2 a = make_float2(0.f, 0.f);  // lane l: the sums of unit l of the current block
+  const float2 zero = make_float2(0.f, 0.f);
+  float2 a = zero;  // lane l: the sums of unit l of the current block
   bool failed = false;
+  const T* gate = kRelu ? res : nullptr;
+  BwdScalar sc = cu.end ? BwdScalar{0.f, 0.f} : bwd_scalar<kFull, T>(x, dy, gate, urange<kFull>(p, cu.row, cu.k));
   while (!cu.end) {
-    const URange q = urange<kFull>(p, cu.row, cu.k());
+    const URange q = urange<kFull>(p, cu.row, cu.k);
     const int nv = (int)((q.b1 - q.b0) / kVec);
     const float mu = mean[q.row / p.Cg];
+    BwdScalar sc_next{0.f, 0.f};  // the next unit's scalar, in flight while this unit is summed
+    if (!kFull) {
+      UnitWalk nx = cu;
+      nx.next(p);
+      if (!nx.end) sc_next = bwd_scalar<kFull, T>(x, dy, gate, urange<kFull>(p, nx.row, nx.k));
+    }
     const f2 z2 = f2_splat(0.f);
     f2 a1[4] = {z2, z2, z2, z2};
     f2 a2[4] = {z2, z2, z2, z2};
@@ -334,51 +335,66 @@ __global__ void __launch_bounds__(32 * BwdRedShape<T, kRelu>::kWarps, 1)
       }
       __syncwarp();
       if (!ld.w.end) {
-        ring.issue(urange<kFull>(p, ld.w.row, ld.w.k()), ld.part, src);
-        ld.next(p, stride, nblk, kParts);
+        ring.issue(urange<kFull>(p, ld.w.row, ld.w.k), ld.part, src);
+        ld.next(p, kParts);
       }
     }
     if (failed) {
       record_timeout(status);
       break;
     }
-    const float2 v = bwd_finish<kFull, T>(a1, a2, x, dy, q, mu, kRelu ? res : nullptr);
-    if (lane == cu.ui) a = v;
-    if (cu.ui == cu.bsz - 1) {
-      bwd_block_done(p, ws, cu.b, lane < cu.bsz ? a : make_float2(0.f, 0.f), rstd, gamma, dgamma, dbeta);
-      a = make_float2(0.f, 0.f);
+    const float2 v = bwd_finish_sv<kFull>(a1, a2, sc, q, mu);
+    const int ui = cu.ui(), bsz = block_size(p, cu.kb());
+    if (lane == ui) a = v;
+    if (ui == bsz - 1 || (kCut && cu.u + 1 == cu.u1)) {  // the block, or this warp's part of it, is done
+      const int64_t blk = cu.row * p.nb + cu.kb();
+      bool merge = ui == bsz - 1;
+      float2 bs = lane < bsz ? a : zero;
+      if constexpr (kCut) {
+        const int64_t ub = cu.u - ui;
+        const int lo = ub >= cu.u0 ? 0 : (int)(cu.u0 - ub);
+        if (lo > 0 || ui < bsz - 1) {  // a cut block: the warp completing it merges it
+          merge = split_block_arrive(ws.parts + ub, ws.bcnt + blk, lo, ui, bsz, a);
+          if (merge) bs = lane < bsz ? ldcg_unit(ws.parts + ub + lane) : zero;
+        }
+      }
+      if (merge) bwd_block_done(p, ws, blk, bs, rstd, gamma, dgamma, dbeta);
+      a = zero;
     }
-    cu.next(p, stride, nblk);
+    sc = sc_next;
+    cu.next(p);
   }
   ring.drain(kDrainPolls);
 }
 
-template <class T, bool kFull, bool kRelu>
+template <class T, bool kFull, bool kRelu, bool kCut>
 __global__ void __launch_bounds__(32 * kElemWarps, 1)
     k_bwd_dx(const T* __restrict__ dy, const T* __restrict__ x, const T* __restrict__ res, T* __restrict__ dx,
              Plan p, const float* __restrict__ mean, const float* __restrict__ rstd,
              const float* __restrict__ gamma, const float2* __restrict__ coef) {
-  using Own = OwnedBlocks<BwdRedShape<T, kRelu>::kWarps>;
-  const Own own;
-  const int64_t nblk = p.NC * p.nb;
+  UnitWalkDown w = owned_units<BwdRedShape<T, kRelu>::kWarps, kCut>(p);
   pdl_wait();  // the reduction kernel's coefficients
-  for (int64_t b = own.last(nblk); b >= own.b0; b -= own.stride) {
-    const int64_t row = b / p.nb, kb = b - row * p.nb;
-    const int bsz = block_size(p, kb);
-    const int64_t c = channel_of(row, p.C), g = row / p.Cg;
-    const float2 ab = __ldcg(coef + g);
-    const DxCoef k{mean[g], rstd[g], ab.x, ab.y, p.M == 1};
-    const float gm = gamma ? gamma[c] : 1.f;
-    for (int ui = bsz - 1 - own.share; ui >= 0; ui -= Own::kSplit) {
-      const URange q = urange<kFull>(p, row, kb * kBlockUnits + ui);
-      const int nv = (int)((q.b1 - q.b0) / kVec);
-      if constexpr (kRelu) {
-        bwd_norm<kFull, T>(MemView<T, FromGlobal>{x + q.b0, nv}, GatedView<T, FromGlobal>{dy + q.b0, res + q.b0, nv},
-                           x, dy, dx, q, k, gm, res);
-      } else {
-        bwd_norm<kFull, T>(MemView<T, FromGlobal>{x + q.b0, nv}, MemView<T, FromGlobal>{dy + q.b0, nv}, x, dy,
-                           dx, q, k, gm);
-      }
+  int64_t row = -1;
+  DxCoef k{0.f, 0.f, 0.f, 0.f, false};
+  float gm = 1.f;
+  for (; !w.end(); w.next(p)) {
+    if (w.row != row) {  // the row's coefficients
+      row = w.row;
+      const int64_t c = channel_of(row, p.C), g = row / p.Cg;
+      const float2 ab = __ldcg(coef + g);
+      k = DxCoef{mean[g], rstd[g], ab.x, ab.y, p.M == 1};
+      gm = gamma ? gamma[c] : 1.f;
+    }
+    const URange q = urange<kFull>(p, w.row, w.k);
+    const int nv = (int)((q.b1 - q.b0) / kVec);
+    if constexpr (!kFull) {
+      bwd_norm_staged<T, kRelu, (kRelu ? 4 : 8) / Vec<T>::kRaw>(x, dy, res, dx, q, k, gm);
+    } else if constexpr (kRelu) {
+      bwd_norm<kFull, T>(MemView<T, FromGlobal>{x + q.b0, nv}, GatedView<T, FromGlobal>{dy + q.b0, res + q.b0, nv},
+                         x, dy, dx, q, k, gm, res);
+    } else {
+      bwd_norm<kFull, T>(MemView<T, FromGlobal>{x + q.b0, nv}, MemView<T, FromGlobal>{dy + q.b0, nv}, x, dy, dx,
+                         q, k, gm);
     }
   }
 }

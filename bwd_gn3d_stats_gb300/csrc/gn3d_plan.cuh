@@ -139,4 +139,173 @@ __host__ __device__ inline int block_size(const Plan& p, int64_t kb) {
   return (int)(rest < kBlockUnits ? rest : kBlockUnits);
 }
 
+// Work shares of the streaming kernels, in one of two layouts:
+//   strided blocks (cut = false): worker w of W takes whole merge blocks w,
+//     w + W, w + 2W, ...; no block is ever split;
+//   unit shares (cut = true): worker w takes the contiguous units
+//     [units*w/W, units*(w+1)/W) in (row, k) order, so shares differ by at most
+//     one unit; a block cut by a share boundary is merged by whichever worker
+//     completes it.
+// Shares decide placement only: every unit, block and group merge is the same
+// whatever W and the layout are.
+__host__ __device__ inline int64_t share_begin(const Plan& p, int64_t w, int64_t nw) { return p.units * w / nw; }
+
+// The first unit of unit u's merge block, and one past its last.
+__host__ __device__ inline void block_span(const Plan& p, int64_t u, int64_t& b0, int64_t& b1) {
+  const int64_t row = u / p.R, k = u - row * p.R, kb0 = k / kBlockUnits * kBlockUnits;
+  b0 = row * p.R + kb0;
+  b1 = row * p.R + (kb0 + kBlockUnits < p.R ? kb0 + kBlockUnits : p.R);
+}
+
+// Where a unit share's walk starts.  When a block is cut at the share's end,
+// the walk takes that piece first and then wraps to the share's start: both
+// cut pieces (their merges need global round trips between workers) are then
+// done early, and the walk ends on whole blocks, merged in registers.
+__host__ __device__ inline int64_t share_walk_start(const Plan& p, int64_t u0, int64_t u1) {
+  if (u0 >= u1) return u0;
+  int64_t lb, le;
+  block_span(p, u1 - 1, lb, le);
+  return (le > u1 && lb > u0) ? lb : u0;
+}
+
+// A worker's units in the reduction kernels' order.  Unit shares: a .. u1-1,
+// then u0 .. a-1 (a = share_walk_start).  Strided blocks: each block's units
+// in order, blocks w, w + W, ...  A block ends where ui() == its size - 1 or,
+// in a unit share, at u1 - 1; it is cut when this worker holds only part of it.
+struct UnitWalk {
+  int64_t u, row, k;     // the current unit, its row and index in the row
+  int64_t u0, u1, a;     // unit share [u0, u1), walk start a (strided: 0, max, 0)
+  int64_t b, bstride;    // strided: the current block, the block stride
+  bool cut, end;
+  __host__ __device__ void go(const Plan& p, int64_t v) {
+    u = v;
+    row = v / p.R;
+    k = v - row * p.R;
+  }
+  __host__ __device__ void go_block(const Plan& p) {
+    row = b / p.nb;
+    k = (b - row * p.nb) * kBlockUnits;
+    u = row * p.R + k;
+  }
+  __host__ __device__ void set(const Plan& p, int64_t w, int64_t nw, bool cut_) {
+    cut = cut_;
+    u = row = k = 0;
+    b = w;
+    bstride = nw;
+    if (cut) {
+      u0 = share_begin(p, w, nw);
+      u1 = share_begin(p, w + 1, nw);
+      a = share_walk_start(p, u0, u1);
+      end = u0 >= u1;
+      if (!end) go(p, a);
+    } else {
+      u0 = a = 0;
+      u1 = INT64_MAX;
+      end = b >= p.NC * p.nb;
+      if (!end) go_block(p);
+    }
+  }
+  __host__ __device__ void next(const Plan& p) {
+    ++u;
+    ++k;
+    if (!cut) {
+      if (k % kBlockUnits == 0 || k == p.R) {  // the block is done
+        b += bstride;
+        end = b >= p.NC * p.nb;
+        if (!end) go_block(p);
+      }
+      return;
+    }
+    if (k == p.R) {
+      k = 0;
+      ++row;
+    }
+    if (u == u1) {
+      if (a == u0) end = true;
+      else go(p, u0);  // wrap to the share's start
+    } else if (u == a) {
+      end = true;
+    }
+  }
+  __host__ __device__ int ui() const { return (int)(k % kBlockUnits); }  // unit in its block
+  __host__ __device__ int64_t kb() const { return k / kBlockUnits; }     // block in its row
+};
+
+// A worker's units in the elementwise kernels' order, `step` warps splitting
+// them (this one starts `skip` in), so that what the reduction read last is
+// read again first.  Unit shares: positions skip, skip+step, ... of the reverse
+// of UnitWalk's order.  Strided blocks: the blocks from the last one down, in
+// each block units size-1-skip, size-1-skip-step, ... down.
+struct UnitWalkDown {
+  int64_t u, row, k;       // the current unit
+  int64_t u0, u1, a, i;    // unit shares: the share, walk start, position
+  int64_t b, b0, bstride;  // strided: the current block, the first block, the stride
+  int64_t kb;              // strided: the current block's index in its row
+  int ui, skip, step;
+  bool cut, done;
+  __host__ __device__ void at_share(const Plan& p) {
+    u = i < a - u0 ? a - 1 - i : u1 - 1 - (i - (a - u0));
+    row = u / p.R;
+    k = u - row * p.R;
+  }
+  // strided: block b, or the next one down that holds a unit for this warp
+  __host__ __device__ void enter_block(const Plan& p) {
+    for (; b >= b0; b -= bstride) {
+      row = b / p.nb;
+      kb = b - row * p.nb;
+      ui = block_size(p, kb) - 1 - skip;
+      if (ui >= 0) {
+        k = kb * kBlockUnits + ui;
+        u = row * p.R + k;
+        return;
+      }
+    }
+    done = true;
+  }
+  __host__ __device__ void set(const Plan& p, int64_t w, int64_t nw, bool cut_, int skip_, int step_) {
+    cut = cut_;
+    skip = skip_;
+    step = step_;
+    u = row = k = kb = 0;
+    ui = 0;
+    done = false;
+    if (cut) {
+      u0 = share_begin(p, w, nw);
+      u1 = share_begin(p, w + 1, nw);
+      a = share_walk_start(p, u0, u1);
+      i = skip;
+      done = i >= u1 - u0;
+      if (!done) at_share(p);
+    } else {
+      const int64_t nblk = p.NC * p.nb;
+      b0 = w;
+      bstride = nw;
+      b = b0 < nblk ? b0 + (nblk - 1 - b0) / nw * nw : -1;  // the last block
+      enter_block(p);
+    }
+  }
+  __host__ __device__ bool end() const { return done; }
+  __host__ __device__ void next(const Plan& p) {
+    if (cut) {
+      i += step;
+      done = i >= u1 - u0;
+      if (!done) at_share(p);
+    } else if (ui - step >= 0) {
+      ui -= step;
+      k -= step;
+      u -= step;
+    } else {
+      b -= bstride;
+      enter_block(p);
+    }
+  }
+};
+
+// Unit shares pay two cut blocks per worker and suit large tensors (contiguous
+// runs per SM); they are used when shares hold two merge blocks or more on
+// average, strided blocks otherwise.
+__host__ __device__ inline bool use_unit_shares(const Plan& p, int64_t nw) {
+  return p.units >= 2 * kBlockUnits * nw;
+}
+
 }  // namespace gn3d

@@ -239,6 +239,11 @@ uint64_t gn3d_launch_count(void);
  *   GN3D_DEBUG_TIMING        1 clears the per-kernel times and starts recording
  *                            them: every kernel launch is bracketed by two CUDA
  *                            events on its stream (see gn3d_kernel_time); 0 stops.
+ *   GN3D_DEBUG_SHARES        -1 automatic, 0 strided blocks, 1 unit shares:
+ *                            how the NCDHW streaming kernels split the units
+ *                            among their warps (whole merge blocks dealt out in
+ *                            turn, or equal contiguous runs of units that may
+ *                            cut a block between two warps).  Placement only.
  * Returns GN3D_OK or GN3D_ERR_INVALID_ARG for an unknown setting or value.
  */
 enum {
@@ -247,7 +252,8 @@ enum {
   GN3D_DEBUG_FORCE_TIMEOUT = 2,
   GN3D_DEBUG_LAG = 3,
   GN3D_DEBUG_SLOTS = 4,
-  GN3D_DEBUG_TIMING = 5
+  GN3D_DEBUG_TIMING = 5,
+  GN3D_DEBUG_SHARES = 6
 };
 int gn3d_debug_set(int what, long long value);
 

@@ -9,6 +9,9 @@
 //     group pieces tile each range's channels and every group's pieces exist; the
 //     ring parts (n_ring_part) of one-range shapes are aligned, inside the tensor,
 //     fit a slot, and hold exactly each lane's vectors of their steps.
+//   work shares (gn3d_plan.cuh), strided blocks and unit shares: the reduction
+//     kernels' walks visit every unit once, whole and cut merge blocks complete
+//     exactly once, and the elementwise kernels' walks cover every unit once.
 // Prints "ok <shapes>" or the first failure.
 #include <cstdint>
 #include <cstdio>
@@ -27,6 +30,7 @@
 using namespace gn3d;
 
 static const char* g_what = "";
+static int64_t g_rotated = 0;  // shares whose walk starts with the piece cut at their end
 static int64_t g_shape[4];
 #define CHECK(c)                                                                                     \
   do {                                                                                               \
@@ -70,6 +74,93 @@ static void walk_ncdhw(int64_t N, int64_t C, int64_t S, int64_t G) {
     }
   }
   for (int64_t e = 0; e < numel; ++e) CHECK(cover[e] == 1);
+}
+
+// The streaming kernels' work shares (UnitWalk, UnitWalkDown), in both layouts
+// and for several worker counts: every unit is visited once with consistent
+// (row, k); unit shares tile [0, units) in order; at each block end, whole
+// blocks are merged once and the pieces of a cut block publish disjoint lanes
+// that add up to its size; strided blocks cut none; the downward walks of a
+// worker's `step` warps cover its units exactly once (for unit shares, in the
+// reverse of the upward walk's order).
+static void walk_shares(int64_t N, int64_t C, int64_t S, int64_t G) {
+  g_what = "shares";
+  const Plan p = make_plan(N, C, S, G);
+  const int64_t nblk = p.NC * p.nb;
+  for (bool cut : {false, true})
+    for (int64_t nw : {(int64_t)1, (int64_t)7, (int64_t)608, (int64_t)1216, p.units + 3}) {
+      std::vector<int64_t> cnt(nblk, 0), whole(nblk, 0);
+      std::vector<uint32_t> lanes(nblk, 0);
+      std::vector<uint8_t> seen(p.units, 0);
+      int64_t prev_u1 = 0;
+      for (int64_t w = 0; w < nw; ++w) {
+        UnitWalk cu;
+        cu.set(p, w, nw, cut);
+        if (cut) {
+          CHECK(cu.u0 == prev_u1 && cu.u1 >= cu.u0 && cu.u1 - cu.u0 <= p.units / nw + 1);
+          prev_u1 = cu.u1;
+          if (cu.a != cu.u0) ++g_rotated;
+        }
+        int64_t visited = 0;
+        for (; !cu.end; cu.next(p)) {
+          CHECK(cu.u >= 0 && cu.u < p.units && seen[cu.u] == 0);
+          if (cut) CHECK(cu.u >= cu.u0 && cu.u < cu.u1);
+          seen[cu.u] = 1;
+          ++visited;
+          CHECK(cu.u == cu.row * p.R + cu.k && cu.k >= 0 && cu.k < p.R && cu.row < p.NC);
+          const int ui = cu.ui(), bsz = block_size(p, cu.kb());
+          CHECK(ui < bsz && (int64_t)ui == cu.k - cu.kb() * kBlockUnits);
+          if (!cut) CHECK((cu.row * p.nb + cu.kb()) % nw == w);
+          if (ui == bsz - 1 || cu.u + 1 == cu.u1) {
+            const int64_t ub = cu.u - ui, blk = cu.row * p.nb + cu.kb();
+            const int lo = ub >= cu.u0 ? 0 : (int)(cu.u0 - ub);
+            CHECK(lo >= 0 && lo <= ui && blk < nblk);
+            if (lo == 0 && ui == bsz - 1) {
+              ++whole[blk];
+            } else {
+              CHECK(cut);
+              for (int l = lo; l <= ui; ++l) {
+                CHECK(!(lanes[blk] >> l & 1u));
+                lanes[blk] |= 1u << l;
+              }
+              cnt[blk] += ui - lo + 1;
+            }
+          }
+        }
+        if (cut) CHECK(visited == cu.u1 - cu.u0);
+      }
+      if (cut) CHECK(prev_u1 == p.units);
+      for (int64_t u = 0; u < p.units; ++u) CHECK(seen[u] == 1);
+      for (int64_t b = 0; b < nblk; ++b) {
+        const int bsz = block_size(p, b % p.nb);
+        CHECK((whole[b] == 1 && cnt[b] == 0) || (whole[b] == 0 && cnt[b] == bsz));
+      }
+      for (int step : {2, 4}) {
+        if (nw % step) continue;
+        const int64_t owners = nw / step;
+        std::vector<uint8_t> hit(p.units, 0);
+        for (int64_t w = 0; w < owners; ++w) {
+          UnitWalk up;
+          up.set(p, w, owners, cut);
+          std::vector<int64_t> seq;
+          for (; !up.end; up.next(p)) seq.push_back(up.u);
+          std::vector<uint8_t> mine(p.units, 0);
+          for (int64_t v : seq) mine[v] = 1;
+          for (int skip = 0; skip < step; ++skip) {
+            UnitWalkDown d;
+            d.set(p, w, owners, cut, skip, step);
+            for (int64_t j = skip; !d.end(); d.next(p), j += step) {
+              CHECK(d.u >= 0 && d.u < p.units && mine[d.u] == 1);
+              if (cut) CHECK(j < (int64_t)seq.size() && d.u == seq[seq.size() - 1 - j]);
+              CHECK(d.u == d.row * p.R + d.k && d.k >= 0 && d.k < p.R);
+              CHECK(hit[d.u] == 0);
+              hit[d.u] = 1;
+            }
+          }
+        }
+        for (int64_t u = 0; u < p.units; ++u) CHECK(hit[u] == 1);
+      }
+    }
 }
 
 static void walk_ndhwc(int64_t N, int64_t C, int64_t S, int64_t G) {
@@ -177,10 +268,15 @@ int main() {
           if (N * C * S > 4000000) continue;
           g_shape[0] = N; g_shape[1] = C; g_shape[2] = S; g_shape[3] = G;
           walk_ncdhw(N, C, S, G);
+          walk_shares(N, C, S, G);
           if (C % kNVec == 0) walk_ndhwc(N, C, S, G);
           ++shapes;
         }
       }
+  if (g_rotated == 0) {
+    printf("FAIL no share walk started at its end's cut piece\n");
+    return 1;
+  }
   printf("ok %d\n", shapes);
   return 0;
 }

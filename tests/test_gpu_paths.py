@@ -7,11 +7,12 @@ import pytest
 import bwd_gn3d_stats_gb300 as gn
 from bwd_gn3d_stats_gb300 import synth
 
-from .gpu_util import device_inputs, run_backward, run_forward, to_np, torch
+from .gpu_util import (device_inputs, run_backward, run_backward_relu, run_forward, run_forward_relu, to_np,
+                       torch)
 
 pytestmark = pytest.mark.gpu
 
-DEFAULTS = {gn.DEBUG_PATH: 0, gn.DEBUG_LAG: -1, gn.DEBUG_SLOTS: -1, gn.DEBUG_SPIN_LIMIT: 0}
+DEFAULTS = {gn.DEBUG_PATH: 0, gn.DEBUG_LAG: -1, gn.DEBUG_SLOTS: -1, gn.DEBUG_SPIN_LIMIT: 0, gn.DEBUG_SHARES: -1}
 
 
 @pytest.fixture(autouse=True)
@@ -46,10 +47,21 @@ SHAPES = [
     # against the persistent kernels' general path
     (1, 16, 16, 16, 32, 4, synth.BF16),
     (2, 8, 16, 16, 16, 2, synth.F32),
+    # odd rows of many units, each with head and tail scalars: the reduction
+    # kernels' scalars loaded a unit ahead, across blocks and rows
+    (1, 24, 33, 31, 29, 8, synth.BF16),
+    (1, 12, 37, 35, 33, 4, synth.F32),
+]
+
+# the streaming kernels in unit shares by default (shares of 2 merge blocks or
+# more): equal runs of units per warp, blocks cut between warps
+LARGE = [
+    (1, 40, 160, 160, 160, 8, synth.BF16),
+    (1, 30, 181, 181, 181, 6, synth.BF16),
 ]
 
 
-@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s[:6])) + "_" + s[6])
+@pytest.mark.parametrize("shape", SHAPES + LARGE, ids=lambda s: "x".join(map(str, s[:6])) + "_" + s[6])
 def test_fused_and_streaming_bit_identical(shape):
     site = synth.Site(*shape)
     d = device_inputs(synth.make_inputs(site, seed=11))
@@ -95,3 +107,23 @@ def test_launch_count(path, launches):
     n0 = gn.gn3d_launch_count()
     run_all(site, d)
     assert gn.gn3d_launch_count() - n0 == launches
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s[:6])) + "_" + s[6])
+def test_block_and_unit_shares_bit_identical(shape):
+    """Strided blocks (whole merge blocks dealt out to the warps in turn) and
+    unit shares (equal contiguous runs of units, blocks cut between warps and
+    merged by the warp completing them) place work differently and compute the
+    same bits, with and without the fused ReLU."""
+    site = synth.Site(*shape)
+    d = device_inputs(synth.make_inputs(site, seed=13))
+    gn.gn3d_debug_set(gn.DEBUG_PATH, gn.PATH_STREAMING)
+    out = {}
+    for mode in (0, 1):
+        gn.gn3d_debug_set(gn.DEBUG_SHARES, mode)
+        out[mode] = run_all(site, d)
+        y, mean, rstd = run_forward_relu(site, d["x"], d["gamma"], d["beta"])
+        dx, dg, db = run_backward_relu(site, d["dy"], d["x"], y, mean, rstd, d["gamma"])
+        torch().cuda.synchronize()
+        out[mode] += [to_np(t) for t in (y, mean, rstd, dx, dg, db)]
+    assert same(out[0], out[1])

@@ -3,9 +3,11 @@
 tests/plan_walk.cpp includes the real plan headers (csrc/gn3d_plan.cuh and
 csrc/gn3d_ndhwc_plan.cuh, host-compilable) and walks, for a few thousand
 shapes, every vector and scalar the kernels read, every workspace entry they
-write and read, and the channels-last rings' bulk-copy parts; it fails on the
-first element read twice or never, or any access outside its tensor, unit,
-range or slot."""
+write and read, the channels-last rings' bulk-copy parts, and the NCDHW
+streaming kernels' work shares in both layouts (strided blocks, unit shares
+with cut blocks); it fails on the first element read twice or never, any
+access outside its tensor, unit, range or slot, or a merge block completed
+other than exactly once."""
 import os
 import shutil
 import subprocess
