@@ -197,6 +197,29 @@ def test_kernel_timing_hooks_without_launches(L):
         gn.gn3d_debug_set(gn.DEBUG_TIMING, 0)
 
 
+def test_debug_settings_ranges(L):
+    # every hook accepts its documented range and rejects the rest; none needs a GPU
+    ok = {gn.DEBUG_PATH: (0, 1, 2), gn.DEBUG_LAG: (-1, 0, 8), gn.DEBUG_SLOTS: (-1, 1, 32),
+          gn.DEBUG_SHARES: (-1, 0, 1), gn.DEBUG_SPIN_LIMIT: (0, 1 << 20)}
+    bad = {gn.DEBUG_PATH: (-1, 3), gn.DEBUG_LAG: (-2, 9), gn.DEBUG_SLOTS: (0, -2, 33),
+           gn.DEBUG_SHARES: (-2, 2), gn.DEBUG_SPIN_LIMIT: (-1,)}
+    default = {gn.DEBUG_PATH: 0, gn.DEBUG_LAG: -1, gn.DEBUG_SLOTS: -1, gn.DEBUG_SHARES: -1,
+               gn.DEBUG_SPIN_LIMIT: 0}
+    try:
+        for what, values in ok.items():
+            for v in values:
+                gn.gn3d_debug_set(what, v)
+        for what, values in bad.items():
+            for v in values:
+                with pytest.raises(gn.GN3DError):
+                    gn.gn3d_debug_set(what, v)
+        with pytest.raises(gn.GN3DError):
+            gn.gn3d_debug_set(99, 0)
+    finally:
+        for what, v in default.items():
+            gn.gn3d_debug_set(what, v)
+
+
 @pytest.mark.gpu
 def test_gpu_ndhwc_empty_tensors_and_pointer_checks(L):
     """The channels-last entry points share the argument checks and the empty-
