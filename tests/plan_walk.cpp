@@ -256,8 +256,21 @@ static void walk_ndhwc(int64_t N, int64_t C, int64_t S, int64_t G) {
   }
 }
 
+// The layout each bench volume gets on 152 SMs x 8 reduction warps: strided
+// blocks below two merge blocks per warp (128^3, 96^3, the ragged 97^3 site),
+// unit shares above (256^3).
+static void layouts_of_the_bench_volumes() {
+  g_what = "layouts";
+  const int64_t nw = 152 * 8;
+  CHECK(!use_unit_shares(make_plan(1, 32, 128 * 128 * 128, 8), nw));
+  CHECK(!use_unit_shares(make_plan(2, 64, 96 * 96 * 96, 32), nw));
+  CHECK(!use_unit_shares(make_plan(1, 48, 97 * 97 * 97, 8), nw));
+  CHECK(use_unit_shares(make_plan(1, 32, 256 * 256 * 256, 8), nw));
+}
+
 int main() {
   int shapes = 0;
+  layouts_of_the_bench_volumes();
   const int64_t Cs[] = {1, 3, 4, 6, 8, 16, 24, 32, 40, 48, 64, 96, 128, 192, 256, 264, 320, 512, 768};
   const int64_t Ss[] = {1, 2, 3, 7, 8, 9, 63, 64, 65, 255, 256, 257, 1000, 4096, 4097, 8191, 12345};
   for (int64_t C : Cs)
