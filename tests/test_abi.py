@@ -1,6 +1,5 @@
 """The C ABI: the library builds, loads and exports what include/gn3d.h declares;
 argument checks return the documented status codes."""
-import ctypes
 import os
 import re
 import subprocess

@@ -5,7 +5,6 @@ import numpy as np
 import pytest
 
 import bwd_gn3d_stats_gb300 as gn
-from bwd_gn3d_stats_gb300 import synth
 
 from .gpu_util import to_np, torch
 
