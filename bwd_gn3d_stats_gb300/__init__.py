@@ -264,8 +264,9 @@ def backward(dy, x, mean, rstd, gamma, G: int, out=None):
 
 # ------------------------------------------------------------ testing hooks
 
-DEBUG_PATH, DEBUG_SPIN_LIMIT, DEBUG_FORCE_TIMEOUT, DEBUG_LAG, DEBUG_SLOTS, DEBUG_TIMING, DEBUG_SHARES = range(7)
-PATH_AUTO, PATH_STREAMING, PATH_FUSED = 0, 1, 2
+(DEBUG_PATH, DEBUG_SPIN_LIMIT, DEBUG_FORCE_TIMEOUT, DEBUG_LAG, DEBUG_SLOTS, DEBUG_TIMING, DEBUG_SHARES,
+ DEBUG_RES_HELD, DEBUG_RES_WINDOW, DEBUG_RES_PASS) = range(10)
+PATH_AUTO, PATH_STREAMING, PATH_FUSED, PATH_RESIDENT = 0, 1, 2, 3
 
 
 def gn3d_debug_set(what: int, value: int):
@@ -277,7 +278,7 @@ def gn3d_debug_set(what: int, value: int):
 
 KERNELS = ("k_fwd_fused", "k_bwd_fused", "k_fwd_stats", "k_fwd_norm", "k_bwd_reduce", "k_bwd_dx",
            "k_ndhwc_stats", "k_ndhwc_stats_final", "k_ndhwc_norm", "k_ndhwc_reduce", "k_ndhwc_reduce_final",
-           "k_ndhwc_dx")
+           "k_ndhwc_dx", "k_fwd_resident", "k_bwd_resident")
 
 
 def gn3d_kernel_time(name: str):

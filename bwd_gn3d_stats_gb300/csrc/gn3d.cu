@@ -1,10 +1,13 @@
 // gn3d.cu -- libgn3d's C ABI: argument checks, the launch plan, per-call scratch
 // and the kernel launches for GroupNorm forward and backward (include/gn3d.h).
 //
-// Two launch forms run the same units with the same arithmetic (bit-identical
-// results): the persistent cooperative kernels (gn3d_fused.cuh), used by
-// default, and the streaming kernels (gn3d_kernels.cuh), selectable through
-// gn3d_debug_set for cross-checks and A/B timing.
+// Three launch forms run the same units with the same arithmetic (bit-identical
+// results): the streaming kernels (gn3d_kernels.cuh, two launches per
+// direction), used by default; the persistent cooperative kernels
+// (gn3d_fused.cuh); and the group-wave kernels (gn3d_resident.cuh, one
+// cooperative launch per direction, each group's share held on chip between the
+// two passes).  The last two are selected through gn3d_debug_set, for
+// cross-checks and A/B timing.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdio.h>
@@ -18,6 +21,7 @@
 #include "gn3d_fused.cuh"
 #include "gn3d_kernels.cuh"
 #include "gn3d_ndhwc.cuh"
+#include "gn3d_resident.cuh"
 
 namespace gn3d {
 
@@ -37,6 +41,9 @@ std::atomic<long long> g_hook_timeout{0};  // 1: the next fused launch waits on 
 std::atomic<long long> g_hook_lag{-1};     // -1 auto
 std::atomic<long long> g_hook_slots{-1};   // -1 auto
 std::atomic<int> g_hook_shares{-1};        // -1 auto, 0 strided blocks, 1 unit shares
+std::atomic<long long> g_hook_rheld{-1};   // -1 auto: held units per share of the group-wave kernels
+std::atomic<long long> g_hook_window{-1};  // -1 auto: the group-wave producer's lead, in units
+std::atomic<long long> g_hook_rpass{-1};   // -1 auto: pass-ring slots of the group-wave kernels
 
 constexpr unsigned long long kDefaultSpin = 1ull << 26;  // ~4 s of polls at 64 ns sleeps
 
@@ -161,12 +168,13 @@ int64_t rup(int64_t b) { return ((b + 255) / 256) * 256; }
 // CUDA events on its stream; gn3d_kernel_time resolves them per kernel.
 enum {
   KK_FWD_FUSED, KK_BWD_FUSED, KK_FWD_STATS, KK_FWD_NORM, KK_BWD_REDUCE, KK_BWD_DX,
-  KK_N_STATS, KK_N_STATS_FINAL, KK_N_NORM, KK_N_REDUCE, KK_N_REDUCE_FINAL, KK_N_DX, KK_COUNT
+  KK_N_STATS, KK_N_STATS_FINAL, KK_N_NORM, KK_N_REDUCE, KK_N_REDUCE_FINAL, KK_N_DX, KK_FWD_RES, KK_BWD_RES,
+  KK_COUNT
 };
 const char* const kKernelNames[KK_COUNT] = {
     "k_fwd_fused",   "k_bwd_fused",         "k_fwd_stats",  "k_fwd_norm",     "k_bwd_reduce",
     "k_bwd_dx",      "k_ndhwc_stats",       "k_ndhwc_stats_final", "k_ndhwc_norm", "k_ndhwc_reduce",
-    "k_ndhwc_reduce_final", "k_ndhwc_dx"};
+    "k_ndhwc_reduce_final", "k_ndhwc_dx", "k_fwd_resident", "k_bwd_resident"};
 std::atomic<int> g_timing{0};
 std::mutex g_tmu;
 struct TimedLaunch {
@@ -219,12 +227,58 @@ struct LaunchTimer {
   }
 };
 
-bool use_fused() { return g_hook_path.load() == 2; }
-
 unsigned long long spin_budget() {
   const long long s = g_hook_spin.load();
   return s > 0 ? (unsigned long long)s : kDefaultSpin;
 }
+
+bool use_fused() { return g_hook_path.load() == 2; }
+
+// The group-wave (resident) kernels: every unit full, enough units for every
+// SM to hold a share of each group most of the time.
+bool use_resident(const Plan& p, const DevInfo& di) {
+  const long long h = g_hook_path.load();
+  if (h == 3) return plan_all_full(p);
+  if (h != 0) return false;
+  return false;
+}
+
+// Ring sizes of a group-wave launch: as many slots as fit next to the piece
+// records, three of them in the pass ring; held units per share: half the held
+// ring (so a share of the next group loads while the current one waits for its
+// statistics); the producer's lead: half of L2's share per SM.
+ResCfg resident_cfg(const DevInfo& di, const Plan& p, int kred, int slot_bytes, int fixed_bytes, int* smem) {
+  ResCfg c;
+  const int fixed = 2048 + fixed_bytes;  // 2 KB: static shared memory and slack
+  const int nslots = (di.smem_optin - fixed) / (slot_bytes + 16);
+  // both rings a multiple of the reduction warps (each slot read by one warp)
+  const long long hp = g_hook_rpass.load();
+  int kp = hp >= 1 ? (int)hp : kred;
+  kp = (kp + kred - 1) / kred * kred;
+  if (kp > nslots - kred) kp = (nslots - kred) / kred * kred;
+  const int kh = (nslots - kp) / kred * kred;
+  int rh = kh / 2 > 0 ? kh / 2 : 1;
+  const long long hr = g_hook_rheld.load(), hw = g_hook_window.load();
+  if (hr >= 0 && hr <= kh) rh = (int)hr;
+  c.geo = res_geo(p, di.sms, rh, kh, kp, 0);
+  c.window = (long long)di.l2_bytes / 2 / di.sms / slot_bytes;
+  if (c.window < nslots) c.window = nslots;
+  if (hw >= 1) c.window = hw;
+  // a whole share of a group must fit in the lead, else nothing could ever be normalized
+  if (c.window < res_min_window(p, di.sms)) c.window = res_min_window(p, di.sms);
+  c.force_timeout = g_hook_timeout.exchange(0) != 0;
+  c.spin = spin_budget();
+  *smem = (kh + kp) * slot_bytes + 2 * (kh + kp) * 8 + fixed_bytes;
+  return c;
+}
+
+// The lead's bound from the per-CTA group counters: fewer groups in flight than
+// the counters (each group in flight holds at least max(q, 1) of the lead's units).
+bool resident_lead_ok(const ResCfg& c) {
+  const long long per = c.geo.q > 0 ? c.geo.q : 1;
+  return c.window / per + 2 < kCtrRing;
+}
+
 
 // Shared-memory slots of a persistent launch (one CTA per SM) and its schedule.
 // Dynamic shared memory: slots, two mbarriers per slot, slots + 2 block records.
@@ -332,7 +386,25 @@ int launch_forward(const void* x, const float* gamma, const float* beta, const P
   cudaError_t e = cudaMemsetAsync(sync, 0, (size_t)nsync * sizeof(uint32_t), st);
   const TI* xp = static_cast<const TI*>(x);
   TO* yp = static_cast<TO*>(y);
-  if (e == cudaSuccess && fused) {
+  if (e == cudaSuccess && use_resident(p, di)) {
+    int smem = 0;
+    using Shape = ResFwdShape<TI>;
+    using Lay = ResLayout<Shape::kSlotBytes, Part, Shape::kRound>;
+    ResCfg cfg = resident_cfg(di, p, Shape::kRed, Shape::kSlotBytes, Lay::bytes(0, 0), &smem);
+    auto k = relu ? k_fwd_resident<TI, TO, true> : k_fwd_resident<TI, TO, false>;
+    int rc = resident_lead_ok(cfg) ? raise_smem((const void*)k, smem, di) : arg_fail("group-wave lead too long");
+    const int threads = 32 * ResFwdShape<TI>::kWarps;
+    int grid = 0;
+    if (!rc) rc = coop_grid((const void*)k, threads, smem, di, &grid);
+    if (rc) { cudaFreeAsync(s.base, st); return rc; }
+    ResSync rs{fs.abort, fs.never, fs.status};
+    void* args[] = {(void*)&xp, (void*)&yp, (void*)&p, (void*)&w, (void*)&cfg, (void*)&rs, (void*)&eps,
+                    (void*)&gamma, (void*)&beta, (void*)&mean, (void*)&rstd};
+    g_launches += 1;
+    LaunchTimer tm(KK_FWD_RES, st, di);
+    e = cudaLaunchCooperativeKernel((const void*)k, dim3(grid), dim3(threads), args, (size_t)smem, st);
+    tm.done();
+  } else if (e == cudaSuccess && fused) {
     const int slot = kUnitElems * (int)sizeof(TI);
     const int rec = (int)sizeof(BlockRec<Part>);
     FusedCfg cfg = fused_cfg(di, slot, rec, p.M * (int64_t)sizeof(TI));
@@ -440,7 +512,25 @@ int launch_backward(const void* dy, const void* x, const void* res, const float*
   const T* dyp = static_cast<const T*>(dy);
   const T* xp = static_cast<const T*>(x);
   T* dxp = static_cast<T*>(dx);
-  if (e == cudaSuccess && fused) {
+  if (e == cudaSuccess && !res && sizeof(T) == 2 && use_resident(p, di)) {
+    int smem = 0;
+    using Shape = ResBwdShape<T>;
+    using Lay = ResLayout<Shape::kSlotBytes, float2, Shape::kRound>;
+    ResCfg cfg = resident_cfg(di, p, Shape::kRed, Shape::kSlotBytes, Lay::bytes(0, 0), &smem);
+    auto k = k_bwd_resident<T>;
+    int rc = resident_lead_ok(cfg) ? raise_smem((const void*)k, smem, di) : arg_fail("group-wave lead too long");
+    const int threads = 32 * ResBwdShape<T>::kWarps;
+    int grid = 0;
+    if (!rc) rc = coop_grid((const void*)k, threads, smem, di, &grid);
+    if (rc) { cudaFreeAsync(s.base, st); return rc; }
+    ResSync rs{fs.abort, fs.never, fs.status};
+    void* args[] = {(void*)&dyp, (void*)&xp, (void*)&dxp, (void*)&p, (void*)&mean, (void*)&rstd, (void*)&gamma,
+                    (void*)&w, (void*)&cfg, (void*)&rs, (void*)&dgamma, (void*)&dbeta};
+    g_launches += 1;
+    LaunchTimer tm(KK_BWD_RES, st, di);
+    e = cudaLaunchCooperativeKernel((const void*)k, dim3(grid), dim3(threads), args, (size_t)smem, st);
+    tm.done();
+  } else if (e == cudaSuccess && fused) {
     const int slot = 2 * kUnitElems * (int)sizeof(T);
     const int rec = (int)sizeof(BlockRec<float2>);
     FusedCfg cfg = fused_cfg(di, slot, rec, 2 * p.M * (int64_t)sizeof(T));
@@ -921,7 +1011,7 @@ extern "C" int gn3d_stream_status(void* stream) {
 extern "C" int gn3d_debug_set(int what, long long value) {
   switch (what) {
     case GN3D_DEBUG_PATH:
-      if (value < 0 || value > 2) return arg_fail("path: 0, 1 or 2");
+      if (value < 0 || value > 3) return arg_fail("path: 0 .. 3");
       g_hook_path = value;
       break;
     case GN3D_DEBUG_SPIN_LIMIT:
@@ -959,6 +1049,18 @@ extern "C" int gn3d_debug_set(int what, long long value) {
     case GN3D_DEBUG_SHARES:
       if (value < -1 || value > 1) return arg_fail("shares: -1, 0 or 1");
       g_hook_shares = (int)value;
+      break;
+    case GN3D_DEBUG_RES_HELD:
+      if (value < -1) return arg_fail("held units: -1 or >= 0");
+      g_hook_rheld = value;
+      break;
+    case GN3D_DEBUG_RES_PASS:
+      if (value < -1 || value == 0) return arg_fail("pass slots: -1 or >= 1");
+      g_hook_rpass = value;
+      break;
+    case GN3D_DEBUG_RES_WINDOW:
+      if (value < -1 || value == 0) return arg_fail("window: -1 or >= 1");
+      g_hook_window = value;
       break;
     default:
       return arg_fail("unknown debug setting");

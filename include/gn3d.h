@@ -220,7 +220,13 @@ uint64_t gn3d_launch_count(void);
  * result bit: both launch forms run the same units and reduction trees.
  *   GN3D_DEBUG_PATH          0 automatic (the streaming kernels: two launches
  *                            per direction), 1 streaming, 2 persistent (one
- *                            cooperative launch per direction).
+ *                            cooperative launch per direction), 3 group-wave
+ *                            (one cooperative launch per direction; every CTA
+ *                            holds a share of every group in shared memory
+ *                            between the two passes; shapes whose rows are
+ *                            whole 4096-element units, and not the fused-ReLU
+ *                            or fp32 backward, which stay on the streaming
+ *                            kernels).
  *   GN3D_DEBUG_SPIN_LIMIT    poll budget of every bounded device-side wait
  *                            (0 = default, about four seconds).  A kernel
  *                            whose wait gave up still waits for its own bulk
@@ -244,6 +250,15 @@ uint64_t gn3d_launch_count(void);
  *                            among their warps (whole merge blocks dealt out in
  *                            turn, or equal contiguous runs of units that may
  *                            cut a block between two warps).  Placement only.
+ *   GN3D_DEBUG_RES_HELD      -1 automatic, else >= 0: units of each CTA's share
+ *                            of a group the group-wave kernels keep in shared
+ *                            memory (the others are read again from L2).
+ *   GN3D_DEBUG_RES_WINDOW    -1 automatic, else >= 1: units the group-wave
+ *                            producer may run ahead of the elementwise pass (at
+ *                            least one share of a group is always allowed).
+ *   GN3D_DEBUG_RES_PASS      -1 automatic, else >= 1: slots of the group-wave
+ *                            kernels' pass ring (rounded up to a multiple of
+ *                            their reduction warps).
  * Returns GN3D_OK or GN3D_ERR_INVALID_ARG for an unknown setting or value.
  */
 enum {
@@ -253,7 +268,10 @@ enum {
   GN3D_DEBUG_LAG = 3,
   GN3D_DEBUG_SLOTS = 4,
   GN3D_DEBUG_TIMING = 5,
-  GN3D_DEBUG_SHARES = 6
+  GN3D_DEBUG_SHARES = 6,
+  GN3D_DEBUG_RES_HELD = 7,
+  GN3D_DEBUG_RES_WINDOW = 8,
+  GN3D_DEBUG_RES_PASS = 9
 };
 int gn3d_debug_set(int what, long long value);
 
@@ -262,7 +280,7 @@ int gn3d_debug_set(int what, long long value);
  * GN3D_DEBUG_TIMING was last set to 1.  `name` is one of "k_fwd_fused",
  * "k_bwd_fused", "k_fwd_stats", "k_fwd_norm", "k_bwd_reduce", "k_bwd_dx",
  * "k_ndhwc_stats", "k_ndhwc_stats_final", "k_ndhwc_norm", "k_ndhwc_reduce",
- * "k_ndhwc_reduce_final", "k_ndhwc_dx".
+ * "k_ndhwc_reduce_final", "k_ndhwc_dx", "k_fwd_resident", "k_bwd_resident".
  * Waits for the recorded events (host-blocking), then writes the total
  * milliseconds to *ms and the launch count to *launches.  Returns GN3D_OK,
  * GN3D_ERR_INVALID_ARG (NULL argument, unknown name) or GN3D_ERR_CUDA.

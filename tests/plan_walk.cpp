@@ -12,6 +12,13 @@
 //   work shares (gn3d_plan.cuh), strided blocks and unit shares: the reduction
 //     kernels' walks visit every unit once, whole and cut merge blocks complete
 //     exactly once, and the elementwise kernels' walks cover every unit once.
+//   group-wave placement (gn3d_resident_plan.cuh): the shares of every group
+//     tile it in CTA order and every CTA's total differs from every other's by
+//     at most one unit; each CTA's sequence visits its units in order with
+//     consistent (row, k), group, held/pass ring positions and piece spans; the
+//     pieces of each merge block cover its units exactly once; the elementwise
+//     order covers the same units once (also split over several warps) and
+//     finds each held unit at the held position the sequence gave it.
 // Prints "ok <shapes>" or the first failure.
 #include <cstdint>
 #include <cstdio>
@@ -24,8 +31,12 @@
 #ifndef __device__
 #define __device__
 #endif
+#ifndef __forceinline__
+#define __forceinline__ inline
+#endif
 #include "../bwd_gn3d_stats_gb300/csrc/gn3d_plan.cuh"
 #include "../bwd_gn3d_stats_gb300/csrc/gn3d_ndhwc_plan.cuh"
+#include "../bwd_gn3d_stats_gb300/csrc/gn3d_resident_plan.cuh"
 
 using namespace gn3d;
 
@@ -259,6 +270,301 @@ static void walk_ndhwc(int64_t N, int64_t C, int64_t S, int64_t G) {
 // The layout each bench volume gets on 152 SMs x 8 reduction warps: strided
 // blocks below two merge blocks per warp (128^3, 96^3, the ragged 97^3 site),
 // unit shares above (256^3).
+
+// The group-wave kernels' placement for P CTAs, rh held units per share and
+// rings of kh held and kp pass slots.
+static void walk_resident(const Plan& p, int P, int rh, int kh, int kp, int recs) {
+  g_what = "resident";
+  const ResGeo G = res_geo(p, P, rh, kh, kp, recs);
+  const int64_t nblk = p.NC * p.nb;
+  std::vector<int32_t> owner(p.units, -1);
+  std::vector<int64_t> held_at(p.units, -1);
+  std::vector<int64_t> block_units(nblk, 0);
+  std::vector<uint32_t> block_lanes(nblk, 0);
+  std::vector<int64_t> total(P, 0);
+  for (int64_t g = 0; g < p.NG; ++g) {  // shares tile the group in CTA order
+    int64_t at = g * p.upg;
+    for (int c = 0; c < P; ++c) {
+      const ResShare sh = res_share(p, G, g, c);
+      CHECK(sh.start == at && sh.n >= 0 && sh.nh == (sh.n < rh ? sh.n : rh));
+      at += sh.n;
+      total[c] += sh.n;
+    }
+    CHECK(at == (g + 1) * p.upg);
+  }
+  int64_t tmin = INT64_MAX, tmax = 0;
+  for (int c = 0; c < P; ++c) {
+    tmin = total[c] < tmin ? total[c] : tmin;
+    tmax = total[c] > tmax ? total[c] : tmax;
+  }
+  CHECK(tmax - tmin <= 1);
+  for (int c = 0; c < P; ++c) {
+    ResSeq s;
+    s.begin(p, G, c);
+    int64_t h = 0, q = 0, piece = -1, pblk = -1, n = 0;
+    int plo = -1, phi = -1;
+    std::vector<int64_t> order;
+    while (!s.end) {
+      const int64_t u = s.unit_index();
+      CHECK(u >= 0 && u < p.units && s.k == u % p.R && s.g == (u / p.R) / p.Cg);
+      CHECK(u >= s.sh.start && u < s.sh.start + s.sh.n && s.j == u - s.sh.start);
+      CHECK(s.h == h && s.q == q);
+      CHECK(owner[u] == -1);
+      owner[u] = c;
+      const bool hd = s.held();
+      CHECK(hd == (s.j >= s.sh.n - s.sh.nh));
+      const int64_t ri = hd ? h : q, rn = hd ? kh : kp;
+      CHECK(s.ring_index() == ri && s.slot() == ri % rn && s.parity() == (uint32_t)((ri / rn) & 1));
+      if (hd) held_at[u] = h++;
+      else ++q;
+      int64_t b0;
+      int lo, hi, bsz;
+      s.piece_span(p, b0, lo, hi, bsz);
+      const int ui = (int)(s.k % kBlockUnits);
+      const int64_t blk = (u / p.R) * p.nb + s.k / kBlockUnits;
+      CHECK(s.block(p) == blk && b0 == u - ui && lo >= 0 && lo <= ui && ui <= hi && hi < bsz && bsz <= kBlockUnits);
+      if (blk != pblk) {  // a new piece
+        ++piece;
+        pblk = blk;
+        plo = lo;
+        phi = hi;
+        const uint32_t m = (uint32_t)((((uint64_t)1 << (hi + 1)) - 1) & ~(((uint64_t)1 << lo) - 1));
+        CHECK((block_lanes[blk] & m) == 0);
+        block_lanes[blk] |= m;
+        block_units[blk] += hi - lo + 1;
+      } else {
+        CHECK(lo == plo && hi == phi);
+      }
+      order.push_back(u);
+      ++n;
+      s.next(p, G, c);
+    }
+    CHECK(n == total[c] && s.h + s.q == n);
+    // the kernels' per-share walks: the producer's order is the sequence; each
+    // reduction warp takes, per share, the pass units then the held units at
+    // ring positions = warp (mod 4), with the slot and parity the sequence gave
+    for (int w = 0; w < 4 && kh % 4 == 0 && kp % 4 == 0; ++w) {
+      std::vector<int64_t> mine;  // (unit) in the warp's order, from the sequence
+      std::vector<std::pair<int, uint32_t>> ring;
+      ResSeq t;
+      t.begin(p, G, c);
+      for (; !t.end; t.next(p, G, c))
+        if (t.slot() % 4 == w) {
+          mine.push_back(t.unit_index());
+          ring.push_back({t.slot(), t.parity()});
+        }
+      size_t at = 0;
+      int hb = 0, qb = 0;
+      for (int64_t g = 0; g < p.NG; ++g) {
+        const ResShare sh = res_share(p, G, g, c);
+        if (sh.n == 0) continue;
+        const int npass = sh.n - sh.nh;
+        for (int part = 0; part < 2; ++part) {
+          const bool hd = part == 1;
+          const int first = hd ? npass : 0, count = hd ? sh.nh : npass, before = hd ? hb : qb;
+          const int nr = hd ? kh : kp;
+          int j = res_first_of_warp(before, w, 4);
+          if (j >= count) continue;
+          RingPos r;
+          r.at(before + j, nr);
+          for (; j < count; j += 4, r.step(4, nr)) {
+            CHECK(at < mine.size() && mine[at] == sh.start + first + j);
+            CHECK(ring[at].first == r.slot && ring[at].second == r.par);
+            ++at;
+          }
+        }
+        hb += sh.nh;
+        qb += npass;
+      }
+      CHECK(at == mine.size());
+    }
+    std::vector<int64_t> pos_of(p.units, -1);
+    for (int64_t i = 0; i < (int64_t)order.size(); ++i) pos_of[order[i]] = i;
+    // the elementwise order: the same units, each share last unit first, held
+    // units at the slots the sequence gave them; split over 1 or 7 warps
+    for (int step : {1, 7}) {
+      std::vector<uint8_t> got(order.size(), 0);
+      int64_t count = 0;
+      for (int w = 0; w < step; ++w) {
+        ResElemSeq e;
+        e.begin(p, G, c);
+        e.advance(p, G, c, w);
+        while (!e.end) {
+          const int64_t u = e.unit();
+          CHECK(u >= 0 && u < p.units && owner[u] == c);
+          CHECK(e.j() >= 0 && e.j() < e.sh.n && e.g == (u / p.R) / p.Cg);
+          CHECK(e.held() == (held_at[u] >= 0));
+          if (e.held()) {
+            CHECK(e.hidx() == held_at[u]);
+            int slot;
+            uint32_t par;
+            e.held_slot(G, slot, par);
+            CHECK(slot == held_at[u] % kh && par == (uint32_t)((held_at[u] / kh) & 1));
+          }
+          const int64_t pos = pos_of[u];
+          CHECK(pos >= 0 && got[pos] == 0);
+          got[pos] = 1;
+          ++count;
+          e.advance(p, G, c, step);
+        }
+      }
+      CHECK(count == (int64_t)order.size());
+    }
+  }
+  for (int64_t u = 0; u < p.units; ++u) CHECK(owner[u] >= 0);
+  for (int64_t b = 0; b < nblk; ++b) {
+    const int bsz = block_size(p, b % p.nb);
+    CHECK(block_units[b] == bsz && block_lanes[b] == (uint32_t)((((uint64_t)1) << bsz) - 1));
+  }
+}
+
+static void walk_resident_shapes() {
+  // rows of whole units (the group-wave kernels' domain), the bench volumes among them
+  struct Sh { int64_t N, C, S, G; };
+  const Sh shapes[] = {{1, 32, 128 * 128 * 128, 8}, {1, 32, 256 * 256 * 256, 8}, {2, 64, 96 * 96 * 96, 32},
+                       {1, 64, 128 * 128 * 128, 8}, {1, 128, 64 * 64 * 64, 8}, {1, 256, 32 * 32 * 32, 8},
+                       {1, 512, 16 * 16 * 16, 8},   {2, 16, 16 * 16 * 16, 4},   {1, 4, 4096, 1},
+                       {3, 6, 4096 * 5, 3},          {1, 12, 4096 * 33, 4},      {2, 40, 4096 * 17, 8},
+                       {1, 1, 4096 * 3, 1},          {1, 8, 4096 * 300, 2}};
+  for (const Sh& sh : shapes) {
+    g_shape[0] = sh.N; g_shape[1] = sh.C; g_shape[2] = sh.S; g_shape[3] = sh.G;
+    const Plan p = make_plan(sh.N, sh.C, sh.S, sh.G);
+    CHECK(plan_all_full(p));
+    for (int P : {1, 7, 152, 160})
+      for (int rh : {1, 5, 10, 1000}) {
+        if ((P > 1 && p.units > 200000 && rh != 10) || (p.units > 50000 && P < 152)) continue;  // bounded run time
+        walk_resident(p, P, rh < 20 ? rh : 20, 20, 4, 16);
+        if (rh == 5) walk_resident(p, P, rh, 8, 4, 3);
+      }
+  }
+}
+
+// The group-wave kernels' synchronization, simulated: per CTA a producer that
+// issues the sequence's copies in order (a held or pass slot's next use only
+// after its previous use was released, and at most `window` units ahead of the
+// elementwise pass), kRed reduction warps (slot s of either ring read by warp
+// s mod kRed, in order; a pass slot released after the reduction; a group is
+// ready once every unit of it is reduced), and the elementwise warps, which
+// move through the CTA's shares together (named barriers), a share once its
+// group is ready, releasing its held slots.  Agents take enabled steps in a
+// seeded random order; the run must finish every unit with no state in which
+// nothing can move.
+struct SimPos { int64_t u, g, use; bool held; int slot; };
+static void sim_resident(const Plan& p, int P, int kh, int kp, int rh, int64_t window, int kRed, uint64_t seed) {
+  g_what = "resident-sim";
+  std::vector<int64_t> gleft(p.NG, p.upg);
+  std::vector<uint8_t> ready(p.NG, 0);
+  struct Cta {
+    std::vector<SimPos> seq;                 // sequence order
+    std::vector<std::vector<int64_t>> shares;  // per share (group order): its positions
+    int64_t issued = 0, normed = 0, next_share = 0;
+    std::vector<int64_t> hrel, prel;         // uses released per slot
+    std::vector<std::vector<int64_t>> rpos;  // positions of each reduction warp, in order
+    std::vector<int64_t> rnext;
+  };
+  std::vector<Cta> ctas(P);
+  int64_t total = 0;
+  const ResGeo G = res_geo(p, P, rh, kh, kp, 0);
+  for (int c = 0; c < P; ++c) {
+    Cta& t = ctas[c];
+    ResSeq s;
+    s.begin(p, G, c);
+    int64_t gprev = -1;
+    while (!s.end) {
+      const bool hd = s.held();
+      const int64_t i = s.ring_index();
+      if (s.g != gprev) {
+        t.shares.push_back({});
+        gprev = s.g;
+      }
+      t.shares.back().push_back((int64_t)t.seq.size());
+      t.seq.push_back(SimPos{s.unit_index(), s.g, i / (hd ? kh : kp), hd, s.slot()});
+      s.next(p, G, c);
+    }
+    t.hrel.assign(kh, 0);
+    t.prel.assign(kp, 0);
+    t.rpos.assign(kRed, {});
+    for (int64_t i = 0; i < (int64_t)t.seq.size(); ++i) t.rpos[t.seq[i].slot % kRed].push_back(i);
+    t.rnext.assign(kRed, 0);
+    total += (int64_t)t.seq.size();
+  }
+  uint64_t rng = seed * 0x9E3779B97F4A7C15ull + 1;
+  auto rnd = [&](uint64_t n) {
+    rng ^= rng << 13; rng ^= rng >> 7; rng ^= rng << 17;
+    return rng % n;
+  };
+  const int agents = 2 + kRed;  // producer, reduction warps, the elementwise warps together
+  auto step = [&](Cta& t, int a) -> bool {
+    if (a == 0) {  // producer
+      if (t.issued >= (int64_t)t.seq.size()) return false;
+      const SimPos& q = t.seq[t.issued];
+      const int64_t rel = q.held ? t.hrel[q.slot] : t.prel[q.slot];
+      if (rel < q.use) return false;  // the slot's previous use not yet released
+      if (t.issued >= t.normed + window) return false;
+      ++t.issued;
+      return true;
+    }
+    if (a <= kRed) {  // reduction warp
+      int64_t& k = t.rnext[a - 1];
+      const std::vector<int64_t>& mine = t.rpos[a - 1];
+      if (k >= (int64_t)mine.size() || mine[k] >= t.issued) return false;
+      const SimPos& q = t.seq[mine[k]];
+      if (!q.held) ++t.prel[q.slot];
+      if (--gleft[q.g] == 0) ready[q.g] = 1;
+      ++k;
+      return true;
+    }
+    // the elementwise warps: the next share, once its group is ready
+    if (t.next_share >= (int64_t)t.shares.size()) return false;
+    const std::vector<int64_t>& sh = t.shares[t.next_share];
+    if (!ready[t.seq[sh[0]].g]) return false;
+    for (int64_t i : sh) {
+      const SimPos& q = t.seq[i];
+      if (q.held) {
+        CHECK(t.hrel[q.slot] == q.use);  // released in use order
+        ++t.hrel[q.slot];
+      }
+    }
+    t.normed += (int64_t)sh.size();
+    ++t.next_share;
+    return true;
+  };
+  for (;;) {
+    bool moved = false;
+    const int c0 = (int)rnd(P);
+    for (int dc = 0; dc < P && !moved; ++dc) {
+      Cta& t = ctas[(c0 + dc) % P];
+      const int a0 = (int)rnd(agents);
+      for (int da = 0; da < agents && !moved; ++da)
+        if (step(t, (a0 + da) % agents)) moved = true;
+    }
+    if (!moved) break;
+  }
+  int64_t done = 0;
+  for (const Cta& t : ctas) done += t.normed;
+  CHECK(done == total);  // else: no agent could move -- a deadlock
+  for (int64_t g = 0; g < p.NG; ++g) CHECK(ready[g]);
+}
+
+static void sim_resident_shapes() {
+  struct Sh { int64_t N, C, S, G; };
+  const Sh shapes[] = {{1, 32, 128 * 128 * 128, 8}, {2, 64, 96 * 96 * 96, 32}, {1, 512, 16 * 16 * 16, 8},
+                       {1, 256, 32 * 32 * 32, 8},   {3, 6, 4096 * 5, 3},        {1, 12, 4096 * 33, 4}};
+  for (const Sh& sh : shapes) {
+    g_shape[0] = sh.N; g_shape[1] = sh.C; g_shape[2] = sh.S; g_shape[3] = sh.G;
+    const Plan p = make_plan(sh.N, sh.C, sh.S, sh.G);
+    // forward bf16 rings (20 held + 4 pass), backward bf16 rings (8 + 4), minimal
+    // rings; held slots a multiple of the 4 reduction warps
+    const int rings[3][2] = {{20, 4}, {8, 4}, {4, 4}};
+    for (const auto& rg : rings)
+      for (int rh : {0, rg[0] / 2, rg[0]})
+        // the window must admit a whole share of a group (its statistics need it)
+        for (int64_t window : {res_min_window(p, 152), res_min_window(p, 152) + rg[0] + rg[1], (int64_t)1000000})
+          for (uint64_t seed : {1ull, 2ull})
+            sim_resident(p, 152, rg[0], rg[1], rh, window, 4, seed);
+  }
+}
+
 static void layouts_of_the_bench_volumes() {
   g_what = "layouts";
   const int64_t nw = 152 * 8;
@@ -271,6 +577,8 @@ static void layouts_of_the_bench_volumes() {
 int main() {
   int shapes = 0;
   layouts_of_the_bench_volumes();
+  walk_resident_shapes();
+  sim_resident_shapes();
   const int64_t Cs[] = {1, 3, 4, 6, 8, 16, 24, 32, 40, 48, 64, 96, 128, 192, 256, 264, 320, 512, 768};
   const int64_t Ss[] = {1, 2, 3, 7, 8, 9, 63, 64, 65, 255, 256, 257, 1000, 4096, 4097, 8191, 12345};
   for (int64_t C : Cs)

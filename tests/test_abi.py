@@ -198,12 +198,14 @@ def test_kernel_timing_hooks_without_launches(L):
 
 def test_debug_settings_ranges(L):
     # every hook accepts its documented range and rejects the rest; none needs a GPU
-    ok = {gn.DEBUG_PATH: (0, 1, 2), gn.DEBUG_LAG: (-1, 0, 8), gn.DEBUG_SLOTS: (-1, 1, 32),
-          gn.DEBUG_SHARES: (-1, 0, 1), gn.DEBUG_SPIN_LIMIT: (0, 1 << 20)}
-    bad = {gn.DEBUG_PATH: (-1, 3), gn.DEBUG_LAG: (-2, 9), gn.DEBUG_SLOTS: (0, -2, 33),
-           gn.DEBUG_SHARES: (-2, 2), gn.DEBUG_SPIN_LIMIT: (-1,)}
+    ok = {gn.DEBUG_PATH: (0, 1, 2, 3), gn.DEBUG_LAG: (-1, 0, 8), gn.DEBUG_SLOTS: (-1, 1, 32),
+          gn.DEBUG_SHARES: (-1, 0, 1), gn.DEBUG_SPIN_LIMIT: (0, 1 << 20), gn.DEBUG_RES_HELD: (-1, 0, 7),
+          gn.DEBUG_RES_WINDOW: (-1, 1, 500), gn.DEBUG_RES_PASS: (-1, 1, 12)}
+    bad = {gn.DEBUG_PATH: (-1, 4), gn.DEBUG_LAG: (-2, 9), gn.DEBUG_SLOTS: (0, -2, 33),
+           gn.DEBUG_SHARES: (-2, 2), gn.DEBUG_SPIN_LIMIT: (-1,), gn.DEBUG_RES_HELD: (-2,),
+           gn.DEBUG_RES_WINDOW: (-2, 0), gn.DEBUG_RES_PASS: (-2, 0)}
     default = {gn.DEBUG_PATH: 0, gn.DEBUG_LAG: -1, gn.DEBUG_SLOTS: -1, gn.DEBUG_SHARES: -1,
-               gn.DEBUG_SPIN_LIMIT: 0}
+               gn.DEBUG_SPIN_LIMIT: 0, gn.DEBUG_RES_HELD: -1, gn.DEBUG_RES_WINDOW: -1, gn.DEBUG_RES_PASS: -1}
     try:
         for what, values in ok.items():
             for v in values:

@@ -12,7 +12,8 @@ from .gpu_util import (device_inputs, run_backward, run_backward_relu, run_forwa
 
 pytestmark = pytest.mark.gpu
 
-DEFAULTS = {gn.DEBUG_PATH: 0, gn.DEBUG_LAG: -1, gn.DEBUG_SLOTS: -1, gn.DEBUG_SPIN_LIMIT: 0, gn.DEBUG_SHARES: -1}
+DEFAULTS = {gn.DEBUG_PATH: 0, gn.DEBUG_LAG: -1, gn.DEBUG_SLOTS: -1, gn.DEBUG_SPIN_LIMIT: 0, gn.DEBUG_SHARES: -1,
+            gn.DEBUG_RES_HELD: -1, gn.DEBUG_RES_WINDOW: -1, gn.DEBUG_RES_PASS: -1}
 
 
 @pytest.fixture(autouse=True)
@@ -127,3 +128,77 @@ def test_block_and_unit_shares_bit_identical(shape):
         torch().cuda.synchronize()
         out[mode] += [to_np(t) for t in (y, mean, rstd, dx, dg, db)]
     assert same(out[0], out[1])
+
+
+# rows of whole 4096-element units: the group-wave kernels' domain (several
+# shares per group, groups smaller than the SM count, N > 1, fp32, one group)
+RESIDENT = [
+    (1, 32, 32, 32, 32, 8, synth.BF16),
+    (2, 64, 32, 32, 48, 32, synth.BF16),
+    (1, 512, 16, 16, 16, 8, synth.BF16),
+    (1, 32, 128, 128, 128, 8, synth.BF16),
+    (2, 16, 16, 16, 16, 4, synth.F32),
+    (1, 16, 64, 64, 64, 1, synth.F32),
+    (3, 12, 16, 32, 40, 3, synth.BF16),
+]
+
+
+@pytest.mark.parametrize("shape", RESIDENT, ids=lambda s: "x".join(map(str, s[:6])) + "_" + s[6])
+def test_group_wave_and_streaming_bit_identical(shape):
+    """The group-wave kernels (each CTA a share of every group, the group merged
+    from its unit partials by every CTA) and the streaming kernels give the same
+    bits: the same units, merge blocks and group merges, placed differently."""
+    site = synth.Site(*shape)
+    d = device_inputs(synth.make_inputs(site, seed=21))
+    gn.gn3d_debug_set(gn.DEBUG_PATH, gn.PATH_STREAMING)
+    a = run_all(site, d)
+    gn.gn3d_debug_set(gn.DEBUG_PATH, gn.PATH_RESIDENT)
+    b = run_all(site, d)
+    gn.gn3d_stream_status(torch().cuda.current_stream().cuda_stream)
+    assert same(a, b)
+
+
+@pytest.mark.parametrize("held,passes,window", [(0, 8, -1), (3, 4, -1), (20, 4, -1), (5, 4, 30), (10, 12, 200)])
+def test_group_wave_ring_settings_do_not_move_a_bit(held, passes, window):
+    """Held units per share, pass-ring slots and the producer's lead decide what
+    stays on chip and what is read again from L2, never a value."""
+    site = synth.Site(1, 24, 48, 48, 64, 6, synth.BF16)
+    d = device_inputs(synth.make_inputs(site, seed=22))
+    gn.gn3d_debug_set(gn.DEBUG_PATH, gn.PATH_STREAMING)
+    ref = run_all(site, d)
+    gn.gn3d_debug_set(gn.DEBUG_PATH, gn.PATH_RESIDENT)
+    gn.gn3d_debug_set(gn.DEBUG_RES_HELD, held)
+    gn.gn3d_debug_set(gn.DEBUG_RES_PASS, passes)
+    gn.gn3d_debug_set(gn.DEBUG_RES_WINDOW, window)
+    assert same(ref, run_all(site, d))
+
+
+def test_group_wave_mixed_dtypes_and_relu():
+    """bf16 -> fp32 and fp32 -> bf16 forwards and the fused ReLU forward on the
+    group-wave kernel match the streaming kernels bit for bit."""
+    site = synth.Site(1, 16, 32, 32, 32, 4, synth.BF16)
+    d = device_inputs(synth.make_inputs(site, seed=23))
+    outs = {}
+    for path in (gn.PATH_STREAMING, gn.PATH_RESIDENT):
+        gn.gn3d_debug_set(gn.DEBUG_PATH, path)
+        r = [to_np(t) for t in run_forward(site, d["x"], d["gamma"], d["beta"], out_dtype=synth.F32)]
+        r += [to_np(t) for t in run_forward_relu(site, d["x"], d["gamma"], d["beta"])]
+        torch().cuda.synchronize()
+        outs[path] = r
+    assert same(outs[gn.PATH_STREAMING], outs[gn.PATH_RESIDENT])
+
+
+def test_group_wave_timeout_reports_and_recovers():
+    site = synth.Site(1, 8, 32, 32, 32, 4, synth.BF16)
+    d = device_inputs(synth.make_inputs(site, seed=24))
+    ref = run_all(site, d)
+    st = torch().cuda.current_stream().cuda_stream
+    gn.gn3d_debug_set(gn.DEBUG_PATH, gn.PATH_RESIDENT)
+    gn.gn3d_debug_set(gn.DEBUG_SPIN_LIMIT, 20000)
+    gn.gn3d_debug_set(gn.DEBUG_FORCE_TIMEOUT, 1)
+    run_forward(site, d["x"], d["gamma"], d["beta"])
+    L = gn.lib()
+    assert L.gn3d_stream_status(st) == gn.ERR_TIMEOUT
+    assert L.gn3d_stream_status(st) == gn.OK
+    gn.gn3d_debug_set(gn.DEBUG_SPIN_LIMIT, 0)
+    assert same(ref, run_all(site, d))
