@@ -198,7 +198,7 @@ def time_device(vols, steps, warmup, flush, stream, kernel_timing=False):
                 v.bwd(st)
         stream.synchronize()
         if kernel_timing:
-            gn.gn3d_debug_set(gn.DEBUG_TIMING, 1)
+            gn.gn3d_timing(True)
         evs = []
         for _ in range(steps):
             flush.fill_(1)
@@ -217,7 +217,7 @@ def time_device(vols, steps, warmup, flush, stream, kernel_timing=False):
                 ms, n = gn.gn3d_kernel_time(name)
                 if n:
                     kernels[name] = {"launches": n, "ms_per_launch": ms / n}
-            gn.gn3d_debug_set(gn.DEBUG_TIMING, 0)
+            gn.gn3d_timing(False)
         tot, tf, tb = [], [], []
         for ev in evs:
             tot.append(ev[0].elapsed_time(ev[-1]))
@@ -231,7 +231,7 @@ def time_device(vols, steps, warmup, flush, stream, kernel_timing=False):
 # Algorithmic HBM bytes per launch of each kernel, in tensors of the volume's
 # size: what it must read and write at least (re-reads from L2 are not counted).
 KERNEL_TENSORS = {"k_fwd_fused": 2, "k_fwd_stats": 1, "k_fwd_norm": 2,
-                  "k_bwd_fused": 3, "k_bwd_reduce": 2, "k_bwd_dx": 3,
+                  "k_bwd_fused": 3, "k_bwd_reduce": 2, "k_bwd_dx": 3, "k_fwd_resident": 2, "k_bwd_resident": 3,
                   "k_ndhwc_stats": 1, "k_ndhwc_stats_final": 0, "k_ndhwc_norm": 2,
                   "k_ndhwc_reduce": 2, "k_ndhwc_reduce_final": 0, "k_ndhwc_dx": 3}
 
@@ -494,7 +494,9 @@ def run_gpu(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     build.build()
-    gn.gn3d_debug_set(gn.DEBUG_PATH, {"auto": 0, "streaming": 1, "fused": 2}[args.path])
+    if args.path != "auto":  # another launch form: the testing build's hook (an experiment, not the product)
+        gn.use_library("testing")
+        gn.gn3d_debug_set(gn.DEBUG_PATH, {"streaming": 1, "fused": 2, "resident": 3}[args.path])
     site = synth.WORKLOADS[args.workload].sites[0]
     vol = Volume(site, dev, pinned=True, layout=args.layout)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -631,7 +633,7 @@ def main():
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--layout", choices=["ncdhw", "ndhwc"], default="ncdhw",
                     help="storage of the timed volume: NCDHW (default) or channels-last NDHWC")
-    ap.add_argument("--path", default="auto", choices=["auto", "streaming", "fused"],
+    ap.add_argument("--path", default="auto", choices=["auto", "streaming", "fused", "resident"],
                     help="launch form (results are bit-identical; for A/B timing)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -24,7 +24,8 @@ OK, ERR_INVALID_ARG, ERR_DEVICE, ERR_CUDA, ERR_TIMEOUT = 0, 1, 2, 3, 4
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _lock = threading.Lock()
-_lib = None
+_libs = {}
+_current = "product"
 
 
 class GN3DError(RuntimeError):
@@ -33,18 +34,34 @@ class GN3DError(RuntimeError):
         self.status = status
 
 
-def library_path() -> str:
+def library_path(kind: str = "product") -> str:
+    """The in-tree build of libgn3d: "product" (the shipped library) or "testing"
+    (the same sources compiled with the testing and tuning hooks)."""
     from . import build as _b
 
-    return _b.LIB
+    return {"product": _b.LIB, "testing": _b.TESTING_LIB}[kind]
+
+
+def use_library(kind: str) -> str:
+    """Route every call of this module to the product or the testing build;
+    returns the previous choice.  The tests that set debug hooks run all their
+    calls on the testing build (each library keeps its own settings)."""
+    global _current
+    if kind not in ("product", "testing"):
+        raise ValueError("library kind: 'product' or 'testing'")
+    prev, _current = _current, kind
+    return prev
 
 
 def lib():
-    """Load libgn3d (built in-tree by ``bwd_gn3d_stats_gb300.build``)."""
-    global _lib
+    """The library calls go to (the product build unless use_library('testing'))."""
+    return _load(_current)
+
+
+def _load(kind: str):
     with _lock:
-        if _lib is None:
-            path = library_path()
+        if kind not in _libs:
+            path = library_path(kind)
             if not os.path.exists(path):
                 raise RuntimeError(f"libgn3d is not built ({path} missing): run "
                                    "python -m bwd_gn3d_stats_gb300.build")
@@ -59,7 +76,7 @@ def lib():
             L.gn3d_backward_relu.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, ci, vp, vp, vp,
                                              vp]
             L.gn3d_backward_relu.restype = ci
-            for name in ("gn3d_forward_ndhwc", "gn3d_forward_ndhwc_relu"):
+            for name in ("gn3d_forward_ndhwc", "gn3d_forward_ndhwc_relu", "gn3d_forward_noalloc"):
                 getattr(L, name).argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, dbl, ci, ci, vp, vp, vp, vp]
                 getattr(L, name).restype = ci
             L.gn3d_backward_ndhwc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, ci, vp, vp, vp, vp]
@@ -75,8 +92,18 @@ def lib():
             L.gn3d_launch_count.restype = ctypes.c_uint64
             L.gn3d_version.argtypes = []
             L.gn3d_version.restype = ctypes.c_char_p
-            _lib = L
-    return _lib
+            L.gn3d_timing.argtypes = [ci]
+            L.gn3d_timing.restype = ci
+            L.gn3d_kernel_time.argtypes = [ctypes.c_char_p, ctypes.POINTER(ctypes.c_double),
+                                           ctypes.POINTER(ctypes.c_uint64)]
+            L.gn3d_kernel_time.restype = ci
+            if kind == "testing":
+                L.gn3d_debug_set.argtypes = [ci, ctypes.c_longlong]
+                L.gn3d_debug_set.restype = ci
+                L.gn3d_debug_get.argtypes = [ci, ctypes.POINTER(ctypes.c_longlong)]
+                L.gn3d_debug_get.restype = ci
+            _libs[kind] = L
+    return _libs[kind]
 
 
 def _check(status: int):
@@ -263,17 +290,31 @@ def backward(dy, x, mean, rstd, gamma, G: int, out=None):
 
 
 # ------------------------------------------------------------ testing hooks
+# Present in the testing build only (use_library("testing")).
 
-(DEBUG_PATH, DEBUG_SPIN_LIMIT, DEBUG_FORCE_TIMEOUT, DEBUG_LAG, DEBUG_SLOTS, DEBUG_TIMING, DEBUG_SHARES,
- DEBUG_RES_HELD, DEBUG_RES_WINDOW, DEBUG_RES_PASS) = range(10)
+(DEBUG_PATH, DEBUG_SPIN_LIMIT, DEBUG_FORCE_TIMEOUT, DEBUG_LAG, DEBUG_SLOTS) = range(5)
+(DEBUG_SHARES, DEBUG_RES_HELD, DEBUG_RES_WINDOW, DEBUG_RES_PASS, DEBUG_FAIL_NEXT) = range(6, 11)
 PATH_AUTO, PATH_STREAMING, PATH_FUSED, PATH_RESIDENT = 0, 1, 2, 3
+FAIL_NONE, FAIL_ALLOC, FAIL_LAUNCH = 0, 1, 2
+DEBUG_POOL_USED = 0
+
+
+def _testing():
+    if _current != "testing":
+        raise RuntimeError("the debug settings exist in the testing build only: call use_library('testing') first")
+    return lib()
 
 
 def gn3d_debug_set(what: int, value: int):
-    L = lib()
-    L.gn3d_debug_set.argtypes = [ctypes.c_int, ctypes.c_longlong]
-    L.gn3d_debug_set.restype = ctypes.c_int
+    L = _testing()
     _check(L.gn3d_debug_set(what, value))
+
+
+def gn3d_debug_get(what: int) -> int:
+    L = _testing()
+    v = ctypes.c_longlong(0)
+    _check(L.gn3d_debug_get(what, ctypes.byref(v)))
+    return int(v.value)
 
 
 KERNELS = ("k_fwd_fused", "k_bwd_fused", "k_fwd_stats", "k_fwd_norm", "k_bwd_reduce", "k_bwd_dx",
@@ -281,22 +322,20 @@ KERNELS = ("k_fwd_fused", "k_bwd_fused", "k_fwd_stats", "k_fwd_norm", "k_bwd_red
            "k_ndhwc_dx", "k_fwd_resident", "k_bwd_resident")
 
 
+def gn3d_timing(on: bool):
+    """Start (clearing earlier records) or stop per-kernel timing (C entry point gn3d_timing)."""
+    _check(lib().gn3d_timing(1 if on else 0))
+
+
 def gn3d_kernel_time(name: str):
-    """(total milliseconds, launches) of one kernel since timing was switched on
-    with gn3d_debug_set(DEBUG_TIMING, 1) (C entry point gn3d_kernel_time)."""
-    L = lib()
-    L.gn3d_kernel_time.argtypes = [ctypes.c_char_p, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_uint64)]
-    L.gn3d_kernel_time.restype = ctypes.c_int
+    """(total milliseconds, launches) of one kernel since gn3d_timing(True)
+    (C entry point gn3d_kernel_time)."""
     ms, n = ctypes.c_double(0.0), ctypes.c_uint64(0)
-    _check(L.gn3d_kernel_time(name.encode(), ctypes.byref(ms), ctypes.byref(n)))
+    _check(lib().gn3d_kernel_time(name.encode(), ctypes.byref(ms), ctypes.byref(n)))
     return ms.value, n.value
 
 
 def gn3d_forward_noalloc(x, gamma, beta, N, C, D, H, W, G, eps, in_dtype, out_dtype, y, mean, rstd, stream):
     """The allocation-free forward (C entry point gn3d_forward_noalloc)."""
-    L = lib()
-    i64, vp, dbl, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_double, ctypes.c_int
-    L.gn3d_forward_noalloc.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, dbl, ci, ci, vp, vp, vp, vp]
-    L.gn3d_forward_noalloc.restype = ci
-    _check(L.gn3d_forward_noalloc(x, gamma, beta, N, C, D, H, W, G, eps, in_dtype, out_dtype, y, mean, rstd,
-                                  stream))
+    _check(lib().gn3d_forward_noalloc(x, gamma, beta, N, C, D, H, W, G, eps, in_dtype, out_dtype, y, mean, rstd,
+                                      stream))

@@ -44,6 +44,9 @@ std::atomic<int> g_hook_shares{-1};        // -1 auto, 0 strided blocks, 1 unit 
 std::atomic<long long> g_hook_rheld{-1};   // -1 auto: held units per share of the group-wave kernels
 std::atomic<long long> g_hook_window{-1};  // -1 auto: the group-wave producer's lead, in units
 std::atomic<long long> g_hook_rpass{-1};   // -1 auto: pass-ring slots of the group-wave kernels
+#ifdef GN3D_TESTING
+std::atomic<int> g_inject{0};              // 1: the next scratch allocation fails, 2: the next launch
+#endif
 
 constexpr unsigned long long kDefaultSpin = 1ull << 26;  // ~4 s of polls at 64 ns sleeps
 
@@ -66,24 +69,29 @@ int arg_fail(const char* what) {
 // Per-device facts and objects, created once.
 struct DevInfo {
   bool ready = false;
+  int dev = 0;
   int sms = 0;
   int l2_bytes = 0;
   int smem_optin = 0;
   int smem_per_sm = 0;
   cudaMemPool_t pool = nullptr;
   uint32_t* status = nullptr;
-  std::vector<std::pair<const void*, int>> attr_smem;  // dynamic shared memory raised to, per kernel
   std::vector<cudaEvent_t> free_events;                // timing events of this device, for reuse
 };
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 DevInfo g_dev[kMaxDevices];
+// The dynamic shared memory each kernel's attribute was raised to, per device:
+// one table for every launch path, so no path can believe an attribute is
+// higher than another path left it.
+std::vector<std::pair<const void*, int>> g_attr_smem[kMaxDevices];
 
 int device_info(int dev, DevInfo** out) {
   if (dev < 0 || dev >= kMaxDevices) return arg_fail("device ordinal out of range");
   std::lock_guard<std::mutex> lk(g_mu);
   DevInfo& d = g_dev[dev];
   if (!d.ready) {
+    d.dev = dev;
     GN3D_CUDA(cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev), "device attribute");
     GN3D_CUDA(cudaDeviceGetAttribute(&d.l2_bytes, cudaDevAttrL2CacheSize, dev), "device attribute");
     GN3D_CUDA(cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev),
@@ -149,6 +157,27 @@ bool unit_shares(const Plan& p, int64_t nw) {
   return h < 0 ? use_unit_shares(p, nw) : h == 1;
 }
 
+// The per-call scratch allocation, stream-ordered from the library's pool.  In
+// the testing build an armed injection (GN3D_DEBUG_FAIL_NEXT) makes it fail as
+// an out-of-memory would, to exercise the callers' error paths.
+cudaError_t scratch_alloc(void** p, int64_t bytes, const DevInfo& di, cudaStream_t st) {
+#ifdef GN3D_TESTING
+  int armed = 1;
+  if (g_inject.compare_exchange_strong(armed, 0)) return cudaErrorMemoryAllocation;
+#endif
+  return cudaMallocFromPoolAsync(p, (size_t)bytes, di.pool, st);
+}
+
+// Called before a call's first kernel launch: cudaSuccess, or (testing build,
+// injection armed) the error a failed launch returns.
+cudaError_t injected_launch_error() {
+#ifdef GN3D_TESTING
+  int armed = 2;
+  if (g_inject.compare_exchange_strong(armed, 0)) return cudaErrorLaunchFailure;
+#endif
+  return cudaSuccess;
+}
+
 // Scratch carved out of one stream-ordered allocation, 256-byte aligned pieces.
 struct Scratch {
   void* base = nullptr;
@@ -164,7 +193,7 @@ struct Scratch {
 int64_t rup(int64_t b) { return ((b + 255) / 256) * 256; }
 
 // ------------------------------------------------------------ kernel timing
-// While timing is on (GN3D_DEBUG_TIMING), each kernel launch is bracketed by two
+// While timing is on (gn3d_timing), each kernel launch is bracketed by two
 // CUDA events on its stream; gn3d_kernel_time resolves them per kernel.
 enum {
   KK_FWD_FUSED, KK_BWD_FUSED, KK_FWD_STATS, KK_FWD_NORM, KK_BWD_REDUCE, KK_BWD_DX,
@@ -304,9 +333,12 @@ FusedCfg fused_cfg(const DevInfo& di, int slot_bytes, int rec_bytes, int64_t gro
   return c;
 }
 
-int raise_smem(const void* func, int bytes, DevInfo& di) {
+// Raise a kernel's dynamic shared memory limit to at least `bytes` on the
+// device (the limit only ever goes up, so a smaller launch never lowers it
+// under a larger one).
+int raise_smem(const void* func, int bytes, const DevInfo& di) {
   std::lock_guard<std::mutex> lk(g_mu);
-  for (auto& e : di.attr_smem) {
+  for (auto& e : g_attr_smem[di.dev]) {
     if (e.first != func) continue;
     if (e.second < bytes) {
       GN3D_CUDA(cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes),
@@ -316,7 +348,7 @@ int raise_smem(const void* func, int bytes, DevInfo& di) {
     return GN3D_OK;
   }
   GN3D_CUDA(cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes), "cudaFuncSetAttribute");
-  di.attr_smem.emplace_back(func, bytes);
+  g_attr_smem[di.dev].emplace_back(func, bytes);
   return GN3D_OK;
 }
 
@@ -372,7 +404,7 @@ int launch_forward(const void* x, const float* gamma, const float* beta, const P
   const int64_t bytes = rup(nsync * 4) + rup(p.units * (int64_t)sizeof(Part)) +
                         rup(nblk * (int64_t)sizeof(Part)) + rup(p.NG * (int64_t)sizeof(float4));
   Scratch s;
-  GN3D_CUDA(cudaMallocFromPoolAsync(&s.base, (size_t)bytes, di.pool, st), "scratch allocation");
+  GN3D_CUDA(scratch_alloc(&s.base, bytes, di, st), "scratch allocation");
   s.cur = static_cast<char*>(s.base);
   uint32_t* sync = s.take<uint32_t>(nsync);
   FwdWs w;
@@ -384,6 +416,7 @@ int launch_forward(const void* x, const float* gamma, const float* beta, const P
   w.stats = s.take<float4>(p.NG);
   FusedSync fs{sync + nblk + 2 * p.NG, sync + nblk + 2 * p.NG + 1, di.status};
   cudaError_t e = cudaMemsetAsync(sync, 0, (size_t)nsync * sizeof(uint32_t), st);
+  if (e == cudaSuccess) e = injected_launch_error();
   const TI* xp = static_cast<const TI*>(x);
   TO* yp = static_cast<TO*>(y);
   if (e == cudaSuccess && use_resident(p, di)) {
@@ -495,7 +528,7 @@ int launch_backward(const void* dy, const void* x, const void* res, const float*
                         rup(nblk * (int64_t)sizeof(float2)) + rup(p.NC * (int64_t)sizeof(float2)) +
                         rup(p.NG * (int64_t)sizeof(float2));
   Scratch s;
-  GN3D_CUDA(cudaMallocFromPoolAsync(&s.base, (size_t)bytes, di.pool, st), "scratch allocation");
+  GN3D_CUDA(scratch_alloc(&s.base, bytes, di, st), "scratch allocation");
   s.cur = static_cast<char*>(s.base);
   uint32_t* sync = s.take<uint32_t>(nsync);
   BwdWs w;
@@ -509,6 +542,7 @@ int launch_backward(const void* dy, const void* x, const void* res, const float*
   w.coef = s.take<float2>(p.NG);
   FusedSync fs{sync + nblk + 2 * p.NG + 1, sync + nblk + 2 * p.NG + 2, di.status};
   cudaError_t e = cudaMemsetAsync(sync, 0, (size_t)nsync * sizeof(uint32_t), st);
+  if (e == cudaSuccess) e = injected_launch_error();
   const T* dyp = static_cast<const T*>(dy);
   const T* xp = static_cast<const T*>(x);
   T* dxp = static_cast<T*>(dx);
@@ -573,7 +607,7 @@ int launch_forward_ndhwc(const void* x, const float* gamma, const float* beta, c
   const int64_t bytes = rup((p.NG + 1) * 4) + rup(p.rows * p.P * p.R * (int64_t)sizeof(Part)) +
                         rup(tasks * (int64_t)sizeof(Part)) + rup(p.NG * (int64_t)sizeof(float4));
   Scratch s;
-  GN3D_CUDA(cudaMallocFromPoolAsync(&s.base, (size_t)bytes, di.pool, st), "scratch allocation");
+  GN3D_CUDA(scratch_alloc(&s.base, bytes, di, st), "scratch allocation");
   s.cur = static_cast<char*>(s.base);
   NFwdWs w;
   w.gcnt = s.take<uint32_t>(p.NG + 1);
@@ -592,6 +626,7 @@ int launch_forward_ndhwc(const void* x, const float* gamma, const float* beta, c
   if (rc) { cudaFreeAsync(s.base, st); return rc; }
   const int grid = grid_for(di, p.units, 1);
   cudaError_t e = cudaMemsetAsync(w.gcnt, 0, (size_t)(p.NG + 1) * sizeof(uint32_t), st);
+  if (e == cudaSuccess) e = injected_launch_error();
   if (e == cudaSuccess) {
     g_launches += 3;
     LaunchTimer t1(KK_N_STATS, st, di);
@@ -630,7 +665,7 @@ int launch_backward_ndhwc(const void* dy, const void* x, const void* res, const 
                         rup(tasks * (int64_t)sizeof(float2)) + rup(NC * (int64_t)sizeof(float2)) +
                         rup(p.NG * (int64_t)sizeof(float2));
   Scratch s;
-  GN3D_CUDA(cudaMallocFromPoolAsync(&s.base, (size_t)bytes, di.pool, st), "scratch allocation");
+  GN3D_CUDA(scratch_alloc(&s.base, bytes, di, st), "scratch allocation");
   s.cur = static_cast<char*>(s.base);
   NBwdWs w;
   uint32_t* sync = s.take<uint32_t>(nsync);
@@ -641,6 +676,7 @@ int launch_backward_ndhwc(const void* dy, const void* x, const void* res, const 
   w.rows = s.take<float2>(NC);
   w.coef = s.take<float2>(p.NG);
   cudaError_t e = cudaMemsetAsync(sync, 0, (size_t)nsync * sizeof(uint32_t), st);
+  if (e == cudaSuccess) e = injected_launch_error();
   const T* dyp = static_cast<const T*>(dy);
   const T* xp = static_cast<const T*>(x);
   const T* resp = static_cast<const T*>(res);
@@ -704,7 +740,6 @@ struct NoAllocDev {
   unsigned char* scratch = nullptr;  // device address of g_noalloc_scratch
   uint32_t* status = nullptr;        // device address of the status word
   DevInfo facts;                     // SM count, L2 and shared-memory sizes (no pool)
-  int attr_smem[4] = {0, 0, 0, 0};
 };
 NoAllocDev g_noalloc[kMaxDevices];
 
@@ -713,6 +748,7 @@ int noalloc_setup(int dev, NoAllocDev** out) {
   std::lock_guard<std::mutex> lk(g_mu);
   NoAllocDev& d = g_noalloc[dev];
   if (!d.ready) {
+    d.facts.dev = dev;
     GN3D_CUDA(cudaDeviceGetAttribute(&d.facts.sms, cudaDevAttrMultiProcessorCount, dev), "device attribute");
     GN3D_CUDA(cudaDeviceGetAttribute(&d.facts.l2_bytes, cudaDevAttrL2CacheSize, dev), "device attribute");
     GN3D_CUDA(cudaDeviceGetAttribute(&d.facts.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev),
@@ -760,18 +796,11 @@ int launch_forward_noalloc(const void* x, const float* gamma, const float* beta,
   FusedCfg cfg = fused_cfg(nd.facts, slot, rec, p.M * (int64_t)sizeof(TI));
   const int smem = cfg.slots * (slot + 16) + cfg.recs * rec;
   auto k = k_fwd_fused<TI, TO>;
-  const int which = (sizeof(TI) == 2 ? 0 : 2) + (sizeof(TO) == 2 ? 0 : 1);
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (nd.attr_smem[which] < smem) {
-      GN3D_CUDA(cudaFuncSetAttribute((const void*)k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem),
-                "cudaFuncSetAttribute");
-      nd.attr_smem[which] = smem;
-    }
-  }
+  int rc = raise_smem((const void*)k, smem, nd.facts);
+  if (rc) return rc;
   const int threads = 32 * (FwdPolicy<TI>::kWarps + 1);
   int grid = 0;
-  int rc = coop_grid((const void*)k, threads, smem, nd.facts, &grid);
+  rc = coop_grid((const void*)k, threads, smem, nd.facts, &grid);
   if (rc) return rc;
   const TI* xp = static_cast<const TI*>(x);
   TO* yp = static_cast<TO*>(y);
@@ -1008,6 +1037,7 @@ extern "C" int gn3d_stream_status(void* stream) {
   return GN3D_OK;
 }
 
+#ifdef GN3D_TESTING
 extern "C" int gn3d_debug_set(int what, long long value) {
   switch (what) {
     case GN3D_DEBUG_PATH:
@@ -1029,23 +1059,10 @@ extern "C" int gn3d_debug_set(int what, long long value) {
       if (value < -1 || value == 0 || value > 32) return arg_fail("slots: -1, 1 .. 32");
       g_hook_slots = value;
       break;
-    case GN3D_DEBUG_TIMING: {
-      if (value != 0 && value != 1) return arg_fail("timing: 0 or 1");
-      std::lock_guard<std::mutex> lk(g_tmu);
-      if (value) {
-        for (TimedLaunch& t : g_timed) {
-          t.dev->free_events.push_back(t.a);
-          t.dev->free_events.push_back(t.b);
-        }
-        g_timed.clear();
-        for (int k = 0; k < KK_COUNT; ++k) {
-          g_kernel_ms[k] = 0.0;
-          g_kernel_n[k] = 0;
-        }
-      }
-      g_timing = (int)value;
+    case GN3D_DEBUG_FAIL_NEXT:
+      if (value < 0 || value > 2) return arg_fail("fail next: 0 none, 1 allocation, 2 launch");
+      g_inject = (int)value;
       break;
-    }
     case GN3D_DEBUG_SHARES:
       if (value < -1 || value > 1) return arg_fail("shares: -1, 0 or 1");
       g_hook_shares = (int)value;
@@ -1065,6 +1082,44 @@ extern "C" int gn3d_debug_set(int what, long long value) {
     default:
       return arg_fail("unknown debug setting");
   }
+  return GN3D_OK;
+}
+
+extern "C" int gn3d_debug_get(int what, long long* value) {
+  if (!value) return arg_fail("gn3d_debug_get: NULL value");
+  switch (what) {
+    case GN3D_DEBUG_POOL_USED: {
+      int dev = 0;
+      GN3D_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+      DevInfo* di = nullptr;
+      int rc = device_info(dev, &di);
+      if (rc) return rc;
+      unsigned long long used = 0;  // the attribute is a 64-bit count
+      GN3D_CUDA(cudaMemPoolGetAttribute(di->pool, cudaMemPoolAttrUsedMemCurrent, &used), "pool attribute");
+      *value = (long long)used;
+      return GN3D_OK;
+    }
+    default:
+      return arg_fail("unknown debug query");
+  }
+}
+#endif  // GN3D_TESTING
+
+extern "C" int gn3d_timing(int on) {
+  if (on != 0 && on != 1) return arg_fail("gn3d_timing: 0 or 1");
+  std::lock_guard<std::mutex> lk(g_tmu);
+  if (on) {
+    for (TimedLaunch& t : g_timed) {
+      t.dev->free_events.push_back(t.a);
+      t.dev->free_events.push_back(t.b);
+    }
+    g_timed.clear();
+    for (int k = 0; k < KK_COUNT; ++k) {
+      g_kernel_ms[k] = 0.0;
+      g_kernel_n[k] = 0;
+    }
+  }
+  g_timing = on;
   return GN3D_OK;
 }
 

@@ -214,10 +214,13 @@ const char* gn3d_error_string(int status);
  * region).  Memory-set and copy operations are not counted. */
 uint64_t gn3d_launch_count(void);
 
+#ifdef GN3D_TESTING
 /*
- * Testing and tuning hooks (process-wide, not thread-scoped; not needed for
- * normal use -- every setting defaults to automatic).  None of them changes a
- * result bit: both launch forms run the same units and reduction trees.
+ * Testing and tuning hooks, present only in the testing build of the library
+ * (compiled with GN3D_TESTING; the tests load it, the shipped library has none
+ * of them).  Process-wide, not thread-scoped; every setting defaults to
+ * automatic.  None of them changes a result bit: every launch form runs the
+ * same units and reduction trees.
  *   GN3D_DEBUG_PATH          0 automatic (the streaming kernels: two launches
  *                            per direction), 1 streaming, 2 persistent (one
  *                            cooperative launch per direction), 3 group-wave
@@ -242,9 +245,6 @@ uint64_t gn3d_launch_count(void);
  *                            between the statistics pass and the elementwise pass.
  *   GN3D_DEBUG_SLOTS         -1 automatic, else the number of shared-memory
  *                            slots of the persistent kernels (at most what fits).
- *   GN3D_DEBUG_TIMING        1 clears the per-kernel times and starts recording
- *                            them: every kernel launch is bracketed by two CUDA
- *                            events on its stream (see gn3d_kernel_time); 0 stops.
  *   GN3D_DEBUG_SHARES        -1 automatic, 0 strided blocks, 1 unit shares:
  *                            how the NCDHW streaming kernels split the units
  *                            among their warps (whole merge blocks dealt out in
@@ -259,6 +259,12 @@ uint64_t gn3d_launch_count(void);
  *   GN3D_DEBUG_RES_PASS      -1 automatic, else >= 1: slots of the group-wave
  *                            kernels' pass ring (rounded up to a multiple of
  *                            their reduction warps).
+ *   GN3D_DEBUG_FAIL_NEXT     1: the next per-call scratch allocation fails as an
+ *                            out-of-memory would; 2: the next call's first
+ *                            kernel launch fails; 0 disarms.  The call returns
+ *                            GN3D_ERR_CUDA having enqueued no kernel and freed
+ *                            its scratch (a host-side fault injection: nothing
+ *                            faults on the GPU).
  * Returns GN3D_OK or GN3D_ERR_INVALID_ARG for an unknown setting or value.
  */
 enum {
@@ -267,17 +273,32 @@ enum {
   GN3D_DEBUG_FORCE_TIMEOUT = 2,
   GN3D_DEBUG_LAG = 3,
   GN3D_DEBUG_SLOTS = 4,
-  GN3D_DEBUG_TIMING = 5,
   GN3D_DEBUG_SHARES = 6,
   GN3D_DEBUG_RES_HELD = 7,
   GN3D_DEBUG_RES_WINDOW = 8,
-  GN3D_DEBUG_RES_PASS = 9
+  GN3D_DEBUG_RES_PASS = 9,
+  GN3D_DEBUG_FAIL_NEXT = 10
 };
 int gn3d_debug_set(int what, long long value);
 
+/* Testing build: GN3D_DEBUG_POOL_USED writes the bytes currently allocated from
+ * the current device's scratch pool (0 once every call's scratch is freed and
+ * the stream has reached the frees).  GN3D_OK or GN3D_ERR_INVALID_ARG. */
+enum { GN3D_DEBUG_POOL_USED = 0 };
+int gn3d_debug_get(int what, long long* value);
+#endif /* GN3D_TESTING */
+
+/*
+ * Per-kernel timing (diagnostics): gn3d_timing(1) clears the recorded times
+ * and starts recording -- every kernel launch is then bracketed by two CUDA
+ * events on its stream (see gn3d_kernel_time); gn3d_timing(0) stops.  Returns
+ * GN3D_OK or GN3D_ERR_INVALID_ARG (value other than 0 or 1).
+ */
+int gn3d_timing(int on);
+
 /*
  * Device time of one kernel, summed over the launches recorded since
- * GN3D_DEBUG_TIMING was last set to 1.  `name` is one of "k_fwd_fused",
+ * gn3d_timing(1) was last called.  `name` is one of "k_fwd_fused",
  * "k_bwd_fused", "k_fwd_stats", "k_fwd_norm", "k_bwd_reduce", "k_bwd_dx",
  * "k_ndhwc_stats", "k_ndhwc_stats_final", "k_ndhwc_norm", "k_ndhwc_reduce",
  * "k_ndhwc_reduce_final", "k_ndhwc_dx", "k_fwd_resident", "k_bwd_resident".

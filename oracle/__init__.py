@@ -12,6 +12,11 @@ Functions (all cite the ScaFFold pages' GroupNorm definition; see the C file):
   forward_at(..., mean, rstd, idx)             -> y64 at flat indices
   backward(dy, x, dtype, mean, rstd, gamma, N, C, S, G) -> dx64, dgamma, dbeta
   backward_at(..., idx)                        -> dx64 at indices, dgamma, dbeta
+  backward_sums(dy, x, mean, rstd, gamma, N, C, S, G, out=None)
+                                               -> a, b (per group), s1 = sum dy, s2 = sum dy*xhat (per row)
+  backward_relu / backward_relu_at             -> the backward behind the fused ReLU (out: its result)
+  moments(x, N, C, S, G) / combine_moments(list) -> sharded statistics: per-shard (count, mean, M2),
+                                               combined in rank order (Chan's parallel formula)
   round_bf16(v64) -> uint16 bit patterns (RNE straight from fp64)
   round_f32(v64)  -> float32 (RNE)
 Channels-last (NDHWC) tensors: the same GroupNorm of the same logical tensor,
@@ -79,12 +84,14 @@ def _load():
                                                       dp, dp, dp]
             lib.gn3d_oracle_backward_relu_at.argtypes = [vp, vp, vp, ctypes.c_int, dp, dp, fp, i64, i64, i64,
                                                          i64, vp, i64, dp, dp, dp]
+            lib.gn3d_oracle_backward_sums.argtypes = [vp, vp, vp, ctypes.c_int, dp, dp, fp, i64, i64, i64, i64,
+                                                      dp, dp, dp, dp]
             lib.gn3d_oracle_relu.argtypes = [dp, i64, dp]
             lib.gn3d_oracle_relu.restype = None
             lib.gn3d_oracle_round_bf16.argtypes = [dp, i64, vp]
             lib.gn3d_oracle_round_f32.argtypes = [dp, i64, fp]
             for f in ("stats", "forward", "forward_at", "backward", "backward_at", "backward_relu",
-                      "backward_relu_at"):
+                      "backward_relu_at", "backward_sums"):
                 getattr(lib, "gn3d_oracle_" + f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -170,6 +177,67 @@ def backward_at(dy, x, mean, rstd, gamma, N, C, S, G, idx):
                                            N, C, S, G, _ptr(idx), idx.size, _ptr(dx), _ptr(dgamma),
                                            _ptr(dbeta)))
     return dx, dgamma, dbeta
+
+
+def backward_sums(dy, x, mean, rstd, gamma, N, C, S, G, out=None):
+    """The backward's sums at given statistics: a = mean(dy*gamma), b =
+    mean(dy*gamma*xhat) per group [N*G]; s1 = sum dy, s2 = sum dy*xhat per row
+    (n, c) [N*C].  With `out` (the fused ReLU forward's result), dy is zeroed
+    where out <= 0 first."""
+    xr, dt = _raw(x)
+    dyr, dt2 = _raw(dy)
+    outr = None
+    if out is not None:
+        outr, dt3 = _raw(out)
+        if dt3 != dt:
+            raise TypeError("out must share x's dtype")
+    if dt != dt2:
+        raise TypeError("dy and x must share a dtype")
+    g = _params(gamma)
+    mean = np.ascontiguousarray(mean, dtype=np.float64)
+    rstd = np.ascontiguousarray(rstd, dtype=np.float64)
+    a, b = np.empty(N * G), np.empty(N * G)
+    s1, s2 = np.empty(N * C), np.empty(N * C)
+    _check(_load().gn3d_oracle_backward_sums(_ptr(dyr), _ptr(outr), _ptr(xr), dt, _ptr(mean), _ptr(rstd), _ptr(g),
+                                             N, C, S, G, _ptr(a), _ptr(b), _ptr(s1), _ptr(s2)))
+    return a, b, s1, s2
+
+
+# ------------------------------------------------------- sharded statistics
+# A volume cut into K shards along D (each rank's slab, its own contiguous
+# [N, C, D_k, H, W] tensor) has per-shard moments (count, mean, M2) per group;
+# the global statistics are those moments combined in rank order with the
+# parallel-variance formula of Chan, Golub and LeVeque, which the ScaFFold
+# GroupNorm pages name for merging partial statistics.
+
+def moments(x, N, C, S, G):
+    """Per group (n, g) of this tensor: count, mean and M2 = sum (x - mean)^2,
+    fp64 (the definition: two compensated passes, as stats())."""
+    mean, var, _ = stats(x, N, C, S, G, 0.0)
+    count = np.full(N * G, (C // G) * S, dtype=np.float64)
+    return count, mean, var * count
+
+
+def combine_moments(parts):
+    """Combine [(count, mean, M2), ...] (one per shard, rank order) pairwise left
+    to right: n = na + nb, d = mb - ma, mean = ma + d*nb/n, M2 = M2a + M2b +
+    d^2*na*nb/n.  Returns (count, mean, M2)."""
+    n, m, q = (np.array(v, dtype=np.float64) for v in parts[0])
+    for nb, mb, qb in parts[1:]:
+        nb, mb, qb = (np.asarray(v, dtype=np.float64) for v in (nb, mb, qb))
+        tot = n + nb
+        safe = np.where(tot > 0, tot, 1.0)
+        d = mb - m
+        m = np.where(tot > 0, m + d * nb / safe, 0.0)
+        q = q + qb + np.where(tot > 0, d * d * n * nb / safe, 0.0)
+        n = tot
+    return n, m, q
+
+
+def rstd_of(count, M2, eps):
+    """rstd = 1/sqrt(M2/count + eps), eps used at its fp32 value (as the library does)."""
+    var = np.where(count > 0, M2 / np.where(count > 0, count, 1.0), 0.0)
+    return 1.0 / np.sqrt(var + float(np.float32(eps)))
 
 
 def relu(v):

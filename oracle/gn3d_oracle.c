@@ -313,6 +313,29 @@ int gn3d_oracle_backward_relu_at(const void* dy, const void* x, const void* out,
   return backward_at_impl(dy, out, x, dtype, mean, rstd, gamma, N, C, S, G, idx, k, dx, dgamma, dbeta);
 }
 
+/* The backward's sums at given statistics: per group a = mean(g), b =
+ * mean(g * xhat); per (n, c) row s1 = sum dy and s2 = sum dy * xhat (dbeta and
+ * dgamma before the sum over n).  `gate` (the fused ReLU forward's result, or
+ * NULL) zeroes dy where it is <= 0.  a, b: [N*G]; s1, s2: [N*C] (any may be NULL). */
+int gn3d_oracle_backward_sums(const void* dy, const void* gate, const void* x, int dtype, const double* mean,
+                              const double* rstd, const float* gamma, int64_t N, int64_t C, int64_t S, int64_t G,
+                              double* a, double* b, double* s1, double* s2) {
+  if (check_shape(N, C, S, G)) return ORC_EINVAL;
+  const int64_t NG = N * G, NC = N * C;
+  double* ta = (double*)malloc(sizeof(double) * (size_t)(NG + 1));
+  double* tb = (double*)malloc(sizeof(double) * (size_t)(NG + 1));
+  double* dg = (double*)malloc(sizeof(double) * (size_t)(NC + 1));
+  double* db = (double*)malloc(sizeof(double) * (size_t)(NC + 1));
+  if (!ta || !tb || !dg || !db) { free(ta); free(tb); free(dg); free(db); return ORC_EINVAL; }
+  bwd_sums(dy, gate, x, dtype, mean, rstd, gamma, N, C, S, G, ta, tb, dg, db);
+  if (a) memcpy(a, ta, sizeof(double) * (size_t)NG);
+  if (b) memcpy(b, tb, sizeof(double) * (size_t)NG);
+  if (s1) memcpy(s1, db, sizeof(double) * (size_t)NC);
+  if (s2) memcpy(s2, dg, sizeof(double) * (size_t)NC);
+  free(ta); free(tb); free(dg); free(db);
+  return ORC_OK;
+}
+
 /* ------------------------------------------------------------- fused ReLU */
 
 /* F.relu on values already rounded to the output type (widened to fp64):

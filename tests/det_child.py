@@ -13,12 +13,14 @@ def digests():
     import bwd_gn3d_stats_gb300 as gn
     from bwd_gn3d_stats_gb300 import synth
 
+    prev = gn.use_library("testing")  # the launch-form setting is a testing-build hook
     out = {}
     cases = [("ncdhw_stream", (1, 32, 24, 24, 24, 8, synth.BF16), gn.PATH_STREAMING, False),
              ("ncdhw_fused", (1, 32, 24, 24, 24, 8, synth.BF16), gn.PATH_FUSED, False),
              ("ncdhw_f32", (2, 16, 16, 16, 16, 4, synth.F32), gn.PATH_AUTO, False),
              ("ndhwc", (1, 48, 13, 11, 7, 8, synth.BF16), gn.PATH_AUTO, True),
-             ("ndhwc_512", (1, 512, 4, 4, 5, 8, synth.BF16), gn.PATH_AUTO, True)]
+             ("ndhwc_512", (1, 512, 4, 4, 5, 8, synth.BF16), gn.PATH_AUTO, True),
+             ("ncdhw_128", (1, 32, 128, 128, 128, 8, synth.BF16), gn.PATH_AUTO, False)]
     for name, shape, path, cl in cases:
         gn.gn3d_debug_set(gn.DEBUG_PATH, path)
         site = synth.Site(*shape)
@@ -42,6 +44,7 @@ def digests():
             h.update(t.detach().contiguous().cpu().view(torch.uint8).numpy().tobytes())
         out[name] = h.hexdigest()
     gn.gn3d_debug_set(gn.DEBUG_PATH, gn.PATH_AUTO)
+    gn.use_library(prev)
     return out
 
 

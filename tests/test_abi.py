@@ -33,21 +33,27 @@ def test_header_declares_entry_points():
 
 
 def test_library_exports_every_declared_symbol(L):
-    out = subprocess.run(["nm", "-D", "--defined-only", build.LIB], capture_output=True, text=True,
-                         check=True).stdout
-    exported = set(re.findall(r"\bT (gn3d_\w+)", out))
+    # the testing build exports everything the header declares (the hooks are
+    # declared under GN3D_TESTING); the shipped one everything but the hooks
+    testing = gn._load("testing")
+    exported = set(re.findall(r"\bT (gn3d_\w+)", subprocess.run(
+        ["nm", "-D", "--defined-only", build.TESTING_LIB], capture_output=True, text=True, check=True).stdout))
     missing = [n for n in declared_functions() if n not in exported]
     assert not missing, f"declared but not exported: {missing}"
     for n in declared_functions():
-        assert hasattr(L, n)
+        assert hasattr(testing, n)
+        if n not in ("gn3d_debug_set", "gn3d_debug_get"):
+            assert hasattr(L, n)
 
 
-def test_header_compiles_as_c(tmp_path):
+@pytest.mark.parametrize("testing", [False, True])
+def test_header_compiles_as_c(tmp_path, testing):
     src = tmp_path / "t.c"
     src.write_text('#include "gn3d.h"\nint (*f)(void*) = gn3d_stream_status;\n'
                    'int main(void){ return f == 0; }\n')
-    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), "-c", str(src),
-                    "-o", str(tmp_path / "t.o")], check=True)
+    flags = ["-DGN3D_TESTING"] if testing else []
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror"] + flags + ["-I", os.path.join(ROOT, "include"), "-c",
+                    str(src), "-o", str(tmp_path / "t.o")], check=True)
 
 
 def test_version(L):
@@ -182,43 +188,54 @@ def test_gpu_torch_level_wrappers():
     assert dx.dtype == torch.bfloat16 and dg.shape == (8,)
 
 
-def test_kernel_timing_hooks_without_launches(L):
+def test_kernel_timing_without_launches(L):
     # starting a timing window clears it; nothing launched -> zero time, zero launches
-    gn.gn3d_debug_set(gn.DEBUG_TIMING, 1)
+    gn.gn3d_timing(True)
     try:
         for name in gn.KERNELS:
             assert gn.gn3d_kernel_time(name) == (0.0, 0)
         with pytest.raises(gn.GN3DError):
             gn.gn3d_kernel_time("k_not_a_kernel")
-        with pytest.raises(gn.GN3DError):
-            gn.gn3d_debug_set(gn.DEBUG_TIMING, 2)
+        assert L.gn3d_timing(2) == gn.ERR_INVALID_ARG
     finally:
-        gn.gn3d_debug_set(gn.DEBUG_TIMING, 0)
+        gn.gn3d_timing(False)
 
 
-def test_debug_settings_ranges(L):
+def _exports(path):
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True, check=True).stdout
+    return set(re.findall(r"\bT (gn3d_\w+)", out))
+
+
+def test_shipped_library_carries_no_test_hooks(L):
+    """The testing and tuning hooks exist in the testing build only; the shipped
+    library exports the GroupNorm entry points and diagnostics."""
+    product, testing = _exports(build.LIB), _exports(build.TESTING_LIB)
+    assert "gn3d_debug_set" not in product and "gn3d_debug_get" not in product
+    assert {"gn3d_debug_set", "gn3d_debug_get"} <= testing
+    assert product == testing - {"gn3d_debug_set", "gn3d_debug_get"}
+    with pytest.raises(RuntimeError):
+        gn.gn3d_debug_set(gn.DEBUG_PATH, 0)  # the product build is the current one
+
+
+def test_debug_settings_ranges(testing_build):
     # every hook accepts its documented range and rejects the rest; none needs a GPU
     ok = {gn.DEBUG_PATH: (0, 1, 2, 3), gn.DEBUG_LAG: (-1, 0, 8), gn.DEBUG_SLOTS: (-1, 1, 32),
           gn.DEBUG_SHARES: (-1, 0, 1), gn.DEBUG_SPIN_LIMIT: (0, 1 << 20), gn.DEBUG_RES_HELD: (-1, 0, 7),
-          gn.DEBUG_RES_WINDOW: (-1, 1, 500), gn.DEBUG_RES_PASS: (-1, 1, 12)}
+          gn.DEBUG_RES_WINDOW: (-1, 1, 500), gn.DEBUG_RES_PASS: (-1, 1, 12), gn.DEBUG_FAIL_NEXT: (0, 1, 2)}
     bad = {gn.DEBUG_PATH: (-1, 4), gn.DEBUG_LAG: (-2, 9), gn.DEBUG_SLOTS: (0, -2, 33),
            gn.DEBUG_SHARES: (-2, 2), gn.DEBUG_SPIN_LIMIT: (-1,), gn.DEBUG_RES_HELD: (-2,),
-           gn.DEBUG_RES_WINDOW: (-2, 0), gn.DEBUG_RES_PASS: (-2, 0)}
-    default = {gn.DEBUG_PATH: 0, gn.DEBUG_LAG: -1, gn.DEBUG_SLOTS: -1, gn.DEBUG_SHARES: -1,
-               gn.DEBUG_SPIN_LIMIT: 0, gn.DEBUG_RES_HELD: -1, gn.DEBUG_RES_WINDOW: -1, gn.DEBUG_RES_PASS: -1}
-    try:
-        for what, values in ok.items():
-            for v in values:
-                gn.gn3d_debug_set(what, v)
-        for what, values in bad.items():
-            for v in values:
-                with pytest.raises(gn.GN3DError):
-                    gn.gn3d_debug_set(what, v)
-        with pytest.raises(gn.GN3DError):
-            gn.gn3d_debug_set(99, 0)
-    finally:
-        for what, v in default.items():
+           gn.DEBUG_RES_WINDOW: (-2, 0), gn.DEBUG_RES_PASS: (-2, 0), gn.DEBUG_FAIL_NEXT: (-1, 3)}
+    for what, values in ok.items():
+        for v in values:
             gn.gn3d_debug_set(what, v)
+    for what, values in bad.items():
+        for v in values:
+            with pytest.raises(gn.GN3DError):
+                gn.gn3d_debug_set(what, v)
+    with pytest.raises(gn.GN3DError):
+        gn.gn3d_debug_set(99, 0)
+    with pytest.raises(gn.GN3DError):
+        gn.gn3d_debug_get(7)
 
 
 @pytest.mark.gpu

@@ -215,13 +215,12 @@ def test_ndhwc_full_size_sampled(name):
     assert np.all(parity.check_reduction(to_np(dbeta).astype(np.float64), db64, l2))
 
 
-def test_ndhwc_bounded_wait_timeout_reports_and_recovers():
+def test_ndhwc_bounded_wait_timeout_reports_and_recovers(testing_build):
     """The channels-last statistics kernel's bounded wait: a forced wait on a
     word nothing sets gives up, the kernel drains its bulk copies and exits,
     gn3d_stream_status reports GN3D_ERR_TIMEOUT once, and the next calls are
     correct again."""
-    import bwd_gn3d_stats_gb300 as gn
-
+    gn = testing_build
     site = synth.Site(1, 32, 16, 16, 16, 8, synth.BF16)
     inp = synth.make_inputs(site, seed=18)
     ref = run_cl(site, inp)

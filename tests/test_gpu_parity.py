@@ -163,6 +163,20 @@ def test_determinism_and_dtype_independence():
     assert np.array_equal(to_np(dx32.to(t.bfloat16)), outs[0][3])
 
 
+@pytest.mark.parametrize("path", ["fused", "resident"])
+@pytest.mark.parametrize("shape", [(2, 16, 16, 16, 16, 4, synth.F32), (1, 8, 24, 24, 24, 2, synth.BF16),
+                                   (1, 32, 16, 16, 32, 8, synth.BF16), (2, 6, 1, 1, 1, 6, synth.BF16)],
+                         ids=lambda s: "x".join(map(str, s[:6])) + "_" + s[6])
+def test_parity_other_launch_forms(path, shape, testing_build):
+    """The persistent and the group-wave launch forms against the oracle directly
+    (not only against the streaming form); shapes the group-wave kernels do not
+    take run on the streaming kernels under that setting."""
+    gn = testing_build
+    site = synth.Site(*shape)
+    gn.gn3d_debug_set(gn.DEBUG_PATH, gn.PATH_FUSED if path == "fused" else gn.PATH_RESIDENT)
+    full_parity(site, synth.make_inputs(site, seed=6))
+
+
 # ------------------------------------------------------- full-size volumes
 
 def sampled_parity(site, inp, k=200_000, seed=7):
@@ -186,8 +200,11 @@ def sampled_parity(site, inp, k=200_000, seed=7):
     check_out(site.dtype, ys, y64, tg, "y(sampled)")
     dx64, dg64, db64 = oracle.backward_at(inp["dy"], inp["x"], mg, rg, inp["gamma"], N, C, S, G, idx)
     dxs = to_np(dx)[idx]
-    # a, b magnitudes from the oracle's group sums are not returned; bound them by |dy*gamma| scale
-    td = rg[ng] * (np.abs(dyv) * np.abs(inp["gamma"][c]) + 1.0 + (np.abs(xv) + np.abs(mg[ng])) * rg[ng])
+    # the magnitudes entering dx = rstd*((dy*gamma - a) - xhat*b), with the
+    # group's a and b from the oracle's sums at the same statistics
+    a, b, _, _ = oracle.backward_sums(inp["dy"], inp["x"], mg, rg, inp["gamma"], N, C, S, G)
+    td = rg[ng] * (np.abs(dyv) * np.abs(inp["gamma"][c]) + np.abs(a[ng])
+                   + (np.abs(xv) + np.abs(mg[ng])) * rg[ng] * np.abs(b[ng]))
     check_out(site.dtype, dxs, dx64, td, "dx(sampled)")
     dgg, dbg = to_np(dgamma).astype(np.float64), to_np(dbeta).astype(np.float64)
     # L2 of summed terms, from a sample of each channel's terms scaled to the full count

@@ -1,6 +1,7 @@
-"""The two launch forms (persistent cooperative kernels and streaming kernels)
-and every tuning setting give bit-identical results; the bounded-wait failure
-path reports GN3D_ERR_TIMEOUT and leaves the library usable."""
+"""The launch forms (streaming, persistent and group-wave kernels) and every
+tuning setting give bit-identical results; the bounded-wait failure path
+reports GN3D_ERR_TIMEOUT and leaves the library usable.  (Run on the testing
+build of the library, which carries the hooks.)"""
 import numpy as np
 import pytest
 
@@ -12,18 +13,10 @@ from .gpu_util import (device_inputs, run_backward, run_backward_relu, run_forwa
 
 pytestmark = pytest.mark.gpu
 
-DEFAULTS = {gn.DEBUG_PATH: 0, gn.DEBUG_LAG: -1, gn.DEBUG_SLOTS: -1, gn.DEBUG_SPIN_LIMIT: 0, gn.DEBUG_SHARES: -1,
-            gn.DEBUG_RES_HELD: -1, gn.DEBUG_RES_WINDOW: -1, gn.DEBUG_RES_PASS: -1}
-
-
 @pytest.fixture(autouse=True)
-def _reset():
-    from bwd_gn3d_stats_gb300 import build
-
-    build.build()
+def _testing(testing_build):
+    """Every test here sets hooks of the testing build and runs on it."""
     yield
-    for k, v in DEFAULTS.items():
-        gn.gn3d_debug_set(k, v)
 
 
 def run_all(site, d):

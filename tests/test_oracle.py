@@ -474,3 +474,142 @@ def test_ndhwc_index_and_permutations_agree(orc):
     assert np.array_equal(orc.ndhwc_to_ncdhw(cl, N, C, S), a)
     idx = np.arange(N * C * S)
     assert np.array_equal(a[orc.ndhwc_index(idx, N, C, S)], cl)
+
+
+# ------------------------------------------- the backward's sums, the ReLU at indices
+
+@pytest.mark.parametrize("dtype", [synth.F32, synth.BF16])
+@pytest.mark.parametrize("gated", [False, True])
+def test_backward_sums_closed_forms(orc, dtype, gated):
+    """a = mean(dy*gamma) and b = mean(dy*gamma*xhat) per group, s1 = sum dy and
+    s2 = sum dy*xhat per row, written out here with numpy on the widened inputs
+    (behind the ReLU: dy zeroed where the forward's result is <= 0)."""
+    site = synth.Site(2, 6, 3, 4, 5, 3, dtype)
+    inp = synth.make_inputs(site, seed=41)
+    N, C, S, G = site.N, site.C, site.S, site.G
+    y64, mean, rstd = orc.forward(inp["x"], inp["gamma"], inp["beta"], N, C, S, G, site.eps)
+    out = None
+    dyv = synth.bits_to_f32(inp["dy"]).astype(np.float64)
+    if gated:
+        if dtype == synth.BF16:
+            out = orc.round_bf16(orc.relu(y64))
+        else:
+            out = orc.relu(orc.round_f32(y64).astype(np.float64)).astype(np.float32)
+        dyv = np.where(synth.bits_to_f32(out).astype(np.float64) <= 0.0, 0.0, dyv)
+    a, b, s1, s2 = orc.backward_sums(inp["dy"], inp["x"], mean, rstd, inp["gamma"], N, C, S, G, out=out)
+    xv = synth.bits_to_f32(inp["x"]).astype(np.float64).reshape(N, G, C // G, S)
+    xh = (xv - mean.reshape(N, G, 1, 1)) * rstd.reshape(N, G, 1, 1)
+    d = dyv.reshape(N, G, C // G, S)
+    gm = inp["gamma"].astype(np.float64).reshape(1, G, C // G, 1)
+    assert np.allclose(a, (d * gm).mean((2, 3)).reshape(-1), rtol=1e-12, atol=1e-14)
+    assert np.allclose(b, (d * gm * xh).mean((2, 3)).reshape(-1), rtol=1e-12, atol=1e-14)
+    assert np.allclose(s1, d.sum(3).reshape(-1), rtol=1e-12, atol=1e-12)
+    assert np.allclose(s2, (d * xh).sum(3).reshape(-1), rtol=1e-12, atol=1e-12)
+
+
+def test_backward_relu_at_matches_full(orc):
+    """dx at chosen indices and the full dgamma/dbeta behind the ReLU equal the
+    full backward behind the ReLU (itself pinned to torch autograd above)."""
+    site = synth.Site(2, 8, 4, 4, 4, 4, synth.BF16)
+    inp = synth.make_inputs(site, seed=42)
+    N, C, S, G = site.N, site.C, site.S, site.G
+    y64, mean, rstd = orc.forward(inp["x"], inp["gamma"], inp["beta"], N, C, S, G, site.eps)
+    out = orc.round_bf16(orc.relu(y64))
+    assert 0.2 < np.mean(synth.bits_to_f32(out) <= 0) < 0.8  # both sides of the gate are exercised
+    dx, dg, db = orc.backward_relu(inp["dy"], inp["x"], out, mean, rstd, inp["gamma"], N, C, S, G)
+    idx = np.array([0, 3, 17, 63, 64, 300, 511, site.numel - 1])
+    dxk, dgk, dbk = orc.backward_relu_at(inp["dy"], inp["x"], out, mean, rstd, inp["gamma"], N, C, S, G, idx)
+    assert np.array_equal(dxk, dx[idx]) and np.array_equal(dgk, dg) and np.array_equal(dbk, db)
+
+
+def test_backward_relu_ndhwc_matches_torch_channels_last(orc):
+    """The channels-last backward behind the ReLU against torch's float64
+    channels-last relu(group_norm) and its autograd."""
+    rng = np.random.default_rng(43)
+    N, C, D, H, W, G = 2, 8, 2, 3, 4, 2
+    S = D * H * W
+    x, gamma, beta, dy = rand_case(rng, N, C, S, G, scale=1.5)
+    xt = torch.from_numpy(x.astype(np.float64)).reshape(N, C, D, H, W).contiguous(
+        memory_format=torch.channels_last_3d).requires_grad_(True)
+    gt = torch.from_numpy(gamma.astype(np.float64)).requires_grad_(True)
+    bt = torch.from_numpy(beta.astype(np.float64)).requires_grad_(True)
+    yt = F.relu(F.group_norm(xt, G, gt, bt, EPS32))
+    yt.backward(torch.from_numpy(dy.astype(np.float64)).reshape(N, C, D, H, W).contiguous(
+        memory_format=torch.channels_last_3d))
+    xcl, dycl = orc.ncdhw_to_ndhwc(x, N, C, S), orc.ncdhw_to_ndhwc(dy, N, C, S)
+    y, mean, rstd = orc.forward_ndhwc(xcl, gamma, beta, N, C, S, G, EPS32)
+    out = orc.relu(orc.round_f32(y).astype(np.float64)).astype(np.float32)
+    dx, dgamma, dbeta = orc.backward_relu_ndhwc(dycl, xcl, out, mean, rstd, gamma, N, C, S, G)
+    assert np.allclose(dx, xt.grad.permute(0, 2, 3, 4, 1).reshape(-1).numpy(), rtol=1e-9, atol=1e-11)
+    assert np.allclose(dgamma, gt.grad.numpy(), rtol=1e-9, atol=1e-10)
+    assert np.allclose(dbeta, bt.grad.numpy(), rtol=1e-9, atol=1e-10)
+
+
+# ------------------------------------------------------- sharded statistics
+
+def test_combine_moments_textbook(orc):
+    """Two sets {1, 2, 3} and {10, 20}: the combined moments are those of the
+    union, {1, 2, 3, 10, 20} (mean 36/5, M2 = sum of squared deviations)."""
+    a = (np.array([3.0]), np.array([2.0]), np.array([2.0]))
+    b = (np.array([2.0]), np.array([15.0]), np.array([50.0]))
+    n, m, q = orc.combine_moments([a, b])
+    u = np.array([1.0, 2.0, 3.0, 10.0, 20.0])
+    assert n[0] == 5 and abs(m[0] - u.mean()) < 1e-15 and abs(q[0] - ((u - u.mean()) ** 2).sum()) < 1e-12
+    n1, m1, q1 = orc.combine_moments([a])
+    assert n1[0] == 3 and m1[0] == 2.0 and q1[0] == 2.0
+
+
+@pytest.mark.parametrize("cuts", [[4], [2, 2], [1, 2, 1], [3, 1]])
+def test_sharded_moments_combine_to_the_whole(orc, cuts):
+    """A volume cut along D into slabs (each slab its own contiguous tensor):
+    the slabs' moments combined in rank order give the whole volume's count,
+    mean and M2 -- and so its rstd -- to fp64 rounding."""
+    rng = np.random.default_rng(44)
+    N, C, D, H, W, G = 2, 6, sum(cuts), 3, 5, 3
+    x = (3.0 + rng.standard_normal((N, C, D, H, W))).astype(np.float32)
+    mean, var, rstd = orc.stats(x.reshape(-1), N, C, D * H * W, G, EPS32)
+    parts, d0 = [], 0
+    for dk in cuts:
+        slab = np.ascontiguousarray(x[:, :, d0:d0 + dk]).reshape(-1)
+        parts.append(orc.moments(slab, N, C, dk * H * W, G))
+        d0 += dk
+    n, m, q = orc.combine_moments(parts)
+    M = (C // G) * D * H * W
+    assert np.all(n == M)
+    assert np.allclose(m, mean, rtol=1e-13, atol=1e-14)
+    assert np.allclose(q / M, var, rtol=1e-12, atol=1e-14)
+    assert np.allclose(orc.rstd_of(n, q, 1e-5), rstd, rtol=1e-12)
+
+
+def test_sharded_backward_sums_add_up(orc):
+    """At the whole volume's statistics, the slabs' per-row sums s1, s2 added in
+    rank order are the whole volume's; a and b formed from them (A = sum_c
+    gamma_c s1_c, B = sum_c gamma_c s2_c, over the group's M elements) are the
+    whole volume's a and b, and rstd*(dy*gamma - a - xhat*b) is its dx."""
+    rng = np.random.default_rng(45)
+    N, C, D, H, W, G = 2, 6, 5, 2, 3, 2
+    S = D * H * W
+    x, gamma, beta, dy = rand_case(rng, N, C, S, G, scale=2.0, offset=1.0)
+    _, mean, rstd = orc.forward(x, gamma, beta, N, C, S, G, EPS32)
+    a, b, s1, s2 = orc.backward_sums(dy, x, mean, rstd, gamma, N, C, S, G)
+    dx, dgamma, dbeta = orc.backward(dy, x, mean, rstd, gamma, N, C, S, G)
+    x5, dy5 = x.reshape(N, C, D, H, W), dy.reshape(N, C, D, H, W)
+    t1, t2, d0 = np.zeros(N * C), np.zeros(N * C), 0
+    for dk in (2, 1, 2):
+        xs = np.ascontiguousarray(x5[:, :, d0:d0 + dk]).reshape(-1)
+        ds = np.ascontiguousarray(dy5[:, :, d0:d0 + dk]).reshape(-1)
+        _, _, p1, p2 = orc.backward_sums(ds, xs, mean, rstd, gamma, N, C, dk * H * W, G)
+        t1, t2 = t1 + p1, t2 + p2
+        d0 += dk
+    assert np.allclose(t1, s1, rtol=1e-12, atol=1e-12) and np.allclose(t2, s2, rtol=1e-12, atol=1e-12)
+    Cg, M = C // G, (C // G) * S
+    gm = gamma.astype(np.float64).reshape(G, Cg)
+    A = (t1.reshape(N, G, Cg) * gm).sum(2).reshape(-1)
+    B = (t2.reshape(N, G, Cg) * gm).sum(2).reshape(-1)
+    assert np.allclose(A / M, a, rtol=1e-12, atol=1e-14) and np.allclose(B / M, b, rtol=1e-12, atol=1e-14)
+    xh = (x.astype(np.float64).reshape(N, G, Cg * S) - mean.reshape(N, G, 1)) * rstd.reshape(N, G, 1)
+    g = (dy.astype(np.float64).reshape(N, G, Cg, S) * gm.reshape(1, G, Cg, 1)).reshape(N, G, Cg * S)
+    want = rstd.reshape(N, G, 1) * (g - (A / M).reshape(N, G, 1) - xh * (B / M).reshape(N, G, 1))
+    assert np.allclose(dx, want.reshape(-1), rtol=1e-10, atol=1e-12)
+    assert np.allclose(dbeta, t1.reshape(N, C).sum(0), rtol=1e-12, atol=1e-12)
+    assert np.allclose(dgamma, t2.reshape(N, C).sum(0), rtol=1e-12, atol=1e-12)

@@ -43,6 +43,9 @@ MUTANTS = {
     "relu_minus_zero": ("out[i] = (v[i] < 0.0) ? 0.0 : v[i];", "out[i] = (v[i] <= 0.0) ? 0.0 : v[i];"),
     "relu_gate_strict": ("if (gate && widen(gate, dtype, i) <= 0.0) return 0.0;",
                          "if (gate && widen(gate, dtype, i) < 0.0) return 0.0;"),
+    "relu_at_gated_by_x": ("return backward_at_impl(dy, out, x, dtype,", "return backward_at_impl(dy, x, x, dtype,"),
+    "sums_rows_swapped": ("if (s1) memcpy(s1, db, sizeof(double) * (size_t)NC);",
+                          "if (s1) memcpy(s1, dg, sizeof(double) * (size_t)NC);"),
 }
 
 
@@ -113,3 +116,52 @@ def test_channels_last_pins_reject_mutants():
                 caught = True
                 break
         assert caught, f"channels-last mutant {name} survived the pins"
+
+
+def _relu_ndhwc_gated_by_x(dy, x, out, mean, rstd, gamma, N, C, S, G, want_dx=True):
+    return oracle.backward_relu_ndhwc(dy, x, x, mean, rstd, gamma, N, C, S, G, want_dx)  # x passed as the gate
+
+
+def _combine_without_cross_term(parts):
+    n, m, q = (np.array(v, dtype=np.float64) for v in parts[0])
+    for nb, mb, qb in parts[1:]:
+        tot = n + nb
+        m = m + (mb - m) * nb / tot
+        q = q + qb  # the d^2 * na * nb / n term dropped
+        n = tot
+    return n, m, q
+
+
+def _combine_unweighted_mean(parts):
+    n, m, q = (np.array(v, dtype=np.float64) for v in parts[0])
+    for nb, mb, qb in parts[1:]:
+        d = mb - m
+        tot = n + nb
+        q = q + qb + d * d * n * nb / tot
+        m = (m + mb) / 2  # means averaged, not weighted by the counts
+        n = tot
+    return n, m, q
+
+
+def test_relu_ndhwc_and_sharded_pins_reject_mutants():
+    cases = {
+        "relu_ndhwc_gated_by_x": (_mutated_oracle(backward_relu_ndhwc=_relu_ndhwc_gated_by_x),
+                                  [test_oracle.test_backward_relu_ndhwc_matches_torch_channels_last]),
+        "combine_without_cross_term": (
+            _mutated_oracle(combine_moments=_combine_without_cross_term),
+            [test_oracle.test_combine_moments_textbook,
+             lambda o: test_oracle.test_sharded_moments_combine_to_the_whole(o, [1, 2, 1])]),
+        "combine_unweighted_mean": (
+            _mutated_oracle(combine_moments=_combine_unweighted_mean),
+            [test_oracle.test_combine_moments_textbook,
+             lambda o: test_oracle.test_sharded_moments_combine_to_the_whole(o, [3, 1])]),
+    }
+    for name, (orc, pins) in cases.items():
+        caught = False
+        for pin in pins:
+            try:
+                pin(orc)
+            except (AssertionError, ValueError, IndexError):
+                caught = True
+                break
+        assert caught, f"mutant {name} survived the pins"
