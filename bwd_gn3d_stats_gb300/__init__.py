@@ -92,6 +92,17 @@ def _load(kind: str):
             L.gn3d_launch_count.restype = ctypes.c_uint64
             L.gn3d_version.argtypes = []
             L.gn3d_version.restype = ctypes.c_char_p
+            L.gn3d_forward_moments.argtypes = [vp, i64, i64, i64, i64, i64, i64, ci, vp, vp]
+            L.gn3d_moments_combine.argtypes = [vp, i64, i64, vp, vp]
+            L.gn3d_forward_apply.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, dbl, ci, ci, vp, vp, vp, vp,
+                                             vp]
+            L.gn3d_backward_sums.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, ci, vp, vp]
+            L.gn3d_sums_combine.argtypes = [vp, i64, i64, vp, vp]
+            L.gn3d_backward_dx_from_sums.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, ci,
+                                                     vp, vp, vp, vp]
+            for name in ("gn3d_forward_moments", "gn3d_moments_combine", "gn3d_forward_apply", "gn3d_backward_sums",
+                         "gn3d_sums_combine", "gn3d_backward_dx_from_sums"):
+                getattr(L, name).restype = ci
             L.gn3d_timing.argtypes = [ci]
             L.gn3d_timing.restype = ci
             L.gn3d_kernel_time.argtypes = [ctypes.c_char_p, ctypes.POINTER(ctypes.c_double),
@@ -149,6 +160,33 @@ def gn3d_backward_ndhwc(dy, x, mean, rstd, gamma, N, C, D, H, W, G, dtype, dx, d
 def gn3d_backward_ndhwc_relu(dy, x, out, mean, rstd, gamma, N, C, D, H, W, G, dtype, dx, dgamma, dbeta, stream):
     _check(lib().gn3d_backward_ndhwc_relu(dy, x, out, mean, rstd, gamma, N, C, D, H, W, G, dtype, dx, dgamma,
                                           dbeta, stream))
+
+
+def gn3d_forward_moments(x, N, C, D, H, W, G, in_dtype, moments, stream):
+    _check(lib().gn3d_forward_moments(x, N, C, D, H, W, G, in_dtype, moments, stream))
+
+
+def gn3d_moments_combine(shards, K, NG, combined, stream):
+    _check(lib().gn3d_moments_combine(shards, K, NG, combined, stream))
+
+
+def gn3d_forward_apply(x, gamma, beta, N, C, D, H, W, G, eps, in_dtype, out_dtype, moments, y, mean, rstd, stream):
+    _check(lib().gn3d_forward_apply(x, gamma, beta, N, C, D, H, W, G, eps, in_dtype, out_dtype, moments, y, mean,
+                                    rstd, stream))
+
+
+def gn3d_backward_sums(dy, x, mean, rstd, N, C, D, H, W, G, dtype, sums, stream):
+    _check(lib().gn3d_backward_sums(dy, x, mean, rstd, N, C, D, H, W, G, dtype, sums, stream))
+
+
+def gn3d_sums_combine(shards, K, NC, total, stream):
+    _check(lib().gn3d_sums_combine(shards, K, NC, total, stream))
+
+
+def gn3d_backward_dx_from_sums(dy, x, mean, rstd, gamma, sums, group_count, N, C, D, H, W, G, dtype, dx, dgamma,
+                               dbeta, stream):
+    _check(lib().gn3d_backward_dx_from_sums(dy, x, mean, rstd, gamma, sums, group_count, N, C, D, H, W, G, dtype,
+                                            dx, dgamma, dbeta, stream))
 
 
 def gn3d_stream_status(stream):

@@ -22,6 +22,7 @@
 #include "gn3d_kernels.cuh"
 #include "gn3d_ndhwc.cuh"
 #include "gn3d_resident.cuh"
+#include "gn3d_shard.cuh"
 
 namespace gn3d {
 
@@ -408,6 +409,7 @@ int launch_forward(const void* x, const float* gamma, const float* beta, const P
   s.cur = static_cast<char*>(s.base);
   uint32_t* sync = s.take<uint32_t>(nsync);
   FwdWs w;
+  w.moments = nullptr;
   w.bcnt = sync;
   w.gcnt = sync + nblk;
   w.ready = sync + nblk + p.NG;
@@ -726,6 +728,166 @@ int launch_backward_ndhwc(const void* dy, const void* x, const void* res, const 
 
 bool valid_dtype(int d) { return d == GN3D_F32 || d == GN3D_BF16; }
 
+// ------------------------------------------------------ sharded statistics
+// The forward statistics kernel alone, exporting each group's moments.
+template <class TI>
+int launch_moments(const void* x, const Plan& p, Moments* moments, cudaStream_t st, DevInfo& di) {
+  const int64_t nblk = p.NC * p.nb;
+  const int64_t nsync = nblk + 2 * p.NG;
+  const int64_t bytes = rup(nsync * 4) + rup(p.units * (int64_t)sizeof(Part)) + rup(nblk * (int64_t)sizeof(Part));
+  Scratch s;
+  GN3D_CUDA(scratch_alloc(&s.base, bytes, di, st), "scratch allocation");
+  s.cur = static_cast<char*>(s.base);
+  uint32_t* sync = s.take<uint32_t>(nsync);
+  FwdWs w;
+  w.moments = moments;
+  w.bcnt = sync;
+  w.gcnt = sync + nblk;
+  w.ready = sync + nblk + p.NG;
+  w.parts = s.take<Part>(p.units);
+  w.bparts = s.take<Part>(nblk);
+  w.stats = nullptr;
+  cudaError_t e = cudaMemsetAsync(sync, 0, (size_t)nsync * sizeof(uint32_t), st);
+  if (e == cudaSuccess) e = injected_launch_error();
+  using Shape = FwdStatShape<TI>;
+  const int smem = Shape::kWarps * WarpRing<TI, 1, Shape::kSlots>::kWarpBytes;
+  const bool full = plan_all_full(p);
+  const int sgrid = grid_for(di, p.units, 1);
+  const bool cut = unit_shares(p, (int64_t)sgrid * Shape::kWarps);
+  auto ks = full ? (cut ? k_fwd_stats<TI, true, true> : k_fwd_stats<TI, true, false>)
+                 : (cut ? k_fwd_stats<TI, false, true> : k_fwd_stats<TI, false, false>);
+  int rc = raise_smem((const void*)ks, smem, di);
+  if (rc) { cudaFreeAsync(s.base, st); return rc; }
+  if (e == cudaSuccess) {
+    g_launches += 1;
+    LaunchTimer t1(KK_FWD_STATS, st, di);
+    ks<<<sgrid, 32 * Shape::kWarps, smem, st>>>(static_cast<const TI*>(x), p, w, 1.f, nullptr, nullptr,
+                                                spin_budget(), di.status);
+    t1.done();
+    e = cudaGetLastError();
+  }
+  cudaError_t ef = cudaFreeAsync(s.base, st);
+  if (e != cudaSuccess) return cuda_fail(e, "moments launch");
+  if (ef != cudaSuccess) return cuda_fail(ef, "scratch free");
+  return GN3D_OK;
+}
+
+// The normalize pass with statistics formed from given (combined) moments.
+template <class TI, class TO>
+int launch_apply(const void* x, const float* gamma, const float* beta, const Plan& p, float eps,
+                 const Moments* moments, void* y, float* mean, float* rstd, cudaStream_t st, DevInfo& di) {
+  Scratch s;
+  GN3D_CUDA(scratch_alloc(&s.base, rup(p.NG * (int64_t)sizeof(float4)), di, st), "scratch allocation");
+  s.cur = static_cast<char*>(s.base);
+  float4* stats = s.take<float4>(p.NG);
+  cudaError_t e = injected_launch_error();
+  if (e == cudaSuccess) {
+    g_launches += 2;
+    k_stats_from_moments<<<(unsigned)((p.NG + 127) / 128), 128, 0, st>>>(moments, p.NG, eps, stats, mean, rstd);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) {
+    using Shape = FwdStatShape<TI>;
+    const bool full = plan_all_full(p);
+    const int sgrid = grid_for(di, p.units, 1);
+    const bool cut = unit_shares(p, (int64_t)sgrid * Shape::kWarps);
+    LaunchTimer t2(KK_FWD_NORM, st, di);
+    auto kn = norm_kernel<TI, TO>(full, false, cut);
+    e = launch_dependent(kn, sgrid, 32 * kElemWarps, st, static_cast<const TI*>(x), static_cast<TO*>(y), p,
+                         (const float4*)stats, gamma, beta);
+    t2.done();
+  }
+  cudaError_t ef = cudaFreeAsync(s.base, st);
+  if (e != cudaSuccess) return cuda_fail(e, "apply launch");
+  if (ef != cudaSuccess) return cuda_fail(ef, "scratch free");
+  return GN3D_OK;
+}
+
+// The backward reduction alone, its per-row totals written to `sums`.
+template <class T>
+int launch_row_sums(const void* dy, const void* x, const float* mean, const float* rstd, const Plan& p,
+                    float2* sums, cudaStream_t st, DevInfo& di) {
+  const int64_t nblk = p.NC * p.nb;
+  const int64_t nsync = nblk + 2 * p.NG + 1;  // bcnt, gcnt, ready, done
+  const int64_t bytes = rup(nsync * 4) + rup(p.units * (int64_t)sizeof(float2)) +
+                        rup(nblk * (int64_t)sizeof(float2)) + rup(p.NG * (int64_t)sizeof(float2));
+  Scratch s;
+  GN3D_CUDA(scratch_alloc(&s.base, bytes, di, st), "scratch allocation");
+  s.cur = static_cast<char*>(s.base);
+  uint32_t* sync = s.take<uint32_t>(nsync);
+  BwdWs w;
+  w.bcnt = sync;
+  w.gcnt = sync + nblk;
+  w.ready = sync + nblk + p.NG;
+  w.done = sync + nblk + 2 * p.NG;
+  w.parts = s.take<float2>(p.units);
+  w.bparts = s.take<float2>(nblk);
+  w.rows = sums;
+  w.coef = s.take<float2>(p.NG);
+  cudaError_t e = cudaMemsetAsync(sync, 0, (size_t)nsync * sizeof(uint32_t), st);
+  if (e == cudaSuccess) e = injected_launch_error();
+  using Shape = BwdRedShape<T, false>;
+  const int smem = Shape::kWarps * WarpRing<T, Shape::kTensors, Shape::kSlots, Shape::kElems>::kWarpBytes;
+  const bool full = plan_all_full(p);
+  const int rgrid = grid_for(di, p.units, 1);
+  const bool cut = unit_shares(p, (int64_t)rgrid * Shape::kWarps);
+  auto kr = full ? (cut ? k_bwd_reduce<T, true, false, true> : k_bwd_reduce<T, true, false, false>)
+                 : (cut ? k_bwd_reduce<T, false, false, true> : k_bwd_reduce<T, false, false, false>);
+  int rc = raise_smem((const void*)kr, smem, di);
+  if (rc) { cudaFreeAsync(s.base, st); return rc; }
+  if (e == cudaSuccess) {
+    g_launches += 1;
+    LaunchTimer t1(KK_BWD_REDUCE, st, di);
+    kr<<<rgrid, 32 * Shape::kWarps, smem, st>>>(static_cast<const T*>(dy), static_cast<const T*>(x), nullptr, p,
+                                               mean, rstd, nullptr, w, nullptr, nullptr, spin_budget(), di.status);
+    t1.done();
+    e = cudaGetLastError();
+  }
+  cudaError_t ef = cudaFreeAsync(s.base, st);
+  if (e != cudaSuccess) return cuda_fail(e, "sums launch");
+  if (ef != cudaSuccess) return cuda_fail(ef, "scratch free");
+  return GN3D_OK;
+}
+
+// The dx pass (and dgamma, dbeta) from given per-row totals over groups of M elements.
+template <class T>
+int launch_dx_from_sums(const void* dy, const void* x, const float* mean, const float* rstd, const float* gamma,
+                        const float2* sums, int64_t M, const Plan& p, void* dx, float* dgamma, float* dbeta,
+                        cudaStream_t st, DevInfo& di) {
+  Scratch s;
+  GN3D_CUDA(scratch_alloc(&s.base, rup(p.NG * (int64_t)sizeof(float2)), di, st), "scratch allocation");
+  s.cur = static_cast<char*>(s.base);
+  float2* coef = s.take<float2>(p.NG);
+  cudaError_t e = injected_launch_error();
+  if (e == cudaSuccess) {
+    g_launches += 1;
+    k_coef_from_sums<<<(unsigned)((p.NG + 127) / 128), 128, 0, st>>>(p, sums, rstd, gamma, M, coef);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess && (dgamma || dbeta)) {
+    g_launches += 1;
+    k_param_grads<<<1, 32, 0, st>>>(p, rstd, sums, dgamma, dbeta);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) {
+    using Shape = BwdRedShape<T, false>;
+    const bool full = plan_all_full(p);
+    const int rgrid = grid_for(di, p.units, 1);
+    const bool cut = unit_shares(p, (int64_t)rgrid * Shape::kWarps);
+    g_launches += 1;
+    LaunchTimer t2(KK_BWD_DX, st, di);
+    auto kd = full ? (cut ? k_bwd_dx<T, true, false, true> : k_bwd_dx<T, true, false, false>)
+                   : (cut ? k_bwd_dx<T, false, false, true> : k_bwd_dx<T, false, false, false>);
+    e = launch_dependent(kd, rgrid, 32 * kElemWarps, st, static_cast<const T*>(dy), static_cast<const T*>(x),
+                         (const T*)nullptr, static_cast<T*>(dx), p, mean, rstd, gamma, (const float2*)coef);
+    t2.done();
+  }
+  cudaError_t ef = cudaFreeAsync(s.base, st);
+  if (e != cudaSuccess) return cuda_fail(e, "dx launch");
+  if (ef != cudaSuccess) return cuda_fail(ef, "scratch free");
+  return GN3D_OK;
+}
+
 // ------------------------------------------------- allocation-free forward
 // Scratch of gn3d_forward_noalloc: one fixed area in the module's global memory,
 // present on every device that loads the library, for as long as it is loaded.
@@ -782,6 +944,7 @@ int launch_forward_noalloc(const void* x, const float* gamma, const float* beta,
   s.cur = reinterpret_cast<char*>(nd.scratch);
   uint32_t* sync = s.take<uint32_t>(nsync);
   FwdWs w;
+  w.moments = nullptr;
   w.bcnt = sync;
   w.gcnt = sync + nblk;
   w.ready = sync + nblk + p.NG;
@@ -1016,6 +1179,190 @@ extern "C" int gn3d_backward_ndhwc_relu(const void* dy, const void* x, const voi
                                         int64_t H, int64_t W, int64_t G, gn3d_dtype dtype, void* dx, float* dgamma,
                                         float* dbeta, void* stream) {
   return backward_impl(dy, x, out, mean, rstd, gamma, N, C, D, H, W, G, dtype, dx, dgamma, dbeta, stream, true, true);
+}
+
+// ------------------------------------------------------ sharded statistics
+namespace {
+// Shapes of one shard: a shard may hold a single element of a group.
+int check_dims(int64_t N, int64_t C, int64_t D, int64_t H, int64_t W, int64_t G) {
+  if (N < 0 || C < 0 || D < 0 || H < 0 || W < 0) return arg_fail("negative dimension");
+  if (G <= 0) return arg_fail("G must be >= 1");
+  if (C % G != 0) return arg_fail("C must be divisible by G");
+  const double total = (double)N * (double)C * (double)D * (double)H * (double)W;
+  if (total > 4.0e18) return arg_fail("tensor too large");
+  return GN3D_OK;
+}
+
+bool aligned8(const void* p) { return ((uintptr_t)p & 7u) == 0; }
+
+// The current device's facts and a device pointer check of each non-null argument.
+int setup(DevInfo** di, int* dev) {
+  GN3D_CUDA(cudaGetDevice(dev), "cudaGetDevice");
+  return device_info(*dev, di);
+}
+}  // namespace
+
+extern "C" int gn3d_forward_moments(const void* x, int64_t N, int64_t C, int64_t D, int64_t H, int64_t W, int64_t G,
+                                    gn3d_dtype in_dtype, gn3d_moments* moments, void* stream) {
+  static_assert(sizeof(gn3d_moments) == sizeof(Moments), "gn3d_moments layout");
+  int rc = check_dims(N, C, D, H, W, G);
+  if (rc) return rc;
+  if (!valid_dtype(in_dtype)) return arg_fail("unsupported dtype");
+  const Plan p = make_plan(N, C, D * H * W, G);
+  int dev = 0;
+  DevInfo* di = nullptr;
+  if ((rc = setup(&di, &dev))) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (p.NG == 0) return GN3D_OK;
+  if (!moments || !aligned8(moments)) return arg_fail("moments is required, 8-byte aligned");
+  if ((rc = check_ptr(moments, dev, "moments"))) return rc;
+  if (p.NC * p.S == 0) {  // no elements: count 0, mean 0, M2 0
+    GN3D_CUDA(cudaMemsetAsync(moments, 0, (size_t)p.NG * sizeof(gn3d_moments), st), "memset");
+    return GN3D_OK;
+  }
+  if (!x || !aligned16(x)) return arg_fail("x is required, 16-byte aligned");
+  if ((rc = check_ptr(x, dev, "x"))) return rc;
+  Moments* m = reinterpret_cast<Moments*>(moments);
+  return in_dtype == GN3D_BF16 ? launch_moments<__nv_bfloat16>(x, p, m, st, *di) : launch_moments<float>(x, p, m, st, *di);
+}
+
+extern "C" int gn3d_moments_combine(const gn3d_moments* shards, int64_t K, int64_t NG, gn3d_moments* combined,
+                                    void* stream) {
+  if (K < 1 || NG < 0) return arg_fail("K >= 1 shards, NG >= 0 groups");
+  int dev = 0, rc;
+  DevInfo* di = nullptr;
+  if ((rc = setup(&di, &dev))) return rc;
+  if (NG == 0) return GN3D_OK;
+  if (!shards || !combined || !aligned8(shards) || !aligned8(combined))
+    return arg_fail("shards and combined are required, 8-byte aligned");
+  if ((rc = check_ptr(shards, dev, "shards")) || (rc = check_ptr(combined, dev, "combined"))) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  g_launches += 1;
+  k_moments_combine<<<(unsigned)((NG + 127) / 128), 128, 0, st>>>(reinterpret_cast<const Moments*>(shards), K, NG,
+                                                                  reinterpret_cast<Moments*>(combined));
+  GN3D_CUDA(cudaGetLastError(), "combine launch");
+  return GN3D_OK;
+}
+
+extern "C" int gn3d_forward_apply(const void* x, const float* gamma, const float* beta, int64_t N, int64_t C,
+                                  int64_t D, int64_t H, int64_t W, int64_t G, double eps, gn3d_dtype in_dtype,
+                                  gn3d_dtype out_dtype, const gn3d_moments* moments, void* y, float* mean, float* rstd,
+                                  void* stream) {
+  int rc = check_dims(N, C, D, H, W, G);
+  if (rc) return rc;
+  if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype)) return arg_fail("unsupported dtype");
+  if (!(eps >= 0.0) || !isfinite(eps)) return arg_fail("eps must be finite and >= 0");
+  const Plan p = make_plan(N, C, D * H * W, G);
+  int dev = 0;
+  DevInfo* di = nullptr;
+  if ((rc = setup(&di, &dev))) return rc;
+  if (p.NG == 0) return GN3D_OK;
+  if (!moments || !aligned8(moments)) return arg_fail("moments is required, 8-byte aligned");
+  if ((rc = check_ptr(moments, dev, "moments"))) return rc;
+  if (p.NC * p.S > 0) {
+    if (!x || !y) return arg_fail("x and y are required");
+    if (!aligned16(x) || !aligned16(y)) return arg_fail("x and y must be 16-byte aligned");
+    if ((rc = check_ptr(x, dev, "x")) || (rc = check_ptr(y, dev, "y"))) return rc;
+  }
+  if (mean && (rc = check_ptr(mean, dev, "mean"))) return rc;
+  if (rstd && (rc = check_ptr(rstd, dev, "rstd"))) return rc;
+  if (gamma && (rc = check_ptr(gamma, dev, "gamma"))) return rc;
+  if (beta && (rc = check_ptr(beta, dev, "beta"))) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const float feps = (float)eps;
+  const Moments* m = reinterpret_cast<const Moments*>(moments);
+  using bf = __nv_bfloat16;
+  if (in_dtype == GN3D_BF16 && out_dtype == GN3D_BF16)
+    return launch_apply<bf, bf>(x, gamma, beta, p, feps, m, y, mean, rstd, st, *di);
+  if (in_dtype == GN3D_BF16 && out_dtype == GN3D_F32)
+    return launch_apply<bf, float>(x, gamma, beta, p, feps, m, y, mean, rstd, st, *di);
+  if (in_dtype == GN3D_F32 && out_dtype == GN3D_BF16)
+    return launch_apply<float, bf>(x, gamma, beta, p, feps, m, y, mean, rstd, st, *di);
+  return launch_apply<float, float>(x, gamma, beta, p, feps, m, y, mean, rstd, st, *di);
+}
+
+extern "C" int gn3d_backward_sums(const void* dy, const void* x, const float* mean, const float* rstd, int64_t N,
+                                  int64_t C, int64_t D, int64_t H, int64_t W, int64_t G, gn3d_dtype dtype, float* sums,
+                                  void* stream) {
+  int rc = check_dims(N, C, D, H, W, G);
+  if (rc) return rc;
+  if (!valid_dtype(dtype)) return arg_fail("unsupported dtype");
+  const Plan p = make_plan(N, C, D * H * W, G);
+  int dev = 0;
+  DevInfo* di = nullptr;
+  if ((rc = setup(&di, &dev))) return rc;
+  if (p.NC == 0) return GN3D_OK;
+  if (!sums || !aligned8(sums)) return arg_fail("sums is required, 8-byte aligned");
+  if ((rc = check_ptr(sums, dev, "sums"))) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (p.NC * p.S == 0) {
+    GN3D_CUDA(cudaMemsetAsync(sums, 0, (size_t)p.NC * 2 * sizeof(float), st), "memset");
+    return GN3D_OK;
+  }
+  if (!dy || !x || !mean || !rstd) return arg_fail("dy, x, mean and rstd are required");
+  if (!aligned16(dy) || !aligned16(x)) return arg_fail("dy and x must be 16-byte aligned");
+  if ((rc = check_ptr(dy, dev, "dy")) || (rc = check_ptr(x, dev, "x")) || (rc = check_ptr(mean, dev, "mean")) ||
+      (rc = check_ptr(rstd, dev, "rstd")))
+    return rc;
+  float2* s2 = reinterpret_cast<float2*>(sums);
+  return dtype == GN3D_BF16 ? launch_row_sums<__nv_bfloat16>(dy, x, mean, rstd, p, s2, st, *di)
+                            : launch_row_sums<float>(dy, x, mean, rstd, p, s2, st, *di);
+}
+
+extern "C" int gn3d_sums_combine(const float* shards, int64_t K, int64_t NC, float* total, void* stream) {
+  if (K < 1 || NC < 0) return arg_fail("K >= 1 shards, NC >= 0 rows");
+  int dev = 0, rc;
+  DevInfo* di = nullptr;
+  if ((rc = setup(&di, &dev))) return rc;
+  if (NC == 0) return GN3D_OK;
+  if (!shards || !total || !aligned8(shards) || !aligned8(total))
+    return arg_fail("shards and total are required, 8-byte aligned");
+  if ((rc = check_ptr(shards, dev, "shards")) || (rc = check_ptr(total, dev, "total"))) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  g_launches += 1;
+  k_sums_combine<<<(unsigned)((NC + 127) / 128), 128, 0, st>>>(reinterpret_cast<const float2*>(shards), K, NC,
+                                                              reinterpret_cast<float2*>(total));
+  GN3D_CUDA(cudaGetLastError(), "combine launch");
+  return GN3D_OK;
+}
+
+extern "C" int gn3d_backward_dx_from_sums(const void* dy, const void* x, const float* mean, const float* rstd,
+                                          const float* gamma, const float* sums, int64_t group_count, int64_t N,
+                                          int64_t C, int64_t D, int64_t H, int64_t W, int64_t G, gn3d_dtype dtype,
+                                          void* dx, float* dgamma, float* dbeta, void* stream) {
+  int rc = check_dims(N, C, D, H, W, G);
+  if (rc) return rc;
+  if (!valid_dtype(dtype)) return arg_fail("unsupported dtype");
+  if (group_count < 1) return arg_fail("group_count (elements per group of the whole tensor) must be >= 1");
+  const Plan p = make_plan(N, C, D * H * W, G);
+  int dev = 0;
+  DevInfo* di = nullptr;
+  if ((rc = setup(&di, &dev))) return rc;
+  if (p.NC == 0) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (dgamma && C > 0) GN3D_CUDA(cudaMemsetAsync(dgamma, 0, (size_t)C * sizeof(float), st), "memset");
+    if (dbeta && C > 0) GN3D_CUDA(cudaMemsetAsync(dbeta, 0, (size_t)C * sizeof(float), st), "memset");
+    return GN3D_OK;
+  }
+  if (!sums || !mean || !rstd || !aligned8(sums)) return arg_fail("sums (8-byte aligned), mean and rstd are required");
+  if ((rc = check_ptr(sums, dev, "sums")) || (rc = check_ptr(mean, dev, "mean")) ||
+      (rc = check_ptr(rstd, dev, "rstd")))
+    return rc;
+  if (p.NC * p.S > 0) {
+    if (!dy || !x || !dx) return arg_fail("dy, x and dx are required");
+    if (!aligned16(dy) || !aligned16(x) || !aligned16(dx)) return arg_fail("dy, x and dx must be 16-byte aligned");
+    if ((rc = check_ptr(dy, dev, "dy")) || (rc = check_ptr(x, dev, "x")) || (rc = check_ptr(dx, dev, "dx")))
+      return rc;
+  }
+  if (gamma && (rc = check_ptr(gamma, dev, "gamma"))) return rc;
+  if (dgamma && (rc = check_ptr(dgamma, dev, "dgamma"))) return rc;
+  if (dbeta && (rc = check_ptr(dbeta, dev, "dbeta"))) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const float2* s2 = reinterpret_cast<const float2*>(sums);
+  return dtype == GN3D_BF16
+             ? launch_dx_from_sums<__nv_bfloat16>(dy, x, mean, rstd, gamma, s2, group_count, p, dx, dgamma, dbeta, st,
+                                                  *di)
+             : launch_dx_from_sums<float>(dy, x, mean, rstd, gamma, s2, group_count, p, dx, dgamma, dbeta, st, *di);
 }
 
 extern "C" int gn3d_stream_status(void* stream) {

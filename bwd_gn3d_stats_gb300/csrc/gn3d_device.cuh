@@ -445,9 +445,9 @@ __device__ __forceinline__ Part merge_lanes(const Part a, int n) {
 }
 
 // Group merge of its Cg*nb block partials (contiguous), by one warp: lane l takes
-// blocks l, l+32, ... in order, then the butterfly.  Returns (mean hi, mean lo,
-// rstd) with mean = hi + lo and rstd = 1/sqrt(M2/M + eps).
-__device__ __forceinline__ float4 merge_group(const Part* blocks, int64_t nblk, int64_t M, float eps) {
+// blocks l, l+32, ... in order, then the butterfly.  Returns the group's moments
+// (mean = m1 + cn, M2).
+__device__ __forceinline__ Part merge_group_part(const Part* blocks, int64_t nblk, int64_t M) {
   const int lane = threadIdx.x & 31;
   const Part b0 = ldcg_part(blocks);
   const float K = fadd(b0.m1, b0.cn);
@@ -469,9 +469,18 @@ __device__ __forceinline__ float4 merge_group(const Part* blocks, int64_t nblk, 
     }
   }
   const float2 t = warp_sum2(S, Q);
-  const Part g = finish_merge(K, t.x, t.y, M);
+  return finish_merge(K, t.x, t.y, M);
+}
+
+// A group's statistics from its moments over M elements: (mean hi, mean lo,
+// rstd) with rstd = 1/sqrt(M2/M + eps).
+__device__ __forceinline__ float4 group_stats(const Part& g, int64_t M, float eps) {
   const float var = __fdiv_rn(g.m2, (float)M);
   return make_float4(g.m1, g.cn, __frsqrt_rn(fadd(var, eps)), 0.f);
+}
+
+__device__ __forceinline__ float4 merge_group(const Part* blocks, int64_t nblk, int64_t M, float eps) {
+  return group_stats(merge_group_part(blocks, nblk, M), M, eps);
 }
 
 // The gradient arriving at GroupNorm behind a fused ReLU: dy read from `body`,
@@ -581,6 +590,12 @@ __device__ __forceinline__ Part unit_moments(const View& u, const T* __restrict_
 }
 
 // --------------------------------------------------------------- forward
+// The moments of one group as the C ABI exports them (gn3d_moments).
+struct Moments {
+  long long count;
+  float mean_hi, mean_lo, m2, reserved;
+};
+
 struct FwdWs {
   Part* parts;      // [units]
   Part* bparts;     // [NC * nb]
@@ -588,6 +603,7 @@ struct FwdWs {
   uint32_t* bcnt;   // [NC * nb] unit arrivals per block
   uint32_t* gcnt;   // [NG] block arrivals per group
   uint32_t* ready;  // [NG] 1 once stats[g] is published
+  Moments* moments; // [NG] or null: export each group's moments instead of its statistics
 };
 
 // A completed forward block, by one warp: publish its partial, arrive on the
@@ -598,7 +614,12 @@ __device__ __forceinline__ void fwd_block_done(const Plan& p, const FwdWs& ws, i
   if (lane == 0) ws.bparts[blk] = b;
   const int64_t g = (blk / p.nb) / p.Cg;
   if (!warp_arrive_last(ws.gcnt + g, (uint32_t)(p.Cg * p.nb))) return;
-  const float4 st = merge_group(ws.bparts + g * p.Cg * p.nb, p.Cg * p.nb, p.M, eps);
+  const Part gp = merge_group_part(ws.bparts + g * p.Cg * p.nb, p.Cg * p.nb, p.M);
+  if (ws.moments) {  // the group's moments only (a shard's partial statistics)
+    if (lane == 0) ws.moments[g] = Moments{(long long)p.M, gp.m1, gp.cn, gp.m2, 0.f};
+    return;
+  }
+  const float4 st = group_stats(gp, p.M, eps);
   if (lane == 0) {
     ws.stats[g] = st;
     if (mean_out) mean_out[g] = fadd(st.x, st.y);

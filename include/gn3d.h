@@ -200,6 +200,84 @@ int gn3d_backward_ndhwc_relu(const void* dy, const void* x, const void* out, con
                              float* dbeta, void* stream);
 
 /*
+ * Global statistics under spatial sharding, and a backward driven by
+ * externally produced sums.
+ *
+ * A volume split into shards -- e.g. one D-slab per rank under DistConv, each
+ * held as its own contiguous [N, C, D_k, H, W] tensor -- needs the GroupNorm
+ * of the whole volume, whose statistics span every shard.  The ScaFFold
+ * GroupNorm pages (PR #93, the commit that unwraps DCTensors) normalize each
+ * shard with its own statistics and leave global statistics as an open
+ * question; these entry points implement the one exchange per direction that
+ * gives the whole volume's result:
+ *
+ *   forward:  gn3d_forward_moments on each shard -> exchange the [N*G]
+ *             moments (e.g. all-gather, rank order) -> gn3d_moments_combine
+ *             -> gn3d_forward_apply on each shard with the combined moments;
+ *   backward: gn3d_backward_sums on each shard at the global (mean, rstd) ->
+ *             exchange the [N*C] sums -> gn3d_sums_combine ->
+ *             gn3d_backward_dx_from_sums on each shard with the totals.
+ *
+ * The moments of a group are combined in rank order with the parallel-variance
+ * merge of Chan, Golub and LeVeque (the merge the pages name for partial
+ * statistics), in the shifted-sum form used by every merge of this library;
+ * the sums are added in rank order.  With one shard every combine is the
+ * identity and the results are bit-identical to gn3d_forward / gn3d_backward.
+ * The exchange itself is the caller's (this library makes no collective
+ * call).  NCDHW layout, no fused ReLU.  All pointers are device memory of the
+ * current device; calls are ordered on `stream`.
+ *
+ * gn3d_backward_dx_from_sums is also the dx pass for a caller that produces
+ * the backward's sums itself (for example fused into the kernel that produces
+ * dy): it reads x and dy once and writes dx, with no reduction pass.
+ */
+typedef struct {
+  int64_t count;   /* elements of the group in this shard */
+  float mean_hi;   /* the group mean is mean_hi + mean_lo (an unevaluated pair) */
+  float mean_lo;
+  float m2;        /* sum of (x - mean)^2 */
+  float reserved;
+} gn3d_moments;    /* 24 bytes */
+
+/* Per group (n, g) moments of x [N,C,D,H,W] (a shard): moments[n*G + g].
+ * x 16-byte aligned, moments 8-byte aligned.  A shard may hold any number of a
+ * group's elements (zero gives count 0). */
+int gn3d_forward_moments(const void* x, int64_t N, int64_t C, int64_t D, int64_t H, int64_t W, int64_t G,
+                         gn3d_dtype in_dtype, gn3d_moments* moments, void* stream);
+
+/* Combine K shards' moments, shards[k*NG + i] (rank-major), per group i in rank
+ * order into combined[i] (may not alias shards). */
+int gn3d_moments_combine(const gn3d_moments* shards, int64_t K, int64_t NG, gn3d_moments* combined, void* stream);
+
+/* The forward's normalize pass of a shard with the whole volume's moments
+ * [N*G]: y as gn3d_forward writes it, and mean [N*G] / rstd [N*G] (either may
+ * be NULL) with rstd = 1/sqrt(M2/count + eps). */
+int gn3d_forward_apply(const void* x, const float* gamma, const float* beta, int64_t N, int64_t C, int64_t D,
+                       int64_t H, int64_t W, int64_t G, double eps, gn3d_dtype in_dtype, gn3d_dtype out_dtype,
+                       const gn3d_moments* moments, void* y, float* mean, float* rstd, void* stream);
+
+/* Per row (n, c) of a shard at the given (global) statistics: sums[2*(n*C+c)] =
+ * sum dy, sums[2*(n*C+c)+1] = sum dy*(x - mean).  dy, x 16-byte aligned, sums
+ * 8-byte aligned. */
+int gn3d_backward_sums(const void* dy, const void* x, const float* mean, const float* rstd, int64_t N, int64_t C,
+                       int64_t D, int64_t H, int64_t W, int64_t G, gn3d_dtype dtype, float* sums, void* stream);
+
+/* Add K shards' row sums, shards[(k*NC + r)*2 + {0,1}], per row in rank order
+ * into total[NC*2] (may not alias shards). */
+int gn3d_sums_combine(const float* shards, int64_t K, int64_t NC, float* total, void* stream);
+
+/* The backward's dx pass of a shard from the whole volume's row sums
+ * [N*C*2] (as gn3d_backward_sums defines them): with M = group_count (the
+ * elements of one group of the whole volume), per group a = A/M, b = B/M with
+ * A = sum_c gamma_c*S1_c, B = rstd * sum_c gamma_c*S2_c, and dx = rstd*((dy*gamma
+ * - a) - xhat*b); dgamma_c = sum_n rstd*S2, dbeta_c = sum_n S1 (either may be
+ * NULL).  GN3D_ERR_INVALID_ARG if group_count < 1. */
+int gn3d_backward_dx_from_sums(const void* dy, const void* x, const float* mean, const float* rstd,
+                               const float* gamma, const float* sums, int64_t group_count, int64_t N, int64_t C,
+                               int64_t D, int64_t H, int64_t W, int64_t G, gn3d_dtype dtype, void* dx,
+                               float* dgamma, float* dbeta, void* stream);
+
+/*
  * Synchronizes `stream`, then returns and clears the device-side error word
  * that bounded waits inside the kernels set (GN3D_ERR_TIMEOUT), or
  * GN3D_ERR_CUDA if the stream reports a CUDA error, else GN3D_OK.
