@@ -34,7 +34,10 @@ METRIC = "GroupNorm fwd+bwd effective HBM GB/s (bf16, 128³/256³) and % of 8 TB
 UNIT = "GB/s"
 NOMINAL_HBM_GBS = 8000.0
 DEFAULT_WORKLOAD = "bf16_1x32x128^3_G8"
-SECONDARY = ["bf16_1x32x256^3_G8"]
+# the other configurations of the workload list, timed the same way (the
+# headline's metric on each); the 1e3-offset variant probes variance cancellation
+SECONDARY = ["bf16_1x32x256^3_G8", "fp32_2x16x16^3_G4", "bf16_2x64x96^3_G32", "bf16_2x64x96^3_G32_offset1e3"]
+SPREAD_STEPS = 200  # a second, longer pass for the distribution of per-step times
 UNET = "bf16_unet_stack_G8"  # the UNet's GroupNorm sites, reported per site and rolled up
 FLUSH_BYTES = 256 << 20
 
@@ -516,6 +519,13 @@ def run_gpu(args):
     # events sit between the kernels, so this pass is kept apart from `value`)
     ktot, _, _, kernels = time_device([vol], args.steps, 1, flush, stream, kernel_timing=True)
     kstep_ms = sum(ktot) / len(ktot)
+    # the distribution of per-step times: the K timed steps, and a longer pass
+    spread, _, _ = time_device([vol], SPREAD_STEPS, 3, flush, stream)
+
+    def dist_of(v):
+        v = sorted(v)
+        return {"n": len(v), "median_ms": round(statistics.median(v), 4), "min_ms": round(v[0], 4),
+                "max_ms": round(v[-1], 4)}
     ms = sum(tot) / len(tot)
     ms = max_over_ranks(ms, ws, dev)
     fb, bb = site.min_bytes()
@@ -563,7 +573,8 @@ def run_gpu(args):
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "vs_baseline": None, "dtype": site.dtype, "data": "synthetic",
+            "per_step": dist_of(tot), "per_step_long": dist_of(spread),
             "config": {"workload": args.workload, "N": site.N, "C": site.C, "D": site.D, "H": site.H,
                        "W": site.W, "G": site.G, "eps": site.eps, "parallelism": f"replicas x{ws}",
                        "min_bytes_per_step": fb + bb, "l2": "flushed between steps (256 MiB write)",
@@ -616,7 +627,9 @@ def run_reference(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
             "config": {"workload": args.workload, "N": site.N, "C": site.C, "D": site.D, "H": site.H,
-                       "W": site.W, "G": site.G, "sample": what},
+                       "W": site.W, "G": site.G, "eps": site.eps, "parallelism": f"replicas x{ws}",
+                       "min_bytes_per_step": sum(site.min_bytes()), "l2": "flushed between steps (256 MiB write)",
+                       "path": "auto", "layout": "ncdhw", "sample": what},
             "cpu_baseline": {"value": round(v, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": what + " per step, fwd+bwd"},
             "e2e": {"value": round(v, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}

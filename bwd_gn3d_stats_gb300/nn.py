@@ -13,9 +13,17 @@ with no layout conversion; any other input runs the NCDHW entry points on its
 contiguous form.  The NDHWC kernels need C % 8 == 0; other channel counts take
 the NCDHW path.
 
+Gradient dtype: the backward runs in x's dtype when the incoming gradient has
+it (or is narrower: a bf16 gradient of an fp32 input widens exactly).  With
+out_dtype=float32 on a bf16 input the incoming gradient is fp32; it is not
+narrowed -- the backward then runs on fp32 copies of x (exact) and of the
+gradient, and dx is rounded once to bf16, so no gradient precision is lost
+before the backward's sums (PR #105 "Preserve GroupNorm dtype": compute in
+fp32, round once on the store).
+
 Every computation runs in libgn3d's kernels: this file only allocates outputs,
-saves what the backward needs and converts the incoming gradient to x's dtype
-and layout.  There is no CPU path -- a CPU tensor raises.
+saves what the backward needs and converts the incoming gradient to the
+backward's dtype and layout.  There is no CPU path -- a CPU tensor raises.
 """
 from __future__ import annotations
 
@@ -73,12 +81,19 @@ class GroupNorm3dFunction(torch.autograd.Function):
     @staticmethod
     def backward(ctx, dy):
         x, w, mean, rstd, y = ctx.saved_tensors
+        xb = x
+        if dy.dtype == torch.float32 and x.dtype == torch.bfloat16:
+            # an fp32 gradient of a bf16 input (out_dtype=float32): keep it; the
+            # backward runs on x widened to fp32 (exact) and dx is rounded once
+            xb = x.float()
+        mf = torch.channels_last_3d if ctx.ndhwc else torch.contiguous_format
+        dy = _aligned(dy.to(xb.dtype), mf)
+        xb = _aligned(xb, mf)
         if ctx.ndhwc:
-            dy = _aligned(dy.to(x.dtype), torch.channels_last_3d)
-            dx, dgamma, dbeta = _backward_ndhwc(dy, x, mean, rstd, w, ctx.num_groups, out=y if ctx.relu else None)
+            dx, dgamma, dbeta = _backward_ndhwc(dy, xb, mean, rstd, w, ctx.num_groups, out=y if ctx.relu else None)
         else:
-            dy = _aligned(dy.to(x.dtype))
-            dx, dgamma, dbeta = _backward(dy, x, mean, rstd, w, ctx.num_groups, out=y if ctx.relu else None)
+            dx, dgamma, dbeta = _backward(dy, xb, mean, rstd, w, ctx.num_groups, out=y if ctx.relu else None)
+        dx = dx.to(x.dtype)
         gw = dgamma.to(ctx.weight_dtype) if ctx.weight_dtype is not None and ctx.needs_input_grad[1] else None
         gb = dbeta.to(ctx.bias_dtype) if ctx.bias_dtype is not None and ctx.needs_input_grad[2] else None
         return dx, gw, gb, None, None, None, None

@@ -161,3 +161,37 @@ def test_misaligned_views_are_handled():
     xr3 = x.clone().requires_grad_()
     group_norm_3d(xr3, 4, w, b).backward(dy.clone())
     assert t.equal(xr2.grad.view(t.int16), xr3.grad.view(t.int16))
+
+
+@pytest.mark.parametrize("channels_last", [False, True])
+def test_fp32_gradient_of_bf16_input_is_not_narrowed(channels_last):
+    """out_dtype=float32 on a bf16 input: the fp32 gradient reaches the backward
+    unrounded (the backward runs on x widened exactly to fp32), and dx is
+    rounded once to bf16 -- not the backward of the gradient rounded to bf16."""
+    from bwd_gn3d_stats_gb300.nn import GroupNorm3d
+
+    t = torch()
+    g = t.Generator(device="cuda").manual_seed(9)
+    x = (t.randn((2, 16, 6, 7, 8), generator=g, device="cuda") * 2 + 1).to(t.bfloat16)
+    if channels_last:
+        x = x.contiguous(memory_format=t.channels_last_3d)
+    dy = t.randn((2, 16, 6, 7, 8), generator=g, device="cuda") * (1 + 2 ** -12)  # not bf16 values
+    m = GroupNorm3d(4, 16, out_dtype=t.float32).cuda()
+    with t.no_grad():
+        m.weight.uniform_(0.5, 1.5)
+        m.bias.normal_(0, 0.1)
+    xr = x.detach().requires_grad_(True)
+    y = m(xr)
+    assert y.dtype == t.float32
+    y.backward(dy)
+    # the same backward through the C ABI on the widened input and the fp32 gradient
+    xf = x.float().contiguous(memory_format=t.channels_last_3d if channels_last else t.contiguous_format)
+    _, mean, rstd = (gn.forward_ndhwc if channels_last else gn.forward)(x, m.weight.detach(), m.bias.detach(), 4,
+                                                                       1e-5, t.float32)
+    fn = gn.backward_ndhwc if channels_last else gn.backward
+    mf = t.channels_last_3d if channels_last else t.contiguous_format
+    dx32, dg32, db32 = fn(dy.contiguous(memory_format=mf), xf, mean, rstd, m.weight.detach(), 4)
+    assert same(xr.grad, dx32.to(t.bfloat16)) and same(m.weight.grad, dg32) and same(m.bias.grad, db32)
+    # and it differs from the backward of the gradient narrowed to bf16
+    _, dgn, _ = fn(dy.to(t.bfloat16).contiguous(memory_format=mf), x, mean, rstd, m.weight.detach(), 4)
+    assert not same(m.weight.grad, dgn)
