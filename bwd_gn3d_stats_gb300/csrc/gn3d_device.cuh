@@ -756,35 +756,52 @@ __device__ __forceinline__ float2 unit_bwd_sums(const View& ux, const View& ud, 
 }
 
 // Group finalize of the backward, by one warp: per-row totals of the block sums
-// (lane l takes blocks l, l+32, ... of the row, then the butterfly), then
+// (rows of more than 32 blocks: lane l takes blocks l, l+32, ... of the row,
+// then the butterfly; shorter rows: one lane per row, below), then
 // A = sum_c gamma_c*S1_c and B = rstd * sum_c gamma_c*S2_c in channel order;
 // a = A/M and b = B/M.
 __device__ __forceinline__ void bwd_group(const Plan& p, const BwdWs& ws, int64_t g, const float* rstd,
                                           const float* gamma) {
   const int lane = threadIdx.x & 31;
   float A = 0.f, B = 0.f;
-  // rows of at most 32 blocks: each lane holds one block of a row, so the loads
-  // of kMergeBatch rows go out together (a group of many short rows would
-  // otherwise wait out one L2 round trip per row); the sums are the same
-  for (int64_t cl0 = 0; p.nb <= 32 && cl0 < p.Cg; cl0 += kMergeBatch) {
-    float2 v[kMergeBatch];
-    float gm[kMergeBatch];
+  // rows of at most 32 blocks: lane c takes row c of each pass of 32 rows and
+  // forms the row's totals as warp_sum2 would with lane k holding block k
+  // (lanes >= nb zero) -- the xor butterfly's additions on the same operands,
+  // so the same bits -- then every lane takes the pass's totals in channel
+  // order from the row lanes.  A group of many short rows costs one L2 round
+  // trip per pass, not one butterfly and round trip per row.
+  for (int64_t cl0 = 0; p.nb <= 32 && cl0 < p.Cg; cl0 += 32) {
+    const int64_t cl = cl0 + lane;
+    float2 t = make_float2(0.f, 0.f);
+    float gm = 1.f;
+    if (cl < p.Cg) {
+      const int64_t row = g * p.Cg + cl;
+      const float2* bp = ws.bparts + row * p.nb;
+      float bx[16], by[16];
 #pragma unroll
-    for (int j = 0; j < kMergeBatch; ++j) {
-      const int64_t cl = cl0 + j, row = g * p.Cg + cl;
-      v[j] = cl < p.Cg && lane < p.nb ? __ldcg(ws.bparts + row * p.nb + lane) : make_float2(0.f, 0.f);
-      gm[j] = cl < p.Cg && gamma ? gamma[(g % p.G) * p.Cg + cl] : 1.f;
+      for (int k = 0; k < 16; ++k) {
+        const float2 lo = k < p.nb ? __ldcg(bp + k) : make_float2(0.f, 0.f);
+        const float2 hi = k + 16 < p.nb ? __ldcg(bp + k + 16) : make_float2(0.f, 0.f);
+        bx[k] = fadd(k < p.nb ? fadd(0.f, lo.x) : 0.f, k + 16 < p.nb ? fadd(0.f, hi.x) : 0.f);
+        by[k] = fadd(k < p.nb ? fadd(0.f, lo.y) : 0.f, k + 16 < p.nb ? fadd(0.f, hi.y) : 0.f);
+      }
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1)
+#pragma unroll
+        for (int k = 0; k < o; ++k) {
+          bx[k] = fadd(bx[k], bx[k + o]);
+          by[k] = fadd(by[k], by[k + o]);
+        }
+      t = make_float2(bx[0], by[0]);
+      ws.rows[row] = t;
+      gm = gamma ? gamma[(g % p.G) * p.Cg + cl] : 1.f;
     }
-#pragma unroll
-    for (int j = 0; j < kMergeBatch; ++j) {
-      const int64_t cl = cl0 + j;
-      if (cl >= p.Cg) break;
-      const float s1 = lane < p.nb ? fadd(0.f, v[j].x) : 0.f;
-      const float s2 = lane < p.nb ? fadd(0.f, v[j].y) : 0.f;
-      const float2 t = warp_sum2(s1, s2);
-      if (lane == 0) ws.rows[g * p.Cg + cl] = t;
-      A = fadd(A, fmul(gm[j], t.x));
-      B = fadd(B, fmul(gm[j], t.y));
+    const int nr = p.Cg - cl0 < 32 ? (int)(p.Cg - cl0) : 32;
+    for (int j = 0; j < nr; ++j) {
+      const float tx = __shfl_sync(kFull, t.x, j), ty = __shfl_sync(kFull, t.y, j);
+      const float gj = __shfl_sync(kFull, gm, j);
+      A = fadd(A, fmul(gj, tx));
+      B = fadd(B, fmul(gj, ty));
     }
   }
   for (int64_t cl = 0; p.nb > 32 && cl < p.Cg; ++cl) {

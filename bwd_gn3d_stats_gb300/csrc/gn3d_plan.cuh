@@ -303,9 +303,12 @@ struct UnitWalkDown {
 
 // Unit shares pay two cut blocks per worker and suit large tensors (contiguous
 // runs per SM); they are used when shares hold two merge blocks or more on
-// average, strided blocks otherwise.
+// average, and when there are so few merge blocks (a third of the workers or
+// fewer) that strided blocks would leave most warps idle and the rest each a
+// long serial run; strided blocks otherwise.
 __host__ __device__ inline bool use_unit_shares(const Plan& p, int64_t nw) {
-  return p.units >= 2 * kBlockUnits * nw;
+  const int64_t nblk = p.NC * p.nb;
+  return p.units >= 2 * kBlockUnits * nw || (3 * nblk <= nw && p.units > nblk);
 }
 
 }  // namespace gn3d

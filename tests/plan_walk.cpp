@@ -572,6 +572,11 @@ static void layouts_of_the_bench_volumes() {
   CHECK(!use_unit_shares(make_plan(2, 64, 96 * 96 * 96, 32), nw));
   CHECK(!use_unit_shares(make_plan(1, 48, 97 * 97 * 97, 8), nw));
   CHECK(use_unit_shares(make_plan(1, 32, 256 * 256 * 256, 8), nw));
+  // few merge blocks: 256 rows of 8 units (shares), 512 rows of one unit (no
+  // unit to share out), 512 blocks of 16 units (strided)
+  CHECK(use_unit_shares(make_plan(1, 256, 32 * 32 * 32, 8), nw));
+  CHECK(!use_unit_shares(make_plan(1, 512, 16 * 16 * 16, 8), nw));
+  CHECK(!use_unit_shares(make_plan(1, 128, 64 * 64 * 64, 8), nw));
 }
 
 int main() {
