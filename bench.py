@@ -240,6 +240,7 @@ def time_device(vols, steps, warmup, flush, stream, kernel_timing=False):
 # size: what it must read and write at least (re-reads from L2 are not counted).
 KERNEL_TENSORS = {"k_fwd_fused": 2, "k_fwd_stats": 1, "k_fwd_norm": 2,
                   "k_bwd_fused": 3, "k_bwd_reduce": 2, "k_bwd_dx": 3, "k_fwd_resident": 2, "k_bwd_resident": 3,
+                  "k_fwd_cluster": 2, "k_bwd_cluster": 3,
                   "k_ndhwc_stats": 1, "k_ndhwc_stats_final": 0, "k_ndhwc_norm": 2,
                   "k_ndhwc_reduce": 2, "k_ndhwc_reduce_final": 0, "k_ndhwc_dx": 3}
 

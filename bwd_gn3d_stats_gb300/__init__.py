@@ -332,7 +332,7 @@ def backward(dy, x, mean, rstd, gamma, G: int, out=None):
 
 (DEBUG_PATH, DEBUG_SPIN_LIMIT, DEBUG_FORCE_TIMEOUT, DEBUG_LAG, DEBUG_SLOTS) = range(5)
 (DEBUG_SHARES, DEBUG_RES_HELD, DEBUG_RES_WINDOW, DEBUG_RES_PASS, DEBUG_FAIL_NEXT) = range(6, 11)
-PATH_AUTO, PATH_STREAMING, PATH_FUSED, PATH_RESIDENT = 0, 1, 2, 3
+PATH_AUTO, PATH_STREAMING, PATH_FUSED, PATH_RESIDENT, PATH_CLUSTER = 0, 1, 2, 3, 4
 FAIL_NONE, FAIL_ALLOC, FAIL_LAUNCH = 0, 1, 2
 DEBUG_POOL_USED = 0
 
@@ -357,7 +357,7 @@ def gn3d_debug_get(what: int) -> int:
 
 KERNELS = ("k_fwd_fused", "k_bwd_fused", "k_fwd_stats", "k_fwd_norm", "k_bwd_reduce", "k_bwd_dx",
            "k_ndhwc_stats", "k_ndhwc_stats_final", "k_ndhwc_norm", "k_ndhwc_reduce", "k_ndhwc_reduce_final",
-           "k_ndhwc_dx", "k_fwd_resident", "k_bwd_resident")
+           "k_ndhwc_dx", "k_fwd_resident", "k_bwd_resident", "k_fwd_cluster", "k_bwd_cluster")
 
 
 def gn3d_timing(on: bool):

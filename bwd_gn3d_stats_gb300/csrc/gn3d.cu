@@ -18,6 +18,7 @@
 #include <vector>
 
 #include "../../include/gn3d.h"
+#include "gn3d_cluster.cuh"
 #include "gn3d_fused.cuh"
 #include "gn3d_kernels.cuh"
 #include "gn3d_ndhwc.cuh"
@@ -36,7 +37,7 @@ thread_local std::string g_msg;
 std::atomic<uint64_t> g_launches{0};
 
 // testing / tuning hooks (gn3d_debug_set)
-std::atomic<long long> g_hook_path{0};     // 0 auto (streaming), 1 streaming kernels, 2 fused kernels
+std::atomic<long long> g_hook_path{0};  // 0 auto, 1 streaming, 2 persistent, 3 group-wave, 4 cluster
 std::atomic<long long> g_hook_spin{0};     // 0 default poll budget
 std::atomic<long long> g_hook_timeout{0};  // 1: the next fused launch waits on a flag nothing sets
 std::atomic<long long> g_hook_lag{-1};     // -1 auto
@@ -199,12 +200,13 @@ int64_t rup(int64_t b) { return ((b + 255) / 256) * 256; }
 enum {
   KK_FWD_FUSED, KK_BWD_FUSED, KK_FWD_STATS, KK_FWD_NORM, KK_BWD_REDUCE, KK_BWD_DX,
   KK_N_STATS, KK_N_STATS_FINAL, KK_N_NORM, KK_N_REDUCE, KK_N_REDUCE_FINAL, KK_N_DX, KK_FWD_RES, KK_BWD_RES,
+  KK_FWD_CLUSTER, KK_BWD_CLUSTER,
   KK_COUNT
 };
 const char* const kKernelNames[KK_COUNT] = {
     "k_fwd_fused",   "k_bwd_fused",         "k_fwd_stats",  "k_fwd_norm",     "k_bwd_reduce",
     "k_bwd_dx",      "k_ndhwc_stats",       "k_ndhwc_stats_final", "k_ndhwc_norm", "k_ndhwc_reduce",
-    "k_ndhwc_reduce_final", "k_ndhwc_dx", "k_fwd_resident", "k_bwd_resident"};
+    "k_ndhwc_reduce_final", "k_ndhwc_dx", "k_fwd_resident", "k_bwd_resident", "k_fwd_cluster", "k_bwd_cluster"};
 std::atomic<int> g_timing{0};
 std::mutex g_tmu;
 struct TimedLaunch {
@@ -263,6 +265,13 @@ unsigned long long spin_budget() {
 }
 
 bool use_fused() { return g_hook_path.load() == 2; }
+
+// The cluster kernels run wherever they apply, unless a testing hook picks
+// another launch form (path 4 asks for them explicitly).
+bool want_cluster() {
+  const long long h = g_hook_path.load();
+  return h == 0 || h == 4;
+}
 
 // The group-wave (resident) kernels: every unit full, enough units for every
 // SM to hold a share of each group most of the time.
@@ -353,6 +362,108 @@ int raise_smem(const void* func, int bytes, const DevInfo& di) {
   return GN3D_OK;
 }
 
+// How many clusters of cs CTAs with `smem` bytes of shared memory each kernel
+// `k` can have resident at once on this device (0: none): its attributes
+// raised, then the occupancy calculator asked.  The answer is kept per kernel,
+// cluster size and shared memory; a refusal is an answer (the call takes
+// another launch form), so its error is cleared.
+struct ClusterFit {
+  const void* k;
+  int cs, smem, active;
+};
+std::vector<ClusterFit> g_cluster_fit[kMaxDevices];
+
+int cluster_active(const void* k, int cs, int smem, DevInfo& di) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (const ClusterFit& f : g_cluster_fit[di.dev])
+      if (f.k == k && f.cs == cs && f.smem == smem) return f.active;
+  }
+  int n = 0;
+  bool ok = smem <= di.smem_optin && raise_smem(k, smem, di) == GN3D_OK;
+  if (ok && cs > 8) ok = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+  if (ok) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cs);
+    cfg.blockDim = dim3(32 * kClusterWarps);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cudaLaunchAttribute a[1];
+    a[0].id = cudaLaunchAttributeClusterDimension;
+    a[0].val.clusterDim.x = cs;
+    a[0].val.clusterDim.y = 1;
+    a[0].val.clusterDim.z = 1;
+    cfg.attrs = a;
+    cfg.numAttrs = 1;
+    ok = cudaOccupancyMaxActiveClusters(&n, k, &cfg) == cudaSuccess;
+  }
+  if (!ok) {
+    n = 0;
+    cudaGetLastError();
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_cluster_fit[di.dev].push_back(ClusterFit{k, cs, smem, n});
+  return n;
+}
+
+// The cluster form runs only when every group's cluster is resident at once:
+// a second wave of clusters costs more than the streaming kernels' second pass
+// (measured: 256 channels at 32^3, 7 of 8 clusters resident, 26 against 23 us).
+bool cluster_one_wave(const void* k, const Plan& p, int cs, int smem, DevInfo& di) {
+  return smem > 0 && p.NG <= (int64_t)cluster_active(k, cs, smem, di);
+}
+
+// A launch in clusters of cs CTAs (one cluster per group).
+template <class... KArgs, class... Args>
+cudaError_t launch_cluster(void (*k)(KArgs...), int grid, int cs, int smem, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(32 * kClusterWarps);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = st;
+  cudaLaunchAttribute a[1];
+  a[0].id = cudaLaunchAttributeClusterDimension;
+  a[0].val.clusterDim.x = cs;
+  a[0].val.clusterDim.y = 1;
+  a[0].val.clusterDim.z = 1;
+  cfg.attrs = a;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, args...);
+}
+
+// The cluster form's shared memory per CTA for a plan, or 0 where it does not
+// apply: whole units only, and the CTA's units, their results and the group's
+// block results must fit.
+template <class T, int kTensors, class V>
+int cluster_smem(const Plan& p, const ClusterGeo& c, const DevInfo& di) {
+  if (!plan_all_full(p) || p.NG < 1 || c.upc < 1 || p.NG * c.cs > (int64_t)0x7fffffff) return 0;
+  const int64_t b = ClusterLayout<T, kTensors, V>::bytes(c.upc, c.nbg);
+  return b <= di.smem_optin ? (int)b : 0;
+}
+
+// The forward in one cluster launch, where it applies (*done); nothing is
+// allocated.
+template <class TI, class TO>
+int launch_forward_cluster(const void* x, const float* gamma, const float* beta, const Plan& p, float eps, void* y,
+                           float* mean, float* rstd, cudaStream_t st, DevInfo& di, bool relu, bool* done) {
+  *done = false;
+  if (!want_cluster()) return GN3D_OK;
+  const ClusterGeo c = cluster_geo(p);
+  const int smem = cluster_smem<TI, 1, Part>(p, c, di);
+  auto k = relu ? k_fwd_cluster<TI, TO, true> : k_fwd_cluster<TI, TO, false>;
+  if (!cluster_one_wave((const void*)k, p, c.cs, smem, di)) return GN3D_OK;
+  *done = true;
+  cudaError_t e = injected_launch_error();
+  if (e == cudaSuccess) {
+    g_launches += 1;
+    LaunchTimer tm(KK_FWD_CLUSTER, st, di);
+    e = launch_cluster(k, (int)(p.NG * c.cs), c.cs, smem, st, static_cast<const TI*>(x), static_cast<TO*>(y), p, c,
+                       eps, gamma, beta, mean, rstd, spin_budget(), di.status, g_hook_timeout.exchange(0) != 0 ? 1 : 0);
+    tm.done();
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+  return GN3D_OK;
+}
+
 // Launch of a kernel that may start before the previous kernel on the stream
 // has finished (programmatic dependent launch); it waits in-kernel (pdl_wait)
 // before reading that kernel's results.
@@ -399,6 +510,9 @@ auto norm_kernel(bool full, bool relu, bool cut) {
 template <class TI, class TO>
 int launch_forward(const void* x, const float* gamma, const float* beta, const Plan& p, float eps, void* y,
                    float* mean, float* rstd, cudaStream_t st, DevInfo& di, bool relu) {
+  bool done = false;
+  const int rc = launch_forward_cluster<TI, TO>(x, gamma, beta, p, eps, y, mean, rstd, st, di, relu, &done);
+  if (done) return rc;
   const bool fused = use_fused() && !relu;  // the fused ReLU runs in the streaming kernels
   const int64_t nblk = p.NC * p.nb;
   const int64_t nsync = nblk + 2 * p.NG + 2;  // bcnt, gcnt, ready, abort, never
@@ -548,7 +662,16 @@ int launch_backward(const void* dy, const void* x, const void* res, const float*
   const T* dyp = static_cast<const T*>(dy);
   const T* xp = static_cast<const T*>(x);
   T* dxp = static_cast<T*>(dx);
-  if (e == cudaSuccess && !res && sizeof(T) == 2 && use_resident(p, di)) {
+  const ClusterGeo cg = cluster_geo(p);
+  const int csmem = !res && want_cluster() ? cluster_smem<T, 2, float2>(p, cg, di) : 0;
+  if (e == cudaSuccess && cluster_one_wave((const void*)k_bwd_cluster<T>, p, cg.cs, csmem, di)) {
+    g_launches += 1;
+    LaunchTimer tm(KK_BWD_CLUSTER, st, di);
+    e = launch_cluster(k_bwd_cluster<T>, (int)(p.NG * cg.cs), cg.cs, csmem, st, dyp, xp, dxp, p, cg, mean, rstd,
+                       gamma, w.rows, w.done, dgamma, dbeta, spin_budget(), di.status,
+                       g_hook_timeout.exchange(0) != 0 ? 1 : 0);
+    tm.done();
+  } else if (e == cudaSuccess && !res && sizeof(T) == 2 && use_resident(p, di)) {
     int smem = 0;
     using Shape = ResBwdShape<T>;
     using Lay = ResLayout<Shape::kSlotBytes, float2, Shape::kRound>;
@@ -1388,7 +1511,7 @@ extern "C" int gn3d_stream_status(void* stream) {
 extern "C" int gn3d_debug_set(int what, long long value) {
   switch (what) {
     case GN3D_DEBUG_PATH:
-      if (value < 0 || value > 3) return arg_fail("path: 0 .. 3");
+      if (value < 0 || value > 4) return arg_fail("path: 0 .. 4");
       g_hook_path = value;
       break;
     case GN3D_DEBUG_SPIN_LIMIT:

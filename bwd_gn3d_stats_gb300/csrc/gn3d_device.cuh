@@ -444,12 +444,14 @@ __device__ __forceinline__ Part merge_lanes(const Part a, int n) {
   return finish_merge(K, t.x, t.y, n);
 }
 
-// Group merge of its Cg*nb block partials (contiguous), by one warp: lane l takes
-// blocks l, l+32, ... in order, then the butterfly.  Returns the group's moments
-// (mean = m1 + cn, M2).
-__device__ __forceinline__ Part merge_group_part(const Part* blocks, int64_t nblk, int64_t M) {
+// Group merge of its Cg*nb block partials, by one warp: lane l takes blocks l,
+// l+32, ... in order, then the butterfly.  Returns the group's moments (mean =
+// m1 + cn, M2).  ld(i) gives block i's partial (from global memory, or from
+// shared memory in the cluster kernels).
+template <class Load>
+__device__ __forceinline__ Part merge_group_part_from(Load ld, int64_t nblk, int64_t M) {
   const int lane = threadIdx.x & 31;
-  const Part b0 = ldcg_part(blocks);
+  const Part b0 = ld(0);
   const float K = fadd(b0.m1, b0.cn);
   float S = 0.f, Q = 0.f;
   // loads in batches of kMergeBatch (independent), sums in the same order
@@ -457,7 +459,7 @@ __device__ __forceinline__ Part merge_group_part(const Part* blocks, int64_t nbl
     Part v[kMergeBatch];
 #pragma unroll
     for (int j = 0; j < kMergeBatch; ++j)
-      if (i0 + 32 * j < nblk) v[j] = ldcg_part(blocks + i0 + 32 * j);
+      if (i0 + 32 * j < nblk) v[j] = ld(i0 + 32 * j);
 #pragma unroll
     for (int j = 0; j < kMergeBatch; ++j) {
       if (i0 + 32 * j < nblk) {
@@ -470,6 +472,11 @@ __device__ __forceinline__ Part merge_group_part(const Part* blocks, int64_t nbl
   }
   const float2 t = warp_sum2(S, Q);
   return finish_merge(K, t.x, t.y, M);
+}
+
+// The group merge of Cg*nb contiguous block partials in global memory.
+__device__ __forceinline__ Part merge_group_part(const Part* blocks, int64_t nblk, int64_t M) {
+  return merge_group_part_from([&](int64_t i) { return ldcg_part(blocks + i); }, nblk, M);
 }
 
 // A group's statistics from its moments over M elements: (mean hi, mean lo,
@@ -759,9 +766,11 @@ __device__ __forceinline__ float2 unit_bwd_sums(const View& ux, const View& ud, 
 // (rows of more than 32 blocks: lane l takes blocks l, l+32, ... of the row,
 // then the butterfly; shorter rows: one lane per row, below), then
 // A = sum_c gamma_c*S1_c and B = rstd * sum_c gamma_c*S2_c in channel order;
-// a = A/M and b = B/M.
-__device__ __forceinline__ void bwd_group(const Plan& p, const BwdWs& ws, int64_t g, const float* rstd,
-                                          const float* gamma) {
+// returns (a, b) = (A/M, B/M).  ld(i) gives block i of the group (row-major:
+// row cl, block kb at cl*nb + kb); row(cl, t) receives row cl's totals.
+template <class Load, class Row>
+__device__ __forceinline__ float2 bwd_group_from(const Plan& p, int64_t g, const float* rstd, const float* gamma,
+                                                 Load ld, Row row) {
   const int lane = threadIdx.x & 31;
   float A = 0.f, B = 0.f;
   // rows of at most 32 blocks: lane c takes row c of each pass of 32 rows and
@@ -775,13 +784,12 @@ __device__ __forceinline__ void bwd_group(const Plan& p, const BwdWs& ws, int64_
     float2 t = make_float2(0.f, 0.f);
     float gm = 1.f;
     if (cl < p.Cg) {
-      const int64_t row = g * p.Cg + cl;
-      const float2* bp = ws.bparts + row * p.nb;
+      const int64_t bb = cl * p.nb;
       float bx[16], by[16];
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
-        const float2 lo = k < p.nb ? __ldcg(bp + k) : make_float2(0.f, 0.f);
-        const float2 hi = k + 16 < p.nb ? __ldcg(bp + k + 16) : make_float2(0.f, 0.f);
+        const float2 lo = k < p.nb ? ld(bb + k) : make_float2(0.f, 0.f);
+        const float2 hi = k + 16 < p.nb ? ld(bb + k + 16) : make_float2(0.f, 0.f);
         bx[k] = fadd(k < p.nb ? fadd(0.f, lo.x) : 0.f, k + 16 < p.nb ? fadd(0.f, hi.x) : 0.f);
         by[k] = fadd(k < p.nb ? fadd(0.f, lo.y) : 0.f, k + 16 < p.nb ? fadd(0.f, hi.y) : 0.f);
       }
@@ -793,7 +801,7 @@ __device__ __forceinline__ void bwd_group(const Plan& p, const BwdWs& ws, int64_
           by[k] = fadd(by[k], by[k + o]);
         }
       t = make_float2(bx[0], by[0]);
-      ws.rows[row] = t;
+      row(cl, t);
       gm = gamma ? gamma[(g % p.G) * p.Cg + cl] : 1.f;
     }
     const int nr = p.Cg - cl0 < 32 ? (int)(p.Cg - cl0) : 32;
@@ -805,14 +813,13 @@ __device__ __forceinline__ void bwd_group(const Plan& p, const BwdWs& ws, int64_
     }
   }
   for (int64_t cl = 0; p.nb > 32 && cl < p.Cg; ++cl) {
-    const int64_t row = g * p.Cg + cl;
-    const float2* bp = ws.bparts + row * p.nb;
+    const int64_t bb = cl * p.nb;
     float s1 = 0.f, s2 = 0.f;
     for (int64_t i0 = lane; i0 < p.nb; i0 += 32 * kMergeBatch) {
       float2 v[kMergeBatch];
 #pragma unroll
       for (int j = 0; j < kMergeBatch; ++j)
-        if (i0 + 32 * j < p.nb) v[j] = __ldcg(bp + i0 + 32 * j);
+        if (i0 + 32 * j < p.nb) v[j] = ld(bb + i0 + 32 * j);
 #pragma unroll
       for (int j = 0; j < kMergeBatch; ++j) {
         if (i0 + 32 * j < p.nb) {
@@ -822,16 +829,29 @@ __device__ __forceinline__ void bwd_group(const Plan& p, const BwdWs& ws, int64_
       }
     }
     const float2 t = warp_sum2(s1, s2);
-    if (lane == 0) ws.rows[row] = t;
+    if (lane == 0) row(cl, t);
     const float gm = gamma ? gamma[(g % p.G) * p.Cg + cl] : 1.f;
     A = fadd(A, fmul(gm, t.x));
     B = fadd(B, fmul(gm, t.y));
   }
   B = fmul(rstd[g], B);
-  if (lane == 0) {
-    const float fM = (float)p.M;
-    ws.coef[g] = make_float2(__fdiv_rn(A, fM), __fdiv_rn(B, fM));
-  }
+  const float fM = (float)p.M;
+  return make_float2(__fdiv_rn(A, fM), __fdiv_rn(B, fM));
+}
+
+// The streaming kernels' group step: block sums from global memory, row totals
+// and (a, b) stored to the workspace.
+__device__ __forceinline__ void bwd_group(const Plan& p, const BwdWs& ws, int64_t g, const float* rstd,
+                                          const float* gamma) {
+  const float2* bp = ws.bparts + g * p.Cg * p.nb;
+  float2* rows = ws.rows + g * p.Cg;
+  const float2 ab = bwd_group_from(
+      p, g, rstd, gamma, [&](int64_t i) { return __ldcg(bp + i); }, [&](int64_t cl, float2 t) { rows[cl] = t; });
+  if ((threadIdx.x & 31) == 0) ws.coef[g] = ab;
+  // every lane's row stores before lane 0's release arrivals (the warp that
+  // completes the last group reads all rows for the parameter gradients)
+  __threadfence();
+  __syncwarp();
 }
 
 // dgamma_c = sum_n rstd[n,g] * S2[n,c], dbeta_c = sum_n S1[n,c], in n order, by one warp.

@@ -299,9 +299,15 @@ uint64_t gn3d_launch_count(void);
  * of them).  Process-wide, not thread-scoped; every setting defaults to
  * automatic.  None of them changes a result bit: every launch form runs the
  * same units and reduction trees.
- *   GN3D_DEBUG_PATH          0 automatic (the streaming kernels: two launches
- *                            per direction), 1 streaming, 2 persistent (one
- *                            cooperative launch per direction), 3 group-wave
+ *   GN3D_DEBUG_PATH          0 automatic (the cluster kernels where they
+ *                            apply -- whole 4096-element units, a group held
+ *                            in the shared memory of one cluster of at most 16
+ *                            CTAs, every group's cluster resident at once, no
+ *                            fused ReLU in the backward -- else the
+ *                            streaming kernels: two launches per direction),
+ *                            1 streaming, 2 persistent (one cooperative launch
+ *                            per direction), 4 cluster where they apply (else
+ *                            streaming), 3 group-wave
  *                            (one cooperative launch per direction; every CTA
  *                            holds a share of every group in shared memory
  *                            between the two passes; shapes whose rows are
@@ -313,8 +319,9 @@ uint64_t gn3d_launch_count(void);
  *                            whose wait gave up still waits for its own bulk
  *                            copies in flight with the default budget before
  *                            it exits.
- *   GN3D_DEBUG_FORCE_TIMEOUT 1: the next persistent launch (or the next
- *                            channels-last statistics launch with C <= 256)
+ *   GN3D_DEBUG_FORCE_TIMEOUT 1: the next persistent, group-wave or cluster
+ *                            launch (or the next channels-last statistics
+ *                            launch with C <= 256)
  *                            waits for a flag that nothing sets, so its bounded
  *                            wait runs out and gn3d_stream_status reports
  *                            GN3D_ERR_TIMEOUT (tests the failure path without a
@@ -379,7 +386,8 @@ int gn3d_timing(int on);
  * gn3d_timing(1) was last called.  `name` is one of "k_fwd_fused",
  * "k_bwd_fused", "k_fwd_stats", "k_fwd_norm", "k_bwd_reduce", "k_bwd_dx",
  * "k_ndhwc_stats", "k_ndhwc_stats_final", "k_ndhwc_norm", "k_ndhwc_reduce",
- * "k_ndhwc_reduce_final", "k_ndhwc_dx", "k_fwd_resident", "k_bwd_resident".
+ * "k_ndhwc_reduce_final", "k_ndhwc_dx", "k_fwd_resident", "k_bwd_resident",
+ * "k_fwd_cluster", "k_bwd_cluster".
  * Waits for the recorded events (host-blocking), then writes the total
  * milliseconds to *ms and the launch count to *launches.  Returns GN3D_OK,
  * GN3D_ERR_INVALID_ARG (NULL argument, unknown name) or GN3D_ERR_CUDA.

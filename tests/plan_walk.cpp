@@ -37,6 +37,7 @@
 #include "../bwd_gn3d_stats_gb300/csrc/gn3d_plan.cuh"
 #include "../bwd_gn3d_stats_gb300/csrc/gn3d_ndhwc_plan.cuh"
 #include "../bwd_gn3d_stats_gb300/csrc/gn3d_resident_plan.cuh"
+#include "../bwd_gn3d_stats_gb300/csrc/gn3d_cluster_plan.cuh"
 
 using namespace gn3d;
 
@@ -565,6 +566,52 @@ static void sim_resident_shapes() {
   }
 }
 
+// The cluster kernels' split of a group: the CTAs' block runs tile the group's
+// blocks in order; CTA-local unit j is unit ui of the run's blocks in block
+// order (consecutive units of a row); every unit of the group is visited
+// exactly once; upc is the largest CTA's unit count; the cluster size keeps a
+// block and two units per CTA on average.
+static void walk_cluster(int64_t N, int64_t C, int64_t S, int64_t G) {
+  g_what = "cluster";
+  const Plan p = make_plan(N, C, S, G);
+  if (!plan_all_full(p)) return;
+  const ClusterGeo c = cluster_geo(p);
+  CHECK(c.nbg == p.Cg * p.nb);
+  CHECK(c.cs >= 1 && c.cs <= kClusterMaxCTAs && (c.cs & (c.cs - 1)) == 0);
+  CHECK(c.cs == 1 || (c.cs <= c.nbg && 2 * c.cs <= p.upg));
+  CHECK(c.cs == kClusterMaxCTAs || 2 * c.cs > c.nbg || 4 * c.cs > p.upg);  // the largest such size
+  for (int64_t g : {(int64_t)0, p.NG - 1}) {
+    std::vector<int> seen((size_t)p.upg, 0);
+    int upc = 0;
+    int64_t prev = 0;
+    for (int r = 0; r < c.cs; ++r) {
+      const int64_t b0 = cl_block_begin(c.nbg, c.cs, r), b1 = cl_block_begin(c.nbg, c.cs, r + 1);
+      CHECK(b0 == prev && b1 >= b0);
+      prev = b1;
+      const int nu = cl_units(p, b0, b1);
+      if (nu > upc) upc = nu;
+      int64_t lastb = -1;
+      int lastui = -1;
+      for (int j = 0; j < nu; ++j) {
+        int64_t b, row, k;
+        int ui;
+        cl_unit(p, b0, j, b, ui);
+        CHECK(b >= b0 && b < b1 && ui >= 0 && ui < cl_block_units(p, b));
+        CHECK((b == lastb && ui == lastui + 1) || (b == lastb + 1 && ui == 0) || (j == 0 && b == b0 && ui == 0));
+        lastb = b;
+        lastui = ui;
+        cl_row_k(p, g, b, ui, row, k);
+        CHECK(row >= g * p.Cg && row < (g + 1) * p.Cg && k >= 0 && k < p.R);
+        CHECK(k / kBlockUnits == b % p.nb && row - g * p.Cg == b / p.nb);
+        seen[(size_t)((row - g * p.Cg) * p.R + k)] += 1;
+      }
+    }
+    CHECK(prev == c.nbg);
+    CHECK(upc == c.upc);
+    for (int v : seen) CHECK(v == 1);
+  }
+}
+
 static void layouts_of_the_bench_volumes() {
   g_what = "layouts";
   const int64_t nw = 152 * 8;
@@ -577,6 +624,11 @@ static void layouts_of_the_bench_volumes() {
   CHECK(use_unit_shares(make_plan(1, 256, 32 * 32 * 32, 8), nw));
   CHECK(!use_unit_shares(make_plan(1, 512, 16 * 16 * 16, 8), nw));
   CHECK(!use_unit_shares(make_plan(1, 128, 64 * 64 * 64, 8), nw));
+  // the cluster form's split at the UNet's small sites and the small fp32 volume
+  g_what = "cluster sizes";
+  CHECK(cluster_geo(make_plan(1, 512, 16 * 16 * 16, 8)).cs == 16 && cluster_geo(make_plan(1, 512, 4096, 8)).upc == 4);
+  CHECK(cluster_geo(make_plan(1, 256, 32 * 32 * 32, 8)).cs == 16 && cluster_geo(make_plan(1, 256, 32768, 8)).upc == 16);
+  CHECK(cluster_geo(make_plan(2, 16, 16 * 16 * 16, 4)).cs == 2 && cluster_geo(make_plan(2, 16, 4096, 4)).upc == 2);
 }
 
 int main() {
@@ -597,6 +649,16 @@ int main() {
           walk_shares(N, C, S, G);
           if (C % kNVec == 0) walk_ndhwc(N, C, S, G);
           ++shapes;
+        }
+      }
+  // whole-unit rows for the cluster split (rows of 1 .. 40 units)
+  for (int64_t C : Cs)
+    for (int64_t R : {1, 2, 3, 8, 15, 16, 17, 31, 33, 40})
+      for (int64_t G : {(int64_t)1, (int64_t)2, (int64_t)3, C / 8, C / 2, C}) {
+        if (G < 1 || C % G) continue;
+        for (int64_t N : {(int64_t)1, (int64_t)2}) {
+          g_shape[0] = N; g_shape[1] = C; g_shape[2] = R * kUnitElems; g_shape[3] = G;
+          walk_cluster(N, C, R * kUnitElems, G);
         }
       }
   if (g_rotated == 0) {

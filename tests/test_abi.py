@@ -219,10 +219,10 @@ def test_shipped_library_carries_no_test_hooks(L):
 
 def test_debug_settings_ranges(testing_build):
     # every hook accepts its documented range and rejects the rest; none needs a GPU
-    ok = {gn.DEBUG_PATH: (0, 1, 2, 3), gn.DEBUG_LAG: (-1, 0, 8), gn.DEBUG_SLOTS: (-1, 1, 32),
+    ok = {gn.DEBUG_PATH: (0, 1, 2, 3, 4), gn.DEBUG_LAG: (-1, 0, 8), gn.DEBUG_SLOTS: (-1, 1, 32),
           gn.DEBUG_SHARES: (-1, 0, 1), gn.DEBUG_SPIN_LIMIT: (0, 1 << 20), gn.DEBUG_RES_HELD: (-1, 0, 7),
           gn.DEBUG_RES_WINDOW: (-1, 1, 500), gn.DEBUG_RES_PASS: (-1, 1, 12), gn.DEBUG_FAIL_NEXT: (0, 1, 2)}
-    bad = {gn.DEBUG_PATH: (-1, 4), gn.DEBUG_LAG: (-2, 9), gn.DEBUG_SLOTS: (0, -2, 33),
+    bad = {gn.DEBUG_PATH: (-1, 5), gn.DEBUG_LAG: (-2, 9), gn.DEBUG_SLOTS: (0, -2, 33),
            gn.DEBUG_SHARES: (-2, 2), gn.DEBUG_SPIN_LIMIT: (-1,), gn.DEBUG_RES_HELD: (-2,),
            gn.DEBUG_RES_WINDOW: (-2, 0), gn.DEBUG_RES_PASS: (-2, 0), gn.DEBUG_FAIL_NEXT: (-1, 3)}
     for what, values in ok.items():

@@ -101,12 +101,13 @@ def test_outputs_stay_inside_their_buffers(name, shape, kw):
         assert g.intact(), f"{name}: a guard band around {what} was written"
 
 
-@pytest.mark.parametrize("path", ["fused", "resident"])
+@pytest.mark.parametrize("path", ["streaming", "fused", "resident", "cluster"])
 @pytest.mark.parametrize("shape", [(1, 48, 9, 9, 9, 8, synth.BF16), (2, 16, 16, 16, 16, 4, synth.F32),
-                                   (1, 32, 32, 32, 32, 8, synth.BF16)],
+                                   (1, 32, 32, 32, 32, 8, synth.BF16), (1, 512, 16, 16, 16, 8, synth.BF16)],
                          ids=lambda s: "x".join(map(str, s[:6])) + "_" + s[6])
 def test_other_launch_forms_stay_inside(path, shape, testing_build):
-    testing_build.gn3d_debug_set(testing_build.DEBUG_PATH, 2 if path == "fused" else 3)
+    testing_build.gn3d_debug_set(testing_build.DEBUG_PATH,
+                                 {"streaming": 1, "fused": 2, "resident": 3, "cluster": 4}[path])
     site = synth.Site(*shape)
     d = device_inputs(synth.make_inputs(site, seed=52))
     outs = run_guarded(site, d)

@@ -163,17 +163,19 @@ def test_determinism_and_dtype_independence():
     assert np.array_equal(to_np(dx32.to(t.bfloat16)), outs[0][3])
 
 
-@pytest.mark.parametrize("path", ["fused", "resident"])
+@pytest.mark.parametrize("path", ["streaming", "fused", "resident", "cluster"])
 @pytest.mark.parametrize("shape", [(2, 16, 16, 16, 16, 4, synth.F32), (1, 8, 24, 24, 24, 2, synth.BF16),
-                                   (1, 32, 16, 16, 32, 8, synth.BF16), (2, 6, 1, 1, 1, 6, synth.BF16)],
+                                   (1, 32, 16, 16, 32, 8, synth.BF16), (2, 6, 1, 1, 1, 6, synth.BF16),
+                                   (1, 128, 16, 16, 16, 8, synth.BF16)],
                          ids=lambda s: "x".join(map(str, s[:6])) + "_" + s[6])
 def test_parity_other_launch_forms(path, shape, testing_build):
-    """The persistent and the group-wave launch forms against the oracle directly
-    (not only against the streaming form); shapes the group-wave kernels do not
-    take run on the streaming kernels under that setting."""
+    """Each launch form against the oracle directly (not only against the
+    streaming form): streaming, persistent, group-wave and cluster kernels;
+    shapes a form does not take run on the streaming kernels under its setting."""
     gn = testing_build
     site = synth.Site(*shape)
-    gn.gn3d_debug_set(gn.DEBUG_PATH, gn.PATH_FUSED if path == "fused" else gn.PATH_RESIDENT)
+    gn.gn3d_debug_set(gn.DEBUG_PATH, {"streaming": gn.PATH_STREAMING, "fused": gn.PATH_FUSED,
+                                      "resident": gn.PATH_RESIDENT, "cluster": gn.PATH_CLUSTER}[path])
     full_parity(site, synth.make_inputs(site, seed=6))
 
 

@@ -1,4 +1,4 @@
-"""The launch forms (streaming, persistent and group-wave kernels) and every
+"""The launch forms (streaming, persistent, group-wave and cluster kernels) and every
 tuning setting give bit-identical results; the bounded-wait failure path
 reports GN3D_ERR_TIMEOUT and leaves the library usable.  (Run on the testing
 build of the library, which carries the hooks.)"""
@@ -93,7 +93,8 @@ def test_bounded_wait_timeout_reports_and_recovers():
     assert same(ref, run_all(site, d))
 
 
-@pytest.mark.parametrize("path,launches", [(gn.PATH_AUTO, 4), (gn.PATH_STREAMING, 4), (gn.PATH_FUSED, 2)])
+@pytest.mark.parametrize("path,launches", [(gn.PATH_AUTO, 2), (gn.PATH_STREAMING, 4), (gn.PATH_FUSED, 2),
+                                          (gn.PATH_CLUSTER, 2)])
 def test_launch_count(path, launches):
     site = synth.Site(1, 8, 16, 16, 16, 4, synth.BF16)
     d = device_inputs(synth.make_inputs(site, seed=14))
@@ -193,5 +194,95 @@ def test_group_wave_timeout_reports_and_recovers():
     L = gn.lib()
     assert L.gn3d_stream_status(st) == gn.ERR_TIMEOUT
     assert L.gn3d_stream_status(st) == gn.OK
+    gn.gn3d_debug_set(gn.DEBUG_SPIN_LIMIT, 0)
+    assert same(ref, run_all(site, d))
+
+
+# The cluster kernels (one cluster per group, the group held in the cluster's
+# shared memory): groups of 1 .. 64 rows, rows of 1, 3, 8, 17 (a second block
+# of one unit) units, 1 .. 16 CTAs per cluster, N > 1 (the parameter gradients
+# across clusters), fp32; the backward of the 17-unit rows holds too many units
+# per CTA and stays on the streaming kernels.
+CLUSTER = [
+    (1, 512, 16, 16, 16, 8, synth.BF16),
+    (1, 64, 16, 16, 16, 8, synth.BF16),
+    (2, 32, 32, 32, 32, 8, synth.BF16),
+    (1, 8, 17, 64, 64, 2, synth.BF16),
+    (1, 16, 16, 16, 16, 16, synth.BF16),
+    (3, 24, 8, 32, 48, 6, synth.BF16),
+    (2, 16, 16, 16, 16, 4, synth.F32),
+    (1, 12, 3, 64, 64, 3, synth.F32),
+]
+
+
+def _launches(site, d):
+    """Kernel launches of one forward and of one backward."""
+    n0 = gn.gn3d_launch_count()
+    y, mean, rstd = run_forward(site, d["x"], d["gamma"], d["beta"])
+    n1 = gn.gn3d_launch_count()
+    run_backward(site, d["dy"], d["x"], mean, rstd, d["gamma"])
+    torch().cuda.synchronize()
+    return n1 - n0, gn.gn3d_launch_count() - n1
+
+
+@pytest.mark.parametrize("shape", CLUSTER, ids=lambda s: "x".join(map(str, s[:6])) + "_" + s[6])
+def test_cluster_and_streaming_bit_identical(shape):
+    """The cluster kernels and the streaming kernels give the same bits: the
+    same units, merge blocks and group merges, the block results gathered in
+    distributed shared memory instead of global memory.  The cluster forward is
+    one launch; so is the backward where its units fit."""
+    site = synth.Site(*shape)
+    d = device_inputs(synth.make_inputs(site, seed=25))
+    gn.gn3d_debug_set(gn.DEBUG_PATH, gn.PATH_STREAMING)
+    a = run_all(site, d)
+    assert _launches(site, d) == (2, 2)
+    gn.gn3d_debug_set(gn.DEBUG_PATH, gn.PATH_CLUSTER)
+    b = run_all(site, d)
+    gn.gn3d_stream_status(torch().cuda.current_stream().cuda_stream)
+    assert same(a, b)
+    fwd, bwd = _launches(site, d)
+    assert fwd == 1
+    assert bwd == (2 if shape[2:5] == (17, 64, 64) else 1)
+    gn.gn3d_debug_set(gn.DEBUG_PATH, gn.PATH_AUTO)  # the automatic choice takes them too
+    assert _launches(site, d) == (fwd, bwd)
+
+
+def test_cluster_mixed_dtypes_relu_and_no_affine():
+    """bf16 -> fp32 and fp32 -> bf16 forwards, the fused ReLU forward, and no
+    affine parameters, on the cluster kernels, match the streaming kernels bit
+    for bit (the fused ReLU's backward stays on the streaming kernels)."""
+    site = synth.Site(1, 64, 16, 16, 16, 8, synth.BF16)
+    d = device_inputs(synth.make_inputs(site, seed=26))
+    outs = {}
+    for path in (gn.PATH_STREAMING, gn.PATH_CLUSTER):
+        gn.gn3d_debug_set(gn.DEBUG_PATH, path)
+        r = [to_np(t) for t in run_forward(site, d["x"], d["gamma"], d["beta"], out_dtype=synth.F32)]
+        r += [to_np(t) for t in run_forward_relu(site, d["x"], d["gamma"], d["beta"])]
+        y, mean, rstd = run_forward(site, d["x"], None, None)
+        r += [to_np(t) for t in (y, mean, rstd)]
+        r += [to_np(t) for t in run_backward(site, d["dy"], d["x"], mean, rstd, None)]
+        torch().cuda.synchronize()
+        outs[path] = r
+    assert same(outs[gn.PATH_STREAMING], outs[gn.PATH_CLUSTER])
+
+
+def test_cluster_timeout_reports_and_recovers():
+    site = synth.Site(1, 64, 16, 16, 16, 8, synth.BF16)
+    d = device_inputs(synth.make_inputs(site, seed=27))
+    ref = run_all(site, d)
+    st = torch().cuda.current_stream().cuda_stream
+    L = gn.lib()
+    gn.gn3d_debug_set(gn.DEBUG_PATH, gn.PATH_CLUSTER)
+    gn.gn3d_debug_set(gn.DEBUG_SPIN_LIMIT, 20000)
+    for direction in ("forward", "backward"):
+        y, mean, rstd = run_forward(site, d["x"], d["gamma"], d["beta"])
+        torch().cuda.synchronize()
+        gn.gn3d_debug_set(gn.DEBUG_FORCE_TIMEOUT, 1)
+        if direction == "forward":
+            run_forward(site, d["x"], d["gamma"], d["beta"])
+        else:
+            run_backward(site, d["dy"], d["x"], mean, rstd, d["gamma"])
+        assert L.gn3d_stream_status(st) == gn.ERR_TIMEOUT
+        assert L.gn3d_stream_status(st) == gn.OK
     gn.gn3d_debug_set(gn.DEBUG_SPIN_LIMIT, 0)
     assert same(ref, run_all(site, d))
