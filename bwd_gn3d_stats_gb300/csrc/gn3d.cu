@@ -1634,4 +1634,4 @@ extern "C" int gn3d_kernel_time(const char* name, double* ms, uint64_t* launches
   return GN3D_OK;
 }
 
-extern "C" const char* gn3d_version(void) { return "gn3d 0.3.0 sm_103a"; }
+extern "C" const char* gn3d_version(void) { return "gn3d 0.4.0 sm_103a"; }

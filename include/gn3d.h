@@ -394,7 +394,7 @@ int gn3d_timing(int on);
  */
 int gn3d_kernel_time(const char* name, double* ms, uint64_t* launches);
 
-/* Library version, e.g. "gn3d 0.3.0 sm_103a". */
+/* Library version, e.g. "gn3d 0.4.0 sm_103a". */
 const char* gn3d_version(void);
 
 #ifdef __cplusplus
