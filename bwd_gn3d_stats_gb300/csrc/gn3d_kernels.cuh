@@ -215,20 +215,30 @@ __global__ void __launch_bounds__(32 * FwdStatShape<TI>::kWarps, 1)
   ring.drain(kDrainPolls);
 }
 
-// Elementwise passes: 16 warps per CTA, on the reduction kernel's grid.  Warp w
-// takes the units of reduction warp w % kOwners of the same CTA, every
-// (16 / kOwners)-th, in the reverse of that warp's order (UnitWalkDown): what a
-// reduction warp read last is read again first, while it is still in L2.
-// Placement only decides what is found in L2, never a result.
+// Elementwise passes: 16 warps per CTA, on the reduction kernel's grid, each
+// taking units so that what the reduction read last is read again first, while
+// it is still in L2.  Under unit shares warp w takes the units of reduction
+// warp w % kOwners of the same CTA, every (16 / kOwners)-th, in the reverse of
+// that warp's order (UnitWalkDown).  Under strided blocks the units are spread
+// evenly over all the grid's warps, freshest first (UnitWalkFresh): a block is
+// one reduction warp's whole work there, so following the owner would leave
+// the warps of idle owners idle.  Placement only decides what is found in L2,
+// never a result.
 constexpr int kElemWarps = 16;
 
 template <int kOwners, bool kCut>
-__device__ __forceinline__ UnitWalkDown owned_units(const Plan& p) {
+__device__ __forceinline__ auto owned_units(const Plan& p) {
   const int warp = threadIdx.x >> 5;
-  UnitWalkDown w;
-  w.set(p, worker_index<kOwners>(kCut, warp % kOwners), (int64_t)gridDim.x * kOwners, kCut, warp / kOwners,
-        kElemWarps / kOwners);
-  return w;
+  if constexpr (kCut) {
+    UnitWalkDown w;
+    w.set(p, worker_index<kOwners>(kCut, warp % kOwners), (int64_t)gridDim.x * kOwners, kCut, warp / kOwners,
+          kElemWarps / kOwners);
+    return w;
+  } else {
+    UnitWalkFresh w;
+    w.set(p, (int64_t)warp * gridDim.x + blockIdx.x, (int64_t)gridDim.x * kElemWarps, (int64_t)gridDim.x * kOwners);
+    return w;
+  }
 }
 
 template <class TI, class TO, bool kFull, bool kRelu, bool kCut>
@@ -236,7 +246,7 @@ __global__ void __launch_bounds__(32 * kElemWarps, 1)
     k_fwd_norm(const TI* __restrict__ x, TO* __restrict__ y, Plan p, const float4* __restrict__ stats,
                const float* __restrict__ gamma, const float* __restrict__ beta) {
   constexpr bool kRegs = Vec<TI>::kRaw == 1;  // bf16: all 16 loads in flight before any use
-  UnitWalkDown w = owned_units<FwdStatShape<TI>::kWarps, kCut>(p);
+  auto w = owned_units<FwdStatShape<TI>::kWarps, kCut>(p);
   // The warp's first unit is read before the statistics kernel has finished
   // (x is not written there); everything the statistics kernel writes is read
   // after pdl_wait.
@@ -372,7 +382,7 @@ __global__ void __launch_bounds__(32 * kElemWarps, 1)
     k_bwd_dx(const T* __restrict__ dy, const T* __restrict__ x, const T* __restrict__ res, T* __restrict__ dx,
              Plan p, const float* __restrict__ mean, const float* __restrict__ rstd,
              const float* __restrict__ gamma, const float2* __restrict__ coef) {
-  UnitWalkDown w = owned_units<BwdRedShape<T, kRelu>::kWarps, kCut>(p);
+  auto w = owned_units<BwdRedShape<T, kRelu>::kWarps, kCut>(p);
   pdl_wait();  // the reduction kernel's coefficients
   int64_t row = -1;
   DxCoef k{0.f, 0.f, 0.f, 0.f, false};

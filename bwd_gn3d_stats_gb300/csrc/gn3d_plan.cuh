@@ -301,6 +301,54 @@ struct UnitWalkDown {
   }
 };
 
+// The elementwise kernels' units under strided blocks, spread evenly over all
+// their warps, freshest first.  Reduction worker v (of Wr) reads its blocks v,
+// v + Wr, ... in rounds, each block's units in order, so unit p of a block of
+// round r is read at about r*kBlockUnits + p.  Items enumerate (round from the
+// last, position p from kBlockUnits - 1 down, block of the round): what the
+// reduction read last comes first, while it is still in L2.  Warp w of W takes
+// items w, w + W, ... (positions past a short block's size are skipped).
+// Placement only: no result depends on it.
+struct UnitWalkFresh {
+  int64_t u, row, k;  // the current unit
+  int64_t i, W, Wr, nitems, nrounds, nblk;
+  bool done;
+  __host__ __device__ bool item(const Plan& p) {  // the unit of item i, if it exists
+    const int64_t per = Wr * kBlockUnits;
+    const int64_t r = nrounds - 1 - i / per, rem = i % per;
+    const int64_t pos = kBlockUnits - 1 - rem / Wr;
+    const int64_t b = r * Wr + rem % Wr;
+    if (b >= nblk) return false;
+    const int64_t kb = b % p.nb;
+    if (pos >= block_size(p, kb)) return false;
+    row = b / p.nb;
+    k = kb * kBlockUnits + pos;
+    u = row * p.R + k;
+    return true;
+  }
+  __host__ __device__ void seek(const Plan& p) {
+    for (; i < nitems; i += W)
+      if (item(p)) return;
+    done = true;
+  }
+  __host__ __device__ void set(const Plan& p, int64_t w, int64_t W_, int64_t Wr_) {
+    W = W_;
+    Wr = Wr_;
+    nblk = p.NC * p.nb;
+    nrounds = (nblk + Wr - 1) / Wr;
+    nitems = nrounds * Wr * kBlockUnits;
+    i = w;
+    u = row = k = 0;
+    done = false;
+    seek(p);
+  }
+  __host__ __device__ bool end() const { return done; }
+  __host__ __device__ void next(const Plan& p) {
+    i += W;
+    seek(p);
+  }
+};
+
 // Unit shares pay two cut blocks per worker and suit large tensors (contiguous
 // runs per SM); they are used when shares hold two merge blocks or more on
 // average, and when there are so few merge blocks (a third of the workers or

@@ -172,6 +172,25 @@ static void walk_shares(int64_t N, int64_t C, int64_t S, int64_t G) {
         }
         for (int64_t u = 0; u < p.units; ++u) CHECK(hit[u] == 1);
       }
+      if (!cut) {  // the elementwise kernels' even walk: every unit once, freshest round first
+        for (int64_t ew : {(int64_t)16, (int64_t)4, (int64_t)9}) {
+          const int64_t W = nw * ew / 8 > 0 ? nw * ew / 8 : 1;  // nw: the reduction warps, grid * 8
+          std::vector<uint8_t> hit(p.units, 0);
+          for (int64_t w = 0; w < W; ++w) {
+            UnitWalkFresh f;
+            f.set(p, w, W, nw);
+            int64_t last_i = -1;
+            for (; !f.end(); f.next(p)) {
+              CHECK(f.u >= 0 && f.u < p.units && f.u == f.row * p.R + f.k && f.k >= 0 && f.k < p.R);
+              CHECK(f.i > last_i && f.i % W == w);
+              last_i = f.i;
+              CHECK(hit[f.u] == 0);
+              hit[f.u] = 1;
+            }
+          }
+          for (int64_t u = 0; u < p.units; ++u) CHECK(hit[u] == 1);
+        }
+      }
     }
 }
 
