@@ -49,8 +49,8 @@ def test_noalloc_matches_forward_twice_in_a_row(shape):
         assert same_bytes(got, ref)
 
 
-def _scratch_verdict(C):
-    """The area's verdict on shape (1, C, 1, 1, 8) with G = 1, before any pointer
+def _scratch_fits(C):
+    """Whether the area takes shape (1, C, 1, 1, 8) with G = 1, before any pointer
     is looked at: True if the shape's scratch fits (the call then fails on the
     missing pointers instead), False if it is rejected for its scratch."""
     try:
@@ -67,10 +67,10 @@ def test_noalloc_at_the_edge_of_its_area():
     and matches gn3d_forward bit for bit; one more channel is rejected with a
     message naming the bytes needed."""
     lo, hi = 1, 1 << 22
-    assert _scratch_verdict(lo) and not _scratch_verdict(hi)
+    assert _scratch_fits(lo) and not _scratch_fits(hi)
     while hi - lo > 1:  # largest C that fits
         mid = (lo + hi) // 2
-        if _scratch_verdict(mid):
+        if _scratch_fits(mid):
             lo = mid
         else:
             hi = mid
