@@ -401,7 +401,9 @@ int cluster_active(const void* k, int cs, int smem, DevInfo& di) {
     cudaGetLastError();
   }
   std::lock_guard<std::mutex> lk(g_mu);
-  g_cluster_fit[di.dev].push_back(ClusterFit{k, cs, smem, n});
+  std::vector<ClusterFit>& fits = g_cluster_fit[di.dev];
+  if (fits.size() >= 4096) fits.clear();  // many distinct shapes: start the cache over
+  fits.push_back(ClusterFit{k, cs, smem, n});
   return n;
 }
 
