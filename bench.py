@@ -635,7 +635,7 @@ def run_reference(args):
             "config": {"workload": args.workload, "N": site.N, "C": site.C, "D": site.D, "H": site.H,
                        "W": site.W, "G": site.G, "eps": site.eps, "parallelism": f"replicas x{ws}",
                        "min_bytes_per_step": sum(site.min_bytes()), "l2": "flushed between steps (256 MiB write)",
-                       "path": "auto", "layout": "ncdhw", "sample": what},
+                       "path": "auto", "layout": "ncdhw"},
             "cpu_baseline": {"value": round(v, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": what + " per step, fwd+bwd"},
             "e2e": {"value": round(v, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
