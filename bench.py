@@ -202,11 +202,11 @@ def time_device(vols, steps, warmup, flush, stream, kernel_timing=False):
         stream.synchronize()
         if kernel_timing:
             gn.gn3d_timing(True)
-        # about 1 ms of device-side sleep ahead of the first timed step: the host
+        # about 3 ms of device-side sleep ahead of the first timed step: the host
         # enqueues the steps while it runs, so the first step's events do not
         # include the host's launch latency (the sleep is outside every event pair)
         if hasattr(torch.cuda, "_sleep"):
-            torch.cuda._sleep(2_000_000)
+            torch.cuda._sleep(6_000_000)
         evs = []
         for _ in range(steps):
             flush.fill_(1)
