@@ -195,7 +195,8 @@ def time_device(vols, steps, warmup, flush, stream, kernel_timing=False):
 
     st = stream.cuda_stream
     with torch.cuda.stream(stream):
-        for _ in range(warmup):
+        for _ in range(warmup):  # as the timed steps, the L2 flush included
+            flush.fill_(1)
             for v in vols:
                 v.fwd(st)
                 v.bwd(st)
