@@ -166,7 +166,7 @@ def test_determinism_and_dtype_independence():
 @pytest.mark.parametrize("path", ["streaming", "fused", "resident", "cluster"])
 @pytest.mark.parametrize("shape", [(2, 16, 16, 16, 16, 4, synth.F32), (1, 8, 24, 24, 24, 2, synth.BF16),
                                    (1, 32, 16, 16, 32, 8, synth.BF16), (2, 6, 1, 1, 1, 6, synth.BF16),
-                                   (1, 128, 16, 16, 16, 8, synth.BF16)],
+                                   (1, 128, 16, 16, 16, 8, synth.BF16), (1, 512, 16, 16, 16, 8, synth.BF16)],
                          ids=lambda s: "x".join(map(str, s[:6])) + "_" + s[6])
 def test_parity_other_launch_forms(path, shape, testing_build):
     """Each launch form against the oracle directly (not only against the
