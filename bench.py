@@ -507,7 +507,7 @@ def run_gpu(args):
     build.build()
     if args.path != "auto":  # another launch form: the testing build's hook (an experiment, not the product)
         gn.use_library("testing")
-        gn.gn3d_debug_set(gn.DEBUG_PATH, {"streaming": 1, "fused": 2, "resident": 3}[args.path])
+        gn.gn3d_debug_set(gn.DEBUG_PATH, {"streaming": 1, "fused": 2, "resident": 3, "cluster": 4}[args.path])
     site = synth.WORKLOADS[args.workload].sites[0]
     vol = Volume(site, dev, pinned=True, layout=args.layout)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -654,7 +654,7 @@ def main():
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--layout", choices=["ncdhw", "ndhwc"], default="ncdhw",
                     help="storage of the timed volume: NCDHW (default) or channels-last NDHWC")
-    ap.add_argument("--path", default="auto", choices=["auto", "streaming", "fused", "resident"],
+    ap.add_argument("--path", default="auto", choices=["auto", "streaming", "fused", "resident", "cluster"],
                     help="launch form (results are bit-identical; for A/B timing)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
