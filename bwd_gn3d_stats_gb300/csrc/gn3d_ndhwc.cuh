@@ -814,7 +814,8 @@ __device__ __forceinline__ void n_reduce_unit_done(const NPlan& p, const NBwdWs&
 // butterflies, then the warps in order); the CTA that completes a row adds its
 // chunk sums in order (S1, S2 of the row); the CTA that completes the last row
 // forms the group coefficients, A = sum_c gamma_c*S1_c and
-// B = rstd * sum_c gamma_c*S2_c in channel order (a = A/M, b = B/M), and
+// B = rstd * sum_c gamma_c*S2_c (one warp per group: lane-strided over the
+// channels, then the butterfly; a = A/M, b = B/M), and
 // dgamma_c = sum_n rstd[n,g]*S2[n,c], dbeta_c = sum_n S1[n,c] in n order.
 __global__ void __launch_bounds__(kNFinThreads)
     k_ndhwc_reduce_final(NPlan p, NBwdWs ws, const float* __restrict__ rstd, const float* __restrict__ gamma,
@@ -862,19 +863,38 @@ __global__ void __launch_bounds__(kNFinThreads)
     if (n_cta_arrive_last(ws.done, (uint32_t)NC)) last_row = true;
   }
   if (!last_row) return;
-  for (int64_t gi = threadIdx.x; gi < p.NG; gi += blockDim.x) {
+  // one warp per group: lane l takes the group's channels l, l + 32, ... in
+  // order (their loads issued kNCoefBatch at a time), then the butterfly
+  constexpr int kNCoefBatch = 4;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int64_t gi = warp; gi < p.NG; gi += blockDim.x >> 5) {
     const int64_t n = gi / p.G, g = gi - n * p.G;
     float A = 0.f, Bs = 0.f;
-    for (int64_t cl = 0; cl < p.Cg; ++cl) {
-      const int64_t c = g * p.Cg + cl;
-      const float2 t = __ldcg(ws.rows + n * p.C + c);
-      const float gm = gamma ? gamma[c] : 1.f;
-      A = fadd(A, fmul(gm, t.x));
-      Bs = fadd(Bs, fmul(gm, t.y));
+    for (int64_t c0 = 0; c0 < p.Cg; c0 += 32 * kNCoefBatch) {
+      float2 v[kNCoefBatch];
+      float gm[kNCoefBatch];
+#pragma unroll
+      for (int k = 0; k < kNCoefBatch; ++k) {
+        const int64_t cl = c0 + lane + 32 * k;
+        if (cl < p.Cg) {
+          const int64_t c = g * p.Cg + cl;
+          v[k] = __ldcg(ws.rows + n * p.C + c);
+          gm[k] = gamma ? gamma[c] : 1.f;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kNCoefBatch; ++k) {
+        if (c0 + lane + 32 * k < p.Cg) {
+          A = fadd(A, fmul(gm[k], v[k].x));
+          Bs = fadd(Bs, fmul(gm[k], v[k].y));
+        }
+      }
     }
-    Bs = fmul(rstd[gi], Bs);
-    const float fM = (float)p.M;
-    ws.coef[gi] = make_float2(__fdiv_rn(A, fM), __fdiv_rn(Bs, fM));
+    const float2 t = warp_sum2(A, Bs);
+    if (lane == 0) {
+      const float fM = (float)p.M;
+      ws.coef[gi] = make_float2(__fdiv_rn(t.x, fM), __fdiv_rn(fmul(rstd[gi], t.y), fM));
+    }
   }
   for (int64_t c = threadIdx.x; c < p.C; c += blockDim.x) {
     const int64_t g = c / p.Cg;
