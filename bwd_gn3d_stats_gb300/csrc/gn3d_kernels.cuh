@@ -173,19 +173,23 @@ __global__ void __launch_bounds__(32 * FwdStatShape<TI>::kWarps, 1)
       record_timeout(status);
       break;
     }
+    // a full unit of a ragged plan takes the full-unit code: the same
+    // operations on the same operands, so the same bits (unit_moments_sv)
+    const bool fu = kFull || unit_is_full(q);
     Part m;
     if (kRegs) {
       RegView<TI> v;
-      if (kFull) v.template load_full<FromShared>(reinterpret_cast<const TI*>(slot));
+      if (fu) v.template load_full<FromShared>(reinterpret_cast<const TI*>(slot));
       else v.template load<FromShared>(reinterpret_cast<const TI*>(slot), nv);
       __syncwarp();
       if (!ld.end) {
         ring.issue(urange<kFull>(p, ld.row, ld.k), 0, src);
         ld.next(p);
       }
-      m = unit_moments_sv<kFull, TI>(v, sv, q);
+      m = fu ? unit_moments_sv<true, TI>(v, sv, q) : unit_moments_sv<kFull, TI>(v, sv, q);
     } else {
-      m = unit_moments_sv<kFull, TI>(MemView<TI, FromShared>{reinterpret_cast<const TI*>(slot), nv}, sv, q);
+      const MemView<TI, FromShared> v{reinterpret_cast<const TI*>(slot), nv};
+      m = fu ? unit_moments_sv<true, TI>(v, sv, q) : unit_moments_sv<kFull, TI>(v, sv, q);
       __syncwarp();
       if (!ld.end) {
         ring.issue(urange<kFull>(p, ld.row, ld.k), 0, src);
@@ -272,16 +276,19 @@ __global__ void __launch_bounds__(32 * kElemWarps, 1)
     }
     const URange q = urange<kFull>(p, w.row, w.k);
     const int nv = (int)((q.b1 - q.b0) / kVec);
+    const bool fu = kFull || unit_is_full(q);  // a full unit of a ragged plan: the full-unit code, the same bits
     if (kRegs) {
       if (!pre) {
-        if (kFull) v.template load_full<FromGlobal>(x + q.b0);
+        if (fu) v.template load_full<FromGlobal>(x + q.b0);
         else v.template load<FromGlobal>(x + q.b0, nv);
       }
       pre = false;
-      fwd_norm<kFull, TI, TO, RegView<TI>, kRelu>(v, x, y, q, st, gm, bt);
+      if (fu) fwd_norm<true, TI, TO, RegView<TI>, kRelu>(v, x, y, q, st, gm, bt);
+      else fwd_norm<kFull, TI, TO, RegView<TI>, kRelu>(v, x, y, q, st, gm, bt);
     } else {
-      fwd_norm<kFull, TI, TO, MemView<TI, FromGlobal>, kRelu>(MemView<TI, FromGlobal>{x + q.b0, nv}, x, y, q, st, gm,
-                                                              bt);
+      const MemView<TI, FromGlobal> mv{x + q.b0, nv};
+      if (fu) fwd_norm<true, TI, TO, MemView<TI, FromGlobal>, kRelu>(mv, x, y, q, st, gm, bt);
+      else fwd_norm<kFull, TI, TO, MemView<TI, FromGlobal>, kRelu>(mv, x, y, q, st, gm, bt);
     }
   }
 }
@@ -325,6 +332,9 @@ __global__ void __launch_bounds__(32 * BwdRedShape<T, kRelu>::kWarps, 1)
     const f2 z2 = f2_splat(0.f);
     f2 a1[4] = {z2, z2, z2, z2};
     f2 a2[4] = {z2, z2, z2, z2};
+    // a full unit of a ragged plan takes the full-unit code: the same
+    // operations on the same operands, so the same bits (bwd_accum, bwd_finish_sv)
+    const bool fu = kFull || unit_is_full(q);
 #pragma unroll
     for (int part = 0; part < kParts; ++part) {
       const unsigned char* slot = ring.take(spin);
@@ -335,13 +345,17 @@ __global__ void __launch_bounds__(32 * BwdRedShape<T, kRelu>::kWarps, 1)
       // views placed so that vector i of the unit is read from this part's slot
       const T* xs = reinterpret_cast<const T*>(slot) - (size_t)part * Shape::kElems;
       const T* ds = reinterpret_cast<const T*>(slot + Ring::kTensorBytes) - (size_t)part * Shape::kElems;
+      const int i0 = part * kPartVecs, i1 = (part + 1) * kPartVecs;
       if constexpr (kRelu) {
         const T* rs = reinterpret_cast<const T*>(slot + 2 * Ring::kTensorBytes) - (size_t)part * Shape::kElems;
-        bwd_accum<kFull, T>(MemView<T, FromShared>{xs, nv}, GatedView<T, FromShared>{ds, rs, nv},
-                            part * kPartVecs, (part + 1) * kPartVecs, mu, a1, a2);
+        const MemView<T, FromShared> vx{xs, nv};
+        const GatedView<T, FromShared> vd{ds, rs, nv};
+        if (fu) bwd_accum<true, T>(vx, vd, i0, i1, mu, a1, a2);
+        else bwd_accum<kFull, T>(vx, vd, i0, i1, mu, a1, a2);
       } else {
-        bwd_accum<kFull, T>(MemView<T, FromShared>{xs, nv}, MemView<T, FromShared>{ds, nv}, part * kPartVecs,
-                            (part + 1) * kPartVecs, mu, a1, a2);
+        const MemView<T, FromShared> vx{xs, nv}, vd{ds, nv};
+        if (fu) bwd_accum<true, T>(vx, vd, i0, i1, mu, a1, a2);
+        else bwd_accum<kFull, T>(vx, vd, i0, i1, mu, a1, a2);
       }
       __syncwarp();
       if (!ld.w.end) {
@@ -353,7 +367,7 @@ __global__ void __launch_bounds__(32 * BwdRedShape<T, kRelu>::kWarps, 1)
       record_timeout(status);
       break;
     }
-    const float2 v = bwd_finish_sv<kFull>(a1, a2, sc, q, mu);
+    const float2 v = fu ? bwd_finish_sv<true>(a1, a2, sc, q, mu) : bwd_finish_sv<kFull>(a1, a2, sc, q, mu);
     const int ui = cu.ui(), bsz = block_size(p, cu.kb());
     if (lane == ui) a = v;
     if (ui == bsz - 1 || (kCut && cu.u + 1 == cu.u1)) {  // the block, or this warp's part of it, is done
