@@ -1,13 +1,17 @@
 // gn3d.cu -- libgn3d's C ABI: argument checks, the launch plan, per-call scratch
 // and the kernel launches for GroupNorm forward and backward (include/gn3d.h).
 //
-// Three launch forms run the same units with the same arithmetic (bit-identical
+// Four launch forms run the same units with the same arithmetic (bit-identical
 // results): the streaming kernels (gn3d_kernels.cuh, two launches per
-// direction), used by default; the persistent cooperative kernels
-// (gn3d_fused.cuh); and the group-wave kernels (gn3d_resident.cuh, one
-// cooperative launch per direction, each group's share held on chip between the
-// two passes).  The last two are selected through gn3d_debug_set, for
-// cross-checks and A/B timing.
+// direction); the cluster kernels (gn3d_cluster.cuh, one launch per direction,
+// one thread-block cluster per group holding its units in shared memory); the
+// persistent cooperative kernels (gn3d_fused.cuh); and the group-wave kernels
+// (gn3d_resident.cuh, one cooperative launch per direction, each group's share
+// held on chip between the two passes).  The automatic choice takes the cluster
+// form where every group's cluster is resident at once and the streaming
+// kernels otherwise; the testing build's gn3d_debug_set selects any form, for
+// cross-checks and A/B timing.  The channels-last entry points run their own
+// kernels (gn3d_ndhwc.cuh).
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdio.h>
