@@ -1149,7 +1149,7 @@ int forward_impl(const void* x, const float* gamma, const float* beta, int64_t N
   }
   using bf = __nv_bfloat16;
   if (ndhwc) {
-    const NPlan np = make_nplan(N, C, D * H * W, G);
+    const NPlan np = make_nplan(N, C, D * H * W, G, kNMinUnitsFwd);
     if (in_dtype == GN3D_BF16 && out_dtype == GN3D_BF16)
       return launch_forward_ndhwc<bf, bf>(x, gamma, beta, np, feps, y, mean, rstd, st, *di, relu);
     if (in_dtype == GN3D_BF16 && out_dtype == GN3D_F32)
@@ -1203,7 +1203,7 @@ int backward_impl(const void* dy, const void* x, const void* res, const float* m
     if ((rc = check_ptr(res, dev, "out"))) return rc;
   }
   if (ndhwc) {
-    const NPlan np = make_nplan(N, C, D * H * W, G);
+    const NPlan np = make_nplan(N, C, D * H * W, G, kNMinUnitsBwd);
     if (dtype == GN3D_BF16)
       return launch_backward_ndhwc<__nv_bfloat16>(dy, x, relu ? res : nullptr, mean, rstd, gamma, np, dx, dgamma,
                                                   dbeta, st, *di);

@@ -18,8 +18,9 @@
 // (lanes >= lp*vr idle).
 //
 // Units and groups.  Row (n, r) -- sample n, range r -- is cut into units of
-// Pu = kNSteps * lp0 positions (lp0: the lp of range 0, the widest), one warp
-// per unit, at most kNSteps vectors per lane.  Statistics merge in a fixed tree
+// Pu = steps * lp0 positions (lp0: the lp of range 0, the widest; steps = kNSteps,
+// halved down to kNMinSteps for small volumes), one warp per unit, at most
+// steps vectors per lane.  Statistics merge in a fixed tree
 // that depends on the shape alone: lane -> channel (the lp lanes of a channel,
 // pairwise) -> piece (the channels of one group inside the range), per unit,
 // in the streaming kernel; the pieces -> group in the finalize kernel, one CTA

@@ -14,7 +14,16 @@ namespace gn3d {
 
 constexpr int kNVec = 8;     // elements per vector: 8 channels of one position
 constexpr int kNSpan = 32;   // vectors per channel range (256 channels)
-constexpr int kNSteps = 64;  // steps (vectors per lane) per unit
+constexpr int kNSteps = 64;  // steps (vectors per lane) per unit, at most
+constexpr int kNMinSteps = 16;     // ... and at least (one pilot-shifted chunk)
+// Units wanted before a unit is halved.  The forward's statistics kernel merges
+// each unit's lanes into channels and pieces, so it keeps long units unless
+// they are very few (a quarter of a 152-CTA grid's reduction warps); the
+// backward's reduction and dx kernels want one unit per elementwise warp of that
+// grid.  The backward takes the statistics as inputs, so the two directions'
+// plans need not agree.
+constexpr int64_t kNMinUnitsFwd = 304;
+constexpr int64_t kNMinUnitsBwd = 2432;
 constexpr int kNChunk = 16;  // steps of a lane's first chunk (pilot-shifted)
 constexpr int kNPilot = 4;   // steps of the pilot mean
 constexpr int kNRedWarps = 8;    // warps per CTA of the statistics and reduction kernels
@@ -24,6 +33,7 @@ struct NPlan {
   int64_t N, C, S, G, Cg, NG, M;
   int64_t V;      // vectors per position (C / 8)
   int64_t nr;     // channel ranges
+  int64_t steps;  // steps per unit: kNSteps, halved while units are fewer than wanted
   int64_t Pu;     // positions per unit
   int64_t R;      // units per row
   int64_t P;      // pieces (groups met) per range, the most of any range
@@ -50,7 +60,8 @@ __host__ __device__ inline NRange n_range(const NPlan& p, int64_t r) {
   return q;
 }
 
-inline NPlan make_nplan(int64_t N, int64_t C, int64_t S, int64_t G) {
+// min_units: kNMinUnitsFwd for the forward, kNMinUnitsBwd for the backward.
+inline NPlan make_nplan(int64_t N, int64_t C, int64_t S, int64_t G, int64_t min_units) {
   NPlan p;
   p.N = N; p.C = C; p.S = S; p.G = G;
   p.Cg = C / G;
@@ -59,8 +70,14 @@ inline NPlan make_nplan(int64_t N, int64_t C, int64_t S, int64_t G) {
   p.V = C / kNVec;
   p.nr = (p.V + kNSpan - 1) / kNSpan;
   const int64_t v0 = p.V < kNSpan ? p.V : kNSpan;
-  p.Pu = (int64_t)kNSteps * (32 / v0);
-  p.R = S > 0 ? (S + p.Pu - 1) / p.Pu : 0;
+  // small volumes: shorter units, so that their work spreads over the grid
+  p.steps = kNSteps;
+  for (;;) {
+    p.Pu = p.steps * (32 / v0);
+    p.R = S > 0 ? (S + p.Pu - 1) / p.Pu : 0;
+    if (p.steps <= kNMinSteps || N * p.nr * p.R >= min_units) break;
+    p.steps /= 2;
+  }
   p.P = 0;
   for (int64_t r = 0; r < p.nr; ++r) {
     const NRange q = n_range(p, r);

@@ -194,9 +194,9 @@ static void walk_shares(int64_t N, int64_t C, int64_t S, int64_t G) {
     }
 }
 
-static void walk_ndhwc(int64_t N, int64_t C, int64_t S, int64_t G) {
+static void walk_ndhwc(int64_t N, int64_t C, int64_t S, int64_t G, int64_t min_units) {
   g_what = "ndhwc";
-  const NPlan p = make_nplan(N, C, S, G);
+  const NPlan p = make_nplan(N, C, S, G, min_units);
   const int64_t numel = N * S * C;
   std::vector<uint8_t> cover(numel, 0);
   std::vector<uint8_t> piece(p.rows * p.P * p.R, 0);
@@ -207,7 +207,7 @@ static void walk_ndhwc(int64_t N, int64_t C, int64_t S, int64_t G) {
     for (int lane = 0; lane < 32; ++lane) {
       const NUnit q = n_unit(p, u, lane);
       CHECK(q.row == q0.row && q.k == q0.k && q.len == q0.len && q.len >= 1);
-      CHECK(q.cnt <= kNSteps && q.b >= 0 && q.b < q.rg.vr);
+      CHECK(q.cnt <= p.steps && p.steps <= kNSteps && p.steps >= kNMinSteps && q.b >= 0 && q.b < q.rg.vr);
       if (lane < q.rg.vr) CHECK(q.m == 0 && q.cnt >= 1);  // the lanes whose means shift the others
       for (int t = 0; t < q.cnt; ++t) {
         const int64_t o = q.off + t * q.step;
@@ -666,7 +666,10 @@ int main() {
           g_shape[0] = N; g_shape[1] = C; g_shape[2] = S; g_shape[3] = G;
           walk_ncdhw(N, C, S, G);
           walk_shares(N, C, S, G);
-          if (C % kNVec == 0) walk_ndhwc(N, C, S, G);
+          if (C % kNVec == 0) {
+            walk_ndhwc(N, C, S, G, kNMinUnitsFwd);
+            walk_ndhwc(N, C, S, G, kNMinUnitsBwd);
+          }
           ++shapes;
         }
       }

@@ -80,7 +80,7 @@ def full_parity_cl(site, inp, out_dtype=None, affine=True):
 # straddling ranges (Cg = 96 at C = 768), ragged last units and blocks.
 SHAPES = [
     (2, 16, 16, 16, 16, 4, synth.F32),    # the small fp32 workload, channels-last
-    (1, 32, 16, 16, 16, 8, synth.BF16),   # the UNet's first site in miniature: 8 units of 512 positions
+    (1, 32, 16, 16, 16, 8, synth.BF16),   # the UNet's first site in miniature: 32 short units of 128 positions
     (1, 48, 13, 11, 7, 8, synth.BF16),    # C = 48: 6 vectors, 5 positions per step; Cg = 6; odd S
     (2, 64, 8, 9, 10, 32, synth.F32),     # 2 channels per group
     (1, 8, 20, 20, 20, 1, synth.BF16),    # one vector per position, one group
@@ -89,7 +89,7 @@ SHAPES = [
     (1, 512, 4, 4, 5, 8, synth.BF16),     # two full ranges, 80 positions
     (1, 768, 2, 2, 3, 8, synth.BF16),     # groups of 96 channels across range boundaries
     (2, 16, 1, 1, 1, 16, synth.F32),      # single-element groups
-    (1, 32, 40, 40, 40, 8, synth.BF16),   # 125 units: several merge blocks, ragged last block
+    (1, 32, 40, 40, 40, 8, synth.BF16),   # 500 short units of 128 positions, ragged last unit
 ]
 
 
