@@ -241,6 +241,15 @@ def test_ndhwc_bounded_wait_timeout_reports_and_recovers(testing_build):
         assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
 
 
+def test_ndhwc_plans_differ_by_direction():
+    """1x32x86^3: 1243 units of 64 steps for the forward, and 2485 units of 32
+    steps for the backward (which halves its units below 2432), so the two
+    directions run different plans. The backward at the forward's statistics,
+    and everything else, element by element against the oracle."""
+    site = synth.Site(1, 32, 86, 86, 86, 8, synth.BF16)
+    full_parity_cl(site, synth.make_inputs(site, seed=20))
+
+
 def test_ndhwc_two_level_finalize_sampled():
     """A shape whose rows hold more than one finalize chunk (256 channels: units
     of 64 positions, 66^3 positions -> 4493 units per row, two chunks), so both
