@@ -839,7 +839,8 @@ int launch_backward_ndhwc(const void* dy, const void* x, const void* res, const 
   }
   if (e == cudaSuccess) {
     LaunchTimer t2(KK_N_REDUCE_FINAL, st, di);
-    e = launch_dependent(k_ndhwc_reduce_final, grid_for(di, tasks, 4), kNFinThreads, st, p, w, rstd, gamma, dgamma,
+    const int64_t ftasks = n_fin_short_rows(p) ? (NC + kNFinThreads / 32 - 1) / (kNFinThreads / 32) : tasks;
+    e = launch_dependent(k_ndhwc_reduce_final, grid_for(di, ftasks, 4), kNFinThreads, st, p, w, rstd, gamma, dgamma,
                          dbeta);
     t2.done();
   }

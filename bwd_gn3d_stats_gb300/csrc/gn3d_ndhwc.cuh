@@ -562,6 +562,11 @@ __host__ __device__ inline int64_t n_fin_maxr(const NPlan& p) {
 }
 __host__ __device__ inline int64_t n_fin_nkc(const NPlan& p) { return (p.R + kNFinChunk - 1) / kNFinChunk; }
 
+// Rows of at most kNFinShortRow units: the backward finalize sums each with one
+// warp instead of one CTA.
+constexpr int64_t kNFinShortRow = 512;
+__host__ __device__ inline bool n_fin_short_rows(const NPlan& p) { return p.R <= kNFinShortRow; }
+
 __device__ __forceinline__ float2 n_cta_sum2(float a, float b) {
   __shared__ float2 part[kNFinThreads / 32];
   const float2 t = warp_sum2(a, b);
@@ -810,7 +815,9 @@ __device__ __forceinline__ void n_reduce_unit_done(const NPlan& p, const NBwdWs&
 }
 
 // ----------------------------------------------------- backward finalize
-// Row (n, c): its unit sums cut into chunks of kNFinChunk units; one CTA sums a
+// Row (n, c): rows of at most kNFinShortRow units are summed one warp per row,
+// with one CTA arrival per pass of the CTA's warps.  Longer rows: the unit sums
+// cut into chunks of kNFinChunk units; one CTA sums a
 // chunk (thread t takes units t, t + kNFinThreads, ... in order, then the warps'
 // butterflies, then the warps in order); the CTA that completes a row adds its
 // chunk sums in order (S1, S2 of the row); the CTA that completes the last row
@@ -825,7 +832,34 @@ __global__ void __launch_bounds__(kNFinThreads)
   pdl_wait();  // the reduction kernel's unit sums
   const int64_t nkc = n_fin_nkc(p), NC = p.N * p.C;
   bool last_row = false;
-  for (int64_t t = blockIdx.x; t < NC * nkc; t += gridDim.x) {
+  if (n_fin_short_rows(p)) {
+    // short rows: one warp per row (lane l takes units l, l + 32, ... in order,
+    // then the butterfly) and one CTA arrival per pass of the CTA's warps
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = kNFinThreads / 32;
+    const int64_t passes = (NC + nw - 1) / nw;
+    for (int64_t ps = blockIdx.x; ps < passes; ps += gridDim.x) {
+      const int64_t rc = ps * nw + warp;
+      if (rc < NC) {
+        const float2* us = ws.usum + rc * p.R;
+        float2 v[kNFinShortRow / 32];
+#pragma unroll
+        for (int k = 0; k < kNFinShortRow / 32; ++k)
+          if (lane + 32 * k < p.R) v[k] = __ldcg(us + lane + 32 * k);
+        float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+        for (int k = 0; k < kNFinShortRow / 32; ++k) {
+          if (lane + 32 * k < p.R) {
+            s1 = fadd(s1, v[k].x);
+            s2 = fadd(s2, v[k].y);
+          }
+        }
+        const float2 row = warp_sum2(s1, s2);
+        if (lane == 0) ws.rows[rc] = row;
+      }
+      if (n_cta_arrive_last(ws.done, (uint32_t)passes)) last_row = true;
+    }
+  }
+  for (int64_t t = n_fin_short_rows(p) ? NC * nkc : blockIdx.x; t < NC * nkc; t += gridDim.x) {
     const int64_t rc = t / nkc, kc = t - rc * nkc;
     const float2* us = ws.usum + rc * p.R;
     const int64_t k0 = kc * kNFinChunk, k1 = k0 + kNFinChunk < p.R ? k0 + kNFinChunk : p.R;
